@@ -1,0 +1,318 @@
+"""CPU oracle of the QuantWM quantise-and-attend path (ctypes front end of qwm_oracle.c).
+
+TEST INFRASTRUCTURE ONLY.  Only `tests/`, `__graft_entry__.smoke()` and the
+CPU-baseline leg of `bench.py` may import this package.  It shares nothing
+with the CUDA library (`bit_kv_cache_qsac_gb300`) and never calls it.
+
+Every function works on one head at a time and takes numpy arrays; bf16 and
+fp16 values travel as their uint16 bit patterns.  The per-stage functions
+follow the QuantWM summaries' step list ("方法步骤详情" steps 1-5 of the
+Chinese summary; §4.1, §4.2, §C.3 and §D.1 of the v2 summary) and the QVG
+summary's k-means smoothing (§2A) and warm start (§2C).
+
+Parity pins: every function here is pinned by `tests/test_oracle_pins.py`
+against closed forms, special cases, library routines or worked examples;
+none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "qwm_oracle.c")
+_LIB_DIR = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_LIB_DIR, "liboracle.so")
+_CFLAGS = ["-std=c11", "-O2", "-fopenmp", "-frounding-math", "-ffp-contract=off",
+           "-fno-fast-math", "-shared", "-fPIC"]
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile qwm_oracle.c with gcc into oracle/_build/liboracle.so."""
+    os.makedirs(_LIB_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", *_CFLAGS, "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+P = C.c_void_p
+I64 = C.c_int64
+I32 = C.c_int32
+
+
+class QuantArgs(C.Structure):
+    _fields_ = [
+        ("k", P), ("v", P), ("cent_k", P), ("cent_v", P), ("w", P), ("u_r", P), ("u_r_f64", P),
+        ("force_idx_k", P), ("force_idx_v", P),
+        ("n", I64), ("d", I32), ("C", I32), ("group", I32), ("top_m", I32), ("rank", I32),
+        ("idx_k", P), ("idx_v", P), ("k_codes", P), ("v_codes", P),
+        ("k_scale", P), ("k_min", P), ("v_scale", P), ("v_min", P),
+        ("c", P), ("c_scale", P), ("c_real", P), ("cand", P), ("score2", P), ("dq_edge", P),
+        ("vdist2", P),
+    ]
+
+
+class ChunkHead(C.Structure):
+    _fields_ = [
+        ("n", I64), ("rank", I32),
+        ("idx_k", P), ("idx_v", P), ("k_codes", P), ("v_codes", P),
+        ("k_scale", P), ("k_min", P), ("v_scale", P), ("v_min", P),
+        ("cent_k", P), ("cent_v", P), ("c", P), ("c_scale", P), ("u_r", P),
+    ]
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            l = C.CDLL(build())
+            l.oracle_stats_accumulate.argtypes = [P, I64, C.c_int, P]
+            l.oracle_weights.argtypes = [P, I64, C.c_int, P]
+            l.oracle_eig_sym.argtypes = [P, C.c_int, C.c_double, C.c_int, P, P]
+            l.oracle_eig_sym.restype = C.c_int
+            l.oracle_basis_bf16.argtypes = [P, C.c_int, C.c_int, P]
+            l.oracle_kmeans.argtypes = [P, I64, C.c_int, C.c_int, P, C.c_int, P, P, P, P]
+            l.oracle_kmeans_objective.argtypes = [P, I64, C.c_int, P, C.c_int]
+            l.oracle_kmeans_objective.restype = C.c_double
+            l.oracle_int2_encode_group.argtypes = [P, C.c_int, P, P, P]
+            l.oracle_pack2.argtypes = [P, C.c_int, P]
+            l.oracle_int8_encode_token.argtypes = [P, C.c_int, P, P]
+            l.oracle_quantize_head.argtypes = [C.POINTER(QuantArgs)]
+            l.oracle_attend_rows.argtypes = [P, C.c_int, C.c_int, P, I64, C.POINTER(ChunkHead),
+                                             C.c_int, C.c_double, P]
+            l.oracle_dequantize_head.argtypes = [C.POINTER(ChunkHead), C.c_int, C.c_int, P, P, P, P]
+            l.oracle_fp16_val.argtypes = [C.c_uint16]
+            l.oracle_fp16_val.restype = C.c_double
+            l.oracle_round_fp16.argtypes = [C.c_double, C.c_int]
+            l.oracle_round_fp16.restype = C.c_double
+            l.oracle_fp16_bits.argtypes = [C.c_double]
+            l.oracle_fp16_bits.restype = C.c_uint16
+            l.oracle_bf16_rne.argtypes = [C.c_double]
+            l.oracle_bf16_rne.restype = C.c_uint16
+            _lib = l
+    return _lib
+
+
+def _c(a, dtype):
+    """Contiguous array of the given dtype (a copy only when needed)."""
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(P)
+
+
+# ---------------------------------------------------------------- step 1: statistics
+
+
+def stats_accumulate(q_bf16: np.ndarray, S: np.ndarray) -> None:
+    """S += sum_q q q^T for one head (q: uint16 [nq][d]; S: float64 [d][d], updated in place)."""
+    q = _c(q_bf16, np.uint16)
+    assert S.dtype == np.float64 and S.flags.c_contiguous
+    lib().oracle_stats_accumulate(_p(q), q.shape[0], q.shape[1], _p(S))
+
+
+def weights(S: np.ndarray, n: int) -> np.ndarray:
+    """w_c = S_cc / n, or 1 at cold start (n == 0)."""
+    S = _c(S, np.float64)
+    w = np.empty(S.shape[0], np.float64)
+    lib().oracle_weights(_p(S), int(n), S.shape[0], _p(w))
+    return w
+
+
+def eig(M: np.ndarray, tol_rel: float = 1e-14, max_sweeps: int = 60):
+    """(lambda descending, U with U[:, k] the k-th eigenvector, sweeps or -1)."""
+    M = _c(M, np.float64)
+    d = M.shape[0]
+    lam = np.empty(d, np.float64)
+    U = np.empty((d, d), np.float64)
+    sweeps = lib().oracle_eig_sym(_p(M), d, tol_rel, max_sweeps, _p(lam), _p(U))
+    return lam, U, sweeps
+
+
+def basis_bf16(U: np.ndarray, r: int) -> np.ndarray:
+    """First r eigenvectors rounded to bf16: uint16 [d][r]."""
+    U = _c(U, np.float64)
+    d = U.shape[0]
+    out = np.empty((d, r), np.uint16)
+    if r:
+        lib().oracle_basis_bf16(_p(U), d, r, _p(out))
+    return out
+
+
+def update_query_stats(q_bf16: np.ndarray, S: np.ndarray, n: np.ndarray, rank: int):
+    """All heads: fold q [H][nq][d] into S [H][d][d] (float64, in place) and n [H] (in place);
+    return (w [H][d], eigvals [H][d], U_r bf16 [H][d][rank], U float64 [H][d][d], sweeps [H])."""
+    H, nq, d = q_bf16.shape
+    w = np.empty((H, d)); lam = np.empty((H, d)); ur = np.empty((H, d, rank), np.uint16)
+    U = np.empty((H, d, d)); sweeps = np.empty(H, np.int64)
+    for h in range(H):
+        stats_accumulate(q_bf16[h], S[h])
+        n[h] += nq
+        w[h] = weights(S[h], int(n[h]))
+        if n[h] > 0:
+            lam[h], U[h], sweeps[h] = eig(S[h] / float(n[h]))
+        else:
+            lam[h], U[h], sweeps[h] = 0.0, np.eye(d), 0
+        ur[h] = basis_bf16(U[h], rank)
+    return w, lam, ur, U, sweeps
+
+
+# ---------------------------------------------------------------- step 2a: k-means
+
+
+def kmeans(x_bf16: np.ndarray, n_centroids: int, init_bf16: np.ndarray | None, iters: int):
+    """Lloyd k-means of one head: returns (cent bf16 [C][d], cent float64, last assignment, objective per iteration)."""
+    x = _c(x_bf16, np.uint16)
+    n, d = x.shape
+    init = None if init_bf16 is None else _c(init_bf16, np.uint16)
+    cent = np.empty((n_centroids, d), np.uint16)
+    cent64 = np.empty((n_centroids, d), np.float64)
+    asg = np.empty(max(n, 1), np.int32)
+    obj = np.empty(max(iters, 1), np.float64)
+    lib().oracle_kmeans(_p(x), n, d, n_centroids, _p(init), iters, _p(cent), _p(cent64), _p(asg), _p(obj))
+    return cent, cent64, asg[:n], obj[:iters]
+
+
+def kmeans_objective(x_bf16: np.ndarray, cent_bf16: np.ndarray) -> float:
+    x = _c(x_bf16, np.uint16)
+    cent = _c(cent_bf16, np.uint16)
+    return lib().oracle_kmeans_objective(_p(x), x.shape[0], x.shape[1], _p(cent), cent.shape[0])
+
+
+# ---------------------------------------------------------------- steps 2-4: quantiser
+
+
+def int2_encode_group(r: np.ndarray):
+    """(codes uint8 [g], s fp16 bits, m fp16 bits) for one group of float32 residuals."""
+    r = _c(r, np.float32)
+    codes = np.empty(r.size, np.uint8)
+    s = C.c_uint16()
+    m = C.c_uint16()
+    lib().oracle_int2_encode_group(_p(r), r.size, _p(codes), C.byref(s), C.byref(m))
+    return codes, s.value, m.value
+
+
+def pack2(codes: np.ndarray) -> np.ndarray:
+    codes = _c(codes, np.uint8)
+    out = np.empty(codes.size // 4, np.uint8)
+    lib().oracle_pack2(_p(codes), codes.size, _p(out))
+    return out
+
+
+def int8_encode_token(Cf: np.ndarray):
+    """(c int8 [r], sC fp16 bits) for one token's float32 PSAC coefficients."""
+    Cf = _c(Cf, np.float32)
+    c = np.empty(Cf.size, np.int8)
+    sc = C.c_uint16()
+    lib().oracle_int8_encode_token(_p(Cf), Cf.size, _p(c), C.byref(sc))
+    return c, sc.value
+
+
+def quantize_head(k, v, cent_k, cent_v, w=None, u_r=None, *, group=64, top_m=4, rank=None,
+                  u_r_f64=None, force_idx_k=None, force_idx_v=None):
+    """QSAC Key assignment, nearest-centroid Value assignment, INT2 residuals and PSAC for one head.
+
+    k, v: uint16 [n][d]; cent_k, cent_v: uint16 [C][d]; w: float [d] or None (uniform);
+    u_r: uint16 [d][r] or None (PSAC off).  Returns a dict of every output and diagnostic."""
+    k = _c(k, np.uint16); v = _c(v, np.uint16)
+    cent_k = _c(cent_k, np.uint16); cent_v = _c(cent_v, np.uint16)
+    n, d = k.shape
+    Cn = cent_k.shape[0]
+    if rank is None:
+        rank = 0 if (u_r is None and u_r_f64 is None) else (u_r if u_r is not None else u_r_f64).shape[1]
+    G = d // group
+    w64 = None if w is None else _c(w, np.float64)
+    ur = None if u_r is None else _c(u_r, np.uint16)
+    ur64 = None if u_r_f64 is None else _c(u_r_f64, np.float64)
+    fk = None if force_idx_k is None else _c(force_idx_k, np.int32)
+    fv = None if force_idx_v is None else _c(force_idx_v, np.int32)
+    o = dict(
+        idx_k=np.empty(n, np.int32), idx_v=np.empty(n, np.int32),
+        k_codes=np.empty((n, d // 4), np.uint8), v_codes=np.empty((n, d // 4), np.uint8),
+        k_scale=np.empty((n, G), np.uint16), k_min=np.empty((n, G), np.uint16),
+        v_scale=np.empty((n, G), np.uint16), v_min=np.empty((n, G), np.uint16),
+        c=np.zeros((n, max(rank, 1)), np.int8), c_scale=np.zeros(n, np.uint16),
+        c_real=np.zeros((n, max(rank, 1)), np.float64),
+        cand=np.empty((n, top_m), np.int32), score2=np.empty((n, 2)), dq_edge=np.empty((n, 2)),
+        vdist2=np.empty((n, 2)),
+    )
+    a = QuantArgs(k=_p(k), v=_p(v), cent_k=_p(cent_k), cent_v=_p(cent_v), w=_p(w64), u_r=_p(ur),
+                  u_r_f64=_p(ur64), force_idx_k=_p(fk), force_idx_v=_p(fv), n=n, d=d, C=Cn,
+                  group=group, top_m=top_m, rank=rank,
+                  **{key: _p(val) for key, val in o.items()})
+    if n:
+        lib().oracle_quantize_head(C.byref(a))
+    o["c"] = o["c"][:, :rank]
+    o["c_real"] = o["c_real"][:, :rank]
+    o["rank"] = rank
+    return o
+
+
+# ---------------------------------------------------------------- step 5: attention, decoder
+
+
+def _chunk_struct(ch: dict, keep: list) -> ChunkHead:
+    """ch: per-head dict with idx_k, idx_v, k_codes, v_codes, k_scale, k_min, v_scale, v_min,
+    cent_k, cent_v and, when rank > 0, c, c_scale, u_r."""
+    def arr(name, dtype):
+        a = _c(ch[name], dtype)
+        keep.append(a)
+        return _p(a)
+    rank = int(ch.get("rank", 0))
+    return ChunkHead(
+        n=int(np.asarray(ch["idx_k"]).shape[0]), rank=rank,
+        idx_k=arr("idx_k", np.int32), idx_v=arr("idx_v", np.int32),
+        k_codes=arr("k_codes", np.uint8), v_codes=arr("v_codes", np.uint8),
+        k_scale=arr("k_scale", np.uint16), k_min=arr("k_min", np.uint16),
+        v_scale=arr("v_scale", np.uint16), v_min=arr("v_min", np.uint16),
+        cent_k=arr("cent_k", np.uint16), cent_v=arr("cent_v", np.uint16),
+        c=arr("c", np.int8) if rank else None, c_scale=arr("c_scale", np.uint16) if rank else None,
+        u_r=arr("u_r", np.uint16) if rank else None,
+    )
+
+
+def attend_rows(q_bf16: np.ndarray, rows, chunks: list[dict], scale: float, group: int = 64) -> np.ndarray:
+    """Attention output (float64 [len(rows)][d]) of the listed query rows of one head over
+    every token of every chunk in `chunks` (per-head chunk dicts)."""
+    q = _c(q_bf16, np.uint16)
+    rows = _c(np.asarray(rows), np.int64)
+    d = q.shape[1]
+    keep: list = []
+    arr = (ChunkHead * max(1, len(chunks)))(*[_chunk_struct(ch, keep) for ch in chunks])
+    out = np.empty((rows.size, d), np.float64)
+    lib().oracle_attend_rows(_p(q), d, group, _p(rows), rows.size, arr, len(chunks), float(scale), _p(out))
+    return out
+
+
+def dequantize_head(ch: dict, d: int = 128, group: int = 64):
+    """(K_hat bf16 [n][d], V_hat bf16 [n][d], K_hat float64, V_hat float64) of one head of one chunk."""
+    keep: list = []
+    s = _chunk_struct(ch, keep)
+    n = s.n
+    kh = np.empty((n, d), np.uint16); vh = np.empty((n, d), np.uint16)
+    kh64 = np.empty((n, d)); vh64 = np.empty((n, d))
+    lib().oracle_dequantize_head(C.byref(s), d, group, _p(kh), _p(vh), _p(kh64), _p(vh64))
+    return kh, vh, kh64, vh64
+
+
+def fp16_val(bits) -> np.ndarray:
+    """fp16 bit patterns -> float64 values."""
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def round_fp16(x: float, direction: int) -> float:
+    return lib().oracle_round_fp16(float(x), int(direction))
+
+
+def bf16_rne(x: float) -> int:
+    return lib().oracle_bf16_rne(float(x))

@@ -1,0 +1,678 @@
+/*
+ * qwm_oracle.c -- plain, slow CPU oracle of the QuantWM quantise-and-attend path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  It shares no code,
+ * header, table or helper with the CUDA library and never calls it.
+ *
+ * Sources (cited by page and section):
+ *   [QWM-zh]  QuantWM summary (Chinese), "前置知识" (affine quantiser, centroid-residual
+ *             form, logits, second-order Query statistics), "核心方法" (QSAC score,
+ *             INT2 error estimate, PSAC logit form), "方法步骤详情" steps 1-5.
+ *   [QWM-ko]  QuantWM summary (Korean), "무엇과 다른가" (QSAC), "어떻게 쓰나" (PSAC).
+ *   [QWM-en]  QuantWM v2 summary, §4.1, §4.2, §5.1, §C.3, §D.1.
+ *   [QVG-ko]  Quant VideoGen summary, §2A (k-means smoothing), §2C (streaming centroid caching).
+ *
+ * Floating point: accumulations in double (fp64).  The two places where the
+ * pages' format fixes a 32-bit computation -- the residual r = k - mu and the
+ * INT2 / INT8 encoders -- are written in float with explicit IEEE rounding
+ * modes, so that integer codes can be compared bit for bit.
+ * Build: gcc -std=c11 -O2 -fopenmp -frounding-math -ffp-contract=off -fno-fast-math.
+ *
+ * Readings of the pages (where they are silent or garbled):
+ *   - Affine quantiser ([QWM-zh] 前置知识) prints X_q = clip(X/s + z) without a
+ *     rounding step; round-half-even is used.  Per (token, group of 64 channels):
+ *     m = round_down_fp16(min r), s = round_up_fp16(round_up_f32(round_up_f32(max r - m) / 3)),
+ *     q = clamp(rint((r - m) * (1/s)), 0, 3), r_hat = m + s q.  This makes
+ *     |r - r_hat| <= s/2 hold for every element.  When max r == m, s = 0 and q = 0.
+ *   - INT8 of C: per token, symmetric, sC = round_up_fp16(round_up_f32(max|C| / 127)),
+ *     c = clamp(rint(C * (1/sC)), -127, 127).
+ *   - Eigenvector signs: the largest-magnitude component is made positive
+ *     (lowest channel on ties); eigenvalues descend (lower index on ties).
+ *   - k-means: Lloyd iterations, Euclidean, ties to the lower centroid,
+ *     empty clusters keep their previous centroid, output rounded to bf16.
+ */
+#include <fenv.h>
+#include <float.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* dynamic rounding modes are honoured because the file is built with -frounding-math */
+
+/* ------------------------------------------------------------------ */
+/* number formats                                                      */
+/* ------------------------------------------------------------------ */
+
+static double bf16_val(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+static float bf16_valf(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+
+/* Round a double to a binary format with `p` significand bits, minimum normal
+ * exponent `emin` (value 2^emin) -- i.e. quantum max(2^(e-p), 2^(emin-p+1)) --
+ * in the given direction: 0 nearest-even, -1 down, +1 up.  Exact in double. */
+static double round_to_format(double x, int p, int emin, int dir) {
+  if (x == 0.0 || !isfinite(x)) return x;
+  int e;
+  frexp(x, &e); /* |x| in [2^(e-1), 2^e) */
+  int qexp = e - p;
+  if (qexp < emin - p + 1) qexp = emin - p + 1;
+  double scaled = ldexp(x, -qexp); /* exact */
+  double r;
+  if (dir < 0) r = floor(scaled);
+  else if (dir > 0) r = ceil(scaled);
+  else r = nearbyint(scaled); /* current mode is to-nearest-even */
+  return ldexp(r, qexp);
+}
+
+static uint16_t bf16_bits_of(double x) { /* x must already be a bf16 value */
+  float f = (float)x;
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  return (uint16_t)(u >> 16);
+}
+
+static uint16_t bf16_rne(double x) { return bf16_bits_of(round_to_format(x, 8, -126, 0)); }
+
+#define FP16_MAX 65504.0
+static double fp16_round(double x, int dir) { return round_to_format(x, 11, -14, dir); }
+
+static uint16_t fp16_bits_of(double v) { /* v must be an fp16 value (or +-inf) */
+  uint16_t sign = (v < 0 || (v == 0 && signbit(v))) ? 0x8000 : 0;
+  double a = fabs(v);
+  if (isinf(a) || a > FP16_MAX) return sign | 0x7C00;
+  if (a == 0) return sign;
+  if (a < ldexp(1.0, -14)) return sign | (uint16_t)(a / ldexp(1.0, -24));
+  int e;
+  double m = frexp(a, &e); /* a = m 2^e, m in [0.5, 1) */
+  uint16_t ef = (uint16_t)(e - 1 + 15);
+  uint16_t mant = (uint16_t)((m * 2.0 - 1.0) * 1024.0);
+  return sign | (uint16_t)(ef << 10) | mant;
+}
+
+double oracle_fp16_val(uint16_t h) {
+  int e = (h >> 10) & 31, m = h & 1023;
+  double v;
+  if (e == 0) v = ldexp((double)m, -24);
+  else if (e == 31) v = m ? NAN : INFINITY;
+  else v = ldexp(1.0 + m / 1024.0, e - 15);
+  return (h & 0x8000) ? -v : v;
+}
+
+static float f32_sub_up(float a, float b) {
+  int old = fegetround();
+  fesetround(FE_UPWARD);
+  volatile float va = a, vb = b;
+  volatile float r = va - vb;
+  fesetround(old);
+  return r;
+}
+
+static float f32_div_up(float a, float b) {
+  int old = fegetround();
+  fesetround(FE_UPWARD);
+  volatile float va = a, vb = b;
+  volatile float r = va / vb;
+  fesetround(old);
+  return r;
+}
+
+/* round-to-nearest float ops (default mode); volatile keeps each one a single rounding */
+static float f32_sub(float a, float b) { volatile float r = a - b; return r; }
+static float f32_add(float a, float b) { volatile float r = a + b; return r; }
+static float f32_mul(float a, float b) { volatile float r = a * b; return r; }
+static float f32_rcp(float a) { volatile float one = 1.0f; volatile float r = one / a; return r; }
+
+/* ------------------------------------------------------------------ */
+/* step 1: Query statistics  ([QWM-zh] 二阶Query统计; steps (1),(4); [QWM-en] §D.1) */
+/* ------------------------------------------------------------------ */
+
+/* S[d][d] += sum over the nq Queries of q q^T (fp64).  Incremental: no Query is kept. */
+void oracle_stats_accumulate(const uint16_t *q, int64_t nq, int d, double *S) {
+  double *qd = (double *)malloc(sizeof(double) * d);
+  for (int64_t i = 0; i < nq; i++) {
+    for (int c = 0; c < d; c++) qd[c] = bf16_val(q[i * d + c]);
+    for (int a = 0; a < d; a++)
+      for (int b = 0; b < d; b++) S[a * d + b] += qd[a] * qd[b];
+  }
+  free(qd);
+}
+
+/* Channel sensitivity weights w_c = M_cc = S_cc / N (diagonal of the second moment).
+ * Cold start (N == 0): uniform w = 1 ([QWM-zh] step (1), [QWM-en] §C.3). */
+void oracle_weights(const double *S, int64_t n, int d, double *w) {
+  for (int c = 0; c < d; c++) w[c] = (n == 0) ? 1.0 : S[c * d + c] / (double)n;
+}
+
+/* Symmetric eigendecomposition M = U diag(lambda) U^T by the cyclic Jacobi
+ * method (Golub & Van Loan, "Matrix Computations", sec. 8.5 -- two-sided
+ * rotations zeroing one off-diagonal pair at a time).
+ * Output: lambda[d] descending; U[c*d + k] = component c of eigenvector k.
+ * Returns the number of sweeps used, or -1 when max_sweeps was not enough. */
+int oracle_eig_sym(const double *M, int d, double tol_rel, int max_sweeps, double *lambda, double *U) {
+  double *A = (double *)malloc(sizeof(double) * d * d);
+  double *V = (double *)malloc(sizeof(double) * d * d);
+  memcpy(A, M, sizeof(double) * d * d);
+  for (int i = 0; i < d * d; i++) V[i] = 0.0;
+  for (int i = 0; i < d; i++) V[i * d + i] = 1.0;
+  double fro = 0.0;
+  for (int i = 0; i < d * d; i++) fro += M[i] * M[i];
+  fro = sqrt(fro);
+  int sweeps = 0, converged = 0;
+  for (; sweeps <= max_sweeps; sweeps++) {
+    double off = 0.0;
+    for (int p = 0; p < d; p++)
+      for (int q = 0; q < d; q++)
+        if (p != q) off += A[p * d + q] * A[p * d + q];
+    if (sqrt(off) <= tol_rel * fro || fro == 0.0) { converged = 1; break; }
+    if (sweeps == max_sweeps) break;
+    for (int p = 0; p < d - 1; p++) {
+      for (int q = p + 1; q < d; q++) {
+        double apq = A[p * d + q];
+        if (apq == 0.0) continue;
+        double app = A[p * d + p], aqq = A[q * d + q];
+        double tau = (aqq - app) / (2.0 * apq);
+        double t = (tau >= 0 ? 1.0 : -1.0) / (fabs(tau) + sqrt(1.0 + tau * tau));
+        double c = 1.0 / sqrt(1.0 + t * t), s = t * c;
+        /* A <- J^T A J with J = rotation in the (p, q) plane */
+        for (int k = 0; k < d; k++) { /* columns p and q */
+          double akp = A[k * d + p], akq = A[k * d + q];
+          A[k * d + p] = c * akp - s * akq;
+          A[k * d + q] = s * akp + c * akq;
+        }
+        for (int k = 0; k < d; k++) { /* rows p and q */
+          double apk = A[p * d + k], aqk = A[q * d + k];
+          A[p * d + k] = c * apk - s * aqk;
+          A[q * d + k] = s * apk + c * aqk;
+        }
+        A[p * d + q] = 0.0;
+        A[q * d + p] = 0.0;
+        for (int k = 0; k < d; k++) { /* V <- V J */
+          double vkp = V[k * d + p], vkq = V[k * d + q];
+          V[k * d + p] = c * vkp - s * vkq;
+          V[k * d + q] = s * vkp + c * vkq;
+        }
+      }
+    }
+  }
+  /* order by descending eigenvalue, ties to the lower original index (stable selection) */
+  int *order = (int *)malloc(sizeof(int) * d);
+  char *used = (char *)calloc(d, 1);
+  for (int k = 0; k < d; k++) {
+    int best = -1;
+    for (int i = 0; i < d; i++)
+      if (!used[i] && (best < 0 || A[i * d + i] > A[best * d + best])) best = i;
+    used[best] = 1;
+    order[k] = best;
+  }
+  for (int k = 0; k < d; k++) {
+    int src = order[k];
+    lambda[k] = A[src * d + src];
+    /* sign: largest-magnitude component positive, lowest channel on ties */
+    int arg = 0;
+    for (int c = 1; c < d; c++)
+      if (fabs(V[c * d + src]) > fabs(V[arg * d + src])) arg = c;
+    double sg = V[arg * d + src] < 0 ? -1.0 : 1.0;
+    for (int c = 0; c < d; c++) U[c * d + k] = sg * V[c * d + src];
+  }
+  free(order);
+  free(used);
+  free(A);
+  free(V);
+  return converged ? sweeps : -1;
+}
+
+/* U_r: the first r eigenvectors rounded to bf16 (PSAC stores U_r in BF16: [QWM-ko] 어떻게 쓰나,
+ * [QWM-en] §5.1).  out[c*r + k] = bf16(U[c*d + k]). */
+void oracle_basis_bf16(const double *U, int d, int r, uint16_t *out) {
+  for (int c = 0; c < d; c++)
+    for (int k = 0; k < r; k++) out[c * r + k] = bf16_rne(U[c * d + k]);
+}
+
+/* ------------------------------------------------------------------ */
+/* step 2a: k-means codebook ([QVG-ko] §2A grouping along the sequence axis; §2C warm start) */
+/* ------------------------------------------------------------------ */
+
+static double sqdist_bf16_f64(const uint16_t *x, const double *mu, int d) {
+  double s = 0.0;
+  for (int c = 0; c < d; c++) {
+    double t = bf16_val(x[c]) - mu[c];
+    s += t * t;
+  }
+  return s;
+}
+
+/* Lloyd's algorithm on x[n][d] (bf16) with C centroids, `iters` iterations of
+ * (assign to the nearest centroid; replace each centroid by the mean of its members).
+ * init == NULL: centroid j starts at token floor(j n / C); else at init[j] (bf16).
+ * cent_out[C][d] bf16; optional: assign_out[n] (assignment of the last iteration),
+ * obj_out[iters] (sum of squared distances at each assignment step). */
+void oracle_kmeans(const uint16_t *x, int64_t n, int d, int C, const uint16_t *init, int iters,
+                   uint16_t *cent_out, double *cent_f64_out, int32_t *assign_out, double *obj_out) {
+  double *mu = (double *)malloc(sizeof(double) * C * d);
+  double *sum = (double *)malloc(sizeof(double) * C * d);
+  int64_t *cnt = (int64_t *)malloc(sizeof(int64_t) * C);
+  int32_t *asg = (int32_t *)malloc(sizeof(int32_t) * (n > 0 ? n : 1));
+  for (int j = 0; j < C; j++) {
+    const uint16_t *src = init ? init + (int64_t)j * d : x + ((int64_t)j * n / C) * d;
+    for (int c = 0; c < d; c++) mu[j * d + c] = bf16_val(src[c]);
+  }
+  for (int it = 0; it < iters; it++) {
+    double obj = 0.0;
+#pragma omp parallel for reduction(+ : obj) schedule(static)
+    for (int64_t i = 0; i < n; i++) {
+      int best = 0;
+      double bd = sqdist_bf16_f64(x + i * d, mu, d);
+      for (int j = 1; j < C; j++) {
+        double dj = sqdist_bf16_f64(x + i * d, mu + (int64_t)j * d, d);
+        if (dj < bd) { bd = dj; best = j; }
+      }
+      asg[i] = best;
+      obj += bd;
+    }
+    if (obj_out) obj_out[it] = obj;
+    memset(sum, 0, sizeof(double) * C * d);
+    memset(cnt, 0, sizeof(int64_t) * C);
+    for (int64_t i = 0; i < n; i++) {
+      int j = asg[i];
+      cnt[j]++;
+      for (int c = 0; c < d; c++) sum[j * d + c] += bf16_val(x[i * d + c]);
+    }
+    for (int j = 0; j < C; j++)
+      if (cnt[j] > 0)
+        for (int c = 0; c < d; c++) mu[j * d + c] = sum[j * d + c] / (double)cnt[j];
+  }
+  for (int j = 0; j < C * d; j++) cent_out[j] = bf16_rne(mu[j]);
+  if (cent_f64_out) memcpy(cent_f64_out, mu, sizeof(double) * C * d);
+  if (assign_out) memcpy(assign_out, asg, sizeof(int32_t) * n);
+  free(mu);
+  free(sum);
+  free(cnt);
+  free(asg);
+}
+
+/* Sum over tokens of the squared distance to the nearest centroid (bf16 centroids). */
+double oracle_kmeans_objective(const uint16_t *x, int64_t n, int d, const uint16_t *cent, int C) {
+  double *mu = (double *)malloc(sizeof(double) * C * d);
+  for (int j = 0; j < C * d; j++) mu[j] = bf16_val(cent[j]);
+  double obj = 0.0;
+#pragma omp parallel for reduction(+ : obj) schedule(static)
+  for (int64_t i = 0; i < n; i++) {
+    double bd = INFINITY;
+    for (int j = 0; j < C; j++) {
+      double dj = sqdist_bf16_f64(x + i * d, mu + (int64_t)j * d, d);
+      if (dj < bd) bd = dj;
+    }
+    obj += bd;
+  }
+  free(mu);
+  return obj;
+}
+
+/* ------------------------------------------------------------------ */
+/* step 3: INT2 affine quantiser ([QWM-zh] 前置知识 "低比特KV缓存量化", step (3); [QWM-en] §D.1) */
+/* ------------------------------------------------------------------ */
+
+/* Encode one group of g float residuals.  Writes codes[g] in 0..3 and the fp16
+ * bit patterns of the scale s and the offset m. */
+void oracle_int2_encode_group(const float *r, int g, uint8_t *codes, uint16_t *s_bits, uint16_t *m_bits) {
+  float mn = r[0], mx = r[0];
+  for (int c = 1; c < g; c++) {
+    if (r[c] < mn) mn = r[c];
+    if (r[c] > mx) mx = r[c];
+  }
+  double m = fp16_round((double)mn, -1);            /* m <= min r */
+  float range = f32_sub_up(mx, (float)m);             /* >= max r - m */
+  double s = (range == 0.0f) ? 0.0 : fp16_round((double)f32_div_up(range, 3.0f), +1); /* >= range / 3 */
+  *s_bits = fp16_bits_of(s);
+  *m_bits = fp16_bits_of(m);
+  if (s == 0.0) {
+    for (int c = 0; c < g; c++) codes[c] = 0;
+    return;
+  }
+  float inv = f32_rcp((float)s);
+  for (int c = 0; c < g; c++) {
+    float y = f32_mul(f32_sub(r[c], (float)m), inv);
+    float q = nearbyintf(y); /* ties to even */
+    if (q < 0.0f) q = 0.0f;
+    if (q > 3.0f) q = 3.0f;
+    codes[c] = (uint8_t)q;
+  }
+}
+
+/* r_hat = m + s q, computed in float (s q is exact; one rounding for the sum). */
+static float int2_decode(uint16_t s_bits, uint16_t m_bits, int q) {
+  float s = (float)oracle_fp16_val(s_bits), m = (float)oracle_fp16_val(m_bits);
+  return f32_add(m, f32_mul(s, (float)q));
+}
+
+/* Pack codes[d] (0..3) four per byte: channel 4j+t goes to bits 2t..2t+1 of byte j
+ * ([QWM-zh] step (3): "INT2残差4码并1字节"). */
+void oracle_pack2(const uint8_t *codes, int d, uint8_t *packed) {
+  for (int j = 0; j < d / 4; j++) {
+    uint8_t b = 0;
+    for (int t = 0; t < 4; t++) b |= (uint8_t)((codes[4 * j + t] & 3) << (2 * t));
+    packed[j] = b;
+  }
+}
+
+static int unpack2(const uint8_t *packed, int c) { return (packed[c >> 2] >> (2 * (c & 3))) & 3; }
+
+/* INT8 of one token's PSAC coefficients C[r] (fp32 in): per-token symmetric scale. */
+void oracle_int8_encode_token(const float *C, int r, int8_t *c_out, uint16_t *sc_bits) {
+  float a = 0.0f;
+  for (int k = 0; k < r; k++)
+    if (fabsf(C[k]) > a) a = fabsf(C[k]);
+  double sc = (a == 0.0f) ? 0.0 : fp16_round((double)f32_div_up(a, 127.0f), +1);
+  *sc_bits = fp16_bits_of(sc);
+  if (sc == 0.0) {
+    for (int k = 0; k < r; k++) c_out[k] = 0;
+    return;
+  }
+  float inv = f32_rcp((float)sc);
+  for (int k = 0; k < r; k++) {
+    float q = nearbyintf(f32_mul(C[k], inv));
+    if (q < -127.0f) q = -127.0f;
+    if (q > 127.0f) q = 127.0f;
+    c_out[k] = (int8_t)q;
+  }
+}
+
+/* ------------------------------------------------------------------ */
+/* steps 2-4 for one head of one chunk                                 */
+/* ------------------------------------------------------------------ */
+
+/* Query-aware distance d_Q(k, mu) = sum_c w_c (k_c - mu_c)^2  ([QWM-zh] 核心方法; [QWM-ko] 무엇과 다른가) */
+static double dq_dist(const uint16_t *k, const uint16_t *mu, const double *w, int d) {
+  double s = 0.0;
+  for (int c = 0; c < d; c++) {
+    double t = bf16_val(k[c]) - bf16_val(mu[c]);
+    s += w[c] * t * t;
+  }
+  return s;
+}
+
+/* QSAC score S(k, mu) = sum_g (sum_{c in G_g} w_c) R_g(k - mu)^2 with R_g = max - min of the
+ * residual over the group (INT2 error estimate R_g^2 / [12 (2^b - 1)^2] with the constant dropped). */
+static double qsac_score(const uint16_t *k, const uint16_t *mu, const double *w, int d, int group) {
+  double S = 0.0;
+  for (int g0 = 0; g0 < d; g0 += group) {
+    float mn = INFINITY, mx = -INFINITY;
+    double W = 0.0;
+    for (int c = g0; c < g0 + group; c++) {
+      float r = f32_sub(bf16_valf(k[c]), bf16_valf(mu[c]));
+      if (r < mn) mn = r;
+      if (r > mx) mx = r;
+      W += w[c];
+    }
+    double R = (double)mx - (double)mn;
+    S += W * R * R;
+  }
+  return S;
+}
+
+typedef struct {
+  /* inputs */
+  const uint16_t *k, *v;          /* [n][d] bf16 */
+  const uint16_t *cent_k, *cent_v;/* [C][d] bf16 */
+  const double *w;                /* [d] or NULL (uniform) */
+  const uint16_t *u_r;            /* [d][rank] bf16 or NULL (PSAC off) */
+  const double *u_r_f64;          /* optional [d][rank] double basis used instead of u_r (exactness checks) */
+  const int32_t *force_idx_k;     /* [n] or NULL: use these Key centroids instead of QSAC */
+  const int32_t *force_idx_v;     /* [n] or NULL */
+  int64_t n;
+  int32_t d, C, group, top_m, rank;
+  /* outputs */
+  int32_t *idx_k, *idx_v;         /* [n] */
+  uint8_t *k_codes, *v_codes;     /* [n][d/4] */
+  uint16_t *k_scale, *k_min, *v_scale, *v_min; /* fp16 [n][d/group] */
+  int8_t *c;                      /* [n][rank] (when u_r) */
+  uint16_t *c_scale;              /* fp16 [n] (when u_r) */
+  double *c_real;                 /* optional [n][rank]: C before INT8 */
+  int32_t *cand;                  /* optional [n][top_m]: candidates, ascending d_Q */
+  double *score2;                 /* optional [n][2]: best and second-best S over the candidates */
+  double *dq_edge;                /* optional [n][2]: the M-th and (M+1)-th smallest d_Q */
+  double *vdist2;                 /* optional [n][2]: best and second-best Value distance */
+} oracle_quant_args;
+
+void oracle_quantize_head(const oracle_quant_args *a) {
+  const int d = a->d, C = a->C, G = d / a->group, M = a->top_m, r = a->rank;
+  double *w = (double *)malloc(sizeof(double) * d);
+  for (int c = 0; c < d; c++) w[c] = a->w ? a->w[c] : 1.0;
+#pragma omp parallel
+  {
+    double *dq = (double *)malloc(sizeof(double) * C);
+    int *sel = (int *)malloc(sizeof(int) * (M + 1));
+    float *res = (float *)malloc(sizeof(float) * d);
+    uint8_t *codes = (uint8_t *)malloc(d);
+    float *khat0 = (float *)malloc(sizeof(float) * d);
+    float *Cf = (float *)malloc(sizeof(float) * (r > 0 ? r : 1));
+#pragma omp for schedule(static)
+    for (int64_t i = 0; i < a->n; i++) {
+      const uint16_t *k = a->k + i * d, *v = a->v + i * d;
+      int jk;
+      /* ---- step 2: QSAC Key centroid ---- */
+      for (int j = 0; j < C; j++) dq[j] = dq_dist(k, a->cent_k + (int64_t)j * d, w, d);
+      int nsel = (M + 1 <= C) ? M + 1 : C;
+      for (int t = 0; t < nsel; t++) { /* t-th smallest d_Q, ties to the lower index */
+        int best = -1;
+        for (int j = 0; j < C; j++) {
+          int taken = 0;
+          for (int u = 0; u < t; u++) taken |= (sel[u] == j);
+          if (!taken && (best < 0 || dq[j] < dq[best])) best = j;
+        }
+        sel[t] = best;
+      }
+      int ncand = (M <= C) ? M : C;
+      int bj = -1;
+      double bs = INFINITY, s2 = INFINITY;
+      for (int t = 0; t < ncand; t++) {
+        int j = sel[t];
+        double S = qsac_score(k, a->cent_k + (int64_t)j * d, w, d, a->group);
+        if (S < bs || (S == bs && j < bj)) { s2 = bs; bs = S; bj = j; }
+        else if (S < s2) s2 = S;
+      }
+      if (a->cand) for (int t = 0; t < M; t++) a->cand[i * M + t] = (t < ncand) ? sel[t] : -1;
+      if (a->score2) { a->score2[2 * i] = bs; a->score2[2 * i + 1] = s2; }
+      if (a->dq_edge) {
+        a->dq_edge[2 * i] = dq[sel[ncand - 1]];
+        a->dq_edge[2 * i + 1] = (nsel > ncand) ? dq[sel[ncand]] : INFINITY;
+      }
+      jk = a->force_idx_k ? a->force_idx_k[i] : bj;
+      a->idx_k[i] = jk;
+      /* ---- Values: nearest centroid, as in QVG ---- */
+      int jv = 0;
+      double bv = INFINITY, bv2 = INFINITY;
+      for (int j = 0; j < C; j++) {
+        double s = 0.0;
+        const uint16_t *mu = a->cent_v + (int64_t)j * d;
+        for (int c = 0; c < d; c++) {
+          double t = bf16_val(v[c]) - bf16_val(mu[c]);
+          s += t * t;
+        }
+        if (s < bv) { bv2 = bv; bv = s; jv = j; }
+        else if (s < bv2) bv2 = s;
+      }
+      if (a->vdist2) { a->vdist2[2 * i] = bv; a->vdist2[2 * i + 1] = bv2; }
+      if (a->force_idx_v) jv = a->force_idx_v[i];
+      a->idx_v[i] = jv;
+      /* ---- step 3: INT2 residuals, Keys then Values ---- */
+      for (int pass = 0; pass < 2; pass++) {
+        const uint16_t *x = pass ? v : k;
+        const uint16_t *mu = pass ? a->cent_v + (int64_t)jv * d : a->cent_k + (int64_t)jk * d;
+        uint8_t *packed = (pass ? a->v_codes : a->k_codes) + i * (d / 4);
+        uint16_t *sc = (pass ? a->v_scale : a->k_scale) + i * G;
+        uint16_t *mn = (pass ? a->v_min : a->k_min) + i * G;
+        for (int c = 0; c < d; c++) res[c] = f32_sub(bf16_valf(x[c]), bf16_valf(mu[c]));
+        for (int g = 0; g < G; g++)
+          oracle_int2_encode_group(res + g * a->group, a->group, codes + g * a->group, sc + g, mn + g);
+        oracle_pack2(codes, d, packed);
+        if (pass == 0) /* K_hat_0 = mu + r_hat, float */
+          for (int c = 0; c < d; c++) {
+            int g = c / a->group;
+            khat0[c] = f32_add(bf16_valf(mu[c]), int2_decode(sc[g], mn[g], codes[c]));
+          }
+      }
+      /* ---- step 4: PSAC  E = K - K_hat_0,  C = E U_r ---- */
+      if ((a->u_r || a->u_r_f64) && r > 0) {
+        for (int kk = 0; kk < r; kk++) {
+          double acc = 0.0;
+          for (int c = 0; c < d; c++) {
+            double e = (double)bf16_valf(k[c]) - (double)khat0[c];
+            acc += e * (a->u_r_f64 ? a->u_r_f64[c * r + kk] : bf16_val(a->u_r[c * r + kk]));
+          }
+          if (a->c_real) a->c_real[i * r + kk] = acc;
+          Cf[kk] = (float)acc;
+        }
+        oracle_int8_encode_token(Cf, r, a->c + i * r, a->c_scale + i);
+      }
+    }
+    free(dq);
+    free(sel);
+    free(res);
+    free(codes);
+    free(khat0);
+    free(Cf);
+  }
+  free(w);
+}
+
+/* ------------------------------------------------------------------ */
+/* step 5: attention over the compressed cache, and the BF16 decoder     */
+/* ([QWM-zh] logits L = Q K^T / sqrt(d); PSAC form Q K_hat_0^T + (Q U_r) C^T; step (5)) */
+/* ------------------------------------------------------------------ */
+
+typedef struct {
+  int64_t n;
+  int32_t rank; /* 0: no PSAC term */
+  const int32_t *idx_k, *idx_v;
+  const uint8_t *k_codes, *v_codes;
+  const uint16_t *k_scale, *k_min, *v_scale, *v_min;
+  const uint16_t *cent_k, *cent_v;
+  const int8_t *c;
+  const uint16_t *c_scale;
+  const uint16_t *u_r; /* [d][rank] */
+} oracle_chunk_head;
+
+/* dequantised Key base k_hat_0 = mu_idx + r_hat and Value v_hat, as doubles */
+static void decode_token(const oracle_chunk_head *ch, int d, int group, int64_t j, double *kh0, double *vh) {
+  const int G = d / group;
+  const uint16_t *muk = ch->cent_k + (int64_t)ch->idx_k[j] * d;
+  const uint16_t *muv = ch->cent_v + (int64_t)ch->idx_v[j] * d;
+  for (int c = 0; c < d; c++) {
+    int g = c / group;
+    kh0[c] = bf16_val(muk[c]) + (double)int2_decode(ch->k_scale[j * G + g], ch->k_min[j * G + g],
+                                                    unpack2(ch->k_codes + j * (d / 4), c));
+    vh[c] = bf16_val(muv[c]) + (double)int2_decode(ch->v_scale[j * G + g], ch->v_min[j * G + g],
+                                                   unpack2(ch->v_codes + j * (d / 4), c));
+  }
+}
+
+/* For each listed query row, o = softmax(l) V_hat over every token of every chunk, with
+ * l_j = scale * (q . k_hat_0_j + (q U_r^(chunk)) . c_hat_j),  c_hat = sC * c.
+ * Softmax in double with the running maximum subtracted.  out[rows][d] double. */
+void oracle_attend_rows(const uint16_t *q, int d, int group, const int64_t *rows, int64_t n_rows,
+                        const oracle_chunk_head *chunks, int n_chunks, double scale, double *out) {
+  int64_t total = 0;
+  for (int t = 0; t < n_chunks; t++) total += chunks[t].n;
+#pragma omp parallel
+  {
+    double *l = (double *)malloc(sizeof(double) * (total > 0 ? total : 1));
+    double *kh0 = (double *)malloc(sizeof(double) * d);
+    double *vh = (double *)malloc(sizeof(double) * d);
+    double *qd = (double *)malloc(sizeof(double) * d);
+    double *qu = (double *)malloc(sizeof(double) * 64);
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t ri = 0; ri < n_rows; ri++) {
+      const uint16_t *qq = q + rows[ri] * d;
+      for (int c = 0; c < d; c++) qd[c] = bf16_val(qq[c]);
+      double lmax = -INFINITY;
+      int64_t off = 0;
+      for (int t = 0; t < n_chunks; t++) {
+        const oracle_chunk_head *ch = &chunks[t];
+        for (int kk = 0; kk < ch->rank; kk++) {
+          double s = 0.0;
+          for (int c = 0; c < d; c++) s += qd[c] * bf16_val(ch->u_r[c * ch->rank + kk]);
+          qu[kk] = s;
+        }
+        for (int64_t j = 0; j < ch->n; j++) {
+          decode_token(ch, d, group, j, kh0, vh);
+          double s = 0.0;
+          for (int c = 0; c < d; c++) s += qd[c] * kh0[c];
+          if (ch->rank > 0) {
+            double sc = oracle_fp16_val(ch->c_scale[j]);
+            for (int kk = 0; kk < ch->rank; kk++) s += qu[kk] * (sc * (double)ch->c[j * ch->rank + kk]);
+          }
+          l[off + j] = scale * s;
+          if (l[off + j] > lmax) lmax = l[off + j];
+        }
+        off += ch->n;
+      }
+      double *o = out + ri * d;
+      for (int c = 0; c < d; c++) o[c] = 0.0;
+      double denom = 0.0;
+      off = 0;
+      for (int t = 0; t < n_chunks; t++) {
+        const oracle_chunk_head *ch = &chunks[t];
+        for (int64_t j = 0; j < ch->n; j++) {
+          double p = exp(l[off + j] - lmax);
+          denom += p;
+          decode_token(ch, d, group, j, kh0, vh);
+          for (int c = 0; c < d; c++) o[c] += p * vh[c];
+        }
+        off += ch->n;
+      }
+      for (int c = 0; c < d; c++) o[c] /= denom;
+    }
+    free(l);
+    free(kh0);
+    free(vh);
+    free(qd);
+    free(qu);
+  }
+}
+
+/* BF16 reconstruction of one head of one chunk ([QWM-zh] step (5) fused decoder semantics):
+ * K_hat = K_hat_0 + c_hat U_r^T, V_hat = mu^V_idx + r_hat; optional double outputs. */
+void oracle_dequantize_head(const oracle_chunk_head *ch, int d, int group, uint16_t *k_hat, uint16_t *v_hat,
+                            double *k_hat_f64, double *v_hat_f64) {
+#pragma omp parallel
+  {
+    double *kh0 = (double *)malloc(sizeof(double) * d);
+    double *vh = (double *)malloc(sizeof(double) * d);
+#pragma omp for schedule(static)
+    for (int64_t j = 0; j < ch->n; j++) {
+      decode_token(ch, d, group, j, kh0, vh);
+      for (int c = 0; c < d; c++) {
+        double kv = kh0[c];
+        if (ch->rank > 0) {
+          double sc = oracle_fp16_val(ch->c_scale[j]);
+          for (int kk = 0; kk < ch->rank; kk++)
+            kv += sc * (double)ch->c[j * ch->rank + kk] * bf16_val(ch->u_r[c * ch->rank + kk]);
+        }
+        if (k_hat) k_hat[j * d + c] = bf16_rne(kv);
+        if (v_hat) v_hat[j * d + c] = bf16_rne(vh[c]);
+        if (k_hat_f64) k_hat_f64[j * d + c] = kv;
+        if (v_hat_f64) v_hat_f64[j * d + c] = vh[c];
+      }
+    }
+    free(kh0);
+    free(vh);
+  }
+}
+
+/* Small helpers exported for the oracle's own tests. */
+double oracle_round_fp16(double x, int dir) { return fp16_round(x, dir); }
+uint16_t oracle_fp16_bits(double v) { return fp16_bits_of(v); }
+uint16_t oracle_bf16_rne(double x) { return bf16_rne(x); }
