@@ -1,0 +1,255 @@
+"""Python binding of libqwm.so, the GB300 (sm_103a) QuantWM quantise-and-attend library.
+
+The functions mirror the C ABI in include/qwm.h one to one (same names, same
+argument order) and only marshal arguments: every step of the path runs in the
+library's CUDA kernels.  Tensors are torch CUDA tensors (PyTorch provides the
+device memory and the stream); bf16 data may be torch.bfloat16 or 16-bit integer
+tensors holding the bit patterns, fp16 data torch.float16 or 16-bit integers.
+
+Importing this package loads the in-tree libqwm.so and raises when it is missing:
+there is no fallback path.  Build it with `python -m bit_kv_cache_qsac_gb300.build`
+(or `__graft_entry__.build()`).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libqwm.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libqwm.so not found at {LIB_PATH}: build it with "
+                      "`python -m bit_kv_cache_qsac_gb300.build` before importing this package")
+
+_lib = C.CDLL(LIB_PATH)
+
+QWM_OK, QWM_ERR_ARG, QWM_ERR_SHAPE, QWM_ERR_ALIGN, QWM_ERR_CUDA, QWM_ERR_NOT_CONVERGED, \
+    QWM_ERR_UNSUPPORTED, QWM_ERR_RANGE = range(8)
+
+EXPORTED = ("qwm_status_string", "qwm_workspace_bytes", "qwm_create", "qwm_destroy",
+            "qwm_update_query_stats", "qwm_fit_centroids", "qwm_quantize_kv", "qwm_attend",
+            "qwm_dequantize", "qwm_sync_status")
+
+
+class QwmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _lib.qwm_status_string(status).decode()
+        super().__init__(f"{where}: {msg} (status {status})")
+
+
+class qwm_config(C.Structure):
+    _fields_ = [("heads", C.c_int32), ("head_dim", C.c_int32), ("n_centroids", C.c_int32),
+                ("group", C.c_int32), ("top_m", C.c_int32), ("rank", C.c_int32), ("bits", C.c_int32),
+                ("kmeans_iters", C.c_int32), ("seed", C.c_uint64)]
+
+
+class qwm_chunk(C.Structure):
+    _fields_ = [("n_tokens", C.c_int64), ("rank_eff", C.c_int32), ("reserved", C.c_int32),
+                ("k_codes", C.c_void_p), ("v_codes", C.c_void_p), ("k_idx", C.c_void_p), ("v_idx", C.c_void_p),
+                ("k_scale", C.c_void_p), ("k_min", C.c_void_p), ("v_scale", C.c_void_p), ("v_min", C.c_void_p),
+                ("cent_k", C.c_void_p), ("cent_v", C.c_void_p), ("c", C.c_void_p), ("c_scale", C.c_void_p),
+                ("u_r", C.c_void_p)]
+
+
+class qwm_debug(C.Structure):
+    _fields_ = [("c_f32", C.c_void_p), ("cand", C.c_void_p), ("score", C.c_void_p)]
+
+
+_P = C.c_void_p
+_lib.qwm_status_string.argtypes = [C.c_int]
+_lib.qwm_status_string.restype = C.c_char_p
+_lib.qwm_workspace_bytes.argtypes = [C.POINTER(qwm_config)]
+_lib.qwm_workspace_bytes.restype = C.c_size_t
+_lib.qwm_create.argtypes = [C.POINTER(qwm_config), C.POINTER(C.c_void_p)]
+_lib.qwm_destroy.argtypes = [_P]
+_lib.qwm_update_query_stats.argtypes = [_P, _P, C.c_int64, _P, _P, _P, _P, _P, _P]
+_lib.qwm_fit_centroids.argtypes = [_P, _P, C.c_int64, _P, _P, _P]
+_lib.qwm_quantize_kv.argtypes = [_P, _P, _P, C.c_int64, _P, _P, C.POINTER(qwm_chunk), C.POINTER(qwm_debug), _P]
+_lib.qwm_attend.argtypes = [_P, _P, C.c_int64, C.POINTER(qwm_chunk), C.c_int32, C.c_float, _P, _P]
+_lib.qwm_dequantize.argtypes = [_P, C.POINTER(qwm_chunk), _P, _P, _P]
+_lib.qwm_sync_status.argtypes = [_P, _P]
+for _name in EXPORTED[2:]:
+    getattr(_lib, _name).restype = C.c_int
+
+
+def _check(status: int, where: str) -> None:
+    if status != QWM_OK:
+        raise QwmError(status, where)
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+_WIDTH = {torch.bfloat16: 2, torch.float16: 2, torch.int16: 2, torch.uint16: 2, torch.float32: 4,
+          torch.int32: 4, torch.int64: 8, torch.uint8: 1, torch.int8: 1}
+
+
+def _ptr(t: torch.Tensor | None, name: str, width: int, shape: tuple | None = None) -> int | None:
+    """Device pointer of a dense CUDA tensor with the given element width (and shape, when given)."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name}: expected a CUDA tensor")
+    if _WIDTH.get(t.dtype) != width:
+        raise TypeError(f"{name}: expected {width}-byte elements, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: tensor must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t.data_ptr()
+
+
+class Context:
+    """Owns a qwm_ctx (its device workspace lives on the current device)."""
+
+    def __init__(self, heads: int, n_centroids: int = 256, top_m: int = 4, rank: int = 8,
+                 kmeans_iters: int = 10, head_dim: int = 128, group: int = 64, bits: int = 2):
+        self.cfg = qwm_config(heads, head_dim, n_centroids, group, top_m, rank, bits, kmeans_iters, 0)
+        h = C.c_void_p()
+        _check(_lib.qwm_create(C.byref(self.cfg), C.byref(h)), "qwm_create")
+        self.handle = h
+
+    @property
+    def heads(self):
+        return self.cfg.heads
+
+    def close(self):
+        if self.handle:
+            _check(_lib.qwm_destroy(self.handle), "qwm_destroy")
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def qwm_workspace_bytes(cfg: qwm_config) -> int:
+    return _lib.qwm_workspace_bytes(C.byref(cfg))
+
+
+@dataclass
+class Chunk:
+    """Device tensors of one packed chunk (all heads), mirroring qwm_chunk."""
+    n_tokens: int
+    rank_eff: int
+    k_codes: torch.Tensor
+    v_codes: torch.Tensor
+    k_idx: torch.Tensor
+    v_idx: torch.Tensor
+    k_scale: torch.Tensor
+    k_min: torch.Tensor
+    v_scale: torch.Tensor
+    v_min: torch.Tensor
+    cent_k: torch.Tensor
+    cent_v: torch.Tensor
+    c: torch.Tensor
+    c_scale: torch.Tensor
+    u_r: torch.Tensor
+
+    @staticmethod
+    def empty(ctx: Context, n: int, device=None) -> "Chunk":
+        cfg = ctx.cfg
+        H, d, G, Cn, r = cfg.heads, cfg.head_dim, cfg.head_dim // cfg.group, cfg.n_centroids, cfg.rank
+        dev = device or torch.device("cuda", torch.cuda.current_device())
+        u8 = dict(dtype=torch.uint8, device=dev)
+        f16 = dict(dtype=torch.float16, device=dev)
+        return Chunk(n, 0,
+                     torch.empty(H, n, d // 4, **u8), torch.empty(H, n, d // 4, **u8),
+                     torch.empty(H, n, **u8), torch.empty(H, n, **u8),
+                     torch.empty(H, n, G, **f16), torch.empty(H, n, G, **f16),
+                     torch.empty(H, n, G, **f16), torch.empty(H, n, G, **f16),
+                     torch.empty(H, Cn, d, dtype=torch.bfloat16, device=dev),
+                     torch.empty(H, Cn, d, dtype=torch.bfloat16, device=dev),
+                     torch.zeros(H, n, max(r, 1), dtype=torch.int8, device=dev),
+                     torch.zeros(H, n, **f16),
+                     torch.zeros(H, d, max(r, 1), dtype=torch.bfloat16, device=dev))
+
+    def nbytes(self) -> int:
+        """Bytes of the packed representation (codebooks and PSAC basis included)."""
+        tot = sum(t.numel() * t.element_size() for t in (self.k_codes, self.v_codes, self.k_idx, self.v_idx,
+                                                         self.k_scale, self.k_min, self.v_scale, self.v_min,
+                                                         self.cent_k, self.cent_v))
+        if self.rank_eff:
+            tot += sum(t.numel() * t.element_size() for t in (self.c, self.c_scale, self.u_r))
+        return tot
+
+    def struct(self) -> qwm_chunk:
+        def p(t, width):
+            return _ptr(t, "chunk field", width)
+        return qwm_chunk(self.n_tokens, self.rank_eff, 0,
+                         p(self.k_codes, 1), p(self.v_codes, 1), p(self.k_idx, 1), p(self.v_idx, 1),
+                         p(self.k_scale, 2), p(self.k_min, 2), p(self.v_scale, 2), p(self.v_min, 2),
+                         p(self.cent_k, 2), p(self.cent_v, 2), p(self.c, 1), p(self.c_scale, 2), p(self.u_r, 2))
+
+
+def qwm_update_query_stats(ctx: Context, q, nq: int, S, n, w, eigvals, u_r, stream=None) -> None:
+    H, d, r = ctx.cfg.heads, ctx.cfg.head_dim, ctx.cfg.rank
+    st = _lib.qwm_update_query_stats(
+        ctx.handle, _ptr(q, "q", 2, (H, nq, d)) if nq else None, nq,
+        _ptr(S, "S", 4, (H, d, d)), _ptr(n, "n", 8, (H,)), _ptr(w, "w", 4, (H, d)),
+        _ptr(eigvals, "eigvals", 4, (H, d)), _ptr(u_r, "u_r", 2, (H, d, r)) if r else None, _stream(stream))
+    _check(st, "qwm_update_query_stats")
+
+
+def qwm_fit_centroids(ctx: Context, x, n: int, init, cent, stream=None) -> None:
+    H, d, Cn = ctx.cfg.heads, ctx.cfg.head_dim, ctx.cfg.n_centroids
+    st = _lib.qwm_fit_centroids(ctx.handle, _ptr(x, "x", 2, (H, n, d)), n, _ptr(init, "init", 2, (H, Cn, d)),
+                                _ptr(cent, "cent", 2, (H, Cn, d)), _stream(stream))
+    _check(st, "qwm_fit_centroids")
+
+
+def qwm_quantize_kv(ctx: Context, k, v, n: int, w, u_r, out: Chunk, debug: dict | None = None,
+                    stream=None) -> None:
+    """Fill `out` (whose cent_k / cent_v hold the chunk's codebooks).  When u_r is given, out.u_r
+    must be a tensor holding the same basis (the chunk keeps its own snapshot)."""
+    H, d, r = ctx.cfg.heads, ctx.cfg.head_dim, ctx.cfg.rank
+    s = out.struct()
+    dbg = None
+    if debug is not None:
+        dbg = qwm_debug(_ptr(debug.get("c_f32"), "c_f32", 4), _ptr(debug.get("cand"), "cand", 4),
+                        _ptr(debug.get("score"), "score", 4))
+    st = _lib.qwm_quantize_kv(ctx.handle, _ptr(k, "k", 2, (H, n, d)), _ptr(v, "v", 2, (H, n, d)), n,
+                              _ptr(w, "w", 4, (H, d)), _ptr(u_r, "u_r", 2, (H, d, r)) if r else None,
+                              C.byref(s), C.byref(dbg) if dbg is not None else None, _stream(stream))
+    _check(st, "qwm_quantize_kv")
+    out.rank_eff = s.rank_eff
+
+
+def qwm_attend(ctx: Context, q, nq: int, chunks: list, softmax_scale: float, out, stream=None) -> None:
+    H, d = ctx.cfg.heads, ctx.cfg.head_dim
+    arr = (qwm_chunk * len(chunks))(*[c.struct() for c in chunks])
+    st = _lib.qwm_attend(ctx.handle, _ptr(q, "q", 2, (H, nq, d)), nq, arr, len(chunks), float(softmax_scale),
+                         _ptr(out, "out", 2, (H, nq, d)), _stream(stream))
+    _check(st, "qwm_attend")
+
+
+def qwm_dequantize(ctx: Context, chunk: Chunk, k_hat, v_hat, stream=None) -> None:
+    H, d = ctx.cfg.heads, ctx.cfg.head_dim
+    s = chunk.struct()
+    st = _lib.qwm_dequantize(ctx.handle, C.byref(s), _ptr(k_hat, "k_hat", 2, (H, chunk.n_tokens, d)),
+                             _ptr(v_hat, "v_hat", 2, (H, chunk.n_tokens, d)), _stream(stream))
+    _check(st, "qwm_dequantize")
+
+
+def qwm_sync_status(ctx: Context, stream=None) -> int:
+    """Wait for the stream and return (and clear) the first device-side error status (0 = none)."""
+    return _lib.qwm_sync_status(ctx.handle, _stream(stream))
+
+
+def qwm_status_string(status: int) -> str:
+    return _lib.qwm_status_string(status).decode()
+
+
+def raw_library() -> C.CDLL:
+    """The loaded libqwm.so (for tests that inspect its exported symbols)."""
+    return _lib

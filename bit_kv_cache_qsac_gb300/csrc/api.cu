@@ -1,0 +1,227 @@
+// C ABI entry points of libqwm.so: argument checks, context, workspace, dispatch.
+#include <stdlib.h>
+#include <string.h>
+
+#include "qwm_internal.cuh"
+
+namespace {
+
+constexpr int kStatsSplits = 8;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Layout {
+  size_t status, stats_part, km_sum, km_cnt, km_cent, total;
+};
+
+Layout layout_of(const qwm_config &c) {
+  Layout L{};
+  size_t off = 0;
+  L.status = off; off = align_up(off + 256, 256);
+  L.stats_part = off; off = align_up(off + (size_t)kStatsSplits * c.heads * QWM_D * QWM_D * sizeof(float), 256);
+  L.km_sum = off; off = align_up(off + (size_t)c.heads * c.n_centroids * QWM_D * sizeof(float), 256);
+  L.km_cnt = off; off = align_up(off + (size_t)c.heads * c.n_centroids * sizeof(int32_t), 256);
+  L.km_cent = off; off = align_up(off + (size_t)c.heads * c.n_centroids * QWM_D * sizeof(float), 256);
+  L.total = off;
+  return L;
+}
+
+qwm_status check_config(const qwm_config *c) {
+  if (!c) return QWM_ERR_ARG;
+  if (c->heads < 1 || c->head_dim < 1 || c->n_centroids < 1 || c->group < 1 || c->top_m < 1 || c->rank < 0 ||
+      c->bits < 1 || c->kmeans_iters < 1)
+    return QWM_ERR_ARG;
+  if (c->head_dim != QWM_D || c->group != QWM_GROUP) return QWM_ERR_SHAPE;
+  if (c->bits != 2) return QWM_ERR_UNSUPPORTED;
+  if (!(c->n_centroids == 64 || c->n_centroids == 128 || c->n_centroids == 256)) return QWM_ERR_SHAPE;
+  if (c->top_m > QWM_MAX_TOPM || c->top_m > c->n_centroids) return QWM_ERR_SHAPE;
+  if (c->rank > QWM_MAX_RANK) return QWM_ERR_SHAPE;
+  if (c->kmeans_iters > 100) return QWM_ERR_SHAPE;
+  if ((int64_t)c->heads > 4096) return QWM_ERR_SHAPE;
+  return QWM_OK;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+qwm_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QWM_OK : QWM_ERR_CUDA; }
+
+// A chunk descriptor is usable when every pointer it needs is set and aligned.
+qwm_status check_chunk(const qwm_config &c, const qwm_chunk *ch, bool need_outputs) {
+  if (!ch) return QWM_ERR_ARG;
+  if (ch->n_tokens < 0) return QWM_ERR_ARG;
+  if (ch->rank_eff != 0 && ch->rank_eff != c.rank) return QWM_ERR_SHAPE;
+  const void *req[] = {ch->k_codes, ch->v_codes, ch->k_idx,  ch->v_idx,  ch->k_scale,
+                       ch->k_min,   ch->v_scale, ch->v_min, ch->cent_k, ch->cent_v};
+  for (const void *p : req) {
+    if (!p) return QWM_ERR_ARG;
+    if (!aligned16(p)) return QWM_ERR_ALIGN;
+  }
+  (void)need_outputs;
+  if (ch->rank_eff > 0) {
+    const void *psac[] = {ch->c, ch->c_scale, ch->u_r};
+    for (const void *p : psac) {
+      if (!p) return QWM_ERR_ARG;
+      if (!aligned16(p)) return QWM_ERR_ALIGN;
+    }
+  }
+  return QWM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *qwm_status_string(qwm_status s) {
+  switch (s) {
+    case QWM_OK: return "ok";
+    case QWM_ERR_ARG: return "invalid argument";
+    case QWM_ERR_SHAPE: return "unsupported shape";
+    case QWM_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case QWM_ERR_CUDA: return "CUDA error";
+    case QWM_ERR_NOT_CONVERGED: return "eigensolver did not converge within its sweep limit";
+    case QWM_ERR_UNSUPPORTED: return "unsupported configuration";
+    case QWM_ERR_RANGE: return "value outside the fp16 range";
+  }
+  return "unknown status";
+}
+
+size_t qwm_workspace_bytes(const qwm_config *cfg) {
+  if (check_config(cfg) != QWM_OK) return 0;
+  return layout_of(*cfg).total;
+}
+
+qwm_status qwm_create(const qwm_config *cfg, qwm_ctx **out) {
+  if (!out) return QWM_ERR_ARG;
+  *out = nullptr;
+  qwm_status s = check_config(cfg);
+  if (s != QWM_OK) return s;
+  qwm_ctx *ctx = (qwm_ctx *)calloc(1, sizeof(qwm_ctx));
+  if (!ctx) return QWM_ERR_ARG;
+  ctx->cfg = *cfg;
+  if (cudaGetDevice(&ctx->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, ctx->device) != cudaSuccess) {
+    free(ctx);
+    return QWM_ERR_CUDA;
+  }
+  Layout L = layout_of(*cfg);
+  if (cudaMalloc(&ctx->ws, L.total) != cudaSuccess) {
+    free(ctx);
+    return QWM_ERR_CUDA;
+  }
+  if (cudaMemset(ctx->ws, 0, L.total) != cudaSuccess) {
+    cudaFree(ctx->ws);
+    free(ctx);
+    return QWM_ERR_CUDA;
+  }
+  char *base = (char *)ctx->ws;
+  ctx->ws_bytes = L.total;
+  ctx->status = (int32_t *)(base + L.status);
+  ctx->stats_part = (float *)(base + L.stats_part);
+  ctx->stats_splits = kStatsSplits;
+  ctx->km_sum = (float *)(base + L.km_sum);
+  ctx->km_cnt = (int32_t *)(base + L.km_cnt);
+  ctx->km_cent = (float *)(base + L.km_cent);
+  *out = ctx;
+  return QWM_OK;
+}
+
+qwm_status qwm_destroy(qwm_ctx *ctx) {
+  if (!ctx) return QWM_ERR_ARG;
+  cudaError_t e = cudaFree(ctx->ws);
+  free(ctx);
+  return cuda_status(e);
+}
+
+qwm_status qwm_update_query_stats(qwm_ctx *ctx, const uint16_t *q, int64_t nq, float *S, int64_t *n, float *w,
+                                  float *eigvals, uint16_t *u_r, qwm_stream stream) {
+  if (!ctx || !S || !n || !w || !eigvals || nq < 0) return QWM_ERR_ARG;
+  if (nq > 0 && !q) return QWM_ERR_ARG;
+  if (ctx->cfg.rank > 0 && !u_r) return QWM_ERR_ARG;
+  if ((q && !aligned16(q)) || !aligned16(S) || !aligned16(n) || !aligned16(w) || !aligned16(eigvals) ||
+      (u_r && !aligned16(u_r)))
+    return QWM_ERR_ALIGN;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int H = ctx->cfg.heads;
+  cudaError_t e = cudaSuccess;
+  if (nq > 0) e = launch_stats_partial(q, nq, H, ctx->stats_part, ctx->stats_splits, st);
+  if (e == cudaSuccess) e = launch_stats_finish(ctx->stats_part, nq > 0 ? ctx->stats_splits : 0, nq, H, S, n, w, st);
+  if (e == cudaSuccess) e = launch_jacobi(S, n, nq, H, ctx->cfg.rank, eigvals, u_r, ctx->status, st);
+  return cuda_status(e);
+}
+
+qwm_status qwm_fit_centroids(qwm_ctx *ctx, const uint16_t *x, int64_t n, const uint16_t *init, uint16_t *cent,
+                             qwm_stream stream) {
+  if (!ctx || !x || !cent || n < 0) return QWM_ERR_ARG;
+  if (n < ctx->cfg.n_centroids) return QWM_ERR_SHAPE;
+  if (n > ((int64_t)1 << 31) / QWM_D) return QWM_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(cent) || (init && !aligned16(init))) return QWM_ERR_ALIGN;
+  cudaError_t e = launch_kmeans(x, n, ctx->cfg.heads, ctx->cfg.n_centroids, init, ctx->cfg.kmeans_iters, cent,
+                                ctx->km_cent, ctx->km_sum, ctx->km_cnt, ctx->num_sms, (cudaStream_t)stream);
+  return cuda_status(e);
+}
+
+qwm_status qwm_quantize_kv(qwm_ctx *ctx, const uint16_t *k, const uint16_t *v, int64_t n, const float *w,
+                           const uint16_t *u_r, qwm_chunk *out, const qwm_debug *dbg, qwm_stream stream) {
+  if (!ctx || !k || !v || !out || n < 0) return QWM_ERR_ARG;
+  if (out->n_tokens != n) return QWM_ERR_SHAPE;
+  if (n > ((int64_t)1 << 31) / QWM_D) return QWM_ERR_SHAPE;
+  if (!aligned16(k) || !aligned16(v) || (w && !aligned16(w)) || (u_r && !aligned16(u_r))) return QWM_ERR_ALIGN;
+  const bool psac = (u_r != nullptr) && ctx->cfg.rank > 0;
+  out->rank_eff = psac ? ctx->cfg.rank : 0;
+  qwm_status s = check_chunk(ctx->cfg, out, true);
+  if (s != QWM_OK) return s;
+  if (dbg) {
+    if ((dbg->c_f32 && !aligned16(dbg->c_f32)) || (dbg->cand && !aligned16(dbg->cand)) ||
+        (dbg->score && !aligned16(dbg->score)))
+      return QWM_ERR_ALIGN;
+  }
+  if (n == 0) return QWM_OK;
+  cudaError_t e = launch_quantize(ctx->cfg, k, v, n, w, psac ? u_r : nullptr, *out, dbg, ctx->status,
+                                  ctx->num_sms, (cudaStream_t)stream);
+  return cuda_status(e);
+}
+
+qwm_status qwm_attend(qwm_ctx *ctx, const uint16_t *q, int64_t nq, const qwm_chunk *chunks, int32_t n_chunks,
+                      float softmax_scale, uint16_t *out, qwm_stream stream) {
+  if (!ctx || !chunks || !out || nq < 0 || n_chunks < 1) return QWM_ERR_ARG;
+  if (nq > 0 && !q) return QWM_ERR_ARG;
+  if ((q && !aligned16(q)) || !aligned16(out)) return QWM_ERR_ALIGN;
+  if (nq > ((int64_t)1 << 31) / QWM_D) return QWM_ERR_SHAPE;
+  if (n_chunks > 4096) return QWM_ERR_SHAPE;
+  int64_t total = 0;
+  for (int i = 0; i < n_chunks; i++) {
+    qwm_status s = check_chunk(ctx->cfg, &chunks[i], false);
+    if (s != QWM_OK) return s;
+    total += chunks[i].n_tokens;
+  }
+  if (total < 1) return QWM_ERR_SHAPE;
+  if (nq == 0) return QWM_OK;
+  cudaError_t e = launch_attend(ctx->cfg, q, nq, chunks, n_chunks, softmax_scale, out, ctx->num_sms,
+                                (cudaStream_t)stream);
+  return cuda_status(e);
+}
+
+qwm_status qwm_dequantize(qwm_ctx *ctx, const qwm_chunk *chunk, uint16_t *k_hat, uint16_t *v_hat,
+                          qwm_stream stream) {
+  if (!ctx || !chunk) return QWM_ERR_ARG;
+  qwm_status s = check_chunk(ctx->cfg, chunk, false);
+  if (s != QWM_OK) return s;
+  if ((k_hat && !aligned16(k_hat)) || (v_hat && !aligned16(v_hat))) return QWM_ERR_ALIGN;
+  if (chunk->n_tokens == 0 || (!k_hat && !v_hat)) return QWM_OK;
+  cudaError_t e = launch_dequantize(ctx->cfg, *chunk, k_hat, v_hat, (cudaStream_t)stream);
+  return cuda_status(e);
+}
+
+qwm_status qwm_sync_status(qwm_ctx *ctx, qwm_stream stream) {
+  if (!ctx) return QWM_ERR_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  int32_t h = 0;
+  if (cudaMemcpyAsync(&h, ctx->status, sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return QWM_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return QWM_ERR_CUDA;
+  if (h != 0 && cudaMemsetAsync(ctx->status, 0, sizeof(int32_t), st) != cudaSuccess) return QWM_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return QWM_ERR_CUDA;
+  return (qwm_status)h;
+}
+
+}  // extern "C"

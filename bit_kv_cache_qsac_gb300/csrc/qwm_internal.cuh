@@ -1,0 +1,58 @@
+// Internal declarations shared by the CUDA translation units of libqwm.so.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/qwm.h"
+
+#define QWM_D 128          // head_dim supported by the kernels
+#define QWM_GROUP 64       // INT2 group size supported by the kernels
+#define QWM_MAX_RANK 16
+#define QWM_MAX_TOPM 16
+#define QWM_MAX_CENTROIDS 256
+
+struct qwm_ctx {
+  qwm_config cfg;
+  int device;
+  int num_sms;
+  // device workspace (one allocation)
+  void *ws;
+  size_t ws_bytes;
+  int32_t *status;       // [1] first device-side error (qwm_status), 0 if none
+  float *stats_part;     // [splits][H][d][d] per-split partial sums of q q^T
+  int stats_splits;
+  float *km_sum;         // [H][C][d] k-means cluster sums
+  int32_t *km_cnt;       // [H][C] k-means cluster counts
+  float *km_cent;        // [H][C][d] fp32 centroids during the iterations
+};
+
+// record the first device-side error (kernels call this; never traps)
+__device__ __forceinline__ void qwm_dev_error(int32_t *status, int32_t code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+__device__ __forceinline__ float f16_to_f32(uint16_t h) { return __half2float(__ushort_as_half(h)); }
+
+// Launchers (each returns cudaGetLastError() of its launch).
+cudaError_t launch_stats_partial(const uint16_t *q, int64_t nq, int H, float *part, int splits, cudaStream_t st);
+cudaError_t launch_stats_finish(const float *part, int splits, int64_t nq, int H, float *S, int64_t *n, float *w,
+                                cudaStream_t st);
+cudaError_t launch_jacobi(const float *S, int64_t *n, int64_t nq, int H, int rank, float *eigvals, uint16_t *u_r,
+                          int32_t *status, cudaStream_t st);
+cudaError_t launch_kmeans(const uint16_t *x, int64_t n, int H, int C, const uint16_t *init, int iters,
+                          uint16_t *cent, float *km_cent, float *km_sum, int32_t *km_cnt, int num_sms,
+                          cudaStream_t st);
+cudaError_t launch_quantize(const qwm_config &cfg, const uint16_t *k, const uint16_t *v, int64_t n,
+                            const float *w, const uint16_t *u_r, const qwm_chunk &out, const qwm_debug *dbg,
+                            int32_t *status, int num_sms, cudaStream_t st);
+cudaError_t launch_attend(const qwm_config &cfg, const uint16_t *q, int64_t nq, const qwm_chunk *chunks,
+                          int n_chunks, float scale, uint16_t *out, int num_sms, cudaStream_t st);
+cudaError_t launch_dequantize(const qwm_config &cfg, const qwm_chunk &ch, uint16_t *k_hat, uint16_t *v_hat,
+                              cudaStream_t st);

@@ -1,0 +1,93 @@
+"""Chunk-streaming driver of one attention layer's compressed KV cache.
+
+QuantWM processes the cache chunk by chunk (English v2 summary §5.1 and §D.1;
+Chinese summary steps (1)-(5)): at each chunk boundary the previous chunk's
+Queries are folded into the per-head statistics and the principal basis is
+recomputed, the new chunk's Keys and Values are packed once, and the Queries of
+the step attend over every packed chunk.  The first chunk has no statistics
+(uniform weights, PSAC off).  This module only sequences the library calls; all
+arithmetic runs in libqwm.so.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import (Chunk, Context, qwm_attend, qwm_dequantize, qwm_fit_centroids, qwm_quantize_kv,
+               qwm_sync_status, qwm_update_query_stats)
+
+
+class CompressedLayer:
+    """Running state of one layer: Query statistics, basis, packed chunks, last codebooks."""
+
+    def __init__(self, ctx: Context, device=None):
+        self.ctx = ctx
+        cfg = ctx.cfg
+        H, d, r = cfg.heads, cfg.head_dim, cfg.rank
+        dev = device or torch.device("cuda", torch.cuda.current_device())
+        self.device = dev
+        self.S = torch.zeros(H, d, d, dtype=torch.float32, device=dev)
+        self.n = torch.zeros(H, dtype=torch.int64, device=dev)
+        self.w = torch.ones(H, d, dtype=torch.float32, device=dev)
+        self.eigvals = torch.zeros(H, d, dtype=torch.float32, device=dev)
+        self.u_r = torch.zeros(H, d, max(r, 1), dtype=torch.bfloat16, device=dev)
+        self.n_seen = 0          # Queries folded in so far (host copy of n)
+        self.chunks: list[Chunk] = []
+        self.prev_cent_k = None
+        self.prev_cent_v = None
+
+    def fold_queries(self, q: torch.Tensor, stream=None) -> None:
+        """Step 1: fold Queries [H][nq][d] into the statistics and recompute w and U_r."""
+        nq = q.shape[1] if q is not None else 0
+        qwm_update_query_stats(self.ctx, q, nq, self.S, self.n, self.w, self.eigvals,
+                               self.u_r if self.ctx.cfg.rank else None, stream)
+        self.n_seen += nq
+
+    def append_chunk(self, k: torch.Tensor, v: torch.Tensor, warm_start: bool = True, stream=None,
+                     debug: dict | None = None) -> Chunk:
+        """Steps 2-4: fit the chunk's codebooks and pack its Keys and Values."""
+        n = k.shape[1]
+        ch = Chunk.empty(self.ctx, n, self.device)
+        init_k = self.prev_cent_k if warm_start else None
+        init_v = self.prev_cent_v if warm_start else None
+        qwm_fit_centroids(self.ctx, k, n, init_k, ch.cent_k, stream)
+        qwm_fit_centroids(self.ctx, v, n, init_v, ch.cent_v, stream)
+        psac = self.n_seen > 0 and self.ctx.cfg.rank > 0
+        if psac:
+            ch.u_r.copy_(self.u_r)   # per-chunk snapshot of the basis
+        w = self.w if self.n_seen > 0 else None
+        qwm_quantize_kv(self.ctx, k, v, n, w, ch.u_r if psac else None, ch, debug, stream)
+        self.chunks.append(ch)
+        self.prev_cent_k, self.prev_cent_v = ch.cent_k, ch.cent_v
+        return ch
+
+    def attend(self, q: torch.Tensor, out: torch.Tensor | None = None, scale: float | None = None,
+               stream=None) -> torch.Tensor:
+        """Step 5: attention of Queries [H][nq][d] over every packed chunk."""
+        H, nq, d = q.shape
+        if out is None:
+            out = torch.empty(H, nq, d, dtype=torch.bfloat16, device=q.device)
+        qwm_attend(self.ctx, q, nq, self.chunks, 1.0 / math.sqrt(d) if scale is None else scale, out, stream)
+        return out
+
+    def dequantize(self, i: int, stream=None):
+        ch = self.chunks[i]
+        H, d = self.ctx.cfg.heads, self.ctx.cfg.head_dim
+        kh = torch.empty(H, ch.n_tokens, d, dtype=torch.bfloat16, device=self.device)
+        vh = torch.empty_like(kh)
+        qwm_dequantize(self.ctx, ch, kh, vh, stream)
+        return kh, vh
+
+    def step(self, q_prev, k, v, q, stream=None) -> torch.Tensor:
+        """One streaming step: fold q_prev (may be None), pack (k, v), attend with q."""
+        if q_prev is not None:
+            self.fold_queries(q_prev, stream)
+        self.append_chunk(k, v, stream=stream)
+        return self.attend(q, stream=stream)
+
+    def check(self, stream=None) -> int:
+        return qwm_sync_status(self.ctx, stream)
+
+    def nbytes(self) -> int:
+        return sum(c.nbytes() for c in self.chunks)

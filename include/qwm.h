@@ -1,0 +1,185 @@
+/*
+ * qwm.h -- C ABI of libqwm.so, the GB300 (sm_103a) QuantWM quantise-and-attend path.
+ *
+ * QuantWM ("QuantWM: Temporally Consistent 2-Bit KV Cache Quantization for
+ * Video World Models"; summaries in Chinese, Korean and English) compresses
+ * each completed chunk of a video model's KV cache to 2 bits:
+ *   1. per-head Query second moment M_h = (1/N) sum q q^T, its diagonal
+ *      channel weights w_{h,c} and its top-r eigenvectors U_r;
+ *   2. QSAC: the top-M centroids by the weighted distance
+ *      d_Q = sum_c w_c (k_c - mu_c)^2, then the one minimising
+ *      S = sum_g (sum_{c in G_g} w_c) R_g(k - mu)^2 (R_g = range of the residual
+ *      over a group of 64 channels); Values take their nearest centroid (QVG);
+ *   3. INT2 affine codes of the residual per group of 64, four codes per byte;
+ *   4. PSAC: E = K - K_hat_0, C = E U_r stored as INT8, U_r as BF16;
+ *   5. attention with logits Q K_hat_0^T + (Q U_r) C^T over the packed cache.
+ * Cited passages: Chinese summary, "前置知识" (affine quantiser, centroid-residual
+ * form, logits, Query second moment), "核心方法" (QSAC, PSAC), "方法步骤详情"
+ * steps (1)-(5); English v2 summary §4.1, §4.2, §5.1, §C.3, §D.1; QVG summary
+ * §2A (k-means along the sequence axis) and §2C (warm-started centroids).
+ *
+ * Conventions (every entry point):
+ *  - Returns a qwm_status; no exception or abort crosses the ABI.
+ *  - Asynchronous on the caller's stream.  Errors that only the device can see
+ *    (a Jacobi solve that ran out of sweeps, a residual out of fp16 range) are
+ *    recorded in a status word inside the context; qwm_sync_status() waits on
+ *    the stream, returns the first recorded error and clears it.
+ *  - Every device buffer is owned by the caller.  The library allocates device
+ *    memory only in qwm_create (its workspace, qwm_workspace_bytes() bytes)
+ *    and frees it in qwm_destroy.
+ *  - Every pointer must be 16-byte aligned and the tensor dense, in the layout
+ *    given; bf16 and fp16 values travel as uint16_t bit patterns.
+ *  - Head-major layouts: [H][tokens][channels] with H = config.heads.
+ *  - A context is not thread-safe; calls that share a context must be
+ *    ordered on one stream (the workspace is reused between calls).
+ */
+#ifndef QWM_H_
+#define QWM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QWM_API __attribute__((visibility("default")))
+#else
+#define QWM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *qwm_stream; /* a cudaStream_t; NULL = the legacy default stream */
+
+typedef enum {
+  QWM_OK = 0,
+  QWM_ERR_ARG = 1,           /* NULL pointer, negative size, bad enum value */
+  QWM_ERR_SHAPE = 2,         /* a size the kernels do not support (see qwm_config) */
+  QWM_ERR_ALIGN = 3,         /* a pointer that is not 16-byte aligned */
+  QWM_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
+  QWM_ERR_NOT_CONVERGED = 5, /* the Jacobi eigensolver hit its sweep limit (results still written) */
+  QWM_ERR_UNSUPPORTED = 6,   /* a configuration this build does not implement */
+  QWM_ERR_RANGE = 7          /* a residual, scale or coefficient outside the fp16 range */
+} qwm_status;
+
+/* Hyper-parameters (Chinese summary "复现评估": 256 centroids, group size 64, BF16
+ * centroids + INT2 residuals, r = 8, INT8 C, BF16 U_r, M = 4). */
+typedef struct {
+  int32_t heads;        /* H >= 1 */
+  int32_t head_dim;     /* d; must be 128 */
+  int32_t n_centroids;  /* C in {64, 128, 256} (uint8 indices) */
+  int32_t group;        /* channels per INT2 group; must be 64 */
+  int32_t top_m;        /* QSAC candidates M, 1..16 and <= n_centroids */
+  int32_t rank;         /* PSAC rank r, 0..16 */
+  int32_t bits;         /* residual bits; must be 2 */
+  int32_t kmeans_iters; /* Lloyd iterations per qwm_fit_centroids call, 1..100 */
+  uint64_t seed;        /* reserved (no randomness on the path); pass 0 */
+} qwm_config;
+
+typedef struct qwm_ctx qwm_ctx;
+
+/* One compressed chunk of the cache, all heads.  Every pointer is caller-owned
+ * device memory; N = n_tokens, H = heads, d = head_dim, G = d / group, r = rank. */
+typedef struct {
+  int64_t n_tokens;      /* N >= 0 */
+  int32_t rank_eff;      /* r used for this chunk: 0 (cold start, PSAC off) or config.rank */
+  int32_t reserved;
+  uint8_t *k_codes;      /* [H][N][d/4]: channel 4j+t -> bits 2t..2t+1 of byte j */
+  uint8_t *v_codes;      /* [H][N][d/4] */
+  uint8_t *k_idx;        /* [H][N] Key centroid index */
+  uint8_t *v_idx;        /* [H][N] Value centroid index */
+  uint16_t *k_scale;     /* fp16 [H][N][G]: INT2 step s */
+  uint16_t *k_min;       /* fp16 [H][N][G]: INT2 offset m (r_hat = m + s q) */
+  uint16_t *v_scale;     /* fp16 [H][N][G] */
+  uint16_t *v_min;       /* fp16 [H][N][G] */
+  uint16_t *cent_k;      /* bf16 [H][C][d] Key codebook of this chunk */
+  uint16_t *cent_v;      /* bf16 [H][C][d] Value codebook of this chunk */
+  int8_t *c;             /* [H][N][r] PSAC coefficients (unused when rank_eff == 0) */
+  uint16_t *c_scale;     /* fp16 [H][N]: C_hat = c_scale * c */
+  uint16_t *u_r;         /* bf16 [H][d][r]: the basis C was built with (snapshot per chunk) */
+} qwm_chunk;
+
+/* Optional stage outputs of qwm_quantize_kv for parity checks (NULL members are skipped). */
+typedef struct {
+  float *c_f32;          /* [H][N][r] PSAC coefficients before INT8 */
+  int32_t *cand;         /* [H][N][M] QSAC candidates (any order) */
+  float *score;          /* [H][N] QSAC score S of the chosen Key centroid */
+} qwm_debug;
+
+QWM_API const char *qwm_status_string(qwm_status s);
+
+/* Bytes of device workspace qwm_create allocates for this configuration. */
+QWM_API size_t qwm_workspace_bytes(const qwm_config *cfg);
+
+/* Validate cfg and allocate a context (host struct + device workspace) on the
+ * current device.  *out is NULL on failure. */
+QWM_API qwm_status qwm_create(const qwm_config *cfg, qwm_ctx **out);
+QWM_API qwm_status qwm_destroy(qwm_ctx *ctx);
+
+/* Step 1 -- Query statistics (Chinese summary "二阶Query统计与低秩分解" and step (1);
+ * English v2 summary §D.1: statistics kept incrementally, no Query tensor kept;
+ * principal basis recomputed at each chunk boundary).
+ *   q        bf16 [H][nq][d]      Queries to fold in (nq >= 0; nq == 0 only recomputes)
+ *   S        fp32 [H][d][d] inout running sum of q q^T
+ *   n        int64 [H]     inout  running Query count
+ *   w        fp32 [H][d]   out    w_c = S_cc / n, or 1 when n == 0 (cold start, §C.3)
+ *   eigvals  fp32 [H][d]   out    eigenvalues of M = S / n, descending (0 when n == 0)
+ *   u_r      bf16 [H][d][r] out   top-r eigenvectors of M (column k = k-th), rounded to
+ *                                 nearest-even; each column's largest-magnitude component
+ *                                 is positive.  May be NULL when config.rank == 0.
+ * The eigensolver is a parallel cyclic Jacobi method (fp32) with a sweep limit;
+ * reaching it records QWM_ERR_NOT_CONVERGED in the status word. */
+QWM_API qwm_status qwm_update_query_stats(qwm_ctx *ctx, const uint16_t *q, int64_t nq, float *S, int64_t *n,
+                                  float *w, float *eigvals, uint16_t *u_r, qwm_stream stream);
+
+/* Step 2a -- codebook (QVG summary §2A: k-means of the tokens along the sequence
+ * axis; §2C: each chunk's k-means starts from the previous chunk's centroids).
+ *   x     bf16 [H][n][d]  tokens of one chunk (n >= config.n_centroids)
+ *   init  bf16 [H][C][d]  starting centroids, or NULL: centroid j starts at token floor(j n / C)
+ *   cent  bf16 [H][C][d]  out: centroids after config.kmeans_iters Lloyd iterations
+ *                          (Euclidean assignment, lower index on ties; a cluster left
+ *                          empty keeps its centroid), rounded to nearest-even. */
+QWM_API qwm_status qwm_fit_centroids(qwm_ctx *ctx, const uint16_t *x, int64_t n, const uint16_t *init, uint16_t *cent,
+                             qwm_stream stream);
+
+/* Steps 2-4 -- QSAC assignment, INT2 residual codes and PSAC coefficients for one chunk
+ * (Chinese summary "核心方法" and steps (2)-(4); Korean summary "무엇과 다른가", "어떻게 쓰나").
+ *   k, v  bf16 [H][n][d]   the chunk's Keys and Values
+ *   w     fp32 [H][d]      channel weights, or NULL for uniform weights (cold start)
+ *   u_r   bf16 [H][d][r]   PSAC basis, or NULL to switch PSAC off (cold start)
+ *   out   chunk to fill: out->n_tokens must equal n, out->cent_k / out->cent_v must hold the
+ *         chunk's codebooks; the codes, indices, scales and (when u_r) c, c_scale are written,
+ *         out->rank_eff is set on the host (r or 0) and, when u_r is given, out->u_r must
+ *         point at a caller-owned copy of the basis (the library does not copy it).
+ *   dbg   optional stage outputs, or NULL.
+ * INT2 per (token, group): m = fp16 round-down of min r, s = fp16 round-up of
+ * (max r - m)/3 (s = 0 when max r == m), q = clamp(rint((r - m)/s), 0, 3); so |r - r_hat| <= s/2.
+ * INT8 per token: sC = fp16 round-up of max|C|/127, c = clamp(rint(C/sC), -127, 127). */
+QWM_API qwm_status qwm_quantize_kv(qwm_ctx *ctx, const uint16_t *k, const uint16_t *v, int64_t n, const float *w,
+                           const uint16_t *u_r, qwm_chunk *out, const qwm_debug *dbg, qwm_stream stream);
+
+/* Step 5 -- attention over the compressed cache (Chinese summary "注意力logits与时空token
+ * 选择": L = Q K^T / sqrt(d); "核心方法": PSAC logits Q K_hat_0^T + Q U_r C^T).
+ *   q        bf16 [H][nq][d]
+ *   chunks   HOST array of n_chunks >= 1 chunk descriptors (device pointers inside)
+ *   softmax_scale  multiplies both logit terms (usually 1/sqrt(d))
+ *   out      bf16 [H][nq][d] = softmax(l) V_hat over every token of every chunk (no mask)
+ * The INT2/centroid/PSAC decode happens inside the kernel's tile loads; no decoded
+ * K or V is written to memory. */
+QWM_API qwm_status qwm_attend(qwm_ctx *ctx, const uint16_t *q, int64_t nq, const qwm_chunk *chunks, int32_t n_chunks,
+                      float softmax_scale, uint16_t *out, qwm_stream stream);
+
+/* Step 5' -- BF16 reconstruction of one chunk (the pages' fused decoder, English v2 §D.1):
+ * K_hat = mu^K_idx + r_hat + C_hat U_r^T and V_hat = mu^V_idx + r_hat, rounded to nearest-even.
+ *   k_hat, v_hat  bf16 [H][N][d] out (either may be NULL). */
+QWM_API qwm_status qwm_dequantize(qwm_ctx *ctx, const qwm_chunk *chunk, uint16_t *k_hat, uint16_t *v_hat,
+                          qwm_stream stream);
+
+/* Wait for `stream`, return (and clear) the first error recorded on the device since
+ * the last call, else QWM_OK. */
+QWM_API qwm_status qwm_sync_status(qwm_ctx *ctx, qwm_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QWM_H_ */

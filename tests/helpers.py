@@ -1,0 +1,38 @@
+"""Conversions between the CUDA path's torch tensors and the oracle's numpy arrays (tests only)."""
+import numpy as np
+
+
+def to_u16(t) -> np.ndarray:
+    """A 16-bit torch tensor (bf16 / fp16 / int16) -> numpy uint16 bit patterns."""
+    import torch
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def from_u16(a: np.ndarray, dtype, device="cuda"):
+    """numpy uint16 bit patterns -> torch tensor of a 16-bit dtype on the device."""
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint16).view(np.int16)).to(device).view(dtype)
+
+
+def chunk_head(chunk, h: int) -> dict:
+    """Per-head numpy view of a packed chunk, in the oracle's chunk dict format."""
+    r = chunk.rank_eff
+    d = dict(
+        idx_k=chunk.k_idx[h].cpu().numpy().astype(np.int32), idx_v=chunk.v_idx[h].cpu().numpy().astype(np.int32),
+        k_codes=chunk.k_codes[h].cpu().numpy(), v_codes=chunk.v_codes[h].cpu().numpy(),
+        k_scale=to_u16(chunk.k_scale[h]), k_min=to_u16(chunk.k_min[h]),
+        v_scale=to_u16(chunk.v_scale[h]), v_min=to_u16(chunk.v_min[h]),
+        cent_k=to_u16(chunk.cent_k[h]), cent_v=to_u16(chunk.cent_v[h]), rank=r,
+    )
+    if r:
+        d.update(c=chunk.c[h].cpu().numpy()[:, :r], c_scale=to_u16(chunk.c_scale[h]),
+                 u_r=to_u16(chunk.u_r[h])[:, :r])
+    return d
+
+
+def bf16_ulp_close(a_bits: np.ndarray, b: np.ndarray, ulps: float = 1.0) -> np.ndarray:
+    """|bf16(a) - b| <= ulps * one bf16 step at the larger magnitude (elementwise mask)."""
+    a = (a_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    m = np.maximum(np.abs(a), np.abs(b))
+    step = np.where(m > 0, 2.0 ** (np.floor(np.log2(np.maximum(m, 1e-300))) - 7), 2.0 ** -133)
+    return np.abs(a - b) <= ulps * step

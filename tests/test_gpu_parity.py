@@ -1,0 +1,269 @@
+"""GPU-vs-oracle parity of every step of the path, called through the C ABI.
+
+Stage-wise protocol: each GPU stage is compared with the oracle run on the GPU's own
+upstream outputs (statistics -> basis -> codebooks -> packing -> attention), so that
+tolerances do not compound.  Bars (from the method's definition of equivalence):
+  * centroid indices: bit-exact except where the oracle's best and second-best QSAC
+    score (Values: distance), or its M-th and (M+1)-th d_Q, lie within a relative 1e-5;
+  * INT2 codes, packed bytes, fp16 scales and offsets: bit-exact given the index;
+  * INT8 PSAC codes and scales: bit-exact given the unquantised fp32 coefficients;
+    those coefficients within a relative 1e-3 of the oracle's (of the token's max |C|);
+  * eigenvalues within a relative 1e-3;
+  * attention output: max |error| <= 2e-2 x RMS(O);
+  * decoder: within one bf16 step.
+"""
+import math
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import oracle  # noqa: E402
+import synth  # noqa: E402
+from helpers import bf16_ulp_close, chunk_head, from_u16, to_u16  # noqa: E402
+
+D = 128
+TIE = 1e-5
+
+
+@pytest.fixture(scope="module")
+def q():
+    import __graft_entry__
+    __graft_entry__.build_library()
+    import bit_kv_cache_qsac_gb300 as qq
+    assert torch.cuda.is_available()
+    return qq
+
+
+def _bf(a):
+    return from_u16(a, torch.bfloat16)
+
+
+def _f32(bits):
+    return synth.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+# ------------------------------------------------------------------ step 1
+
+
+def test_stats_weights_and_basis(q):
+    w_ = synth.TINY
+    H = w_.heads
+    ctx = q.Context(heads=H)
+    S = torch.zeros(H, D, D, device="cuda"); n = torch.zeros(H, dtype=torch.int64, device="cuda")
+    w = torch.empty(H, D, device="cuda"); lam = torch.empty(H, D, device="cuda")
+    ur = torch.empty(H, D, 8, dtype=torch.bfloat16, device="cuda")
+    # cold start: no Queries yet
+    q.qwm_update_query_stats(ctx, None, 0, S, n, w, lam, ur)
+    assert q.qwm_sync_status(ctx) == 0
+    assert torch.all(w == 1) and torch.all(lam == 0) and torch.all(n == 0)
+    S64 = np.zeros((H, D, D)); n64 = np.zeros(H, np.int64)
+    for batch, nq in enumerate((256, 100)):    # second batch: incremental, ragged size
+        qb = synth.queries(w_, batch - 1, nq)
+        q.qwm_update_query_stats(ctx, _bf(qb), nq, S, n, w, lam, ur)
+        assert q.qwm_sync_status(ctx) == 0
+        ow, olam, our, oU, _ = oracle.update_query_stats(qb, S64, n64, 8)
+        assert np.array_equal(n.cpu().numpy(), n64)
+        np.testing.assert_allclose(S.cpu().numpy(), S64, rtol=1e-5, atol=1e-5 * np.abs(S64).max())
+        np.testing.assert_allclose(w.cpu().numpy(), ow, rtol=1e-5)
+        gl = lam.cpu().numpy()
+        assert np.all(np.abs(gl - olam) <= 1e-3 * np.abs(olam) + 1e-6 * np.abs(olam).max())
+        gu = _f32(to_u16(ur))
+        for h in range(H):
+            for kk in range(8):
+                u_ref = oU[h][:, kk]
+                cosv = gu[h][:, kk] @ u_ref / np.linalg.norm(gu[h][:, kk])
+                assert cosv > 0.999, (h, kk, cosv)            # same direction and sign convention
+            # bf16 rounding of the same vector: within one bf16 step where the vectors agree closely
+            assert np.mean(bf16_ulp_close(to_u16(ur[h]), oU[h][:, :8], 1.0)) > 0.95
+
+
+# ------------------------------------------------------------------ step 2a
+
+
+@pytest.mark.parametrize("n,C,init", [(1024, 256, False), (1000, 64, False), (1024, 256, True)])
+def test_kmeans_objective(q, n, C, init):
+    w_ = synth.TINY
+    H = w_.heads
+    x = synth.keys(w_)[:, :n]
+    ctx = q.Context(heads=H, n_centroids=C, top_m=min(4, C))
+    init_np = None
+    if init:
+        init_np = np.stack([oracle.kmeans(x[h], C, None, 2)[0] for h in range(H)])
+    cent = torch.empty(H, C, D, dtype=torch.bfloat16, device="cuda")
+    q.qwm_fit_centroids(ctx, _bf(x), n, None if init_np is None else _bf(init_np), cent)
+    assert q.qwm_sync_status(ctx) == 0
+    for h in range(H):
+        ref, _, _, _ = oracle.kmeans(x[h], C, None if init_np is None else init_np[h], 10)
+        j_gpu = oracle.kmeans_objective(x[h], to_u16(cent[h]))
+        j_ref = oracle.kmeans_objective(x[h], ref)
+        assert abs(j_gpu - j_ref) <= 1e-3 * j_ref, (h, j_gpu, j_ref)
+
+
+# ------------------------------------------------------------------ steps 2-4
+
+
+def _upstream(q, w_, H, n, C=256, top_m=4, rank=8, psac=True):
+    """GPU statistics and codebooks for a small case; returns numpy and device pieces."""
+    k = synth.keys(w_)[:H, :n]; v = synth.values(w_)[:H, :n]
+    ctx = q.Context(heads=H, n_centroids=C, top_m=top_m, rank=rank)
+    layer_S = torch.zeros(H, D, D, device="cuda"); n_ = torch.zeros(H, dtype=torch.int64, device="cuda")
+    w = torch.empty(H, D, device="cuda"); lam = torch.empty(H, D, device="cuda")
+    ur = torch.zeros(H, D, max(rank, 1), dtype=torch.bfloat16, device="cuda")
+    if psac:
+        qs = synth.queries(w_, -1, 256)[:H]
+        q.qwm_update_query_stats(ctx, _bf(qs), 256, layer_S, n_, w, lam, ur if rank else None)
+    ch = q.Chunk.empty(ctx, n)
+    K, V = _bf(k), _bf(v)
+    q.qwm_fit_centroids(ctx, K, n, None, ch.cent_k)
+    q.qwm_fit_centroids(ctx, V, n, None, ch.cent_v)
+    if psac and rank:
+        ch.u_r.copy_(ur)
+    return ctx, k, v, K, V, ch, (w if psac else None), (ch.u_r if psac and rank else None)
+
+
+def _check_quantize(q, ctx, k, v, K, V, ch, w, ur, top_m, rank):
+    H, n = k.shape[:2]
+    dbg = dict(c_f32=torch.zeros(H, n, max(rank, 1), device="cuda"),
+               cand=torch.zeros(H, n, top_m, dtype=torch.int32, device="cuda"),
+               score=torch.zeros(H, n, device="cuda"))
+    q.qwm_quantize_kv(ctx, K, V, n, w, ur, ch, dbg)
+    assert q.qwm_sync_status(ctx) == 0
+    assert ch.rank_eff == (rank if ur is not None else 0)
+    stats = dict(k_ties=0, v_ties=0, k_edge=0, tokens=H * n)
+    for h in range(H):
+        wh = None if w is None else w[h].cpu().numpy().astype(np.float64)
+        urh = None if ur is None else to_u16(ur[h])[:, :rank]
+        o = oracle.quantize_head(k[h], v[h], to_u16(ch.cent_k[h]), to_u16(ch.cent_v[h]), wh, urh,
+                                 top_m=top_m, rank=rank if ur is not None else 0)
+        gk = ch.k_idx[h].cpu().numpy().astype(np.int32)
+        gv = ch.v_idx[h].cpu().numpy().astype(np.int32)
+        s2 = o["score2"]; de = o["dq_edge"]; vd = o["vdist2"]
+        k_tie = np.abs(s2[:, 1] - s2[:, 0]) <= TIE * np.abs(s2[:, 0])
+        k_edge = np.abs(de[:, 1] - de[:, 0]) <= TIE * np.abs(de[:, 0])
+        v_tie = np.abs(vd[:, 1] - vd[:, 0]) <= TIE * np.abs(vd[:, 0])
+        bad_k = (gk != o["idx_k"]) & ~(k_tie | k_edge)
+        bad_v = (gv != o["idx_v"]) & ~v_tie
+        assert not bad_k.any(), f"head {h}: {bad_k.sum()} Key index mismatches outside ties"
+        assert not bad_v.any(), f"head {h}: {bad_v.sum()} Value index mismatches outside ties"
+        stats["k_ties"] += int(k_tie.sum()); stats["k_edge"] += int(k_edge.sum()); stats["v_ties"] += int(v_tie.sum())
+        # candidate sets agree (as sets) wherever the boundary is not a tie
+        gc = np.sort(dbg["cand"][h].cpu().numpy(), axis=1)
+        oc = np.sort(o["cand"], axis=1)
+        assert np.all((gc == oc).all(1) | k_edge)
+        # re-encode with the GPU's indices: codes, scales and offsets bit-exact
+        o2 = oracle.quantize_head(k[h], v[h], to_u16(ch.cent_k[h]), to_u16(ch.cent_v[h]), wh, urh,
+                                  top_m=top_m, rank=rank if ur is not None else 0, force_idx_k=gk, force_idx_v=gv)
+        for name in ("k_codes", "v_codes"):
+            assert np.array_equal(getattr(ch, name)[h].cpu().numpy(), o2[name]), name
+        for name in ("k_scale", "k_min", "v_scale", "v_min"):
+            assert np.array_equal(to_u16(getattr(ch, name)[h]), o2[name]), name
+        if ur is not None:
+            cg = dbg["c_f32"][h].cpu().numpy()[:, :rank].astype(np.float64)
+            cr = o2["c_real"]
+            scale_ = np.maximum(np.abs(cr).max(1, keepdims=True), 1e-30)
+            assert np.all(np.abs(cg - cr) <= 1e-3 * scale_)
+            # INT8 encoding of the GPU's fp32 coefficients: bit-exact
+            gc8 = ch.c[h].cpu().numpy()[:, :rank]
+            gsc = to_u16(ch.c_scale[h])
+            for i in range(n):
+                c8, sc = oracle.int8_encode_token(cg[i].astype(np.float32))
+                assert sc == gsc[i] and np.array_equal(c8, gc8[i]), i
+    return stats
+
+
+def test_quantize_tiny_with_psac(q):
+    ctx, k, v, K, V, ch, w, ur = _upstream(q, synth.TINY, 2, 1024)
+    st = _check_quantize(q, ctx, k, v, K, V, ch, w, ur, 4, 8)
+    print("tie fractions", {key: val / st["tokens"] for key, val in st.items() if key != "tokens"})
+
+
+def test_quantize_cold_start(q):
+    ctx, k, v, K, V, ch, w, ur = _upstream(q, synth.TINY, 2, 1024, psac=False)
+    _check_quantize(q, ctx, k, v, K, V, ch, None, None, 4, 8)
+
+
+@pytest.mark.parametrize("n,C,top_m,rank", [(333, 64, 16, 16), (257, 128, 1, 0), (300, 256, 4, 8)])
+def test_quantize_ragged_and_shapes(q, n, C, top_m, rank):
+    ctx, k, v, K, V, ch, w, ur = _upstream(q, synth.TINY, 2, n, C=C, top_m=top_m, rank=rank)
+    _check_quantize(q, ctx, k, v, K, V, ch, w, ur, top_m, rank)
+
+
+# ------------------------------------------------------------------ step 5', step 5
+
+
+def _packed(q, n=1024, H=2, psac=True, C=256, rank=8):
+    ctx, k, v, K, V, ch, w, ur = _upstream(q, synth.TINY, H, n, C=C, rank=rank, psac=psac)
+    q.qwm_quantize_kv(ctx, K, V, n, w, ur, ch)
+    assert q.qwm_sync_status(ctx) == 0
+    return ctx, ch
+
+
+@pytest.mark.parametrize("psac", [True, False])
+def test_dequantize_within_one_bf16_step(q, psac):
+    ctx, ch = _packed(q, psac=psac)
+    H, n = 2, ch.n_tokens
+    kh = torch.empty(H, n, D, dtype=torch.bfloat16, device="cuda"); vh = torch.empty_like(kh)
+    q.qwm_dequantize(ctx, ch, kh, vh)
+    assert q.qwm_sync_status(ctx) == 0
+    for h in range(H):
+        _, _, k64, v64 = oracle.dequantize_head(chunk_head(ch, h))
+        assert bf16_ulp_close(to_u16(kh[h]), k64).all()
+        assert bf16_ulp_close(to_u16(vh[h]), v64).all()
+
+
+def _attn_err(got, ref):
+    return np.abs(got - ref).max() / math.sqrt(np.mean(ref ** 2))
+
+
+@pytest.mark.parametrize("nq", [256, 200, 1])
+def test_attend_tiny(q, nq):
+    ctx, ch = _packed(q)
+    H = 2
+    qa = synth.queries(synth.TINY, 0, nq)
+    out = torch.empty(H, nq, D, dtype=torch.bfloat16, device="cuda")
+    q.qwm_attend(ctx, _bf(qa), nq, [ch], 1 / math.sqrt(D), out)
+    assert q.qwm_sync_status(ctx) == 0
+    for h in range(H):
+        ref = oracle.attend_rows(qa[h], np.arange(nq), [chunk_head(ch, h)], 1 / math.sqrt(D))
+        err = _attn_err(_f32(to_u16(out[h])), ref)
+        assert err <= 2e-2, err
+
+
+def test_attend_several_chunks_mixed_rank(q):
+    """A cold-start chunk (no PSAC) followed by PSAC chunks with different bases and a ragged size."""
+    w_ = synth.TINY
+    H = 2
+    ctx = q.Context(heads=H)
+    from bit_kv_cache_qsac_gb300 import stream
+    layer = stream.CompressedLayer(ctx)
+    kk, vv = synth.keys(w_), synth.values(w_)
+    parts = [(0, 300), (300, 700), (700, 1024)]
+    for i, (a, b) in enumerate(parts):
+        if i > 0:
+            layer.fold_queries(_bf(synth.queries(w_, 10 + i, 128)))
+        layer.append_chunk(_bf(np.ascontiguousarray(kk[:, a:b])), _bf(np.ascontiguousarray(vv[:, a:b])))
+    assert [c.rank_eff for c in layer.chunks] == [0, 8, 8]
+    qa = synth.queries(w_, 0, 96)
+    out = layer.attend(_bf(qa))
+    assert layer.check() == 0
+    for h in range(H):
+        ref = oracle.attend_rows(qa[h], np.arange(96), [chunk_head(c, h) for c in layer.chunks], 1 / math.sqrt(D))
+        assert _attn_err(_f32(to_u16(out[h])), ref) <= 2e-2
+
+
+def test_bad_arguments_raise(q):
+    ctx = q.Context(heads=2)
+    x = torch.zeros(2, 300, D, dtype=torch.bfloat16, device="cuda")
+    cent = torch.empty(2, 256, D, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(q.QwmError) as e:
+        q.qwm_fit_centroids(ctx, x[:, :200].contiguous(), 200, None, cent)   # fewer tokens than centroids
+    assert e.value.status == q.QWM_ERR_SHAPE
+    lib = q.raw_library()
+    bad = x.data_ptr() + 2   # misaligned
+    assert lib.qwm_fit_centroids(ctx.handle, bad, 300, None, cent.data_ptr(), None) == q.QWM_ERR_ALIGN
+    with pytest.raises(ValueError):
+        q.qwm_fit_centroids(ctx, x, 299, None, cent)
+    assert q.qwm_sync_status(ctx) == 0
