@@ -28,7 +28,7 @@ if not os.path.exists(LIB_PATH):
 _lib = C.CDLL(LIB_PATH)
 
 QWM_OK, QWM_ERR_ARG, QWM_ERR_SHAPE, QWM_ERR_ALIGN, QWM_ERR_CUDA, QWM_ERR_NOT_CONVERGED, \
-    QWM_ERR_UNSUPPORTED, QWM_ERR_RANGE = range(8)
+    QWM_ERR_UNSUPPORTED, QWM_ERR_RANGE, QWM_ERR_DEVICE_TIMEOUT = range(9)
 
 EXPORTED = ("qwm_status_string", "qwm_workspace_bytes", "qwm_create", "qwm_destroy",
             "qwm_update_query_stats", "qwm_fit_centroids", "qwm_quantize_kv", "qwm_attend",

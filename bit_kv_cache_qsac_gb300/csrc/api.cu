@@ -19,8 +19,9 @@ Layout layout_of(const qwm_config &c) {
   size_t off = 0;
   L.status = off; off = align_up(off + 256, 256);
   L.stats_part = off; off = align_up(off + (size_t)kStatsSplits * c.heads * QWM_D * QWM_D * sizeof(float), 256);
-  L.km_sum = off; off = align_up(off + (size_t)c.heads * c.n_centroids * QWM_D * sizeof(float), 256);
-  L.km_cnt = off; off = align_up(off + (size_t)c.heads * c.n_centroids * sizeof(int32_t), 256);
+  const size_t G = (size_t)kmeans_ctas_per_head(c.heads, QWM_MAX_SMS);
+  L.km_sum = off; off = align_up(off + G * c.heads * c.n_centroids * QWM_D * sizeof(float), 256);
+  L.km_cnt = off; off = align_up(off + G * c.heads * c.n_centroids * sizeof(int32_t), 256);
   L.km_cent = off; off = align_up(off + (size_t)c.heads * c.n_centroids * QWM_D * sizeof(float), 256);
   L.total = off;
   return L;
@@ -81,6 +82,7 @@ const char *qwm_status_string(qwm_status s) {
     case QWM_ERR_NOT_CONVERGED: return "eigensolver did not converge within its sweep limit";
     case QWM_ERR_UNSUPPORTED: return "unsupported configuration";
     case QWM_ERR_RANGE: return "value outside the fp16 range";
+    case QWM_ERR_DEVICE_TIMEOUT: return "a kernel gave up after its internal wait limit";
   }
   return "unknown status";
 }
@@ -153,10 +155,11 @@ qwm_status qwm_fit_centroids(qwm_ctx *ctx, const uint16_t *x, int64_t n, const u
                              qwm_stream stream) {
   if (!ctx || !x || !cent || n < 0) return QWM_ERR_ARG;
   if (n < ctx->cfg.n_centroids) return QWM_ERR_SHAPE;
-  if (n > ((int64_t)1 << 31) / QWM_D) return QWM_ERR_SHAPE;
+  if (n * ctx->cfg.heads >= ((int64_t)1 << 31)) return QWM_ERR_SHAPE;
   if (!aligned16(x) || !aligned16(cent) || (init && !aligned16(init))) return QWM_ERR_ALIGN;
+  const int sms = ctx->num_sms < QWM_MAX_SMS ? ctx->num_sms : QWM_MAX_SMS;
   cudaError_t e = launch_kmeans(x, n, ctx->cfg.heads, ctx->cfg.n_centroids, init, ctx->cfg.kmeans_iters, cent,
-                                ctx->km_cent, ctx->km_sum, ctx->km_cnt, ctx->num_sms, (cudaStream_t)stream);
+                                ctx->km_cent, ctx->km_sum, ctx->km_cnt, sms, ctx->status, (cudaStream_t)stream);
   return cuda_status(e);
 }
 
@@ -187,7 +190,7 @@ qwm_status qwm_attend(qwm_ctx *ctx, const uint16_t *q, int64_t nq, const qwm_chu
   if (nq > 0 && !q) return QWM_ERR_ARG;
   if ((q && !aligned16(q)) || !aligned16(out)) return QWM_ERR_ALIGN;
   if (nq > ((int64_t)1 << 31) / QWM_D) return QWM_ERR_SHAPE;
-  if (n_chunks > 4096) return QWM_ERR_SHAPE;
+  if (n_chunks > 128) return QWM_ERR_SHAPE;
   int64_t total = 0;
   for (int i = 0; i < n_chunks; i++) {
     qwm_status s = check_chunk(ctx->cfg, &chunks[i], false);
@@ -196,7 +199,7 @@ qwm_status qwm_attend(qwm_ctx *ctx, const uint16_t *q, int64_t nq, const qwm_chu
   }
   if (total < 1) return QWM_ERR_SHAPE;
   if (nq == 0) return QWM_OK;
-  cudaError_t e = launch_attend(ctx->cfg, q, nq, chunks, n_chunks, softmax_scale, out, ctx->num_sms,
+  cudaError_t e = launch_attend(ctx->cfg, q, nq, chunks, n_chunks, softmax_scale, out, ctx->num_sms, ctx->status,
                                 (cudaStream_t)stream);
   return cuda_status(e);
 }

@@ -29,7 +29,8 @@ __global__ void dequant_kernel(qwm_chunk ch, int H, int C, int R, uint16_t *__re
       const uint16_t *cent = pass ? ch.cent_v : ch.cent_k;
       const float s = f16_to_f32(sc[row * G + g]), m = f16_to_f32(mn[row * G + g]);
       const uint32_t b2 = *(const uint16_t *)(codes + row * (D / 4) + 2 * cb);  // 8 codes
-      const uint4 mu = *(const uint4 *)(cent + ((int64_t)h * C + idx[row]) * D + c0);
+      const int j = min((int)idx[row], C - 1);  // never read past the codebook
+      const uint4 mu = *(const uint4 *)(cent + ((int64_t)h * C + j) * D + c0);
       const uint32_t muw[4] = {mu.x, mu.y, mu.z, mu.w};
       float x[8];
 #pragma unroll

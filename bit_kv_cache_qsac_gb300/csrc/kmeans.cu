@@ -1,129 +1,288 @@
-// Step 2a: per-head Lloyd k-means codebook of one chunk.
+// Step 2a: per-head Lloyd k-means codebook of one chunk, on the tensor cores.
 //
-// QVG summary §2A: tokens are grouped by k-means along the sequence axis and each
-// token is represented by its centroid plus a residual; §2C: the k-means of a new
-// chunk starts from the previous chunk's centroids (warm start).  Every Lloyd
-// iteration assigns each token to its nearest centroid (Euclidean, lower index on
-// ties) and replaces each centroid by the mean of its members; a centroid left
-// without members keeps its position.  Centroids stay fp32 between iterations and
-// are rounded to bf16 at the end.
+// QVG summary §2A: tokens are grouped by k-means along the sequence axis and each token is
+// represented by its centroid plus a residual; §2C: the k-means of a new chunk starts from
+// the previous chunk's centroids (warm start).  Each Lloyd iteration assigns every token to
+// its nearest centroid (Euclidean, lower index on ties) and moves each centroid to the mean of
+// its members; a centroid left without members keeps its position.  Centroids stay fp32
+// between iterations and are rounded to bf16 at the end.
 //
-// Kernels: kmeans_init_kernel (starting centroids), kmeans_assign_kernel (one warp per
-// token, exact fp32 distances against the fp32 codebook held transposed in shared
-// memory; cluster sums by fp32 atomics), kmeans_update_kernel (means; clears sums).
+// Assignment = distance GEMM: ||x - mu_j||^2 = ||x||^2 + ||mu_j||^2 - 2 x.mu_j, and only
+// ||mu_j||^2 - 2 x.mu_j matters for the argmin.  x is bf16 (exact); the fp32 centroid is split
+// as mu = hi + lo with hi, lo bf16, so two bf16 MMAs give x.mu to about 2^-17 relative.
+//
+// km_assign_kernel (one CTA = one head x a contiguous range of 128-token tiles; 192 threads):
+//   warp 0    TMA producer: token tiles (2 x [128][64] bf16, 128-byte swizzle) into 2 stages
+//   warp 1    TMEM owner and MMA issuer: D[128 x C] = X hi^T + X lo^T into 2 TMEM buffers
+//   warps 2-5 epilogue: thread = token = TMEM lane; argmin over the C columns
+// The assignments of up to 4096 tokens stay in shared memory; then each warp adds its tokens
+// into per-CTA cluster sums in shared memory (over the codebook area) and the CTA adds them to
+// its own slice of the workspace.  km_update_kernel reduces the slices in a fixed order.
+// All waits are bounded; on expiry the kernel records QWM_ERR_DEVICE_TIMEOUT and stops.
 #include "qwm_internal.cuh"
+#include "tc.cuh"
 
 namespace {
 
 constexpr int D = QWM_D;
-constexpr int kAssignThreads = 256;
+constexpr int TILE = 128;
+constexpr int kMaxTok = 4096;  // tokens per super-chunk (assignments kept in shared memory)
+constexpr int kThreads = 192;
+constexpr uint64_t kWaitNs = 1000000000ull;
+
+struct KmSmem {  // offsets from a 1024-aligned base, for a codebook of C centroids
+  int bh, bl, x, norm, asg, total;
+  __host__ __device__ explicit KmSmem(int C) {
+    bh = 0;                        // 2 blocks of [C][64] bf16 (hi)
+    bl = bh + 2 * C * 128;         // 2 blocks of [C][64] bf16 (lo)
+    x = bl + 2 * C * 128;          // 2 stages x 2 blocks of [128][64]
+    norm = x + 2 * 2 * TILE * 128; // C floats
+    asg = norm + 4 * C;            // kMaxTok bytes
+    total = asg + kMaxTok;
+  }
+};
 
 __global__ void kmeans_init_kernel(const uint16_t *__restrict__ x, int64_t n, int C, const uint16_t *__restrict__ init,
-                                   float *__restrict__ cent, float *__restrict__ sum, int32_t *__restrict__ cnt) {
+                                   float *__restrict__ cent) {
   const int h = blockIdx.y, j = blockIdx.x, c = threadIdx.x;
   const uint16_t *src = init ? init + ((int64_t)h * C + j) * D : x + ((int64_t)h * n + (int64_t)j * n / C) * D;
   cent[((int64_t)h * C + j) * D + c] = bf16_to_f32(src[c]);
-  sum[((int64_t)h * C + j) * D + c] = 0.f;
-  if (c == 0) cnt[(int64_t)h * C + j] = 0;
 }
 
-// grid (ceil(n / tokens_per_cta), H); dynamic smem: centroids transposed [D][C] fp32
-__global__ void __launch_bounds__(kAssignThreads) kmeans_assign_kernel(const uint16_t *__restrict__ x, int64_t n,
-                                                                       int C, const float *__restrict__ cent,
-                                                                       float *__restrict__ sum,
-                                                                       int32_t *__restrict__ cnt, int tok_per_cta) {
-  extern __shared__ __align__(16) float ksm[];
-  float *cT = ksm;  // [D][C]
-  __shared__ float tokbuf[kAssignThreads / 32][D];
-  const int h = blockIdx.y;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const float *ch = cent + (int64_t)h * C * D;
-  for (int e = threadIdx.x; e < C * (D / 4); e += kAssignThreads) {  // lanes write consecutive centroids
-    const int j = e % C, cb = e / C;
-    const float4 a = *(const float4 *)(ch + (int64_t)j * D + 4 * cb);
-    cT[(4 * cb + 0) * C + j] = a.x;
-    cT[(4 * cb + 1) * C + j] = a.y;
-    cT[(4 * cb + 2) * C + j] = a.z;
-    cT[(4 * cb + 3) * C + j] = a.w;
+struct AssignParams {
+  const uint16_t *x;     // [H][n][D] bf16
+  const float *cent;     // [H][C][D] fp32
+  float *part_sum;       // [H][G][C][D]
+  int32_t *part_cnt;     // [H][G][C]
+  int64_t n;
+  int C, G;
+  int32_t *status;
+};
+
+__global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_constant__ TensorMap128 tmap,
+                                                                 const AssignParams p) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  unsigned char *sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+  __shared__ uint64_t x_full[2], x_empty[2], t_full[2], t_empty[2], drain;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag;
+  const int C = p.C;
+  const KmSmem L(C);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.y, cta = blockIdx.x;
+  const int64_t tiles = (p.n + TILE - 1) / TILE;
+  const int64_t per = (tiles + p.G - 1) / p.G;
+  const int64_t tile0 = (int64_t)cta * per;
+  const int64_t tile1 = tile0 + per < tiles ? tile0 + per : tiles;
+  float *sums = (float *)sm;                    // phase 2: [C][D] fp32 over the codebook area
+  int32_t *cnts = (int32_t *)(sm + C * D * 4);  // phase 2: [C], over the token stages
+  float *norm = (float *)(sm + L.norm);
+  uint8_t *asg = sm + L.asg;
+  volatile int *abort_v = &abort_flag;
+
+  if (tid == 0) {
+    for (int i = 0; i < 2; i++) {
+      tc::mbar_init(&x_full[i], 1);
+      tc::mbar_init(&x_empty[i], 1);
+      tc::mbar_init(&t_full[i], 1);
+      tc::mbar_init(&t_empty[i], 4);
+    }
+    tc::mbar_init(&drain, 1);
+    abort_flag = 0;
+    tc::fence_mbar_init();
   }
+  if (warp == 1) {
+    tc::tmem_alloc(&tmem_base_sh, 512);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
   __syncthreads();
-  const int per_lane = C / 32;  // 2, 4 or 8
-  const int64_t t_begin = (int64_t)blockIdx.x * tok_per_cta;
-  const int64_t t_end = min(n, t_begin + tok_per_cta);
-  for (int64_t i = t_begin + warp; i < t_end; i += kAssignThreads / 32) {
-    const uint16_t *xi = x + ((int64_t)h * n + i) * D;
-    const uint2 raw = *(const uint2 *)(xi + 4 * lane);
-    float xv[4];
-    xv[0] = __uint_as_float(raw.x << 16); xv[1] = __uint_as_float(raw.x & 0xFFFF0000u);
-    xv[2] = __uint_as_float(raw.y << 16); xv[3] = __uint_as_float(raw.y & 0xFFFF0000u);
-    __syncwarp();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_base_sh;
+  const float *cent = p.cent + (int64_t)h * C * D;
+  const uint16_t *xh = p.x + (int64_t)h * p.n * D;
+  float *psum = p.part_sum + ((int64_t)h * p.G + cta) * C * D;
+  int32_t *pcnt = p.part_cnt + ((int64_t)h * p.G + cta) * C;
+  int64_t g_tile = 0;  // tiles this CTA has processed (barrier phases)
+  for (int64_t sc0 = tile0, first = 1; first || sc0 < tile1; sc0 += kMaxTok / TILE, first = 0) {
+    const int64_t left = tile1 - sc0;
+    const int nt = left <= 0 ? 0 : (left < kMaxTok / TILE ? (int)left : kMaxTok / TILE);
+    // ---- codebook -> hi/lo bf16 operand blocks, and squared norms ----
+    for (int e = tid; e < C * (D / 8); e += kThreads) {
+      const int j = e / (D / 8), ci = e % (D / 8);
+      const float4 a = *(const float4 *)(cent + (int64_t)j * D + 8 * ci);
+      const float4 b = *(const float4 *)(cent + (int64_t)j * D + 8 * ci + 4);
+      const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      uint32_t hw[4], lw[4];
 #pragma unroll
-    for (int u = 0; u < 4; u++) tokbuf[warp][4 * lane + u] = xv[u];
-    __syncwarp();
-    float dist[8];
-#pragma unroll
-    for (int t = 0; t < 8; t++) dist[t] = 0.f;
-    for (int c = 0; c < D; c++) {
-      const float xc = tokbuf[warp][c];
-#pragma unroll
-      for (int t = 0; t < 8; t++) {
-        if (t < per_lane) {
-          const float df = __fsub_rn(xc, cT[c * C + lane + 32 * t]);
-          dist[t] = __fmaf_rn(df, df, dist[t]);
+      for (int u = 0; u < 4; u++) {
+        const float h0 = __bfloat162float(__float2bfloat16_rn(v[2 * u]));
+        const float h1 = __bfloat162float(__float2bfloat16_rn(v[2 * u + 1]));
+        hw[u] = (uint32_t)f32_to_bf16_rn(h0) | ((uint32_t)f32_to_bf16_rn(h1) << 16);
+        lw[u] = (uint32_t)f32_to_bf16_rn(v[2 * u] - h0) | ((uint32_t)f32_to_bf16_rn(v[2 * u + 1] - h1) << 16);
+      }
+      const uint32_t off = (ci / 8) * C * 128 + tc::sw128_offset(j, 8 * (ci % 8));
+      *(uint4 *)(sm + L.bh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *(uint4 *)(sm + L.bl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
+    for (int j = tid; j < C; j += kThreads) {
+      float s = 0.f;
+      for (int c = 0; c < D; c++) s = fmaf(cent[(int64_t)j * D + c], cent[(int64_t)j * D + c], s);
+      norm[j] = s;
+    }
+    tc::fence_proxy_async_smem();
+    __syncthreads();
+    // ---- phase 1: assignments of nt tiles ----
+    if (warp == 0) {
+      if (lane == 0) {
+        for (int i = 0; i < nt && !*abort_v; i++) {
+          const int64_t g = g_tile + i;
+          const int s = (int)(g & 1);
+          if (g >= 2 && !tc::mbar_wait(&x_empty[s], (uint32_t)(((g >> 1) - 1) & 1), kWaitNs)) {
+            *abort_v = 1;
+            break;
+          }
+          tc::mbar_arrive_expect_tx(&x_full[s], 2 * TILE * 128);
+          const int row = (int)((int64_t)h * p.n + (sc0 + i) * TILE);
+          unsigned char *dst = sm + L.x + s * 2 * TILE * 128;
+          tc::tma_load_2d(dst, &tmap, 0, row, &x_full[s]);
+          tc::tma_load_2d(dst + TILE * 128, &tmap, 64, row, &x_full[s]);
         }
       }
-    }
-    // argmin over the warp (centroid j = lane + 32 t), lower index on ties
-    float best = dist[0];
-    int arg = lane;
+    } else if (warp == 1) {
+      if (lane == 0) {
+        const uint32_t idesc = tc::idesc_bf16_f32(TILE, C);
+        const uint32_t sx = tc::smem_u32(sm + L.x), sbh = tc::smem_u32(sm + L.bh), sbl = tc::smem_u32(sm + L.bl);
+        for (int i = 0; i < nt && !*abort_v; i++) {
+          const int64_t g = g_tile + i;
+          const int s = (int)(g & 1);
+          if (!tc::mbar_wait(&x_full[s], (uint32_t)((g >> 1) & 1), kWaitNs) ||
+              (g >= 2 && !tc::mbar_wait(&t_empty[s], (uint32_t)(((g >> 1) - 1) & 1), kWaitNs))) {
+            *abort_v = 1;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t d = tmem + 256u * s;
 #pragma unroll
-    for (int t = 1; t < 8; t++)
-      if (t < per_lane && dist[t] < best) { best = dist[t]; arg = lane + 32 * t; }
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ob = __shfl_xor_sync(0xffffffffu, best, off);
-      const int oa = __shfl_xor_sync(0xffffffffu, arg, off);
-      if (ob < best || (ob == best && oa < arg)) { best = ob; arg = oa; }
-    }
-    float *sj = sum + ((int64_t)h * C + arg) * D + 4 * lane;
+          for (int kk = 0; kk < D / 16; kk++) {
+            const uint32_t xo = sx + s * 2 * TILE * 128 + (kk / 4) * TILE * 128 + 32 * (kk % 4);
+            const uint32_t bo = (kk / 4) * C * 128 + 32 * (kk % 4);
+            tc::mma_ss(d, tc::desc_sw128(xo), tc::desc_sw128(sbh + bo), idesc, kk > 0);
+          }
 #pragma unroll
-    for (int u = 0; u < 4; u++) atomicAdd(sj + u, xv[u]);
-    if (lane == 0) atomicAdd(cnt + (int64_t)h * C + arg, 1);
+          for (int kk = 0; kk < D / 16; kk++) {
+            const uint32_t xo = sx + s * 2 * TILE * 128 + (kk / 4) * TILE * 128 + 32 * (kk % 4);
+            const uint32_t bo = (kk / 4) * C * 128 + 32 * (kk % 4);
+            tc::mma_ss(d, tc::desc_sw128(xo), tc::desc_sw128(sbl + bo), idesc, 1);
+          }
+          tc::mma_commit(&x_empty[s]);
+          tc::mma_commit(&t_full[s]);
+        }
+      }
+    } else {
+      const int sub = warp & 3, row = 32 * sub + lane;
+      const uint32_t lane_addr = (uint32_t)(32 * sub) << 16;
+      for (int i = 0; i < nt; i++) {
+        const int64_t g = g_tile + i;
+        const int s = (int)(g & 1);
+        if (!tc::mbar_wait(&t_full[s], (uint32_t)((g >> 1) & 1), kWaitNs)) *abort_v = 1;
+        if (*abort_v) break;
+        tc::fence_after_sync();
+        float best = INFINITY;
+        int arg = 0;
+        uint32_t r[32];
+        for (int c0 = 0; c0 < C; c0 += 32) {
+          tc::tmem_ld32(tmem + lane_addr + 256u * s + c0, r);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int k = 0; k < 32; k++) {
+            const float dist = fmaf(-2.f, __uint_as_float(r[k]), norm[c0 + k]);
+            if (dist < best) { best = dist; arg = c0 + k; }
+          }
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&t_empty[s]);
+        asg[i * TILE + row] = (uint8_t)arg;
+      }
+    }
+    __syncthreads();
+    if (*abort_v) break;
+    g_tile += nt;
+    // ---- phase 2: cluster sums of this super-chunk (over the codebook area) ----
+    for (int e = tid; e < C * D; e += kThreads) sums[e] = 0.f;
+    for (int j = tid; j < C; j += kThreads) cnts[j] = 0;
+    __syncthreads();
+    const int64_t t_begin = sc0 * TILE;
+    const int64_t t_stop = (sc0 + nt) * TILE;
+    const int64_t t_end = t_stop < p.n ? t_stop : p.n;
+    for (int64_t tok = t_begin + warp; tok < t_end; tok += kThreads / 32) {
+      const int j = asg[tok - t_begin];
+      const uint2 raw = *(const uint2 *)(xh + tok * D + 4 * lane);
+      float *sj = sums + j * D + 4 * lane;
+      atomicAdd(sj + 0, __uint_as_float(raw.x << 16));
+      atomicAdd(sj + 1, __uint_as_float(raw.x & 0xFFFF0000u));
+      atomicAdd(sj + 2, __uint_as_float(raw.y << 16));
+      atomicAdd(sj + 3, __uint_as_float(raw.y & 0xFFFF0000u));
+      if (lane == 0) atomicAdd(cnts + j, 1);
+    }
+    __syncthreads();
+    for (int e = tid; e < C * D; e += kThreads) psum[e] = first ? sums[e] : psum[e] + sums[e];
+    for (int j = tid; j < C; j += kThreads) pcnt[j] = first ? cnts[j] : pcnt[j] + cnts[j];
+    __syncthreads();
+  }
+  // drain outstanding MMAs, then release TMEM
+  if (warp == 1 && lane == 0) {
+    tc::mma_commit(&drain);
+    if (!tc::mbar_wait(&drain, 0, kWaitNs)) *abort_v = 1;
+  }
+  __syncthreads();
+  if (*abort_v && tid == 0) qwm_dev_error(p.status, QWM_ERR_DEVICE_TIMEOUT);
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, 512);
   }
 }
 
-__global__ void kmeans_update_kernel(int C, float *__restrict__ cent, float *__restrict__ sum, int32_t *__restrict__ cnt,
-                                     uint16_t *__restrict__ out_bf16) {
+// New centroid = (sum of the G partial sums, in order) / count; empty clusters keep theirs.
+__global__ void km_update_kernel(int C, int G, float *__restrict__ cent, const float *__restrict__ part_sum,
+                                 const int32_t *__restrict__ part_cnt, uint16_t *__restrict__ out_bf16) {
   const int h = blockIdx.y, j = blockIdx.x, c = threadIdx.x;
+  float s = 0.f;
+  int cnt = 0;
+  for (int g = 0; g < G; g++) {
+    s += part_sum[(((int64_t)h * G + g) * C + j) * D + c];
+    cnt += part_cnt[((int64_t)h * G + g) * C + j];
+  }
   const int64_t e = ((int64_t)h * C + j) * D + c;
-  const int m = cnt[(int64_t)h * C + j];
   float mu = cent[e];
-  if (m > 0) mu = (float)((double)sum[e] / (double)m);
+  if (cnt > 0) mu = (float)((double)s / (double)cnt);
   cent[e] = mu;
-  sum[e] = 0.f;
-  __syncthreads();
-  if (c == 0) cnt[(int64_t)h * C + j] = 0;
   if (out_bf16) out_bf16[e] = f32_to_bf16_rn(mu);
 }
 
 }  // namespace
 
+int kmeans_ctas_per_head(int H, int num_sms) { return (num_sms + H - 1) / H; }
+
 cudaError_t launch_kmeans(const uint16_t *x, int64_t n, int H, int C, const uint16_t *init, int iters,
                           uint16_t *cent, float *km_cent, float *km_sum, int32_t *km_cnt, int num_sms,
-                          cudaStream_t st) {
-  kmeans_init_kernel<<<dim3(C, H), D, 0, st>>>(x, n, C, init, km_cent, km_sum, km_cnt);
+                          int32_t *status, cudaStream_t st) {
+  TensorMap128 tmap;
+  if (!make_tmap_rows128_bf16(&tmap, x, (uint64_t)H * n, TILE)) return cudaErrorInvalidValue;
+  kmeans_init_kernel<<<dim3(C, H), D, 0, st>>>(x, n, C, init, km_cent);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const size_t smem = (size_t)C * D * sizeof(float);
-  e = cudaFuncSetAttribute(kmeans_assign_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const int G = kmeans_ctas_per_head(H, num_sms);
+  const int smem = KmSmem(C).total + 1024;
+  e = cudaFuncSetAttribute(km_assign_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  // enough CTAs to cover the SMs about twice
-  int64_t blocks_per_head = (2LL * num_sms + H - 1) / H;
-  int tok_per_cta = (int)((n + blocks_per_head - 1) / blocks_per_head);
-  if (tok_per_cta < 64) tok_per_cta = 64;
-  const int gx = (int)((n + tok_per_cta - 1) / tok_per_cta);
+  AssignParams p{x, km_cent, km_sum, km_cnt, n, C, G, status};
   for (int it = 0; it < iters; it++) {
-    kmeans_assign_kernel<<<dim3(gx, H), kAssignThreads, smem, st>>>(x, n, C, km_cent, km_sum, km_cnt, tok_per_cta);
-    kmeans_update_kernel<<<dim3(C, H), D, 0, st>>>(C, km_cent, km_sum, km_cnt, it == iters - 1 ? cent : nullptr);
+    km_assign_kernel<<<dim3(G, H), kThreads, smem, st>>>(tmap, p);
+    km_update_kernel<<<dim3(C, H), D, 0, st>>>(C, G, km_cent, km_sum, km_cnt, it == iters - 1 ? cent : nullptr);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

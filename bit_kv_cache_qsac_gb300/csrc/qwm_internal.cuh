@@ -24,8 +24,8 @@ struct qwm_ctx {
   int32_t *status;       // [1] first device-side error (qwm_status), 0 if none
   float *stats_part;     // [splits][H][d][d] per-split partial sums of q q^T
   int stats_splits;
-  float *km_sum;         // [H][C][d] k-means cluster sums
-  int32_t *km_cnt;       // [H][C] k-means cluster counts
+  float *km_sum;         // [H][G][C][d] k-means per-CTA cluster sums (G CTAs per head)
+  int32_t *km_cnt;       // [H][G][C] k-means per-CTA cluster counts
   float *km_cent;        // [H][C][d] fp32 centroids during the iterations
 };
 
@@ -40,19 +40,27 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
 }
 __device__ __forceinline__ float f16_to_f32(uint16_t h) { return __half2float(__ushort_as_half(h)); }
 
+// TMA tensor map (a 128-byte-aligned 128-byte blob, CUtensorMap) over rows of 128 bf16.
+struct alignas(128) TensorMap128 {
+  unsigned char bytes[128];
+};
+bool make_tmap_rows128_bf16(void *tmap_out, const void *base, uint64_t rows, uint32_t box_rows);
+
 // Launchers (each returns cudaGetLastError() of its launch).
 cudaError_t launch_stats_partial(const uint16_t *q, int64_t nq, int H, float *part, int splits, cudaStream_t st);
 cudaError_t launch_stats_finish(const float *part, int splits, int64_t nq, int H, float *S, int64_t *n, float *w,
                                 cudaStream_t st);
 cudaError_t launch_jacobi(const float *S, int64_t *n, int64_t nq, int H, int rank, float *eigvals, uint16_t *u_r,
                           int32_t *status, cudaStream_t st);
+#define QWM_MAX_SMS 192  // workspace sizing bound on the SM count
+int kmeans_ctas_per_head(int H, int num_sms);
 cudaError_t launch_kmeans(const uint16_t *x, int64_t n, int H, int C, const uint16_t *init, int iters,
                           uint16_t *cent, float *km_cent, float *km_sum, int32_t *km_cnt, int num_sms,
-                          cudaStream_t st);
+                          int32_t *status, cudaStream_t st);
 cudaError_t launch_quantize(const qwm_config &cfg, const uint16_t *k, const uint16_t *v, int64_t n,
                             const float *w, const uint16_t *u_r, const qwm_chunk &out, const qwm_debug *dbg,
                             int32_t *status, int num_sms, cudaStream_t st);
 cudaError_t launch_attend(const qwm_config &cfg, const uint16_t *q, int64_t nq, const qwm_chunk *chunks,
-                          int n_chunks, float scale, uint16_t *out, int num_sms, cudaStream_t st);
+                          int n_chunks, float scale, uint16_t *out, int num_sms, int32_t *status, cudaStream_t st);
 cudaError_t launch_dequantize(const qwm_config &cfg, const qwm_chunk &ch, uint16_t *k_hat, uint16_t *v_hat,
                               cudaStream_t st);

@@ -59,7 +59,8 @@ typedef enum {
   QWM_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
   QWM_ERR_NOT_CONVERGED = 5, /* the Jacobi eigensolver hit its sweep limit (results still written) */
   QWM_ERR_UNSUPPORTED = 6,   /* a configuration this build does not implement */
-  QWM_ERR_RANGE = 7          /* a residual, scale or coefficient outside the fp16 range */
+  QWM_ERR_RANGE = 7,         /* a residual, scale or coefficient outside the fp16 range */
+  QWM_ERR_DEVICE_TIMEOUT = 8 /* a kernel's internal wait ran past its time limit and the kernel gave up */
 } qwm_status;
 
 /* Hyper-parameters (Chinese summary "复现评估": 256 centroids, group size 64, BF16
@@ -161,7 +162,8 @@ QWM_API qwm_status qwm_quantize_kv(qwm_ctx *ctx, const uint16_t *k, const uint16
 /* Step 5 -- attention over the compressed cache (Chinese summary "注意力logits与时空token
  * 选择": L = Q K^T / sqrt(d); "核心方法": PSAC logits Q K_hat_0^T + Q U_r C^T).
  *   q        bf16 [H][nq][d]
- *   chunks   HOST array of n_chunks >= 1 chunk descriptors (device pointers inside)
+ *   chunks   HOST array of 1 <= n_chunks <= 128 chunk descriptors (device pointers inside);
+ *            chunks with n_tokens == 0 are skipped
  *   softmax_scale  multiplies both logit terms (usually 1/sqrt(d))
  *   out      bf16 [H][nq][d] = softmax(l) V_hat over every token of every chunk (no mask)
  * The INT2/centroid/PSAC decode happens inside the kernel's tile loads; no decoded

@@ -1,0 +1,129 @@
+"""Full-size parity at the 720p-shaped layer (40 heads, 8 chunks of 10,800 tokens, cache 86,400),
+in the launch configuration the benchmark times.  The GPU streams all 8 chunks; the oracle then
+recomputes sampled outputs one by one from the GPU's upstream state: statistics of two heads,
+the k-means objective of one head, packing of 3 heads x 192 tokens, the decoder on one head and
+attention rows (first, last and random) of two heads over the whole cache."""
+import math
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import oracle  # noqa: E402
+import synth  # noqa: E402
+from helpers import bf16_ulp_close, chunk_head, from_u16, to_u16  # noqa: E402
+
+W = synth.P720
+D = 128
+TIE = 1e-5
+
+
+@pytest.fixture(scope="module")
+def run():
+    import __graft_entry__
+    __graft_entry__.build_library()
+    import bit_kv_cache_qsac_gb300 as q
+    from bit_kv_cache_qsac_gb300.stream import CompressedLayer
+    ctx = q.Context(heads=W.heads)
+    layer = CompressedLayer(ctx)
+    ks, vs, qs = [], [], []
+    for t in range(W.n_chunks):
+        a, b = synth.chunk_range(W, t)
+        ks.append(synth.keys(W, 0, a, b)); vs.append(synth.values(W, 0, a, b))
+        qs.append(synth.queries(W, t, W.nq_attend))
+    dbg = None
+    S_before = None
+    for t in range(W.n_chunks):
+        if t > 0:
+            if t == W.n_chunks - 1:
+                S_before = (layer.S.clone(), layer.n.clone())
+            layer.fold_queries(from_u16(qs[t - 1], torch.bfloat16))
+        if t == W.n_chunks - 1:
+            n = W.chunk_tokens
+            dbg = dict(c_f32=torch.zeros(W.heads, n, 8, device="cuda"),
+                       cand=torch.zeros(W.heads, n, 4, dtype=torch.int32, device="cuda"))
+        layer.append_chunk(from_u16(ks[t], torch.bfloat16), from_u16(vs[t], torch.bfloat16), debug=dbg)
+    out = layer.attend(from_u16(qs[-1], torch.bfloat16))
+    torch.cuda.synchronize()
+    assert layer.check() == 0
+    return dict(q=q, layer=layer, ks=ks, vs=vs, qs=qs, out=out, dbg=dbg, S_before=S_before)
+
+
+def test_statistics_two_heads(run):
+    layer, qs = run["layer"], run["qs"]
+    for h in (0, 39):
+        S = np.zeros((D, D))
+        for t in range(W.n_chunks - 1):
+            oracle.stats_accumulate(qs[t][h], S)
+        assert int(layer.n[h]) == (W.n_chunks - 1) * W.nq_attend
+        np.testing.assert_allclose(layer.S[h].cpu().numpy(), S, rtol=1e-4, atol=1e-4 * np.abs(S).max())
+        lam, _, _ = oracle.eig(layer.S[h].cpu().numpy().astype(np.float64) / float(layer.n[h]))
+        gl = layer.eigvals[h].cpu().numpy()
+        assert np.all(np.abs(gl - lam) <= 1e-3 * np.abs(lam) + 1e-6 * lam[0])
+
+
+def test_kmeans_objective_one_head(run):
+    layer, ks = run["layer"], run["ks"]
+    h = 7
+    init = to_u16(layer.chunks[-2].cent_k[h])
+    ref, _, _, _ = oracle.kmeans(ks[-1][h], 256, init, 10)
+    j_gpu = oracle.kmeans_objective(ks[-1][h], to_u16(layer.chunks[-1].cent_k[h]))
+    j_ref = oracle.kmeans_objective(ks[-1][h], ref)
+    assert abs(j_gpu - j_ref) <= 1e-3 * j_ref
+
+
+def test_packing_sampled_tokens(run):
+    layer, ks, vs, dbg = run["layer"], run["ks"], run["vs"], run["dbg"]
+    ch = layer.chunks[-1]
+    rng = np.random.default_rng(0)
+    n = W.chunk_tokens
+    rows = np.unique(np.r_[0, n - 1, rng.choice(n, 190, replace=False)])
+    for h in (0, 21, 39):
+        w = layer.w[h].cpu().numpy().astype(np.float64)
+        ur = to_u16(ch.u_r[h])
+        k, v = ks[-1][h][rows], vs[-1][h][rows]
+        o = oracle.quantize_head(k, v, to_u16(ch.cent_k[h]), to_u16(ch.cent_v[h]), w, ur)
+        gk = ch.k_idx[h].cpu().numpy()[rows].astype(np.int32)
+        gv = ch.v_idx[h].cpu().numpy()[rows].astype(np.int32)
+        s2, de, vd = o["score2"], o["dq_edge"], o["vdist2"]
+        tie_k = (np.abs(s2[:, 1] - s2[:, 0]) <= TIE * np.abs(s2[:, 0])) | \
+                (np.abs(de[:, 1] - de[:, 0]) <= TIE * np.abs(de[:, 0]))
+        tie_v = np.abs(vd[:, 1] - vd[:, 0]) <= TIE * np.abs(vd[:, 0])
+        assert np.all((gk == o["idx_k"]) | tie_k)
+        assert np.all((gv == o["idx_v"]) | tie_v)
+        o2 = oracle.quantize_head(k, v, to_u16(ch.cent_k[h]), to_u16(ch.cent_v[h]), w, ur,
+                                  force_idx_k=gk, force_idx_v=gv)
+        for name in ("k_codes", "v_codes"):
+            assert np.array_equal(getattr(ch, name)[h].cpu().numpy()[rows], o2[name])
+        for name in ("k_scale", "k_min", "v_scale", "v_min"):
+            assert np.array_equal(to_u16(getattr(ch, name)[h])[rows], o2[name])
+        cg = dbg["c_f32"][h].cpu().numpy()[rows].astype(np.float64)
+        scale_ = np.maximum(np.abs(o2["c_real"]).max(1, keepdims=True), 1e-30)
+        assert np.all(np.abs(cg - o2["c_real"]) <= 1e-3 * scale_)
+        gc8 = ch.c[h].cpu().numpy()[rows]
+        gsc = to_u16(ch.c_scale[h])[rows]
+        for i in range(len(rows)):
+            c8, sc = oracle.int8_encode_token(cg[i].astype(np.float32))
+            assert sc == gsc[i] and np.array_equal(c8, gc8[i])
+
+
+def test_decoder_one_head(run):
+    q, layer = run["q"], run["layer"]
+    h = 3
+    kh, vh = layer.dequantize(W.n_chunks - 1)
+    _, _, k64, v64 = oracle.dequantize_head(chunk_head(layer.chunks[-1], h))
+    assert bf16_ulp_close(to_u16(kh[h]), k64).all() and bf16_ulp_close(to_u16(vh[h]), v64).all()
+
+
+def test_attention_rows_two_heads(run):
+    layer, qs, out = run["layer"], run["qs"], run["out"]
+    rng = np.random.default_rng(1)
+    nq = W.nq_attend
+    rows = np.unique(np.r_[0, nq - 1, 255, 256, rng.choice(nq, 4, replace=False)])
+    for h in (0, 39):
+        ref = oracle.attend_rows(qs[-1][h], rows, [chunk_head(c, h) for c in layer.chunks], 1 / math.sqrt(D))
+        got = synth.bf16_bits_to_f32(to_u16(out[h]))[rows].astype(np.float64)
+        err = np.abs(got - ref).max() / math.sqrt(np.mean(ref ** 2))
+        assert err <= 2e-2, err
