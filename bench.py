@@ -33,12 +33,20 @@ sys.path.insert(0, ROOT)
 
 import synth  # noqa: E402
 
+WORKLOADS = {"720p": synth.P720, "480p": synth.P480}
 W = synth.P720
 H, D = W.heads, W.head_dim
-N_CHUNK = W.chunk_tokens               # 10,800
-N_CACHE = W.n_tokens                   # 86,400
-NQ = W.nq_attend                       # 10,800
+N_CHUNK = W.chunk_tokens               # 10,800 at 720p
+N_CACHE = W.n_tokens                   # 86,400 at 720p
+NQ = W.nq_attend                       # 10,800 at 720p
 RANK = W.rank
+
+
+def select_workload(name: str) -> None:
+    global W, H, D, N_CHUNK, N_CACHE, NQ, RANK
+    W = WORKLOADS[name]
+    H, D = W.heads, W.head_dim
+    N_CHUNK, N_CACHE, NQ, RANK = W.chunk_tokens, W.n_tokens, W.nq_attend, W.rank
 FLOPS_PER_PAIR = 2 * (D + RANK + D)    # Q K_hat_0^T (128), (Q U_r) C^T (8), P V (128): 528
 # algorithmic HBM bytes of the packing per token-head: read K, V (512 B); write Key codes 32,
 # index 1, scale+offset 8, PSAC c 8 + sC 2; Value codes 32, index 1, scale+offset 8
@@ -222,7 +230,9 @@ def run_ours(args, rank, world, device):
     with ClockSampler(device.index if device.index is not None else 0) as clk:
         for _ in range(args.steps):
             flush.zero_()                       # L2 flush between steps, outside the events
+            torch.cuda.nvtx.range_push("qwm_step")
             step(Q[last - 1], K[last], V[last], Q[last], out)
+            torch.cuda.nvtx.range_pop()
             ev[4].synchronize()
             times = [ev[i].elapsed_time(ev[i + 1]) for i in range(4)]
             stage += times
@@ -271,11 +281,11 @@ def run_ours(args, rank, world, device):
     res = {
         "metric": "KV tokens quantized/s; quantized-cache attention TFLOP/s (% of roofline)",
         "value": value,
-        "unit": "KV token-heads/s (720p layer step: stats + fit + pack + attend)",
+        "unit": "KV token-heads/s (layer step: stats + fit + pack + attend)",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16 (fp32 accumulate)", "data": "synthetic (seeded generator; no model weights)",
-        "config": {"workload": "720p-shaped layer, step 8 of 8", "heads": H, "head_dim": D,
+        "config": {"workload": f"{W.name}-shaped layer, step 8 of 8", "heads": H, "head_dim": D,
                    "chunk_tokens": N_CHUNK, "cache_tokens": N_CACHE, "queries": NQ,
                    "n_centroids": W.n_centroids, "group": W.group, "top_m": W.top_m, "rank": RANK,
                    "kmeans_iters": 10, "l2": "flushed between steps (256 MiB write, outside the timed events)",
@@ -353,9 +363,9 @@ def oracle_sample(seconds_hint: float = 15.0):
     sample_s = t_stats + t_fit + t_quant + t_att
     cores = len(os.sched_getaffinity(0))
     return {"value": H * N_CHUNK / step_s, "unit": "KV token-heads/s", "cores": cores, "kind": "oracle",
-            "sample": f"head 0 of 40: statistics+Jacobi (10,800 Queries), k-means of Keys and Values "
-                      f"(10 iterations), packing of 10,800 tokens, attention of {rows} of 10,800 Query rows "
-                      f"over 86,400 tokens; extrapolated x40 heads and x{NQ // rows} rows",
+            "sample": f"head 0 of {H}: statistics+Jacobi ({NQ} Queries), k-means of Keys and Values "
+                      f"(10 iterations), packing of {N_CHUNK} tokens, attention of {rows} of {NQ} Query rows "
+                      f"over {N_CACHE} tokens; extrapolated x{H} heads and x{NQ / rows:g} rows",
             "sample_seconds": sample_s, "extrapolated_step_s": step_s,
             "stage_s": {"stats_eig": H * t_stats, "fit_k_v": H * t_fit, "quantize": H * t_quant,
                         "attend": H * t_att * NQ / rows}}
@@ -375,11 +385,11 @@ def run_reference(args, rank, world):
     step_s = statistics.mean(s["extrapolated_step_s"] for s in samples)
     cb = dict(samples[-1]); cb["value"] = val
     return {"impl": "reference", "metric": "KV tokens quantized/s; quantized-cache attention TFLOP/s (% of roofline)",
-            "value": val, "unit": "KV token-heads/s (720p layer step: stats + fit + pack + attend)",
+            "value": val, "unit": "KV token-heads/s (layer step: stats + fit + pack + attend)",
             "n_gpus": 0, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded generator; no model weights)",
-            "config": {"workload": "720p-shaped layer, step 8 of 8", "heads": H, "head_dim": D,
+            "config": {"workload": f"{W.name}-shaped layer, step 8 of 8", "heads": H, "head_dim": D,
                        "chunk_tokens": N_CHUNK, "cache_tokens": N_CACHE, "queries": NQ},
             "cpu_baseline": cb,
             "e2e": {"value": val, "unit": "KV token-heads/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -392,7 +402,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="720p",
+                    help="720p-shaped layer (default) or 480p-shaped layer")
     args = ap.parse_args()
+    select_workload(args.workload)
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     if args.impl == "reference":

@@ -11,7 +11,7 @@ constexpr int kStatsSplits = 8;
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
-  size_t status, stats_part, km_sum, km_cnt, km_cent, total;
+  size_t status, stats_part, km_sum, km_cnt, km_cent, jac_basis, jac_valid, total;
 };
 
 Layout layout_of(const qwm_config &c) {
@@ -23,6 +23,8 @@ Layout layout_of(const qwm_config &c) {
   L.km_sum = off; off = align_up(off + G * c.heads * c.n_centroids * QWM_D * sizeof(float), 256);
   L.km_cnt = off; off = align_up(off + G * c.heads * c.n_centroids * sizeof(int32_t), 256);
   L.km_cent = off; off = align_up(off + (size_t)c.heads * c.n_centroids * QWM_D * sizeof(float), 256);
+  L.jac_basis = off; off = align_up(off + (size_t)c.heads * QWM_D * QWM_D * sizeof(float), 256);
+  L.jac_valid = off; off = align_up(off + (size_t)c.heads * sizeof(int32_t), 256);
   L.total = off;
   return L;
 }
@@ -123,6 +125,8 @@ qwm_status qwm_create(const qwm_config *cfg, qwm_ctx **out) {
   ctx->km_sum = (float *)(base + L.km_sum);
   ctx->km_cnt = (int32_t *)(base + L.km_cnt);
   ctx->km_cent = (float *)(base + L.km_cent);
+  ctx->jac_basis = (float *)(base + L.jac_basis);
+  ctx->jac_valid = (int32_t *)(base + L.jac_valid);
   *out = ctx;
   return QWM_OK;
 }
@@ -145,9 +149,14 @@ qwm_status qwm_update_query_stats(qwm_ctx *ctx, const uint16_t *q, int64_t nq, f
   cudaStream_t st = (cudaStream_t)stream;
   const int H = ctx->cfg.heads;
   cudaError_t e = cudaSuccess;
-  if (nq > 0) e = launch_stats_partial(q, nq, H, ctx->stats_part, ctx->stats_splits, st);
-  if (e == cudaSuccess) e = launch_stats_finish(ctx->stats_part, nq > 0 ? ctx->stats_splits : 0, nq, H, S, n, w, st);
-  if (e == cudaSuccess) e = launch_jacobi(S, n, nq, H, ctx->cfg.rank, eigvals, u_r, ctx->status, st);
+  // splits: enough CTAs to cover the SMs, at most the workspace's partial slots
+  int splits = (ctx->num_sms + H - 1) / H;
+  if (splits > ctx->stats_splits) splits = ctx->stats_splits;
+  if (splits < 1) splits = 1;
+  if (nq > 0) e = launch_stats_partial(q, nq, H, ctx->stats_part, splits, ctx->status, st);
+  if (e == cudaSuccess) e = launch_stats_finish(ctx->stats_part, nq > 0 ? splits : 0, nq, H, S, n, w, st);
+  if (e == cudaSuccess)
+    e = launch_jacobi(S, n, nq, H, ctx->cfg.rank, eigvals, u_r, ctx->status, ctx->jac_basis, ctx->jac_valid, st);
   return cuda_status(e);
 }
 

@@ -5,6 +5,9 @@
 //   l_ij = scale * ([q_i | q_i U_r^(t)] . [k_hat_0_j | c_hat_j]),  o_i = softmax(l_i) V_hat,
 // with k_hat_0 = mu^K_idx + m + s q, c_hat = sC c and v_hat = mu^V_idx + m + s q decoded from the
 // packed chunk inside the kernel.  Nothing decoded is written back to memory.
+// Operands of both MMAs are fp16 (fp32 accumulate): the decode is exact in fp32 and rounded once
+// to fp16, whose 11-bit mantissa keeps the logits of the outlier channels (|k| up to ~40)
+// accurate; Q (bf16 in memory) converts to fp16 exactly for every normal value.
 //
 // One CTA = one head x 256 Queries (two 128-row tiles that share every decoded K/V tile).
 // Warp roles (512 threads):
@@ -13,7 +16,7 @@
 //                   the logits, rescales O in TMEM when the max grows by more than 2^8;
 //   warp 8          allocates TMEM and issues every tcgen05.mma (one thread);
 //   warps 9-15      producers: decode each 128-token tile of the packed cache into shared memory
-//                   (K_hat_0 rows and V_hat^T rows as 128-byte-swizzled bf16, c_hat in the
+//                   (K_hat_0 rows and V_hat^T rows as 128-byte-swizzled fp16, c_hat in the
 //                   no-swizzle layout) and, at each chunk start, Q U_r for both Query tiles.
 // Tensor memory (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each; P_x overlays S_x.
 // MMA order per tile j: S0(j), PV1(j-1), S1(j), PV0(j).  tcgen05 operations complete in issue
@@ -70,34 +73,28 @@ struct Bars {
   uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_ready[2], o_done, drain;
 };
 
-__device__ __forceinline__ __nv_bfloat162 u32_as_bf2(uint32_t u) { return *reinterpret_cast<__nv_bfloat162 *>(&u); }
-__device__ __forceinline__ uint32_t bf2_as_u32(__nv_bfloat162 v) { return *reinterpret_cast<uint32_t *>(&v); }
-
-// q (0..3) of two channels as exact bf16x2, from a word holding the first code at bit 0 and the
-// second at bit 16 (the remaining bits are masked off): bf16(128 + q) = 0x4300 | q, minus 128.
-__device__ __forceinline__ __nv_bfloat162 codes_to_bf2(uint32_t w) {
-  const uint32_t y = (w & 0x00030003u) | 0x43004300u;
-  return __hsub2(u32_as_bf2(y), u32_as_bf2(0x43004300u));
-}
-
 __device__ __forceinline__ float half_bits_to_f32(uint16_t h) { return __half2float(__ushort_as_half(h)); }
 
-// Decode 32 channels (quarter qd of a token) of a Key: 16 bf16x2 words, channel pairs.
+// 2^23 + q as a float for a 2-bit code q in the low bits of c (exact), and its removal.
+__device__ __forceinline__ float magic_code(uint32_t c) { return __uint_as_float((c & 3u) | 0x4B000000u); }
+constexpr float kMagic = 8388608.0f;
+
+// Decode 32 channels (quarter of a token) of a Key exactly in fp32 -- r_hat = fl(m + s q) and
+// k_hat_0 = fl(mu + r_hat), as in the packing -- then round to fp16: 16 words, channel pairs.
 __device__ __forceinline__ void decode_key_quarter(const uint2 codes, const uint4 (&mu)[4], float s, float m,
                                                    uint32_t (&out)[16]) {
-  const __nv_bfloat162 s2 = __float2bfloat162_rn(s);
-  const __nv_bfloat162 m2 = __float2bfloat162_rn(m);
+  const uint64_t s2 = tc::f2(s, s), m2 = tc::f2(m, m), neg = tc::f2(-kMagic, -kMagic);
   const uint32_t cw[2] = {codes.x, codes.y};
 #pragma unroll
   for (int hw = 0; hw < 4; hw++) {  // 8 channels per 16-bit halfword of codes
-    const uint32_t h16 = (cw[hw >> 1] >> (16 * (hw & 1))) & 0xFFFFu;
-    const uint32_t spread = h16 | (h16 << 14);  // channel 2i at bit 4i, channel 2i+1 at bit 4i+16
+    const uint32_t h16 = cw[hw >> 1] >> (16 * (hw & 1));
     const uint32_t muw[4] = {mu[hw].x, mu[hw].y, mu[hw].z, mu[hw].w};
 #pragma unroll
     for (int i = 0; i < 4; i++) {
-      const __nv_bfloat162 q2 = codes_to_bf2(spread >> (4 * i));
-      const __nv_bfloat162 base = __hadd2(u32_as_bf2(muw[i]), m2);
-      out[4 * hw + i] = bf2_as_u32(__hfma2(q2, s2, base));
+      const uint64_t q2 = tc::add2(tc::f2(magic_code(h16 >> (4 * i)), magic_code(h16 >> (4 * i + 2))), neg);
+      const uint64_t r2 = tc::fma2(s2, q2, m2);
+      const uint64_t k2 = tc::add2(tc::f2(__uint_as_float(muw[i] << 16), __uint_as_float(muw[i] & 0xFFFF0000u)), r2);
+      out[4 * hw + i] = tc::pack_f16x2(tc::f2lo(k2), tc::f2hi(k2));
     }
   }
 }
@@ -125,7 +122,12 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     const int64_t qi = q0 + row;
     uint4 v = make_uint4(0, 0, 0, 0);
     if (qi < p.nq) v = *(const uint4 *)(p.q + ((int64_t)h * p.nq + qi) * D + 8 * ci);
-    *(uint4 *)(sm + OFF_Q + (x * 2 + b) * kBlk + tc::sw128_offset(rr, 8 * (ci % 8))) = v;
+    const uint32_t bw[4] = {v.x, v.y, v.z, v.w};
+    uint32_t hw[4];
+#pragma unroll
+    for (int u = 0; u < 4; u++) hw[u] = tc::pack_f16x2(__uint_as_float(bw[u] << 16), __uint_as_float(bw[u] & 0xFFFF0000u));
+    *(uint4 *)(sm + OFF_Q + (x * 2 + b) * kBlk + tc::sw128_offset(rr, 8 * (ci % 8))) =
+        make_uint4(hw[0], hw[1], hw[2], hw[3]);
   }
   if (tid == 0) {
     for (int i = 0; i < 2; i++) {
@@ -205,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
           const float x1 =
               (c + 2 * i + 1 < nk) ? tc::ex2_approx(__uint_as_float(r[2 * i + 1]) * p.scale_log2 - m_used) : 0.f;
           l += x0 + x1;
-          pw[i] = tc::pack_bf16x2(x0, x1);
+          pw[i] = tc::pack_f16x2(x0, x1);
         }
         tc::tmem_st16(tS + c / 2, pw);  // P overlays the first 64 columns of S
       }
@@ -243,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
   } else if (warp == kMmaWarp) {
     // ======================= MMA issue (one thread) =======================
     if (lane == 0) {
-      const uint32_t idesc = tc::idesc_bf16_f32(BM, BN);
+      const uint32_t idesc = tc::idesc_f16_f32(BM, BN);
       const uint32_t tS[2] = {tmem, tmem + 128u}, tO[2] = {tmem + 256u, tmem + 384u};
       const uint32_t sQ = tc::smem_u32(sm + OFF_Q), sK = tc::smem_u32(sm + OFF_K), sV = tc::smem_u32(sm + OFF_V);
       const uint32_t sC = tc::smem_u32(sm + OFF_C), sQU = tc::smem_u32(sm + OFF_QU);
@@ -327,9 +329,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
           float acc[16];
 #pragma unroll
           for (int kq = 0; kq < 16; kq++) acc[kq] = 0.f;
+          const int64_t qi = q0 + row;
           for (int ci = 0; ci < D / 8; ci++) {
-            const uint4 qv =
-                *(const uint4 *)(sm + OFF_Q + (x * 2 + ci / 8) * kBlk + tc::sw128_offset(rr, 8 * (ci % 8)));
+            uint4 qv = make_uint4(0, 0, 0, 0);
+            if (qi < p.nq) qv = *(const uint4 *)(p.q + ((int64_t)h * p.nq + qi) * D + 8 * ci);
             const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
             for (int u = 0; u < 8; u++) {
@@ -342,38 +345,61 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
           }
           uint32_t w[8];
 #pragma unroll
-          for (int i = 0; i < 8; i++) w[i] = tc::pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
+          for (int i = 0; i < 8; i++) w[i] = tc::pack_f16x2(acc[2 * i], acc[2 * i + 1]);
           unsigned char *dst = sm + OFF_QU + ((t & 1) * NQT + x) * 4096;
           *(uint4 *)(dst + tc::noswz16_offset(rr, 0)) = make_uint4(w[0], w[1], w[2], w[3]);
           *(uint4 *)(dst + tc::noswz16_offset(rr, 8)) = make_uint4(w[4], w[5], w[6], w[7]);
         }
       }
-      // --- K_hat_0 rows: item = (token row, quarter of 32 channels) ---
-      for (int it = pt; it < BN * 4; it += kProdThreads) {
-        const int row = it >> 2, qd = it & 3, g = qd >> 1, b = qd >> 1;
-        uint32_t w[16];
-        if (row < nk) {
-          const int64_t gi = (int64_t)h * ch.n + k0 + row;
-          const int idx = min((int)ch.k_idx[gi], p.C - 1);  // never read past the codebook
-          const float s_ = half_bits_to_f32(ch.k_scale[gi * 2 + g]);
-          const float m_ = half_bits_to_f32(ch.k_min[gi * 2 + g]);
-          const uint2 codes = *(const uint2 *)(ch.k_codes + gi * (D / 4) + 8 * qd);
-          const uint4 *mu = (const uint4 *)(ch.cent_k + ((int64_t)h * p.C + idx) * D + 32 * qd);
-          uint4 muv[4];
+      // --- K_hat_0 rows: item = (token row, quarter of 32 channels), up to 3 per thread.  All
+      // index loads are issued first, then all centroid gathers, then the decode, so that each
+      // thread has its loads in flight together instead of one dependent chain per item. ---
+      {
+        constexpr int kItems = (BN * 4 + kProdThreads - 1) / kProdThreads;  // 3
+        int idx[kItems];
+        float sc[kItems], mn[kItems];
+        uint2 cd[kItems];
+        bool ok[kItems];
 #pragma unroll
-          for (int v = 0; v < 4; v++) muv[v] = mu[v];
-          decode_key_quarter(codes, muv, s_, m_, w);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; i++) w[i] = 0u;
+        for (int i = 0; i < kItems; i++) {
+          const int it = pt + i * kProdThreads, row = it >> 2, qd = it & 3;
+          ok[i] = it < BN * 4 && row < nk;
+          idx[i] = 0; sc[i] = 0.f; mn[i] = 0.f; cd[i] = make_uint2(0, 0);
+          if (ok[i]) {
+            const int64_t gi = (int64_t)h * ch.n + k0 + row;
+            idx[i] = min((int)ch.k_idx[gi], p.C - 1);  // never read past the codebook
+            sc[i] = half_bits_to_f32(ch.k_scale[gi * 2 + (qd >> 1)]);
+            mn[i] = half_bits_to_f32(ch.k_min[gi * 2 + (qd >> 1)]);
+            cd[i] = *(const uint2 *)(ch.k_codes + gi * (D / 4) + 8 * qd);
+          }
         }
-        unsigned char *blk = sm + OFF_K + (s * 2 + b) * kBlk;
+        uint4 muv[kItems][4];
 #pragma unroll
-        for (int v = 0; v < 4; v++)
-          *(uint4 *)(blk + tc::sw128_offset(row, 32 * (qd & 1) + 8 * v)) =
-              make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+        for (int i = 0; i < kItems; i++) {
+          const int qd = (pt + i * kProdThreads) & 3;
+          const uint4 *mu = (const uint4 *)(ch.cent_k + ((int64_t)h * p.C + idx[i]) * D + 32 * qd);
+#pragma unroll
+          for (int v = 0; v < 4; v++) muv[i][v] = ok[i] ? mu[v] : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int i = 0; i < kItems; i++) {
+          const int it = pt + i * kProdThreads, row = it >> 2, qd = it & 3;
+          if (it >= BN * 4) continue;
+          uint32_t w[16];
+          if (ok[i]) {
+            decode_key_quarter(cd[i], muv[i], sc[i], mn[i], w);
+          } else {
+#pragma unroll
+            for (int u = 0; u < 16; u++) w[u] = 0u;
+          }
+          unsigned char *blk = sm + OFF_K + (s * 2 + (qd >> 1)) * kBlk;
+#pragma unroll
+          for (int v = 0; v < 4; v++)
+            *(uint4 *)(blk + tc::sw128_offset(row, 32 * (qd & 1) + 8 * v)) =
+                make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+        }
       }
-      // --- c_hat rows (PSAC coefficients, bf16, zero past the rank) ---
+      // --- c_hat rows (PSAC coefficients, fp16, zero past the rank) ---
       if (R > 0) {
         for (int row = pt; row < BN; row += kProdThreads) {
           uint32_t w[8];
@@ -387,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
             for (int i = 0; i < 8; i++) {
               const float a = (2 * i < R) ? sc * (float)cc[2 * i] : 0.f;
               const float bq = (2 * i + 1 < R) ? sc * (float)cc[2 * i + 1] : 0.f;
-              w[i] = tc::pack_bf16x2(a, bq);
+              w[i] = tc::pack_f16x2(a, bq);
             }
           }
           unsigned char *dst = sm + OFF_C + s * 4096;
@@ -424,26 +450,25 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
           }
         }
         const bool valid0 = (2 * pair) < nk, valid1 = (2 * pair + 1) < nk;
-        const __nv_bfloat162 s2 = __floats2bfloat162_rn(sv[0], sv[1]);
-        const __nv_bfloat162 m2 = __floats2bfloat162_rn(mv[0], mv[1]);
+        const uint64_t s2 = tc::f2(sv[0], sv[1]), m2 = tc::f2(mv[0], mv[1]), neg = tc::f2(-kMagic, -kMagic);
         const uint32_t cw0[2] = {codes[0].x, codes[0].y}, cw1[2] = {codes[1].x, codes[1].y};
         const int key = 2 * pair, vb = key / 64, kin = key % 64;
         unsigned char *blk = sm + OFF_V + (s * 2 + vb) * kBlk;
 #pragma unroll
         for (int hw = 0; hw < 4; hw++) {  // 8 channels each
-          const uint32_t a16 = (cw0[hw >> 1] >> (16 * (hw & 1))) & 0xFFFFu;
-          const uint32_t b16 = (cw1[hw >> 1] >> (16 * (hw & 1))) & 0xFFFFu;
-          const uint32_t both = a16 | (b16 << 16);  // token 0 codes low, token 1 codes high
+          const uint32_t a16 = cw0[hw >> 1] >> (16 * (hw & 1));
+          const uint32_t b16 = cw1[hw >> 1] >> (16 * (hw & 1));
           const uint32_t mu0[4] = {muv[0][hw].x, muv[0][hw].y, muv[0][hw].z, muv[0][hw].w};
           const uint32_t mu1[4] = {muv[1][hw].x, muv[1][hw].y, muv[1][hw].z, muv[1][hw].w};
 #pragma unroll
           for (int u = 0; u < 8; u++) {
             const int c = 32 * qd + 8 * hw + u;  // channel = V_hat^T row
-            const uint32_t sel = (u & 1) ? 0x7632u : 0x5410u;  // high or low halves of both words
-            const uint32_t mup = __byte_perm(mu0[u >> 1], mu1[u >> 1], sel);
-            const __nv_bfloat162 q2 = codes_to_bf2(both >> (2 * u));
-            const __nv_bfloat162 v2 = __hfma2(q2, s2, __hadd2(u32_as_bf2(mup), m2));
-            uint32_t vw = bf2_as_u32(v2);
+            const uint64_t q2 = tc::add2(tc::f2(magic_code(a16 >> (2 * u)), magic_code(b16 >> (2 * u))), neg);
+            const uint64_t r2 = tc::fma2(s2, q2, m2);
+            const float mua = __uint_as_float((u & 1) ? (mu0[u >> 1] & 0xFFFF0000u) : (mu0[u >> 1] << 16));
+            const float mub = __uint_as_float((u & 1) ? (mu1[u >> 1] & 0xFFFF0000u) : (mu1[u >> 1] << 16));
+            const uint64_t v2 = tc::add2(tc::f2(mua, mub), r2);
+            uint32_t vw = tc::pack_f16x2(tc::f2lo(v2), tc::f2hi(v2));
             if (!valid1) vw &= 0x0000FFFFu;
             if (!valid0) vw = 0u;
             *(uint32_t *)(blk + tc::sw128_offset(c, kin)) = vw;

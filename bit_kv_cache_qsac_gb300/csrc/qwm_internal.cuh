@@ -27,6 +27,8 @@ struct qwm_ctx {
   float *km_sum;         // [H][G][C][d] k-means per-CTA cluster sums (G CTAs per head)
   int32_t *km_cnt;       // [H][G][C] k-means per-CTA cluster counts
   float *km_cent;        // [H][C][d] fp32 centroids during the iterations
+  float *jac_basis;      // [H][d][d] last eigenbasis per head (Jacobi warm start)
+  int32_t *jac_valid;    // [H] 1 once jac_basis holds a basis
 };
 
 // record the first device-side error (kernels call this; never traps)
@@ -47,11 +49,12 @@ struct alignas(128) TensorMap128 {
 bool make_tmap_rows128_bf16(void *tmap_out, const void *base, uint64_t rows, uint32_t box_rows);
 
 // Launchers (each returns cudaGetLastError() of its launch).
-cudaError_t launch_stats_partial(const uint16_t *q, int64_t nq, int H, float *part, int splits, cudaStream_t st);
+cudaError_t launch_stats_partial(const uint16_t *q, int64_t nq, int H, float *part, int splits, int32_t *status,
+                                 cudaStream_t st);
 cudaError_t launch_stats_finish(const float *part, int splits, int64_t nq, int H, float *S, int64_t *n, float *w,
                                 cudaStream_t st);
 cudaError_t launch_jacobi(const float *S, int64_t *n, int64_t nq, int H, int rank, float *eigvals, uint16_t *u_r,
-                          int32_t *status, cudaStream_t st);
+                          int32_t *status, float *basis, int32_t *valid, cudaStream_t st);
 #define QWM_MAX_SMS 192  // workspace sizing bound on the SM count
 int kmeans_ctas_per_head(int H, int num_sms);
 cudaError_t launch_kmeans(const uint16_t *x, int64_t n, int H, int C, const uint16_t *init, int iters,

@@ -197,3 +197,33 @@ __device__ __forceinline__ void tma_load_2d(void *dst_smem, const void *tmap, in
       : "memory");
 }
 }  // namespace tc
+
+namespace tc {
+// kind::f16 instruction descriptor: fp16 A and B, fp32 D, both K-major, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4)                      // D format: f32
+         | ((uint32_t)(N >> 3) << 17)   // N / 8   (A, B format fields 0: f16)
+         | ((uint32_t)(M >> 4) << 24);  // M / 16
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Two fp32 lanes in one 64-bit register; IEEE round-to-nearest on each lane.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  return ((uint64_t)__float_as_uint(hi) << 32) | (uint64_t)__float_as_uint(lo);
+}
+__device__ __forceinline__ float f2lo(uint64_t v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float f2hi(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+}  // namespace tc
