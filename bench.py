@@ -190,7 +190,7 @@ def run_ours(args, rank, world, device):
     prev = layer.chunks[-1]
     ch = q.Chunk.empty(ctx, N_CHUNK, device)
     chunks = layer.chunks + [ch]
-    out = torch.empty(H, NQ, D, dtype=torch.bfloat16, device=device)
+    out = torch.empty(H, NQ, D, dtype=torch.float32, device=device)
     scale = 1.0 / math.sqrt(D)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream()
@@ -246,7 +246,7 @@ def run_ours(args, rank, world, device):
     # end to end through the C ABI with host buffers: H2D of the step's inputs (previous Queries,
     # Keys, Values, Queries) from pinned memory and D2H of the attention output, each step
     hQp, hK, hV, hQ = pinned(qs[last - 1]), pinned(ks[last]), pinned(vs[last]), pinned(qs[last])
-    hO = torch.empty(H, NQ, D, dtype=torch.bfloat16).pin_memory()
+    hO = torch.empty(H, NQ, D, dtype=torch.float32).pin_memory()
     dQp, dK, dV, dQ = (torch.empty_like(x, device=device) for x in (hQp, hK, hV, hQ))
     h2d = sum(x.numel() * x.element_size() for x in (hQp, hK, hV, hQ))
     d2h = hO.numel() * hO.element_size()

@@ -229,7 +229,7 @@ def qwm_attend(ctx: Context, q, nq: int, chunks: list, softmax_scale: float, out
     H, d = ctx.cfg.heads, ctx.cfg.head_dim
     arr = (qwm_chunk * len(chunks))(*[c.struct() for c in chunks])
     st = _lib.qwm_attend(ctx.handle, _ptr(q, "q", 2, (H, nq, d)), nq, arr, len(chunks), float(softmax_scale),
-                         _ptr(out, "out", 2, (H, nq, d)), _stream(stream))
+                         _ptr(out, "out", 4, (H, nq, d)), _stream(stream))
     _check(st, "qwm_attend")
 
 

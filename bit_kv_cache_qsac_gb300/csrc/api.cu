@@ -194,7 +194,7 @@ qwm_status qwm_quantize_kv(qwm_ctx *ctx, const uint16_t *k, const uint16_t *v, i
 }
 
 qwm_status qwm_attend(qwm_ctx *ctx, const uint16_t *q, int64_t nq, const qwm_chunk *chunks, int32_t n_chunks,
-                      float softmax_scale, uint16_t *out, qwm_stream stream) {
+                      float softmax_scale, float *out, qwm_stream stream) {
   if (!ctx || !chunks || !out || nq < 0 || n_chunks < 1) return QWM_ERR_ARG;
   if (nq > 0 && !q) return QWM_ERR_ARG;
   if ((q && !aligned16(q)) || !aligned16(out)) return QWM_ERR_ALIGN;

@@ -64,6 +64,6 @@ cudaError_t launch_quantize(const qwm_config &cfg, const uint16_t *k, const uint
                             const float *w, const uint16_t *u_r, const qwm_chunk &out, const qwm_debug *dbg,
                             int32_t *status, int num_sms, cudaStream_t st);
 cudaError_t launch_attend(const qwm_config &cfg, const uint16_t *q, int64_t nq, const qwm_chunk *chunks,
-                          int n_chunks, float scale, uint16_t *out, int num_sms, int32_t *status, cudaStream_t st);
+                          int n_chunks, float scale, float *out, int num_sms, int32_t *status, cudaStream_t st);
 cudaError_t launch_dequantize(const qwm_config &cfg, const qwm_chunk &ch, uint16_t *k_hat, uint16_t *v_hat,
                               cudaStream_t st);

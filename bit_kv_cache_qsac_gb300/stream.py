@@ -67,7 +67,7 @@ class CompressedLayer:
         """Step 5: attention of Queries [H][nq][d] over every packed chunk."""
         H, nq, d = q.shape
         if out is None:
-            out = torch.empty(H, nq, d, dtype=torch.bfloat16, device=q.device)
+            out = torch.empty(H, nq, d, dtype=torch.float32, device=q.device)
         qwm_attend(self.ctx, q, nq, self.chunks, 1.0 / math.sqrt(d) if scale is None else scale, out, stream)
         return out
 

@@ -165,11 +165,14 @@ QWM_API qwm_status qwm_quantize_kv(qwm_ctx *ctx, const uint16_t *k, const uint16
  *   chunks   HOST array of 1 <= n_chunks <= 128 chunk descriptors (device pointers inside);
  *            chunks with n_tokens == 0 are skipped
  *   softmax_scale  multiplies both logit terms (usually 1/sqrt(d))
- *   out      bf16 [H][nq][d] = softmax(l) V_hat over every token of every chunk (no mask)
+ *   out      fp32 [H][nq][d] = softmax(l) V_hat over every token of every chunk (no mask); fp32
+ *            because the output averages thousands of values and its largest entries are many
+ *            times its RMS, so a bf16 result would carry a rounding error larger than the
+ *            computation's
  * The INT2/centroid/PSAC decode happens inside the kernel's tile loads; no decoded
  * K or V is written to memory. */
 QWM_API qwm_status qwm_attend(qwm_ctx *ctx, const uint16_t *q, int64_t nq, const qwm_chunk *chunks, int32_t n_chunks,
-                      float softmax_scale, uint16_t *out, qwm_stream stream);
+                      float softmax_scale, float *out, qwm_stream stream);
 
 /* Step 5' -- BF16 reconstruction of one chunk (the pages' fused decoder, English v2 §D.1):
  * K_hat = mu^K_idx + r_hat + C_hat U_r^T and V_hat = mu^V_idx + r_hat, rounded to nearest-even.
