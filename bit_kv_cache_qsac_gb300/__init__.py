@@ -32,7 +32,7 @@ QWM_OK, QWM_ERR_ARG, QWM_ERR_SHAPE, QWM_ERR_ALIGN, QWM_ERR_CUDA, QWM_ERR_NOT_CON
 
 EXPORTED = ("qwm_status_string", "qwm_workspace_bytes", "qwm_create", "qwm_destroy",
             "qwm_update_query_stats", "qwm_fit_centroids", "qwm_quantize_kv", "qwm_attend",
-            "qwm_dequantize", "qwm_sync_status")
+            "qwm_dequantize", "qwm_sync_status", "qwm_update_query_stats_noalloc")
 
 
 class QwmError(RuntimeError):
@@ -73,6 +73,7 @@ _lib.qwm_quantize_kv.argtypes = [_P, _P, _P, C.c_int64, _P, _P, C.POINTER(qwm_ch
 _lib.qwm_attend.argtypes = [_P, _P, C.c_int64, C.POINTER(qwm_chunk), C.c_int32, C.c_float, _P, _P]
 _lib.qwm_dequantize.argtypes = [_P, C.POINTER(qwm_chunk), _P, _P, _P]
 _lib.qwm_sync_status.argtypes = [_P, _P]
+_lib.qwm_update_query_stats_noalloc.argtypes = [C.POINTER(qwm_config), _P, C.c_int64, _P, _P, _P, _P, _P, _P, _P]
 for _name in EXPORTED[2:]:
     getattr(_lib, _name).restype = C.c_int
 
@@ -244,6 +245,19 @@ def qwm_dequantize(ctx: Context, chunk: Chunk, k_hat, v_hat, stream=None) -> Non
 def qwm_sync_status(ctx: Context, stream=None) -> int:
     """Wait for the stream and return (and clear) the first device-side error status (0 = none)."""
     return _lib.qwm_sync_status(ctx.handle, _stream(stream))
+
+
+def qwm_update_query_stats_noalloc(cfg: qwm_config, q, nq: int, S, n, w, eigvals, u_r, dev_status=None,
+                                   stream=None) -> None:
+    """qwm_update_query_stats without a context and without any device allocation (for callers
+    whose device memory is owned by someone else); see include/qwm.h."""
+    H, d, r = cfg.heads, cfg.head_dim, cfg.rank
+    st = _lib.qwm_update_query_stats_noalloc(
+        C.byref(cfg), _ptr(q, "q", 2, (H, nq, d)) if nq else None, nq,
+        _ptr(S, "S", 4, (H, d, d)), _ptr(n, "n", 8, (H,)), _ptr(w, "w", 4, (H, d)),
+        _ptr(eigvals, "eigvals", 4, (H, d)), _ptr(u_r, "u_r", 2, (H, d, r)) if r else None,
+        _ptr(dev_status, "dev_status", 4, (1,)), _stream(stream))
+    _check(st, "qwm_update_query_stats_noalloc")
 
 
 def qwm_status_string(status: int) -> str:

@@ -184,6 +184,30 @@ QWM_API qwm_status qwm_dequantize(qwm_ctx *ctx, const qwm_chunk *chunk, uint16_t
  * the last call, else QWM_OK. */
 QWM_API qwm_status qwm_sync_status(qwm_ctx *ctx, qwm_stream stream);
 
+/* qwm_update_query_stats for callers that cannot allocate device memory.
+ * (This entry point has no counterpart in the paper; it is a deployment convenience.)
+ * Some callers cannot call cudaMalloc: an application whose device memory is handed out by its
+ * own pool or by a host framework that owns every allocation, or a service whose memory budget is
+ * fixed at start-up and must not grow.  Such callers cannot create a qwm_ctx, because
+ * qwm_create allocates the context's workspace.  This call needs no context: it computes
+ * exactly what qwm_update_query_stats computes (same arguments, layouts and meaning, with the
+ * configuration passed directly) and allocates nothing -- no cudaMalloc, no cudaFree, no
+ * allocating library routine.  Its scratch memory (partial sums and the eigensolver's basis) is
+ * one fixed array inside the library, about 12 MiB, that every GPU which loads the library
+ * keeps until the process exits.
+ *   cfg          only heads (1..64), head_dim (128) and rank (0..16) are used; heads > 64 is
+ *                rejected with QWM_ERR_SHAPE
+ *   dev_status   device int32 where a device-side error (QWM_ERR_NOT_CONVERGED, ...) is recorded
+ *                if the word is still 0, or NULL
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.  All calls share the one
+ * array and each call leaves its contents behind: calls that can run on the GPU at the same time
+ * (on different streams) race on it and must be ordered by the caller.  The eigensolver starts
+ * from the identity on every call (no warm start). */
+QWM_API qwm_status qwm_update_query_stats_noalloc(const qwm_config *cfg, const uint16_t *q, int64_t nq, float *S,
+                                                  int64_t *n, float *w, float *eigvals, uint16_t *u_r,
+                                                  int32_t *dev_status, qwm_stream stream);
+
 #ifdef __cplusplus
 }
 #endif
