@@ -53,7 +53,7 @@ class qwm_chunk(C.Structure):
                 ("k_codes", C.c_void_p), ("v_codes", C.c_void_p), ("k_idx", C.c_void_p), ("v_idx", C.c_void_p),
                 ("k_scale", C.c_void_p), ("k_min", C.c_void_p), ("v_scale", C.c_void_p), ("v_min", C.c_void_p),
                 ("cent_k", C.c_void_p), ("cent_v", C.c_void_p), ("c", C.c_void_p), ("c_scale", C.c_void_p),
-                ("u_r", C.c_void_p)]
+                ("u_r", C.c_void_p), ("cent_k16", C.c_void_p), ("cent_v16", C.c_void_p)]
 
 
 class qwm_debug(C.Structure):
@@ -156,6 +156,8 @@ class Chunk:
     c: torch.Tensor
     c_scale: torch.Tensor
     u_r: torch.Tensor
+    cent_k16: torch.Tensor
+    cent_v16: torch.Tensor
 
     @staticmethod
     def empty(ctx: Context, n: int, device=None) -> "Chunk":
@@ -173,15 +175,19 @@ class Chunk:
                      torch.empty(H, Cn, d, dtype=torch.bfloat16, device=dev),
                      torch.zeros(H, n, max(r, 1), dtype=torch.int8, device=dev),
                      torch.zeros(H, n, **f16),
-                     torch.zeros(H, d, max(r, 1), dtype=torch.bfloat16, device=dev))
+                     torch.zeros(H, d, max(r, 1), dtype=torch.bfloat16, device=dev),
+                     torch.empty(H, Cn, d, **f16), torch.empty(H, Cn, d, **f16))
 
-    def nbytes(self) -> int:
-        """Bytes of the packed representation (codebooks and PSAC basis included)."""
+    def nbytes(self, operand_copies: bool = False) -> int:
+        """Bytes of the packed representation (codebooks and PSAC basis included); with
+        `operand_copies`, also the fp16 codebook copies the attention kernel reads."""
         tot = sum(t.numel() * t.element_size() for t in (self.k_codes, self.v_codes, self.k_idx, self.v_idx,
                                                          self.k_scale, self.k_min, self.v_scale, self.v_min,
                                                          self.cent_k, self.cent_v))
         if self.rank_eff:
             tot += sum(t.numel() * t.element_size() for t in (self.c, self.c_scale, self.u_r))
+        if operand_copies:
+            tot += sum(t.numel() * t.element_size() for t in (self.cent_k16, self.cent_v16))
         return tot
 
     def struct(self) -> qwm_chunk:
@@ -190,7 +196,8 @@ class Chunk:
         return qwm_chunk(self.n_tokens, self.rank_eff, 0,
                          p(self.k_codes, 1), p(self.v_codes, 1), p(self.k_idx, 1), p(self.v_idx, 1),
                          p(self.k_scale, 2), p(self.k_min, 2), p(self.v_scale, 2), p(self.v_min, 2),
-                         p(self.cent_k, 2), p(self.cent_v, 2), p(self.c, 1), p(self.c_scale, 2), p(self.u_r, 2))
+                         p(self.cent_k, 2), p(self.cent_v, 2), p(self.c, 1), p(self.c_scale, 2), p(self.u_r, 2),
+                         p(self.cent_k16, 2), p(self.cent_v16, 2))
 
 
 def qwm_update_query_stats(ctx: Context, q, nq: int, S, n, w, eigvals, u_r, stream=None) -> None:

@@ -49,7 +49,7 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 qwm_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QWM_OK : QWM_ERR_CUDA; }
 
 // A chunk descriptor is usable when every pointer it needs is set and aligned.
-qwm_status check_chunk(const qwm_config &c, const qwm_chunk *ch, bool need_outputs) {
+qwm_status check_chunk(const qwm_config &c, const qwm_chunk *ch, bool need_f16) {
   if (!ch) return QWM_ERR_ARG;
   if (ch->n_tokens < 0) return QWM_ERR_ARG;
   if (ch->rank_eff != 0 && ch->rank_eff != c.rank) return QWM_ERR_SHAPE;
@@ -59,7 +59,13 @@ qwm_status check_chunk(const qwm_config &c, const qwm_chunk *ch, bool need_outpu
     if (!p) return QWM_ERR_ARG;
     if (!aligned16(p)) return QWM_ERR_ALIGN;
   }
-  (void)need_outputs;
+  if (need_f16) {  // fp16 codebook copies: written by qwm_quantize_kv, read by qwm_attend
+    const void *f16[] = {ch->cent_k16, ch->cent_v16};
+    for (const void *p : f16) {
+      if (!p) return QWM_ERR_ARG;
+      if (!aligned16(p)) return QWM_ERR_ALIGN;
+    }
+  }
   if (ch->rank_eff > 0) {
     const void *psac[] = {ch->c, ch->c_scale, ch->u_r};
     for (const void *p : psac) {
@@ -202,7 +208,7 @@ qwm_status qwm_attend(qwm_ctx *ctx, const uint16_t *q, int64_t nq, const qwm_chu
   if (n_chunks > 128) return QWM_ERR_SHAPE;
   int64_t total = 0;
   for (int i = 0; i < n_chunks; i++) {
-    qwm_status s = check_chunk(ctx->cfg, &chunks[i], false);
+    qwm_status s = check_chunk(ctx->cfg, &chunks[i], true);
     if (s != QWM_OK) return s;
     total += chunks[i].n_tokens;
   }

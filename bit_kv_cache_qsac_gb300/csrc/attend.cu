@@ -2,31 +2,43 @@
 //
 // QuantWM (Chinese summary, "注意力logits与时空token选择": L = Q K^T / sqrt(d); "核心方法":
 // PSAC logits Q K_hat_0^T + (Q U_r) C^T; English v2 summary §D.1):
-//   l_ij = scale * ([q_i | q_i U_r^(t)] . [k_hat_0_j | c_hat_j]),  o_i = softmax(l_i) V_hat,
+//   l_ij = scale * (q_i . k_hat_0_j + (q_i U_r) . c_hat_j),  o_i = softmax(l_i) V_hat,
 // with k_hat_0 = mu^K_idx + m + s q, c_hat = sC c and v_hat = mu^V_idx + m + s q decoded from the
-// packed chunk inside the kernel.  Nothing decoded is written back to memory.
-// Operands of both MMAs are fp16 (fp32 accumulate): the decode is exact in fp32 and rounded once
-// to fp16, whose 11-bit mantissa keeps the logits of the outlier channels (|k| up to ~40)
-// accurate; Q (bf16 in memory) converts to fp16 exactly for every normal value.
+// packed chunk inside the kernel.  Nothing decoded is written to global memory.
+//
+// Arithmetic.  Both MMAs take fp16 operands (fp32 accumulate): fp16's 11-bit significand keeps the
+// logits of the outlier channels (|k| up to ~40) accurate where bf16 would not, and Q (bf16 in
+// memory) converts to fp16 exactly.  The Key logit is split as
+//   q . k_hat_0 = q . (mu + s q_code) + m_0 sum_{c < 64} q_c + m_1 sum_{c >= 64} q_c,
+// so a Key row is decoded with one fused multiply-add per channel pair, fp16(mu + s q_code), from
+// an fp16 copy of the codebook; the group-offset term rides on a small second MMA whose K columns
+// are [q U_r | hi and lo fp16 parts of the two group sums of q | 1] against
+// [c_hat | m_0 m_0 m_1 m_1 | mask], where mask = -60000 on the zero rows that pad the last tile of
+// a chunk (their probabilities underflow to exactly 0) and 0 elsewhere.  A Value row is decoded as
+// fp16(fp16(mu + m) + s q_code).
+// O is written in fp32: the output is an average over thousands of keys, its largest entries are
+// ~16x its RMS, and rounding those to bf16 alone would cost ~0.03 x RMS(O).
 //
 // One CTA = one head x 256 Queries (two 128-row tiles that share every decoded K/V tile).
-// Warp roles (512 threads):
+// Warp roles (17 warps):
 //   warps 0-3, 4-7  softmax for Query tile 0 / 1: thread = Query row = TMEM lane; reads the
-//                   logits from TMEM, keeps the running max and sum, writes P (bf16) back over
-//                   the logits, rescales O in TMEM when the max grows by more than 2^8;
+//                   logits from TMEM, keeps the running max and sum, writes P (fp16) over the
+//                   logits, rescales O in TMEM when the max grows by more than 2^8;
 //   warp 8          allocates TMEM and issues every tcgen05.mma (one thread);
-//   warps 9-15      producers: decode each 128-token tile of the packed cache into shared memory
-//                   (K_hat_0 rows and V_hat^T rows as 128-byte-swizzled fp16, c_hat in the
-//                   no-swizzle layout) and, at each chunk start, Q U_r for both Query tiles.
+//   warps 9-12      Key producers: thread = key row of the tile; copies the row's centroid
+//                   (cp.async, 16 bytes at a time) into the 128-byte-swizzled K-major stage,
+//                   decodes it in place, writes the row of the second MMA's B operand, and at
+//                   each chunk start builds the second MMA's A operand for both Query tiles;
+//   warps 13-16     Value producers: the same for V_hat rows ([key][d], read as an N-major B).
+// Each producer thread keeps its row's index data two tiles ahead in registers and its centroid
+// copies one tile ahead in the other shared-memory stage.
 // Tensor memory (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each; P_x overlays S_x.
 // MMA order per tile j: S0(j), PV1(j-1), S1(j), PV0(j).  tcgen05 operations complete in issue
 // order, so the commit after S_x(j) also certifies PV_x(j-1): when softmax x sees S_x(j), O_x
 // is stable and may be rescaled.
-// O is written in fp32: the output is an average over thousands of keys, its largest entries are
-// ~16x its RMS, and rounding those to bf16 alone would cost ~0.03 x RMS(O).
 // Every wait is bounded (about one second of wall time); on expiry the CTA records
 // QWM_ERR_DEVICE_TIMEOUT, every role stops, outstanding MMAs are drained and TMEM is freed.
-#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "qwm_internal.cuh"
 #include "tc.cuh"
@@ -35,29 +47,36 @@ namespace {
 
 constexpr int D = QWM_D;
 constexpr int BM = 128, BN = 128, NQT = 2;
-constexpr int kSoftmaxWarps = 8, kMmaWarp = 8, kProdWarp0 = 9, kProdWarps = 7;
-constexpr int kThreads = 32 * (kSoftmaxWarps + 1 + kProdWarps);  // 512
-constexpr int kProdThreads = 32 * kProdWarps;
+constexpr int kSoftmaxWarps = 8, kMmaWarp = 8, kKWarp0 = 9, kVWarp0 = 13, kProdWarps = 4;
+constexpr int kThreads = 32 * (kSoftmaxWarps + 1 + 2 * kProdWarps);  // 544
 constexpr int kMaxChunks = 128;
 constexpr uint64_t kWaitNs = 1000000000ull;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
+constexpr uint32_t kMaskBits = 0xFB53u;    // fp16 -60000
 
 // shared-memory map (bytes from a 1024-aligned base)
-constexpr int kBlk = BM * 128;                    // one [128 rows][64 bf16] swizzled block: 16 KB
-constexpr int OFF_Q = 0;                          // 2 tiles x 2 blocks
-constexpr int OFF_K = OFF_Q + NQT * 2 * kBlk;     // 2 stages x 2 blocks (K_hat_0 rows)
-constexpr int OFF_V = OFF_K + 2 * 2 * kBlk;       // 2 stages x 2 blocks (V_hat^T rows)
-constexpr int OFF_C = OFF_V + 2 * 2 * kBlk;       // 2 stages x [128][16] c_hat (no swizzle)
-constexpr int OFF_QU = OFF_C + 2 * 4096;          // 2 slots x 2 tiles x [128][16] Q U_r
-constexpr int SMEM_BYTES = OFF_QU + 2 * NQT * 4096;
+constexpr int kBlk = BM * 128;                  // one [128 rows][64 fp16] swizzled block: 16 KB
+constexpr int kXBytes = 128 * 32 * 2;           // one [128 rows][32 fp16] no-swizzle operand: 8 KB
+constexpr int OFF_Q = 0;                        // 2 Query tiles x 2 blocks
+constexpr int OFF_K = OFF_Q + NQT * 2 * kBlk;   // 2 stages x 2 blocks of K rows
+constexpr int OFF_V = OFF_K + 2 * 2 * kBlk;     // 2 stages x 2 blocks of V rows
+constexpr int OFF_X = OFF_V + 2 * 2 * kBlk;     // 2 stages: B operand of the second MMA
+constexpr int OFF_QX = OFF_X + 2 * kXBytes;     // 2 Query tiles: A operand of the second MMA
+constexpr int SMEM_BYTES = OFF_QX + NQT * kXBytes;
 constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
+
+// byte offset of (row, column k) in a [128][32] fp16 K-major operand without swizzle: 8x8 core
+// matrices, 128 bytes apart along K and 512 bytes apart along the rows
+__host__ __device__ constexpr uint32_t xoff(uint32_t row, uint32_t k) {
+  return (row >> 3) * 512u + (k >> 3) * 128u + (row & 7u) * 16u + (k & 7u) * 2u;
+}
 
 struct AttnChunk {
   int64_t n;
   int rank;
   int tiles;
   const uint8_t *k_codes, *v_codes, *k_idx, *v_idx;
-  const uint16_t *k_scale, *k_min, *v_scale, *v_min, *cent_k, *cent_v, *c_scale, *u_r;
+  const uint16_t *k_scale, *k_min, *v_scale, *v_min, *cent_k16, *cent_v16, *c_scale, *u_r;
   const int8_t *c;
 };
 
@@ -72,38 +91,271 @@ struct AttnParams {
 };
 
 struct Bars {
-  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_ready[2], o_done, drain;
+  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_ready[2], qx_free, o_done, drain;
 };
 
-__device__ __forceinline__ float half_bits_to_f32(uint16_t h) { return __half2float(__ushort_as_half(h)); }
-
-// 2^23 + q as a float for a 2-bit code q in the low bits of c (exact), and its removal.
-__device__ __forceinline__ float magic_code(uint32_t c) { return __uint_as_float((c & 3u) | 0x4B000000u); }
-constexpr float kMagic = 8388608.0f;
-
-// Decode 32 channels (quarter of a token) of a Key exactly in fp32 -- r_hat = fl(m + s q) and
-// k_hat_0 = fl(mu + r_hat), as in the packing -- then round to fp16: 16 words, channel pairs.
-__device__ __forceinline__ void decode_key_quarter(const uint2 codes, const uint4 (&mu)[4], float s, float m,
-                                                   uint32_t (&out)[16]) {
-  const uint64_t s2 = tc::f2(s, s), m2 = tc::f2(m, m), neg = tc::f2(-kMagic, -kMagic);
-  const uint32_t cw[2] = {codes.x, codes.y};
-#pragma unroll
-  for (int hw = 0; hw < 4; hw++) {  // 8 channels per 16-bit halfword of codes
-    const uint32_t h16 = cw[hw >> 1] >> (16 * (hw & 1));
-    const uint32_t muw[4] = {mu[hw].x, mu[hw].y, mu[hw].z, mu[hw].w};
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-      const uint64_t q2 = tc::add2(tc::f2(magic_code(h16 >> (4 * i)), magic_code(h16 >> (4 * i + 2))), neg);
-      const uint64_t r2 = tc::fma2(s2, q2, m2);
-      const uint64_t k2 = tc::add2(tc::f2(__uint_as_float(muw[i] << 16), __uint_as_float(muw[i] & 0xFFFF0000u)), r2);
-      out[4 * hw + i] = tc::pack_f16x2(tc::f2lo(k2), tc::f2hi(k2));
-    }
-  }
-}
+// Index data of one key row: fp16 scale and offset pairs (group 0 low half), 128 2-bit codes,
+// and (Keys) the PSAC coefficients and their scale.
+struct RowData {
+  int idx;  // centroid, or -1 for a row past the end of the chunk
+  uint32_t scl, mn;
+  uint4 c0, c1;
+  uint2 ca, cb;  // coefficients 0-7 and 8-15
+  uint32_t csc;
+};
 
 __device__ __forceinline__ void fail(int *abort_flag, int32_t *status) {
   *(volatile int *)abort_flag = 1;
   qwm_dev_error(status, QWM_ERR_DEVICE_TIMEOUT);
+}
+
+__device__ __forceinline__ uint32_t f16pair(float lo, float hi) { return tc::pack_f16x2(lo, hi); }
+
+template <bool VAL>
+__device__ __forceinline__ void load_row(const AttnChunk &c, int h, int C, int64_t k0, int nk, int r, RowData &d) {
+  d.idx = -1;
+  d.scl = d.mn = d.csc = 0u;
+  d.c0 = d.c1 = make_uint4(0, 0, 0, 0);
+  d.ca = d.cb = make_uint2(0, 0);
+  if (r >= nk) return;
+  const int64_t gi = (int64_t)h * c.n + k0 + r;
+  const int ix = (VAL ? c.v_idx : c.k_idx)[gi];
+  d.idx = ix < C ? ix : C - 1;  // never past the codebook
+  d.scl = *(const uint32_t *)((VAL ? c.v_scale : c.k_scale) + gi * 2);
+  d.mn = *(const uint32_t *)((VAL ? c.v_min : c.k_min) + gi * 2);
+  const uint4 *cp = (const uint4 *)((VAL ? c.v_codes : c.k_codes) + gi * (D / 4));
+  d.c0 = cp[0];
+  d.c1 = cp[1];
+  if (!VAL && c.rank > 0) {
+    const int R = c.rank;
+    const int8_t *src = c.c + gi * R;
+    if (R == 8) {
+      d.ca = *(const uint2 *)src;  // row offset 8 gi: 8-byte aligned
+    } else if (R == 16) {
+      const uint4 v = *(const uint4 *)src;
+      d.ca = make_uint2(v.x, v.y);
+      d.cb = make_uint2(v.z, v.w);
+    } else {
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int k = 0; k < 16; k++)
+        if (k < R) w[k >> 2] |= ((uint32_t)(uint8_t)src[k]) << (8 * (k & 3));
+      d.ca = make_uint2(w[0], w[1]);
+      d.cb = make_uint2(w[2], w[3]);
+    }
+    d.csc = c.c_scale[gi];
+  }
+}
+
+// Centroid row of `d` -> this thread's row of a swizzled stage (zeros for a row past the end).
+__device__ __forceinline__ void issue_row_copies(const uint16_t *cent16, int h, int C, const RowData &d,
+                                                 uint32_t stage, int r) {
+  const uint32_t rowb = stage + (uint32_t)r * 128u, rx = (uint32_t)r & 7u;
+  const uint32_t bytes = d.idx >= 0 ? 16u : 0u;
+  const uint16_t *src = cent16 + ((int64_t)h * C + (d.idx >= 0 ? d.idx : 0)) * D;
+#pragma unroll
+  for (int v = 0; v < 16; v++)
+    tc::cp_async16_zfill(rowb + (uint32_t)(v >> 3) * kBlk + ((((uint32_t)v & 7u) ^ rx) << 4), src + 8 * v, bytes);
+}
+
+// In-place decode of this thread's row: fp16(mu + s q) for Keys, fp16(fp16(mu + m) + s q) for
+// Values; `lut` maps a 4-bit code pair to the fp16 pair (q_even, q_odd).
+template <bool VAL>
+__device__ __forceinline__ void decode_row(const RowData &d, uint32_t stage, int r, uint32_t lut) {
+  if (d.idx < 0) return;  // zero-filled by the copies
+  const uint32_t rowb = stage + (uint32_t)r * 128u, rx = (uint32_t)r & 7u;
+#pragma unroll
+  for (int g = 0; g < 2; g++) {
+    const uint32_t s2 = __byte_perm(d.scl, 0u, g ? 0x3232u : 0x1010u);
+    const uint32_t m2 = __byte_perm(d.mn, 0u, g ? 0x3232u : 0x1010u);
+    const uint4 cw = g ? d.c1 : d.c0;
+    const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+    for (int v = 0; v < 8; v++) {
+      const uint32_t addr = rowb + (uint32_t)g * kBlk + ((((uint32_t)v) ^ rx) << 4);
+      const uint4 mu = tc::lds128(addr);
+      const uint32_t h16 = words[v >> 1] >> (16 * (v & 1));
+      const uint32_t q0 = tc::lds32(lut + ((h16 << 2) & 0x3Cu));
+      const uint32_t q1 = tc::lds32(lut + ((h16 >> 2) & 0x3Cu));
+      const uint32_t q2 = tc::lds32(lut + ((h16 >> 6) & 0x3Cu));
+      const uint32_t q3 = tc::lds32(lut + ((h16 >> 10) & 0x3Cu));
+      uint4 o;
+      if (VAL) {
+        o.x = tc::hfma2(s2, q0, tc::hadd2(mu.x, m2));
+        o.y = tc::hfma2(s2, q1, tc::hadd2(mu.y, m2));
+        o.z = tc::hfma2(s2, q2, tc::hadd2(mu.z, m2));
+        o.w = tc::hfma2(s2, q3, tc::hadd2(mu.w, m2));
+      } else {
+        o.x = tc::hfma2(s2, q0, mu.x);
+        o.y = tc::hfma2(s2, q1, mu.y);
+        o.z = tc::hfma2(s2, q2, mu.z);
+        o.w = tc::hfma2(s2, q3, mu.w);
+      }
+      tc::sts128(addr, o);
+    }
+  }
+}
+
+// This thread's row of the second MMA's B operand: [c_hat (8 or 16) | m0 m0 m1 m1 | mask | 0 ...].
+__device__ __forceinline__ void write_x_row(const RowData &d, int R, uint32_t xs, int r) {
+  uint32_t w[16];
+#pragma unroll
+  for (int i = 0; i < 16; i++) w[i] = 0u;
+  const float sc = __half2float(__ushort_as_half((uint16_t)d.csc));
+  const uint32_t cwd[4] = {d.ca.x, d.ca.y, d.cb.x, d.cb.y};
+  const uint32_t mm0 = __byte_perm(d.mn, 0u, 0x1010u), mm1 = __byte_perm(d.mn, 0u, 0x3232u);
+  const uint32_t mask = d.idx >= 0 ? 0u : kMaskBits;
+  if (R <= 8) {
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+      const uint32_t cv = cwd[i >> 1] >> (16 * (i & 1));
+      w[i] = f16pair(sc * (float)(int8_t)(cv & 0xFFu), sc * (float)(int8_t)(cv >> 8));
+    }
+    w[4] = mm0;
+    w[5] = mm1;
+    w[6] = mask;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+      const uint32_t cv = cwd[i >> 1] >> (16 * (i & 1));
+      w[i] = f16pair(sc * (float)(int8_t)(cv & 0xFFu), sc * (float)(int8_t)(cv >> 8));
+    }
+    w[8] = mm0;
+    w[9] = mm1;
+    w[10] = mask;
+  }
+#pragma unroll
+  for (int kc = 0; kc < 4; kc++)
+    tc::sts128(xs + xoff((uint32_t)r, 8u * kc), make_uint4(w[4 * kc], w[4 * kc + 1], w[4 * kc + 2], w[4 * kc + 3]));
+}
+
+// Query row qi's row of the second MMA's A operand: [q U_r | hi, lo of both group sums | 1 | 0 ...].
+__device__ __forceinline__ void write_qx_row(const AttnParams &p, const AttnChunk &ch, int h, int64_t qi,
+                                             uint32_t dst, int r) {
+  const int R = ch.rank;
+  float acc[16];
+#pragma unroll
+  for (int k = 0; k < 16; k++) acc[k] = 0.f;
+  float s0 = 0.f, s1 = 0.f;
+  const bool live = qi < p.nq;
+  if (live) {
+    const uint16_t *U = ch.u_r + (int64_t)h * D * R;
+    const uint4 *qrow = (const uint4 *)(p.q + ((int64_t)h * p.nq + qi) * D);
+    for (int ci = 0; ci < D / 8; ci++) {
+      const uint4 qv = qrow[ci];
+      const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+      for (int u = 0; u < 8; u++) {
+        const float qc = __uint_as_float((u & 1) ? (qw[u >> 1] & 0xFFFF0000u) : (qw[u >> 1] << 16));
+        if (ci < 8) s0 += qc;
+        else s1 += qc;
+        const int c = 8 * ci + u;
+        if (R == 8) {
+          const uint4 uv = *(const uint4 *)(U + c * 8);
+          const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
+#pragma unroll
+          for (int k = 0; k < 8; k++)
+            acc[k] = fmaf(qc, __uint_as_float((k & 1) ? (uw[k >> 1] & 0xFFFF0000u) : (uw[k >> 1] << 16)), acc[k]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 16; k++)
+            if (k < R) acc[k] = fmaf(qc, bf16_to_f32(U[c * R + k]), acc[k]);
+        }
+      }
+    }
+  }
+  uint32_t w[16];
+#pragma unroll
+  for (int i = 0; i < 16; i++) w[i] = 0u;
+  const float h0 = __half2float(__float2half_rn(s0)), h1 = __half2float(__float2half_rn(s1));
+  const uint32_t g0 = f16pair(h0, s0 - h0), g1 = f16pair(h1, s1 - h1);
+  const uint32_t one = live ? 0x3C00u : 0u;
+  if (R <= 8) {
+#pragma unroll
+    for (int i = 0; i < 4; i++) w[i] = f16pair(acc[2 * i], acc[2 * i + 1]);
+    w[4] = g0;
+    w[5] = g1;
+    w[6] = one;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; i++) w[i] = f16pair(acc[2 * i], acc[2 * i + 1]);
+    w[8] = g0;
+    w[9] = g1;
+    w[10] = one;
+  }
+#pragma unroll
+  for (int kc = 0; kc < 4; kc++)
+    tc::sts128(dst + xoff((uint32_t)r, 8u * kc), make_uint4(w[4 * kc], w[4 * kc + 1], w[4 * kc + 2], w[4 * kc + 3]));
+}
+
+// Key (VAL = false) or Value (VAL = true) producer loop of one thread (row r of every tile).
+template <bool VAL>
+__device__ __forceinline__ void producer(const AttnParams &p, unsigned char *sm, Bars &bars, int *abort_flag,
+                                         uint32_t lut, int h, int64_t q0, int r, int lane) {
+  volatile int *abort_v = abort_flag;
+  const int J = p.total_tiles, C = p.C;
+  uint64_t *full = VAL ? bars.v_full : bars.k_full;
+  uint64_t *empty = VAL ? bars.v_empty : bars.k_empty;
+  const uint32_t stage0 = tc::smem_u32(sm + (VAL ? OFF_V : OFF_K));
+  const uint32_t xs0 = tc::smem_u32(sm + OFF_X), qx0 = tc::smem_u32(sm + OFF_QX);
+  // positions (chunk, tile in chunk) of tiles j, j+1, j+2
+  int t = 0, tic = 0, t1 = 0, ti1 = 0, t2 = 0, ti2 = 0;
+  auto advance = [&](int &tt, int &ti) {
+    if (++ti == p.ch[tt].tiles) { ti = 0; tt++; }
+  };
+  auto load_at = [&](int tt, int ti, RowData &d) {
+    const AttnChunk &c = p.ch[tt];
+    const int64_t k0 = (int64_t)ti * BN;
+    const int nk = (c.n - k0) < BN ? (int)(c.n - k0) : BN;
+    load_row<VAL>(c, h, C, k0, nk, r, d);
+  };
+  RowData cur, nxt, nxt2;
+  nxt.idx = nxt2.idx = -1;
+  load_at(0, 0, cur);
+  if (J > 1) {
+    advance(t1, ti1);
+    load_at(t1, ti1, nxt);
+  }
+  issue_row_copies(VAL ? p.ch[0].cent_v16 : p.ch[0].cent_k16, h, C, cur, stage0, r);
+  tc::cp_async_commit();
+  for (int j = 0; j < J; j++) {
+    const int s = j & 1;
+    const AttnChunk &ch = p.ch[t];
+    // ---- tile j: wait for this thread's copies, decode in place ----
+    tc::cp_async_wait<0>();
+    decode_row<VAL>(cur, stage0 + (uint32_t)s * 2u * kBlk, r, lut);
+    if (!VAL) {
+      write_x_row(cur, ch.rank, xs0 + (uint32_t)s * kXBytes, r);
+      if (tic == 0) {  // chunk start: the second MMA's A operand for both Query tiles
+        if (t > 0 && !tc::mbar_wait(&bars.qx_free, (t - 1) & 1, kWaitNs)) fail(abort_flag, p.status);
+        if (*abort_v) break;
+        write_qx_row(p, ch, h, q0 + r, qx0, r);
+        write_qx_row(p, ch, h, q0 + BM + r, qx0 + kXBytes, r);
+      }
+    }
+    tc::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(&full[s]);
+    // ---- tile j+1: copies into the other stage once tile j-1 has released it ----
+    if (j + 1 < J) {
+      if (j >= 1 && !tc::mbar_wait(&empty[s ^ 1], ((j - 1) >> 1) & 1, kWaitNs)) fail(abort_flag, p.status);
+      if (*abort_v) break;
+      issue_row_copies(VAL ? p.ch[t1].cent_v16 : p.ch[t1].cent_k16, h, C, nxt, stage0 + (uint32_t)(s ^ 1) * 2u * kBlk,
+                       r);
+      tc::cp_async_commit();
+    }
+    // ---- index data of tile j+2 ----
+    if (j + 2 < J) {
+      t2 = t1; ti2 = ti1;
+      advance(t2, ti2);
+      load_at(t2, ti2, nxt2);
+    }
+    cur = nxt;
+    nxt = nxt2;
+    t = t1; tic = ti1;
+    t1 = t2; ti1 = ti2;
+  }
+  tc::cp_async_wait<0>();
 }
 
 __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_constant__ AttnParams p) {
@@ -112,12 +364,13 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
   __shared__ Bars bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
+  __shared__ __align__(64) uint32_t code_lut[16];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.y;
   const int64_t q0 = (int64_t)blockIdx.x * (BM * NQT);
   volatile int *abort_v = &abort_flag;
 
-  // ---- Query tiles -> shared memory (zero rows past nq) ----
+  // ---- Query tiles -> shared memory as fp16 (zero rows past nq) ----
   for (int e = tid; e < NQT * BM * (D / 8); e += kThreads) {
     const int row = e / (D / 8), ci = e % (D / 8);  // row in [0, 256), 16-byte chunk in [0, 16)
     const int x = row / BM, rr = row % BM, b = ci / 8;
@@ -127,9 +380,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     const uint32_t bw[4] = {v.x, v.y, v.z, v.w};
     uint32_t hw[4];
 #pragma unroll
-    for (int u = 0; u < 4; u++) hw[u] = tc::pack_f16x2(__uint_as_float(bw[u] << 16), __uint_as_float(bw[u] & 0xFFFF0000u));
+    for (int u = 0; u < 4; u++) hw[u] = f16pair(__uint_as_float(bw[u] << 16), __uint_as_float(bw[u] & 0xFFFF0000u));
     *(uint4 *)(sm + OFF_Q + (x * 2 + b) * kBlk + tc::sw128_offset(rr, 8 * (ci % 8))) =
         make_uint4(hw[0], hw[1], hw[2], hw[3]);
+  }
+  if (tid < 16) {  // fp16 bits of the code values 0, 1, 2, 3: 0x0000, 0x3C00, 0x4000, 0x4200
+    const uint32_t lo = ((0x42403C00u >> (8 * (tid & 3))) & 0xFFu) << 8;
+    const uint32_t hi = ((0x42403C00u >> (8 * (tid >> 2))) & 0xFFu) << 8;
+    code_lut[tid] = lo | (hi << 16);
   }
   if (tid == 0) {
     for (int i = 0; i < 2; i++) {
@@ -140,6 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
       tc::mbar_init(&bars.s_full[i], 1);
       tc::mbar_init(&bars.p_ready[i], 4);
     }
+    tc::mbar_init(&bars.qx_free, 1);
     tc::mbar_init(&bars.o_done, 1);
     tc::mbar_init(&bars.drain, 1);
     abort_flag = 0;
@@ -161,81 +420,88 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     const int x = warp / 4, sub = warp % 4, row = 32 * sub + lane;
     const uint32_t lane_addr = (uint32_t)(32 * sub) << 16;
     const uint32_t tS = tmem + lane_addr + 128u * x, tO = tmem + lane_addr + 256u + 128u * x;
-    float m_used = -INFINITY, l = 0.f;
-    int t = 0, tile_in_chunk = 0;
+    const float sl2 = p.scale_log2;
+    float m_used = -INFINITY;
+    float l0 = 0.f, l1 = 0.f;  // running row sum (two partial sums)
     bool ok = true;
     for (int j = 0; j < J; j++) {
-      const AttnChunk &ch = p.ch[t];
-      const int64_t left = ch.n - (int64_t)tile_in_chunk * BN;
-      const int nk = left < BN ? (int)left : BN;
       if (!tc::mbar_wait(&bars.s_full[x], j & 1, kWaitNs)) fail(&abort_flag, p.status);
       if (*abort_v) { ok = false; break; }
       tc::fence_after_sync();
       uint32_t r[32];
-      float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < BN; c += 32) {
-        tc::tmem_ld32(tS + c, r);
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll 1
+      for (int cq = 0; cq < 4; cq++) {
+        tc::tmem_ld16(tS + 32u * cq, r);
+        tc::tmem_ld16(tS + 32u * cq + 16u, r + 16);
         tc::tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; i++)
-          if (c + i < nk) mx = fmaxf(mx, __uint_as_float(r[i]));
+        for (int i = 0; i < 32; i += 8) {
+          mx0 = tc::max3(mx0, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+          mx1 = tc::max3(mx1, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+          mx2 = tc::max3(mx2, __uint_as_float(r[i + 4]), __uint_as_float(r[i + 5]));
+          mx3 = tc::max3(mx3, __uint_as_float(r[i + 6]), __uint_as_float(r[i + 7]));
+        }
       }
-      const float m_new = fmaxf(m_used, mx * p.scale_log2);
-      const bool need = (j == 0) || (m_new > m_used + kRescaleThreshold);
-      if (__any_sync(0xffffffffu, need)) {
+      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      const float m_new = fmaxf(m_used, mx * sl2);
+      if (__any_sync(0xffffffffu, m_new > m_used + kRescaleThreshold)) {
         if (j > 0) {
           const float alpha = tc::ex2_approx(m_used - m_new);
-          l *= alpha;
-#pragma unroll
+          l0 *= alpha;
+          l1 *= alpha;
+#pragma unroll 1
           for (int c = 0; c < D; c += 32) {
-            tc::tmem_ld32(tO + c, r);
+            uint32_t o[32];
+            tc::tmem_ld32(tO + c, o);
             tc::tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; i++) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            tc::tmem_st32(tO + c, r);
+            for (int i = 0; i < 32; i++) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tc::tmem_st32(tO + c, o);
           }
         }
         m_used = m_new;
       }
-#pragma unroll
-      for (int c = 0; c < BN; c += 32) {
-        tc::tmem_ld32(tS + c, r);
+      const float nm = -m_used;
+#pragma unroll 1
+      for (int cq = 0; cq < 4; cq++) {
+        tc::tmem_ld16(tS + 32u * cq, r);
+        tc::tmem_ld16(tS + 32u * cq + 16u, r + 16);
         tc::tmem_ld_wait();
         uint32_t pw[16];
 #pragma unroll
         for (int i = 0; i < 16; i++) {
-          const float x0 = (c + 2 * i < nk) ? tc::ex2_approx(__uint_as_float(r[2 * i]) * p.scale_log2 - m_used) : 0.f;
-          const float x1 =
-              (c + 2 * i + 1 < nk) ? tc::ex2_approx(__uint_as_float(r[2 * i + 1]) * p.scale_log2 - m_used) : 0.f;
-          l += x0 + x1;
-          pw[i] = tc::pack_f16x2(x0, x1);
+          const float e0 = tc::ex2_approx(fmaf(__uint_as_float(r[2 * i]), sl2, nm));
+          const float e1 = tc::ex2_approx(fmaf(__uint_as_float(r[2 * i + 1]), sl2, nm));
+          if (i & 1) l1 += e0 + e1;
+          else l0 += e0 + e1;
+          pw[i] = f16pair(e0, e1);
         }
-        tc::tmem_st16(tS + c / 2, pw);  // P overlays the first 64 columns of S
+        tc::tmem_st16(tS + 16u * cq, pw);  // P (fp16 pairs) overlays the logits already read
       }
       tc::tmem_st_wait();
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&bars.p_ready[x]);
-      if (++tile_in_chunk == ch.tiles) { tile_in_chunk = 0; t++; }
     }
-    // ---- epilogue: O / l -> bf16 ----
+    // ---- epilogue: O / l -> fp32 ----
     if (ok && !tc::mbar_wait(&bars.o_done, 0, kWaitNs)) fail(&abort_flag, p.status);
     if (ok && !*abort_v) {
       tc::fence_after_sync();
+      const float l = l0 + l1;
       const int64_t qi = q0 + (int64_t)x * BM + row;
       const float inv = 1.f / l;
-      uint32_t r[32];
-#pragma unroll
+      uint32_t o[32];
+#pragma unroll 1
       for (int c = 0; c < D; c += 32) {
-        tc::tmem_ld32(tO + c, r);
+        tc::tmem_ld32(tO + c, o);
         tc::tmem_ld_wait();
         if (qi < p.nq) {
           float4 *dst = (float4 *)(p.out + ((int64_t)h * p.nq + qi) * D + c);
 #pragma unroll
           for (int v = 0; v < 8; v++)
-            dst[v] = make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
-                                 __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv);
+            dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
+                                 __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
         }
       }
     }
@@ -243,36 +509,37 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     // ======================= MMA issue (one thread) =======================
     if (lane == 0) {
       const uint32_t idesc = tc::idesc_f16_f32(BM, BN);
+      const uint32_t idesc_pv = tc::idesc_f16_f32_bmn(BM, D);  // V_hat tiles are [key][d]: N-major
       const uint32_t tS[2] = {tmem, tmem + 128u}, tO[2] = {tmem + 256u, tmem + 384u};
       const uint32_t sQ = tc::smem_u32(sm + OFF_Q), sK = tc::smem_u32(sm + OFF_K), sV = tc::smem_u32(sm + OFF_V);
-      const uint32_t sC = tc::smem_u32(sm + OFF_C), sQU = tc::smem_u32(sm + OFF_QU);
+      const uint32_t sX = tc::smem_u32(sm + OFF_X), sQX = tc::smem_u32(sm + OFF_QX);
       int t = 0, tile_in_chunk = 0, prev_stage = 0;
       bool ok = true;
-      auto qk = [&](int x, int s, int slot, int rank) {
+      auto qk = [&](int x, int s, int nx) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; kk++) {
           const uint32_t off = (uint32_t)((kk / 4) * kBlk + 32 * (kk % 4));
           tc::mma_ss(tS[x], tc::desc_sw128(sQ + (x * 2) * kBlk + off), tc::desc_sw128(sK + (s * 2) * kBlk + off),
                      idesc, kk > 0);
         }
-        if (rank > 0)
-          tc::mma_ss(tS[x], tc::desc_noswz(sQU + (slot * NQT + x) * 4096, 128, 256),
-                     tc::desc_noswz(sC + s * 4096, 128, 256), idesc, 1);
+        for (int ks = 0; ks < nx; ks++)
+          tc::mma_ss(tS[x], tc::desc_noswz(sQX + x * kXBytes + 256u * ks, 128, 512),
+                     tc::desc_noswz(sX + s * kXBytes + 256u * ks, 128, 512), idesc, 1);
       };
       auto pv = [&](int x, int s, bool first) {
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; kk++) {
-          const uint32_t off = (uint32_t)((kk / 4) * kBlk + 32 * (kk % 4));
-          tc::mma_ts(tO[x], tS[x] + 8u * kk, tc::desc_sw128(sV + (s * 2) * kBlk + off), idesc, (!first || kk > 0));
-        }
+        for (int kk = 0; kk < BN / 16; kk++)
+          tc::mma_ts(tO[x], tS[x] + 8u * kk, tc::desc_sw128_mn(sV + (s * 2) * kBlk + 2048u * kk, kBlk, 1024), idesc_pv,
+                     (!first || kk > 0));
       };
       for (int j = 0; j < J; j++) {
         const int s = j & 1;
         const AttnChunk &ch = p.ch[t];
+        const int nx = ch.rank <= 8 ? 1 : 2;
         ok = tc::mbar_wait(&bars.k_full[s], (j >> 1) & 1, kWaitNs) && !*abort_v;
         if (!ok) break;
         tc::fence_after_sync();
-        qk(0, s, t & 1, ch.rank);
+        qk(0, s, nx);
         tc::mma_commit(&bars.s_full[0]);
         if (j > 0) {
           ok = tc::mbar_wait(&bars.p_ready[1], (j - 1) & 1, kWaitNs) && !*abort_v;
@@ -281,16 +548,19 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
           pv(1, prev_stage, j - 1 == 0);
           tc::mma_commit(&bars.v_empty[prev_stage]);
         }
-        qk(1, s, t & 1, ch.rank);
+        qk(1, s, nx);
         tc::mma_commit(&bars.s_full[1]);
         tc::mma_commit(&bars.k_empty[s]);
+        const bool last_of_chunk = tile_in_chunk + 1 == ch.tiles;
+        if (last_of_chunk) tc::mma_commit(&bars.qx_free);
         ok = tc::mbar_wait(&bars.v_full[s], (j >> 1) & 1, kWaitNs) && tc::mbar_wait(&bars.p_ready[0], j & 1, kWaitNs) &&
              !*abort_v;
         if (!ok) break;
         tc::fence_after_sync();
         pv(0, s, j == 0);
         prev_stage = s;
-        if (++tile_in_chunk == ch.tiles) { tile_in_chunk = 0; t++; }
+        if (last_of_chunk) { tile_in_chunk = 0; t++; }
+        else tile_in_chunk++;
       }
       if (ok && J > 0) {
         ok = tc::mbar_wait(&bars.p_ready[1], (J - 1) & 1, kWaitNs) && !*abort_v;
@@ -305,178 +575,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
       tc::mma_commit(&bars.drain);
       if (!tc::mbar_wait(&bars.drain, 0, kWaitNs)) qwm_dev_error(p.status, QWM_ERR_DEVICE_TIMEOUT);
     }
+  } else if (warp < kVWarp0) {
+    producer<false>(p, sm, bars, &abort_flag, tc::smem_u32(code_lut), h, q0, tid - 32 * kKWarp0, lane);
   } else {
-    // ======================= producers: decode tiles of the packed cache =======================
-    const int pt = tid - 32 * kProdWarp0;  // 0..223
-    int t = 0, tile_in_chunk = 0;
-    for (int j = 0; j < J; j++) {
-      const int s = j & 1;
-      const AttnChunk &ch = p.ch[t];
-      const int64_t k0 = (int64_t)tile_in_chunk * BN;
-      const int64_t left = ch.n - k0;
-      const int nk = left < BN ? (int)left : BN;
-      const int R = ch.rank;
-      if (j >= 2 && !tc::mbar_wait(&bars.k_empty[s], ((j >> 1) - 1) & 1, kWaitNs)) fail(&abort_flag, p.status);
-      if (*abort_v) break;
-      // --- Q U_r of this chunk, for both Query tiles (first tile of the chunk only) ---
-      if (tile_in_chunk == 0 && R > 0) {
-        const uint16_t *U = ch.u_r + (int64_t)h * D * R;
-        for (int row = pt; row < NQT * BM; row += kProdThreads) {
-          const int x = row / BM, rr = row % BM;
-          float acc[16];
-#pragma unroll
-          for (int kq = 0; kq < 16; kq++) acc[kq] = 0.f;
-          const int64_t qi = q0 + row;
-          for (int ci = 0; ci < D / 8; ci++) {
-            uint4 qv = make_uint4(0, 0, 0, 0);
-            if (qi < p.nq) qv = *(const uint4 *)(p.q + ((int64_t)h * p.nq + qi) * D + 8 * ci);
-            const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
-#pragma unroll
-            for (int u = 0; u < 8; u++) {
-              const float qc = __uint_as_float((u & 1) ? (qw[u / 2] & 0xFFFF0000u) : (qw[u / 2] << 16));
-              const uint16_t *Uc = U + (8 * ci + u) * R;
-#pragma unroll
-              for (int kq = 0; kq < 16; kq++)
-                if (kq < R) acc[kq] = fmaf(qc, bf16_to_f32(Uc[kq]), acc[kq]);
-            }
-          }
-          uint32_t w[8];
-#pragma unroll
-          for (int i = 0; i < 8; i++) w[i] = tc::pack_f16x2(acc[2 * i], acc[2 * i + 1]);
-          unsigned char *dst = sm + OFF_QU + ((t & 1) * NQT + x) * 4096;
-          *(uint4 *)(dst + tc::noswz16_offset(rr, 0)) = make_uint4(w[0], w[1], w[2], w[3]);
-          *(uint4 *)(dst + tc::noswz16_offset(rr, 8)) = make_uint4(w[4], w[5], w[6], w[7]);
-        }
-      }
-      // --- K_hat_0 rows: item = (token row, quarter of 32 channels), up to 3 per thread.  All
-      // index loads are issued first, then all centroid gathers, then the decode, so that each
-      // thread has its loads in flight together instead of one dependent chain per item. ---
-      {
-        constexpr int kItems = (BN * 4 + kProdThreads - 1) / kProdThreads;  // 3
-        int idx[kItems];
-        float sc[kItems], mn[kItems];
-        uint2 cd[kItems];
-        bool ok[kItems];
-#pragma unroll
-        for (int i = 0; i < kItems; i++) {
-          const int it = pt + i * kProdThreads, row = it >> 2, qd = it & 3;
-          ok[i] = it < BN * 4 && row < nk;
-          idx[i] = 0; sc[i] = 0.f; mn[i] = 0.f; cd[i] = make_uint2(0, 0);
-          if (ok[i]) {
-            const int64_t gi = (int64_t)h * ch.n + k0 + row;
-            idx[i] = min((int)ch.k_idx[gi], p.C - 1);  // never read past the codebook
-            sc[i] = half_bits_to_f32(ch.k_scale[gi * 2 + (qd >> 1)]);
-            mn[i] = half_bits_to_f32(ch.k_min[gi * 2 + (qd >> 1)]);
-            cd[i] = *(const uint2 *)(ch.k_codes + gi * (D / 4) + 8 * qd);
-          }
-        }
-        uint4 muv[kItems][4];
-#pragma unroll
-        for (int i = 0; i < kItems; i++) {
-          const int qd = (pt + i * kProdThreads) & 3;
-          const uint4 *mu = (const uint4 *)(ch.cent_k + ((int64_t)h * p.C + idx[i]) * D + 32 * qd);
-#pragma unroll
-          for (int v = 0; v < 4; v++) muv[i][v] = ok[i] ? mu[v] : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int i = 0; i < kItems; i++) {
-          const int it = pt + i * kProdThreads, row = it >> 2, qd = it & 3;
-          if (it >= BN * 4) continue;
-          uint32_t w[16];
-          if (ok[i]) {
-            decode_key_quarter(cd[i], muv[i], sc[i], mn[i], w);
-          } else {
-#pragma unroll
-            for (int u = 0; u < 16; u++) w[u] = 0u;
-          }
-          unsigned char *blk = sm + OFF_K + (s * 2 + (qd >> 1)) * kBlk;
-#pragma unroll
-          for (int v = 0; v < 4; v++)
-            *(uint4 *)(blk + tc::sw128_offset(row, 32 * (qd & 1) + 8 * v)) =
-                make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
-        }
-      }
-      // --- c_hat rows (PSAC coefficients, fp16, zero past the rank) ---
-      if (R > 0) {
-        for (int row = pt; row < BN; row += kProdThreads) {
-          uint32_t w[8];
-#pragma unroll
-          for (int i = 0; i < 8; i++) w[i] = 0u;
-          if (row < nk) {
-            const int64_t gi = (int64_t)h * ch.n + k0 + row;
-            const float sc = half_bits_to_f32(ch.c_scale[gi]);
-            const int8_t *cc = ch.c + gi * R;
-#pragma unroll
-            for (int i = 0; i < 8; i++) {
-              const float a = (2 * i < R) ? sc * (float)cc[2 * i] : 0.f;
-              const float bq = (2 * i + 1 < R) ? sc * (float)cc[2 * i + 1] : 0.f;
-              w[i] = tc::pack_f16x2(a, bq);
-            }
-          }
-          unsigned char *dst = sm + OFF_C + s * 4096;
-          *(uint4 *)(dst + tc::noswz16_offset(row, 0)) = make_uint4(w[0], w[1], w[2], w[3]);
-          *(uint4 *)(dst + tc::noswz16_offset(row, 8)) = make_uint4(w[4], w[5], w[6], w[7]);
-        }
-      }
-      tc::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&bars.k_full[s]);
-      // --- V_hat^T rows: item = (token pair, quarter of 32 channels) ---
-      if (j >= 2 && !tc::mbar_wait(&bars.v_empty[s], ((j >> 1) - 1) & 1, kWaitNs)) fail(&abort_flag, p.status);
-      if (*abort_v) break;
-      for (int it = pt; it < (BN / 2) * 4; it += kProdThreads) {
-        const int pair = it >> 2, qd = it & 3, g = qd >> 1;
-        uint2 codes[2] = {make_uint2(0, 0), make_uint2(0, 0)};
-        uint4 muv[2][4];
-        float sv[2] = {0.f, 0.f}, mv[2] = {0.f, 0.f};
-#pragma unroll
-        for (int u = 0; u < 2; u++) {
-          const int row = 2 * pair + u;
-          if (row < nk) {
-            const int64_t gi = (int64_t)h * ch.n + k0 + row;
-            const int idx = min((int)ch.v_idx[gi], p.C - 1);
-            sv[u] = half_bits_to_f32(ch.v_scale[gi * 2 + g]);
-            mv[u] = half_bits_to_f32(ch.v_min[gi * 2 + g]);
-            codes[u] = *(const uint2 *)(ch.v_codes + gi * (D / 4) + 8 * qd);
-            const uint4 *mu = (const uint4 *)(ch.cent_v + ((int64_t)h * p.C + idx) * D + 32 * qd);
-#pragma unroll
-            for (int v = 0; v < 4; v++) muv[u][v] = mu[v];
-          } else {
-#pragma unroll
-            for (int v = 0; v < 4; v++) muv[u][v] = make_uint4(0, 0, 0, 0);
-          }
-        }
-        const bool valid0 = (2 * pair) < nk, valid1 = (2 * pair + 1) < nk;
-        const uint64_t s2 = tc::f2(sv[0], sv[1]), m2 = tc::f2(mv[0], mv[1]), neg = tc::f2(-kMagic, -kMagic);
-        const uint32_t cw0[2] = {codes[0].x, codes[0].y}, cw1[2] = {codes[1].x, codes[1].y};
-        const int key = 2 * pair, vb = key / 64, kin = key % 64;
-        unsigned char *blk = sm + OFF_V + (s * 2 + vb) * kBlk;
-#pragma unroll
-        for (int hw = 0; hw < 4; hw++) {  // 8 channels each
-          const uint32_t a16 = cw0[hw >> 1] >> (16 * (hw & 1));
-          const uint32_t b16 = cw1[hw >> 1] >> (16 * (hw & 1));
-          const uint32_t mu0[4] = {muv[0][hw].x, muv[0][hw].y, muv[0][hw].z, muv[0][hw].w};
-          const uint32_t mu1[4] = {muv[1][hw].x, muv[1][hw].y, muv[1][hw].z, muv[1][hw].w};
-#pragma unroll
-          for (int u = 0; u < 8; u++) {
-            const int c = 32 * qd + 8 * hw + u;  // channel = V_hat^T row
-            const uint64_t q2 = tc::add2(tc::f2(magic_code(a16 >> (2 * u)), magic_code(b16 >> (2 * u))), neg);
-            const uint64_t r2 = tc::fma2(s2, q2, m2);
-            const float mua = __uint_as_float((u & 1) ? (mu0[u >> 1] & 0xFFFF0000u) : (mu0[u >> 1] << 16));
-            const float mub = __uint_as_float((u & 1) ? (mu1[u >> 1] & 0xFFFF0000u) : (mu1[u >> 1] << 16));
-            const uint64_t v2 = tc::add2(tc::f2(mua, mub), r2);
-            uint32_t vw = tc::pack_f16x2(tc::f2lo(v2), tc::f2hi(v2));
-            if (!valid1) vw &= 0x0000FFFFu;
-            if (!valid0) vw = 0u;
-            *(uint32_t *)(blk + tc::sw128_offset(c, kin)) = vw;
-          }
-        }
-      }
-      tc::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&bars.v_full[s]);
-      if (++tile_in_chunk == ch.tiles) { tile_in_chunk = 0; t++; }
-    }
+    producer<true>(p, sm, bars, &abort_flag, tc::smem_u32(code_lut), h, q0, tid - 32 * kVWarp0, lane);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -504,7 +606,7 @@ cudaError_t launch_attend(const qwm_config &cfg, const uint16_t *q, int64_t nq, 
     a.n = c.n_tokens; a.rank = c.rank_eff; a.tiles = (int)((c.n_tokens + BN - 1) / BN);
     a.k_codes = c.k_codes; a.v_codes = c.v_codes; a.k_idx = c.k_idx; a.v_idx = c.v_idx;
     a.k_scale = c.k_scale; a.k_min = c.k_min; a.v_scale = c.v_scale; a.v_min = c.v_min;
-    a.cent_k = c.cent_k; a.cent_v = c.cent_v; a.c_scale = c.c_scale; a.u_r = c.u_r; a.c = c.c;
+    a.cent_k16 = c.cent_k16; a.cent_v16 = c.cent_v16; a.c_scale = c.c_scale; a.u_r = c.u_r; a.c = c.c;
     tiles += a.tiles;
   }
   p.n_chunks = used;

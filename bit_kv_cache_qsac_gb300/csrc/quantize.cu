@@ -14,21 +14,32 @@
 //           sC = fp16 round-up of max|C|/127.
 //
 // Distance GEMM.  d_Q(k, mu_j) = sum_c w_c k_c^2 - 2 k.(w . mu_j) + sum_c w_c mu_jc^2; the first
-// term is the same for every j, so the ranking uses score_j = nw_j - 2 k.b_j with b_j = w . mu_j
-// split as b = hi + lo (bf16 each): two bf16 MMAs per 128-token tile (M = 128, N = C, K = 128)
-// accumulate k.b_j in TMEM.  Values use b_j = mu_j (exact in bf16, one MMA) and nw_j = |mu_j|^2.
-// The approximate scores pick the candidates; whenever the gap at the candidate boundary (Keys:
-// between the M-th and (M+1)-th score; Values: between the best and the runner-up) is not
-// larger than twice an error bound of the scores, the token falls back to exact fp32 distances
-// against every centroid, so the candidate set is the exact one.  The range score S, the INT2
-// codes and the PSAC coefficients are computed exactly in fp32 with explicitly rounded
-// intrinsics, so that indices and codes match a plain IEEE implementation bit for bit.
+// term is the same for every j, so the ranking uses T_j = k.b_j - nw_j / 2 (the largest T is the
+// nearest centroid) with b_j = w . mu_j and nw_j = sum_c w_c mu_jc^2.  The tensor cores produce T
+// directly in TMEM: two bf16 MMAs against b = hi + lo (each bf16; Values use b = mu, exact, one
+// MMA) and a third, K = 16 MMA of a constant [1 1 0 ...] row block against [-nw/2 hi, lo, 0 ...].
+// The approximate T pick the candidates: with |T_approx - T| <= delta, every centroid outside
+// the window T_approx >= T_M - 2 delta (T_M = the M-th largest) is outside the exact top-M.  When
+// the window holds exactly M centroids (almost always) it is the exact candidate set; otherwise
+// the warp computes exact fp32 distances for the window and keeps the M nearest (lower index on
+// ties).  The range score S, the INT2 codes and the PSAC coefficients are exact fp32 with
+// explicitly rounded intrinsics, so indices and codes match a plain IEEE implementation bit for
+// bit.
 //
 // One CTA = one head x a contiguous range of 128-token tiles; 320 threads:
 //   warp 0     TMA producer: K (or V) tiles as two [128][64] bf16 blocks, 128-byte swizzle, 2 stages
 //   warp 1     TMEM owner and MMA issuer: tile g into TMEM buffer g % 2
-//   warps 2-9  two epilogue warpgroups; group e owns the tiles g with g % 2 == e, thread = token
+//   warps 2-9  two epilogue warpgroups; group e owns the tiles g with g % 2 == e.  Per tile:
+//     (1) thread = token: the M+1 largest T from TMEM (branch-free insertion network), then the
+//         window as a bit mask per token in shared memory; TMEM is released;
+//     (2) warp-cooperative (lane = 4 channels), for the rare tokens whose window holds more than
+//         M centroids: exact distances to the window's centroids, the M nearest kept;
+//     (3) Keys, warp-cooperative: S of every (token, candidate) pair, with the centroid row read
+//         coalesced from global memory and the group ranges reduced across half-warps;
+//     (4) thread = token: INT2 codes of the chosen centroid's residual, PSAC coefficients.
 // All waits are bounded; on expiry the kernel records QWM_ERR_DEVICE_TIMEOUT and stops.
+#include <cuda_fp16.h>
+
 #include "qwm_internal.cuh"
 #include "tc.cuh"
 
@@ -38,22 +49,23 @@ constexpr int D = QWM_D;
 constexpr int TILE = 128;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
-constexpr int MAXM = QWM_MAX_TOPM + 1;
 constexpr uint64_t kWaitNs = 1000000000ull;
-// error bound of an approximate score: |err| <= kRel |k| max_j |b_j| + kRelN max_j |nw_j|
-constexpr float kRel = 1.0f / 16384.0f;   // 2^-14
-constexpr float kRelN = 1.0f / 65536.0f;  // 2^-16
+// error bound of an approximate T: |err| <= kRel |k| max_j |b_j| + kRelN max_j |nw_j|
+constexpr float kRel = 1.0f / 32768.0f;    // 2^-15
+constexpr float kRelN = 1.0f / 131072.0f;  // 2^-17
 
 struct QSmem {
-  int bh, bl, x, nw, wv, U, total;
+  int bh, bl, bn, an, x, msk, wv, U, total;
   __host__ __device__ QSmem(int C, bool key) {
     bh = 0;                             // 2 blocks of [C][64] bf16: hi of b (or mu for Values)
     bl = bh + 2 * C * 128;              // lo of b (Keys only)
-    x = bl + (key ? 2 * C * 128 : 0);   // 2 stages x 2 blocks of [128][64]
-    nw = x + 2 * 2 * TILE * 128;        // nw[C], then |b_j|[C]
-    wv = nw + 8 * C;                    // w[D]
-    U = wv + 4 * D;                     // U_r as fp32 [D][16], zero past the rank
-    total = U + 4 * D * 16;
+    bn = bl + (key ? 2 * C * 128 : 0);  // [C][16] bf16 no-swizzle: -nw/2 as hi, lo, then zeros
+    an = bn + C * 32;                   // [128][16] bf16 no-swizzle: 1, 1, then zeros
+    x = an + TILE * 32;                 // 2 stages x 2 blocks of [128][64]
+    msk = x + 2 * 2 * TILE * 128;       // window masks: [8 warps][C/32 words][32 tokens]
+    wv = msk + kEpiWarps * (C / 32) * 32 * 4;  // w[D]
+    U = wv + 4 * D;                     // U_r as fp32 [D][16], zero past the rank (Keys)
+    total = U + (key ? 4 * D * 16 : 0);
   }
 };
 
@@ -82,24 +94,9 @@ __device__ __forceinline__ void bf16x8(const uint4 v, float (&f)[8]) {
   }
 }
 
-// Insert (v, j) into the ascending list tv[0..m] of the m+1 smallest seen so far (thr == tv[m]).
-// Indices arrive in increasing order, so the strict comparison keeps the lower index first on
-// ties.  Only compile-time indices are used, so the lists stay in registers.
-__device__ __forceinline__ void topk_insert(float (&tv)[MAXM], int (&ti)[MAXM], float &thr, int m, float v, int j) {
-  if (!(v < thr)) return;
-  bool placed = false;
-#pragma unroll
-  for (int k = MAXM - 1; k >= 1; k--) {
-    if (k <= m && !placed) {
-      if (tv[k - 1] > v) { tv[k] = tv[k - 1]; ti[k] = ti[k - 1]; }
-      else { tv[k] = v; ti[k] = j; placed = true; }
-    }
-  }
-  if (!placed) { tv[0] = v; ti[0] = j; }
-  thr = tv[0];
-#pragma unroll
-  for (int k = 1; k < MAXM; k++)
-    if (k == m) thr = tv[k];
+// byte offset of (row, column k) in a [rows][16] bf16 K-major operand without swizzle
+__host__ __device__ constexpr uint32_t noswz16(uint32_t row, uint32_t k) {
+  return (row >> 3) * 256u + (k >> 3) * 128u + (row & 7u) * 16u + (k & 7u) * 2u;
 }
 
 // INT2 parameters of one group from its fp32 residual min and max.
@@ -123,8 +120,28 @@ __device__ __forceinline__ uint32_t int2_code(float r, float m, float s, float i
   return (uint32_t)qf;
 }
 
+// Byte offset, inside a [128][64] x 2 swizzled tile, of this lane's 4 channels (4 lane .. 4 lane + 3)
+// of token row t.
+__device__ __forceinline__ uint32_t lane4_offset(int t, int lane) {
+  return (uint32_t)(lane >> 4) * TILE * 128u + (uint32_t)t * 128u +
+         ((((uint32_t)(lane & 15) >> 1) ^ ((uint32_t)t & 7u)) << 4) + 8u * (uint32_t)(lane & 1);
+}
+__device__ __forceinline__ void unpack4(uint2 v, float (&f)[4]) {
+  f[0] = __uint_as_float(v.x << 16);
+  f[1] = __uint_as_float(v.x & 0xFFFF0000u);
+  f[2] = __uint_as_float(v.y << 16);
+  f[3] = __uint_as_float(v.y & 0xFFFF0000u);
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
 // KEY: Keys (QSAC + PSAC) or Values (nearest centroid).  RMAX: 8 or 16, bound on the PSAC rank.
-template <bool KEY, int RMAX>
+// MP1: length of the largest-T list, top_m + 1 (exact for the common M; QWM_MAX_TOPM + 1 covers
+// every M, with the list's tail unused).
+template <bool KEY, int RMAX, int MP1>
 __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constant__ TensorMap128 tmap,
                                                              const QParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -134,6 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
   __shared__ int abort_flag;
   __shared__ float Wg[2], bmax_sh, nwmax_sh;
   const int C = p.C, M = KEY ? p.top_m : 1, R = KEY ? p.rank : 0;
+  const int NW = C / 32;  // mask words per token
   const QSmem L(C, KEY);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.y, cta = blockIdx.x;
@@ -142,8 +160,6 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
   const int64_t tile0 = (int64_t)cta * per;
   const int64_t tile1 = tile0 + per < tiles ? tile0 + per : tiles;
   const int nt = tile1 > tile0 ? (int)(tile1 - tile0) : 0;
-  float *nw = (float *)(sm + L.nw);
-  float *bn = nw + C;
   float *wv = (float *)(sm + L.wv);
   float *Us = (float *)(sm + L.U);
   volatile int *abort_v = &abort_flag;
@@ -158,19 +174,28 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
     }
     tc::mbar_init(&drain, 1);
     abort_flag = 0;
+    bmax_sh = 0.f;
+    nwmax_sh = 0.f;
     tc::fence_mbar_init();
   }
   if (warp == 1) {
     tc::tmem_alloc(&tmem_base_sh, 512);
     tc::tmem_relinquish();
   }
-  // ---- per-head constants: weights, basis, distance operand (b = w . mu as hi/lo), nw, |b| ----
+  // ---- per-head constants: weights, basis, distance operands ----
   for (int c = tid; c < D; c += kThreads) wv[c] = (KEY && p.w) ? p.w[(int64_t)h * D + c] : 1.0f;
-  for (int e = tid; e < D * 16; e += kThreads) {
-    const int c = e / 16, k = e % 16;
-    Us[e] = (k < R) ? bf16_to_f32(p.u_r[((int64_t)h * D + c) * R + k]) : 0.f;
+  if (KEY) {
+    for (int e = tid; e < D * 16; e += kThreads) {
+      const int c = e / 16, k = e % 16;
+      Us[e] = (k < R) ? bf16_to_f32(p.u_r[((int64_t)h * D + c) * R + k]) : 0.f;
+    }
+  }
+  for (int e = tid; e < TILE * 8; e += kThreads) {  // constant A block of the nw MMA
+    const int row = e >> 3, kw = e & 7;           // 8 words of 2 bf16 per row
+    *(uint32_t *)(sm + L.an + noswz16(row, 2 * kw)) = kw == 0 ? 0x3F803F80u : 0u;
   }
   __syncthreads();
+  // b = w . mu split into bf16 hi + lo (Keys) or mu itself (Values), 128-byte swizzled K-major
   for (int e = tid; e < C * (D / 8); e += kThreads) {
     const int j = e / (D / 8), ci = e % (D / 8);
     float mu[8];
@@ -188,28 +213,39 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
     *(uint4 *)(sm + L.bh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
     if (KEY) *(uint4 *)(sm + L.bl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
   }
-  for (int j = tid; j < C; j += kThreads) {
+  // nw_j and |b_j| (one warp per centroid, lane = 4 channels), the nw operand, the maxima
+  for (int j = warp; j < C; j += kThreads / 32) {
+    float mu[4];
+    unpack4(*(const uint2 *)(cent + (int64_t)j * D + 4 * lane), mu);
     float s = 0.f, bb = 0.f;
-    for (int ci = 0; ci < D / 8; ci++) {
-      float mu[8];
-      bf16x8(*(const uint4 *)(cent + (int64_t)j * D + 8 * ci), mu);
 #pragma unroll
-      for (int u = 0; u < 8; u++) {
-        const float wm = __fmul_rn(wv[8 * ci + u], mu[u]);
-        s = fmaf(wm, mu[u], s);
-        bb = fmaf(wm, wm, bb);
-      }
+    for (int u = 0; u < 4; u++) {
+      const float wm = __fmul_rn(wv[4 * lane + u], mu[u]);
+      s = fmaf(wm, mu[u], s);
+      bb = fmaf(wm, wm, bb);
     }
-    nw[j] = s;
-    bn[j] = sqrtf(bb);
+    s = warp_sum(s);
+    bb = warp_sum(bb);
+    if (lane < 8) {  // row j of the nw operand: [-nw/2 hi, lo, 0 ...]
+      uint32_t wd = 0u;
+      if (lane == 0) {
+        const float t = -0.5f * s, th = __bfloat162float(__float2bfloat16_rn(t));
+        wd = (uint32_t)f32_to_bf16_rn(th) | ((uint32_t)f32_to_bf16_rn(t - th) << 16);
+      }
+      *(uint32_t *)(sm + L.bn + noswz16(j, 2 * lane)) = wd;
+    }
+    if (lane == 0) {
+      atomicMax((int *)&bmax_sh, __float_as_int(sqrtf(bb)));  // non-negative floats order as ints
+      atomicMax((int *)&nwmax_sh, __float_as_int(fabsf(s)));
+    }
   }
   __syncthreads();
   if (tid == 0) {
-    float a = 0.f, b = 0.f, bm = 0.f, nm = 0.f;
+    float a = 0.f, b = 0.f;
     for (int c = 0; c < 64; c++) a += wv[c];
     for (int c = 64; c < 128; c++) b += wv[c];
-    for (int j = 0; j < C; j++) { bm = fmaxf(bm, bn[j]); nm = fmaxf(nm, fabsf(nw[j])); }
-    Wg[0] = a; Wg[1] = b; bmax_sh = bm; nwmax_sh = nm;
+    Wg[0] = a;
+    Wg[1] = b;
   }
   tc::fence_proxy_async_smem();
   tc::fence_before_sync();
@@ -235,6 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
     if (lane == 0) {
       const uint32_t idesc = tc::idesc_bf16_f32(TILE, C);
       const uint32_t sx = tc::smem_u32(sm + L.x), sbh = tc::smem_u32(sm + L.bh), sbl = tc::smem_u32(sm + L.bl);
+      const uint32_t sbn = tc::smem_u32(sm + L.bn), san = tc::smem_u32(sm + L.an);
       for (int g = 0; g < nt && !*abort_v; g++) {
         const int s = g & 1;
         if (!tc::mbar_wait(&x_full[s], (g >> 1) & 1, kWaitNs) ||
@@ -244,10 +281,11 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
         }
         tc::fence_after_sync();
         const uint32_t d = tmem + 256u * s;
+        tc::mma_ss(d, tc::desc_noswz(san, 128, 256), tc::desc_noswz(sbn, 128, 256), idesc, 0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; kk++) {
           const uint32_t xo = sx + s * 2 * TILE * 128 + (kk / 4) * TILE * 128 + 32 * (kk % 4);
-          tc::mma_ss(d, tc::desc_sw128(xo), tc::desc_sw128(sbh + (kk / 4) * C * 128 + 32 * (kk % 4)), idesc, kk > 0);
+          tc::mma_ss(d, tc::desc_sw128(xo), tc::desc_sw128(sbh + (kk / 4) * C * 128 + 32 * (kk % 4)), idesc, 1);
         }
         if (KEY) {
 #pragma unroll
@@ -262,11 +300,15 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
       if (!tc::mbar_wait(&drain, 0, kWaitNs)) *abort_v = 1;
     }
   } else {
-    // ======================= epilogue: thread = token =======================
-    const int e = (warp - 2) >> 2, sub = warp & 3, row = 32 * sub + lane;
+    // ======================= epilogue =======================
+    const int ew = warp - 2, e = ew >> 2, sub = warp & 3, row = 32 * sub + lane;
     const uint32_t lane_addr = (uint32_t)(32 * sub) << 16;
     const float W0 = Wg[0], W1 = Wg[1];
-    const float knorm_coef = kRel * bmax_sh, nw_err = kRelN * nwmax_sh;
+    const float dcoef = kRel * bmax_sh, dconst = kRelN * nwmax_sh;
+    uint32_t *msk = (uint32_t *)(sm + L.msk) + ew * NW * 32;  // [word][token] for this warp
+    float wl[4];  // this lane's 4 channel weights (cooperative phases)
+#pragma unroll
+    for (int u = 0; u < 4; u++) wl[u] = wv[4 * lane + u];
     for (int g = e; g < nt; g += 2) {
       const int s = g & 1;
       if (!tc::mbar_wait(&t_full[s], (g >> 1) & 1, kWaitNs) || !tc::mbar_wait(&x_full[s], (g >> 1) & 1, kWaitNs))
@@ -274,80 +316,170 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
       if (*abort_v) break;
       tc::fence_after_sync();
       const unsigned char *xt = sm + L.x + s * 2 * TILE * 128;
-      // the token's values (bf16, exact in fp32) are read back from the swizzled tile
-      auto xchunk = [&](int ci, float (&f)[8]) {
-        bf16x8(*(const uint4 *)(xt + (ci / 8) * TILE * 128 + tc::sw128_offset(row, 8 * (ci % 8))), f);
-      };
-      // ---- approximate scores -> the M+1 smallest ----
-      float tv[MAXM], thr = INFINITY;
-      int ti[MAXM];
+      const uint32_t xts = tc::smem_u32(xt);
+      const int64_t tok0 = (tile0 + g) * TILE + 32 * sub;  // token of lane 0 of this warp
+      const int64_t tok = tok0 + lane;
+      const bool valid = tok < p.n;
+      // ---- (1) the M+1 largest T, then the window mask (thread = token) ----
+      float kn2 = 0.f;
 #pragma unroll
-      for (int k = 0; k < MAXM; k++) { tv[k] = INFINITY; ti[k] = C; }
+      for (int ci = 0; ci < D / 8; ci++) {
+        float f[8];
+        bf16x8(tc::lds128(xts + (ci / 8) * TILE * 128 + tc::sw128_offset(row, 8 * (ci % 8))), f);
+#pragma unroll
+        for (int u = 0; u < 8; u++) kn2 = fmaf(f[u], f[u], kn2);
+      }
+      const float delta2 = 2.f * (dcoef * sqrtf(kn2) + dconst);
+      float tv[MP1];
+#pragma unroll
+      for (int k = 0; k < MP1; k++) tv[k] = -INFINITY;
       uint32_t r[32];
+#pragma unroll 1
       for (int c0 = 0; c0 < C; c0 += 32) {
-        tc::tmem_ld32(tmem + lane_addr + 256u * s + c0, r);
+        tc::tmem_ld16(tmem + lane_addr + 256u * s + c0, r);
+        tc::tmem_ld16(tmem + lane_addr + 256u * s + c0 + 16, r + 16);
         tc::tmem_ld_wait();
 #pragma unroll
-        for (int k = 0; k < 32; k++)
-          topk_insert(tv, ti, thr, M, fmaf(-2.f, __uint_as_float(r[k]), nw[c0 + k]), c0 + k);
+        for (int k = 0; k < 32; k++) {
+          const float v = __uint_as_float(r[k]);
+          // descending list: new tv[i] = median(tv[i-1], tv[i], v), updated from the bottom up
+#pragma unroll
+          for (int i = MP1 - 1; i >= 1; i--) tv[i] = fminf(tv[i - 1], fmaxf(tv[i], v));
+          tv[0] = fmaxf(tv[0], v);
+        }
+      }
+      float tM = tv[0], tM1 = tv[0];  // the M-th and (M+1)-th largest (compile-time indexing)
+#pragma unroll
+      for (int k = 1; k < MP1; k++) {
+        if (k == M - 1) tM = tv[k];
+        if (k == M) tM1 = tv[k];
+      }
+      const float thr = tM - delta2;
+      const bool amb = valid && (M < C) && !(tM1 < thr);
+#pragma unroll 1
+      for (int c0 = 0; c0 < C; c0 += 32) {
+        tc::tmem_ld16(tmem + lane_addr + 256u * s + c0, r);
+        tc::tmem_ld16(tmem + lane_addr + 256u * s + c0 + 16, r + 16);
+        tc::tmem_ld_wait();
+        uint32_t word = 0u;
+#pragma unroll
+        for (int k = 0; k < 32; k++) word |= (__uint_as_float(r[k]) >= thr ? 1u : 0u) << k;
+        msk[(c0 >> 5) * 32 + lane] = valid ? word : 0u;
       }
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&t_empty[s]);
-      const int64_t tok = (tile0 + g) * TILE + row;
-      const bool valid = tok < p.n;
-      const int64_t grow = (int64_t)h * p.n + tok;
-      // ---- exact fallback when the candidate boundary lies within the error bound ----
-      float kn2 = 0.f;
-      for (int ci = 0; ci < D / 8; ci++) {
-        float f[8];
-        xchunk(ci, f);
+      // ---- (2) exact candidate set for tokens whose window holds more than M centroids ----
+      uint32_t ambs = __ballot_sync(0xffffffffu, amb);
+      while (ambs) {
+        const int t = __ffs(ambs) - 1;
+        ambs &= ambs - 1;
+        float xf[4];
+        unpack4(*(const uint2 *)(xt + lane4_offset(32 * sub + t, lane)), xf);
+        float ev[17];
+        int ei[17];
 #pragma unroll
-        for (int u = 0; u < 8; u++) kn2 = fmaf(f[u], f[u], kn2);
-      }
-      const float delta = knorm_coef * sqrtf(kn2) + nw_err;
-      float vM = tv[0], vM1 = tv[0];  // the M-th and (M+1)-th smallest (compile-time indexing)
+        for (int k = 0; k < 17; k++) { ev[k] = INFINITY; ei[k] = C; }
+        for (int wi = 0; wi < NW; wi++) {
+          uint32_t m = msk[wi * 32 + t];
+          while (m) {
+            const int j = 32 * wi + __ffs(m) - 1;
+            m &= m - 1;
+            float mu[4];
+            unpack4(*(const uint2 *)(cent + (int64_t)j * D + 4 * lane), mu);
+            float dq = 0.f;
 #pragma unroll
-      for (int k = 1; k < MAXM; k++) {
-        if (k == M - 1) vM = tv[k];
-        if (k == M) vM1 = tv[k];
-      }
-      const bool amb = valid && (M < C) && !(vM1 - vM > 2.f * delta);
-      if (amb) {
-        thr = INFINITY;
+            for (int u = 0; u < 4; u++) {
+              const float df = __fsub_rn(xf[u], mu[u]);
+              dq = __fmaf_rn(wl[u], __fmul_rn(df, df), dq);
+            }
+            dq = warp_sum(dq);  // identical on every lane
+            // insert (dq, j) into the ascending exact list (j increasing: a strict comparison
+            // keeps the lower index first on ties)
+            if (dq < ev[16]) {
+              float cv = dq;
+              int cj = j;
 #pragma unroll
-        for (int k = 0; k < MAXM; k++) { tv[k] = INFINITY; ti[k] = C; }
-        for (int j = 0; j < C; j++) {
-          float dq = 0.f;
-          for (int ci = 0; ci < D / 8; ci++) {
-            float f[8], mu[8];
-            xchunk(ci, f);
-            bf16x8(*(const uint4 *)(cent + (int64_t)j * D + 8 * ci), mu);
-#pragma unroll
-            for (int u = 0; u < 8; u++) {
-              const float df = __fsub_rn(f[u], mu[u]);
-              dq = __fmaf_rn(wv[8 * ci + u], __fmul_rn(df, df), dq);
+              for (int k = 0; k < 17; k++) {
+                const bool sw = cv < ev[k];
+                const float tvv = ev[k];
+                const int tj = ei[k];
+                ev[k] = sw ? cv : ev[k];
+                ei[k] = sw ? cj : ei[k];
+                cv = sw ? tvv : cv;
+                cj = sw ? tj : cj;
+              }
             }
           }
-          topk_insert(tv, ti, thr, M, dq, j);
+        }
+        __syncwarp();
+        // the token's candidate mask := the M nearest
+        if (lane < NW) {
+          uint32_t word = 0u;
+#pragma unroll
+          for (int k = 0; k < 17; k++)
+            if (k < M && (ei[k] >> 5) == lane) word |= 1u << (ei[k] & 31);
+          msk[lane * 32 + t] = word;
+        }
+        __syncwarp();
+      }
+      // ---- (3) Keys: range score S of every candidate (warp-cooperative), best per token ----
+      int best = 0;
+      float best_S = 0.f;
+      if (KEY) {
+        const int tmax = (int)((p.n - tok0) < 32 ? (p.n - tok0) : 32);
+        for (int t = 0; t < tmax; t++) {
+          float xf[4];
+          unpack4(*(const uint2 *)(xt + lane4_offset(32 * sub + t, lane)), xf);
+          float bS = INFINITY;
+          int bj = C, m_i = 0;
+          for (int wi = 0; wi < NW; wi++) {
+            uint32_t m = msk[wi * 32 + t];
+            while (m) {
+              const int j = 32 * wi + __ffs(m) - 1;
+              m &= m - 1;
+              float mu[4];
+              unpack4(*(const uint2 *)(cent + (int64_t)j * D + 4 * lane), mu);
+              float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+              for (int u = 0; u < 4; u++) {
+                const float rr = __fsub_rn(xf[u], mu[u]);
+                mn = fminf(mn, rr);
+                mx = fmaxf(mx, rr);
+              }
+#pragma unroll
+              for (int o = 8; o > 0; o >>= 1) {  // within each half-warp (= one group)
+                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+              }
+              const float Rg = __fsub_rn(mx, mn);
+              const float Ro = __shfl_xor_sync(0xffffffffu, Rg, 16);
+              const float R0 = lane < 16 ? Rg : Ro, R1 = lane < 16 ? Ro : Rg;
+              const float S = __fadd_rn(__fmul_rn(W0, __fmul_rn(R0, R0)), __fmul_rn(W1, __fmul_rn(R1, R1)));
+              if (S < bS) { bS = S; bj = j; }
+              if (p.dbg_cand && lane == 0 && m_i < M) p.dbg_cand[((int64_t)h * p.n + tok0 + t) * M + m_i] = j;
+              m_i++;
+            }
+          }
+          if (lane == t) { best = bj; best_S = bS; }
+        }
+      } else {
+        for (int wi = 0; wi < NW; wi++) {
+          const uint32_t m = msk[wi * 32 + lane];
+          if (m) best = 32 * wi + __ffs(m) - 1;
         }
       }
-      // ---- QSAC: exact range score of each candidate (Values: the single nearest) ----
-      int best = 0;
-      float best_S = INFINITY, bmn0 = 0.f, bmx0 = 0.f, bmn1 = 0.f, bmx1 = 0.f;
-#pragma unroll 1
-      for (int m = 0; m < MAXM - 1; m++) {
-        if (m >= M) break;
-        int j = ti[0];
-#pragma unroll
-        for (int k = 1; k < MAXM; k++)
-          if (k == m) j = ti[k];
-        if (j >= C) j = 0;
+      if (best >= C) best = 0;
+      // ---- (4) INT2 codes of the chosen centroid's residual; PSAC coefficients (thread = token) ----
+      if (valid) {
+        const int64_t grow = (int64_t)h * p.n + tok;
+        const uint16_t *mub = cent + (int64_t)best * D;
         float mn0 = INFINITY, mx0 = -INFINITY, mn1 = INFINITY, mx1 = -INFINITY;
+#pragma unroll
         for (int ci = 0; ci < D / 8; ci++) {
           float f[8], mu[8];
-          xchunk(ci, f);
-          bf16x8(*(const uint4 *)(cent + (int64_t)j * D + 8 * ci), mu);
+          bf16x8(tc::lds128(xts + (ci / 8) * TILE * 128 + tc::sw128_offset(row, 8 * (ci % 8))), f);
+          bf16x8(*(const uint4 *)(mub + 8 * ci), mu);
 #pragma unroll
           for (int u = 0; u < 8; u++) {
             const float rr = __fsub_rn(f[u], mu[u]);
@@ -355,48 +487,36 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
             else { mn1 = fminf(mn1, rr); mx1 = fmaxf(mx1, rr); }
           }
         }
-        float S = 0.f;
-        if (KEY) {
-          const float R0 = __fsub_rn(mx0, mn0), R1 = __fsub_rn(mx1, mn1);
-          S = __fadd_rn(__fmul_rn(W0, __fmul_rn(R0, R0)), __fmul_rn(W1, __fmul_rn(R1, R1)));
-          if (p.dbg_cand && valid) p.dbg_cand[grow * M + m] = j;
-        }
-        if (m == 0 || S < best_S || (S == best_S && j < best)) {
-          best_S = S; best = j; bmn0 = mn0; bmx0 = mx0; bmn1 = mn1; bmx1 = mx1;
-        }
-      }
-      // ---- INT2 codes of the chosen centroid's residual; PSAC coefficients ----
-      float m0, s0, i0, m1, s1, i1;
-      uint16_t mb0, sb0, mb1, sb1;
-      int2_params(bmn0, bmx0, m0, s0, i0, mb0, sb0, p.status);
-      int2_params(bmn1, bmx1, m1, s1, i1, mb1, sb1, p.status);
-      uint32_t packed[8];
-      float Cv[RMAX];
+        float m0, s0, i0, m1, s1, i1;
+        uint16_t mb0, sb0, mb1, sb1;
+        int2_params(mn0, mx0, m0, s0, i0, mb0, sb0, p.status);
+        int2_params(mn1, mx1, m1, s1, i1, mb1, sb1, p.status);
+        uint32_t packed[8];
+        float Cv[RMAX];
 #pragma unroll
-      for (int k = 0; k < RMAX; k++) Cv[k] = 0.f;
+        for (int k = 0; k < RMAX; k++) Cv[k] = 0.f;
 #pragma unroll
-      for (int ci = 0; ci < D / 8; ci++) {
-        float f[8], mu[8];
-        xchunk(ci, f);
-        bf16x8(*(const uint4 *)(cent + (int64_t)best * D + 8 * ci), mu);
-        const bool g1 = ci >= 8;
-        const float mm = g1 ? m1 : m0, ss = g1 ? s1 : s0, ii = g1 ? i1 : i0;
-        uint32_t bits = 0;
+        for (int ci = 0; ci < D / 8; ci++) {
+          float f[8], mu[8];
+          bf16x8(tc::lds128(xts + (ci / 8) * TILE * 128 + tc::sw128_offset(row, 8 * (ci % 8))), f);
+          bf16x8(*(const uint4 *)(mub + 8 * ci), mu);
+          const bool g1 = ci >= 8;
+          const float mm = g1 ? m1 : m0, ss = g1 ? s1 : s0, ii = g1 ? i1 : i0;
+          uint32_t bits = 0;
 #pragma unroll
-        for (int u = 0; u < 8; u++) {
-          const uint32_t q = int2_code(__fsub_rn(f[u], mu[u]), mm, ss, ii);
-          bits |= q << (2 * u);
-          if (KEY && R > 0) {
-            const float ev = __fsub_rn(f[u], __fadd_rn(mu[u], __fmaf_rn(ss, (float)q, mm)));
-            const float *Uc = Us + (8 * ci + u) * 16;
+          for (int u = 0; u < 8; u++) {
+            const uint32_t q = int2_code(__fsub_rn(f[u], mu[u]), mm, ss, ii);
+            bits |= q << (2 * u);
+            if (KEY && R > 0) {
+              const float ev = __fsub_rn(f[u], __fadd_rn(mu[u], __fmaf_rn(ss, (float)q, mm)));
+              const float *Uc = Us + (8 * ci + u) * 16;
 #pragma unroll
-            for (int k = 0; k < RMAX; k++) Cv[k] = fmaf(ev, Uc[k], Cv[k]);
+              for (int k = 0; k < RMAX; k++) Cv[k] = fmaf(ev, Uc[k], Cv[k]);
+            }
           }
+          if (ci & 1) packed[ci >> 1] |= bits << 16;
+          else packed[ci >> 1] = bits;
         }
-        if (ci & 1) packed[ci >> 1] |= bits << 16;
-        else packed[ci >> 1] = bits;
-      }
-      if (valid) {
         uint4 *cdst = (uint4 *)(p.codes + grow * (D / 4));
         cdst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
         cdst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
@@ -440,11 +560,35 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
   }
 }
 
-template <bool KEY, int RMAX>
+// fp16 copies of both codebooks for the attention kernel (exact for bf16 values of normal fp16
+// magnitude; a centroid beyond the fp16 range records QWM_ERR_RANGE).
+__global__ void codebook_f16_kernel(const uint16_t *__restrict__ ck, const uint16_t *__restrict__ cv, uint16_t *ok,
+                                    uint16_t *ov, int64_t n8, int32_t *status) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < 2 * n8; i += (int64_t)gridDim.x * blockDim.x) {
+    const bool key = i < n8;
+    const int64_t e = key ? i : i - n8;
+    const uint4 v = ((const uint4 *)(key ? ck : cv))[e];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+    bool bad = false;
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const float lo = __uint_as_float(w[u] << 16), hi = __uint_as_float(w[u] & 0xFFFF0000u);
+      const __half hl = __float2half_rn(lo), hh = __float2half_rn(hi);
+      bad |= (__hisinf(hl) != 0 && !isinf(lo)) || (__hisinf(hh) != 0 && !isinf(hi));
+      o[u] = (uint32_t)__half_as_ushort(hl) | ((uint32_t)__half_as_ushort(hh) << 16);
+    }
+    if (bad) qwm_dev_error(status, QWM_ERR_RANGE);
+    ((uint4 *)(key ? ok : ov))[e] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+template <bool KEY, int RMAX, int MP1>
 cudaError_t launch_one(const TensorMap128 &tmap, const QParams &p, int H, int smem, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(quant_kernel<KEY, RMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e =
+      cudaFuncSetAttribute(quant_kernel<KEY, RMAX, MP1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  quant_kernel<KEY, RMAX><<<dim3(p.G, H), kThreads, smem, st>>>(tmap, p);
+  quant_kernel<KEY, RMAX, MP1><<<dim3(p.G, H), kThreads, smem, st>>>(tmap, p);
   return cudaGetLastError();
 }
 
@@ -455,9 +599,16 @@ cudaError_t launch_quantize(const qwm_config &cfg, const uint16_t *k, const uint
                             int num_sms, cudaStream_t st) {
   const int H = cfg.heads, C = cfg.n_centroids;
   const int64_t tiles = (n + TILE - 1) / TILE;
-  int G = (num_sms + H - 1) / H;
+  // one CTA per SM at most (each holds ~220 KB of shared memory): a single wave
+  int G = num_sms / H;
   if (G > tiles) G = (int)tiles;
   if (G < 1) G = 1;
+  {
+    const int64_t n8 = (int64_t)H * C * QWM_D / 8;
+    codebook_f16_kernel<<<num_sms, 256, 0, st>>>(out.cent_k, out.cent_v, out.cent_k16, out.cent_v16, n8, status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   for (int pass = 0; pass < 2; pass++) {
     const bool key = pass == 0;
     TensorMap128 tmap;
@@ -475,9 +626,11 @@ cudaError_t launch_quantize(const qwm_config &cfg, const uint16_t *k, const uint
     p.status = status;
     const int smem = QSmem(C, key).total + 1024;
     cudaError_t e;
-    if (!key) e = launch_one<false, 8>(tmap, p, H, smem, st);
-    else if (p.rank <= 8) e = launch_one<true, 8>(tmap, p, H, smem, st);
-    else e = launch_one<true, 16>(tmap, p, H, smem, st);
+    if (!key) e = launch_one<false, 8, 2>(tmap, p, H, smem, st);
+    else if (p.rank <= 8 && p.top_m == 4) e = launch_one<true, 8, 5>(tmap, p, H, smem, st);
+    else if (p.rank <= 8) e = launch_one<true, 8, QWM_MAX_TOPM + 1>(tmap, p, H, smem, st);
+    else if (p.top_m == 4) e = launch_one<true, 16, 5>(tmap, p, H, smem, st);
+    else e = launch_one<true, 16, QWM_MAX_TOPM + 1>(tmap, p, H, smem, st);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

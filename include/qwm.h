@@ -98,6 +98,11 @@ typedef struct {
   int8_t *c;             /* [H][N][r] PSAC coefficients (unused when rank_eff == 0) */
   uint16_t *c_scale;     /* fp16 [H][N]: C_hat = c_scale * c */
   uint16_t *u_r;         /* bf16 [H][d][r]: the basis C was built with (snapshot per chunk) */
+  uint16_t *cent_k16;    /* fp16 [H][C][d]: the Key codebook converted to fp16 by qwm_quantize_kv;
+                            qwm_attend reads it as a tensor-core operand.  fp16 holds every bf16
+                            value of magnitude in [2^-14, 65504] exactly; a centroid beyond 65504
+                            records QWM_ERR_RANGE. */
+  uint16_t *cent_v16;    /* fp16 [H][C][d]: the Value codebook, likewise */
 } qwm_chunk;
 
 /* Optional stage outputs of qwm_quantize_kv for parity checks (NULL members are skipped). */
@@ -149,7 +154,8 @@ QWM_API qwm_status qwm_fit_centroids(qwm_ctx *ctx, const uint16_t *x, int64_t n,
  *   w     fp32 [H][d]      channel weights, or NULL for uniform weights (cold start)
  *   u_r   bf16 [H][d][r]   PSAC basis, or NULL to switch PSAC off (cold start)
  *   out   chunk to fill: out->n_tokens must equal n, out->cent_k / out->cent_v must hold the
- *         chunk's codebooks; the codes, indices, scales and (when u_r) c, c_scale are written,
+ *         chunk's codebooks; the codes, indices, scales, the fp16 codebook copies
+ *         out->cent_k16 / out->cent_v16 and (when u_r) c, c_scale are written,
  *         out->rank_eff is set on the host (r or 0) and, when u_r is given, out->u_r must
  *         point at a caller-owned copy of the basis (the library does not copy it).
  *   dbg   optional stage outputs, or NULL.

@@ -2,7 +2,9 @@
 //   S = [A | A16] [B | B16]^T   (M = N = 128, K = 128 via two 128-byte-swizzled blocks + 16 via
 //                                the no-swizzle layout), fp32 in tensor memory;
 //   O = P V^T                   with P (bf16) stored into tensor memory over S's columns and
-//                                used as the A operand from tensor memory.
+//                                used as the A operand from tensor memory;
+//   O = P V                     (second kernel) with V stored [key][d] -- N contiguous -- and read
+//                                as an MN-major, 128-byte-swizzled B operand.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -112,7 +114,72 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(const __nv_bfloat16 
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem_base, 256);
 }
+// O = P V with V [128 keys][128 d] row-major: in shared memory as two [128 keys][64 d] swizzled
+// blocks (d 0-63, d 64-127); K-step kk (16 keys) starts 16 rows = 2048 bytes further; the two
+// 64-element N atoms are one block (16 KB) apart; 8-key groups are 1024 bytes apart.
+__global__ void __launch_bounds__(128) umma_mn_selftest_kernel(const __nv_bfloat16 *P, const __nv_bfloat16 *V,
+                                                               float *O_out, int *err) {
+  extern __shared__ __align__(16) unsigned char sm_raw[];
+  unsigned char *sm = sm_raw + ((1024 - (tc::smem_u32(sm_raw) & 1023)) & 1023);
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tmem_base;
+  const int tid = threadIdx.x, warp = tid / 32;
+  put_sw128(sm, V, K, N);  // rows = keys, columns = d
+  tc::fence_proxy_async_smem();
+  if (tid == 0) {
+    tc::mbar_init(&bar, 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(&tmem_base, 256);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tP = tmem_base, tO = tmem_base + 128;
+  const uint32_t lane_addr = ((uint32_t)(32 * warp)) << 16;
+  const int row = tid;
+  for (int c = 0; c < 64; c += 16) {
+    uint32_t pw[16];
+    for (int i = 0; i < 16; i++) {
+      const __nv_bfloat16 lo = P[row * K + 2 * (c + i)], hi = P[row * K + 2 * (c + i) + 1];
+      pw[i] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+    }
+    tc::tmem_st16(tP + lane_addr + c, pw);
+  }
+  tc::tmem_st_wait();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (tid == 0) {
+    const uint32_t idesc = tc::idesc_bf16_f32(M, N) | (1u << 16);  // B MN-major
+    for (int kk = 0; kk < K / 16; kk++)
+      tc::mma_ts(tO, tP + 8 * kk, tc::desc_sw128_mn(tc::smem_u32(sm) + 2048u * kk, K * 128, 1024), idesc, kk > 0);
+    tc::mma_commit(&bar);
+  }
+  if (!tc::mbar_wait(&bar, 0, kLimitNs)) atomicExch(err, 3);
+  tc::fence_after_sync();
+  uint32_t r[32];
+  for (int c = 0; c < N; c += 32) {
+    tc::tmem_ld32(tO + lane_addr + c, r);
+    tc::tmem_ld_wait();
+    for (int i = 0; i < 32; i++) O_out[row * N + c + i] = __uint_as_float(r[i]);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem_base, 256);
+}
 }  // namespace
+
+extern "C" int umma_mn_selftest(const void *P, const void *V, float *O, int *err) {
+  const int smem = 32768 + 1024;
+  if (cudaFuncSetAttribute(umma_mn_selftest_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return -1;
+  umma_mn_selftest_kernel<<<1, 128, smem>>>((const __nv_bfloat16 *)P, (const __nv_bfloat16 *)V, O, err);
+  if (cudaGetLastError() != cudaSuccess) return -2;
+  return cudaDeviceSynchronize() == cudaSuccess ? 0 : -3;
+}
 
 extern "C" int umma_selftest(const void *A, const void *B, const void *P, const void *Vt, float *S, float *O,
                              int *err) {

@@ -1,6 +1,6 @@
 """GPU self-test of the tcgen05 building blocks (shared-memory descriptors with and without
 swizzle, the kind::f16 instruction descriptor, tensor-memory loads/stores and the MMA with its
-A operand in tensor memory) against torch matmuls."""
+A operand in tensor memory, the MN-major B operand) against torch matmuls."""
 import ctypes as C
 import os
 import subprocess
@@ -23,6 +23,7 @@ def lib():
                     "-Xcompiler", "-fPIC", "-shared", "-o", so, src], check=True)
     l = C.CDLL(so)
     l.umma_selftest.argtypes = [C.c_void_p] * 7
+    l.umma_mn_selftest.argtypes = [C.c_void_p] * 4
     return l
 
 
@@ -41,4 +42,17 @@ def test_umma_building_blocks(lib):
     S_ref = A.float() @ B.float().T
     O_ref = P.float() @ Vt.float().T
     assert torch.allclose(S, S_ref, rtol=1e-4, atol=1e-3), (S - S_ref).abs().max()
+    assert torch.allclose(O, O_ref, rtol=1e-4, atol=1e-3), (O - O_ref).abs().max()
+
+
+def test_umma_mn_major_b_operand(lib):
+    """P V with V stored [key][d] (N contiguous) and read as an MN-major swizzled B operand."""
+    g = torch.Generator(device="cpu").manual_seed(1)
+    P = torch.rand(128, 128, generator=g).to(torch.bfloat16).cuda()
+    V = torch.randn(128, 128, generator=g).to(torch.bfloat16).cuda()
+    O = torch.zeros(128, 128, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = lib.umma_mn_selftest(P.data_ptr(), V.data_ptr(), O.data_ptr(), err.data_ptr())
+    assert rc == 0 and err.item() == 0
+    O_ref = P.float() @ V.float()
     assert torch.allclose(O, O_ref, rtol=1e-4, atol=1e-3), (O - O_ref).abs().max()
