@@ -125,10 +125,15 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
       *(uint4 *)(sm + L.bh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
       *(uint4 *)(sm + L.bl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
-    for (int j = tid; j < C; j += kThreads) {
-      float s = 0.f;
-      for (int c = 0; c < D; c++) s = fmaf(cent[(int64_t)j * D + c], cent[(int64_t)j * D + c], s);
-      norm[j] = s;
+    for (int j = warp; j < C; j += kThreads / 32) {  // one warp per centroid, 4 channels per lane
+      const float4 a = *(const float4 *)(cent + (int64_t)j * D + 4 * lane);
+      float s = a.x * a.x;
+      s = fmaf(a.y, a.y, s);
+      s = fmaf(a.z, a.z, s);
+      s = fmaf(a.w, a.w, s);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (lane == 0) norm[j] = s;
     }
     tc::fence_proxy_async_smem();
     __syncthreads();
@@ -216,15 +221,31 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
     const int64_t t_begin = sc0 * TILE;
     const int64_t t_stop = (sc0 + nt) * TILE;
     const int64_t t_end = t_stop < p.n ? t_stop : p.n;
-    for (int64_t tok = t_begin + warp; tok < t_end; tok += kThreads / 32) {
-      const int j = asg[tok - t_begin];
-      const uint2 raw = *(const uint2 *)(xh + tok * D + 4 * lane);
-      float *sj = sums + j * D + 4 * lane;
-      atomicAdd(sj + 0, __uint_as_float(raw.x << 16));
-      atomicAdd(sj + 1, __uint_as_float(raw.x & 0xFFFF0000u));
-      atomicAdd(sj + 2, __uint_as_float(raw.y << 16));
-      atomicAdd(sj + 3, __uint_as_float(raw.y & 0xFFFF0000u));
-      if (lane == 0) atomicAdd(cnts + j, 1);
+    // warp w takes tokens w, w + 6, w + 12, ...: 8 of them at a time, loads first, then the adds
+    constexpr int kStep = kThreads / 32, kUnroll = 8;
+    for (int64_t tb = t_begin + warp; tb < t_end; tb += (int64_t)kStep * kUnroll) {
+      uint2 raw[kUnroll];
+      int jj[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; u++) {
+        const int64_t tok = tb + (int64_t)u * kStep;
+        jj[u] = -1;
+        raw[u] = make_uint2(0u, 0u);
+        if (tok < t_end) {
+          jj[u] = asg[tok - t_begin];
+          raw[u] = *(const uint2 *)(xh + tok * D + 4 * lane);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; u++) {
+        if (jj[u] < 0) continue;
+        float *sj = sums + jj[u] * D + 4 * lane;
+        atomicAdd(sj + 0, __uint_as_float(raw[u].x << 16));
+        atomicAdd(sj + 1, __uint_as_float(raw[u].x & 0xFFFF0000u));
+        atomicAdd(sj + 2, __uint_as_float(raw[u].y << 16));
+        atomicAdd(sj + 3, __uint_as_float(raw[u].y & 0xFFFF0000u));
+        if (lane == 0) atomicAdd(cnts + jj[u], 1);
+      }
     }
     __syncthreads();
     for (int e = tid; e < C * D; e += kThreads) psum[e] = first ? sums[e] : psum[e] + sums[e];
@@ -265,7 +286,8 @@ __global__ void km_update_kernel(int C, int G, float *__restrict__ cent, const f
 
 }  // namespace
 
-int kmeans_ctas_per_head(int H, int num_sms) { return (num_sms + H - 1) / H; }
+// CTAs per head: one wave at most (each CTA holds ~200 KB of shared memory).
+int kmeans_ctas_per_head(int H, int num_sms) { return num_sms / H > 1 ? num_sms / H : 1; }
 
 cudaError_t launch_kmeans(const uint16_t *x, int64_t n, int H, int C, const uint16_t *init, int iters,
                           uint16_t *cent, float *km_cent, float *km_sum, int32_t *km_cnt, int num_sms,

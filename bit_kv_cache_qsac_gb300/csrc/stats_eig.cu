@@ -142,7 +142,8 @@ constexpr int kJacThreads = 512;
 constexpr int LD = D + 4;  // padded row stride of the shared matrices (16-byte aligned rows)
 constexpr int NP = D / 2;  // disjoint pairs per round
 constexpr int kMaxSweeps = 30;
-constexpr float kRotTol = 1e-6f;  // rotate (p,q) while |a_pq| > tol * sqrt(|a_pp a_qq|)
+constexpr float kRotTol = 1e-6f;  // rotate (p,q) while |a_pq| > tol * sqrt(|a_pp a_qq|) ...
+constexpr float kAbsTol = 1.2e-7f;  // ... and |a_pq| > kAbsTol ||A||_F (fp32 rounding level of A)
 
 // C = op(X) Y for 128x128 shared matrices (row stride LD), op(X) = X or X^T; 512 threads, each
 // owning an 8x4 block of C.
@@ -217,6 +218,28 @@ __global__ void __launch_bounds__(kJacThreads) jacobi_kernel(const float *__rest
     }
     __syncthreads();
   }
+  // ||A||_F, reduced in a fixed order: off-diagonal entries at the rounding level of A carry no
+  // information and would otherwise keep the sweeps going on rotation noise
+  __shared__ float fro_part[kJacThreads / 32];
+  __shared__ float abs_tol;
+  {
+    float f = 0.f;
+    for (int i = tid; i < D * D; i += kJacThreads) {
+      const float a = A[(i / D) * LD + i % D];
+      f = fmaf(a, a, f);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) f += __shfl_xor_sync(0xffffffffu, f, o);
+    if ((tid & 31) == 0) fro_part[tid / 32] = f;
+    __syncthreads();
+    if (tid == 0) {
+      float t = 0.f;
+      for (int w = 0; w < kJacThreads / 32; w++) t += fro_part[w];
+      abs_tol = kAbsTol * sqrtf(t);
+    }
+    __syncthreads();
+  }
+  const float atol = abs_tol;
   bool converged = false;
   for (int sweep = 0; sweep < kMaxSweeps; sweep++) {
     if (tid == 0) rotated = 0;
@@ -230,7 +253,7 @@ __global__ void __launch_bounds__(kJacThreads) jacobi_kernel(const float *__rest
         const int p = min(a, b), qd = max(a, b);
         const float apq = A[p * LD + qd], app = A[p * LD + p], aqq = A[qd * LD + qd];
         float c = 1.f, s = 0.f;
-        if (apq != 0.f && fabsf(apq) > kRotTol * sqrtf(fabsf(app * aqq))) {
+        if (fabsf(apq) > atol && fabsf(apq) > kRotTol * sqrtf(fabsf(app * aqq))) {
           // Golub & Van Loan, sym.schur2: the rotation that diagonalises [[app, apq], [apq, aqq]]
           const float tau = (aqq - app) / (2.f * apq);
           const float t = (tau >= 0.f ? 1.f : -1.f) / (fabsf(tau) + sqrtf(1.f + tau * tau));
