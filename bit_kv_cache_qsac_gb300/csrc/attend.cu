@@ -289,6 +289,9 @@ __device__ __forceinline__ void write_qx_row(const AttnParams &p, const AttnChun
 }
 
 // Key (VAL = false) or Value (VAL = true) producer loop of one thread (row r of every tile).
+// Two register sets A and B hold the index data of alternate tiles; the loop body is written
+// twice with the sets swapped, so the loads for tile j+2 land in the set tile j just used and
+// have a whole iteration to arrive (no register copies that would wait for them).
 template <bool VAL>
 __device__ __forceinline__ void producer(const AttnParams &p, unsigned char *sm, Bars &bars, int *abort_flag,
                                          uint32_t lut, int h, int64_t q0, int r, int lane) {
@@ -299,7 +302,7 @@ __device__ __forceinline__ void producer(const AttnParams &p, unsigned char *sm,
   const uint32_t stage0 = tc::smem_u32(sm + (VAL ? OFF_V : OFF_K));
   const uint32_t xs0 = tc::smem_u32(sm + OFF_X), qx0 = tc::smem_u32(sm + OFF_QX);
   // positions (chunk, tile in chunk) of tiles j, j+1, j+2
-  int t = 0, tic = 0, t1 = 0, ti1 = 0, t2 = 0, ti2 = 0;
+  int t0 = 0, ti0 = 0, t1 = 0, ti1 = 0, t2 = 0, ti2 = 0;
   auto advance = [&](int &tt, int &ti) {
     if (++ti == p.ch[tt].tiles) { ti = 0; tt++; }
   };
@@ -309,26 +312,26 @@ __device__ __forceinline__ void producer(const AttnParams &p, unsigned char *sm,
     const int nk = (c.n - k0) < BN ? (int)(c.n - k0) : BN;
     load_row<VAL>(c, h, C, k0, nk, r, d);
   };
-  RowData cur, nxt, nxt2;
-  nxt.idx = nxt2.idx = -1;
-  load_at(0, 0, cur);
+  RowData A, B;
+  B.idx = -1;
+  load_at(0, 0, A);
   if (J > 1) {
     advance(t1, ti1);
-    load_at(t1, ti1, nxt);
+    load_at(t1, ti1, B);
   }
-  issue_row_copies(VAL ? p.ch[0].cent_v16 : p.ch[0].cent_k16, h, C, cur, stage0, r);
+  issue_row_copies(VAL ? p.ch[0].cent_v16 : p.ch[0].cent_k16, h, C, A, stage0, r);
   tc::cp_async_commit();
-  for (int j = 0; j < J; j++) {
+  // one tile: decode `cur` (tile j), issue the copies of tile j+1 from `nxt`, load tile j+2 into `cur`
+  auto step = [&](int j, RowData &cur, const RowData &nxt) -> bool {
     const int s = j & 1;
-    const AttnChunk &ch = p.ch[t];
-    // ---- tile j: wait for this thread's copies, decode in place ----
+    const AttnChunk &ch = p.ch[t0];
     tc::cp_async_wait<0>();
     decode_row<VAL>(cur, stage0 + (uint32_t)s * 2u * kBlk, r, lut);
     if (!VAL) {
       write_x_row(cur, ch.rank, xs0 + (uint32_t)s * kXBytes, r);
-      if (tic == 0) {  // chunk start: the second MMA's A operand for both Query tiles
-        if (t > 0 && !tc::mbar_wait(&bars.qx_free, (t - 1) & 1, kWaitNs)) fail(abort_flag, p.status);
-        if (*abort_v) break;
+      if (ti0 == 0) {  // chunk start: the second MMA's A operand for both Query tiles
+        if (t0 > 0 && !tc::mbar_wait(&bars.qx_free, (t0 - 1) & 1, kWaitNs)) fail(abort_flag, p.status);
+        if (*abort_v) return false;
         write_qx_row(p, ch, h, q0 + r, qx0, r);
         write_qx_row(p, ch, h, q0 + BM + r, qx0 + kXBytes, r);
       }
@@ -336,24 +339,25 @@ __device__ __forceinline__ void producer(const AttnParams &p, unsigned char *sm,
     tc::fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(&full[s]);
-    // ---- tile j+1: copies into the other stage once tile j-1 has released it ----
-    if (j + 1 < J) {
+    if (j + 1 < J) {  // copies of tile j+1 into the other stage once tile j-1 has released it
       if (j >= 1 && !tc::mbar_wait(&empty[s ^ 1], ((j - 1) >> 1) & 1, kWaitNs)) fail(abort_flag, p.status);
-      if (*abort_v) break;
-      issue_row_copies(VAL ? p.ch[t1].cent_v16 : p.ch[t1].cent_k16, h, C, nxt, stage0 + (uint32_t)(s ^ 1) * 2u * kBlk,
-                       r);
+      if (*abort_v) return false;
+      issue_row_copies(VAL ? p.ch[t1].cent_v16 : p.ch[t1].cent_k16, h, C, nxt,
+                       stage0 + (uint32_t)(s ^ 1) * 2u * kBlk, r);
       tc::cp_async_commit();
     }
-    // ---- index data of tile j+2 ----
-    if (j + 2 < J) {
-      t2 = t1; ti2 = ti1;
+    t2 = t1; ti2 = ti1;
+    if (j + 2 < J) {  // index data of tile j+2 (used two steps from now)
       advance(t2, ti2);
-      load_at(t2, ti2, nxt2);
+      load_at(t2, ti2, cur);
     }
-    cur = nxt;
-    nxt = nxt2;
-    t = t1; tic = ti1;
+    t0 = t1; ti0 = ti1;
     t1 = t2; ti1 = ti2;
+    return true;
+  };
+  for (int j = 0; j < J; j += 2) {
+    if (!step(j, A, B)) break;
+    if (j + 1 < J && !step(j + 1, B, A)) break;
   }
   tc::cp_async_wait<0>();
 }
