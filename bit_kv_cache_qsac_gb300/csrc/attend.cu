@@ -432,15 +432,15 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
       if (!tc::mbar_wait(&bars.s_full[x], j & 1, kWaitNs)) fail(&abort_flag, p.status);
       if (*abort_v) { ok = false; break; }
       tc::fence_after_sync();
-      uint32_t r[32];
+      uint32_t r[64];
       float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll 1
-      for (int cq = 0; cq < 4; cq++) {
-        tc::tmem_ld16(tS + 32u * cq, r);
-        tc::tmem_ld16(tS + 32u * cq + 16u, r + 16);
+      for (int hh = 0; hh < 2; hh++) {  // 64 columns per TMEM round trip
+#pragma unroll
+        for (int k = 0; k < 4; k++) tc::tmem_ld16(tS + 64u * hh + 16u * k, r + 16 * k);
         tc::tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; i += 8) {
+        for (int i = 0; i < 64; i += 8) {
           mx0 = tc::max3(mx0, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
           mx1 = tc::max3(mx1, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
           mx2 = tc::max3(mx2, __uint_as_float(r[i + 4]), __uint_as_float(r[i + 5]));
@@ -468,20 +468,23 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
       }
       const float nm = -m_used;
 #pragma unroll 1
-      for (int cq = 0; cq < 4; cq++) {
-        tc::tmem_ld16(tS + 32u * cq, r);
-        tc::tmem_ld16(tS + 32u * cq + 16u, r + 16);
-        tc::tmem_ld_wait();
-        uint32_t pw[16];
+      for (int hh = 0; hh < 2; hh++) {
 #pragma unroll
-        for (int i = 0; i < 16; i++) {
-          const float e0 = tc::ex2_approx(fmaf(__uint_as_float(r[2 * i]), sl2, nm));
-          const float e1 = tc::ex2_approx(fmaf(__uint_as_float(r[2 * i + 1]), sl2, nm));
-          if (i & 1) l1 += e0 + e1;
-          else l0 += e0 + e1;
-          pw[i] = f16pair(e0, e1);
+        for (int k = 0; k < 4; k++) tc::tmem_ld16(tS + 64u * hh + 16u * k, r + 16 * k);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int g = 0; g < 2; g++) {
+          uint32_t pw[16];
+#pragma unroll
+          for (int i = 0; i < 16; i++) {
+            const float e0 = tc::ex2_approx(fmaf(__uint_as_float(r[32 * g + 2 * i]), sl2, nm));
+            const float e1 = tc::ex2_approx(fmaf(__uint_as_float(r[32 * g + 2 * i + 1]), sl2, nm));
+            if (i & 1) l1 += e0 + e1;
+            else l0 += e0 + e1;
+            pw[i] = f16pair(e0, e1);
+          }
+          tc::tmem_st16(tS + 32u * hh + 16u * g, pw);  // P (fp16 pairs) overlays the logits already read
         }
-        tc::tmem_st16(tS + 16u * cq, pw);  // P (fp16 pairs) overlays the logits already read
       }
       tc::tmem_st_wait();
       tc::fence_before_sync();
