@@ -110,6 +110,12 @@ __device__ __forceinline__ void fail(int *abort_flag, int32_t *status) {
 }
 
 __device__ __forceinline__ uint32_t f16pair(float lo, float hi) { return tc::pack_f16x2(lo, hi); }
+// two 32-bit registers as one 64-bit operand of the packed fp32 instructions
+__device__ __forceinline__ uint64_t pk64(uint32_t lo, uint32_t hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+  return d;
+}
 
 template <bool VAL>
 __device__ __forceinline__ void load_row(const AttnChunk &c, int h, int C, int64_t k0, int nk, int r, RowData &d) {
@@ -147,12 +153,20 @@ __device__ __forceinline__ void load_row(const AttnChunk &c, int h, int C, int64
   }
 }
 
-// Centroid row of `d` -> this thread's row of a swizzled stage (zeros for a row past the end).
-__device__ __forceinline__ void issue_row_copies(const uint16_t *cent16, int h, int C, const RowData &d,
-                                                 uint32_t stage, int r) {
+// Centroid index of row r of a tile, or -1 past the end of the chunk.
+template <bool VAL>
+__device__ __forceinline__ int load_idx(const AttnChunk &c, int h, int C, int64_t k0, int nk, int r) {
+  if (r >= nk) return -1;
+  const int ix = (VAL ? c.v_idx : c.k_idx)[(int64_t)h * c.n + k0 + r];
+  return ix < C ? ix : C - 1;
+}
+
+// Centroid row `idx` -> this thread's row of a swizzled stage (zeros for idx < 0).
+__device__ __forceinline__ void issue_row_copies(const uint16_t *cent16, int h, int C, int idx, uint32_t stage,
+                                                 int r) {
   const uint32_t rowb = stage + (uint32_t)r * 128u, rx = (uint32_t)r & 7u;
-  const uint32_t bytes = d.idx >= 0 ? 16u : 0u;
-  const uint16_t *src = cent16 + ((int64_t)h * C + (d.idx >= 0 ? d.idx : 0)) * D;
+  const uint32_t bytes = idx >= 0 ? 16u : 0u;
+  const uint16_t *src = cent16 + ((int64_t)h * C + (idx >= 0 ? idx : 0)) * D;
 #pragma unroll
   for (int v = 0; v < 16; v++)
     tc::cp_async16_zfill(rowb + (uint32_t)(v >> 3) * kBlk + ((((uint32_t)v & 7u) ^ rx) << 4), src + 8 * v, bytes);
@@ -289,9 +303,11 @@ __device__ __forceinline__ void write_qx_row(const AttnParams &p, const AttnChun
 }
 
 // Key (VAL = false) or Value (VAL = true) producer loop of one thread (row r of every tile).
-// Two register sets A and B hold the index data of alternate tiles; the loop body is written
-// twice with the sets swapped, so the loads for tile j+2 land in the set tile j just used and
-// have a whole iteration to arrive (no register copies that would wait for them).
+// Step j issues the centroid copies of tile j+1 (as soon as tile j-1 has released the other
+// stage) before decoding tile j, so the copies are in flight during the decode; the centroid
+// index of tile j+2 is loaded one step before its copies are issued, the rest of its row data
+// two steps before its decode.  Two register sets A and B hold the row data of alternate tiles
+// and the loop body is written twice with the sets swapped, so no register copy waits on a load.
 template <bool VAL>
 __device__ __forceinline__ void producer(const AttnParams &p, unsigned char *sm, Bars &bars, int *abort_flag,
                                          uint32_t lut, int h, int64_t q0, int r, int lane) {
@@ -306,26 +322,48 @@ __device__ __forceinline__ void producer(const AttnParams &p, unsigned char *sm,
   auto advance = [&](int &tt, int &ti) {
     if (++ti == p.ch[tt].tiles) { ti = 0; tt++; }
   };
-  auto load_at = [&](int tt, int ti, RowData &d) {
+  auto rows_of = [&](int tt, int ti, int64_t &k0) {
     const AttnChunk &c = p.ch[tt];
-    const int64_t k0 = (int64_t)ti * BN;
-    const int nk = (c.n - k0) < BN ? (int)(c.n - k0) : BN;
-    load_row<VAL>(c, h, C, k0, nk, r, d);
+    k0 = (int64_t)ti * BN;
+    return (c.n - k0) < BN ? (int)(c.n - k0) : BN;
+  };
+  auto load_at = [&](int tt, int ti, RowData &d) {
+    int64_t k0;
+    const int nk = rows_of(tt, ti, k0);
+    load_row<VAL>(p.ch[tt], h, C, k0, nk, r, d);
+  };
+  auto idx_at = [&](int tt, int ti) {
+    int64_t k0;
+    const int nk = rows_of(tt, ti, k0);
+    return load_idx<VAL>(p.ch[tt], h, C, k0, nk, r);
   };
   RowData A, B;
   B.idx = -1;
+  int ix1 = -1;  // centroid index of tile j+1
   load_at(0, 0, A);
   if (J > 1) {
     advance(t1, ti1);
     load_at(t1, ti1, B);
+    ix1 = B.idx;
   }
-  issue_row_copies(VAL ? p.ch[0].cent_v16 : p.ch[0].cent_k16, h, C, A, stage0, r);
+  issue_row_copies(VAL ? p.ch[0].cent_v16 : p.ch[0].cent_k16, h, C, A.idx, stage0, r);
   tc::cp_async_commit();
-  // one tile: decode `cur` (tile j), issue the copies of tile j+1 from `nxt`, load tile j+2 into `cur`
-  auto step = [&](int j, RowData &cur, const RowData &nxt) -> bool {
+  auto step = [&](int j, RowData &cur) -> bool {
     const int s = j & 1;
     const AttnChunk &ch = p.ch[t0];
-    tc::cp_async_wait<0>();
+    t2 = t1; ti2 = ti1;
+    if (j + 2 < J) advance(t2, ti2);
+    if (j + 1 < J) {
+      if (j >= 1 && !tc::mbar_wait(&empty[s ^ 1], ((j - 1) >> 1) & 1, kWaitNs)) fail(abort_flag, p.status);
+      if (*abort_v) return false;
+      issue_row_copies(VAL ? p.ch[t1].cent_v16 : p.ch[t1].cent_k16, h, C, ix1,
+                       stage0 + (uint32_t)(s ^ 1) * 2u * kBlk, r);
+      tc::cp_async_commit();
+      if (j + 2 < J) ix1 = idx_at(t2, ti2);  // used when the next step issues its copies
+      tc::cp_async_wait<1>();                // tile j's copies (all but the group just issued)
+    } else {
+      tc::cp_async_wait<0>();
+    }
     decode_row<VAL>(cur, stage0 + (uint32_t)s * 2u * kBlk, r, lut);
     if (!VAL) {
       write_x_row(cur, ch.rank, xs0 + (uint32_t)s * kXBytes, r);
@@ -339,25 +377,14 @@ __device__ __forceinline__ void producer(const AttnParams &p, unsigned char *sm,
     tc::fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(&full[s]);
-    if (j + 1 < J) {  // copies of tile j+1 into the other stage once tile j-1 has released it
-      if (j >= 1 && !tc::mbar_wait(&empty[s ^ 1], ((j - 1) >> 1) & 1, kWaitNs)) fail(abort_flag, p.status);
-      if (*abort_v) return false;
-      issue_row_copies(VAL ? p.ch[t1].cent_v16 : p.ch[t1].cent_k16, h, C, nxt,
-                       stage0 + (uint32_t)(s ^ 1) * 2u * kBlk, r);
-      tc::cp_async_commit();
-    }
-    t2 = t1; ti2 = ti1;
-    if (j + 2 < J) {  // index data of tile j+2 (used two steps from now)
-      advance(t2, ti2);
-      load_at(t2, ti2, cur);
-    }
+    if (j + 2 < J) load_at(t2, ti2, cur);  // row data of tile j+2 (decoded two steps from now)
     t0 = t1; ti0 = ti1;
     t1 = t2; ti1 = ti2;
     return true;
   };
   for (int j = 0; j < J; j += 2) {
-    if (!step(j, A, B)) break;
-    if (j + 1 < J && !step(j + 1, B, A)) break;
+    if (!step(j, A)) break;
+    if (j + 1 < J && !step(j + 1, B)) break;
   }
   tc::cp_async_wait<0>();
 }
@@ -426,21 +453,22 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     const uint32_t tS = tmem + lane_addr + 128u * x, tO = tmem + lane_addr + 256u + 128u * x;
     const float sl2 = p.scale_log2;
     float m_used = -INFINITY;
-    float l0 = 0.f, l1 = 0.f;  // running row sum (two partial sums)
+    uint64_t acc0 = 0ull, acc1 = 0ull;  // running row sum: two packed fp32 pairs
+    const uint64_t sc2 = pk64(__float_as_uint(sl2), __float_as_uint(sl2));
     bool ok = true;
     for (int j = 0; j < J; j++) {
       if (!tc::mbar_wait(&bars.s_full[x], j & 1, kWaitNs)) fail(&abort_flag, p.status);
       if (*abort_v) { ok = false; break; }
       tc::fence_after_sync();
-      uint32_t r[64];
+      uint32_t r[32];
       float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll 1
-      for (int hh = 0; hh < 2; hh++) {  // 64 columns per TMEM round trip
-#pragma unroll
-        for (int k = 0; k < 4; k++) tc::tmem_ld16(tS + 64u * hh + 16u * k, r + 16 * k);
+      for (int cq = 0; cq < 4; cq++) {  // 32 columns per TMEM round trip (~30 cycles)
+        tc::tmem_ld16(tS + 32u * cq, r);
+        tc::tmem_ld16(tS + 32u * cq + 16u, r + 16);
         tc::tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 64; i += 8) {
+        for (int i = 0; i < 32; i += 8) {
           mx0 = tc::max3(mx0, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
           mx1 = tc::max3(mx1, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
           mx2 = tc::max3(mx2, __uint_as_float(r[i + 4]), __uint_as_float(r[i + 5]));
@@ -452,8 +480,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
       if (__any_sync(0xffffffffu, m_new > m_used + kRescaleThreshold)) {
         if (j > 0) {
           const float alpha = tc::ex2_approx(m_used - m_new);
-          l0 *= alpha;
-          l1 *= alpha;
+          const uint64_t a2 = pk64(__float_as_uint(alpha), __float_as_uint(alpha));
+          acc0 = tc::fma2(acc0, a2, 0ull);
+          acc1 = tc::fma2(acc1, a2, 0ull);
 #pragma unroll 1
           for (int c = 0; c < D; c += 32) {
             uint32_t o[32];
@@ -466,25 +495,23 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
         }
         m_used = m_new;
       }
-      const float nm = -m_used;
+      const uint64_t nm2 = pk64(__float_as_uint(-m_used), __float_as_uint(-m_used));
 #pragma unroll 1
-      for (int hh = 0; hh < 2; hh++) {
-#pragma unroll
-        for (int k = 0; k < 4; k++) tc::tmem_ld16(tS + 64u * hh + 16u * k, r + 16 * k);
+      for (int cq = 0; cq < 4; cq++) {
+        tc::tmem_ld16(tS + 32u * cq, r);
+        tc::tmem_ld16(tS + 32u * cq + 16u, r + 16);
         tc::tmem_ld_wait();
+        uint32_t pw[16];
 #pragma unroll
-        for (int g = 0; g < 2; g++) {
-          uint32_t pw[16];
-#pragma unroll
-          for (int i = 0; i < 16; i++) {
-            const float e0 = tc::ex2_approx(fmaf(__uint_as_float(r[32 * g + 2 * i]), sl2, nm));
-            const float e1 = tc::ex2_approx(fmaf(__uint_as_float(r[32 * g + 2 * i + 1]), sl2, nm));
-            if (i & 1) l1 += e0 + e1;
-            else l0 += e0 + e1;
-            pw[i] = f16pair(e0, e1);
-          }
-          tc::tmem_st16(tS + 32u * hh + 16u * g, pw);  // P (fp16 pairs) overlays the logits already read
+        for (int i = 0; i < 16; i++) {  // packed fp32 pairs: x = S * scale - m, then 2^x
+          const uint64_t x2 = tc::fma2(pk64(r[2 * i], r[2 * i + 1]), sc2, nm2);
+          const float e0 = tc::ex2_approx(tc::f2lo(x2)), e1 = tc::ex2_approx(tc::f2hi(x2));
+          const uint64_t e2 = pk64(__float_as_uint(e0), __float_as_uint(e1));
+          if (i & 1) acc1 = tc::add2(acc1, e2);
+          else acc0 = tc::add2(acc0, e2);
+          pw[i] = f16pair(e0, e1);
         }
+        tc::tmem_st16(tS + 16u * cq, pw);  // P (fp16 pairs) overlays the logits already read
       }
       tc::tmem_st_wait();
       tc::fence_before_sync();
@@ -495,7 +522,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     if (ok && !tc::mbar_wait(&bars.o_done, 0, kWaitNs)) fail(&abort_flag, p.status);
     if (ok && !*abort_v) {
       tc::fence_after_sync();
-      const float l = l0 + l1;
+      const uint64_t lsum = tc::add2(acc0, acc1);
+      const float l = tc::f2lo(lsum) + tc::f2hi(lsum);
       const int64_t qi = q0 + (int64_t)x * BM + row;
       const float inv = 1.f / l;
       uint32_t o[32];
