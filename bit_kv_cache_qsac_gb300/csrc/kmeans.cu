@@ -11,13 +11,15 @@
 // ||mu_j||^2 - 2 x.mu_j matters for the argmin.  x is bf16 (exact); the fp32 centroid is split
 // as mu = hi + lo with hi, lo bf16, so two bf16 MMAs give x.mu to about 2^-17 relative.
 //
-// km_assign_kernel (one CTA = one head x a contiguous range of 128-token tiles; 192 threads):
+// km_assign_kernel (one CTA = one head x a contiguous range of 128-token tiles; 320 threads):
 //   warp 0    TMA producer: token tiles (2 x [128][64] bf16, 128-byte swizzle) into 2 stages
 //   warp 1    TMEM owner and MMA issuer: D[128 x C] = X hi^T + X lo^T into 2 TMEM buffers
-//   warps 2-5 epilogue: thread = token = TMEM lane; argmin over the C columns
+//   warps 2-9 epilogue, two warpgroups taking alternate tiles: thread = token = TMEM lane;
+//             argmin over the C columns (two interleaved chains, lower index on ties)
 // The assignments of up to 4096 tokens stay in shared memory; then each warp adds its tokens
-// into per-CTA cluster sums in shared memory (over the codebook area) and the CTA adds them to
-// its own slice of the workspace.  km_update_kernel reduces the slices in a fixed order.
+// into per-CTA cluster sums in shared memory (over the codebook area; lane l adds channels l,
+// l + 32, l + 64, l + 96, so the 32 lanes of an add hit 32 different banks) and the CTA adds them
+// to its own slice of the workspace.  km_update_kernel reduces the slices in a fixed order.
 // All waits are bounded; on expiry the kernel records QWM_ERR_DEVICE_TIMEOUT and stops.
 #include "qwm_internal.cuh"
 #include "tc.cuh"
@@ -27,7 +29,7 @@ namespace {
 constexpr int D = QWM_D;
 constexpr int TILE = 128;
 constexpr int kMaxTok = 4096;  // tokens per super-chunk (assignments kept in shared memory)
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr uint64_t kWaitNs = 1000000000ull;
 
 struct KmSmem {  // offsets from a 1024-aligned base, for a codebook of C centroids
@@ -185,26 +187,31 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
         }
       }
     } else {
-      const int sub = warp & 3, row = 32 * sub + lane;
+      const int e = (warp - 2) >> 2, sub = warp & 3, row = 32 * sub + lane;
       const uint32_t lane_addr = (uint32_t)(32 * sub) << 16;
-      for (int i = 0; i < nt; i++) {
+      for (int i = e; i < nt; i += 2) {
         const int64_t g = g_tile + i;
         const int s = (int)(g & 1);
         if (!tc::mbar_wait(&t_full[s], (uint32_t)((g >> 1) & 1), kWaitNs)) *abort_v = 1;
         if (*abort_v) break;
         tc::fence_after_sync();
-        float best = INFINITY;
-        int arg = 0;
+        float b0 = INFINITY, b1 = INFINITY;  // even / odd columns
+        int a0 = 0, a1 = 1;
         uint32_t r[32];
+#pragma unroll 1
         for (int c0 = 0; c0 < C; c0 += 32) {
-          tc::tmem_ld32(tmem + lane_addr + 256u * s + c0, r);
+          tc::tmem_ld16(tmem + lane_addr + 256u * s + c0, r);
+          tc::tmem_ld16(tmem + lane_addr + 256u * s + c0 + 16, r + 16);
           tc::tmem_ld_wait();
 #pragma unroll
-          for (int k = 0; k < 32; k++) {
-            const float dist = fmaf(-2.f, __uint_as_float(r[k]), norm[c0 + k]);
-            if (dist < best) { best = dist; arg = c0 + k; }
+          for (int k = 0; k < 32; k += 2) {
+            const float d0 = fmaf(-2.f, __uint_as_float(r[k]), norm[c0 + k]);
+            const float d1 = fmaf(-2.f, __uint_as_float(r[k + 1]), norm[c0 + k + 1]);
+            if (d0 < b0) { b0 = d0; a0 = c0 + k; }
+            if (d1 < b1) { b1 = d1; a1 = c0 + k + 1; }
           }
         }
+        const int arg = (b1 < b0 || (b1 == b0 && a1 < a0)) ? a1 : a0;
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&t_empty[s]);
@@ -221,29 +228,27 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
     const int64_t t_begin = sc0 * TILE;
     const int64_t t_stop = (sc0 + nt) * TILE;
     const int64_t t_end = t_stop < p.n ? t_stop : p.n;
-    // warp w takes tokens w, w + 6, w + 12, ...: 8 of them at a time, loads first, then the adds
+    // warp w takes tokens w, w + 10, w + 20, ...: 8 of them at a time, loads first, then the adds
     constexpr int kStep = kThreads / 32, kUnroll = 8;
     for (int64_t tb = t_begin + warp; tb < t_end; tb += (int64_t)kStep * kUnroll) {
-      uint2 raw[kUnroll];
+      uint16_t xv[kUnroll][4];
       int jj[kUnroll];
 #pragma unroll
       for (int u = 0; u < kUnroll; u++) {
         const int64_t tok = tb + (int64_t)u * kStep;
         jj[u] = -1;
-        raw[u] = make_uint2(0u, 0u);
         if (tok < t_end) {
           jj[u] = asg[tok - t_begin];
-          raw[u] = *(const uint2 *)(xh + tok * D + 4 * lane);
+#pragma unroll
+          for (int k = 0; k < 4; k++) xv[u][k] = xh[tok * D + lane + 32 * k];
         }
       }
 #pragma unroll
       for (int u = 0; u < kUnroll; u++) {
         if (jj[u] < 0) continue;
-        float *sj = sums + jj[u] * D + 4 * lane;
-        atomicAdd(sj + 0, __uint_as_float(raw[u].x << 16));
-        atomicAdd(sj + 1, __uint_as_float(raw[u].x & 0xFFFF0000u));
-        atomicAdd(sj + 2, __uint_as_float(raw[u].y << 16));
-        atomicAdd(sj + 3, __uint_as_float(raw[u].y & 0xFFFF0000u));
+        float *sj = sums + jj[u] * D + lane;
+#pragma unroll
+        for (int k = 0; k < 4; k++) atomicAdd(sj + 32 * k, bf16_to_f32(xv[u][k]));
         if (lane == 0) atomicAdd(cnts + jj[u], 1);
       }
     }
@@ -279,7 +284,7 @@ __global__ void km_update_kernel(int C, int G, float *__restrict__ cent, const f
   }
   const int64_t e = ((int64_t)h * C + j) * D + c;
   float mu = cent[e];
-  if (cnt > 0) mu = (float)((double)s / (double)cnt);
+  if (cnt > 0) mu = __fdiv_rn(s, (float)cnt);  // counts are exact in fp32 (< 2^24)
   cent[e] = mu;
   if (out_bf16) out_bf16[e] = f32_to_bf16_rn(mu);
 }
