@@ -353,14 +353,21 @@ __device__ __forceinline__ void producer(const AttnParams &p, unsigned char *sm,
     const AttnChunk &ch = p.ch[t0];
     t2 = t1; ti2 = ti1;
     if (j + 2 < J) advance(t2, ti2);
-    if (j + 1 < J) {
-      if (j >= 1 && !tc::mbar_wait(&empty[s ^ 1], ((j - 1) >> 1) & 1, kWaitNs)) fail(abort_flag, p.status);
+    // copies of tile j+1 go out before the decode when tile j-1 has already released the other
+    // stage (the producers are behind: hide the copy latency); otherwise after it
+    auto issue_next = [&](bool wait) -> bool {
+      if (wait && j >= 1 && !tc::mbar_wait(&empty[s ^ 1], ((j - 1) >> 1) & 1, kWaitNs)) fail(abort_flag, p.status);
       if (*abort_v) return false;
       issue_row_copies(VAL ? p.ch[t1].cent_v16 : p.ch[t1].cent_k16, h, C, ix1,
                        stage0 + (uint32_t)(s ^ 1) * 2u * kBlk, r);
       tc::cp_async_commit();
       if (j + 2 < J) ix1 = idx_at(t2, ti2);  // used when the next step issues its copies
-      tc::cp_async_wait<1>();                // tile j's copies (all but the group just issued)
+      return true;
+    };
+    const bool early = j + 1 < J && (j == 0 || __all_sync(0xffffffffu, tc::mbar_test(&empty[s ^ 1], ((j - 1) >> 1) & 1)));
+    if (early) {
+      if (!issue_next(false)) return false;
+      tc::cp_async_wait<1>();  // tile j's copies (all but the group just issued)
     } else {
       tc::cp_async_wait<0>();
     }
@@ -377,6 +384,7 @@ __device__ __forceinline__ void producer(const AttnParams &p, unsigned char *sm,
     tc::fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(&full[s]);
+    if (j + 1 < J && !early && !issue_next(true)) return false;
     if (j + 2 < J) load_at(t2, ti2, cur);  // row data of tile j+2 (decoded two steps from now)
     t0 = t1; ti0 = ti1;
     t1 = t2; ti1 = ti2;
