@@ -153,23 +153,23 @@ __device__ __forceinline__ void load_row(const AttnChunk &c, int h, int C, int64
   }
 }
 
-// Centroid index of row r of a tile, or -1 past the end of the chunk.
-template <bool VAL>
-__device__ __forceinline__ int load_idx(const AttnChunk &c, int h, int C, int64_t k0, int nk, int r) {
-  if (r >= nk) return -1;
-  const int ix = (VAL ? c.v_idx : c.k_idx)[(int64_t)h * c.n + k0 + r];
-  return ix < C ? ix : C - 1;
-}
-
-// Centroid row `idx` -> this thread's row of a swizzled stage (zeros for idx < 0).
-__device__ __forceinline__ void issue_row_copies(const uint16_t *cent16, int h, int C, int idx, uint32_t stage,
-                                                 int r) {
-  const uint32_t rowb = stage + (uint32_t)r * 128u, rx = (uint32_t)r & 7u;
-  const uint32_t bytes = idx >= 0 ? 16u : 0u;
-  const uint16_t *src = cent16 + ((int64_t)h * C + (idx >= 0 ? idx : 0)) * D;
+// Centroid rows of this warp's 32 tile rows (rbase .. rbase + 31) -> a swizzled stage; `idx` is
+// the calling lane's row's centroid (< 0: zeros).  Each copy instruction moves two whole rows
+// (lanes 0-15 and 16-31, 16 bytes each), so a row is fetched as two full 128-byte lines.
+// The caller makes the copies visible to the other lanes (wait_group, then __syncwarp) before
+// any lane reads them.
+__device__ __forceinline__ void issue_warp_copies(const uint16_t *cent16, int h, int C, int idx, uint32_t stage,
+                                                  int rbase, int lane) {
+  const uint32_t v = (uint32_t)lane & 15u;
 #pragma unroll
-  for (int v = 0; v < 16; v++)
-    tc::cp_async16_zfill(rowb + (uint32_t)(v >> 3) * kBlk + ((((uint32_t)v & 7u) ^ rx) << 4), src + 8 * v, bytes);
+  for (int i = 0; i < 16; i++) {
+    const int rl = 2 * i + (lane >> 4);
+    const int ix = __shfl_sync(0xffffffffu, idx, rl);
+    const uint32_t row = (uint32_t)(rbase + rl);
+    const uint32_t dst = stage + (v >> 3) * kBlk + row * 128u + (((v & 7u) ^ (row & 7u)) << 4);
+    const uint16_t *src = cent16 + ((int64_t)h * C + (ix >= 0 ? ix : 0)) * D + 8 * v;
+    tc::cp_async16_zfill(dst, src, ix >= 0 ? 16u : 0u);
+  }
 }
 
 // In-place decode of this thread's row: fp16(mu + s q) for Keys, fp16(fp16(mu + m) + s q) for
@@ -303,16 +303,15 @@ __device__ __forceinline__ void write_qx_row(const AttnParams &p, const AttnChun
 }
 
 // Key (VAL = false) or Value (VAL = true) producer loop of one thread (row r of every tile).
-// Step j issues the centroid copies of tile j+1 (as soon as tile j-1 has released the other
-// stage) before decoding tile j, so the copies are in flight during the decode; the centroid
-// index of tile j+2 is loaded one step before its copies are issued, the rest of its row data
-// two steps before its decode.  Two register sets A and B hold the row data of alternate tiles
-// and the loop body is written twice with the sets swapped, so no register copy waits on a load.
+// Step j decodes tile j (its copies were issued one step earlier), then issues the copies of
+// tile j+1 into the other stage once tile j-1 has released it, then loads the row data of tile
+// j+2.  Two register sets A and B hold the row data of alternate tiles and the loop body is
+// written twice with the sets swapped, so no register copy waits on a load.
 template <bool VAL>
 __device__ __forceinline__ void producer(const AttnParams &p, unsigned char *sm, Bars &bars, int *abort_flag,
                                          uint32_t lut, int h, int64_t q0, int r, int lane) {
   volatile int *abort_v = abort_flag;
-  const int J = p.total_tiles, C = p.C;
+  const int J = p.total_tiles, C = p.C, rbase = r - lane;
   uint64_t *full = VAL ? bars.v_full : bars.k_full;
   uint64_t *empty = VAL ? bars.v_empty : bars.k_empty;
   const uint32_t stage0 = tc::smem_u32(sm + (VAL ? OFF_V : OFF_K));
@@ -322,61 +321,32 @@ __device__ __forceinline__ void producer(const AttnParams &p, unsigned char *sm,
   auto advance = [&](int &tt, int &ti) {
     if (++ti == p.ch[tt].tiles) { ti = 0; tt++; }
   };
-  auto rows_of = [&](int tt, int ti, int64_t &k0) {
-    const AttnChunk &c = p.ch[tt];
-    k0 = (int64_t)ti * BN;
-    return (c.n - k0) < BN ? (int)(c.n - k0) : BN;
-  };
   auto load_at = [&](int tt, int ti, RowData &d) {
-    int64_t k0;
-    const int nk = rows_of(tt, ti, k0);
-    load_row<VAL>(p.ch[tt], h, C, k0, nk, r, d);
-  };
-  auto idx_at = [&](int tt, int ti) {
-    int64_t k0;
-    const int nk = rows_of(tt, ti, k0);
-    return load_idx<VAL>(p.ch[tt], h, C, k0, nk, r);
+    const AttnChunk &c = p.ch[tt];
+    const int64_t k0 = (int64_t)ti * BN;
+    const int nk = (c.n - k0) < BN ? (int)(c.n - k0) : BN;
+    load_row<VAL>(c, h, C, k0, nk, r, d);
   };
   RowData A, B;
   B.idx = -1;
-  int ix1 = -1;  // centroid index of tile j+1
   load_at(0, 0, A);
   if (J > 1) {
     advance(t1, ti1);
     load_at(t1, ti1, B);
-    ix1 = B.idx;
   }
-  issue_row_copies(VAL ? p.ch[0].cent_v16 : p.ch[0].cent_k16, h, C, A.idx, stage0, r);
+  issue_warp_copies(VAL ? p.ch[0].cent_v16 : p.ch[0].cent_k16, h, C, A.idx, stage0, rbase, lane);
   tc::cp_async_commit();
-  auto step = [&](int j, RowData &cur) -> bool {
+  auto step = [&](int j, RowData &cur, const RowData &nxt) -> bool {
     const int s = j & 1;
     const AttnChunk &ch = p.ch[t0];
-    t2 = t1; ti2 = ti1;
-    if (j + 2 < J) advance(t2, ti2);
-    // copies of tile j+1 go out before the decode when tile j-1 has already released the other
-    // stage (the producers are behind: hide the copy latency); otherwise after it
-    auto issue_next = [&](bool wait) -> bool {
-      if (wait && j >= 1 && !tc::mbar_wait(&empty[s ^ 1], ((j - 1) >> 1) & 1, kWaitNs)) fail(abort_flag, p.status);
-      if (*abort_v) return false;
-      issue_row_copies(VAL ? p.ch[t1].cent_v16 : p.ch[t1].cent_k16, h, C, ix1,
-                       stage0 + (uint32_t)(s ^ 1) * 2u * kBlk, r);
-      tc::cp_async_commit();
-      if (j + 2 < J) ix1 = idx_at(t2, ti2);  // used when the next step issues its copies
-      return true;
-    };
-    const bool early = j + 1 < J && (j == 0 || __all_sync(0xffffffffu, tc::mbar_test(&empty[s ^ 1], ((j - 1) >> 1) & 1)));
-    if (early) {
-      if (!issue_next(false)) return false;
-      tc::cp_async_wait<1>();  // tile j's copies (all but the group just issued)
-    } else {
-      tc::cp_async_wait<0>();
-    }
+    tc::cp_async_wait<0>();
+    __syncwarp();  // the warp's copies of tile j, made visible to every lane
     decode_row<VAL>(cur, stage0 + (uint32_t)s * 2u * kBlk, r, lut);
     if (!VAL) {
       write_x_row(cur, ch.rank, xs0 + (uint32_t)s * kXBytes, r);
       if (ti0 == 0) {  // chunk start: the second MMA's A operand for both Query tiles
         if (t0 > 0 && !tc::mbar_wait(&bars.qx_free, (t0 - 1) & 1, kWaitNs)) fail(abort_flag, p.status);
-        if (*abort_v) return false;
+        if (__any_sync(0xffffffffu, *abort_v != 0)) return false;  // warp-uniform exit
         write_qx_row(p, ch, h, q0 + r, qx0, r);
         write_qx_row(p, ch, h, q0 + BM + r, qx0 + kXBytes, r);
       }
@@ -384,15 +354,25 @@ __device__ __forceinline__ void producer(const AttnParams &p, unsigned char *sm,
     tc::fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(&full[s]);
-    if (j + 1 < J && !early && !issue_next(true)) return false;
-    if (j + 2 < J) load_at(t2, ti2, cur);  // row data of tile j+2 (decoded two steps from now)
+    if (j + 1 < J) {  // copies of tile j+1 into the other stage once tile j-1 has released it
+      if (j >= 1 && !tc::mbar_wait(&empty[s ^ 1], ((j - 1) >> 1) & 1, kWaitNs)) fail(abort_flag, p.status);
+      if (__any_sync(0xffffffffu, *abort_v != 0)) return false;  // warp-uniform exit
+      issue_warp_copies(VAL ? p.ch[t1].cent_v16 : p.ch[t1].cent_k16, h, C, nxt.idx,
+                        stage0 + (uint32_t)(s ^ 1) * 2u * kBlk, rbase, lane);
+      tc::cp_async_commit();
+    }
+    t2 = t1; ti2 = ti1;
+    if (j + 2 < J) {  // row data of tile j+2 (decoded two steps from now)
+      advance(t2, ti2);
+      load_at(t2, ti2, cur);
+    }
     t0 = t1; ti0 = ti1;
     t1 = t2; ti1 = ti2;
     return true;
   };
   for (int j = 0; j < J; j += 2) {
-    if (!step(j, A)) break;
-    if (j + 1 < J && !step(j + 1, B)) break;
+    if (!step(j, A, B)) break;
+    if (j + 1 < J && !step(j + 1, B, A)) break;
   }
   tc::cp_async_wait<0>();
 }
