@@ -56,20 +56,28 @@ constexpr uint32_t kMaskBits = 0xFB53u;    // fp16 -60000
 
 // shared-memory map (bytes from a 1024-aligned base)
 constexpr int kBlk = BM * 128;                  // one [128 rows][64 fp16] swizzled block: 16 KB
-constexpr int kXBytes = 128 * 32 * 2;           // one [128 rows][32 fp16] no-swizzle operand: 8 KB
 constexpr int OFF_Q = 0;                        // 2 Query tiles x 2 blocks
 constexpr int OFF_K = OFF_Q + NQT * 2 * kBlk;   // 2 stages x 2 blocks of K rows
 constexpr int OFF_V = OFF_K + 2 * 2 * kBlk;     // 2 stages x 2 blocks of V rows
-constexpr int OFF_X = OFF_V + 2 * 2 * kBlk;     // 2 stages: B operand of the second MMA
-constexpr int OFF_QX = OFF_X + 2 * kXBytes;     // 2 Query tiles: A operand of the second MMA
-constexpr int SMEM_BYTES = OFF_QX + NQT * kXBytes;
-constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
+constexpr int OFF_X = OFF_V + 2 * 2 * kBlk;     // 2 stages: B operand of the second MMA, then
+                                                // 2 Query tiles: its A operand
 
-// byte offset of (row, column k) in a [128][32] fp16 K-major operand without swizzle: 8x8 core
-// matrices, 128 bytes apart along K and 512 bytes apart along the rows
-__host__ __device__ constexpr uint32_t xoff(uint32_t row, uint32_t k) {
-  return (row >> 3) * 512u + (k >> 3) * 128u + (row & 7u) * 16u + (k & 7u) * 2u;
-}
+// Layout of the second MMA's operands: [128 rows][16 or 32 fp16 columns], K-major without swizzle
+// (8x8 core matrices, 128 bytes apart along K and 16 x columns bytes apart along the rows).  The
+// narrow form (every chunk of the call has PSAC rank <= 8) leaves room for a byte-indexed code
+// table; the wide form serves ranks up to 16.
+template <bool WIDE>
+struct XL {
+  static constexpr int kCols = WIDE ? 32 : 16;
+  static constexpr int kBytes = 128 * kCols * 2;
+  static constexpr uint32_t kSbo = 16u * kCols;
+  static constexpr int kOffQX = OFF_X + 2 * kBytes;
+  static constexpr int kSmemBytes = kOffQX + NQT * kBytes;
+  static constexpr int kSmemAlloc = kSmemBytes + 1024;
+  __host__ __device__ static constexpr uint32_t off(uint32_t row, uint32_t k) {
+    return (row >> 3) * kSbo + (k >> 3) * 128u + (row & 7u) * 16u + (k & 7u) * 2u;
+  }
+};
 
 struct AttnChunk {
   int64_t n;
@@ -173,8 +181,9 @@ __device__ __forceinline__ void issue_warp_copies(const uint16_t *cent16, int h,
 }
 
 // In-place decode of this thread's row: fp16(mu + s q) for Keys, fp16(fp16(mu + m) + s q) for
-// Values; `lut` maps a 4-bit code pair to the fp16 pair (q_even, q_odd).
-template <bool VAL>
+// Values.  BYTE_LUT: `lut` maps a byte of 4 codes to two fp16 pairs (8 bytes per entry);
+// otherwise it maps a 4-bit code pair to one fp16 pair (q_even, q_odd).
+template <bool VAL, bool BYTE_LUT>
 __device__ __forceinline__ void decode_row(const RowData &d, uint32_t stage, int r, uint32_t lut) {
   if (d.idx < 0) return;  // zero-filled by the copies
   const uint32_t rowb = stage + (uint32_t)r * 128u, rx = (uint32_t)r & 7u;
@@ -189,10 +198,17 @@ __device__ __forceinline__ void decode_row(const RowData &d, uint32_t stage, int
       const uint32_t addr = rowb + (uint32_t)g * kBlk + ((((uint32_t)v) ^ rx) << 4);
       const uint4 mu = tc::lds128(addr);
       const uint32_t h16 = words[v >> 1] >> (16 * (v & 1));
-      const uint32_t q0 = tc::lds32(lut + ((h16 << 2) & 0x3Cu));
-      const uint32_t q1 = tc::lds32(lut + ((h16 >> 2) & 0x3Cu));
-      const uint32_t q2 = tc::lds32(lut + ((h16 >> 6) & 0x3Cu));
-      const uint32_t q3 = tc::lds32(lut + ((h16 >> 10) & 0x3Cu));
+      uint32_t q0, q1, q2, q3;
+      if (BYTE_LUT) {
+        const uint2 qa = tc::lds64(lut + ((h16 << 3) & 0x7F8u));
+        const uint2 qb = tc::lds64(lut + ((h16 >> 5) & 0x7F8u));
+        q0 = qa.x; q1 = qa.y; q2 = qb.x; q3 = qb.y;
+      } else {
+        q0 = tc::lds32(lut + ((h16 << 2) & 0x3Cu));
+        q1 = tc::lds32(lut + ((h16 >> 2) & 0x3Cu));
+        q2 = tc::lds32(lut + ((h16 >> 6) & 0x3Cu));
+        q3 = tc::lds32(lut + ((h16 >> 10) & 0x3Cu));
+      }
       uint4 o;
       if (VAL) {
         o.x = tc::hfma2(s2, q0, tc::hadd2(mu.x, m2));
@@ -211,6 +227,7 @@ __device__ __forceinline__ void decode_row(const RowData &d, uint32_t stage, int
 }
 
 // This thread's row of the second MMA's B operand: [c_hat (8 or 16) | m0 m0 m1 m1 | mask | 0 ...].
+template <bool WIDE>
 __device__ __forceinline__ void write_x_row(const RowData &d, int R, uint32_t xs, int r) {
   uint32_t w[16];
 #pragma unroll
@@ -239,11 +256,13 @@ __device__ __forceinline__ void write_x_row(const RowData &d, int R, uint32_t xs
     w[10] = mask;
   }
 #pragma unroll
-  for (int kc = 0; kc < 4; kc++)
-    tc::sts128(xs + xoff((uint32_t)r, 8u * kc), make_uint4(w[4 * kc], w[4 * kc + 1], w[4 * kc + 2], w[4 * kc + 3]));
+  for (int kc = 0; kc < XL<WIDE>::kCols / 8; kc++)
+    tc::sts128(xs + XL<WIDE>::off((uint32_t)r, 8u * kc),
+               make_uint4(w[4 * kc], w[4 * kc + 1], w[4 * kc + 2], w[4 * kc + 3]));
 }
 
 // Query row qi's row of the second MMA's A operand: [q U_r | hi, lo of both group sums | 1 | 0 ...].
+template <bool WIDE>
 __device__ __forceinline__ void write_qx_row(const AttnParams &p, const AttnChunk &ch, int h, int64_t qi,
                                              uint32_t dst, int r) {
   const int R = ch.rank;
@@ -298,8 +317,9 @@ __device__ __forceinline__ void write_qx_row(const AttnParams &p, const AttnChun
     w[10] = one;
   }
 #pragma unroll
-  for (int kc = 0; kc < 4; kc++)
-    tc::sts128(dst + xoff((uint32_t)r, 8u * kc), make_uint4(w[4 * kc], w[4 * kc + 1], w[4 * kc + 2], w[4 * kc + 3]));
+  for (int kc = 0; kc < XL<WIDE>::kCols / 8; kc++)
+    tc::sts128(dst + XL<WIDE>::off((uint32_t)r, 8u * kc),
+               make_uint4(w[4 * kc], w[4 * kc + 1], w[4 * kc + 2], w[4 * kc + 3]));
 }
 
 // Key (VAL = false) or Value (VAL = true) producer loop of one thread (row r of every tile).
@@ -307,7 +327,7 @@ __device__ __forceinline__ void write_qx_row(const AttnParams &p, const AttnChun
 // tile j+1 into the other stage once tile j-1 has released it, then loads the row data of tile
 // j+2.  Two register sets A and B hold the row data of alternate tiles and the loop body is
 // written twice with the sets swapped, so no register copy waits on a load.
-template <bool VAL>
+template <bool VAL, bool WIDE>
 __device__ __forceinline__ void producer(const AttnParams &p, unsigned char *sm, Bars &bars, int *abort_flag,
                                          uint32_t lut, int h, int64_t q0, int r, int lane) {
   volatile int *abort_v = abort_flag;
@@ -315,7 +335,8 @@ __device__ __forceinline__ void producer(const AttnParams &p, unsigned char *sm,
   uint64_t *full = VAL ? bars.v_full : bars.k_full;
   uint64_t *empty = VAL ? bars.v_empty : bars.k_empty;
   const uint32_t stage0 = tc::smem_u32(sm + (VAL ? OFF_V : OFF_K));
-  const uint32_t xs0 = tc::smem_u32(sm + OFF_X), qx0 = tc::smem_u32(sm + OFF_QX);
+  const uint32_t xs0 = tc::smem_u32(sm + OFF_X), qx0 = tc::smem_u32(sm + XL<WIDE>::kOffQX);
+  constexpr int kXBytes = XL<WIDE>::kBytes;
   // positions (chunk, tile in chunk) of tiles j, j+1, j+2
   int t0 = 0, ti0 = 0, t1 = 0, ti1 = 0, t2 = 0, ti2 = 0;
   auto advance = [&](int &tt, int &ti) {
@@ -341,14 +362,14 @@ __device__ __forceinline__ void producer(const AttnParams &p, unsigned char *sm,
     const AttnChunk &ch = p.ch[t0];
     tc::cp_async_wait<0>();
     __syncwarp();  // the warp's copies of tile j, made visible to every lane
-    decode_row<VAL>(cur, stage0 + (uint32_t)s * 2u * kBlk, r, lut);
+    decode_row<VAL, !WIDE>(cur, stage0 + (uint32_t)s * 2u * kBlk, r, lut);
     if (!VAL) {
-      write_x_row(cur, ch.rank, xs0 + (uint32_t)s * kXBytes, r);
+      write_x_row<WIDE>(cur, ch.rank, xs0 + (uint32_t)s * kXBytes, r);
       if (ti0 == 0) {  // chunk start: the second MMA's A operand for both Query tiles
         if (t0 > 0 && !tc::mbar_wait(&bars.qx_free, (t0 - 1) & 1, kWaitNs)) fail(abort_flag, p.status);
         if (__any_sync(0xffffffffu, *abort_v != 0)) return false;  // warp-uniform exit
-        write_qx_row(p, ch, h, q0 + r, qx0, r);
-        write_qx_row(p, ch, h, q0 + BM + r, qx0 + kXBytes, r);
+        write_qx_row<WIDE>(p, ch, h, q0 + r, qx0, r);
+        write_qx_row<WIDE>(p, ch, h, q0 + BM + r, qx0 + kXBytes, r);
       }
     }
     tc::fence_proxy_async_smem();
@@ -377,13 +398,14 @@ __device__ __forceinline__ void producer(const AttnParams &p, unsigned char *sm,
   tc::cp_async_wait<0>();
 }
 
+template <bool WIDE>
 __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   unsigned char *sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ Bars bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
-  __shared__ __align__(64) uint32_t code_lut[16];
+  __shared__ __align__(64) uint32_t code_lut[WIDE ? 16 : 512];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.y;
   const int64_t q0 = (int64_t)blockIdx.x * (BM * NQT);
@@ -403,7 +425,15 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     *(uint4 *)(sm + OFF_Q + (x * 2 + b) * kBlk + tc::sw128_offset(rr, 8 * (ci % 8))) =
         make_uint4(hw[0], hw[1], hw[2], hw[3]);
   }
-  if (tid < 16) {  // fp16 bits of the code values 0, 1, 2, 3: 0x0000, 0x3C00, 0x4000, 0x4200
+  // code tables; fp16 bits of the code values 0, 1, 2, 3 are 0x0000, 0x3C00, 0x4000, 0x4200
+  if (!WIDE && tid < 256) {  // byte (4 codes) -> two fp16 pairs
+    uint32_t f[4];
+#pragma unroll
+    for (int t = 0; t < 4; t++) f[t] = ((0x42403C00u >> (8 * ((tid >> (2 * t)) & 3))) & 0xFFu) << 8;
+    code_lut[2 * tid] = f[0] | (f[1] << 16);
+    code_lut[2 * tid + 1] = f[2] | (f[3] << 16);
+  }
+  if (WIDE && tid < 16) {  // code pair -> one fp16 pair
     const uint32_t lo = ((0x42403C00u >> (8 * (tid & 3))) & 0xFFu) << 8;
     const uint32_t hi = ((0x42403C00u >> (8 * (tid >> 2))) & 0xFFu) << 8;
     code_lut[tid] = lo | (hi << 16);
@@ -535,7 +565,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
       const uint32_t idesc_pv = tc::idesc_f16_f32_bmn(BM, D);  // V_hat tiles are [key][d]: N-major
       const uint32_t tS[2] = {tmem, tmem + 128u}, tO[2] = {tmem + 256u, tmem + 384u};
       const uint32_t sQ = tc::smem_u32(sm + OFF_Q), sK = tc::smem_u32(sm + OFF_K), sV = tc::smem_u32(sm + OFF_V);
-      const uint32_t sX = tc::smem_u32(sm + OFF_X), sQX = tc::smem_u32(sm + OFF_QX);
+      const uint32_t sX = tc::smem_u32(sm + OFF_X), sQX = tc::smem_u32(sm + XL<WIDE>::kOffQX);
+      constexpr int kXBytes = XL<WIDE>::kBytes;
       int t = 0, tile_in_chunk = 0, prev_stage = 0;
       bool ok = true;
       auto qk = [&](int x, int s, int nx) {
@@ -546,8 +577,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
                      idesc, kk > 0);
         }
         for (int ks = 0; ks < nx; ks++)
-          tc::mma_ss(tS[x], tc::desc_noswz(sQX + x * kXBytes + 256u * ks, 128, 512),
-                     tc::desc_noswz(sX + s * kXBytes + 256u * ks, 128, 512), idesc, 1);
+          tc::mma_ss(tS[x], tc::desc_noswz(sQX + x * kXBytes + 256u * ks, 128, XL<WIDE>::kSbo),
+                     tc::desc_noswz(sX + s * kXBytes + 256u * ks, 128, XL<WIDE>::kSbo), idesc, 1);
       };
       auto pv = [&](int x, int s, bool first) {
 #pragma unroll
@@ -558,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
       for (int j = 0; j < J; j++) {
         const int s = j & 1;
         const AttnChunk &ch = p.ch[t];
-        const int nx = ch.rank <= 8 ? 1 : 2;
+        const int nx = (WIDE && ch.rank > 8) ? 2 : 1;
         ok = tc::mbar_wait(&bars.k_full[s], (j >> 1) & 1, kWaitNs) && !*abort_v;
         if (!ok) break;
         tc::fence_after_sync();
@@ -599,9 +630,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
       if (!tc::mbar_wait(&bars.drain, 0, kWaitNs)) qwm_dev_error(p.status, QWM_ERR_DEVICE_TIMEOUT);
     }
   } else if (warp < kVWarp0) {
-    producer<false>(p, sm, bars, &abort_flag, tc::smem_u32(code_lut), h, q0, tid - 32 * kKWarp0, lane);
+    producer<false, WIDE>(p, sm, bars, &abort_flag, tc::smem_u32(code_lut), h, q0, tid - 32 * kKWarp0, lane);
   } else {
-    producer<true>(p, sm, bars, &abort_flag, tc::smem_u32(code_lut), h, q0, tid - 32 * kVWarp0, lane);
+    producer<true, WIDE>(p, sm, bars, &abort_flag, tc::smem_u32(code_lut), h, q0, tid - 32 * kVWarp0, lane);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -621,6 +652,7 @@ cudaError_t launch_attend(const qwm_config &cfg, const uint16_t *q, int64_t nq, 
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = status;
   int used = 0, tiles = 0;
+  bool wide = false;  // a chunk with PSAC rank above 8: the 32-column second-MMA operands
   for (int i = 0; i < n_chunks; i++) {
     const qwm_chunk &c = chunks[i];
     if (c.n_tokens == 0) continue;  // empty chunks contribute nothing
@@ -631,11 +663,21 @@ cudaError_t launch_attend(const qwm_config &cfg, const uint16_t *q, int64_t nq, 
     a.k_scale = c.k_scale; a.k_min = c.k_min; a.v_scale = c.v_scale; a.v_min = c.v_min;
     a.cent_k16 = c.cent_k16; a.cent_v16 = c.cent_v16; a.c_scale = c.c_scale; a.u_r = c.u_r; a.c = c.c;
     tiles += a.tiles;
+    wide |= a.rank > 8;
   }
   p.n_chunks = used;
   p.total_tiles = tiles;
-  cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
-  if (e != cudaSuccess) return e;
-  attend_tc_kernel<<<dim3((unsigned)((nq + BM * NQT - 1) / (BM * NQT)), cfg.heads), kThreads, SMEM_ALLOC, st>>>(p);
+  const dim3 grid((unsigned)((nq + BM * NQT - 1) / (BM * NQT)), cfg.heads);
+  cudaError_t e;
+  if (wide) {
+    e = cudaFuncSetAttribute(attend_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, XL<true>::kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    attend_tc_kernel<true><<<grid, kThreads, XL<true>::kSmemAlloc, st>>>(p);
+  } else {
+    e = cudaFuncSetAttribute(attend_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             XL<false>::kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    attend_tc_kernel<false><<<grid, kThreads, XL<false>::kSmemAlloc, st>>>(p);
+  }
   return cudaGetLastError();
 }

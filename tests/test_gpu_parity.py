@@ -232,6 +232,21 @@ def test_attend_tiny(q, nq):
         assert err <= 2e-2, err
 
 
+@pytest.mark.parametrize("rank,C,n", [(16, 256, 1024), (12, 128, 777), (5, 64, 300), (0, 256, 513)])
+def test_attend_psac_ranks(q, rank, C, n):
+    """PSAC ranks above 8 take the kernel's 32-column second-MMA operands (ranks 12 and 16, with
+    the coefficient rows read byte by byte for 12); ranks up to 8 the 16-column ones."""
+    ctx, ch = _packed(q, n=n, C=C, rank=rank)
+    H, nq = 2, 300
+    qa = synth.queries(synth.TINY, 1, nq)
+    out = torch.empty(H, nq, D, dtype=torch.float32, device="cuda")
+    q.qwm_attend(ctx, _bf(qa), nq, [ch], 1 / math.sqrt(D), out)
+    assert q.qwm_sync_status(ctx) == 0
+    for h in range(H):
+        ref = oracle.attend_rows(qa[h], np.arange(nq), [chunk_head(ch, h)], 1 / math.sqrt(D))
+        assert _attn_err(out[h].cpu().numpy().astype(np.float64), ref) <= 2e-2
+
+
 def test_attend_several_chunks_mixed_rank(q):
     """A cold-start chunk (no PSAC) followed by PSAC chunks with different bases and a ragged size."""
     w_ = synth.TINY
