@@ -8,14 +8,12 @@
 //
 // Arithmetic.  Both MMAs take fp16 operands (fp32 accumulate): fp16's 11-bit significand keeps the
 // logits of the outlier channels (|k| up to ~40) accurate where bf16 would not, and Q (bf16 in
-// memory) converts to fp16 exactly.  The Key logit is split as
-//   q . k_hat_0 = q . (mu + s q_code) + m_0 sum_{c < 64} q_c + m_1 sum_{c >= 64} q_c,
-// so a Key row is decoded with one fused multiply-add per channel pair, fp16(mu + s q_code), from
-// an fp16 copy of the codebook; the group-offset term rides on a small second MMA whose K columns
-// are [q U_r | hi and lo fp16 parts of the two group sums of q | 1] against
-// [c_hat | m_0 m_0 m_1 m_1 | mask], where mask = -60000 on the zero rows that pad the last tile of
-// a chunk (their probabilities underflow to exactly 0) and 0 elsewhere.  A Value row is decoded as
-// fp16(fp16(mu + m) + s q_code).
+// memory) converts to fp16 exactly.  A Key or Value row is decoded in packed fp16 pairs from an
+// fp16 copy of the codebook as fp16(mu + fp16(m + s q_code)): the small residual first, as in
+// the packing, then the centroid (two roundings, both at the scale of their results).  The PSAC
+// term rides on a small second MMA whose K columns are [q U_r | 0 | 1] against [c_hat | 0 | mask],
+// where mask = -60000 on the zero rows that pad the last tile of a chunk (their probabilities
+// underflow to exactly 0) and 0 elsewhere.
 // O is written in fp32: the output is an average over thousands of keys, its largest entries are
 // ~16x its RMS, and rounding those to bf16 alone would cost ~0.03 x RMS(O).
 //
@@ -180,10 +178,9 @@ __device__ __forceinline__ void issue_warp_copies(const uint16_t *cent16, int h,
   }
 }
 
-// In-place decode of this thread's row: fp16(mu + s q) for Keys, fp16(fp16(mu + m) + s q) for
-// Values.  BYTE_LUT: `lut` maps a byte of 4 codes to two fp16 pairs (8 bytes per entry);
+// In-place decode of this thread's row: fp16(mu + fp16(m + s q)).  BYTE_LUT: `lut` maps a byte of 4 codes to two fp16 pairs (8 bytes per entry);
 // otherwise it maps a 4-bit code pair to one fp16 pair (q_even, q_odd).
-template <bool VAL, bool BYTE_LUT>
+template <bool BYTE_LUT>
 __device__ __forceinline__ void decode_row(const RowData &d, uint32_t stage, int r, uint32_t lut) {
   if (d.idx < 0) return;  // zero-filled by the copies
   const uint32_t rowb = stage + (uint32_t)r * 128u, rx = (uint32_t)r & 7u;
@@ -210,23 +207,16 @@ __device__ __forceinline__ void decode_row(const RowData &d, uint32_t stage, int
         q3 = tc::lds32(lut + ((h16 >> 10) & 0x3Cu));
       }
       uint4 o;
-      if (VAL) {
-        o.x = tc::hfma2(s2, q0, tc::hadd2(mu.x, m2));
-        o.y = tc::hfma2(s2, q1, tc::hadd2(mu.y, m2));
-        o.z = tc::hfma2(s2, q2, tc::hadd2(mu.z, m2));
-        o.w = tc::hfma2(s2, q3, tc::hadd2(mu.w, m2));
-      } else {
-        o.x = tc::hfma2(s2, q0, mu.x);
-        o.y = tc::hfma2(s2, q1, mu.y);
-        o.z = tc::hfma2(s2, q2, mu.z);
-        o.w = tc::hfma2(s2, q3, mu.w);
-      }
+      o.x = tc::hadd2(mu.x, tc::hfma2(s2, q0, m2));
+      o.y = tc::hadd2(mu.y, tc::hfma2(s2, q1, m2));
+      o.z = tc::hadd2(mu.z, tc::hfma2(s2, q2, m2));
+      o.w = tc::hadd2(mu.w, tc::hfma2(s2, q3, m2));
       tc::sts128(addr, o);
     }
   }
 }
 
-// This thread's row of the second MMA's B operand: [c_hat (8 or 16) | m0 m0 m1 m1 | mask | 0 ...].
+// This thread's row of the second MMA's B operand: [c_hat (8 or 16) | 0 0 0 0 | mask | 0 ...].
 template <bool WIDE>
 __device__ __forceinline__ void write_x_row(const RowData &d, int R, uint32_t xs, int r) {
   uint32_t w[16];
@@ -234,7 +224,6 @@ __device__ __forceinline__ void write_x_row(const RowData &d, int R, uint32_t xs
   for (int i = 0; i < 16; i++) w[i] = 0u;
   const float sc = __half2float(__ushort_as_half((uint16_t)d.csc));
   const uint32_t cwd[4] = {d.ca.x, d.ca.y, d.cb.x, d.cb.y};
-  const uint32_t mm0 = __byte_perm(d.mn, 0u, 0x1010u), mm1 = __byte_perm(d.mn, 0u, 0x3232u);
   const uint32_t mask = d.idx >= 0 ? 0u : kMaskBits;
   if (R <= 8) {
 #pragma unroll
@@ -242,8 +231,6 @@ __device__ __forceinline__ void write_x_row(const RowData &d, int R, uint32_t xs
       const uint32_t cv = cwd[i >> 1] >> (16 * (i & 1));
       w[i] = f16pair(sc * (float)(int8_t)(cv & 0xFFu), sc * (float)(int8_t)(cv >> 8));
     }
-    w[4] = mm0;
-    w[5] = mm1;
     w[6] = mask;
   } else {
 #pragma unroll
@@ -251,8 +238,6 @@ __device__ __forceinline__ void write_x_row(const RowData &d, int R, uint32_t xs
       const uint32_t cv = cwd[i >> 1] >> (16 * (i & 1));
       w[i] = f16pair(sc * (float)(int8_t)(cv & 0xFFu), sc * (float)(int8_t)(cv >> 8));
     }
-    w[8] = mm0;
-    w[9] = mm1;
     w[10] = mask;
   }
 #pragma unroll
@@ -261,7 +246,7 @@ __device__ __forceinline__ void write_x_row(const RowData &d, int R, uint32_t xs
                make_uint4(w[4 * kc], w[4 * kc + 1], w[4 * kc + 2], w[4 * kc + 3]));
 }
 
-// Query row qi's row of the second MMA's A operand: [q U_r | hi, lo of both group sums | 1 | 0 ...].
+// Query row qi's row of the second MMA's A operand: [q U_r | 0 0 0 0 | 1 | 0 ...].
 template <bool WIDE>
 __device__ __forceinline__ void write_qx_row(const AttnParams &p, const AttnChunk &ch, int h, int64_t qi,
                                              uint32_t dst, int r) {
@@ -269,7 +254,6 @@ __device__ __forceinline__ void write_qx_row(const AttnParams &p, const AttnChun
   float acc[16];
 #pragma unroll
   for (int k = 0; k < 16; k++) acc[k] = 0.f;
-  float s0 = 0.f, s1 = 0.f;
   const bool live = qi < p.nq;
   if (live) {
     const uint16_t *U = ch.u_r + (int64_t)h * D * R;
@@ -280,8 +264,6 @@ __device__ __forceinline__ void write_qx_row(const AttnParams &p, const AttnChun
 #pragma unroll
       for (int u = 0; u < 8; u++) {
         const float qc = __uint_as_float((u & 1) ? (qw[u >> 1] & 0xFFFF0000u) : (qw[u >> 1] << 16));
-        if (ci < 8) s0 += qc;
-        else s1 += qc;
         const int c = 8 * ci + u;
         if (R == 8) {
           const uint4 uv = *(const uint4 *)(U + c * 8);
@@ -300,20 +282,14 @@ __device__ __forceinline__ void write_qx_row(const AttnParams &p, const AttnChun
   uint32_t w[16];
 #pragma unroll
   for (int i = 0; i < 16; i++) w[i] = 0u;
-  const float h0 = __half2float(__float2half_rn(s0)), h1 = __half2float(__float2half_rn(s1));
-  const uint32_t g0 = f16pair(h0, s0 - h0), g1 = f16pair(h1, s1 - h1);
   const uint32_t one = live ? 0x3C00u : 0u;
   if (R <= 8) {
 #pragma unroll
     for (int i = 0; i < 4; i++) w[i] = f16pair(acc[2 * i], acc[2 * i + 1]);
-    w[4] = g0;
-    w[5] = g1;
     w[6] = one;
   } else {
 #pragma unroll
     for (int i = 0; i < 8; i++) w[i] = f16pair(acc[2 * i], acc[2 * i + 1]);
-    w[8] = g0;
-    w[9] = g1;
     w[10] = one;
   }
 #pragma unroll
@@ -362,7 +338,7 @@ __device__ __forceinline__ void producer(const AttnParams &p, unsigned char *sm,
     const AttnChunk &ch = p.ch[t0];
     tc::cp_async_wait<0>();
     __syncwarp();  // the warp's copies of tile j, made visible to every lane
-    decode_row<VAL, !WIDE>(cur, stage0 + (uint32_t)s * 2u * kBlk, r, lut);
+    decode_row<!WIDE>(cur, stage0 + (uint32_t)s * 2u * kBlk, r, lut);
     if (!VAL) {
       write_x_row<WIDE>(cur, ch.rank, xs0 + (uint32_t)s * kXBytes, r);
       if (ti0 == 0) {  // chunk start: the second MMA's A operand for both Query tiles
