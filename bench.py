@@ -78,21 +78,26 @@ def _peak(d, *names):
 
 
 class ClockSampler:
-    """nvidia-smi SM clock and throttle reasons, sampled every 200 ms while running."""
+    """nvidia-smi SM clock and throttle reasons, sampled every 100 ms while running; `mark()`
+    brackets the timed region and `summary()` keeps the samples taken inside it."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
+        self.window = None
+
+    def mark(self, t0: float, t1: float):
+        self.window = (t0, t1)
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
@@ -109,21 +114,23 @@ class ClockSampler:
             self.lines = [l for l in out.splitlines() if l.strip()]
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
+        import datetime
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for l in getattr(self, "lines", []):
             f = [x.strip() for x in l.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1])); mx = float(f[2])
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(f[2]), float(f[3]), [n for n, v in zip(names, f[6:10]) if v.lower() == "active"]))
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        inside = [r for r in rows if self.window and self.window[0] <= r[0] <= self.window[1]]
+        used, where = (inside, "timed region") if inside else (rows, "warm-up and timed region")
+        sm = [r[1] for r in used]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": used[-1][2] if used else None,
+                "reasons": sorted({n for r in used for n in r[3]}), "samples": len(sm), "window": where}
 
 
 # ---------------------------------------------------------------------------- ranks
@@ -213,6 +220,7 @@ def run_ours(args, rank, world, device):
     # packing 2 (Keys, Values); attention 1
     launches_per_step = 3 + 2 * (1 + 2 * 10) + 2 + 1
 
+    clk = ClockSampler(device.index if device.index is not None else 0).__enter__()
     for _ in range(args.warmup):
         flush.zero_()
         step(Q[last - 1], K[last], V[last], Q[last], out)
@@ -227,17 +235,19 @@ def run_ours(args, rank, world, device):
     stage = np.zeros(4)
     total_ms = 0.0
     barrier(); torch.cuda.synchronize()
-    with ClockSampler(device.index if device.index is not None else 0) as clk:
-        for _ in range(args.steps):
-            flush.zero_()                       # L2 flush between steps, outside the events
-            torch.cuda.nvtx.range_push("qwm_step")
-            step(Q[last - 1], K[last], V[last], Q[last], out)
-            torch.cuda.nvtx.range_pop()
-            ev[4].synchronize()
-            times = [ev[i].elapsed_time(ev[i + 1]) for i in range(4)]
-            stage += times
-            total_ms += sum(times)
-        torch.cuda.synchronize(); barrier()
+    t_begin = time.time()
+    for _ in range(args.steps):
+        flush.zero_()                       # L2 flush between steps, outside the events
+        torch.cuda.nvtx.range_push("qwm_step")
+        step(Q[last - 1], K[last], V[last], Q[last], out)
+        torch.cuda.nvtx.range_pop()
+        ev[4].synchronize()
+        times = [ev[i].elapsed_time(ev[i + 1]) for i in range(4)]
+        stage += times
+        total_ms += sum(times)
+    torch.cuda.synchronize(); barrier()
+    clk.mark(t_begin, time.time())
+    clk.__exit__(None, None, None)
     status = q.qwm_sync_status(ctx)
     assert status == 0, q.qwm_status_string(status)
     ms = total_ms / args.steps
@@ -398,7 +408,7 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")

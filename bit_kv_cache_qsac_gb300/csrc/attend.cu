@@ -131,8 +131,7 @@ __device__ __forceinline__ void load_row(const AttnChunk &c, int h, int C, int64
   d.ca = d.cb = make_uint2(0, 0);
   if (r >= nk) return;
   const int64_t gi = (int64_t)h * c.n + k0 + r;
-  const int ix = (VAL ? c.v_idx : c.k_idx)[gi];
-  d.idx = ix < C ? ix : C - 1;  // never past the codebook
+  d.idx = (VAL ? c.v_idx : c.k_idx)[gi];  // clamped to the codebook where it is used (no wait here)
   d.scl = *(const uint32_t *)((VAL ? c.v_scale : c.k_scale) + gi * 2);
   d.mn = *(const uint32_t *)((VAL ? c.v_min : c.k_min) + gi * 2);
   const uint4 *cp = (const uint4 *)((VAL ? c.v_codes : c.k_codes) + gi * (D / 4));
@@ -170,7 +169,8 @@ __device__ __forceinline__ void issue_warp_copies(const uint16_t *cent16, int h,
 #pragma unroll
   for (int i = 0; i < 16; i++) {
     const int rl = 2 * i + (lane >> 4);
-    const int ix = __shfl_sync(0xffffffffu, idx, rl);
+    int ix = __shfl_sync(0xffffffffu, idx, rl);
+    ix = ix < C ? ix : C - 1;  // never past the codebook
     const uint32_t row = (uint32_t)(rbase + rl);
     const uint32_t dst = stage + (v >> 3) * kBlk + row * 128u + (((v & 7u) ^ (row & 7u)) << 4);
     const uint16_t *src = cent16 + ((int64_t)h * C + (ix >= 0 ? ix : 0)) * D + 8 * v;
@@ -184,34 +184,46 @@ template <bool BYTE_LUT>
 __device__ __forceinline__ void decode_row(const RowData &d, uint32_t stage, int r, uint32_t lut) {
   if (d.idx < 0) return;  // zero-filled by the copies
   const uint32_t rowb = stage + (uint32_t)r * 128u, rx = (uint32_t)r & 7u;
+  // four 8-channel chunks per batch: every shared-memory load of the batch is issued before any
+  // arithmetic, so the batch costs one load latency (the accesses are ordered volatile asm)
 #pragma unroll
-  for (int g = 0; g < 2; g++) {
+  for (int b = 0; b < 4; b++) {
+    const int g = b >> 1;
     const uint32_t s2 = __byte_perm(d.scl, 0u, g ? 0x3232u : 0x1010u);
     const uint32_t m2 = __byte_perm(d.mn, 0u, g ? 0x3232u : 0x1010u);
     const uint4 cw = g ? d.c1 : d.c0;
-    const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+    const uint32_t w2[2] = {(b & 1) ? cw.z : cw.x, (b & 1) ? cw.w : cw.y};  // 32 channels of codes
+    uint32_t q[4][4];
+    uint4 mu[4];
+    uint32_t addr[4];
 #pragma unroll
-    for (int v = 0; v < 8; v++) {
-      const uint32_t addr = rowb + (uint32_t)g * kBlk + ((((uint32_t)v) ^ rx) << 4);
-      const uint4 mu = tc::lds128(addr);
-      const uint32_t h16 = words[v >> 1] >> (16 * (v & 1));
-      uint32_t q0, q1, q2, q3;
+    for (int u = 0; u < 4; u++) {
+      const uint32_t h16 = w2[u >> 1] >> (16 * (u & 1));
       if (BYTE_LUT) {
         const uint2 qa = tc::lds64(lut + ((h16 << 3) & 0x7F8u));
         const uint2 qb = tc::lds64(lut + ((h16 >> 5) & 0x7F8u));
-        q0 = qa.x; q1 = qa.y; q2 = qb.x; q3 = qb.y;
+        q[u][0] = qa.x; q[u][1] = qa.y; q[u][2] = qb.x; q[u][3] = qb.y;
       } else {
-        q0 = tc::lds32(lut + ((h16 << 2) & 0x3Cu));
-        q1 = tc::lds32(lut + ((h16 >> 2) & 0x3Cu));
-        q2 = tc::lds32(lut + ((h16 >> 6) & 0x3Cu));
-        q3 = tc::lds32(lut + ((h16 >> 10) & 0x3Cu));
+        q[u][0] = tc::lds32(lut + ((h16 << 2) & 0x3Cu));
+        q[u][1] = tc::lds32(lut + ((h16 >> 2) & 0x3Cu));
+        q[u][2] = tc::lds32(lut + ((h16 >> 6) & 0x3Cu));
+        q[u][3] = tc::lds32(lut + ((h16 >> 10) & 0x3Cu));
       }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const uint32_t v = (uint32_t)(4 * (b & 1) + u);  // chunk inside the 64-channel block
+      addr[u] = rowb + (uint32_t)g * kBlk + ((v ^ rx) << 4);
+      mu[u] = tc::lds128(addr[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
       uint4 o;
-      o.x = tc::hadd2(mu.x, tc::hfma2(s2, q0, m2));
-      o.y = tc::hadd2(mu.y, tc::hfma2(s2, q1, m2));
-      o.z = tc::hadd2(mu.z, tc::hfma2(s2, q2, m2));
-      o.w = tc::hadd2(mu.w, tc::hfma2(s2, q3, m2));
-      tc::sts128(addr, o);
+      o.x = tc::hadd2(mu[u].x, tc::hfma2(s2, q[u][0], m2));
+      o.y = tc::hadd2(mu[u].y, tc::hfma2(s2, q[u][1], m2));
+      o.z = tc::hadd2(mu[u].z, tc::hfma2(s2, q[u][2], m2));
+      o.w = tc::hadd2(mu[u].w, tc::hfma2(s2, q[u][3], m2));
+      tc::sts128(addr[u], o);
     }
   }
 }
