@@ -184,46 +184,34 @@ template <bool BYTE_LUT>
 __device__ __forceinline__ void decode_row(const RowData &d, uint32_t stage, int r, uint32_t lut) {
   if (d.idx < 0) return;  // zero-filled by the copies
   const uint32_t rowb = stage + (uint32_t)r * 128u, rx = (uint32_t)r & 7u;
-  // four 8-channel chunks per batch: every shared-memory load of the batch is issued before any
-  // arithmetic, so the batch costs one load latency (the accesses are ordered volatile asm)
 #pragma unroll
-  for (int b = 0; b < 4; b++) {
-    const int g = b >> 1;
+  for (int g = 0; g < 2; g++) {
     const uint32_t s2 = __byte_perm(d.scl, 0u, g ? 0x3232u : 0x1010u);
     const uint32_t m2 = __byte_perm(d.mn, 0u, g ? 0x3232u : 0x1010u);
     const uint4 cw = g ? d.c1 : d.c0;
-    const uint32_t w2[2] = {(b & 1) ? cw.z : cw.x, (b & 1) ? cw.w : cw.y};  // 32 channels of codes
-    uint32_t q[4][4];
-    uint4 mu[4];
-    uint32_t addr[4];
+    const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
-    for (int u = 0; u < 4; u++) {
-      const uint32_t h16 = w2[u >> 1] >> (16 * (u & 1));
+    for (int v = 0; v < 8; v++) {
+      const uint32_t addr = rowb + (uint32_t)g * kBlk + ((((uint32_t)v) ^ rx) << 4);
+      const uint4 mu = tc::lds128(addr);
+      const uint32_t h16 = words[v >> 1] >> (16 * (v & 1));
+      uint32_t q0, q1, q2, q3;
       if (BYTE_LUT) {
         const uint2 qa = tc::lds64(lut + ((h16 << 3) & 0x7F8u));
         const uint2 qb = tc::lds64(lut + ((h16 >> 5) & 0x7F8u));
-        q[u][0] = qa.x; q[u][1] = qa.y; q[u][2] = qb.x; q[u][3] = qb.y;
+        q0 = qa.x; q1 = qa.y; q2 = qb.x; q3 = qb.y;
       } else {
-        q[u][0] = tc::lds32(lut + ((h16 << 2) & 0x3Cu));
-        q[u][1] = tc::lds32(lut + ((h16 >> 2) & 0x3Cu));
-        q[u][2] = tc::lds32(lut + ((h16 >> 6) & 0x3Cu));
-        q[u][3] = tc::lds32(lut + ((h16 >> 10) & 0x3Cu));
+        q0 = tc::lds32(lut + ((h16 << 2) & 0x3Cu));
+        q1 = tc::lds32(lut + ((h16 >> 2) & 0x3Cu));
+        q2 = tc::lds32(lut + ((h16 >> 6) & 0x3Cu));
+        q3 = tc::lds32(lut + ((h16 >> 10) & 0x3Cu));
       }
-    }
-#pragma unroll
-    for (int u = 0; u < 4; u++) {
-      const uint32_t v = (uint32_t)(4 * (b & 1) + u);  // chunk inside the 64-channel block
-      addr[u] = rowb + (uint32_t)g * kBlk + ((v ^ rx) << 4);
-      mu[u] = tc::lds128(addr[u]);
-    }
-#pragma unroll
-    for (int u = 0; u < 4; u++) {
       uint4 o;
-      o.x = tc::hadd2(mu[u].x, tc::hfma2(s2, q[u][0], m2));
-      o.y = tc::hadd2(mu[u].y, tc::hfma2(s2, q[u][1], m2));
-      o.z = tc::hadd2(mu[u].z, tc::hfma2(s2, q[u][2], m2));
-      o.w = tc::hadd2(mu[u].w, tc::hfma2(s2, q[u][3], m2));
-      tc::sts128(addr[u], o);
+      o.x = tc::hadd2(mu.x, tc::hfma2(s2, q0, m2));
+      o.y = tc::hadd2(mu.y, tc::hfma2(s2, q1, m2));
+      o.z = tc::hadd2(mu.z, tc::hfma2(s2, q2, m2));
+      o.w = tc::hadd2(mu.w, tc::hfma2(s2, q3, m2));
+      tc::sts128(addr, o);
     }
   }
 }
@@ -258,24 +246,25 @@ __device__ __forceinline__ void write_x_row(const RowData &d, int R, uint32_t xs
                make_uint4(w[4 * kc], w[4 * kc + 1], w[4 * kc + 2], w[4 * kc + 3]));
 }
 
-// Query row qi's row of the second MMA's A operand: [q U_r | 0 0 0 0 | 1 | 0 ...].
+// Query row rr of Query tile x: its row of the second MMA's A operand, [q U_r | 0 0 0 0 | 1 | 0 ...],
+// with q read from the tile's fp16 copy in shared memory (exact: bf16 Queries convert to fp16
+// exactly) and U_r (bf16, the chunk's basis) from global memory (a few KB, L1-resident).
 template <bool WIDE>
-__device__ __forceinline__ void write_qx_row(const AttnParams &p, const AttnChunk &ch, int h, int64_t qi,
-                                             uint32_t dst, int r) {
+__device__ __forceinline__ void write_qx_row(const AttnChunk &ch, int h, bool live, uint32_t qtile, uint32_t dst,
+                                             int rr) {
   const int R = ch.rank;
   float acc[16];
 #pragma unroll
   for (int k = 0; k < 16; k++) acc[k] = 0.f;
-  const bool live = qi < p.nq;
-  if (live) {
+  if (live && R > 0) {
     const uint16_t *U = ch.u_r + (int64_t)h * D * R;
-    const uint4 *qrow = (const uint4 *)(p.q + ((int64_t)h * p.nq + qi) * D);
+#pragma unroll 1
     for (int ci = 0; ci < D / 8; ci++) {
-      const uint4 qv = qrow[ci];
+      const uint4 qv = tc::lds128(qtile + (uint32_t)(ci / 8) * kBlk + tc::sw128_offset(rr, 8 * (ci % 8)));
       const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
       for (int u = 0; u < 8; u++) {
-        const float qc = __uint_as_float((u & 1) ? (qw[u >> 1] & 0xFFFF0000u) : (qw[u >> 1] << 16));
+        const float qc = __half2float(__ushort_as_half((uint16_t)(qw[u >> 1] >> (16 * (u & 1)))));
         const int c = 8 * ci + u;
         if (R == 8) {
           const uint4 uv = *(const uint4 *)(U + c * 8);
@@ -306,7 +295,7 @@ __device__ __forceinline__ void write_qx_row(const AttnParams &p, const AttnChun
   }
 #pragma unroll
   for (int kc = 0; kc < XL<WIDE>::kCols / 8; kc++)
-    tc::sts128(dst + XL<WIDE>::off((uint32_t)r, 8u * kc),
+    tc::sts128(dst + XL<WIDE>::off((uint32_t)rr, 8u * kc),
                make_uint4(w[4 * kc], w[4 * kc + 1], w[4 * kc + 2], w[4 * kc + 3]));
 }
 
@@ -356,8 +345,9 @@ __device__ __forceinline__ void producer(const AttnParams &p, unsigned char *sm,
       if (ti0 == 0) {  // chunk start: the second MMA's A operand for both Query tiles
         if (t0 > 0 && !tc::mbar_wait(&bars.qx_free, (t0 - 1) & 1, kWaitNs)) fail(abort_flag, p.status);
         if (__any_sync(0xffffffffu, *abort_v != 0)) return false;  // warp-uniform exit
-        write_qx_row<WIDE>(p, ch, h, q0 + r, qx0, r);
-        write_qx_row<WIDE>(p, ch, h, q0 + BM + r, qx0 + kXBytes, r);
+        const uint32_t sq = tc::smem_u32(sm + OFF_Q);
+        write_qx_row<WIDE>(ch, h, q0 + r < p.nq, sq, qx0, r);
+        write_qx_row<WIDE>(ch, h, q0 + BM + r < p.nq, sq + 2u * kBlk, qx0 + kXBytes, r);
       }
     }
     tc::fence_proxy_async_smem();
