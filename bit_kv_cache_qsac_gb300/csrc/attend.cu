@@ -23,14 +23,13 @@
 //                   logits from TMEM, keeps the running max and sum, writes P (fp16) over the
 //                   logits, rescales O in TMEM when the max grows by more than 2^8;
 //   warp 8          allocates TMEM and issues every tcgen05.mma (one thread);
-//   warps 9-16      producers: thread = one 64-channel group of one key row; per tile the
-//                   warps copy the centroid rows (cp.async, two whole rows per instruction) into
-//                   the 128-byte-swizzled stages, decode the Key tile in place (K-major for
-//                   Q K^T), write the second MMA's B operand, then decode the Value tile ([key][d],
-//                   read as an N-major B); at each chunk start they build the second MMA's A
-//                   operand for both Query tiles from the fp16 Query tiles.
-// Each producer thread keeps its half row's index data two tiles ahead in registers and the
-// centroid copies one tile ahead in the other shared-memory stage.
+//   warps 9-12      Key producers: thread = key row of the tile; copies the row's centroid
+//                   (cp.async, 16 bytes at a time) into the 128-byte-swizzled K-major stage,
+//                   decodes it in place, writes the row of the second MMA's B operand, and at
+//                   each chunk start builds the second MMA's A operand for both Query tiles;
+//   warps 13-16     Value producers: the same for V_hat rows ([key][d], read as an N-major B).
+// Each producer thread keeps its row's index data two tiles ahead in registers and its centroid
+// copies one tile ahead in the other shared-memory stage.
 // Tensor memory (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each; P_x overlays S_x.
 // MMA order per tile j: S0(j), PV1(j-1), S1(j), PV0(j).  tcgen05 operations complete in issue
 // order, so the commit after S_x(j) also certifies PV_x(j-1): when softmax x sees S_x(j), O_x
@@ -46,8 +45,8 @@ namespace {
 
 constexpr int D = QWM_D;
 constexpr int BM = 128, BN = 128, NQT = 2;
-constexpr int kSoftmaxWarps = 8, kMmaWarp = 8, kProdWarp0 = 9, kProdWarps = 8;
-constexpr int kThreads = 32 * (kSoftmaxWarps + 1 + kProdWarps);  // 544
+constexpr int kSoftmaxWarps = 8, kMmaWarp = 8, kKWarp0 = 9, kVWarp0 = 13, kProdWarps = 4;
+constexpr int kThreads = 32 * (kSoftmaxWarps + 1 + 2 * kProdWarps);  // 544
 constexpr int kMaxChunks = 128;
 constexpr uint64_t kWaitNs = 1000000000ull;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
@@ -101,14 +100,13 @@ struct Bars {
   uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_ready[2], qx_free, o_done, drain;
 };
 
-// Index data of one 64-channel group of one key row (the half row one producer thread decodes):
-// the group's fp16 scale (low half) and offset (high half), its 64 2-bit codes, and for the Key
-// row's group-0 thread the PSAC coefficients and their scale.
-struct HalfRow {
-  int idx;  // centroid (not yet clamped), or -1 for a row past the end of the chunk
-  uint32_t sm;
-  uint4 codes;
-  uint2 ca, cb;  // coefficients 0-7 and 8-15 (Keys, group 0)
+// Index data of one key row: fp16 scale and offset pairs (group 0 low half), 128 2-bit codes,
+// and (Keys) the PSAC coefficients and their scale.
+struct RowData {
+  int idx;  // centroid, or -1 for a row past the end of the chunk
+  uint32_t scl, mn;
+  uint4 c0, c1;
+  uint2 ca, cb;  // coefficients 0-7 and 8-15
   uint32_t csc;
 };
 
@@ -126,17 +124,20 @@ __device__ __forceinline__ uint64_t pk64(uint32_t lo, uint32_t hi) {
 }
 
 template <bool VAL>
-__device__ __forceinline__ void load_half(const AttnChunk &c, int h, int64_t k0, int nk, int r, int g, HalfRow &d) {
+__device__ __forceinline__ void load_row(const AttnChunk &c, int h, int C, int64_t k0, int nk, int r, RowData &d) {
   d.idx = -1;
-  d.sm = d.csc = 0u;
-  d.codes = make_uint4(0, 0, 0, 0);
+  d.scl = d.mn = d.csc = 0u;
+  d.c0 = d.c1 = make_uint4(0, 0, 0, 0);
   d.ca = d.cb = make_uint2(0, 0);
   if (r >= nk) return;
   const int64_t gi = (int64_t)h * c.n + k0 + r;
   d.idx = (VAL ? c.v_idx : c.k_idx)[gi];  // clamped to the codebook where it is used (no wait here)
-  d.sm = (uint32_t)(VAL ? c.v_scale : c.k_scale)[gi * 2 + g] | ((uint32_t)(VAL ? c.v_min : c.k_min)[gi * 2 + g] << 16);
-  d.codes = *(const uint4 *)((VAL ? c.v_codes : c.k_codes) + gi * (D / 4) + 16 * g);
-  if (!VAL && g == 0 && c.rank > 0) {
+  d.scl = *(const uint32_t *)((VAL ? c.v_scale : c.k_scale) + gi * 2);
+  d.mn = *(const uint32_t *)((VAL ? c.v_min : c.k_min) + gi * 2);
+  const uint4 *cp = (const uint4 *)((VAL ? c.v_codes : c.k_codes) + gi * (D / 4));
+  d.c0 = cp[0];
+  d.c1 = cp[1];
+  if (!VAL && c.rank > 0) {
     const int R = c.rank;
     const int8_t *src = c.c + gi * R;
     if (R == 8) {
@@ -157,18 +158,18 @@ __device__ __forceinline__ void load_half(const AttnChunk &c, int h, int64_t k0,
   }
 }
 
-// Centroid rows of this warp's 16 tile rows (rbase .. rbase + 15) -> a swizzled stage.  Lane
-// 2 k + g holds row rbase + k's centroid in `idx` (< 0: zeros).  Each copy instruction moves two
-// whole rows (lanes 0-15 and 16-31, 16 bytes each), so a row is fetched as two full 128-byte
-// lines.  The caller makes the copies visible to the other lanes (wait_group, then __syncwarp)
-// before any lane reads them.
+// Centroid rows of this warp's 32 tile rows (rbase .. rbase + 31) -> a swizzled stage; `idx` is
+// the calling lane's row's centroid (< 0: zeros).  Each copy instruction moves two whole rows
+// (lanes 0-15 and 16-31, 16 bytes each), so a row is fetched as two full 128-byte lines.
+// The caller makes the copies visible to the other lanes (wait_group, then __syncwarp) before
+// any lane reads them.
 __device__ __forceinline__ void issue_warp_copies(const uint16_t *cent16, int h, int C, int idx, uint32_t stage,
                                                   int rbase, int lane) {
   const uint32_t v = (uint32_t)lane & 15u;
 #pragma unroll
-  for (int i = 0; i < 8; i++) {
+  for (int i = 0; i < 16; i++) {
     const int rl = 2 * i + (lane >> 4);
-    int ix = __shfl_sync(0xffffffffu, idx, 2 * rl);
+    int ix = __shfl_sync(0xffffffffu, idx, rl);
     ix = ix < C ? ix : C - 1;  // never past the codebook
     const uint32_t row = (uint32_t)(rbase + rl);
     const uint32_t dst = stage + (v >> 3) * kBlk + row * 128u + (((v & 7u) ^ (row & 7u)) << 4);
@@ -177,44 +178,47 @@ __device__ __forceinline__ void issue_warp_copies(const uint16_t *cent16, int h,
   }
 }
 
-// In-place decode of group g of row r: fp16(mu + fp16(m + s q)).  BYTE_LUT: `lut` maps a byte of
-// 4 codes to two fp16 pairs (8 bytes per entry); otherwise it maps a 4-bit code pair to one fp16
-// pair (q_even, q_odd).
+// In-place decode of this thread's row: fp16(mu + fp16(m + s q)).  BYTE_LUT: `lut` maps a byte of 4 codes to two fp16 pairs (8 bytes per entry);
+// otherwise it maps a 4-bit code pair to one fp16 pair (q_even, q_odd).
 template <bool BYTE_LUT>
-__device__ __forceinline__ void decode_half(const HalfRow &d, uint32_t stage, int r, int g, uint32_t lut) {
+__device__ __forceinline__ void decode_row(const RowData &d, uint32_t stage, int r, uint32_t lut) {
   if (d.idx < 0) return;  // zero-filled by the copies
-  const uint32_t rowb = stage + (uint32_t)g * kBlk + (uint32_t)r * 128u, rx = (uint32_t)r & 7u;
-  const uint32_t s2 = __byte_perm(d.sm, 0u, 0x1010u), m2 = __byte_perm(d.sm, 0u, 0x3232u);
-  const uint32_t words[4] = {d.codes.x, d.codes.y, d.codes.z, d.codes.w};
+  const uint32_t rowb = stage + (uint32_t)r * 128u, rx = (uint32_t)r & 7u;
 #pragma unroll
-  for (int v = 0; v < 8; v++) {
-    const uint32_t addr = rowb + ((((uint32_t)v) ^ rx) << 4);
-    const uint4 mu = tc::lds128(addr);
-    const uint32_t h16 = words[v >> 1] >> (16 * (v & 1));
-    uint32_t q0, q1, q2, q3;
-    if (BYTE_LUT) {
-      const uint2 qa = tc::lds64(lut + ((h16 << 3) & 0x7F8u));
-      const uint2 qb = tc::lds64(lut + ((h16 >> 5) & 0x7F8u));
-      q0 = qa.x; q1 = qa.y; q2 = qb.x; q3 = qb.y;
-    } else {
-      q0 = tc::lds32(lut + ((h16 << 2) & 0x3Cu));
-      q1 = tc::lds32(lut + ((h16 >> 2) & 0x3Cu));
-      q2 = tc::lds32(lut + ((h16 >> 6) & 0x3Cu));
-      q3 = tc::lds32(lut + ((h16 >> 10) & 0x3Cu));
+  for (int g = 0; g < 2; g++) {
+    const uint32_t s2 = __byte_perm(d.scl, 0u, g ? 0x3232u : 0x1010u);
+    const uint32_t m2 = __byte_perm(d.mn, 0u, g ? 0x3232u : 0x1010u);
+    const uint4 cw = g ? d.c1 : d.c0;
+    const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+    for (int v = 0; v < 8; v++) {
+      const uint32_t addr = rowb + (uint32_t)g * kBlk + ((((uint32_t)v) ^ rx) << 4);
+      const uint4 mu = tc::lds128(addr);
+      const uint32_t h16 = words[v >> 1] >> (16 * (v & 1));
+      uint32_t q0, q1, q2, q3;
+      if (BYTE_LUT) {
+        const uint2 qa = tc::lds64(lut + ((h16 << 3) & 0x7F8u));
+        const uint2 qb = tc::lds64(lut + ((h16 >> 5) & 0x7F8u));
+        q0 = qa.x; q1 = qa.y; q2 = qb.x; q3 = qb.y;
+      } else {
+        q0 = tc::lds32(lut + ((h16 << 2) & 0x3Cu));
+        q1 = tc::lds32(lut + ((h16 >> 2) & 0x3Cu));
+        q2 = tc::lds32(lut + ((h16 >> 6) & 0x3Cu));
+        q3 = tc::lds32(lut + ((h16 >> 10) & 0x3Cu));
+      }
+      uint4 o;
+      o.x = tc::hadd2(mu.x, tc::hfma2(s2, q0, m2));
+      o.y = tc::hadd2(mu.y, tc::hfma2(s2, q1, m2));
+      o.z = tc::hadd2(mu.z, tc::hfma2(s2, q2, m2));
+      o.w = tc::hadd2(mu.w, tc::hfma2(s2, q3, m2));
+      tc::sts128(addr, o);
     }
-    uint4 o;
-    o.x = tc::hadd2(mu.x, tc::hfma2(s2, q0, m2));
-    o.y = tc::hadd2(mu.y, tc::hfma2(s2, q1, m2));
-    o.z = tc::hadd2(mu.z, tc::hfma2(s2, q2, m2));
-    o.w = tc::hadd2(mu.w, tc::hfma2(s2, q3, m2));
-    tc::sts128(addr, o);
   }
 }
 
-// Row r of the second MMA's B operand: [c_hat (8 or 16) | 0 0 0 0 | mask | 0 ...] (from the Key
-// row's group-0 data).
+// This thread's row of the second MMA's B operand: [c_hat (8 or 16) | 0 0 0 0 | mask | 0 ...].
 template <bool WIDE>
-__device__ __forceinline__ void write_x_row(const HalfRow &d, int R, uint32_t xs, int r) {
+__device__ __forceinline__ void write_x_row(const RowData &d, int R, uint32_t xs, int r) {
   uint32_t w[16];
 #pragma unroll
   for (int i = 0; i < 16; i++) w[i] = 0u;
@@ -295,97 +299,79 @@ __device__ __forceinline__ void write_qx_row(const AttnChunk &ch, int h, bool li
                make_uint4(w[4 * kc], w[4 * kc + 1], w[4 * kc + 2], w[4 * kc + 3]));
 }
 
-// Producer loop of one thread: group g of row r of every Key and Value tile (the 8 producer warps
-// share each tile, 16 rows per warp).  Step j decodes Key tile j (the MMAs wait on it first),
-// then issues Key tile j+1's copies into the other stage once Key tile j-1 has released it, then
-// decodes Value tile j, then issues Value tile j+1's copies once Value tile j-1 is released, then
-// loads the row data of tile j+2.  Two register sets A and B hold the row data of alternate
-// tiles and the loop body is written twice with the sets swapped, so no register copy waits on a
-// load.
-template <bool WIDE>
+// Key (VAL = false) or Value (VAL = true) producer loop of one thread (row r of every tile).
+// Step j decodes tile j (its copies were issued one step earlier), then issues the copies of
+// tile j+1 into the other stage once tile j-1 has released it, then loads the row data of tile
+// j+2.  Two register sets A and B hold the row data of alternate tiles and the loop body is
+// written twice with the sets swapped, so no register copy waits on a load.
+template <bool VAL, bool WIDE>
 __device__ __forceinline__ void producer(const AttnParams &p, unsigned char *sm, Bars &bars, int *abort_flag,
-                                         uint32_t lut, int h, int64_t q0, int pt, int lane) {
+                                         uint32_t lut, int h, int64_t q0, int r, int lane) {
   volatile int *abort_v = abort_flag;
-  const int J = p.total_tiles, C = p.C;
-  const int r = pt >> 1, g = pt & 1, rbase = (pt - lane) >> 1;
-  const uint32_t sK = tc::smem_u32(sm + OFF_K), sV = tc::smem_u32(sm + OFF_V);
+  const int J = p.total_tiles, C = p.C, rbase = r - lane;
+  uint64_t *full = VAL ? bars.v_full : bars.k_full;
+  uint64_t *empty = VAL ? bars.v_empty : bars.k_empty;
+  const uint32_t stage0 = tc::smem_u32(sm + (VAL ? OFF_V : OFF_K));
   const uint32_t xs0 = tc::smem_u32(sm + OFF_X), qx0 = tc::smem_u32(sm + XL<WIDE>::kOffQX);
-  const uint32_t sQ = tc::smem_u32(sm + OFF_Q);
   constexpr int kXBytes = XL<WIDE>::kBytes;
   // positions (chunk, tile in chunk) of tiles j, j+1, j+2
   int t0 = 0, ti0 = 0, t1 = 0, ti1 = 0, t2 = 0, ti2 = 0;
   auto advance = [&](int &tt, int &ti) {
     if (++ti == p.ch[tt].tiles) { ti = 0; tt++; }
   };
-  auto load_at = [&](int tt, int ti, HalfRow &dk, HalfRow &dv) {
+  auto load_at = [&](int tt, int ti, RowData &d) {
     const AttnChunk &c = p.ch[tt];
     const int64_t k0 = (int64_t)ti * BN;
     const int nk = (c.n - k0) < BN ? (int)(c.n - k0) : BN;
-    load_half<false>(c, h, k0, nk, r, g, dk);
-    load_half<true>(c, h, k0, nk, r, g, dv);
+    load_row<VAL>(c, h, C, k0, nk, r, d);
   };
-  HalfRow AK, AV, BK, BV;
-  BK.idx = BV.idx = -1;
-  load_at(0, 0, AK, AV);
+  RowData A, B;
+  B.idx = -1;
+  load_at(0, 0, A);
   if (J > 1) {
     advance(t1, ti1);
-    load_at(t1, ti1, BK, BV);
+    load_at(t1, ti1, B);
   }
-  issue_warp_copies(p.ch[0].cent_k16, h, C, AK.idx, sK, rbase, lane);
-  issue_warp_copies(p.ch[0].cent_v16, h, C, AV.idx, sV, rbase, lane);
+  issue_warp_copies(VAL ? p.ch[0].cent_v16 : p.ch[0].cent_k16, h, C, A.idx, stage0, rbase, lane);
   tc::cp_async_commit();
-  auto uniform_abort = [&]() { return __any_sync(0xffffffffu, *abort_v != 0); };
-  auto step = [&](int j, HalfRow &ck, HalfRow &cv, const HalfRow &nk_, const HalfRow &nv_) -> bool {
+  auto step = [&](int j, RowData &cur, const RowData &nxt) -> bool {
     const int s = j & 1;
     const AttnChunk &ch = p.ch[t0];
-    // ---- Key tile j ----
-    if (j == 0) tc::cp_async_wait<0>();
-    else tc::cp_async_wait<1>();  // all but the newest group (Value tile j's copies may be pending)
-    __syncwarp();                 // the warp's copies, made visible to every lane
-    decode_half<!WIDE>(ck, sK + (uint32_t)s * 2u * kBlk, r, g, lut);
-    if (g == 0) write_x_row<WIDE>(ck, ch.rank, xs0 + (uint32_t)s * kXBytes, r);
-    if (ti0 == 0) {  // chunk start: the second MMA's A operand, one Query row per thread
-      if (t0 > 0 && !tc::mbar_wait(&bars.qx_free, (t0 - 1) & 1, kWaitNs)) fail(abort_flag, p.status);
-      if (uniform_abort()) return false;
-      const int x = pt >> 7, rr = pt & 127;
-      write_qx_row<WIDE>(ch, h, q0 + (int64_t)pt < p.nq, sQ + (uint32_t)x * 2u * kBlk, qx0 + (uint32_t)x * kXBytes,
-                         rr);
+    tc::cp_async_wait<0>();
+    __syncwarp();  // the warp's copies of tile j, made visible to every lane
+    decode_row<!WIDE>(cur, stage0 + (uint32_t)s * 2u * kBlk, r, lut);
+    if (!VAL) {
+      write_x_row<WIDE>(cur, ch.rank, xs0 + (uint32_t)s * kXBytes, r);
+      if (ti0 == 0) {  // chunk start: the second MMA's A operand for both Query tiles
+        if (t0 > 0 && !tc::mbar_wait(&bars.qx_free, (t0 - 1) & 1, kWaitNs)) fail(abort_flag, p.status);
+        if (__any_sync(0xffffffffu, *abort_v != 0)) return false;  // warp-uniform exit
+        const uint32_t sq = tc::smem_u32(sm + OFF_Q);
+        write_qx_row<WIDE>(ch, h, q0 + r < p.nq, sq, qx0, r);
+        write_qx_row<WIDE>(ch, h, q0 + BM + r < p.nq, sq + 2u * kBlk, qx0 + kXBytes, r);
+      }
     }
     tc::fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) tc::mbar_arrive(&bars.k_full[s]);
-    if (j + 1 < J) {  // Key tile j+1's copies once Key tile j-1 has released the other stage
-      if (j >= 1 && !tc::mbar_wait(&bars.k_empty[s ^ 1], ((j - 1) >> 1) & 1, kWaitNs)) fail(abort_flag, p.status);
-      if (uniform_abort()) return false;
-      issue_warp_copies(p.ch[t1].cent_k16, h, C, nk_.idx, sK + (uint32_t)(s ^ 1) * 2u * kBlk, rbase, lane);
-      tc::cp_async_commit();
-    }
-    // ---- Value tile j ----
-    if (j + 1 < J) tc::cp_async_wait<1>();  // all but Key tile j+1's copies
-    else tc::cp_async_wait<0>();
-    __syncwarp();
-    decode_half<!WIDE>(cv, sV + (uint32_t)s * 2u * kBlk, r, g, lut);
-    tc::fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) tc::mbar_arrive(&bars.v_full[s]);
-    if (j + 1 < J) {  // Value tile j+1's copies once Value tile j-1 has released the other stage
-      if (j >= 1 && !tc::mbar_wait(&bars.v_empty[s ^ 1], ((j - 1) >> 1) & 1, kWaitNs)) fail(abort_flag, p.status);
-      if (uniform_abort()) return false;
-      issue_warp_copies(p.ch[t1].cent_v16, h, C, nv_.idx, sV + (uint32_t)(s ^ 1) * 2u * kBlk, rbase, lane);
+    if (lane == 0) tc::mbar_arrive(&full[s]);
+    if (j + 1 < J) {  // copies of tile j+1 into the other stage once tile j-1 has released it
+      if (j >= 1 && !tc::mbar_wait(&empty[s ^ 1], ((j - 1) >> 1) & 1, kWaitNs)) fail(abort_flag, p.status);
+      if (__any_sync(0xffffffffu, *abort_v != 0)) return false;  // warp-uniform exit
+      issue_warp_copies(VAL ? p.ch[t1].cent_v16 : p.ch[t1].cent_k16, h, C, nxt.idx,
+                        stage0 + (uint32_t)(s ^ 1) * 2u * kBlk, rbase, lane);
       tc::cp_async_commit();
     }
     t2 = t1; ti2 = ti1;
     if (j + 2 < J) {  // row data of tile j+2 (decoded two steps from now)
       advance(t2, ti2);
-      load_at(t2, ti2, ck, cv);
+      load_at(t2, ti2, cur);
     }
     t0 = t1; ti0 = ti1;
     t1 = t2; ti1 = ti2;
     return true;
   };
   for (int j = 0; j < J; j += 2) {
-    if (!step(j, AK, AV, BK, BV)) break;
-    if (j + 1 < J && !step(j + 1, BK, BV, AK, AV)) break;
+    if (!step(j, A, B)) break;
+    if (j + 1 < J && !step(j + 1, B, A)) break;
   }
   tc::cp_async_wait<0>();
 }
@@ -621,8 +607,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
       tc::mma_commit(&bars.drain);
       if (!tc::mbar_wait(&bars.drain, 0, kWaitNs)) qwm_dev_error(p.status, QWM_ERR_DEVICE_TIMEOUT);
     }
+  } else if (warp < kVWarp0) {
+    producer<false, WIDE>(p, sm, bars, &abort_flag, tc::smem_u32(code_lut), h, q0, tid - 32 * kKWarp0, lane);
   } else {
-    producer<WIDE>(p, sm, bars, &abort_flag, tc::smem_u32(code_lut), h, q0, tid - 32 * kProdWarp0, lane);
+    producer<true, WIDE>(p, sm, bars, &abort_flag, tc::smem_u32(code_lut), h, q0, tid - 32 * kVWarp0, lane);
   }
   tc::fence_before_sync();
   __syncthreads();
