@@ -168,6 +168,23 @@ def gen_layer(layer: int):
     return ks, vs, qs
 
 
+# DRAM bytes per launch of the attention kernel (dram__bytes_read.sum + dram__bytes_write.sum from
+# one ncu capture, profiles/attend_tc_kernel_*.md), valid only for the kernel source they were taken
+# on: the SHA-256 of csrc/attend.cu is checked, and the traffic reported as null otherwise.
+ATTEND_TRAFFIC = {"sha256": "63ebf9f4fe9e9ecf8be91b1144f8916911bc945257e83e87935c2ad5eee2e299",
+                  "720p": 473242880 + 192928256, "480p": 227208704 + 66112512}
+
+
+def attend_traffic(workload: str):
+    import hashlib
+    src = os.path.join(ROOT, "bit_kv_cache_qsac_gb300", "csrc", "attend.cu")
+    try:
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    return ATTEND_TRAFFIC.get(workload) if digest == ATTEND_TRAFFIC["sha256"] else None
+
+
 def run_ours(args, rank, world, device):
     import torch
 
@@ -217,8 +234,8 @@ def run_ours(args, rank, world, device):
 
     # kernels launched per step (counted from the library's launch sequence):
     # statistics 3 (partial sums, finish, Jacobi); each fit 1 + 2 x iterations (assign, update);
-    # packing 2 (Keys, Values); attention 1
-    launches_per_step = 3 + 2 * (1 + 2 * 10) + 2 + 1
+    # packing 3 (fp16 codebook copies, Keys, Values); attention 1
+    launches_per_step = 3 + 2 * (1 + 2 * 10) + 3 + 1
 
     clk = ClockSampler(device.index if device.index is not None else 0).__enter__()
     for _ in range(args.warmup):
@@ -305,7 +322,7 @@ def run_ours(args, rank, world, device):
         "quantize_token_heads_per_s": units / (stage[2] / 1e3),
         "roofline": {"bound": "tensor", "kernel": "attend", "achieved": attend_tflops, "peak": peak_tf,
                      "unit": "TFLOP/s", "frac": attend_tflops / peak_tf if peak_tf else None,
-                     "peak_source": f"bf16 sustained, {peak_kind}", "traffic": None,
+                     "peak_source": f"bf16 sustained, {peak_kind}", "traffic": attend_traffic(W.name),
                      "algorithmic": f"{FLOPS_PER_PAIR} flops per (query, key) pair x {pairs} pairs"},
         "roofline_quantize": {"bound": "hbm", "kernel": "quantize", "achieved": q_gbs, "peak": peak_bw,
                               "unit": "GB/s", "frac": q_gbs / peak_bw if peak_bw else None,
@@ -317,7 +334,9 @@ def run_ours(args, rank, world, device):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
         "compression": {"packed_bytes": cache_bytes, "bf16_bytes": 2 * H * N_CACHE * D * 2,
-                        "ratio": 2 * H * N_CACHE * D * 2 / cache_bytes},
+                        "ratio": 2 * H * N_CACHE * D * 2 / cache_bytes,
+                        "ratio_with_fp16_codebook_copies":
+                            2 * H * N_CACHE * D * 2 / sum(c.nbytes(operand_copies=True) for c in chunks)},
         "setup_s": {"generate": gen_s},
     }
     return res

@@ -142,7 +142,11 @@ constexpr int kJacThreads = 512;
 constexpr int LD = D + 4;  // padded row stride of the shared matrices (16-byte aligned rows)
 constexpr int NP = D / 2;  // disjoint pairs per round
 constexpr int kMaxSweeps = 30;
-constexpr float kRotTol = 1e-6f;  // rotate (p,q) while |a_pq| > tol * sqrt(|a_pp a_qq|) ...
+// rotate (p,q) while |a_pq| > kRotTol sqrt(|a_pp a_qq|) ...: a left-over off-diagonal entry at
+// that level moves an eigenvalue by at most about 1e-5 of its size (the noise eigenvalues form a
+// near-degenerate cluster, where the move is first order) and a well-separated eigenvector by
+// far less
+constexpr float kRotTol = 1e-5f;
 constexpr float kAbsTol = 1.2e-7f;  // ... and |a_pq| > kAbsTol ||A||_F (fp32 rounding level of A)
 
 // C = op(X) Y for 128x128 shared matrices (row stride LD), op(X) = X or X^T; 512 threads, each
