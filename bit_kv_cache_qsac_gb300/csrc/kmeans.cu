@@ -16,10 +16,11 @@
 //   warp 1    TMEM owner and MMA issuer: D[128 x C] = X hi^T + X lo^T into 2 TMEM buffers
 //   warps 2-9 epilogue, two warpgroups taking alternate tiles: thread = token = TMEM lane;
 //             argmin over the C columns (two interleaved chains, lower index on ties)
-// The assignments of up to 4096 tokens stay in shared memory; then each warp adds its tokens
-// into per-CTA cluster sums in shared memory (over the codebook area; lane l adds channels l,
-// l + 32, l + 64, l + 96, so the 32 lanes of an add hit 32 different banks) and the CTA adds them
-// to its own slice of the workspace.  km_update_kernel reduces the slices in a fixed order.
+// The assignments of up to 4096 tokens stay in shared memory; then the token tiles stream through
+// the token stages again (TMA) and the warps add each token into per-CTA cluster sums in shared
+// memory (over the codebook area; lane l adds channels l, l + 32, l + 64, l + 96, so the 32 lanes
+// of an add hit 32 different banks); the CTA adds them to its own slice of the workspace and
+// km_update_kernel reduces the slices in a fixed order.
 // All waits are bounded; on expiry the kernel records QWM_ERR_DEVICE_TIMEOUT and stops.
 #include "qwm_internal.cuh"
 #include "tc.cuh"
@@ -65,7 +66,7 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
                                                                  const AssignParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   unsigned char *sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
-  __shared__ uint64_t x_full[2], x_empty[2], t_full[2], t_empty[2], drain;
+  __shared__ uint64_t x_full[2], x_empty[2], t_full[2], t_empty[2], drain, p2_full[2], p2_empty[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
   const int C = p.C;
@@ -77,7 +78,7 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
   const int64_t tile0 = (int64_t)cta * per;
   const int64_t tile1 = tile0 + per < tiles ? tile0 + per : tiles;
   float *sums = (float *)sm;                    // phase 2: [C][D] fp32 over the codebook area
-  int32_t *cnts = (int32_t *)(sm + C * D * 4);  // phase 2: [C], over the token stages
+  int32_t *cnts = (int32_t *)(sm + L.norm);     // phase 2: [C], over the norms
   float *norm = (float *)(sm + L.norm);
   uint8_t *asg = sm + L.asg;
   volatile int *abort_v = &abort_flag;
@@ -88,6 +89,8 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
       tc::mbar_init(&x_empty[i], 1);
       tc::mbar_init(&t_full[i], 1);
       tc::mbar_init(&t_empty[i], 4);
+      tc::mbar_init(&p2_full[i], 1);
+      tc::mbar_init(&p2_empty[i], kThreads / 32 - 1);
     }
     tc::mbar_init(&drain, 1);
     abort_flag = 0;
@@ -102,10 +105,10 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base_sh;
   const float *cent = p.cent + (int64_t)h * C * D;
-  const uint16_t *xh = p.x + (int64_t)h * p.n * D;
   float *psum = p.part_sum + ((int64_t)h * p.G + cta) * C * D;
   int32_t *pcnt = p.part_cnt + ((int64_t)h * p.G + cta) * C;
   int64_t g_tile = 0;  // tiles this CTA has processed (barrier phases)
+  int64_t g2 = 0;      // tiles re-read by phase 2 (barrier phases)
   for (int64_t sc0 = tile0, first = 1; first || sc0 < tile1; sc0 += kMaxTok / TILE, first = 0) {
     const int64_t left = tile1 - sc0;
     const int nt = left <= 0 ? 0 : (left < kMaxTok / TILE ? (int)left : kMaxTok / TILE);
@@ -225,34 +228,52 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
     for (int e = tid; e < C * D; e += kThreads) sums[e] = 0.f;
     for (int j = tid; j < C; j += kThreads) cnts[j] = 0;
     __syncthreads();
-    const int64_t t_begin = sc0 * TILE;
-    const int64_t t_stop = (sc0 + nt) * TILE;
-    const int64_t t_end = t_stop < p.n ? t_stop : p.n;
-    // warp w takes tokens w, w + 10, w + 20, ...: 8 of them at a time, loads first, then the adds
-    constexpr int kStep = kThreads / 32, kUnroll = 8;
-    for (int64_t tb = t_begin + warp; tb < t_end; tb += (int64_t)kStep * kUnroll) {
-      uint16_t xv[kUnroll][4];
-      int jj[kUnroll];
-#pragma unroll
-      for (int u = 0; u < kUnroll; u++) {
-        const int64_t tok = tb + (int64_t)u * kStep;
-        jj[u] = -1;
-        if (tok < t_end) {
-          jj[u] = asg[tok - t_begin];
-#pragma unroll
-          for (int k = 0; k < 4; k++) xv[u][k] = xh[tok * D + lane + 32 * k];
+    // the super-chunk's token tiles stream through the (now idle) token stages again: warp 0
+    // issues the TMA loads, warps 1-9 add each row of a tile into its cluster's sum (lane l adds
+    // channels l, l + 32, l + 64, l + 96: 32 different banks per add)
+    if (warp == 0) {
+      if (lane == 0) {
+        for (int i = 0; i < nt && !*abort_v; i++) {
+          const int64_t g = g2 + i;
+          const int s = (int)(g & 1);
+          if (g >= 2 && !tc::mbar_wait(&p2_empty[s], (uint32_t)(((g >> 1) - 1) & 1), kWaitNs)) {
+            *abort_v = 1;
+            break;
+          }
+          tc::mbar_arrive_expect_tx(&p2_full[s], 2 * TILE * 128);
+          const int row = (int)((int64_t)h * p.n + (sc0 + i) * TILE);
+          unsigned char *dst = sm + L.x + s * 2 * TILE * 128;
+          tc::tma_load_2d(dst, &tmap, 0, row, &p2_full[s]);
+          tc::tma_load_2d(dst + TILE * 128, &tmap, 64, row, &p2_full[s]);
         }
       }
+    } else {
+      for (int i = 0; i < nt; i++) {
+        const int64_t g = g2 + i;
+        const int s = (int)(g & 1);
+        if (!tc::mbar_wait(&p2_full[s], (uint32_t)((g >> 1) & 1), kWaitNs)) *abort_v = 1;
+        if (*abort_v) break;
+        const unsigned char *xt = sm + L.x + s * 2 * TILE * 128;
+        const int64_t tok0 = (sc0 + i) * TILE;
+        const int rows = (int)((p.n - tok0) < TILE ? (p.n - tok0) : TILE);
+        for (int row = warp - 1; row < rows; row += kThreads / 32 - 1) {
+          const int j = asg[i * TILE + row];
+          float *sj = sums + j * D + lane;
 #pragma unroll
-      for (int u = 0; u < kUnroll; u++) {
-        if (jj[u] < 0) continue;
-        float *sj = sums + jj[u] * D + lane;
-#pragma unroll
-        for (int k = 0; k < 4; k++) atomicAdd(sj + 32 * k, bf16_to_f32(xv[u][k]));
-        if (lane == 0) atomicAdd(cnts + jj[u], 1);
+          for (int k = 0; k < 4; k++) {
+            const int c = lane + 32 * k;
+            const uint16_t xv = *(const uint16_t *)(xt + (c >> 6) * TILE * 128 + tc::sw128_offset(row, c & 63));
+            atomicAdd(sj + 32 * k, bf16_to_f32(xv));
+          }
+          if (lane == 0) atomicAdd(cnts + j, 1);
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&p2_empty[s]);
       }
     }
+    g2 += nt;
     __syncthreads();
+    if (*abort_v) break;
     for (int e = tid; e < C * D; e += kThreads) psum[e] = first ? sums[e] : psum[e] + sums[e];
     for (int j = tid; j < C; j += kThreads) pcnt[j] = first ? cnts[j] : pcnt[j] + cnts[j];
     __syncthreads();
