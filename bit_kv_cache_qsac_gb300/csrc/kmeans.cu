@@ -38,7 +38,9 @@ struct KmSmem {  // offsets from a 1024-aligned base, for a codebook of C centro
   __host__ __device__ explicit KmSmem(int C) {
     bh = 0;                        // 2 blocks of [C][64] bf16 (hi)
     bl = bh + 2 * C * 128;         // 2 blocks of [C][64] bf16 (lo)
-    x = bl + 2 * C * 128;          // 2 stages x 2 blocks of [128][64]
+    // the codebook area doubles as the two one-hot buffers of the cluster sums (M >= 128 rows)
+    const int onehot = 2 * ((C + 127) / 128) * 2 * TILE * 128;
+    x = 4 * C * 128 > onehot ? 4 * C * 128 : onehot;  // 2 stages x 2 blocks of [128][64]
     norm = x + 2 * 2 * TILE * 128; // C floats
     asg = norm + 4 * C;            // kMaxTok bytes
     total = asg + kMaxTok;
@@ -66,7 +68,8 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
                                                                  const AssignParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   unsigned char *sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
-  __shared__ uint64_t x_full[2], x_empty[2], t_full[2], t_empty[2], drain, p2_full[2], p2_empty[2];
+  __shared__ uint64_t x_full[2], x_empty[2], t_full[2], t_empty[2], drain;
+  __shared__ uint64_t p2_full[2], p2_empty[2], a_full[2], a_empty[2], p2_done;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
   const int C = p.C;
@@ -77,7 +80,6 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
   const int64_t per = (tiles + p.G - 1) / p.G;
   const int64_t tile0 = (int64_t)cta * per;
   const int64_t tile1 = tile0 + per < tiles ? tile0 + per : tiles;
-  float *sums = (float *)sm;                    // phase 2: [C][D] fp32 over the codebook area
   int32_t *cnts = (int32_t *)(sm + L.norm);     // phase 2: [C], over the norms
   float *norm = (float *)(sm + L.norm);
   uint8_t *asg = sm + L.asg;
@@ -90,8 +92,11 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
       tc::mbar_init(&t_full[i], 1);
       tc::mbar_init(&t_empty[i], 4);
       tc::mbar_init(&p2_full[i], 1);
-      tc::mbar_init(&p2_empty[i], kThreads / 32 - 1);
+      tc::mbar_init(&p2_empty[i], 1);
+      tc::mbar_init(&a_full[i], kThreads / 32 - 2);
+      tc::mbar_init(&a_empty[i], 1);
     }
+    tc::mbar_init(&p2_done, 1);
     tc::mbar_init(&drain, 1);
     abort_flag = 0;
     tc::fence_mbar_init();
@@ -109,6 +114,7 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
   int32_t *pcnt = p.part_cnt + ((int64_t)h * p.G + cta) * C;
   int64_t g_tile = 0;  // tiles this CTA has processed (barrier phases)
   int64_t g2 = 0;      // tiles re-read by phase 2 (barrier phases)
+  int n_sc = 0;        // super-chunks done (phase of p2_done)
   for (int64_t sc0 = tile0, first = 1; first || sc0 < tile1; sc0 += kMaxTok / TILE, first = 0) {
     const int64_t left = tile1 - sc0;
     const int nt = left <= 0 ? 0 : (left < kMaxTok / TILE ? (int)left : kMaxTok / TILE);
@@ -224,15 +230,25 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
     __syncthreads();
     if (*abort_v) break;
     g_tile += nt;
-    // ---- phase 2: cluster sums of this super-chunk (over the codebook area) ----
-    for (int e = tid; e < C * D; e += kThreads) sums[e] = 0.f;
+    // ---- phase 2: cluster sums of this super-chunk on the tensor cores ----
+    // sums[C][D] = A^T X accumulated over the tiles, A = the tile's one-hot assignment matrix
+    // ([C][128 tokens] bf16, 1 where token t belongs to cluster j), X = the token tile ([tokens][D],
+    // read as an N-major B operand); M = 128 centroids per MMA (two MMAs for C = 256) into TMEM
+    // columns 0 .. C-1 (lane = centroid mod 128).  The one-hot matrices (two buffers) live over the
+    // codebook area; the token tiles stream through the token stages again (TMA).
+    const int Mb = (C + 127) / 128;              // 128-centroid blocks
+    const uint32_t aBytes = (uint32_t)Mb * 2u * TILE * 128u;  // one one-hot buffer
+    for (int e = tid; e < (int)(2u * aBytes / 16u); e += kThreads) *(uint4 *)(sm + 16 * e) = make_uint4(0, 0, 0, 0);
     for (int j = tid; j < C; j += kThreads) cnts[j] = 0;
+    tc::fence_proxy_async_smem();
+    tc::fence_before_sync();
     __syncthreads();
-    // the super-chunk's token tiles stream through the (now idle) token stages again: warp 0
-    // issues the TMA loads, warps 1-9 add each row of a tile into its cluster's sum (lane l adds
-    // channels l, l + 32, l + 64, l + 96: 32 different banks per add)
+    tc::fence_after_sync();
+    auto onehot_off = [&](int j, int t) -> uint32_t {  // byte offset of A[j][t] inside a buffer
+      return (uint32_t)(j >> 7) * 2u * TILE * 128u + (uint32_t)(t >> 6) * TILE * 128u + tc::sw128_offset(j & 127, t & 63);
+    };
     if (warp == 0) {
-      if (lane == 0) {
+      if (lane == 0) {  // TMA: token tiles
         for (int i = 0; i < nt && !*abort_v; i++) {
           const int64_t g = g2 + i;
           const int s = (int)(g & 1);
@@ -247,36 +263,100 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
           tc::tma_load_2d(dst + TILE * 128, &tmap, 64, row, &p2_full[s]);
         }
       }
-    } else {
+    } else if (warp == 1) {
+      if (lane == 0) {  // MMA: sums += A^T X
+        const uint32_t idesc = tc::idesc_bf16_f32(TILE, D) | (1u << 16);  // B (token tile) N-major
+        const uint32_t sx = tc::smem_u32(sm + L.x), sa = tc::smem_u32(sm);
+        for (int i = 0; i < nt && !*abort_v; i++) {
+          const int64_t g = g2 + i;
+          const int s = (int)(g & 1);
+          if (!tc::mbar_wait(&p2_full[s], (uint32_t)((g >> 1) & 1), kWaitNs) ||
+              !tc::mbar_wait(&a_full[s], (uint32_t)((g >> 1) & 1), kWaitNs)) {
+            *abort_v = 1;
+            break;
+          }
+          tc::fence_after_sync();
+          for (int mb = 0; mb < Mb; mb++) {
+#pragma unroll
+            for (int kk = 0; kk < TILE / 16; kk++) {  // 16 tokens per K step
+              const uint32_t ao = sa + (uint32_t)s * aBytes + (uint32_t)mb * 2u * TILE * 128u +
+                                  (uint32_t)(kk / 4) * TILE * 128u + 32u * (kk % 4);
+              const uint32_t bo = sx + (uint32_t)s * 2u * TILE * 128u + 2048u * kk;
+              tc::mma_ss(tmem + 128u * mb, tc::desc_sw128(ao), tc::desc_sw128_mn(bo, TILE * 128, 1024), idesc,
+                         (i > 0 || kk > 0) ? 1u : 0u);
+            }
+          }
+          tc::mma_commit(&p2_empty[s]);
+          tc::mma_commit(&a_empty[s]);
+        }
+        tc::mma_commit(&p2_done);
+      }
+    } else {  // warps 2-9 build the one-hot matrices: thread = token of the tile (128 of 256)
+      const int bt = tid - 64;
       for (int i = 0; i < nt; i++) {
         const int64_t g = g2 + i;
         const int s = (int)(g & 1);
-        if (!tc::mbar_wait(&p2_full[s], (uint32_t)((g >> 1) & 1), kWaitNs)) *abort_v = 1;
-        if (*abort_v) break;
-        const unsigned char *xt = sm + L.x + s * 2 * TILE * 128;
+        const bool ok = g < 2 || tc::mbar_wait(&a_empty[s], (uint32_t)(((g >> 1) - 1) & 1), kWaitNs);
+        if (__any_sync(0xffffffffu, !ok || *abort_v != 0)) {  // warp-uniform exit
+          *abort_v = 1;
+          break;
+        }
+        unsigned char *abuf = sm + (uint32_t)s * aBytes;
         const int64_t tok0 = (sc0 + i) * TILE;
         const int rows = (int)((p.n - tok0) < TILE ? (p.n - tok0) : TILE);
-        for (int row = warp - 1; row < rows; row += kThreads / 32 - 1) {
-          const int j = asg[i * TILE + row];
-          float *sj = sums + j * D + lane;
-#pragma unroll
-          for (int k = 0; k < 4; k++) {
-            const int c = lane + 32 * k;
-            const uint16_t xv = *(const uint16_t *)(xt + (c >> 6) * TILE * 128 + tc::sw128_offset(row, c & 63));
-            atomicAdd(sj + 32 * k, bf16_to_f32(xv));
+        if (bt < TILE) {
+          if (i >= 2) {  // clear this buffer's ones of two tiles ago (same super-chunk)
+            const int64_t tokp = (sc0 + i - 2) * TILE;
+            const int rowsp = (int)((p.n - tokp) < TILE ? (p.n - tokp) : TILE);
+            if (bt < rowsp) *(uint16_t *)(abuf + onehot_off(asg[(i - 2) * TILE + bt], bt)) = 0;
           }
-          if (lane == 0) atomicAdd(cnts + j, 1);
+          if (bt < rows) {
+            const int j = asg[i * TILE + bt];
+            *(uint16_t *)(abuf + onehot_off(j, bt)) = 0x3F80u;  // bf16 1.0
+            atomicAdd(cnts + j, 1);
+          }
         }
+        tc::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&p2_empty[s]);
+        if (lane == 0) tc::mbar_arrive(&a_full[s]);
       }
     }
     g2 += nt;
+    if (!*abort_v && !tc::mbar_wait(&p2_done, (uint32_t)(n_sc & 1), kWaitNs)) *abort_v = 1;
+    n_sc++;
+    tc::fence_after_sync();
     __syncthreads();
     if (*abort_v) break;
-    for (int e = tid; e < C * D; e += kThreads) psum[e] = first ? sums[e] : psum[e] + sums[e];
+    // sums from TMEM (warps 2-9: lane quarter warp % 4, centroid block (warp - 2) / 4) -> the workspace
+    if (warp >= 2) {
+      const int mb = (warp - 2) >> 2, sub = warp & 3;
+      const int j = 128 * mb + 32 * sub + lane;
+      if (mb < Mb) {
+        uint32_t r[32];
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          tc::tmem_ld32(tmem + ((uint32_t)(32 * sub) << 16) + 128u * mb + c0, r);
+          tc::tmem_ld_wait();
+          if (j < C) {
+            float4 *dst = (float4 *)(psum + (int64_t)j * D + c0);
+#pragma unroll
+            for (int v = 0; v < 8; v++) {
+              float4 a = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                     __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+              if (nt == 0) a = make_float4(0.f, 0.f, 0.f, 0.f);  // no tiles: no MMA wrote TMEM
+              if (!first) {
+                const float4 o = dst[v];
+                a.x += o.x; a.y += o.y; a.z += o.z; a.w += o.w;
+              }
+              dst[v] = a;
+            }
+          }
+        }
+      }
+    }
     for (int j = tid; j < C; j += kThreads) pcnt[j] = first ? cnts[j] : pcnt[j] + cnts[j];
+    tc::fence_before_sync();
     __syncthreads();
+    tc::fence_after_sync();
   }
   // drain outstanding MMAs, then release TMEM
   if (warp == 1 && lane == 0) {
