@@ -427,41 +427,73 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
       int best = 0;
       float best_S = 0.f;
       if (KEY) {
+        // Each token's candidate rows (this lane's 4 channels of each) are loaded one token ahead,
+        // all at once, so a token costs one load latency, overlapped with the previous token's
+        // scores.  Candidates are kept newest first; ties in S go to the lower index explicitly.
+        constexpr int KM = MP1 - 1;
         const int tmax = (int)((p.n - tok0) < 32 ? (p.n - tok0) : 32);
-        for (int t = 0; t < tmax; t++) {
-          float xf[4];
-          unpack4(*(const uint2 *)(xt + lane4_offset(32 * sub + t, lane)), xf);
-          float bS = INFINITY;
-          int bj = C, m_i = 0;
+        auto prep = [&](int t, int (&cj)[KM], uint2 (&mu2)[KM]) -> int {
+          int cnt = 0;
           for (int wi = 0; wi < NW; wi++) {
             uint32_t m = msk[wi * 32 + t];
             while (m) {
               const int j = 32 * wi + __ffs(m) - 1;
               m &= m - 1;
-              float mu[4];
-              unpack4(*(const uint2 *)(cent + (int64_t)j * D + 4 * lane), mu);
-              float mn = INFINITY, mx = -INFINITY;
 #pragma unroll
-              for (int u = 0; u < 4; u++) {
-                const float rr = __fsub_rn(xf[u], mu[u]);
-                mn = fminf(mn, rr);
-                mx = fmaxf(mx, rr);
-              }
-#pragma unroll
-              for (int o = 8; o > 0; o >>= 1) {  // within each half-warp (= one group)
-                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-              }
-              const float Rg = __fsub_rn(mx, mn);
-              const float Ro = __shfl_xor_sync(0xffffffffu, Rg, 16);
-              const float R0 = lane < 16 ? Rg : Ro, R1 = lane < 16 ? Ro : Rg;
-              const float S = __fadd_rn(__fmul_rn(W0, __fmul_rn(R0, R0)), __fmul_rn(W1, __fmul_rn(R1, R1)));
-              if (S < bS) { bS = S; bj = j; }
-              if (p.dbg_cand && lane == 0 && m_i < M) p.dbg_cand[((int64_t)h * p.n + tok0 + t) * M + m_i] = j;
-              m_i++;
+              for (int k = KM - 1; k >= 1; k--) cj[k] = cj[k - 1];
+              cj[0] = j;
+              cnt++;
             }
           }
+          cnt = cnt < KM ? cnt : KM;
+#pragma unroll
+          for (int k = 0; k < KM; k++)
+            if (k < cnt) mu2[k] = *(const uint2 *)(cent + (int64_t)cj[k] * D + 4 * lane);
+          return cnt;
+        };
+        auto score = [&](int t, int cnt, const int (&cj)[KM], const uint2 (&mu2)[KM]) {
+          float xf[4];
+          unpack4(*(const uint2 *)(xt + lane4_offset(32 * sub + t, lane)), xf);
+          float bS = INFINITY;
+          int bj = C;
+#pragma unroll
+          for (int k = 0; k < KM; k++) {
+            if (k >= cnt) break;
+            const int j = cj[k];
+            float mu[4];
+            unpack4(mu2[k], mu);
+            float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+              const float rr = __fsub_rn(xf[u], mu[u]);
+              mn = fminf(mn, rr);
+              mx = fmaxf(mx, rr);
+            }
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) {  // within each half-warp (= one group)
+              mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            }
+            const float Rg = __fsub_rn(mx, mn);
+            const float Ro = __shfl_xor_sync(0xffffffffu, Rg, 16);
+            const float R0 = lane < 16 ? Rg : Ro, R1 = lane < 16 ? Ro : Rg;
+            const float S = __fadd_rn(__fmul_rn(W0, __fmul_rn(R0, R0)), __fmul_rn(W1, __fmul_rn(R1, R1)));
+            if (S < bS || (S == bS && j < bj)) { bS = S; bj = j; }
+            if (p.dbg_cand && lane == 0 && k < M) p.dbg_cand[((int64_t)h * p.n + tok0 + t) * M + k] = j;
+          }
           if (lane == t) { best = bj; best_S = bS; }
+        };
+        int cA[KM], cB[KM];
+        uint2 uA[KM], uB[KM];
+        int nA = 0, nB = 0;
+        if (tmax > 0) nA = prep(0, cA, uA);
+        for (int t = 0; t < tmax; t += 2) {
+          if (t + 1 < tmax) nB = prep(t + 1, cB, uB);
+          score(t, nA, cA, uA);
+          if (t + 1 < tmax) {
+            if (t + 2 < tmax) nA = prep(t + 2, cA, uA);
+            score(t + 1, nB, cB, uB);
+          }
         }
       } else {
         for (int wi = 0; wi < NW; wi++) {
