@@ -23,12 +23,11 @@
 //                   logits from TMEM, keeps the running max and sum, writes P (fp16) over the
 //                   logits, rescales O in TMEM when the max grows by more than 2^8;
 //   warp 8          allocates TMEM and issues every tcgen05.mma (one thread);
-//   warps 9-12      Key producers: thread = key row of the tile; copy the rows' centroids
-//                   (cp.async, two whole rows per instruction) into the 128-byte-swizzled K-major
-//                   stage and decode them in place;
-//   warps 13-16     Value producers: the same for V_hat rows ([key][d], read as an N-major B),
-//                   and, one tile ahead of the Key producers, the rows of the second MMA's B
-//                   operand and, at each chunk start, its A operand for both Query tiles.
+//   warps 9-12      Key producers: thread = key row of the tile; copies the row's centroid
+//                   (cp.async, 16 bytes at a time) into the 128-byte-swizzled K-major stage,
+//                   decodes it in place, writes the row of the second MMA's B operand, and at
+//                   each chunk start builds the second MMA's A operand for both Query tiles;
+//   warps 13-16     Value producers: the same for V_hat rows ([key][d], read as an N-major B).
 // Each producer thread keeps its row's index data two tiles ahead in registers and its centroid
 // copies one tile ahead in the other shared-memory stage.
 // Tensor memory (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each; P_x overlays S_x.
@@ -102,7 +101,7 @@ struct Bars {
 };
 
 // Index data of one key row: fp16 scale and offset pairs (group 0 low half), 128 2-bit codes,
-// and (in the Value producers' copy) the Key row's PSAC coefficients and their scale.
+// and (Keys) the PSAC coefficients and their scale.
 struct RowData {
   int idx;  // centroid, or -1 for a row past the end of the chunk
   uint32_t scl, mn;
@@ -138,7 +137,7 @@ __device__ __forceinline__ void load_row(const AttnChunk &c, int h, int C, int64
   const uint4 *cp = (const uint4 *)((VAL ? c.v_codes : c.k_codes) + gi * (D / 4));
   d.c0 = cp[0];
   d.c1 = cp[1];
-  if (VAL && c.rank > 0) {  // the Key row's PSAC coefficients: the Value producers write them
+  if (!VAL && c.rank > 0) {
     const int R = c.rank;
     const int8_t *src = c.c + gi * R;
     if (R == 8) {
@@ -335,40 +334,25 @@ __device__ __forceinline__ void producer(const AttnParams &p, unsigned char *sm,
   }
   issue_warp_copies(VAL ? p.ch[0].cent_v16 : p.ch[0].cent_k16, h, C, A.idx, stage0, rbase, lane);
   tc::cp_async_commit();
-  // Value producers: row r of the second MMA's B operand for a Key tile ([c_hat | 0 | mask]) and, at
-  // a chunk start, Query rows r of both tiles of its A operand; then their share of k_full.
-  auto second_operands = [&](int tt, int ti, const RowData &d, uint32_t xs) -> bool {
-    const AttnChunk &c = p.ch[tt];
-    write_x_row<WIDE>(d, c.rank, xs, r);
-    if (ti == 0) {
-      if (tt > 0 && !tc::mbar_wait(&bars.qx_free, (tt - 1) & 1, kWaitNs)) fail(abort_flag, p.status);
-      if (__any_sync(0xffffffffu, *abort_v != 0)) return false;  // warp-uniform exit
-      const uint32_t sq = tc::smem_u32(sm + OFF_Q);
-      write_qx_row<WIDE>(c, h, q0 + r < p.nq, sq, qx0, r);
-      write_qx_row<WIDE>(c, h, q0 + BM + r < p.nq, sq + 2u * kBlk, qx0 + kXBytes, r);
-    }
-    tc::fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) tc::mbar_arrive(&bars.k_full[(xs - xs0) / kXBytes]);
-    return true;
-  };
-  if (VAL && !second_operands(0, 0, A, xs0)) {
-    tc::cp_async_wait<0>();
-    return;
-  }
   auto step = [&](int j, RowData &cur, const RowData &nxt) -> bool {
     const int s = j & 1;
+    const AttnChunk &ch = p.ch[t0];
     tc::cp_async_wait<0>();
     __syncwarp();  // the warp's copies of tile j, made visible to every lane
     decode_row<!WIDE>(cur, stage0 + (uint32_t)s * 2u * kBlk, r, lut);
+    if (!VAL) {
+      write_x_row<WIDE>(cur, ch.rank, xs0 + (uint32_t)s * kXBytes, r);
+      if (ti0 == 0) {  // chunk start: the second MMA's A operand for both Query tiles
+        if (t0 > 0 && !tc::mbar_wait(&bars.qx_free, (t0 - 1) & 1, kWaitNs)) fail(abort_flag, p.status);
+        if (__any_sync(0xffffffffu, *abort_v != 0)) return false;  // warp-uniform exit
+        const uint32_t sq = tc::smem_u32(sm + OFF_Q);
+        write_qx_row<WIDE>(ch, h, q0 + r < p.nq, sq, qx0, r);
+        write_qx_row<WIDE>(ch, h, q0 + BM + r < p.nq, sq + 2u * kBlk, qx0 + kXBytes, r);
+      }
+    }
     tc::fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(&full[s]);
-    if (VAL && j + 1 < J) {  // the second MMA's operands for Key tile j+1 (off the Key producers' path)
-      if (j >= 1 && !tc::mbar_wait(&bars.k_empty[s ^ 1], ((j - 1) >> 1) & 1, kWaitNs)) fail(abort_flag, p.status);
-      if (__any_sync(0xffffffffu, *abort_v != 0)) return false;  // warp-uniform exit
-      if (!second_operands(t1, ti1, nxt, xs0 + (uint32_t)(s ^ 1) * kXBytes)) return false;
-    }
     if (j + 1 < J) {  // copies of tile j+1 into the other stage once tile j-1 has released it
       if (j >= 1 && !tc::mbar_wait(&empty[s ^ 1], ((j - 1) >> 1) & 1, kWaitNs)) fail(abort_flag, p.status);
       if (__any_sync(0xffffffffu, *abort_v != 0)) return false;  // warp-uniform exit
@@ -434,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
   }
   if (tid == 0) {
     for (int i = 0; i < 2; i++) {
-      tc::mbar_init(&bars.k_full[i], 2 * kProdWarps);  // Key producers + the Value producers' operand rows
+      tc::mbar_init(&bars.k_full[i], kProdWarps);
       tc::mbar_init(&bars.v_full[i], kProdWarps);
       tc::mbar_init(&bars.k_empty[i], 1);
       tc::mbar_init(&bars.v_empty[i], 1);
