@@ -36,6 +36,7 @@ class CompressedLayer:
         self.chunks: list[Chunk] = []
         self.prev_cent_k = None
         self.prev_cent_v = None
+        self._side = None        # second stream for the statistics update of step()
 
     def fold_queries(self, q: torch.Tensor, stream=None) -> None:
         """Step 1: fold Queries [H][nq][d] into the statistics and recompute w and U_r."""
@@ -45,14 +46,17 @@ class CompressedLayer:
         self.n_seen += nq
 
     def append_chunk(self, k: torch.Tensor, v: torch.Tensor, warm_start: bool = True, stream=None,
-                     debug: dict | None = None) -> Chunk:
-        """Steps 2-4: fit the chunk's codebooks and pack its Keys and Values."""
+                     debug: dict | None = None, stats_done=None) -> Chunk:
+        """Steps 2-4: fit the chunk's codebooks and pack its Keys and Values.  `stats_done`: an
+        event the packing waits for (a statistics update running on another stream)."""
         n = k.shape[1]
         ch = Chunk.empty(self.ctx, n, self.device)
         init_k = self.prev_cent_k if warm_start else None
         init_v = self.prev_cent_v if warm_start else None
         qwm_fit_centroids(self.ctx, k, n, init_k, ch.cent_k, stream)
         qwm_fit_centroids(self.ctx, v, n, init_v, ch.cent_v, stream)
+        if stats_done is not None:
+            (stream if stream is not None else torch.cuda.current_stream(self.device)).wait_event(stats_done)
         psac = self.n_seen > 0 and self.ctx.cfg.rank > 0
         if psac:
             ch.u_r.copy_(self.u_r)   # per-chunk snapshot of the basis
@@ -80,11 +84,22 @@ class CompressedLayer:
         return kh, vh
 
     def step(self, q_prev, k, v, q, stream=None) -> torch.Tensor:
-        """One streaming step: fold q_prev (may be None), pack (k, v), attend with q."""
+        """One streaming step: fold q_prev (may be None), pack (k, v), attend with q.
+
+        The statistics update and the codebook fits do not depend on each other, so the statistics
+        run on a second stream beside the fits; the packing waits for both."""
+        main = stream if stream is not None else torch.cuda.current_stream(self.device)
+        done = None
         if q_prev is not None:
-            self.fold_queries(q_prev, stream)
-        self.append_chunk(k, v, stream=stream)
-        return self.attend(q, stream=stream)
+            if self._side is None:
+                self._side = torch.cuda.Stream(self.device)
+            self._side.wait_stream(main)
+            q_prev.record_stream(self._side)
+            self.fold_queries(q_prev, self._side)
+            done = torch.cuda.Event()
+            done.record(self._side)
+        self.append_chunk(k, v, stream=main, stats_done=done)
+        return self.attend(q, stream=main)
 
     def check(self, stream=None) -> int:
         return qwm_sync_status(self.ctx, stream)
