@@ -349,7 +349,61 @@ def run_ours(args, rank, world, device):
                             2 * H * N_CACHE * D * 2 / sum(c.nbytes(operand_copies=True) for c in chunks)},
         "setup_s": {"generate": gen_s},
     }
+    if rank == 0 and not args.no_comparisons:
+        res["comparisons"] = comparisons(q, ctx, chunks, ks, vs, Q[last], device, stream, flush)
     return res
+
+
+def comparisons(q, ctx, chunks, ks, vs, Qc, device, stream, flush):
+    """Context for the attention timing (not part of the step): the pages' own decode path
+    (qwm_dequantize every chunk to bf16, then a fused bf16 attention) and the same attention on the
+    uncompressed bf16 Keys/Values, both through torch's scaled_dot_product_attention with a fused
+    backend (never the unfused math one), timed with CUDA events after one warm-up."""
+    import torch
+    from torch.nn.attention import SDPBackend, sdpa_kernel
+    backends = [SDPBackend.CUDNN_ATTENTION, SDPBackend.FLASH_ATTENTION, SDPBackend.EFFICIENT_ATTENTION]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    out = {}
+    try:
+        parts_k = [torch.empty(H, c.n_tokens, D, dtype=torch.bfloat16, device=device) for c in chunks]
+        parts_v = [torch.empty_like(x) for x in parts_k]
+        qb = Qc.unsqueeze(0)
+        for rep in range(2):                     # the first pass warms up
+            flush.zero_()
+            ev[0].record(stream)
+            for c, pk, pv in zip(chunks, parts_k, parts_v):
+                q.qwm_dequantize(ctx, c, pk, pv, stream)
+            ev[1].record(stream)
+            kh = torch.cat(parts_k, dim=1).unsqueeze(0)
+            vh = torch.cat(parts_v, dim=1).unsqueeze(0)
+            ev[2].record(stream)
+            with sdpa_kernel(backends):
+                o = torch.nn.functional.scaled_dot_product_attention(qb, kh, vh)
+            ev[3].record(stream)
+            ev[3].synchronize()
+        deq, sdpa = ev[0].elapsed_time(ev[1]), ev[2].elapsed_time(ev[3])
+        pairs = H * NQ * N_CACHE
+        out["dequantize_then_sdpa"] = {"dequantize_ms": deq, "sdpa_ms": sdpa, "total_ms": deq + sdpa,
+                                       "sdpa_tflops": pairs * 512 / (sdpa / 1e3) / 1e12,
+                                       "note": "bf16 K_hat/V_hat concatenated outside the timing"}
+        del kh, vh, parts_k, parts_v
+        kb = torch.from_numpy(np.concatenate(ks, axis=1).view(np.int16)).to(device).view(torch.bfloat16).unsqueeze(0)
+        vb = torch.from_numpy(np.concatenate(vs, axis=1).view(np.int16)).to(device).view(torch.bfloat16).unsqueeze(0)
+        for rep in range(2):
+            flush.zero_()
+            ev[0].record(stream)
+            with sdpa_kernel(backends):
+                o = torch.nn.functional.scaled_dot_product_attention(qb, kb, vb)
+            ev[1].record(stream)
+            ev[1].synchronize()
+        ms = ev[0].elapsed_time(ev[1])
+        out["bf16_sdpa_uncompressed"] = {"ms": ms, "tflops": pairs * 512 / (ms / 1e3) / 1e12,
+                                         "cache_bytes": 2 * H * N_CACHE * D * 2}
+        del kb, vb, o
+    except Exception as exc:  # no fused backend for this GPU / build
+        out["unavailable"] = f"{type(exc).__name__}: {exc}"[:200]
+    torch.cuda.empty_cache()
+    return out
 
 
 # ---------------------------------------------------------------------------- oracle (CPU) arm
@@ -410,6 +464,128 @@ def oracle_sample(seconds_hint: float = 15.0):
                         "attend": H * t_att * NQ / rows}}
 
 
+# ---------------------------------------------------------------------------- extra reports
+
+
+def _dev_bf16(a, device):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+def run_ablation(device):
+    """Config-4 sweep on the 480p-shaped layer (40 heads, 8 chunks of 4,680 tokens): QSAC candidates
+    M in {1, 4, 16}, PSAC rank r in {0, 8, 16}, codebook size C in {64, 256} (1024 needs 16-bit
+    indices, which this build does not implement).  Per configuration: packing time of the last
+    chunk (k-means fit + quantise), attention time over the whole cache, and the logit error of the
+    decoded cache against the original bf16 Keys on 256 Queries per head -- MSE, MSE relative to
+    the mean squared logit, and the top-1 shift rate (fraction of (head, Query) whose argmax key
+    changes).  One JSON line per configuration."""
+    import torch
+    import bit_kv_cache_qsac_gb300 as q
+    from bit_kv_cache_qsac_gb300.stream import CompressedLayer
+    Wa = synth.P480
+    Hh, Dd, T = Wa.heads, Wa.head_dim, Wa.n_chunks
+    ks = synth.keys(Wa, 0); vs = synth.values(Wa, 0)
+    K = [_dev_bf16(ks[:, a:b], device) for a, b in (synth.chunk_range(Wa, t) for t in range(T))]
+    V = [_dev_bf16(vs[:, a:b], device) for a, b in (synth.chunk_range(Wa, t) for t in range(T))]
+    Q = [_dev_bf16(synth.queries(Wa, t, Wa.nq_attend), device) for t in range(T)]
+    rows = torch.linspace(0, Wa.nq_attend - 1, 256, device=device).long()
+    Qs = Q[-1][:, rows].float()
+    scale = 1.0 / math.sqrt(Dd)
+    Kall = torch.cat(K, dim=1).float()
+    Lref = torch.einsum("hqd,hkd->hqk", Qs, Kall) * scale
+    top_ref = Lref.argmax(-1)
+    ms2_ref = float((Lref ** 2).mean())
+    del Kall
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    pairs = Hh * Wa.nq_attend * Wa.n_tokens
+    for C in (64, 256):
+        for M in (1, 4, 16):
+            for r in (0, 8, 16):
+                ctx = q.Context(heads=Hh, n_centroids=C, top_m=M, rank=r, kmeans_iters=10)
+                layer = CompressedLayer(ctx, device)
+                for t in range(T):
+                    if t > 0:
+                        layer.fold_queries(Q[t - 1])
+                    if t == T - 1:
+                        ev[0].record()
+                    layer.append_chunk(K[t], V[t])
+                    if t == T - 1:
+                        ev[1].record()
+                out = layer.attend(Q[-1])            # warm-up
+                ev[2].record()
+                out = layer.attend(Q[-1], out)
+                ev[3].record()
+                torch.cuda.synchronize()
+                assert layer.check() == 0
+                khat = torch.cat([layer.dequantize(i)[0] for i in range(T)], dim=1).float()
+                L = torch.einsum("hqd,hkd->hqk", Qs, khat) * scale
+                mse = float(((L - Lref) ** 2).mean())
+                shift = float((L.argmax(-1) != top_ref).float().mean())
+                att_ms = ev[2].elapsed_time(ev[3])
+                pack_ms = ev[0].elapsed_time(ev[1])
+                print(json.dumps({"report": "ablation", "workload": "480p-shaped layer, step 8 of 8",
+                                  "n_centroids": C, "top_m": M, "rank": r,
+                                  "pack_ms": pack_ms, "pack_token_heads_per_s": Hh * Wa.chunk_tokens / (pack_ms / 1e3),
+                                  "attend_ms": att_ms,
+                                  "attend_tflops": pairs * 2 * (Dd + r + Dd) / (att_ms / 1e3) / 1e12,
+                                  "logit_mse": mse, "logit_mse_rel": mse / ms2_ref, "top1_shift": shift,
+                                  "compression": 2 * Hh * Wa.n_tokens * Dd * 2 / layer.nbytes()}), flush=True)
+                del layer, ctx, khat, L, out
+                torch.cuda.empty_cache()
+
+
+def run_full_model(device):
+    """Config 3: 40 layers of the 480p-shaped workload streamed chunk by chunk (8 steps per layer:
+    fold the previous chunk's Queries, fit and pack the chunk, attend with the chunk's Queries over
+    every packed chunk).  Every layer's compressed cache stays resident; reports the compressed
+    size against the bf16 size and the per-step times summed over the layers (CUDA events)."""
+    import torch
+    import bit_kv_cache_qsac_gb300 as q
+    from bit_kv_cache_qsac_gb300.stream import CompressedLayer
+    Wf, n_layers = synth.P480, 40
+    Hh, Dd, T = Wf.heads, Wf.head_dim, Wf.n_chunks
+    ctx = q.Context(heads=Hh, n_centroids=Wf.n_centroids, top_m=Wf.top_m, rank=Wf.rank, kmeans_iters=10)
+    stats_ms, pack_ms, att_ms = np.zeros(T), np.zeros(T), np.zeros(T)
+    layers, gen_s = [], 0.0
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for li in range(n_layers):
+        t0 = time.time()
+        ks = synth.keys(Wf, li); vs = synth.values(Wf, li)
+        qs = [synth.queries(Wf, t, Wf.nq_attend, layer=li) for t in range(T)]
+        gen_s += time.time() - t0
+        K = [_dev_bf16(ks[:, a:b], device) for a, b in (synth.chunk_range(Wf, t) for t in range(T))]
+        V = [_dev_bf16(vs[:, a:b], device) for a, b in (synth.chunk_range(Wf, t) for t in range(T))]
+        Q = [_dev_bf16(x, device) for x in qs]
+        layer = CompressedLayer(ctx, device)
+        for t in range(T):
+            ev[0].record()
+            if t > 0:
+                layer.fold_queries(Q[t - 1])
+            ev[1].record()
+            layer.append_chunk(K[t], V[t])
+            ev[2].record()
+            layer.attend(Q[t])
+            ev[3].record()
+            ev[3].synchronize()
+            stats_ms[t] += ev[0].elapsed_time(ev[1])
+            pack_ms[t] += ev[1].elapsed_time(ev[2])
+            att_ms[t] += ev[2].elapsed_time(ev[3])
+        assert layer.check() == 0
+        layers.append(layer)
+        del K, V, Q
+    packed = sum(l.nbytes() for l in layers)
+    packed_ops = sum(sum(c.nbytes(operand_copies=True) for c in l.chunks) for l in layers)
+    bf16 = 2 * n_layers * Hh * Wf.n_tokens * Dd * 2
+    print(json.dumps({"report": "full_model", "workload": f"{n_layers} layers of the 480p-shaped layer",
+                      "bf16_bytes": bf16, "packed_bytes": packed, "packed_gib": packed / 2 ** 30,
+                      "ratio": bf16 / packed, "ratio_with_fp16_codebook_copies": bf16 / packed_ops,
+                      "per_step_ms_all_layers": {"stats_eig": stats_ms.tolist(), "fit_and_pack": pack_ms.tolist(),
+                                                 "attend": att_ms.tolist()},
+                      "total_gpu_ms": float(stats_ms.sum() + pack_ms.sum() + att_ms.sum()),
+                      "generate_s": gen_s}), flush=True)
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return None
@@ -441,9 +617,20 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-comparisons", action="store_true",
+                    help="skip the dequantize+SDPA and bf16 SDPA context timings")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="720p",
                     help="720p-shaped layer (default) or 480p-shaped layer")
+    ap.add_argument("--report", choices=["ablation", "full-model"], default=None,
+                    help="instead of the benchmark line: the M x r x C sweep (config 4) or the 40-layer "
+                         "480p-shaped model (config 3)")
     args = ap.parse_args()
+    if args.report:
+        import torch
+        device = torch.device("cuda", 0)
+        torch.cuda.set_device(device)
+        run_ablation(device) if args.report == "ablation" else run_full_model(device)
+        return
     select_workload(args.workload)
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
