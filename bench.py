@@ -539,16 +539,19 @@ def run_full_model(device):
     """Config 3: 40 layers of the 480p-shaped workload streamed chunk by chunk (8 steps per layer:
     fold the previous chunk's Queries, fit and pack the chunk, attend with the chunk's Queries over
     every packed chunk).  Every layer's compressed cache stays resident; reports the compressed
-    size against the bf16 size and the per-step times summed over the layers (CUDA events)."""
+    size against the bf16 size and the per-step times summed over the layers (CUDA events), beside
+    a fused bf16 attention (torch SDPA) of the same Queries over the same uncompressed Keys/Values."""
     import torch
     import bit_kv_cache_qsac_gb300 as q
     from bit_kv_cache_qsac_gb300.stream import CompressedLayer
     Wf, n_layers = synth.P480, 40
     Hh, Dd, T = Wf.heads, Wf.head_dim, Wf.n_chunks
     ctx = q.Context(heads=Hh, n_centroids=Wf.n_centroids, top_m=Wf.top_m, rank=Wf.rank, kmeans_iters=10)
-    stats_ms, pack_ms, att_ms = np.zeros(T), np.zeros(T), np.zeros(T)
+    from torch.nn.attention import SDPBackend, sdpa_kernel
+    backends = [SDPBackend.CUDNN_ATTENTION, SDPBackend.FLASH_ATTENTION, SDPBackend.EFFICIENT_ATTENTION]
+    stats_ms, pack_ms, att_ms, sdpa_ms = np.zeros(T), np.zeros(T), np.zeros(T), np.zeros(T)
     layers, gen_s = [], 0.0
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
     for li in range(n_layers):
         t0 = time.time()
         ks = synth.keys(Wf, li); vs = synth.values(Wf, li)
@@ -558,6 +561,7 @@ def run_full_model(device):
         V = [_dev_bf16(vs[:, a:b], device) for a, b in (synth.chunk_range(Wf, t) for t in range(T))]
         Q = [_dev_bf16(x, device) for x in qs]
         layer = CompressedLayer(ctx, device)
+        Kc, Vc = torch.cat(K, dim=1).unsqueeze(0), torch.cat(V, dim=1).unsqueeze(0)
         for t in range(T):
             ev[0].record()
             if t > 0:
@@ -567,13 +571,23 @@ def run_full_model(device):
             ev[2].record()
             layer.attend(Q[t])
             ev[3].record()
-            ev[3].synchronize()
+            # the same attention on the uncompressed bf16 Keys/Values of chunks 0..t
+            end = synth.chunk_range(Wf, t)[1]
+            if li == 0 and t == 0:  # warm-up of the fused backend
+                with sdpa_kernel(backends):
+                    torch.nn.functional.scaled_dot_product_attention(Q[t].unsqueeze(0), Kc[:, :, :end], Vc[:, :, :end])
+            ev[4].record()
+            with sdpa_kernel(backends):
+                torch.nn.functional.scaled_dot_product_attention(Q[t].unsqueeze(0), Kc[:, :, :end], Vc[:, :, :end])
+            ev[5].record()
+            ev[5].synchronize()
             stats_ms[t] += ev[0].elapsed_time(ev[1])
             pack_ms[t] += ev[1].elapsed_time(ev[2])
             att_ms[t] += ev[2].elapsed_time(ev[3])
+            sdpa_ms[t] += ev[4].elapsed_time(ev[5])
         assert layer.check() == 0
         layers.append(layer)
-        del K, V, Q
+        del K, V, Q, Kc, Vc
     packed = sum(l.nbytes() for l in layers)
     packed_ops = sum(sum(c.nbytes(operand_copies=True) for c in l.chunks) for l in layers)
     bf16 = 2 * n_layers * Hh * Wf.n_tokens * Dd * 2
@@ -581,8 +595,12 @@ def run_full_model(device):
                       "bf16_bytes": bf16, "packed_bytes": packed, "packed_gib": packed / 2 ** 30,
                       "ratio": bf16 / packed, "ratio_with_fp16_codebook_copies": bf16 / packed_ops,
                       "per_step_ms_all_layers": {"stats_eig": stats_ms.tolist(), "fit_and_pack": pack_ms.tolist(),
-                                                 "attend": att_ms.tolist()},
+                                                 "attend": att_ms.tolist(),
+                                                 "bf16_sdpa_uncompressed": sdpa_ms.tolist()},
                       "total_gpu_ms": float(stats_ms.sum() + pack_ms.sum() + att_ms.sum()),
+                      "total_bf16_sdpa_ms": float(sdpa_ms.sum()),
+                      "note": "each stage is timed alone with a host sync after every layer step, so the "
+                              "per-step figures include launch gaps",
                       "generate_s": gen_s}), flush=True)
 
 
