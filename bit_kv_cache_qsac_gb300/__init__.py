@@ -166,9 +166,10 @@ class Chunk:
         dev = device or torch.device("cuda", torch.cuda.current_device())
         u8 = dict(dtype=torch.uint8, device=dev)
         f16 = dict(dtype=torch.float16, device=dev)
+        ix = dict(dtype=torch.uint8 if Cn <= 256 else torch.int16, device=dev)  # int16 = uint16 bits
         return Chunk(n, 0,
                      torch.empty(H, n, d // 4, **u8), torch.empty(H, n, d // 4, **u8),
-                     torch.empty(H, n, **u8), torch.empty(H, n, **u8),
+                     torch.empty(H, n, **ix), torch.empty(H, n, **ix),
                      torch.empty(H, n, G, **f16), torch.empty(H, n, G, **f16),
                      torch.empty(H, n, G, **f16), torch.empty(H, n, G, **f16),
                      torch.empty(H, Cn, d, dtype=torch.bfloat16, device=dev),
@@ -194,7 +195,8 @@ class Chunk:
         def p(t, width):
             return _ptr(t, "chunk field", width)
         return qwm_chunk(self.n_tokens, self.rank_eff, 0,
-                         p(self.k_codes, 1), p(self.v_codes, 1), p(self.k_idx, 1), p(self.v_idx, 1),
+                         p(self.k_codes, 1), p(self.v_codes, 1),
+                         p(self.k_idx, self.k_idx.element_size()), p(self.v_idx, self.v_idx.element_size()),
                          p(self.k_scale, 2), p(self.k_min, 2), p(self.v_scale, 2), p(self.v_min, 2),
                          p(self.cent_k, 2), p(self.cent_v, 2), p(self.c, 1), p(self.c_scale, 2), p(self.u_r, 2),
                          p(self.cent_k16, 2), p(self.cent_v16, 2))

@@ -11,7 +11,7 @@ constexpr int kStatsSplits = 8;
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
-  size_t status, stats_part, km_sum, km_cnt, km_cent, jac_basis, jac_valid, total;
+  size_t status, stats_part, km_sum, km_cnt, km_cent, jac_basis, jac_valid, km_img, q_img, total;
 };
 
 Layout layout_of(const qwm_config &c) {
@@ -25,6 +25,8 @@ Layout layout_of(const qwm_config &c) {
   L.km_cent = off; off = align_up(off + (size_t)c.heads * c.n_centroids * QWM_D * sizeof(float), 256);
   L.jac_basis = off; off = align_up(off + (size_t)c.heads * QWM_D * QWM_D * sizeof(float), 256);
   L.jac_valid = off; off = align_up(off + (size_t)c.heads * sizeof(int32_t), 256);
+  L.km_img = off; off = align_up(off + kmeans_image_bytes(c.heads, c.n_centroids), 1024);
+  L.q_img = off; off = align_up(off + quantize_image_bytes(c.heads, c.n_centroids), 1024);
   L.total = off;
   return L;
 }
@@ -36,7 +38,8 @@ qwm_status check_config(const qwm_config *c) {
     return QWM_ERR_ARG;
   if (c->head_dim != QWM_D || c->group != QWM_GROUP) return QWM_ERR_SHAPE;
   if (c->bits != 2) return QWM_ERR_UNSUPPORTED;
-  if (!(c->n_centroids == 64 || c->n_centroids == 128 || c->n_centroids == 256)) return QWM_ERR_SHAPE;
+  if (!(c->n_centroids == 64 || c->n_centroids == 128 || c->n_centroids == 256 || c->n_centroids == 1024))
+    return QWM_ERR_SHAPE;
   if (c->top_m > QWM_MAX_TOPM || c->top_m > c->n_centroids) return QWM_ERR_SHAPE;
   if (c->rank > QWM_MAX_RANK) return QWM_ERR_SHAPE;
   if (c->kmeans_iters > 100) return QWM_ERR_SHAPE;
@@ -133,6 +136,8 @@ qwm_status qwm_create(const qwm_config *cfg, qwm_ctx **out) {
   ctx->km_cent = (float *)(base + L.km_cent);
   ctx->jac_basis = (float *)(base + L.jac_basis);
   ctx->jac_valid = (int32_t *)(base + L.jac_valid);
+  ctx->km_img = (unsigned char *)(base + L.km_img);
+  ctx->q_img = (unsigned char *)(base + L.q_img);
   *out = ctx;
   return QWM_OK;
 }
@@ -174,7 +179,8 @@ qwm_status qwm_fit_centroids(qwm_ctx *ctx, const uint16_t *x, int64_t n, const u
   if (!aligned16(x) || !aligned16(cent) || (init && !aligned16(init))) return QWM_ERR_ALIGN;
   const int sms = ctx->num_sms < QWM_MAX_SMS ? ctx->num_sms : QWM_MAX_SMS;
   cudaError_t e = launch_kmeans(x, n, ctx->cfg.heads, ctx->cfg.n_centroids, init, ctx->cfg.kmeans_iters, cent,
-                                ctx->km_cent, ctx->km_sum, ctx->km_cnt, sms, ctx->status, (cudaStream_t)stream);
+                                ctx->km_cent, ctx->km_sum, ctx->km_cnt, sms, ctx->status, ctx->km_img,
+                                (cudaStream_t)stream);
   return cuda_status(e);
 }
 
@@ -195,7 +201,7 @@ qwm_status qwm_quantize_kv(qwm_ctx *ctx, const uint16_t *k, const uint16_t *v, i
   }
   if (n == 0) return QWM_OK;
   cudaError_t e = launch_quantize(ctx->cfg, k, v, n, w, psac ? u_r : nullptr, *out, dbg, ctx->status,
-                                  ctx->num_sms, (cudaStream_t)stream);
+                                  ctx->num_sms, ctx->q_img, (cudaStream_t)stream);
   return cuda_status(e);
 }
 

@@ -131,7 +131,9 @@ __device__ __forceinline__ void load_row(const AttnChunk &c, int h, int C, int64
   d.ca = d.cb = make_uint2(0, 0);
   if (r >= nk) return;
   const int64_t gi = (int64_t)h * c.n + k0 + r;
-  d.idx = (VAL ? c.v_idx : c.k_idx)[gi];  // clamped to the codebook where it is used (no wait here)
+  // uint16 indices for 1024-centroid codebooks; clamped to the codebook where used (no wait here)
+  const uint8_t *ip = VAL ? c.v_idx : c.k_idx;
+  d.idx = C > 256 ? (int)((const uint16_t *)ip)[gi] : (int)ip[gi];
   d.scl = *(const uint32_t *)((VAL ? c.v_scale : c.k_scale) + gi * 2);
   d.mn = *(const uint32_t *)((VAL ? c.v_min : c.k_min) + gi * 2);
   const uint4 *cp = (const uint4 *)((VAL ? c.v_codes : c.k_codes) + gi * (D / 4));
@@ -637,7 +639,8 @@ cudaError_t launch_attend(const qwm_config &cfg, const uint16_t *q, int64_t nq, 
     if (used == kMaxChunks) return cudaErrorInvalidValue;
     AttnChunk &a = p.ch[used++];
     a.n = c.n_tokens; a.rank = c.rank_eff; a.tiles = (int)((c.n_tokens + BN - 1) / BN);
-    a.k_codes = c.k_codes; a.v_codes = c.v_codes; a.k_idx = c.k_idx; a.v_idx = c.v_idx;
+    a.k_codes = c.k_codes; a.v_codes = c.v_codes;
+    a.k_idx = (const uint8_t *)c.k_idx; a.v_idx = (const uint8_t *)c.v_idx;
     a.k_scale = c.k_scale; a.k_min = c.k_min; a.v_scale = c.v_scale; a.v_min = c.v_min;
     a.cent_k16 = c.cent_k16; a.cent_v16 = c.cent_v16; a.c_scale = c.c_scale; a.u_r = c.u_r; a.c = c.c;
     tiles += a.tiles;

@@ -23,13 +23,14 @@ __global__ void dequant_kernel(qwm_chunk ch, int H, int C, int R, uint16_t *__re
       uint16_t *dst = pass ? v_hat : k_hat;
       if (!dst) continue;
       const uint8_t *codes = pass ? ch.v_codes : ch.k_codes;
-      const uint8_t *idx = pass ? ch.v_idx : ch.k_idx;
+      const void *idx = pass ? ch.v_idx : ch.k_idx;  // uint16 for 1024-centroid codebooks
       const uint16_t *sc = pass ? ch.v_scale : ch.k_scale;
       const uint16_t *mn = pass ? ch.v_min : ch.k_min;
       const uint16_t *cent = pass ? ch.cent_v : ch.cent_k;
       const float s = f16_to_f32(sc[row * G + g]), m = f16_to_f32(mn[row * G + g]);
       const uint32_t b2 = *(const uint16_t *)(codes + row * (D / 4) + 2 * cb);  // 8 codes
-      const int j = min((int)idx[row], C - 1);  // never read past the codebook
+      const int j = min(C > 256 ? (int)((const uint16_t *)idx)[row] : (int)((const uint8_t *)idx)[row],
+                        C - 1);  // never read past the codebook
       const uint4 mu = *(const uint4 *)(cent + ((int64_t)h * C + j) * D + c0);
       const uint32_t muw[4] = {mu.x, mu.y, mu.z, mu.w};
       float x[8];

@@ -21,6 +21,12 @@
 // memory (over the codebook area; lane l adds channels l, l + 32, l + 64, l + 96, so the 32 lanes
 // of an add hit 32 different banks); the CTA adds them to its own slice of the workspace and
 // km_update_kernel reduces the slices in a fixed order.
+// Codebooks of 1024 centroids (WIDE) do not fit in shared memory: km_image_kernel writes each
+// head's hi/lo operands as 128-centroid slices in global memory (with the squared norms), the
+// producer streams the slices through one shared-memory buffer for every tile, and the argmin runs
+// slice by slice over two 128-column TMEM halves per epilogue group.  The cluster sums then come
+// from a stable counting sort of the super-chunk's assignments and one warp per centroid adding its
+// members' rows in token order (no one-hot matrix: it would not fit).
 // All waits are bounded; on expiry the kernel records QWM_ERR_DEVICE_TIMEOUT and stops.
 #include "qwm_internal.cuh"
 #include "tc.cuh"
@@ -33,17 +39,24 @@ constexpr int kMaxTok = 4096;  // tokens per super-chunk (assignments kept in sh
 constexpr int kThreads = 320;
 constexpr uint64_t kWaitNs = 1000000000ull;
 
+constexpr int kSlice = 128;      // centroids per streamed slice (WIDE)
+constexpr int kSliceBytes = 4 * kSlice * 128;  // hi and lo blocks of one slice
+
 struct KmSmem {  // offsets from a 1024-aligned base, for a codebook of C centroids
-  int bh, bl, x, norm, asg, total;
-  __host__ __device__ explicit KmSmem(int C) {
-    bh = 0;                        // 2 blocks of [C][64] bf16 (hi)
-    bl = bh + 2 * C * 128;         // 2 blocks of [C][64] bf16 (lo)
-    // the codebook area doubles as the two one-hot buffers of the cluster sums (M >= 128 rows)
-    const int onehot = 2 * ((C + 127) / 128) * 2 * TILE * 128;
-    x = 4 * C * 128 > onehot ? 4 * C * 128 : onehot;  // 2 stages x 2 blocks of [128][64]
+  int bh, bl, x, norm, asg, cnt, cur, mem, total;
+  __host__ __device__ KmSmem(int C, bool wide) {
+    const int CB = wide ? kSlice : C;  // centroids held in shared memory at once
+    bh = 0;                        // 2 blocks of [CB][64] bf16 (hi)
+    bl = bh + 2 * CB * 128;        // 2 blocks of [CB][64] bf16 (lo)
+    // resident: the codebook area doubles as the two one-hot buffers of the cluster sums
+    const int onehot = wide ? 0 : 2 * ((C + 127) / 128) * 2 * TILE * 128;
+    x = 4 * CB * 128 > onehot ? 4 * CB * 128 : onehot;  // 2 stages x 2 blocks of [128][64]
     norm = x + 2 * 2 * TILE * 128; // C floats
-    asg = norm + 4 * C;            // kMaxTok bytes
-    total = asg + kMaxTok;
+    asg = norm + 4 * C;            // kMaxTok indices (uint8, or uint16 when WIDE)
+    cnt = asg + (wide ? 2 : 1) * kMaxTok;  // WIDE cluster sums: counts [C], cursors [C], members
+    cur = cnt + (wide ? 4 * C : 0);
+    mem = cur + (wide ? 4 * C : 0);
+    total = mem + (wide ? 2 * kMaxTok : 0);
   }
 };
 
@@ -54,9 +67,31 @@ __global__ void kmeans_init_kernel(const uint16_t *__restrict__ x, int64_t n, in
   cent[((int64_t)h * C + j) * D + c] = bf16_to_f32(src[c]);
 }
 
+// WIDE operand image of the fp32 centroids: [H][C / kSlice] slices of (hi, lo) 128-byte-swizzled
+// [kSlice][64] block pairs, exactly as the kernel's slice buffer; norms [H][C] = ||mu_j||^2.
+__global__ void km_image_kernel(const float *__restrict__ cent, int C, unsigned char *__restrict__ img,
+                                float *__restrict__ norms) {
+  __shared__ float part[D / 32];
+  const int h = blockIdx.y, j = blockIdx.x, c = threadIdx.x;
+  const float mu = cent[((int64_t)h * C + j) * D + c];
+  const float hi = __bfloat162float(__float2bfloat16_rn(mu));
+  unsigned char *sl = img + ((int64_t)h * (C / kSlice) + j / kSlice) * kSliceBytes;
+  const uint32_t off = (uint32_t)(c / 64) * kSlice * 128u + tc::sw128_offset(j % kSlice, c % 64);
+  *(uint16_t *)(sl + off) = f32_to_bf16_rn(hi);
+  *(uint16_t *)(sl + 2 * kSlice * 128 + off) = f32_to_bf16_rn(mu - hi);
+  float s = mu * mu;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if ((c & 31) == 0) part[c >> 5] = s;
+  __syncthreads();
+  if (c == 0) norms[(int64_t)h * C + j] = (part[0] + part[1]) + (part[2] + part[3]);
+}
+
 struct AssignParams {
   const uint16_t *x;     // [H][n][D] bf16
   const float *cent;     // [H][C][D] fp32
+  const unsigned char *img;  // WIDE: operand slices
+  const float *norms;        // WIDE: [H][C]
   float *part_sum;       // [H][G][C][D]
   int32_t *part_cnt;     // [H][G][C]
   int64_t n;
@@ -64,16 +99,19 @@ struct AssignParams {
   int32_t *status;
 };
 
+template <bool WIDE>
 __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_constant__ TensorMap128 tmap,
                                                                  const AssignParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   unsigned char *sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ uint64_t x_full[2], x_empty[2], t_full[2], t_empty[2], drain;
   __shared__ uint64_t p2_full[2], p2_empty[2], a_full[2], a_empty[2], p2_done;
+  __shared__ uint64_t tw_full[4], tw_empty[4], sl_full, sl_empty;  // WIDE: TMEM halves, slice buffer
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
   const int C = p.C;
-  const KmSmem L(C);
+  const int NSL = WIDE ? C / kSlice : 1;
+  const KmSmem L(C, WIDE);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.y, cta = blockIdx.x;
   const int64_t tiles = (p.n + TILE - 1) / TILE;
@@ -83,6 +121,7 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
   int32_t *cnts = (int32_t *)(sm + L.norm);     // phase 2: [C], over the norms
   float *norm = (float *)(sm + L.norm);
   uint8_t *asg = sm + L.asg;
+  uint16_t *asg16 = (uint16_t *)(sm + L.asg);  // WIDE
   volatile int *abort_v = &abort_flag;
 
   if (tid == 0) {
@@ -96,6 +135,12 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
       tc::mbar_init(&a_full[i], kThreads / 32 - 2);
       tc::mbar_init(&a_empty[i], 1);
     }
+    for (int i = 0; i < 4; i++) {
+      tc::mbar_init(&tw_full[i], 1);
+      tc::mbar_init(&tw_empty[i], 4);
+    }
+    tc::mbar_init(&sl_full, 1);
+    tc::mbar_init(&sl_empty, 1);
     tc::mbar_init(&p2_done, 1);
     tc::mbar_init(&drain, 1);
     abort_flag = 0;
@@ -118,8 +163,10 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
   for (int64_t sc0 = tile0, first = 1; first || sc0 < tile1; sc0 += kMaxTok / TILE, first = 0) {
     const int64_t left = tile1 - sc0;
     const int nt = left <= 0 ? 0 : (left < kMaxTok / TILE ? (int)left : kMaxTok / TILE);
-    // ---- codebook -> hi/lo bf16 operand blocks, and squared norms ----
-    for (int e = tid; e < C * (D / 8); e += kThreads) {
+    // ---- codebook -> hi/lo bf16 operand blocks, and squared norms (WIDE: norms only) ----
+    if (WIDE)
+      for (int j = tid; j < C; j += kThreads) norm[j] = p.norms[(int64_t)h * C + j];
+    for (int e = tid; e < (WIDE ? 0 : C) * (D / 8); e += kThreads) {
       const int j = e / (D / 8), ci = e % (D / 8);
       const float4 a = *(const float4 *)(cent + (int64_t)j * D + 8 * ci);
       const float4 b = *(const float4 *)(cent + (int64_t)j * D + 8 * ci + 4);
@@ -136,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
       *(uint4 *)(sm + L.bh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
       *(uint4 *)(sm + L.bl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
-    for (int j = warp; j < C; j += kThreads / 32) {  // one warp per centroid, 4 channels per lane
+    for (int j = warp; j < (WIDE ? 0 : C); j += kThreads / 32) {  // one warp per centroid, 4 channels per lane
       const float4 a = *(const float4 *)(cent + (int64_t)j * D + 4 * lane);
       float s = a.x * a.x;
       s = fmaf(a.y, a.y, s);
@@ -163,37 +210,106 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
           unsigned char *dst = sm + L.x + s * 2 * TILE * 128;
           tc::tma_load_2d(dst, &tmap, 0, row, &x_full[s]);
           tc::tma_load_2d(dst + TILE * 128, &tmap, 64, row, &x_full[s]);
+          if (WIDE) {  // this tile's pass over the codebook, one slice at a time
+            const unsigned char *img = p.img + (int64_t)h * NSL * kSliceBytes;
+            for (int sl = 0; sl < NSL; sl++) {
+              const int64_t u = g * NSL + sl;
+              if (u >= 1 && !tc::mbar_wait(&sl_empty, (uint32_t)((u - 1) & 1), kWaitNs)) { *abort_v = 1; break; }
+              tc::mbar_arrive_expect_tx(&sl_full, kSliceBytes);
+              tc::bulk_load(tc::smem_u32(sm), img + (int64_t)sl * kSliceBytes, kSliceBytes, &sl_full);
+            }
+          }
         }
       }
     } else if (warp == 1) {
       if (lane == 0) {
-        const uint32_t idesc = tc::idesc_bf16_f32(TILE, C);
+        const int CB = WIDE ? kSlice : C;  // centroids per MMA
+        const uint32_t idesc = tc::idesc_bf16_f32(TILE, CB);
         const uint32_t sx = tc::smem_u32(sm + L.x), sbh = tc::smem_u32(sm + L.bh), sbl = tc::smem_u32(sm + L.bl);
+        auto issue = [&](uint32_t d, int s) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; kk++) {
+            const uint32_t xo = sx + s * 2 * TILE * 128 + (kk / 4) * TILE * 128 + 32 * (kk % 4);
+            const uint32_t bo = (kk / 4) * CB * 128 + 32 * (kk % 4);
+            tc::mma_ss(d, tc::desc_sw128(xo), tc::desc_sw128(sbh + bo), idesc, kk > 0);
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; kk++) {
+            const uint32_t xo = sx + s * 2 * TILE * 128 + (kk / 4) * TILE * 128 + 32 * (kk % 4);
+            const uint32_t bo = (kk / 4) * CB * 128 + 32 * (kk % 4);
+            tc::mma_ss(d, tc::desc_sw128(xo), tc::desc_sw128(sbl + bo), idesc, 1);
+          }
+        };
         for (int i = 0; i < nt && !*abort_v; i++) {
           const int64_t g = g_tile + i;
           const int s = (int)(g & 1);
+          if (WIDE) {
+            if (!tc::mbar_wait(&x_full[s], (uint32_t)((g >> 1) & 1), kWaitNs)) { *abort_v = 1; break; }
+            for (int sl = 0; sl < NSL; sl++) {
+              // slice sl of tile g -> TMEM half (sl & 1) of buffer s; that half's k-th use
+              const int64_t u = g * NSL + sl, k = (g >> 1) * (NSL / 2) + (sl >> 1);
+              const int hb = 2 * s + (sl & 1);
+              if (!tc::mbar_wait(&sl_full, (uint32_t)(u & 1), kWaitNs) ||
+                  (k >= 1 && !tc::mbar_wait(&tw_empty[hb], (uint32_t)((k - 1) & 1), kWaitNs))) {
+                *abort_v = 1;
+                break;
+              }
+              tc::fence_after_sync();
+              issue(tmem + 256u * s + 128u * (sl & 1), s);
+              tc::mma_commit(&tw_full[hb]);
+              tc::mma_commit(&sl_empty);
+            }
+            tc::mma_commit(&x_empty[s]);
+            continue;
+          }
           if (!tc::mbar_wait(&x_full[s], (uint32_t)((g >> 1) & 1), kWaitNs) ||
               (g >= 2 && !tc::mbar_wait(&t_empty[s], (uint32_t)(((g >> 1) - 1) & 1), kWaitNs))) {
             *abort_v = 1;
             break;
           }
           tc::fence_after_sync();
-          const uint32_t d = tmem + 256u * s;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; kk++) {
-            const uint32_t xo = sx + s * 2 * TILE * 128 + (kk / 4) * TILE * 128 + 32 * (kk % 4);
-            const uint32_t bo = (kk / 4) * C * 128 + 32 * (kk % 4);
-            tc::mma_ss(d, tc::desc_sw128(xo), tc::desc_sw128(sbh + bo), idesc, kk > 0);
-          }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; kk++) {
-            const uint32_t xo = sx + s * 2 * TILE * 128 + (kk / 4) * TILE * 128 + 32 * (kk % 4);
-            const uint32_t bo = (kk / 4) * C * 128 + 32 * (kk % 4);
-            tc::mma_ss(d, tc::desc_sw128(xo), tc::desc_sw128(sbl + bo), idesc, 1);
-          }
+          issue(tmem + 256u * s, s);
           tc::mma_commit(&x_empty[s]);
           tc::mma_commit(&t_full[s]);
         }
+      }
+    } else if (WIDE) {
+      const int e = (warp - 2) >> 2, sub = warp & 3, row = 32 * sub + lane;
+      const uint32_t lane_addr = (uint32_t)(32 * sub) << 16;
+      for (int i = e; i < nt; i += 2) {
+        const int64_t g = g_tile + i;
+        const int s = (int)(g & 1);
+        float b0 = INFINITY, b1 = INFINITY;  // even / odd columns
+        int a0 = 0, a1 = 1;
+        uint32_t r[32];
+        bool bad = false;
+#pragma unroll 1
+        for (int sl = 0; sl < NSL; sl++) {
+          const int64_t k = (g >> 1) * (NSL / 2) + (sl >> 1);
+          const int hb = 2 * s + (sl & 1);
+          const bool ok = tc::mbar_wait(&tw_full[hb], (uint32_t)(k & 1), kWaitNs);
+          if (__any_sync(0xffffffffu, !ok || *abort_v != 0)) { bad = true; break; }  // warp-uniform
+          tc::fence_after_sync();
+#pragma unroll 1
+          for (int c0 = 0; c0 < kSlice; c0 += 32) {
+            tc::tmem_ld16(tmem + lane_addr + 256u * s + 128u * (sl & 1) + c0, r);
+            tc::tmem_ld16(tmem + lane_addr + 256u * s + 128u * (sl & 1) + c0 + 16, r + 16);
+            tc::tmem_ld_wait();
+            const int j0 = sl * kSlice + c0;
+#pragma unroll
+            for (int kk = 0; kk < 32; kk += 2) {
+              const float d0 = fmaf(-2.f, __uint_as_float(r[kk]), norm[j0 + kk]);
+              const float d1 = fmaf(-2.f, __uint_as_float(r[kk + 1]), norm[j0 + kk + 1]);
+              if (d0 < b0) { b0 = d0; a0 = j0 + kk; }
+              if (d1 < b1) { b1 = d1; a1 = j0 + kk + 1; }
+            }
+          }
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&tw_empty[hb]);
+        }
+        if (bad) { *abort_v = 1; break; }
+        asg16[i * TILE + row] = (uint16_t)((b1 < b0 || (b1 == b0 && a1 < a0)) ? a1 : a0);
       }
     } else {
       const int e = (warp - 2) >> 2, sub = warp & 3, row = 32 * sub + lane;
@@ -230,6 +346,70 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
     __syncthreads();
     if (*abort_v) break;
     g_tile += nt;
+    if (WIDE) {
+      // ---- phase 2 (WIDE): stable counting sort of the assignments, then per-centroid sums ----
+      int32_t *cnt = (int32_t *)(sm + L.cnt), *cur = (int32_t *)(sm + L.cur);
+      uint16_t *mem = (uint16_t *)(sm + L.mem);
+      const int64_t tok0 = sc0 * TILE;
+      const int64_t span = (int64_t)nt * TILE;
+      const int ntok = nt == 0 ? 0 : (int)((p.n - tok0) < span ? (p.n - tok0) : span);
+      for (int j = tid; j < C; j += kThreads) cnt[j] = 0;
+      __syncthreads();
+      for (int t = tid; t < ntok; t += kThreads) atomicAdd(cnt + asg16[t], 1);
+      __syncthreads();
+      if (warp == 0) {
+        const int per = C / 32;  // lane l owns counts l * per .. l * per + per - 1
+        int tot = 0;
+        for (int q = 0; q < per; q++) tot += cnt[lane * per + q];
+        int incl = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        int run = incl - tot;  // exclusive prefix = where cluster j's members start
+        for (int q = 0; q < per; q++) {
+          cur[lane * per + q] = run;
+          run += cnt[lane * per + q];
+        }
+        __syncwarp();
+        const uint32_t below = (1u << lane) - 1u;
+        for (int base = 0; base < ntok; base += 32) {  // tokens in order: a stable sort
+          const int t = base + lane;
+          const int j = t < ntok ? (int)asg16[t] : -1 - lane;  // past the end: a group of its own
+          const uint32_t peers = __match_any_sync(0xffffffffu, j);
+          const int pos = t < ntok ? cur[j] + __popc(peers & below) : 0;
+          __syncwarp();
+          if (t < ntok) {
+            mem[pos] = (uint16_t)t;
+            if ((peers & below) == 0) cur[j] += __popc(peers);  // the group's first lane moves the cursor
+          }
+          __syncwarp();
+        }
+      }
+      __syncthreads();
+      for (int j = warp; j < C; j += kThreads / 32) {  // one warp per centroid, lane = 4 channels
+        const int nj = cnt[j], m0 = cur[j] - nj;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int m = 0; m < nj; m++) {
+          const int t = mem[m0 + m];
+          const uint2 v = *(const uint2 *)(p.x + ((int64_t)h * p.n + tok0 + t) * D + 4 * lane);
+          a.x += __uint_as_float(v.x << 16);
+          a.y += __uint_as_float(v.x & 0xFFFF0000u);
+          a.z += __uint_as_float(v.y << 16);
+          a.w += __uint_as_float(v.y & 0xFFFF0000u);
+        }
+        float4 *dst = (float4 *)(psum + (int64_t)j * D + 4 * lane);
+        if (!first) {
+          const float4 o = *dst;
+          a.x += o.x; a.y += o.y; a.z += o.z; a.w += o.w;
+        }
+        *dst = a;
+        if (lane == 0) pcnt[j] = first ? nj : pcnt[j] + nj;
+      }
+      __syncthreads();
+      continue;
+    }
     // ---- phase 2: cluster sums of this super-chunk on the tensor cores ----
     // sums[C][D] = A^T X accumulated over the tiles, A = the tile's one-hot assignment matrix
     // ([C][128 tokens] bf16, 1 where token t belongs to cluster j), X = the token tile ([tokens][D],
@@ -395,21 +575,35 @@ __global__ void km_update_kernel(int C, int G, float *__restrict__ cent, const f
 // CTAs per head: one wave at most (each CTA holds ~200 KB of shared memory).
 int kmeans_ctas_per_head(int H, int num_sms) { return num_sms / H > 1 ? num_sms / H : 1; }
 
+// Workspace of the WIDE operand images: [H][C / kSlice] slices, then the norms [H][C].
+size_t kmeans_image_bytes(int H, int C) {
+  if (C <= QWM_MAX_RESIDENT_CENTROIDS) return 0;
+  return (size_t)H * (C / kSlice) * kSliceBytes + (size_t)H * C * sizeof(float);
+}
+
 cudaError_t launch_kmeans(const uint16_t *x, int64_t n, int H, int C, const uint16_t *init, int iters,
                           uint16_t *cent, float *km_cent, float *km_sum, int32_t *km_cnt, int num_sms,
-                          int32_t *status, cudaStream_t st) {
+                          int32_t *status, unsigned char *img, cudaStream_t st) {
   TensorMap128 tmap;
   if (!make_tmap_rows128_bf16(&tmap, x, (uint64_t)H * n, TILE)) return cudaErrorInvalidValue;
   kmeans_init_kernel<<<dim3(C, H), D, 0, st>>>(x, n, C, init, km_cent);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  const bool wide = C > QWM_MAX_RESIDENT_CENTROIDS;
+  float *norms = wide ? (float *)(img + (size_t)H * (C / kSlice) * kSliceBytes) : nullptr;
   const int G = kmeans_ctas_per_head(H, num_sms);
-  const int smem = KmSmem(C).total + 1024;
-  e = cudaFuncSetAttribute(km_assign_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const int smem = KmSmem(C, wide).total + 1024;
+  e = wide ? cudaFuncSetAttribute(km_assign_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
+           : cudaFuncSetAttribute(km_assign_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  AssignParams p{x, km_cent, km_sum, km_cnt, n, C, G, status};
+  AssignParams p{x, km_cent, img, norms, km_sum, km_cnt, n, C, G, status};
   for (int it = 0; it < iters; it++) {
-    km_assign_kernel<<<dim3(G, H), kThreads, smem, st>>>(tmap, p);
+    if (wide) {
+      km_image_kernel<<<dim3(C, H), D, 0, st>>>(km_cent, C, img, norms);
+      km_assign_kernel<true><<<dim3(G, H), kThreads, smem, st>>>(tmap, p);
+    } else {
+      km_assign_kernel<false><<<dim3(G, H), kThreads, smem, st>>>(tmap, p);
+    }
     km_update_kernel<<<dim3(C, H), D, 0, st>>>(C, G, km_cent, km_sum, km_cnt, it == iters - 1 ? cent : nullptr);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

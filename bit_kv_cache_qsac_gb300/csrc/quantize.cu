@@ -37,6 +37,12 @@
 //     (3) Keys, warp-cooperative: S of every (token, candidate) pair, with the centroid row read
 //         coalesced from global memory and the group ranges reduced across half-warps;
 //     (4) thread = token: INT2 codes of the chosen centroid's residual, PSAC coefficients.
+// Codebooks of 1024 centroids (WIDE) do not fit in shared memory: a small kernel writes each head's
+// distance operands as an image of 128-centroid slices in global memory, and the producer streams
+// the slices (bulk copies) through one shared-memory slice buffer, each tile's MMAs running slice by
+// slice into two 128-column TMEM halves per epilogue group.  Phase (1) then keeps the M+3 largest T
+// with their indices while the slices go by; when the window reaches past that list, the token's
+// window becomes the whole codebook and phase (2) finds its exact M nearest.  Indices are uint16.
 // All waits are bounded; on expiry the kernel records QWM_ERR_DEVICE_TIMEOUT and stops.
 #include <cuda_fp16.h>
 
@@ -53,14 +59,18 @@ constexpr uint64_t kWaitNs = 1000000000ull;
 // error bound of an approximate T: |err| <= kRel |k| max_j |b_j| + kRelN max_j |nw_j|
 constexpr float kRel = 1.0f / 32768.0f;    // 2^-15
 constexpr float kRelN = 1.0f / 131072.0f;  // 2^-17
+constexpr int kSlice = 128;                // centroids per streamed slice (WIDE)
 
 struct QSmem {
   int bh, bl, bn, an, x, msk, wv, U, total;
-  __host__ __device__ QSmem(int C, bool key) {
-    bh = 0;                             // 2 blocks of [C][64] bf16: hi of b (or mu for Values)
-    bl = bh + 2 * C * 128;              // lo of b (Keys only)
-    bn = bl + (key ? 2 * C * 128 : 0);  // [C][16] bf16 no-swizzle: -nw/2 as hi, lo, then zeros
-    an = bn + C * 32;                   // [128][16] bf16 no-swizzle: 1, 1, then zeros
+  // CB = centroids held in shared memory at once: the whole codebook, or one slice (WIDE).  The
+  // range [0, an) is also the layout of one slice of the global operand image.
+  __host__ __device__ QSmem(int C, bool key, bool wide) {
+    const int CB = wide ? kSlice : C;
+    bh = 0;                               // 2 blocks of [CB][64] bf16: hi of b (or mu for Values)
+    bl = bh + 2 * CB * 128;               // lo of b (Keys only)
+    bn = bl + (key ? 2 * CB * 128 : 0);   // [CB][16] bf16 no-swizzle: -nw/2 as hi, lo, then zeros
+    an = bn + CB * 32;                    // [128][16] bf16 no-swizzle: 1, 1, then zeros
     x = an + TILE * 32;                 // 2 stages x 2 blocks of [128][64]
     msk = x + 2 * 2 * TILE * 128;       // window masks: [8 warps][C/32 words][32 tokens]
     wv = msk + kEpiWarps * (C / 32) * 32 * 4;  // w[D]
@@ -75,7 +85,10 @@ struct QParams {
   const uint16_t *u_r;      // [H][D][R] or NULL
   const uint16_t *cent;     // [H][C][D] bf16 codebook
   int C, top_m, rank, G;
-  uint8_t *codes, *idx;
+  const unsigned char *img;  // WIDE: [H][C / kSlice] operand slices
+  const float *img_max;      // WIDE: [H][2] max_j |b_j|, max_j |nw_j|
+  uint8_t *codes;
+  void *idx;                 // uint8 [H][n], or uint16 [H][n] (WIDE)
   uint16_t *scale, *minv;
   int8_t *c;
   uint16_t *c_scale;
@@ -140,19 +153,21 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // KEY: Keys (QSAC + PSAC) or Values (nearest centroid).  RMAX: 8 or 16, bound on the PSAC rank.
 // MP1: length of the largest-T list, top_m + 1 (exact for the common M; QWM_MAX_TOPM + 1 covers
-// every M, with the list's tail unused).
-template <bool KEY, int RMAX, int MP1>
+// every M, with the list's tail unused).  WIDE: the codebook streams through in slices.
+template <bool KEY, int RMAX, int MP1, bool WIDE>
 __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constant__ TensorMap128 tmap,
                                                              const QParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   unsigned char *sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ uint64_t x_full[2], x_empty[2], t_full[2], t_empty[2], drain;
+  __shared__ uint64_t tw_full[4], tw_empty[4], sl_full, sl_empty;  // WIDE: TMEM halves, slice buffer
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
   __shared__ float Wg[2], bmax_sh, nwmax_sh;
   const int C = p.C, M = KEY ? p.top_m : 1, R = KEY ? p.rank : 0;
   const int NW = C / 32;  // mask words per token
-  const QSmem L(C, KEY);
+  const int NSL = WIDE ? C / kSlice : 1;
+  const QSmem L(C, KEY, WIDE);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.y, cta = blockIdx.x;
   const int64_t tiles = (p.n + TILE - 1) / TILE;
@@ -172,10 +187,16 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
       tc::mbar_init(&t_full[i], 1);
       tc::mbar_init(&t_empty[i], 4);
     }
+    for (int i = 0; i < 4; i++) {
+      tc::mbar_init(&tw_full[i], 1);
+      tc::mbar_init(&tw_empty[i], 4);
+    }
+    tc::mbar_init(&sl_full, 1);
+    tc::mbar_init(&sl_empty, 1);
     tc::mbar_init(&drain, 1);
     abort_flag = 0;
-    bmax_sh = 0.f;
-    nwmax_sh = 0.f;
+    bmax_sh = WIDE ? p.img_max[2 * h] : 0.f;
+    nwmax_sh = WIDE ? p.img_max[2 * h + 1] : 0.f;
     tc::fence_mbar_init();
   }
   if (warp == 1) {
@@ -196,7 +217,8 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
   }
   __syncthreads();
   // b = w . mu split into bf16 hi + lo (Keys) or mu itself (Values), 128-byte swizzled K-major
-  for (int e = tid; e < C * (D / 8); e += kThreads) {
+  // (WIDE: the operand image already holds them)
+  for (int e = tid; e < (WIDE ? 0 : C) * (D / 8); e += kThreads) {
     const int j = e / (D / 8), ci = e % (D / 8);
     float mu[8];
     bf16x8(*(const uint4 *)(cent + (int64_t)j * D + 8 * ci), mu);
@@ -214,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
     if (KEY) *(uint4 *)(sm + L.bl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
   }
   // nw_j and |b_j| (one warp per centroid, lane = 4 channels), the nw operand, the maxima
-  for (int j = warp; j < C; j += kThreads / 32) {
+  for (int j = warp; j < (WIDE ? 0 : C); j += kThreads / 32) {
     float mu[4];
     unpack4(*(const uint2 *)(cent + (int64_t)j * D + 4 * lane), mu);
     float s = 0.f, bb = 0.f;
@@ -264,36 +286,66 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
         unsigned char *dst = sm + L.x + s * 2 * TILE * 128;
         tc::tma_load_2d(dst, &tmap, 0, row, &x_full[s]);
         tc::tma_load_2d(dst + TILE * 128, &tmap, 64, row, &x_full[s]);
+        if (WIDE) {  // this tile's pass over the codebook, one slice at a time
+          const uint32_t ib = (uint32_t)L.an;
+          const unsigned char *img = p.img + (int64_t)h * NSL * ib;
+          for (int sl = 0; sl < NSL; sl++) {
+            const int u = g * NSL + sl;
+            if (u >= 1 && !tc::mbar_wait(&sl_empty, (u - 1) & 1, kWaitNs)) { *abort_v = 1; break; }
+            tc::mbar_arrive_expect_tx(&sl_full, ib);
+            tc::bulk_load(tc::smem_u32(sm), img + (int64_t)sl * ib, ib, &sl_full);
+          }
+        }
       }
     }
   } else if (warp == 1) {
     // ======================= MMA issuer =======================
     if (lane == 0) {
-      const uint32_t idesc = tc::idesc_bf16_f32(TILE, C);
+      const int CB = WIDE ? kSlice : C;  // centroids per MMA
+      const uint32_t idesc = tc::idesc_bf16_f32(TILE, CB);
       const uint32_t sx = tc::smem_u32(sm + L.x), sbh = tc::smem_u32(sm + L.bh), sbl = tc::smem_u32(sm + L.bl);
       const uint32_t sbn = tc::smem_u32(sm + L.bn), san = tc::smem_u32(sm + L.an);
+      auto issue = [&](uint32_t d, int s) {  // T of one tile against the centroids in shared memory
+        tc::mma_ss(d, tc::desc_noswz(san, 128, 256), tc::desc_noswz(sbn, 128, 256), idesc, 0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; kk++) {
+          const uint32_t xo = sx + s * 2 * TILE * 128 + (kk / 4) * TILE * 128 + 32 * (kk % 4);
+          tc::mma_ss(d, tc::desc_sw128(xo), tc::desc_sw128(sbh + (kk / 4) * CB * 128 + 32 * (kk % 4)), idesc, 1);
+        }
+        if (KEY) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; kk++) {
+            const uint32_t xo = sx + s * 2 * TILE * 128 + (kk / 4) * TILE * 128 + 32 * (kk % 4);
+            tc::mma_ss(d, tc::desc_sw128(xo), tc::desc_sw128(sbl + (kk / 4) * CB * 128 + 32 * (kk % 4)), idesc, 1);
+          }
+        }
+      };
       for (int g = 0; g < nt && !*abort_v; g++) {
         const int s = g & 1;
+        if (WIDE) {
+          if (!tc::mbar_wait(&x_full[s], (g >> 1) & 1, kWaitNs)) { *abort_v = 1; break; }
+          for (int sl = 0; sl < NSL; sl++) {
+            // slice sl of tile g -> TMEM half (sl & 1) of group s; that half's k-th use
+            const int u = g * NSL + sl, hb = 2 * s + (sl & 1), k = (g >> 1) * (NSL / 2) + (sl >> 1);
+            if (!tc::mbar_wait(&sl_full, u & 1, kWaitNs) ||
+                (k >= 1 && !tc::mbar_wait(&tw_empty[hb], (k - 1) & 1, kWaitNs))) {
+              *abort_v = 1;
+              break;
+            }
+            tc::fence_after_sync();
+            issue(tmem + 256u * s + 128u * (sl & 1), s);
+            tc::mma_commit(&tw_full[hb]);
+            tc::mma_commit(&sl_empty);
+          }
+          continue;
+        }
         if (!tc::mbar_wait(&x_full[s], (g >> 1) & 1, kWaitNs) ||
             (g >= 2 && !tc::mbar_wait(&t_empty[s], ((g >> 1) - 1) & 1, kWaitNs))) {
           *abort_v = 1;
           break;
         }
         tc::fence_after_sync();
-        const uint32_t d = tmem + 256u * s;
-        tc::mma_ss(d, tc::desc_noswz(san, 128, 256), tc::desc_noswz(sbn, 128, 256), idesc, 0);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; kk++) {
-          const uint32_t xo = sx + s * 2 * TILE * 128 + (kk / 4) * TILE * 128 + 32 * (kk % 4);
-          tc::mma_ss(d, tc::desc_sw128(xo), tc::desc_sw128(sbh + (kk / 4) * C * 128 + 32 * (kk % 4)), idesc, 1);
-        }
-        if (KEY) {
-#pragma unroll
-          for (int kk = 0; kk < D / 16; kk++) {
-            const uint32_t xo = sx + s * 2 * TILE * 128 + (kk / 4) * TILE * 128 + 32 * (kk % 4);
-            tc::mma_ss(d, tc::desc_sw128(xo), tc::desc_sw128(sbl + (kk / 4) * C * 128 + 32 * (kk % 4)), idesc, 1);
-          }
-        }
+        issue(tmem + 256u * s, s);
         tc::mma_commit(&t_full[s]);
       }
       tc::mma_commit(&drain);
@@ -311,7 +363,8 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
     for (int u = 0; u < 4; u++) wl[u] = wv[4 * lane + u];
     for (int g = e; g < nt; g += 2) {
       const int s = g & 1;
-      if (!tc::mbar_wait(&t_full[s], (g >> 1) & 1, kWaitNs) || !tc::mbar_wait(&x_full[s], (g >> 1) & 1, kWaitNs))
+      if ((!WIDE && !tc::mbar_wait(&t_full[s], (g >> 1) & 1, kWaitNs)) ||
+          !tc::mbar_wait(&x_full[s], (g >> 1) & 1, kWaitNs))
         *abort_v = 1;
       if (*abort_v) break;
       tc::fence_after_sync();
@@ -330,45 +383,105 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
         for (int u = 0; u < 8; u++) kn2 = fmaf(f[u], f[u], kn2);
       }
       const float delta2 = 2.f * (dcoef * sqrtf(kn2) + dconst);
-      float tv[MP1];
-#pragma unroll
-      for (int k = 0; k < MP1; k++) tv[k] = -INFINITY;
       uint32_t r[32];
+      bool amb;
+      if constexpr (WIDE) {
+        // the KL largest T with their indices (descending; equal T keep the lower index first),
+        // fed slice by slice from the two TMEM halves of this group
+        constexpr int KL = MP1 + 2;
+        float tv[KL];
+        int ti[KL];
+#pragma unroll
+        for (int k = 0; k < KL; k++) { tv[k] = -INFINITY; ti[k] = C; }
+        bool bad = false;
 #pragma unroll 1
-      for (int c0 = 0; c0 < C; c0 += 32) {
-        tc::tmem_ld16(tmem + lane_addr + 256u * s + c0, r);
-        tc::tmem_ld16(tmem + lane_addr + 256u * s + c0 + 16, r + 16);
-        tc::tmem_ld_wait();
+        for (int sl = 0; sl < NSL; sl++) {
+          const int hb = 2 * s + (sl & 1), k = (g >> 1) * (NSL / 2) + (sl >> 1);
+          const bool ok = tc::mbar_wait(&tw_full[hb], k & 1, kWaitNs);
+          if (__any_sync(0xffffffffu, !ok || *abort_v != 0)) { bad = true; break; }  // warp-uniform
+          tc::fence_after_sync();
+#pragma unroll 1
+          for (int c0 = 0; c0 < kSlice; c0 += 32) {
+            tc::tmem_ld16(tmem + lane_addr + 256u * s + 128u * (sl & 1) + c0, r);
+            tc::tmem_ld16(tmem + lane_addr + 256u * s + 128u * (sl & 1) + c0 + 16, r + 16);
+            tc::tmem_ld_wait();
 #pragma unroll
-        for (int k = 0; k < 32; k++) {
-          const float v = __uint_as_float(r[k]);
-          // descending list: new tv[i] = median(tv[i-1], tv[i], v), updated from the bottom up
+            for (int kk = 0; kk < 32; kk++) {
+              const float v = __uint_as_float(r[kk]);
+              if (v > tv[KL - 1]) {
+                const int j = sl * kSlice + c0 + kk;
 #pragma unroll
-          for (int i = MP1 - 1; i >= 1; i--) tv[i] = fminf(tv[i - 1], fmaxf(tv[i], v));
-          tv[0] = fmaxf(tv[0], v);
+                for (int i = KL - 1; i >= 1; i--) {
+                  const bool up = v > tv[i - 1], in = v > tv[i];
+                  tv[i] = up ? tv[i - 1] : (in ? v : tv[i]);
+                  ti[i] = up ? ti[i - 1] : (in ? j : ti[i]);
+                }
+                if (v > tv[0]) { tv[0] = v; ti[0] = j; }
+              }
+            }
+          }
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&tw_empty[hb]);
         }
-      }
-      float tM = tv[0], tM1 = tv[0];  // the M-th and (M+1)-th largest (compile-time indexing)
+        if (bad) { *abort_v = 1; break; }
+        float tM = tv[0], tM1 = tv[0];
 #pragma unroll
-      for (int k = 1; k < MP1; k++) {
-        if (k == M - 1) tM = tv[k];
-        if (k == M) tM1 = tv[k];
-      }
-      const float thr = tM - delta2;
-      const bool amb = valid && (M < C) && !(tM1 < thr);
+        for (int k = 1; k < KL; k++) {
+          if (k == M - 1) tM = tv[k];
+          if (k == M) tM1 = tv[k];
+        }
+        const float thr = tM - delta2;
+        amb = valid && (M < C) && !(tM1 < thr);
+        // a window that may reach past the list: every centroid goes to the exact pass
+        const bool over = amb && !(tv[KL - 1] < thr);
+        for (int wi = 0; wi < NW; wi++) msk[wi * 32 + lane] = (valid && over) ? 0xFFFFFFFFu : 0u;
+        if (valid && !over) {
+#pragma unroll
+          for (int k = 0; k < KL; k++)
+            if (tv[k] >= thr && ti[k] < C) msk[(ti[k] >> 5) * 32 + lane] |= 1u << (ti[k] & 31);
+        }
+        __syncwarp();
+      } else {
+        float tv[MP1];
+#pragma unroll
+        for (int k = 0; k < MP1; k++) tv[k] = -INFINITY;
 #pragma unroll 1
-      for (int c0 = 0; c0 < C; c0 += 32) {
-        tc::tmem_ld16(tmem + lane_addr + 256u * s + c0, r);
-        tc::tmem_ld16(tmem + lane_addr + 256u * s + c0 + 16, r + 16);
-        tc::tmem_ld_wait();
-        uint32_t word = 0u;
+        for (int c0 = 0; c0 < C; c0 += 32) {
+          tc::tmem_ld16(tmem + lane_addr + 256u * s + c0, r);
+          tc::tmem_ld16(tmem + lane_addr + 256u * s + c0 + 16, r + 16);
+          tc::tmem_ld_wait();
 #pragma unroll
-        for (int k = 0; k < 32; k++) word |= (__uint_as_float(r[k]) >= thr ? 1u : 0u) << k;
-        msk[(c0 >> 5) * 32 + lane] = valid ? word : 0u;
+          for (int k = 0; k < 32; k++) {
+            const float v = __uint_as_float(r[k]);
+            // descending list: new tv[i] = median(tv[i-1], tv[i], v), updated from the bottom up
+#pragma unroll
+            for (int i = MP1 - 1; i >= 1; i--) tv[i] = fminf(tv[i - 1], fmaxf(tv[i], v));
+            tv[0] = fmaxf(tv[0], v);
+          }
+        }
+        float tM = tv[0], tM1 = tv[0];  // the M-th and (M+1)-th largest (compile-time indexing)
+#pragma unroll
+        for (int k = 1; k < MP1; k++) {
+          if (k == M - 1) tM = tv[k];
+          if (k == M) tM1 = tv[k];
+        }
+        const float thr = tM - delta2;
+        amb = valid && (M < C) && !(tM1 < thr);
+#pragma unroll 1
+        for (int c0 = 0; c0 < C; c0 += 32) {
+          tc::tmem_ld16(tmem + lane_addr + 256u * s + c0, r);
+          tc::tmem_ld16(tmem + lane_addr + 256u * s + c0 + 16, r + 16);
+          tc::tmem_ld_wait();
+          uint32_t word = 0u;
+#pragma unroll
+          for (int k = 0; k < 32; k++) word |= (__uint_as_float(r[k]) >= thr ? 1u : 0u) << k;
+          msk[(c0 >> 5) * 32 + lane] = valid ? word : 0u;
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&t_empty[s]);
       }
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&t_empty[s]);
       // ---- (2) exact candidate set for tokens whose window holds more than M centroids ----
       uint32_t ambs = __ballot_sync(0xffffffffu, amb);
       while (ambs) {
@@ -552,7 +665,8 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
         uint4 *cdst = (uint4 *)(p.codes + grow * (D / 4));
         cdst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
         cdst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-        p.idx[grow] = (uint8_t)best;
+        if (WIDE) ((uint16_t *)p.idx)[grow] = (uint16_t)best;
+        else ((uint8_t *)p.idx)[grow] = (uint8_t)best;
         *(uint32_t *)(p.scale + grow * 2) = (uint32_t)sb0 | ((uint32_t)sb1 << 16);
         *(uint32_t *)(p.minv + grow * 2) = (uint32_t)mb0 | ((uint32_t)mb1 << 16);
         if (KEY && p.dbg_score) p.dbg_score[grow] = best_S;
@@ -615,21 +729,101 @@ __global__ void codebook_f16_kernel(const uint16_t *__restrict__ ck, const uint1
   }
 }
 
-template <bool KEY, int RMAX, int MP1>
+// WIDE operand image: block (slice, head) writes the slice's distance operands exactly as quant_kernel
+// lays them out in shared memory (b = w . mu as bf16 hi + lo for Keys, mu for Values, 128-byte
+// swizzled; the [-nw/2 hi, lo, 0 ...] rows), and raises the head's max |b_j| and max |nw_j| (img_max
+// zeroed beforehand; non-negative floats order as integers).
+__global__ void __launch_bounds__(256) quant_image_kernel(const uint16_t *__restrict__ cent_all,
+                                                          const float *__restrict__ w, int C, int key,
+                                                          unsigned char *__restrict__ img_all, float *img_max) {
+  __shared__ float wv[D];
+  const int sl = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const QSmem L(C, key != 0, true);
+  const int NSL = C / kSlice;
+  unsigned char *img = img_all + ((int64_t)h * NSL + sl) * L.an;
+  const uint16_t *cent = cent_all + ((int64_t)h * C + (int64_t)sl * kSlice) * D;
+  for (int c = tid; c < D; c += 256) wv[c] = (key && w) ? w[(int64_t)h * D + c] : 1.0f;
+  __syncthreads();
+  for (int e = tid; e < kSlice * (D / 8); e += 256) {
+    const int j = e / (D / 8), ci = e % (D / 8);
+    float mu[8];
+    bf16x8(*(const uint4 *)(cent + (int64_t)j * D + 8 * ci), mu);
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const float b0 = key ? __fmul_rn(wv[8 * ci + 2 * u], mu[2 * u]) : mu[2 * u];
+      const float b1 = key ? __fmul_rn(wv[8 * ci + 2 * u + 1], mu[2 * u + 1]) : mu[2 * u + 1];
+      const float h0 = __bfloat162float(__float2bfloat16_rn(b0)), h1 = __bfloat162float(__float2bfloat16_rn(b1));
+      hw[u] = (uint32_t)f32_to_bf16_rn(h0) | ((uint32_t)f32_to_bf16_rn(h1) << 16);
+      lw[u] = (uint32_t)f32_to_bf16_rn(b0 - h0) | ((uint32_t)f32_to_bf16_rn(b1 - h1) << 16);
+    }
+    const uint32_t off = (ci / 8) * kSlice * 128 + tc::sw128_offset(j, 8 * (ci % 8));
+    *(uint4 *)(img + L.bh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    if (key) *(uint4 *)(img + L.bl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  }
+  float bmax = 0.f, nwmax = 0.f;
+  for (int j = warp; j < kSlice; j += 8) {
+    float mu[4];
+    unpack4(*(const uint2 *)(cent + (int64_t)j * D + 4 * lane), mu);
+    float s = 0.f, bb = 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const float wm = __fmul_rn(wv[4 * lane + u], mu[u]);
+      s = fmaf(wm, mu[u], s);
+      bb = fmaf(wm, wm, bb);
+    }
+    s = warp_sum(s);
+    bb = warp_sum(bb);
+    if (lane < 8) {
+      uint32_t wd = 0u;
+      if (lane == 0) {
+        const float t = -0.5f * s, th = __bfloat162float(__float2bfloat16_rn(t));
+        wd = (uint32_t)f32_to_bf16_rn(th) | ((uint32_t)f32_to_bf16_rn(t - th) << 16);
+      }
+      *(uint32_t *)(img + L.bn + noswz16(j, 2 * lane)) = wd;
+    }
+    bmax = fmaxf(bmax, sqrtf(bb));
+    nwmax = fmaxf(nwmax, fabsf(s));
+  }
+  if (lane == 0) {
+    atomicMax((int *)&img_max[2 * h], __float_as_int(bmax));
+    atomicMax((int *)&img_max[2 * h + 1], __float_as_int(nwmax));
+  }
+}
+
+template <bool KEY, int RMAX, int MP1, bool WIDE>
 cudaError_t launch_one(const TensorMap128 &tmap, const QParams &p, int H, int smem, cudaStream_t st) {
   cudaError_t e =
-      cudaFuncSetAttribute(quant_kernel<KEY, RMAX, MP1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      cudaFuncSetAttribute(quant_kernel<KEY, RMAX, MP1, WIDE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  quant_kernel<KEY, RMAX, MP1><<<dim3(p.G, H), kThreads, smem, st>>>(tmap, p);
+  quant_kernel<KEY, RMAX, MP1, WIDE><<<dim3(p.G, H), kThreads, smem, st>>>(tmap, p);
   return cudaGetLastError();
+}
+
+template <bool WIDE>
+cudaError_t launch_pass(const TensorMap128 &tmap, const QParams &p, bool key, int H, int smem, cudaStream_t st) {
+  if (!key) return launch_one<false, 8, 2, WIDE>(tmap, p, H, smem, st);
+  if (p.rank <= 8 && p.top_m == 4) return launch_one<true, 8, 5, WIDE>(tmap, p, H, smem, st);
+  if (p.rank <= 8) return launch_one<true, 8, QWM_MAX_TOPM + 1, WIDE>(tmap, p, H, smem, st);
+  if (p.top_m == 4) return launch_one<true, 16, 5, WIDE>(tmap, p, H, smem, st);
+  return launch_one<true, 16, QWM_MAX_TOPM + 1, WIDE>(tmap, p, H, smem, st);
 }
 
 }  // namespace
 
+// Workspace of the WIDE operand images: [H][C / kSlice] slices (Keys' size; each a multiple of
+// 1024 bytes), then img_max [H][2].
+size_t quantize_image_bytes(int H, int C) {
+  if (C <= QWM_MAX_RESIDENT_CENTROIDS) return 0;
+  return (size_t)H * (C / kSlice) * QSmem(C, true, true).an + (size_t)H * 2 * sizeof(float);
+}
+
 cudaError_t launch_quantize(const qwm_config &cfg, const uint16_t *k, const uint16_t *v, int64_t n, const float *w,
                             const uint16_t *u_r, const qwm_chunk &out, const qwm_debug *dbg, int32_t *status,
-                            int num_sms, cudaStream_t st) {
+                            int num_sms, unsigned char *img, cudaStream_t st) {
   const int H = cfg.heads, C = cfg.n_centroids;
+  const bool wide = C > QWM_MAX_RESIDENT_CENTROIDS;
+  float *img_max = wide ? (float *)(img + (size_t)H * (C / kSlice) * QSmem(C, true, true).an) : nullptr;
   const int64_t tiles = (n + TILE - 1) / TILE;
   // one CTA per SM at most (each holds ~220 KB of shared memory): a single wave
   int G = num_sms / H;
@@ -649,6 +843,7 @@ cudaError_t launch_quantize(const qwm_config &cfg, const uint16_t *k, const uint
     p.n = n; p.w = key ? w : nullptr; p.u_r = key ? u_r : nullptr;
     p.cent = key ? out.cent_k : out.cent_v;
     p.C = C; p.top_m = cfg.top_m; p.rank = (key && u_r) ? cfg.rank : 0; p.G = G;
+    p.img = img; p.img_max = img_max;
     p.codes = key ? out.k_codes : out.v_codes; p.idx = key ? out.k_idx : out.v_idx;
     p.scale = key ? out.k_scale : out.v_scale; p.minv = key ? out.k_min : out.v_min;
     p.c = out.c; p.c_scale = out.c_scale;
@@ -656,13 +851,18 @@ cudaError_t launch_quantize(const qwm_config &cfg, const uint16_t *k, const uint
     p.dbg_cand = (key && dbg) ? dbg->cand : nullptr;
     p.dbg_score = (key && dbg) ? dbg->score : nullptr;
     p.status = status;
-    const int smem = QSmem(C, key).total + 1024;
+    const int smem = QSmem(C, key, wide).total + 1024;
     cudaError_t e;
-    if (!key) e = launch_one<false, 8, 2>(tmap, p, H, smem, st);
-    else if (p.rank <= 8 && p.top_m == 4) e = launch_one<true, 8, 5>(tmap, p, H, smem, st);
-    else if (p.rank <= 8) e = launch_one<true, 8, QWM_MAX_TOPM + 1>(tmap, p, H, smem, st);
-    else if (p.top_m == 4) e = launch_one<true, 16, 5>(tmap, p, H, smem, st);
-    else e = launch_one<true, 16, QWM_MAX_TOPM + 1>(tmap, p, H, smem, st);
+    if (wide) {  // this pass's operand image (the two passes reuse one buffer, in stream order)
+      e = cudaMemsetAsync(img_max, 0, (size_t)H * 2 * sizeof(float), st);
+      if (e != cudaSuccess) return e;
+      quant_image_kernel<<<dim3(C / kSlice, H), 256, 0, st>>>(p.cent, p.w, C, key ? 1 : 0, img, img_max);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+      e = launch_pass<true>(tmap, p, key, H, smem, st);
+    } else {
+      e = launch_pass<false>(tmap, p, key, H, smem, st);
+    }
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

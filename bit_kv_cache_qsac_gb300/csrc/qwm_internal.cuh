@@ -12,7 +12,7 @@
 #define QWM_GROUP 64       // INT2 group size supported by the kernels
 #define QWM_MAX_RANK 16
 #define QWM_MAX_TOPM 16
-#define QWM_MAX_CENTROIDS 256
+#define QWM_MAX_RESIDENT_CENTROIDS 256  // larger codebooks (1024) stream through in slices
 
 struct qwm_ctx {
   qwm_config cfg;
@@ -29,6 +29,8 @@ struct qwm_ctx {
   float *km_cent;        // [H][C][d] fp32 centroids during the iterations
   float *jac_basis;      // [H][d][d] last eigenbasis per head (Jacobi warm start)
   int32_t *jac_valid;    // [H] 1 once jac_basis holds a basis
+  unsigned char *km_img; // 1024-centroid codebooks: k-means operand slices + norms
+  unsigned char *q_img;  // 1024-centroid codebooks: quantiser operand slices + maxima
 };
 
 // record the first device-side error (kernels call this; never traps)
@@ -57,12 +59,14 @@ cudaError_t launch_jacobi(const float *S, int64_t *n, int64_t nq, int H, int ran
                           int32_t *status, float *basis, int32_t *valid, cudaStream_t st);
 #define QWM_MAX_SMS 192  // workspace sizing bound on the SM count
 int kmeans_ctas_per_head(int H, int num_sms);
+size_t kmeans_image_bytes(int H, int C);
 cudaError_t launch_kmeans(const uint16_t *x, int64_t n, int H, int C, const uint16_t *init, int iters,
                           uint16_t *cent, float *km_cent, float *km_sum, int32_t *km_cnt, int num_sms,
-                          int32_t *status, cudaStream_t st);
+                          int32_t *status, unsigned char *img, cudaStream_t st);
+size_t quantize_image_bytes(int H, int C);
 cudaError_t launch_quantize(const qwm_config &cfg, const uint16_t *k, const uint16_t *v, int64_t n,
                             const float *w, const uint16_t *u_r, const qwm_chunk &out, const qwm_debug *dbg,
-                            int32_t *status, int num_sms, cudaStream_t st);
+                            int32_t *status, int num_sms, unsigned char *img, cudaStream_t st);
 cudaError_t launch_attend(const qwm_config &cfg, const uint16_t *q, int64_t nq, const qwm_chunk *chunks,
                           int n_chunks, float scale, float *out, int num_sms, int32_t *status, cudaStream_t st);
 cudaError_t launch_dequantize(const qwm_config &cfg, const qwm_chunk &ch, uint16_t *k_hat, uint16_t *v_hat,

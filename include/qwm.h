@@ -68,7 +68,7 @@ typedef enum {
 typedef struct {
   int32_t heads;        /* H >= 1 */
   int32_t head_dim;     /* d; must be 128 */
-  int32_t n_centroids;  /* C in {64, 128, 256} (uint8 indices) */
+  int32_t n_centroids;  /* C in {64, 128, 256} (uint8 indices) or 1024 (uint16 indices) */
   int32_t group;        /* channels per INT2 group; must be 64 */
   int32_t top_m;        /* QSAC candidates M, 1..16 and <= n_centroids */
   int32_t rank;         /* PSAC rank r, 0..16 */
@@ -87,8 +87,8 @@ typedef struct {
   int32_t reserved;
   uint8_t *k_codes;      /* [H][N][d/4]: channel 4j+t -> bits 2t..2t+1 of byte j */
   uint8_t *v_codes;      /* [H][N][d/4] */
-  uint8_t *k_idx;        /* [H][N] Key centroid index */
-  uint8_t *v_idx;        /* [H][N] Value centroid index */
+  void *k_idx;           /* [H][N] Key centroid index: uint8 when C <= 256, uint16 when C = 1024 */
+  void *v_idx;           /* [H][N] Value centroid index, likewise */
   uint16_t *k_scale;     /* fp16 [H][N][G]: INT2 step s */
   uint16_t *k_min;       /* fp16 [H][N][G]: INT2 offset m (r_hat = m + s q) */
   uint16_t *v_scale;     /* fp16 [H][N][G] */

@@ -105,6 +105,26 @@ def test_kmeans_objective(q, n, C, init):
 # ------------------------------------------------------------------ steps 2-4
 
 
+# 1024-centroid cases: two heads of the ablation-shaped recipe (6 frames of 30 x 52 tokens), enough
+# tokens for a 1024-centroid codebook; these run the kernels' streamed-codebook variants.
+WIDE_W = synth.Workload("ablation-2-heads", 4, heads=2, frames=6, hs=30, ws=52, frames_per_chunk=3,
+                        nq_stats=256, nq_attend=256, n_centroids=1024)
+
+
+def test_kmeans_objective_1024_centroids(q):
+    H, n, C = 2, 2600, 1024
+    x = synth.keys(WIDE_W)[:, :n]
+    ctx = q.Context(heads=H, n_centroids=C, top_m=4)
+    cent = torch.empty(H, C, D, dtype=torch.bfloat16, device="cuda")
+    q.qwm_fit_centroids(ctx, _bf(x), n, None, cent)
+    assert q.qwm_sync_status(ctx) == 0
+    for h in range(H):
+        ref, _, _, _ = oracle.kmeans(x[h], C, None, 10)
+        j_gpu = oracle.kmeans_objective(x[h], to_u16(cent[h]))
+        j_ref = oracle.kmeans_objective(x[h], ref)
+        assert abs(j_gpu - j_ref) <= 1e-3 * j_ref, (h, j_gpu, j_ref)
+
+
 def _upstream(q, w_, H, n, C=256, top_m=4, rank=8, psac=True):
     """GPU statistics and codebooks for a small case; returns numpy and device pieces."""
     k = synth.keys(w_)[:H, :n]; v = synth.values(w_)[:H, :n]
@@ -191,19 +211,58 @@ def test_quantize_ragged_and_shapes(q, n, C, top_m, rank):
     _check_quantize(q, ctx, k, v, K, V, ch, w, ur, top_m, rank)
 
 
+@pytest.mark.parametrize("n,top_m,rank", [(2600, 4, 8), (1500, 16, 16), (1100, 1, 0)])
+def test_quantize_1024_centroids(q, n, top_m, rank):
+    ctx, k, v, K, V, ch, w, ur = _upstream(q, WIDE_W, 2, n, C=1024, top_m=top_m, rank=rank)
+    assert ch.k_idx.element_size() == 2
+    st = _check_quantize(q, ctx, k, v, K, V, ch, w, ur, top_m, rank)
+    print("tie fractions", {key: val / st["tokens"] for key, val in st.items() if key != "tokens"})
+
+
+@pytest.mark.parametrize("C", [256, 1024])
+def test_quantize_duplicated_codebook(q, C):
+    """Every centroid repeated 8 times: each token's candidate window holds at least 8 exactly tied
+    centroids, so the exact fallback resolves every token (for 1024 centroids the window reaches past
+    the kernel's list and the whole codebook is searched).  Ties go to the lower index on both sides."""
+    H, n, M = 2, 1000, 4
+    w_ = WIDE_W if C > 256 else synth.TINY
+    ctx, k, v, K, V, ch, w, ur = _upstream(q, w_, H, n, C=C, top_m=M, rank=8)
+    for cb in (ch.cent_k, ch.cent_v):
+        cb.copy_(cb[:, ::8].repeat_interleave(8, dim=1))
+    q.qwm_quantize_kv(ctx, K, V, n, w, ur, ch)
+    assert q.qwm_sync_status(ctx) == 0
+    for h in range(H):
+        wh = w[h].cpu().numpy().astype(np.float64)
+        o = oracle.quantize_head(k[h], v[h], to_u16(ch.cent_k[h]), to_u16(ch.cent_v[h]), wh,
+                                 to_u16(ur[h])[:, :8], top_m=M, rank=8)
+        gk = ch.k_idx[h].cpu().numpy().astype(np.int32)
+        gv = ch.v_idx[h].cpu().numpy().astype(np.int32)
+        # near-ties between distinct rows (not the planted exact copies) may go either way
+        uk, uv = _f32(to_u16(ch.cent_k[h][::8])), _f32(to_u16(ch.cent_v[h][::8]))
+        kx, vx = _f32(k[h]), _f32(v[h])
+        dk = np.sort(((kx[:, None, :] - uk[None]) ** 2 * wh).sum(-1), axis=1)
+        dv = np.sort(((vx[:, None, :] - uv[None]) ** 2).sum(-1), axis=1)
+        s2 = o["score2"]
+        k_free = (np.abs(dk[:, 1] - dk[:, 0]) <= TIE * dk[:, 0]) | (np.abs(s2[:, 1] - s2[:, 0]) <= TIE * np.abs(s2[:, 0]))
+        v_free = np.abs(dv[:, 1] - dv[:, 0]) <= TIE * dv[:, 0]
+        assert np.all((gk == o["idx_k"]) | k_free), (h, int(((gk != o["idx_k"]) & ~k_free).sum()))
+        assert np.all((gv == o["idx_v"]) | v_free), (h, int(((gv != o["idx_v"]) & ~v_free).sum()))
+        assert np.all(gk % 8 < M) and np.all(gv % 8 == 0)  # the lowest copies win
+
+
 # ------------------------------------------------------------------ step 5', step 5
 
 
 def _packed(q, n=1024, H=2, psac=True, C=256, rank=8):
-    ctx, k, v, K, V, ch, w, ur = _upstream(q, synth.TINY, H, n, C=C, rank=rank, psac=psac)
+    ctx, k, v, K, V, ch, w, ur = _upstream(q, WIDE_W if C > 256 else synth.TINY, H, n, C=C, rank=rank, psac=psac)
     q.qwm_quantize_kv(ctx, K, V, n, w, ur, ch)
     assert q.qwm_sync_status(ctx) == 0
     return ctx, ch
 
 
-@pytest.mark.parametrize("psac", [True, False])
-def test_dequantize_within_one_bf16_step(q, psac):
-    ctx, ch = _packed(q, psac=psac)
+@pytest.mark.parametrize("psac,C,n", [(True, 256, 1024), (False, 256, 1024), (True, 1024, 2000)])
+def test_dequantize_within_one_bf16_step(q, psac, C, n):
+    ctx, ch = _packed(q, n=n, psac=psac, C=C)
     H, n = 2, ch.n_tokens
     kh = torch.empty(H, n, D, dtype=torch.bfloat16, device="cuda"); vh = torch.empty_like(kh)
     q.qwm_dequantize(ctx, ch, kh, vh)
@@ -232,7 +291,8 @@ def test_attend_tiny(q, nq):
         assert err <= 2e-2, err
 
 
-@pytest.mark.parametrize("rank,C,n", [(16, 256, 1024), (12, 128, 777), (5, 64, 300), (0, 256, 513)])
+@pytest.mark.parametrize("rank,C,n", [(16, 256, 1024), (12, 128, 777), (5, 64, 300), (0, 256, 513),
+                                       (8, 1024, 2600), (16, 1024, 1500)])
 def test_attend_psac_ranks(q, rank, C, n):
     """PSAC ranks above 8 take the kernel's 32-column second-MMA operands (ranks 12 and 16, with
     the coefficient rows read byte by byte for 12); ranks up to 8 the 16-column ones."""
