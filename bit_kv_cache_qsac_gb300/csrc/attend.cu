@@ -123,7 +123,7 @@ __device__ __forceinline__ uint64_t pk64(uint32_t lo, uint32_t hi) {
   return d;
 }
 
-template <bool VAL>
+template <bool VAL, bool IDX16>
 __device__ __forceinline__ void load_row(const AttnChunk &c, int h, int C, int64_t k0, int nk, int r, RowData &d) {
   d.idx = -1;
   d.scl = d.mn = d.csc = 0u;
@@ -133,7 +133,7 @@ __device__ __forceinline__ void load_row(const AttnChunk &c, int h, int C, int64
   const int64_t gi = (int64_t)h * c.n + k0 + r;
   // uint16 indices for 1024-centroid codebooks; clamped to the codebook where used (no wait here)
   const uint8_t *ip = VAL ? c.v_idx : c.k_idx;
-  d.idx = C > 256 ? (int)((const uint16_t *)ip)[gi] : (int)ip[gi];
+  d.idx = IDX16 ? (int)((const uint16_t *)ip)[gi] : (int)ip[gi];
   d.scl = *(const uint32_t *)((VAL ? c.v_scale : c.k_scale) + gi * 2);
   d.mn = *(const uint32_t *)((VAL ? c.v_min : c.k_min) + gi * 2);
   const uint4 *cp = (const uint4 *)((VAL ? c.v_codes : c.k_codes) + gi * (D / 4));
@@ -306,7 +306,7 @@ __device__ __forceinline__ void write_qx_row(const AttnChunk &ch, int h, bool li
 // tile j+1 into the other stage once tile j-1 has released it, then loads the row data of tile
 // j+2.  Two register sets A and B hold the row data of alternate tiles and the loop body is
 // written twice with the sets swapped, so no register copy waits on a load.
-template <bool VAL, bool WIDE>
+template <bool VAL, bool WIDE, bool IDX16>
 __device__ __forceinline__ void producer(const AttnParams &p, unsigned char *sm, Bars &bars, int *abort_flag,
                                          uint32_t lut, int h, int64_t q0, int r, int lane) {
   volatile int *abort_v = abort_flag;
@@ -325,7 +325,7 @@ __device__ __forceinline__ void producer(const AttnParams &p, unsigned char *sm,
     const AttnChunk &c = p.ch[tt];
     const int64_t k0 = (int64_t)ti * BN;
     const int nk = (c.n - k0) < BN ? (int)(c.n - k0) : BN;
-    load_row<VAL>(c, h, C, k0, nk, r, d);
+    load_row<VAL, IDX16>(c, h, C, k0, nk, r, d);
   };
   RowData A, B;
   B.idx = -1;
@@ -378,7 +378,8 @@ __device__ __forceinline__ void producer(const AttnParams &p, unsigned char *sm,
   tc::cp_async_wait<0>();
 }
 
-template <bool WIDE>
+// WIDE: PSAC ranks above 8 (32-column second-MMA operands).  IDX16: uint16 centroid indices.
+template <bool WIDE, bool IDX16>
 __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   unsigned char *sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -610,9 +611,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
       if (!tc::mbar_wait(&bars.drain, 0, kWaitNs)) qwm_dev_error(p.status, QWM_ERR_DEVICE_TIMEOUT);
     }
   } else if (warp < kVWarp0) {
-    producer<false, WIDE>(p, sm, bars, &abort_flag, tc::smem_u32(code_lut), h, q0, tid - 32 * kKWarp0, lane);
+    producer<false, WIDE, IDX16>(p, sm, bars, &abort_flag, tc::smem_u32(code_lut), h, q0, tid - 32 * kKWarp0, lane);
   } else {
-    producer<true, WIDE>(p, sm, bars, &abort_flag, tc::smem_u32(code_lut), h, q0, tid - 32 * kVWarp0, lane);
+    producer<true, WIDE, IDX16>(p, sm, bars, &abort_flag, tc::smem_u32(code_lut), h, q0, tid - 32 * kVWarp0, lane);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -620,6 +621,15 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, 512);
   }
+}
+
+template <bool WIDE, bool IDX16>
+cudaError_t launch_variant(const AttnParams &p, dim3 grid, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel<WIDE, IDX16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       XL<WIDE>::kSmemAlloc);
+  if (e != cudaSuccess) return e;
+  attend_tc_kernel<WIDE, IDX16><<<grid, kThreads, XL<WIDE>::kSmemAlloc, st>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -649,16 +659,12 @@ cudaError_t launch_attend(const qwm_config &cfg, const uint16_t *q, int64_t nq, 
   p.n_chunks = used;
   p.total_tiles = tiles;
   const dim3 grid((unsigned)((nq + BM * NQT - 1) / (BM * NQT)), cfg.heads);
+  const bool idx16 = cfg.n_centroids > 256;
   cudaError_t e;
-  if (wide) {
-    e = cudaFuncSetAttribute(attend_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, XL<true>::kSmemAlloc);
-    if (e != cudaSuccess) return e;
-    attend_tc_kernel<true><<<grid, kThreads, XL<true>::kSmemAlloc, st>>>(p);
-  } else {
-    e = cudaFuncSetAttribute(attend_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             XL<false>::kSmemAlloc);
-    if (e != cudaSuccess) return e;
-    attend_tc_kernel<false><<<grid, kThreads, XL<false>::kSmemAlloc, st>>>(p);
-  }
+  if (wide && idx16) e = launch_variant<true, true>(p, grid, st);
+  else if (wide) e = launch_variant<true, false>(p, grid, st);
+  else if (idx16) e = launch_variant<false, true>(p, grid, st);
+  else e = launch_variant<false, false>(p, grid, st);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

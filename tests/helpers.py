@@ -36,3 +36,24 @@ def bf16_ulp_close(a_bits: np.ndarray, b: np.ndarray, ulps: float = 1.0) -> np.n
     m = np.maximum(np.abs(a), np.abs(b))
     step = np.where(m > 0, 2.0 ** (np.floor(np.log2(np.maximum(m, 1e-300))) - 7), 2.0 ** -133)
     return np.abs(a - b) <= ulps * step
+
+
+def decode_term_magnitude(ch: dict, key: bool, group: int = 64) -> np.ndarray:
+    """Sum of the magnitudes of the terms the decoder adds for every element ([n][d]):
+    |mu| + |m| + |s q| (+ sum_k |c_hat_k U_r[c, k]| for Keys).  An fp32 evaluation of a sum that
+    cancels carries an error of a few fp32 units of this, whatever the result's own size."""
+    f16 = lambda b: np.asarray(b, np.uint16).view(np.float16).astype(np.float64)
+    bf = lambda b: (np.asarray(b, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    pre = "k" if key else "v"
+    idx, codes = ch["idx_" + pre], ch[pre + "_codes"]
+    n, d = codes.shape[0], 4 * codes.shape[1]
+    q = np.zeros((n, d))
+    for c in range(d):
+        q[:, c] = (codes[:, c // 4] >> (2 * (c % 4))) & 3
+    g = np.arange(d) // group
+    s, m = f16(ch[pre + "_scale"])[:, g], f16(ch[pre + "_min"])[:, g]
+    t = np.abs(bf(ch["cent_" + pre][idx])) + np.abs(m) + np.abs(s * q)
+    if key and ch["rank"]:
+        chat = f16(ch["c_scale"])[:, None] * ch["c"].astype(np.float64)
+        t += np.abs(chat) @ np.abs(bf(ch["u_r"])).T
+    return t

@@ -10,7 +10,8 @@ tolerances do not compound.  Bars (from the method's definition of equivalence):
     those coefficients within a relative 1e-3 of the oracle's (of the token's max |C|);
   * eigenvalues within a relative 1e-3;
   * attention output: max |error| <= 2e-2 x RMS(O);
-  * decoder: within one bf16 step.
+  * decoder: within one bf16 step, or within 2^-20 x the sum of the decoded terms' magnitudes
+    where that sum cancels (the decoder evaluates in fp32).
 """
 import math
 
@@ -22,7 +23,7 @@ pytestmark = pytest.mark.gpu
 
 import oracle  # noqa: E402
 import synth  # noqa: E402
-from helpers import bf16_ulp_close, chunk_head, from_u16, to_u16  # noqa: E402
+from helpers import bf16_ulp_close, chunk_head, decode_term_magnitude, from_u16, to_u16  # noqa: E402
 
 D = 128
 TIE = 1e-5
@@ -224,7 +225,7 @@ def test_quantize_duplicated_codebook(q, C):
     """Every centroid repeated 8 times: each token's candidate window holds at least 8 exactly tied
     centroids, so the exact fallback resolves every token (for 1024 centroids the window reaches past
     the kernel's list and the whole codebook is searched).  Ties go to the lower index on both sides."""
-    H, n, M = 2, 1000, 4
+    H, n, M = 2, (1100 if C > 256 else 1000), 4
     w_ = WIDE_W if C > 256 else synth.TINY
     ctx, k, v, K, V, ch, w, ur = _upstream(q, w_, H, n, C=C, top_m=M, rank=8)
     for cb in (ch.cent_k, ch.cent_v):
@@ -268,9 +269,13 @@ def test_dequantize_within_one_bf16_step(q, psac, C, n):
     q.qwm_dequantize(ctx, ch, kh, vh)
     assert q.qwm_sync_status(ctx) == 0
     for h in range(H):
-        _, _, k64, v64 = oracle.dequantize_head(chunk_head(ch, h))
-        assert bf16_ulp_close(to_u16(kh[h]), k64).all()
-        assert bf16_ulp_close(to_u16(vh[h]), v64).all()
+        c = chunk_head(ch, h)
+        _, _, k64, v64 = oracle.dequantize_head(c)
+        # one bf16 step, plus the fp32 evaluation error where the decoder's sum cancels
+        for got, ref, key in ((kh[h], k64, True), (vh[h], v64, False)):
+            g = (to_u16(got).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+            slack = 2.0 ** -20 * decode_term_magnitude(c, key)
+            assert (bf16_ulp_close(to_u16(got), ref) | (np.abs(g - ref) <= slack)).all()
 
 
 def _attn_err(got, ref):
