@@ -474,8 +474,8 @@ def _dev_bf16(a, device):
 
 def run_ablation(device):
     """Config-4 sweep on the 480p-shaped layer (40 heads, 8 chunks of 4,680 tokens): QSAC candidates
-    M in {1, 4, 16}, PSAC rank r in {0, 8, 16}, codebook size C in {64, 256} (1024 needs 16-bit
-    indices, which this build does not implement).  Per configuration: packing time of the last
+    M in {1, 4, 16}, PSAC rank r in {0, 8, 16}, codebook size C in {64, 256, 1024} (1024: uint16
+    indices, codebook streamed through shared memory in slices).  Per configuration: packing time of the last
     chunk (k-means fit + quantise), attention time over the whole cache, and the logit error of the
     decoded cache against the original bf16 Keys on 256 Queries per head -- MSE, MSE relative to
     the mean squared logit, and the top-1 shift rate (fraction of (head, Query) whose argmax key
@@ -499,7 +499,7 @@ def run_ablation(device):
     del Kall
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     pairs = Hh * Wa.nq_attend * Wa.n_tokens
-    for C in (64, 256):
+    for C in (64, 256, 1024):
         for M in (1, 4, 16):
             for r in (0, 8, 16):
                 ctx = q.Context(heads=Hh, n_centroids=C, top_m=M, rank=r, kmeans_iters=10)
