@@ -24,6 +24,7 @@ def lib():
     l = C.CDLL(so)
     l.umma_selftest.argtypes = [C.c_void_p] * 7
     l.umma_mn_selftest.argtypes = [C.c_void_p] * 4
+    l.umma_pair_selftest.argtypes = [C.c_void_p] * 7
     return l
 
 
@@ -55,4 +56,24 @@ def test_umma_mn_major_b_operand(lib):
     rc = lib.umma_mn_selftest(P.data_ptr(), V.data_ptr(), O.data_ptr(), err.data_ptr())
     assert rc == 0 and err.item() == 0
     O_ref = P.float() @ V.float()
+    assert torch.allclose(O, O_ref, rtol=1e-4, atol=1e-3), (O - O_ref).abs().max()
+
+
+def test_umma_cta_pair(lib):
+    """cta_group::2: M = 256 split over two CTAs, B's N columns split likewise (K-major S, MN-major
+    P V with P in each CTA's tensor memory), commits multicast to both CTAs."""
+    g = torch.Generator(device="cpu").manual_seed(2)
+    A = torch.randn(256, 144, generator=g).to(torch.bfloat16).cuda()
+    B = torch.randn(128, 144, generator=g).to(torch.bfloat16).cuda()
+    P = torch.rand(256, 128, generator=g).to(torch.bfloat16).cuda()
+    V = torch.randn(128, 128, generator=g).to(torch.bfloat16).cuda()
+    S = torch.zeros(256, 128, device="cuda")
+    O = torch.zeros(256, 128, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = lib.umma_pair_selftest(A.data_ptr(), B.data_ptr(), P.data_ptr(), V.data_ptr(), S.data_ptr(),
+                                O.data_ptr(), err.data_ptr())
+    assert rc == 0 and err.item() == 0, (rc, err.item())
+    S_ref = A.float() @ B.float().T
+    O_ref = P.float() @ V.float()
+    assert torch.allclose(S, S_ref, rtol=1e-4, atol=1e-3), (S - S_ref).abs().max()
     assert torch.allclose(O, O_ref, rtol=1e-4, atol=1e-3), (O - O_ref).abs().max()
