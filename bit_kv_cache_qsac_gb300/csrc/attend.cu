@@ -219,8 +219,8 @@ __device__ __forceinline__ void decode_row(const RowData &d, uint32_t stage, int
 }
 
 // This thread's row of the second MMA's B operand: [c_hat (8 or 16) | 0 0 0 0 | mask | 0 ...].
-template <bool WIDE>
-__device__ __forceinline__ void write_x_row(const RowData &d, int R, uint32_t xs, int r) {
+template <bool WIDE, typename Row>
+__device__ __forceinline__ void write_x_row(const Row &d, int R, uint32_t xs, int r) {
   uint32_t w[16];
 #pragma unroll
   for (int i = 0; i < 16; i++) w[i] = 0u;
@@ -632,6 +632,465 @@ cudaError_t launch_variant(const AttnParams &p, dim3 grid, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+
+// ==================================================================================== CTA pairs
+// The same attention on a pair of CTAs (a cluster of two) working as one with cta_group::2 MMAs:
+// the pair takes 512 Queries, CTA c holding Query rows 256 x + 128 c .. 256 x + 128 c + 127 of its
+// two tiles x.  One M = 256 MMA covers both CTAs' rows of a tile; its B operand is split by N, so
+// CTA c decodes only Key rows 64 c .. 64 c + 63 of each 128-key tile (all channels) for Q K_hat^T,
+// and only channels 64 c .. 64 c + 63 (INT2 group c) of all 128 Value rows for P V_hat: each CTA
+// decodes half of every tile for the same 256 Queries.  The even CTA's MMA thread issues every
+// MMA; the odd CTA's producers and softmax warps arrive on the even CTA's barriers through
+// shared::cluster addresses, and the MMA commits reach both CTAs' barriers by multicast.
+constexpr int kPairQ = 2 * NQT * BM;          // Queries per pair
+constexpr int kBlkH = 64 * 128;               // a [64 rows][64 fp16] swizzled block: 8 KB
+constexpr int P_OFF_Q = 0;                    // 2 Query tiles x 2 blocks
+constexpr int P_OFF_K = P_OFF_Q + NQT * 2 * kBlk;  // 2 stages x 2 blocks [64 keys][64 ch]
+constexpr int P_OFF_V = P_OFF_K + 2 * 2 * kBlkH;   // 2 stages x [128 keys][64 ch] (MN-major B)
+constexpr int P_OFF_X = P_OFF_V + 2 * kBlk;        // 2 stages of X [64][cols], then 2 QX [128][cols]
+
+template <bool WIDE>
+struct PXL {
+  static constexpr int kXBytes = 64 * XL<WIDE>::kCols * 2;
+  static constexpr int kQXBytes = 128 * XL<WIDE>::kCols * 2;
+  static constexpr int kOffQX = P_OFF_X + 2 * kXBytes;
+  static constexpr int kSmemBytes = kOffQX + NQT * kQXBytes;
+  static constexpr int kSmemAlloc = kSmemBytes + 1024;
+};
+
+// Index data of one half row: one INT2 group's fp16 step and offset (each duplicated into a pair),
+// its 64 codes, and (Keys, group 0 only) the PSAC coefficients and their scale.
+struct HalfRow {
+  int idx;  // centroid, or -1 for a row past the end of the chunk
+  uint32_t s2, m2;
+  uint4 c;
+  uint2 ca, cb;
+  uint32_t csc;
+};
+
+template <bool VAL, bool IDX16>
+__device__ __forceinline__ void load_half(const AttnChunk &c, int h, int64_t k0, int nk, int r, int g, bool coef,
+                                          HalfRow &d) {
+  d.idx = -1;
+  d.s2 = d.m2 = d.csc = 0u;
+  d.c = make_uint4(0, 0, 0, 0);
+  d.ca = d.cb = make_uint2(0, 0);
+  if (r >= nk) return;
+  const int64_t gi = (int64_t)h * c.n + k0 + r;
+  const uint8_t *ip = VAL ? c.v_idx : c.k_idx;
+  d.idx = IDX16 ? (int)((const uint16_t *)ip)[gi] : (int)ip[gi];  // clamped where used
+  const uint32_t sv = (VAL ? c.v_scale : c.k_scale)[gi * 2 + g];
+  const uint32_t mv = (VAL ? c.v_min : c.k_min)[gi * 2 + g];
+  d.s2 = sv | (sv << 16);
+  d.m2 = mv | (mv << 16);
+  d.c = ((const uint4 *)((VAL ? c.v_codes : c.k_codes) + gi * (D / 4)))[g];
+  if (!VAL && coef && c.rank > 0) {
+    const int R = c.rank;
+    const int8_t *src = c.c + gi * R;
+    if (R == 8) {
+      d.ca = *(const uint2 *)src;
+    } else if (R == 16) {
+      const uint4 v = *(const uint4 *)src;
+      d.ca = make_uint2(v.x, v.y);
+      d.cb = make_uint2(v.z, v.w);
+    } else {
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int k = 0; k < 16; k++)
+        if (k < R) w[k >> 2] |= ((uint32_t)(uint8_t)src[k]) << (8 * (k & 3));
+      d.ca = make_uint2(w[0], w[1]);
+      d.cb = make_uint2(w[2], w[3]);
+    }
+    d.csc = c.c_scale[gi];
+  }
+}
+
+// Half rows (64 channels from channel ch0) of the centroids of this warp's 32 rows rbase .. rbase + 31
+// -> a [rows][64] swizzled block; each copy instruction moves four half rows (8 lanes each).
+__device__ __forceinline__ void issue_half_copies(const uint16_t *cent16, int h, int C, int idx, uint32_t block,
+                                                  int rbase, int ch0, int lane) {
+  const uint32_t v = (uint32_t)lane & 7u;
+#pragma unroll
+  for (int i = 0; i < 8; i++) {
+    const int rl = 4 * i + (lane >> 3);
+    int ix = __shfl_sync(0xffffffffu, idx, rl);
+    ix = ix < C ? ix : C - 1;  // never past the codebook
+    const uint32_t row = (uint32_t)(rbase + rl);
+    const uint32_t dst = block + row * 128u + ((v ^ (row & 7u)) << 4);
+    const uint16_t *src = cent16 + ((int64_t)h * C + (ix >= 0 ? ix : 0)) * D + ch0 + 8 * v;
+    tc::cp_async16_zfill(dst, src, ix >= 0 ? 16u : 0u);
+  }
+}
+
+// In-place decode of this thread's half row (one 128-byte row of a swizzled block).
+template <bool BYTE_LUT>
+__device__ __forceinline__ void decode_half(const HalfRow &d, uint32_t block, int r, uint32_t lut) {
+  if (d.idx < 0) return;  // zero-filled by the copies
+  const uint32_t rowb = block + (uint32_t)r * 128u, rx = (uint32_t)r & 7u;
+  const uint32_t words[4] = {d.c.x, d.c.y, d.c.z, d.c.w};
+#pragma unroll
+  for (int v = 0; v < 8; v++) {
+    const uint32_t addr = rowb + ((((uint32_t)v) ^ rx) << 4);
+    const uint4 mu = tc::lds128(addr);
+    const uint32_t h16 = words[v >> 1] >> (16 * (v & 1));
+    uint32_t q0, q1, q2, q3;
+    if (BYTE_LUT) {
+      const uint2 qa = tc::lds64(lut + ((h16 << 3) & 0x7F8u));
+      const uint2 qb = tc::lds64(lut + ((h16 >> 5) & 0x7F8u));
+      q0 = qa.x; q1 = qa.y; q2 = qb.x; q3 = qb.y;
+    } else {
+      q0 = tc::lds32(lut + ((h16 << 2) & 0x3Cu));
+      q1 = tc::lds32(lut + ((h16 >> 2) & 0x3Cu));
+      q2 = tc::lds32(lut + ((h16 >> 6) & 0x3Cu));
+      q3 = tc::lds32(lut + ((h16 >> 10) & 0x3Cu));
+    }
+    uint4 o;
+    o.x = tc::hadd2(mu.x, tc::hfma2(d.s2, q0, d.m2));
+    o.y = tc::hadd2(mu.y, tc::hfma2(d.s2, q1, d.m2));
+    o.z = tc::hadd2(mu.z, tc::hfma2(d.s2, q2, d.m2));
+    o.w = tc::hadd2(mu.w, tc::hfma2(d.s2, q3, d.m2));
+    tc::sts128(addr, o);
+  }
+}
+
+// Producer loop of one thread of a pair CTA (rank `cr`).  Keys: thread pr = (group g = pr / 64,
+// row pr % 64), decoding channel group g of key row 64 cr + pr % 64 of every tile.  Values: thread pr
+// = key row pr, decoding channel group cr.  Same schedule as the single-CTA producer.
+template <bool VAL, bool WIDE, bool IDX16>
+__device__ __forceinline__ void producer_pair(const AttnParams &p, unsigned char *sm, Bars &bars, int *abort_flag,
+                                              uint32_t lut, int h, int64_t qrow0, int cr, int pr, int lane) {
+  volatile int *abort_v = abort_flag;
+  const int J = p.total_tiles, C = p.C;
+  const int g = VAL ? cr : pr >> 6;              // channel group
+  const int rr = VAL ? pr : pr & 63;             // row in this CTA's block
+  const int rbase = rr - lane;                   // first row of this warp's 32
+  const int krow = VAL ? pr : 64 * cr + (pr & 63);  // key row in the tile
+  const bool coef = !VAL && g == 0;              // writes the row of the second MMA's B operand
+  uint64_t *empty = VAL ? bars.v_empty : bars.k_empty;
+  const uint32_t full0 = tc::mapa(tc::smem_u32(VAL ? &bars.v_full[0] : &bars.k_full[0]), 0);
+  const uint32_t full1 = tc::mapa(tc::smem_u32(VAL ? &bars.v_full[1] : &bars.k_full[1]), 0);
+  constexpr uint32_t kStage = VAL ? (uint32_t)kBlk : 2u * kBlkH;
+  const uint32_t block0 = tc::smem_u32(sm + (VAL ? P_OFF_V : P_OFF_K)) + (VAL ? 0u : (uint32_t)g * kBlkH);
+  const uint32_t xs0 = tc::smem_u32(sm + P_OFF_X), qx0 = tc::smem_u32(sm + PXL<WIDE>::kOffQX);
+  int t0 = 0, ti0 = 0, t1 = 0, ti1 = 0, t2 = 0, ti2 = 0;
+  auto advance = [&](int &tt, int &ti) {
+    if (++ti == p.ch[tt].tiles) { ti = 0; tt++; }
+  };
+  auto load_at = [&](int tt, int ti, HalfRow &d) {
+    const AttnChunk &c = p.ch[tt];
+    const int64_t k0 = (int64_t)ti * BN;
+    const int nk = (c.n - k0) < BN ? (int)(c.n - k0) : BN;
+    load_half<VAL, IDX16>(c, h, k0, nk, krow, g, coef, d);
+  };
+  HalfRow A, B;
+  B.idx = -1;
+  load_at(0, 0, A);
+  if (J > 1) {
+    advance(t1, ti1);
+    load_at(t1, ti1, B);
+  }
+  issue_half_copies(VAL ? p.ch[0].cent_v16 : p.ch[0].cent_k16, h, C, A.idx, block0, rbase, 64 * g, lane);
+  tc::cp_async_commit();
+  auto step = [&](int j, HalfRow &cur, const HalfRow &nxt) -> bool {
+    const int s = j & 1;
+    const AttnChunk &ch = p.ch[t0];
+    tc::cp_async_wait<0>();
+    __syncwarp();  // the warp's copies of tile j, made visible to every lane
+    decode_half<!WIDE>(cur, block0 + (uint32_t)s * kStage, rr, lut);
+    if (!VAL) {
+      if (coef) write_x_row<WIDE>(cur, ch.rank, xs0 + (uint32_t)s * PXL<WIDE>::kXBytes, rr);
+      if (ti0 == 0) {  // chunk start: the second MMA's A operand for both Query tiles
+        if (t0 > 0 && !tc::mbar_wait(&bars.qx_free, (t0 - 1) & 1, kWaitNs)) fail(abort_flag, p.status);
+        if (__any_sync(0xffffffffu, *abort_v != 0)) return false;  // warp-uniform exit
+        const uint32_t sq = tc::smem_u32(sm + P_OFF_Q);
+        write_qx_row<WIDE>(ch, h, qrow0 + pr < p.nq, sq, qx0, pr);
+        write_qx_row<WIDE>(ch, h, qrow0 + 2 * BM + pr < p.nq, sq + 2u * kBlk, qx0 + PXL<WIDE>::kQXBytes, pr);
+      }
+    }
+    tc::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive_remote(s ? full1 : full0);
+    if (j + 1 < J) {  // copies of tile j+1 into the other stage once tile j-1 has released it
+      if (j >= 1 && !tc::mbar_wait(&empty[s ^ 1], ((j - 1) >> 1) & 1, kWaitNs)) fail(abort_flag, p.status);
+      if (__any_sync(0xffffffffu, *abort_v != 0)) return false;  // warp-uniform exit
+      issue_half_copies(VAL ? p.ch[t1].cent_v16 : p.ch[t1].cent_k16, h, C, nxt.idx,
+                        block0 + (uint32_t)(s ^ 1) * kStage, rbase, 64 * g, lane);
+      tc::cp_async_commit();
+    }
+    t2 = t1; ti2 = ti1;
+    if (j + 2 < J) {
+      advance(t2, ti2);
+      load_at(t2, ti2, cur);
+    }
+    t0 = t1; ti0 = ti1;
+    t1 = t2; ti1 = ti2;
+    return true;
+  };
+  for (int j = 0; j < J; j += 2) {
+    if (!step(j, A, B)) break;
+    if (j + 1 < J && !step(j + 1, B, A)) break;
+  }
+  tc::cp_async_wait<0>();
+}
+
+template <bool WIDE, bool IDX16>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    attend_pair_kernel(const __grid_constant__ AttnParams p) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  unsigned char *sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+  __shared__ Bars bars;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag;
+  __shared__ __align__(64) uint32_t code_lut[WIDE ? 16 : 512];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.y;
+  const int cr = (int)tc::cluster_ctarank();
+  const int64_t qb = (int64_t)(blockIdx.x >> 1) * kPairQ + (int64_t)cr * BM;  // this CTA's row 0 of tile 0
+  volatile int *abort_v = &abort_flag;
+
+  // ---- this CTA's two Query tiles (rows qb + 256 x + rr) -> shared memory as fp16 ----
+  for (int e = tid; e < NQT * BM * (D / 8); e += kThreads) {
+    const int row = e / (D / 8), ci = e % (D / 8);
+    const int x = row / BM, rr = row % BM, b = ci / 8;
+    const int64_t qi = qb + (int64_t)x * 2 * BM + rr;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (qi < p.nq) v = *(const uint4 *)(p.q + ((int64_t)h * p.nq + qi) * D + 8 * ci);
+    const uint32_t bw[4] = {v.x, v.y, v.z, v.w};
+    uint32_t hw[4];
+#pragma unroll
+    for (int u = 0; u < 4; u++) hw[u] = f16pair(__uint_as_float(bw[u] << 16), __uint_as_float(bw[u] & 0xFFFF0000u));
+    *(uint4 *)(sm + P_OFF_Q + (x * 2 + b) * kBlk + tc::sw128_offset(rr, 8 * (ci % 8))) =
+        make_uint4(hw[0], hw[1], hw[2], hw[3]);
+  }
+  if (!WIDE && tid < 256) {
+    uint32_t f[4];
+#pragma unroll
+    for (int t = 0; t < 4; t++) f[t] = ((0x42403C00u >> (8 * ((tid >> (2 * t)) & 3))) & 0xFFu) << 8;
+    code_lut[2 * tid] = f[0] | (f[1] << 16);
+    code_lut[2 * tid + 1] = f[2] | (f[3] << 16);
+  }
+  if (WIDE && tid < 16) {
+    const uint32_t lo = ((0x42403C00u >> (8 * (tid & 3))) & 0xFFu) << 8;
+    const uint32_t hi = ((0x42403C00u >> (8 * (tid >> 2))) & 0xFFu) << 8;
+    code_lut[tid] = lo | (hi << 16);
+  }
+  if (tid == 0) {
+    for (int i = 0; i < 2; i++) {
+      tc::mbar_init(&bars.k_full[i], 2 * kProdWarps);  // both CTAs' producer warps (even CTA's copy used)
+      tc::mbar_init(&bars.v_full[i], 2 * kProdWarps);
+      tc::mbar_init(&bars.k_empty[i], 1);
+      tc::mbar_init(&bars.v_empty[i], 1);
+      tc::mbar_init(&bars.s_full[i], 1);
+      tc::mbar_init(&bars.p_ready[i], 8);              // both CTAs' 4 softmax warps of tile i
+    }
+    tc::mbar_init(&bars.qx_free, 1);
+    tc::mbar_init(&bars.o_done, 1);
+    tc::mbar_init(&bars.drain, 1);
+    abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tc::tmem_alloc2(&tmem_base_sh, 512);
+    tc::tmem_relinquish2();
+  }
+  tc::fence_proxy_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::cluster_sync();  // both CTAs' barriers exist before the first arrival from the peer
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_base_sh;
+  const int J = p.total_tiles;
+
+  if (warp < kSoftmaxWarps) {
+    // ======================= softmax (Query tile x, row = TMEM lane) =======================
+    const int x = warp / 4, sub = warp % 4, row = 32 * sub + lane;
+    const uint32_t lane_addr = (uint32_t)(32 * sub) << 16;
+    const uint32_t tS = tmem + lane_addr + 128u * x, tO = tmem + lane_addr + 256u + 128u * x;
+    const uint32_t p_ready0 = tc::mapa(tc::smem_u32(&bars.p_ready[x]), 0);
+    const float sl2 = p.scale_log2;
+    float m_used = -INFINITY;
+    uint64_t acc0 = 0ull, acc1 = 0ull;
+    const uint64_t sc2 = pk64(__float_as_uint(sl2), __float_as_uint(sl2));
+    bool ok = true;
+    for (int j = 0; j < J; j++) {
+      if (!tc::mbar_wait(&bars.s_full[x], j & 1, kWaitNs)) fail(&abort_flag, p.status);
+      if (*abort_v) { ok = false; break; }
+      tc::fence_after_sync();
+      uint32_t r[32];
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll 1
+      for (int cq = 0; cq < 4; cq++) {
+        tc::tmem_ld16(tS + 32u * cq, r);
+        tc::tmem_ld16(tS + 32u * cq + 16u, r + 16);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; i += 8) {
+          mx0 = tc::max3(mx0, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+          mx1 = tc::max3(mx1, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+          mx2 = tc::max3(mx2, __uint_as_float(r[i + 4]), __uint_as_float(r[i + 5]));
+          mx3 = tc::max3(mx3, __uint_as_float(r[i + 6]), __uint_as_float(r[i + 7]));
+        }
+      }
+      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      const float m_new = fmaxf(m_used, mx * sl2);
+      if (__any_sync(0xffffffffu, m_new > m_used + kRescaleThreshold)) {
+        if (j > 0) {
+          const float alpha = tc::ex2_approx(m_used - m_new);
+          const uint64_t a2 = pk64(__float_as_uint(alpha), __float_as_uint(alpha));
+          acc0 = tc::fma2(acc0, a2, 0ull);
+          acc1 = tc::fma2(acc1, a2, 0ull);
+#pragma unroll 1
+          for (int c = 0; c < D; c += 32) {
+            uint32_t o[32];
+            tc::tmem_ld32(tO + c, o);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; i++) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tc::tmem_st32(tO + c, o);
+          }
+        }
+        m_used = m_new;
+      }
+      const uint64_t nm2 = pk64(__float_as_uint(-m_used), __float_as_uint(-m_used));
+#pragma unroll 1
+      for (int cq = 0; cq < 4; cq++) {
+        tc::tmem_ld16(tS + 32u * cq, r);
+        tc::tmem_ld16(tS + 32u * cq + 16u, r + 16);
+        tc::tmem_ld_wait();
+        uint32_t pw[16];
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+          const uint64_t x2 = tc::fma2(pk64(r[2 * i], r[2 * i + 1]), sc2, nm2);
+          const float e0 = tc::ex2_approx(tc::f2lo(x2)), e1 = tc::ex2_approx(tc::f2hi(x2));
+          const uint64_t e2 = pk64(__float_as_uint(e0), __float_as_uint(e1));
+          if (i & 1) acc1 = tc::add2(acc1, e2);
+          else acc0 = tc::add2(acc0, e2);
+          pw[i] = f16pair(e0, e1);
+        }
+        tc::tmem_st16(tS + 16u * cq, pw);
+      }
+      tc::tmem_st_wait();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_remote(p_ready0);
+    }
+    if (ok && !tc::mbar_wait(&bars.o_done, 0, kWaitNs)) fail(&abort_flag, p.status);
+    if (ok && !*abort_v) {
+      tc::fence_after_sync();
+      const uint64_t lsum = tc::add2(acc0, acc1);
+      const float l = tc::f2lo(lsum) + tc::f2hi(lsum);
+      const int64_t qi = qb + (int64_t)x * 2 * BM + row;
+      const float inv = 1.f / l;
+      uint32_t o[32];
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        tc::tmem_ld32(tO + c, o);
+        tc::tmem_ld_wait();
+        if (qi < p.nq) {
+          float4 *dst = (float4 *)(p.out + ((int64_t)h * p.nq + qi) * D + c);
+#pragma unroll
+          for (int v = 0; v < 8; v++)
+            dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
+                                 __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ======================= MMA issue: one thread of the even CTA, for the pair =======================
+    if (cr == 0 && lane == 0) {
+      const uint32_t idesc = tc::idesc_f16_f32(2 * BM, BN);
+      const uint32_t idesc_pv = tc::idesc_f16_f32_bmn(2 * BM, D);
+      const uint32_t tS[2] = {tmem, tmem + 128u}, tO[2] = {tmem + 256u, tmem + 384u};
+      const uint32_t sQ = tc::smem_u32(sm + P_OFF_Q), sK = tc::smem_u32(sm + P_OFF_K), sV = tc::smem_u32(sm + P_OFF_V);
+      const uint32_t sX = tc::smem_u32(sm + P_OFF_X), sQX = tc::smem_u32(sm + PXL<WIDE>::kOffQX);
+      constexpr uint16_t kBoth = 3;
+      int t = 0, tile_in_chunk = 0, prev_stage = 0;
+      bool ok = true;
+      auto qk = [&](int x, int s, int nx) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; kk++) {
+          const uint32_t qo = (uint32_t)((kk / 4) * kBlk + 32 * (kk % 4));
+          const uint32_t ko = (uint32_t)((kk / 4) * kBlkH + 32 * (kk % 4));
+          tc::mma2_ss(tS[x], tc::desc_sw128(sQ + (x * 2) * kBlk + qo), tc::desc_sw128(sK + s * 2 * kBlkH + ko), idesc,
+                      kk > 0);
+        }
+        for (int ks = 0; ks < nx; ks++)
+          tc::mma2_ss(tS[x], tc::desc_noswz(sQX + x * PXL<WIDE>::kQXBytes + 256u * ks, 128, XL<WIDE>::kSbo),
+                      tc::desc_noswz(sX + s * PXL<WIDE>::kXBytes + 256u * ks, 128, XL<WIDE>::kSbo), idesc, 1);
+      };
+      auto pv = [&](int x, int s, bool first) {
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; kk++)
+          tc::mma2_ts(tO[x], tS[x] + 8u * kk, tc::desc_sw128_mn(sV + s * kBlk + 2048u * kk, kBlk, 1024), idesc_pv,
+                      (!first || kk > 0));
+      };
+      for (int j = 0; j < J; j++) {
+        const int s = j & 1;
+        const AttnChunk &ch = p.ch[t];
+        const int nx = (WIDE && ch.rank > 8) ? 2 : 1;
+        ok = tc::mbar_wait_cluster(&bars.k_full[s], (j >> 1) & 1, kWaitNs) && !*abort_v;
+        if (!ok) break;
+        tc::fence_after_sync();
+        qk(0, s, nx);
+        tc::mma2_commit(&bars.s_full[0], kBoth);
+        if (j > 0) {
+          ok = tc::mbar_wait_cluster(&bars.p_ready[1], (j - 1) & 1, kWaitNs) && !*abort_v;
+          if (!ok) break;
+          tc::fence_after_sync();
+          pv(1, prev_stage, j - 1 == 0);
+          tc::mma2_commit(&bars.v_empty[prev_stage], kBoth);
+        }
+        qk(1, s, nx);
+        tc::mma2_commit(&bars.s_full[1], kBoth);
+        tc::mma2_commit(&bars.k_empty[s], kBoth);
+        const bool last_of_chunk = tile_in_chunk + 1 == ch.tiles;
+        if (last_of_chunk) tc::mma2_commit(&bars.qx_free, kBoth);
+        ok = tc::mbar_wait_cluster(&bars.v_full[s], (j >> 1) & 1, kWaitNs) &&
+             tc::mbar_wait_cluster(&bars.p_ready[0], j & 1, kWaitNs) && !*abort_v;
+        if (!ok) break;
+        tc::fence_after_sync();
+        pv(0, s, j == 0);
+        prev_stage = s;
+        if (last_of_chunk) { tile_in_chunk = 0; t++; }
+        else tile_in_chunk++;
+      }
+      if (ok && J > 0) {
+        ok = tc::mbar_wait_cluster(&bars.p_ready[1], (J - 1) & 1, kWaitNs) && !*abort_v;
+        if (ok) {
+          tc::fence_after_sync();
+          pv(1, prev_stage, J - 1 == 0);
+          tc::mma2_commit(&bars.o_done, kBoth);
+        }
+      }
+      if (!ok) fail(&abort_flag, p.status);
+      tc::mma2_commit(&bars.drain, 1);  // every MMA issued above completes before TMEM is released
+      if (!tc::mbar_wait(&bars.drain, 0, kWaitNs)) qwm_dev_error(p.status, QWM_ERR_DEVICE_TIMEOUT);
+    }
+  } else if (warp < kVWarp0) {
+    producer_pair<false, WIDE, IDX16>(p, sm, bars, &abort_flag, tc::smem_u32(code_lut), h, qb, cr,
+                                      tid - 32 * kKWarp0, lane);
+  } else {
+    producer_pair<true, WIDE, IDX16>(p, sm, bars, &abort_flag, tc::smem_u32(code_lut), h, qb, cr,
+                                     tid - 32 * kVWarp0, lane);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::cluster_sync();  // the peer has finished with this CTA's barriers, shared and tensor memory
+  if (warp == kMmaWarp) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc2(tmem, 512);
+  }
+}
+
+template <bool WIDE, bool IDX16>
+cudaError_t launch_pair(const AttnParams &p, dim3 grid, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(attend_pair_kernel<WIDE, IDX16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       PXL<WIDE>::kSmemAlloc);
+  if (e != cudaSuccess) return e;
+  attend_pair_kernel<WIDE, IDX16><<<grid, kThreads, PXL<WIDE>::kSmemAlloc, st>>>(p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_attend(const qwm_config &cfg, const uint16_t *q, int64_t nq, const qwm_chunk *chunks,
@@ -658,13 +1117,13 @@ cudaError_t launch_attend(const qwm_config &cfg, const uint16_t *q, int64_t nq, 
   }
   p.n_chunks = used;
   p.total_tiles = tiles;
-  const dim3 grid((unsigned)((nq + BM * NQT - 1) / (BM * NQT)), cfg.heads);
   const bool idx16 = cfg.n_centroids > 256;
   cudaError_t e;
-  if (wide && idx16) e = launch_variant<true, true>(p, grid, st);
-  else if (wide) e = launch_variant<true, false>(p, grid, st);
-  else if (idx16) e = launch_variant<false, true>(p, grid, st);
-  else e = launch_variant<false, false>(p, grid, st);
+  const dim3 grid((unsigned)(2 * ((nq + kPairQ - 1) / kPairQ)), cfg.heads);  // CTA pairs
+  if (wide && idx16) e = launch_pair<true, true>(p, grid, st);
+  else if (wide) e = launch_pair<true, false>(p, grid, st);
+  else if (idx16) e = launch_pair<false, true>(p, grid, st);
+  else e = launch_pair<false, false>(p, grid, st);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
