@@ -17,25 +17,36 @@
 // O is written in fp32: the output is an average over thousands of keys, its largest entries are
 // ~16x its RMS, and rounding those to bf16 alone would cost ~0.03 x RMS(O).
 //
-// One CTA = one head x 256 Queries (two 128-row tiles that share every decoded K/V tile).
-// Warp roles (17 warps):
+// Work split: a pair of CTAs (a cluster of two, cta_group::2 MMAs) takes one head x 512 Queries;
+// CTA c of the pair holds Query rows 256 x + 128 c .. 256 x + 128 c + 127 of its two tiles x = 0, 1.
+// One M = 256 MMA covers both CTAs' rows of a tile.  Its B operand is split by N, so CTA c decodes
+// only Key rows 64 c .. 64 c + 63 of each 128-key tile (all channels) for Q K_hat^T, and only
+// channels 64 c .. 64 c + 63 (INT2 group c) of all 128 Value rows for P V_hat: each CTA decodes half
+// of every tile for its 256 Queries.
+// Warp roles of each CTA (17 warps):
 //   warps 0-3, 4-7  softmax for Query tile 0 / 1: thread = Query row = TMEM lane; reads the
 //                   logits from TMEM, keeps the running max and sum, writes P (fp16) over the
 //                   logits, rescales O in TMEM when the max grows by more than 2^8;
-//   warp 8          allocates TMEM and issues every tcgen05.mma (one thread);
-//   warps 9-12      Key producers: thread = key row of the tile; copies the row's centroid
-//                   (cp.async, 16 bytes at a time) into the 128-byte-swizzled K-major stage,
-//                   decodes it in place, writes the row of the second MMA's B operand, and at
-//                   each chunk start builds the second MMA's A operand for both Query tiles;
-//   warps 13-16     Value producers: the same for V_hat rows ([key][d], read as an N-major B).
+//   warp 8          allocates the pair's TMEM; in the even CTA, one thread issues every MMA of the
+//                   pair;
+//   warps 9-12      Key producers: thread = (channel group, key row); copies that half row of the
+//                   row's centroid (cp.async, 16 bytes at a time) into the 128-byte-swizzled K-major
+//                   stage, decodes it in place; group-0 threads write the row of the second MMA's B
+//                   operand; at each chunk start every thread builds one row of its A operand for
+//                   both Query tiles;
+//   warps 13-16     Value producers: thread = key row, channel group c ([key][d], read as an
+//                   MN-major B).
 // Each producer thread keeps its row's index data two tiles ahead in registers and its centroid
-// copies one tile ahead in the other shared-memory stage.
-// Tensor memory (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each; P_x overlays S_x.
-// MMA order per tile j: S0(j), PV1(j-1), S1(j), PV0(j).  tcgen05 operations complete in issue
-// order, so the commit after S_x(j) also certifies PV_x(j-1): when softmax x sees S_x(j), O_x
-// is stable and may be rescaled.
+// copies one tile ahead in the next of three shared-memory stages.
+// The odd CTA's producers and softmax warps arrive on the even CTA's barriers through
+// shared::cluster addresses; the MMA commits reach both CTAs' barriers by multicast.
+// Tensor memory (512 columns in each CTA): S0 | S1 | O0 | O1, 128 fp32 columns each; P_x overlays
+// S_x.  MMA order per tile j: S0(j), PV1(j-1), S1(j), PV0(j).  tcgen05 operations complete in
+// issue order, so the commit after S_x(j) also certifies PV_x(j-1): when softmax x sees S_x(j),
+// O_x is stable and may be rescaled.
 // Every wait is bounded (about one second of wall time); on expiry the CTA records
-// QWM_ERR_DEVICE_TIMEOUT, every role stops, outstanding MMAs are drained and TMEM is freed.
+// QWM_ERR_DEVICE_TIMEOUT, every role stops, outstanding MMAs are drained, the pair meets at a
+// cluster barrier and TMEM is freed.
 #include <cuda_fp16.h>
 
 #include "qwm_internal.cuh"
@@ -52,25 +63,30 @@ constexpr uint64_t kWaitNs = 1000000000ull;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
 constexpr uint32_t kMaskBits = 0xFB53u;    // fp16 -60000
 
-// shared-memory map (bytes from a 1024-aligned base)
-constexpr int kBlk = BM * 128;                  // one [128 rows][64 fp16] swizzled block: 16 KB
-constexpr int OFF_Q = 0;                        // 2 Query tiles x 2 blocks
-constexpr int OFF_K = OFF_Q + NQT * 2 * kBlk;   // 2 stages x 2 blocks of K rows
-constexpr int OFF_V = OFF_K + 2 * 2 * kBlk;     // 2 stages x 2 blocks of V rows
-constexpr int OFF_X = OFF_V + 2 * 2 * kBlk;     // 2 stages: B operand of the second MMA, then
-                                                // 2 Query tiles: its A operand
+constexpr int kStages = 3;                 // K / V / X stages in shared memory
+constexpr int kPairQ = 2 * NQT * BM;       // Queries per CTA pair
 
-// Layout of the second MMA's operands: [128 rows][16 or 32 fp16 columns], K-major without swizzle
-// (8x8 core matrices, 128 bytes apart along K and 16 x columns bytes apart along the rows).  The
-// narrow form (every chunk of the call has PSAC rank <= 8) leaves room for a byte-indexed code
-// table; the wide form serves ranks up to 16.
+// shared-memory map of one CTA (bytes from a 1024-aligned base)
+constexpr int kBlk = BM * 128;             // a [128 rows][64 fp16] swizzled block: 16 KB
+constexpr int kBlkH = 64 * 128;            // a [64 rows][64 fp16] swizzled block: 8 KB
+constexpr int OFF_Q = 0;                   // 2 Query tiles x 2 blocks (channels 0-63, 64-127)
+constexpr int OFF_K = OFF_Q + NQT * 2 * kBlk;          // stages x 2 blocks [64 keys][64 ch]
+constexpr int OFF_V = OFF_K + kStages * 2 * kBlkH;     // stages x [128 keys][64 ch] (MN-major B)
+constexpr int OFF_X = OFF_V + kStages * kBlk;          // stages of X [64][cols], then 2 QX [128][cols]
+
+// Layout of the second MMA's operands, X = [c_hat | 0 | mask] rows of keys and QX = [q U_r | 0 | 1]
+// rows of Queries: [rows][16 or 32 fp16 columns], K-major without swizzle (8x8 core matrices, 128
+// bytes apart along K and 16 x columns bytes apart along the rows).  The narrow form (every chunk
+// of the call has PSAC rank <= 8) leaves room for a byte-indexed code table; the wide form serves
+// ranks up to 16.
 template <bool WIDE>
 struct XL {
   static constexpr int kCols = WIDE ? 32 : 16;
-  static constexpr int kBytes = 128 * kCols * 2;
   static constexpr uint32_t kSbo = 16u * kCols;
-  static constexpr int kOffQX = OFF_X + 2 * kBytes;
-  static constexpr int kSmemBytes = kOffQX + NQT * kBytes;
+  static constexpr int kXBytes = 64 * kCols * 2;    // one X stage: this CTA's 64 key rows
+  static constexpr int kQXBytes = 128 * kCols * 2;  // one QX tile: this CTA's 128 Query rows
+  static constexpr int kOffQX = OFF_X + kStages * kXBytes;
+  static constexpr int kSmemBytes = kOffQX + NQT * kQXBytes;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;
   __host__ __device__ static constexpr uint32_t off(uint32_t row, uint32_t k) {
     return (row >> 3) * kSbo + (k >> 3) * 128u + (row & 7u) * 16u + (k & 7u) * 2u;
@@ -97,125 +113,20 @@ struct AttnParams {
 };
 
 struct Bars {
-  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_ready[2], qx_free, o_done, drain;
-};
-
-// Index data of one key row: fp16 scale and offset pairs (group 0 low half), 128 2-bit codes,
-// and (Keys) the PSAC coefficients and their scale.
-struct RowData {
-  int idx;  // centroid, or -1 for a row past the end of the chunk
-  uint32_t scl, mn;
-  uint4 c0, c1;
-  uint2 ca, cb;  // coefficients 0-7 and 8-15
-  uint32_t csc;
+  uint64_t k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
+  uint64_t s_full[2], p_ready[2], qx_free, o_done, drain;
 };
 
 __device__ __forceinline__ void fail(int *abort_flag, int32_t *status) {
   *(volatile int *)abort_flag = 1;
   qwm_dev_error(status, QWM_ERR_DEVICE_TIMEOUT);
 }
-
 __device__ __forceinline__ uint32_t f16pair(float lo, float hi) { return tc::pack_f16x2(lo, hi); }
 // two 32-bit registers as one 64-bit operand of the packed fp32 instructions
 __device__ __forceinline__ uint64_t pk64(uint32_t lo, uint32_t hi) {
   uint64_t d;
   asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
   return d;
-}
-
-template <bool VAL, bool IDX16>
-__device__ __forceinline__ void load_row(const AttnChunk &c, int h, int C, int64_t k0, int nk, int r, RowData &d) {
-  d.idx = -1;
-  d.scl = d.mn = d.csc = 0u;
-  d.c0 = d.c1 = make_uint4(0, 0, 0, 0);
-  d.ca = d.cb = make_uint2(0, 0);
-  if (r >= nk) return;
-  const int64_t gi = (int64_t)h * c.n + k0 + r;
-  // uint16 indices for 1024-centroid codebooks; clamped to the codebook where used (no wait here)
-  const uint8_t *ip = VAL ? c.v_idx : c.k_idx;
-  d.idx = IDX16 ? (int)((const uint16_t *)ip)[gi] : (int)ip[gi];
-  d.scl = *(const uint32_t *)((VAL ? c.v_scale : c.k_scale) + gi * 2);
-  d.mn = *(const uint32_t *)((VAL ? c.v_min : c.k_min) + gi * 2);
-  const uint4 *cp = (const uint4 *)((VAL ? c.v_codes : c.k_codes) + gi * (D / 4));
-  d.c0 = cp[0];
-  d.c1 = cp[1];
-  if (!VAL && c.rank > 0) {
-    const int R = c.rank;
-    const int8_t *src = c.c + gi * R;
-    if (R == 8) {
-      d.ca = *(const uint2 *)src;  // row offset 8 gi: 8-byte aligned
-    } else if (R == 16) {
-      const uint4 v = *(const uint4 *)src;
-      d.ca = make_uint2(v.x, v.y);
-      d.cb = make_uint2(v.z, v.w);
-    } else {
-      uint32_t w[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-      for (int k = 0; k < 16; k++)
-        if (k < R) w[k >> 2] |= ((uint32_t)(uint8_t)src[k]) << (8 * (k & 3));
-      d.ca = make_uint2(w[0], w[1]);
-      d.cb = make_uint2(w[2], w[3]);
-    }
-    d.csc = c.c_scale[gi];
-  }
-}
-
-// Centroid rows of this warp's 32 tile rows (rbase .. rbase + 31) -> a swizzled stage; `idx` is
-// the calling lane's row's centroid (< 0: zeros).  Each copy instruction moves two whole rows
-// (lanes 0-15 and 16-31, 16 bytes each), so a row is fetched as two full 128-byte lines.
-// The caller makes the copies visible to the other lanes (wait_group, then __syncwarp) before
-// any lane reads them.
-__device__ __forceinline__ void issue_warp_copies(const uint16_t *cent16, int h, int C, int idx, uint32_t stage,
-                                                  int rbase, int lane) {
-  const uint32_t v = (uint32_t)lane & 15u;
-#pragma unroll
-  for (int i = 0; i < 16; i++) {
-    const int rl = 2 * i + (lane >> 4);
-    int ix = __shfl_sync(0xffffffffu, idx, rl);
-    ix = ix < C ? ix : C - 1;  // never past the codebook
-    const uint32_t row = (uint32_t)(rbase + rl);
-    const uint32_t dst = stage + (v >> 3) * kBlk + row * 128u + (((v & 7u) ^ (row & 7u)) << 4);
-    const uint16_t *src = cent16 + ((int64_t)h * C + (ix >= 0 ? ix : 0)) * D + 8 * v;
-    tc::cp_async16_zfill(dst, src, ix >= 0 ? 16u : 0u);
-  }
-}
-
-// In-place decode of this thread's row: fp16(mu + fp16(m + s q)).  BYTE_LUT: `lut` maps a byte of 4 codes to two fp16 pairs (8 bytes per entry);
-// otherwise it maps a 4-bit code pair to one fp16 pair (q_even, q_odd).
-template <bool BYTE_LUT>
-__device__ __forceinline__ void decode_row(const RowData &d, uint32_t stage, int r, uint32_t lut) {
-  if (d.idx < 0) return;  // zero-filled by the copies
-  const uint32_t rowb = stage + (uint32_t)r * 128u, rx = (uint32_t)r & 7u;
-#pragma unroll
-  for (int g = 0; g < 2; g++) {
-    const uint32_t s2 = __byte_perm(d.scl, 0u, g ? 0x3232u : 0x1010u);
-    const uint32_t m2 = __byte_perm(d.mn, 0u, g ? 0x3232u : 0x1010u);
-    const uint4 cw = g ? d.c1 : d.c0;
-    const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-#pragma unroll
-    for (int v = 0; v < 8; v++) {
-      const uint32_t addr = rowb + (uint32_t)g * kBlk + ((((uint32_t)v) ^ rx) << 4);
-      const uint4 mu = tc::lds128(addr);
-      const uint32_t h16 = words[v >> 1] >> (16 * (v & 1));
-      uint32_t q0, q1, q2, q3;
-      if (BYTE_LUT) {
-        const uint2 qa = tc::lds64(lut + ((h16 << 3) & 0x7F8u));
-        const uint2 qb = tc::lds64(lut + ((h16 >> 5) & 0x7F8u));
-        q0 = qa.x; q1 = qa.y; q2 = qb.x; q3 = qb.y;
-      } else {
-        q0 = tc::lds32(lut + ((h16 << 2) & 0x3Cu));
-        q1 = tc::lds32(lut + ((h16 >> 2) & 0x3Cu));
-        q2 = tc::lds32(lut + ((h16 >> 6) & 0x3Cu));
-        q3 = tc::lds32(lut + ((h16 >> 10) & 0x3Cu));
-      }
-      uint4 o;
-      o.x = tc::hadd2(mu.x, tc::hfma2(s2, q0, m2));
-      o.y = tc::hadd2(mu.y, tc::hfma2(s2, q1, m2));
-      o.z = tc::hadd2(mu.z, tc::hfma2(s2, q2, m2));
-      o.w = tc::hadd2(mu.w, tc::hfma2(s2, q3, m2));
-      tc::sts128(addr, o);
-    }
-  }
 }
 
 // This thread's row of the second MMA's B operand: [c_hat (8 or 16) | 0 0 0 0 | mask | 0 ...].
@@ -300,363 +211,6 @@ __device__ __forceinline__ void write_qx_row(const AttnChunk &ch, int h, bool li
     tc::sts128(dst + XL<WIDE>::off((uint32_t)rr, 8u * kc),
                make_uint4(w[4 * kc], w[4 * kc + 1], w[4 * kc + 2], w[4 * kc + 3]));
 }
-
-// Key (VAL = false) or Value (VAL = true) producer loop of one thread (row r of every tile).
-// Step j decodes tile j (its copies were issued one step earlier), then issues the copies of
-// tile j+1 into the other stage once tile j-1 has released it, then loads the row data of tile
-// j+2.  Two register sets A and B hold the row data of alternate tiles and the loop body is
-// written twice with the sets swapped, so no register copy waits on a load.
-template <bool VAL, bool WIDE, bool IDX16>
-__device__ __forceinline__ void producer(const AttnParams &p, unsigned char *sm, Bars &bars, int *abort_flag,
-                                         uint32_t lut, int h, int64_t q0, int r, int lane) {
-  volatile int *abort_v = abort_flag;
-  const int J = p.total_tiles, C = p.C, rbase = r - lane;
-  uint64_t *full = VAL ? bars.v_full : bars.k_full;
-  uint64_t *empty = VAL ? bars.v_empty : bars.k_empty;
-  const uint32_t stage0 = tc::smem_u32(sm + (VAL ? OFF_V : OFF_K));
-  const uint32_t xs0 = tc::smem_u32(sm + OFF_X), qx0 = tc::smem_u32(sm + XL<WIDE>::kOffQX);
-  constexpr int kXBytes = XL<WIDE>::kBytes;
-  // positions (chunk, tile in chunk) of tiles j, j+1, j+2
-  int t0 = 0, ti0 = 0, t1 = 0, ti1 = 0, t2 = 0, ti2 = 0;
-  auto advance = [&](int &tt, int &ti) {
-    if (++ti == p.ch[tt].tiles) { ti = 0; tt++; }
-  };
-  auto load_at = [&](int tt, int ti, RowData &d) {
-    const AttnChunk &c = p.ch[tt];
-    const int64_t k0 = (int64_t)ti * BN;
-    const int nk = (c.n - k0) < BN ? (int)(c.n - k0) : BN;
-    load_row<VAL, IDX16>(c, h, C, k0, nk, r, d);
-  };
-  RowData A, B;
-  B.idx = -1;
-  load_at(0, 0, A);
-  if (J > 1) {
-    advance(t1, ti1);
-    load_at(t1, ti1, B);
-  }
-  issue_warp_copies(VAL ? p.ch[0].cent_v16 : p.ch[0].cent_k16, h, C, A.idx, stage0, rbase, lane);
-  tc::cp_async_commit();
-  auto step = [&](int j, RowData &cur, const RowData &nxt) -> bool {
-    const int s = j & 1;
-    const AttnChunk &ch = p.ch[t0];
-    tc::cp_async_wait<0>();
-    __syncwarp();  // the warp's copies of tile j, made visible to every lane
-    decode_row<!WIDE>(cur, stage0 + (uint32_t)s * 2u * kBlk, r, lut);
-    if (!VAL) {
-      write_x_row<WIDE>(cur, ch.rank, xs0 + (uint32_t)s * kXBytes, r);
-      if (ti0 == 0) {  // chunk start: the second MMA's A operand for both Query tiles
-        if (t0 > 0 && !tc::mbar_wait(&bars.qx_free, (t0 - 1) & 1, kWaitNs)) fail(abort_flag, p.status);
-        if (__any_sync(0xffffffffu, *abort_v != 0)) return false;  // warp-uniform exit
-        const uint32_t sq = tc::smem_u32(sm + OFF_Q);
-        write_qx_row<WIDE>(ch, h, q0 + r < p.nq, sq, qx0, r);
-        write_qx_row<WIDE>(ch, h, q0 + BM + r < p.nq, sq + 2u * kBlk, qx0 + kXBytes, r);
-      }
-    }
-    tc::fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) tc::mbar_arrive(&full[s]);
-    if (j + 1 < J) {  // copies of tile j+1 into the other stage once tile j-1 has released it
-      if (j >= 1 && !tc::mbar_wait(&empty[s ^ 1], ((j - 1) >> 1) & 1, kWaitNs)) fail(abort_flag, p.status);
-      if (__any_sync(0xffffffffu, *abort_v != 0)) return false;  // warp-uniform exit
-      issue_warp_copies(VAL ? p.ch[t1].cent_v16 : p.ch[t1].cent_k16, h, C, nxt.idx,
-                        stage0 + (uint32_t)(s ^ 1) * 2u * kBlk, rbase, lane);
-      tc::cp_async_commit();
-    }
-    t2 = t1; ti2 = ti1;
-    if (j + 2 < J) {  // row data of tile j+2 (decoded two steps from now)
-      advance(t2, ti2);
-      load_at(t2, ti2, cur);
-    }
-    t0 = t1; ti0 = ti1;
-    t1 = t2; ti1 = ti2;
-    return true;
-  };
-  for (int j = 0; j < J; j += 2) {
-    if (!step(j, A, B)) break;
-    if (j + 1 < J && !step(j + 1, B, A)) break;
-  }
-  tc::cp_async_wait<0>();
-}
-
-// WIDE: PSAC ranks above 8 (32-column second-MMA operands).  IDX16: uint16 centroid indices.
-template <bool WIDE, bool IDX16>
-__global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_constant__ AttnParams p) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  unsigned char *sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
-  __shared__ Bars bars;
-  __shared__ uint32_t tmem_base_sh;
-  __shared__ int abort_flag;
-  __shared__ __align__(64) uint32_t code_lut[WIDE ? 16 : 512];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.y;
-  const int64_t q0 = (int64_t)blockIdx.x * (BM * NQT);
-  volatile int *abort_v = &abort_flag;
-
-  // ---- Query tiles -> shared memory as fp16 (zero rows past nq) ----
-  for (int e = tid; e < NQT * BM * (D / 8); e += kThreads) {
-    const int row = e / (D / 8), ci = e % (D / 8);  // row in [0, 256), 16-byte chunk in [0, 16)
-    const int x = row / BM, rr = row % BM, b = ci / 8;
-    const int64_t qi = q0 + row;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (qi < p.nq) v = *(const uint4 *)(p.q + ((int64_t)h * p.nq + qi) * D + 8 * ci);
-    const uint32_t bw[4] = {v.x, v.y, v.z, v.w};
-    uint32_t hw[4];
-#pragma unroll
-    for (int u = 0; u < 4; u++) hw[u] = f16pair(__uint_as_float(bw[u] << 16), __uint_as_float(bw[u] & 0xFFFF0000u));
-    *(uint4 *)(sm + OFF_Q + (x * 2 + b) * kBlk + tc::sw128_offset(rr, 8 * (ci % 8))) =
-        make_uint4(hw[0], hw[1], hw[2], hw[3]);
-  }
-  // code tables; fp16 bits of the code values 0, 1, 2, 3 are 0x0000, 0x3C00, 0x4000, 0x4200
-  if (!WIDE && tid < 256) {  // byte (4 codes) -> two fp16 pairs
-    uint32_t f[4];
-#pragma unroll
-    for (int t = 0; t < 4; t++) f[t] = ((0x42403C00u >> (8 * ((tid >> (2 * t)) & 3))) & 0xFFu) << 8;
-    code_lut[2 * tid] = f[0] | (f[1] << 16);
-    code_lut[2 * tid + 1] = f[2] | (f[3] << 16);
-  }
-  if (WIDE && tid < 16) {  // code pair -> one fp16 pair
-    const uint32_t lo = ((0x42403C00u >> (8 * (tid & 3))) & 0xFFu) << 8;
-    const uint32_t hi = ((0x42403C00u >> (8 * (tid >> 2))) & 0xFFu) << 8;
-    code_lut[tid] = lo | (hi << 16);
-  }
-  if (tid == 0) {
-    for (int i = 0; i < 2; i++) {
-      tc::mbar_init(&bars.k_full[i], kProdWarps);
-      tc::mbar_init(&bars.v_full[i], kProdWarps);
-      tc::mbar_init(&bars.k_empty[i], 1);
-      tc::mbar_init(&bars.v_empty[i], 1);
-      tc::mbar_init(&bars.s_full[i], 1);
-      tc::mbar_init(&bars.p_ready[i], 4);
-    }
-    tc::mbar_init(&bars.qx_free, 1);
-    tc::mbar_init(&bars.o_done, 1);
-    tc::mbar_init(&bars.drain, 1);
-    abort_flag = 0;
-    tc::fence_mbar_init();
-  }
-  if (warp == kMmaWarp) {
-    tc::tmem_alloc(&tmem_base_sh, 512);
-    tc::tmem_relinquish();
-  }
-  tc::fence_proxy_async_smem();
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = tmem_base_sh;
-  const int J = p.total_tiles;
-
-  if (warp < kSoftmaxWarps) {
-    // ======================= softmax (Query tile x, row = TMEM lane) =======================
-    const int x = warp / 4, sub = warp % 4, row = 32 * sub + lane;
-    const uint32_t lane_addr = (uint32_t)(32 * sub) << 16;
-    const uint32_t tS = tmem + lane_addr + 128u * x, tO = tmem + lane_addr + 256u + 128u * x;
-    const float sl2 = p.scale_log2;
-    float m_used = -INFINITY;
-    uint64_t acc0 = 0ull, acc1 = 0ull;  // running row sum: two packed fp32 pairs
-    const uint64_t sc2 = pk64(__float_as_uint(sl2), __float_as_uint(sl2));
-    bool ok = true;
-    for (int j = 0; j < J; j++) {
-      if (!tc::mbar_wait(&bars.s_full[x], j & 1, kWaitNs)) fail(&abort_flag, p.status);
-      if (*abort_v) { ok = false; break; }
-      tc::fence_after_sync();
-      uint32_t r[32];
-      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-#pragma unroll 1
-      for (int cq = 0; cq < 4; cq++) {  // 32 columns per TMEM round trip (~30 cycles)
-        tc::tmem_ld16(tS + 32u * cq, r);
-        tc::tmem_ld16(tS + 32u * cq + 16u, r + 16);
-        tc::tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; i += 8) {
-          mx0 = tc::max3(mx0, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
-          mx1 = tc::max3(mx1, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
-          mx2 = tc::max3(mx2, __uint_as_float(r[i + 4]), __uint_as_float(r[i + 5]));
-          mx3 = tc::max3(mx3, __uint_as_float(r[i + 6]), __uint_as_float(r[i + 7]));
-        }
-      }
-      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-      const float m_new = fmaxf(m_used, mx * sl2);
-      if (__any_sync(0xffffffffu, m_new > m_used + kRescaleThreshold)) {
-        if (j > 0) {
-          const float alpha = tc::ex2_approx(m_used - m_new);
-          const uint64_t a2 = pk64(__float_as_uint(alpha), __float_as_uint(alpha));
-          acc0 = tc::fma2(acc0, a2, 0ull);
-          acc1 = tc::fma2(acc1, a2, 0ull);
-#pragma unroll 1
-          for (int c = 0; c < D; c += 32) {
-            uint32_t o[32];
-            tc::tmem_ld32(tO + c, o);
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; i++) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tc::tmem_st32(tO + c, o);
-          }
-        }
-        m_used = m_new;
-      }
-      const uint64_t nm2 = pk64(__float_as_uint(-m_used), __float_as_uint(-m_used));
-#pragma unroll 1
-      for (int cq = 0; cq < 4; cq++) {
-        tc::tmem_ld16(tS + 32u * cq, r);
-        tc::tmem_ld16(tS + 32u * cq + 16u, r + 16);
-        tc::tmem_ld_wait();
-        uint32_t pw[16];
-#pragma unroll
-        for (int i = 0; i < 16; i++) {  // packed fp32 pairs: x = S * scale - m, then 2^x
-          const uint64_t x2 = tc::fma2(pk64(r[2 * i], r[2 * i + 1]), sc2, nm2);
-          const float e0 = tc::ex2_approx(tc::f2lo(x2)), e1 = tc::ex2_approx(tc::f2hi(x2));
-          const uint64_t e2 = pk64(__float_as_uint(e0), __float_as_uint(e1));
-          if (i & 1) acc1 = tc::add2(acc1, e2);
-          else acc0 = tc::add2(acc0, e2);
-          pw[i] = f16pair(e0, e1);
-        }
-        tc::tmem_st16(tS + 16u * cq, pw);  // P (fp16 pairs) overlays the logits already read
-      }
-      tc::tmem_st_wait();
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&bars.p_ready[x]);
-    }
-    // ---- epilogue: O / l -> fp32 ----
-    if (ok && !tc::mbar_wait(&bars.o_done, 0, kWaitNs)) fail(&abort_flag, p.status);
-    if (ok && !*abort_v) {
-      tc::fence_after_sync();
-      const uint64_t lsum = tc::add2(acc0, acc1);
-      const float l = tc::f2lo(lsum) + tc::f2hi(lsum);
-      const int64_t qi = q0 + (int64_t)x * BM + row;
-      const float inv = 1.f / l;
-      uint32_t o[32];
-#pragma unroll 1
-      for (int c = 0; c < D; c += 32) {
-        tc::tmem_ld32(tO + c, o);
-        tc::tmem_ld_wait();
-        if (qi < p.nq) {
-          float4 *dst = (float4 *)(p.out + ((int64_t)h * p.nq + qi) * D + c);
-#pragma unroll
-          for (int v = 0; v < 8; v++)
-            dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
-                                 __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
-        }
-      }
-    }
-  } else if (warp == kMmaWarp) {
-    // ======================= MMA issue (one thread) =======================
-    if (lane == 0) {
-      const uint32_t idesc = tc::idesc_f16_f32(BM, BN);
-      const uint32_t idesc_pv = tc::idesc_f16_f32_bmn(BM, D);  // V_hat tiles are [key][d]: N-major
-      const uint32_t tS[2] = {tmem, tmem + 128u}, tO[2] = {tmem + 256u, tmem + 384u};
-      const uint32_t sQ = tc::smem_u32(sm + OFF_Q), sK = tc::smem_u32(sm + OFF_K), sV = tc::smem_u32(sm + OFF_V);
-      const uint32_t sX = tc::smem_u32(sm + OFF_X), sQX = tc::smem_u32(sm + XL<WIDE>::kOffQX);
-      constexpr int kXBytes = XL<WIDE>::kBytes;
-      int t = 0, tile_in_chunk = 0, prev_stage = 0;
-      bool ok = true;
-      auto qk = [&](int x, int s, int nx) {
-#pragma unroll
-        for (int kk = 0; kk < D / 16; kk++) {
-          const uint32_t off = (uint32_t)((kk / 4) * kBlk + 32 * (kk % 4));
-          tc::mma_ss(tS[x], tc::desc_sw128(sQ + (x * 2) * kBlk + off), tc::desc_sw128(sK + (s * 2) * kBlk + off),
-                     idesc, kk > 0);
-        }
-        for (int ks = 0; ks < nx; ks++)
-          tc::mma_ss(tS[x], tc::desc_noswz(sQX + x * kXBytes + 256u * ks, 128, XL<WIDE>::kSbo),
-                     tc::desc_noswz(sX + s * kXBytes + 256u * ks, 128, XL<WIDE>::kSbo), idesc, 1);
-      };
-      auto pv = [&](int x, int s, bool first) {
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; kk++)
-          tc::mma_ts(tO[x], tS[x] + 8u * kk, tc::desc_sw128_mn(sV + (s * 2) * kBlk + 2048u * kk, kBlk, 1024), idesc_pv,
-                     (!first || kk > 0));
-      };
-      for (int j = 0; j < J; j++) {
-        const int s = j & 1;
-        const AttnChunk &ch = p.ch[t];
-        const int nx = (WIDE && ch.rank > 8) ? 2 : 1;
-        ok = tc::mbar_wait(&bars.k_full[s], (j >> 1) & 1, kWaitNs) && !*abort_v;
-        if (!ok) break;
-        tc::fence_after_sync();
-        qk(0, s, nx);
-        tc::mma_commit(&bars.s_full[0]);
-        if (j > 0) {
-          ok = tc::mbar_wait(&bars.p_ready[1], (j - 1) & 1, kWaitNs) && !*abort_v;
-          if (!ok) break;
-          tc::fence_after_sync();
-          pv(1, prev_stage, j - 1 == 0);
-          tc::mma_commit(&bars.v_empty[prev_stage]);
-        }
-        qk(1, s, nx);
-        tc::mma_commit(&bars.s_full[1]);
-        tc::mma_commit(&bars.k_empty[s]);
-        const bool last_of_chunk = tile_in_chunk + 1 == ch.tiles;
-        if (last_of_chunk) tc::mma_commit(&bars.qx_free);
-        ok = tc::mbar_wait(&bars.v_full[s], (j >> 1) & 1, kWaitNs) && tc::mbar_wait(&bars.p_ready[0], j & 1, kWaitNs) &&
-             !*abort_v;
-        if (!ok) break;
-        tc::fence_after_sync();
-        pv(0, s, j == 0);
-        prev_stage = s;
-        if (last_of_chunk) { tile_in_chunk = 0; t++; }
-        else tile_in_chunk++;
-      }
-      if (ok && J > 0) {
-        ok = tc::mbar_wait(&bars.p_ready[1], (J - 1) & 1, kWaitNs) && !*abort_v;
-        if (ok) {
-          tc::fence_after_sync();
-          pv(1, prev_stage, J - 1 == 0);
-          tc::mma_commit(&bars.o_done);
-        }
-      }
-      if (!ok) fail(&abort_flag, p.status);
-      // drain: every MMA issued above completes before TMEM is released
-      tc::mma_commit(&bars.drain);
-      if (!tc::mbar_wait(&bars.drain, 0, kWaitNs)) qwm_dev_error(p.status, QWM_ERR_DEVICE_TIMEOUT);
-    }
-  } else if (warp < kVWarp0) {
-    producer<false, WIDE, IDX16>(p, sm, bars, &abort_flag, tc::smem_u32(code_lut), h, q0, tid - 32 * kKWarp0, lane);
-  } else {
-    producer<true, WIDE, IDX16>(p, sm, bars, &abort_flag, tc::smem_u32(code_lut), h, q0, tid - 32 * kVWarp0, lane);
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-  if (warp == kMmaWarp) {
-    tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, 512);
-  }
-}
-
-template <bool WIDE, bool IDX16>
-cudaError_t launch_variant(const AttnParams &p, dim3 grid, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel<WIDE, IDX16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       XL<WIDE>::kSmemAlloc);
-  if (e != cudaSuccess) return e;
-  attend_tc_kernel<WIDE, IDX16><<<grid, kThreads, XL<WIDE>::kSmemAlloc, st>>>(p);
-  return cudaGetLastError();
-}
-
-
-// ==================================================================================== CTA pairs
-// The same attention on a pair of CTAs (a cluster of two) working as one with cta_group::2 MMAs:
-// the pair takes 512 Queries, CTA c holding Query rows 256 x + 128 c .. 256 x + 128 c + 127 of its
-// two tiles x.  One M = 256 MMA covers both CTAs' rows of a tile; its B operand is split by N, so
-// CTA c decodes only Key rows 64 c .. 64 c + 63 of each 128-key tile (all channels) for Q K_hat^T,
-// and only channels 64 c .. 64 c + 63 (INT2 group c) of all 128 Value rows for P V_hat: each CTA
-// decodes half of every tile for the same 256 Queries.  The even CTA's MMA thread issues every
-// MMA; the odd CTA's producers and softmax warps arrive on the even CTA's barriers through
-// shared::cluster addresses, and the MMA commits reach both CTAs' barriers by multicast.
-constexpr int kPairQ = 2 * NQT * BM;          // Queries per pair
-constexpr int kBlkH = 64 * 128;               // a [64 rows][64 fp16] swizzled block: 8 KB
-constexpr int P_OFF_Q = 0;                    // 2 Query tiles x 2 blocks
-constexpr int P_OFF_K = P_OFF_Q + NQT * 2 * kBlk;  // 2 stages x 2 blocks [64 keys][64 ch]
-constexpr int P_OFF_V = P_OFF_K + 2 * 2 * kBlkH;   // 2 stages x [128 keys][64 ch] (MN-major B)
-constexpr int P_OFF_X = P_OFF_V + 2 * kBlk;        // 2 stages of X [64][cols], then 2 QX [128][cols]
-
-template <bool WIDE>
-struct PXL {
-  static constexpr int kXBytes = 64 * XL<WIDE>::kCols * 2;
-  static constexpr int kQXBytes = 128 * XL<WIDE>::kCols * 2;
-  static constexpr int kOffQX = P_OFF_X + 2 * kXBytes;
-  static constexpr int kSmemBytes = kOffQX + NQT * kQXBytes;
-  static constexpr int kSmemAlloc = kSmemBytes + 1024;
-};
 
 // Index data of one half row: one INT2 group's fp16 step and offset (each duplicated into a pair),
 // its 64 codes, and (Keys, group 0 only) the PSAC coefficients and their scale.
@@ -767,11 +321,11 @@ __device__ __forceinline__ void producer_pair(const AttnParams &p, unsigned char
   const int krow = VAL ? pr : 64 * cr + (pr & 63);  // key row in the tile
   const bool coef = !VAL && g == 0;              // writes the row of the second MMA's B operand
   uint64_t *empty = VAL ? bars.v_empty : bars.k_empty;
-  const uint32_t full0 = tc::mapa(tc::smem_u32(VAL ? &bars.v_full[0] : &bars.k_full[0]), 0);
-  const uint32_t full1 = tc::mapa(tc::smem_u32(VAL ? &bars.v_full[1] : &bars.k_full[1]), 0);
+  // the even CTA's full barriers (consecutive 8-byte words), as shared::cluster addresses
+  const uint32_t full_base = tc::mapa(tc::smem_u32(VAL ? &bars.v_full[0] : &bars.k_full[0]), 0);
   constexpr uint32_t kStage = VAL ? (uint32_t)kBlk : 2u * kBlkH;
-  const uint32_t block0 = tc::smem_u32(sm + (VAL ? P_OFF_V : P_OFF_K)) + (VAL ? 0u : (uint32_t)g * kBlkH);
-  const uint32_t xs0 = tc::smem_u32(sm + P_OFF_X), qx0 = tc::smem_u32(sm + PXL<WIDE>::kOffQX);
+  const uint32_t block0 = tc::smem_u32(sm + (VAL ? OFF_V : OFF_K)) + (VAL ? 0u : (uint32_t)g * kBlkH);
+  const uint32_t xs0 = tc::smem_u32(sm + OFF_X), qx0 = tc::smem_u32(sm + XL<WIDE>::kOffQX);
   int t0 = 0, ti0 = 0, t1 = 0, ti1 = 0, t2 = 0, ti2 = 0;
   auto advance = [&](int &tt, int &ti) {
     if (++ti == p.ch[tt].tiles) { ti = 0; tt++; }
@@ -792,29 +346,31 @@ __device__ __forceinline__ void producer_pair(const AttnParams &p, unsigned char
   issue_half_copies(VAL ? p.ch[0].cent_v16 : p.ch[0].cent_k16, h, C, A.idx, block0, rbase, 64 * g, lane);
   tc::cp_async_commit();
   auto step = [&](int j, HalfRow &cur, const HalfRow &nxt) -> bool {
-    const int s = j & 1;
+    const int s = j % kStages;
     const AttnChunk &ch = p.ch[t0];
     tc::cp_async_wait<0>();
     __syncwarp();  // the warp's copies of tile j, made visible to every lane
     decode_half<!WIDE>(cur, block0 + (uint32_t)s * kStage, rr, lut);
     if (!VAL) {
-      if (coef) write_x_row<WIDE>(cur, ch.rank, xs0 + (uint32_t)s * PXL<WIDE>::kXBytes, rr);
+      if (coef) write_x_row<WIDE>(cur, ch.rank, xs0 + (uint32_t)s * XL<WIDE>::kXBytes, rr);
       if (ti0 == 0) {  // chunk start: the second MMA's A operand for both Query tiles
         if (t0 > 0 && !tc::mbar_wait(&bars.qx_free, (t0 - 1) & 1, kWaitNs)) fail(abort_flag, p.status);
         if (__any_sync(0xffffffffu, *abort_v != 0)) return false;  // warp-uniform exit
-        const uint32_t sq = tc::smem_u32(sm + P_OFF_Q);
+        const uint32_t sq = tc::smem_u32(sm + OFF_Q);
         write_qx_row<WIDE>(ch, h, qrow0 + pr < p.nq, sq, qx0, pr);
-        write_qx_row<WIDE>(ch, h, qrow0 + 2 * BM + pr < p.nq, sq + 2u * kBlk, qx0 + PXL<WIDE>::kQXBytes, pr);
+        write_qx_row<WIDE>(ch, h, qrow0 + 2 * BM + pr < p.nq, sq + 2u * kBlk, qx0 + XL<WIDE>::kQXBytes, pr);
       }
     }
     tc::fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) tc::mbar_arrive_remote(s ? full1 : full0);
-    if (j + 1 < J) {  // copies of tile j+1 into the other stage once tile j-1 has released it
-      if (j >= 1 && !tc::mbar_wait(&empty[s ^ 1], ((j - 1) >> 1) & 1, kWaitNs)) fail(abort_flag, p.status);
+    if (lane == 0) tc::mbar_arrive_remote(full_base + 8u * (uint32_t)s);
+    if (j + 1 < J) {  // copies of tile j+1 into its stage once tile j+1-kStages has released it
+      const int sn = (j + 1) % kStages;
+      if (j + 1 >= kStages && !tc::mbar_wait(&empty[sn], ((j + 1) / kStages - 1) & 1, kWaitNs))
+        fail(abort_flag, p.status);
       if (__any_sync(0xffffffffu, *abort_v != 0)) return false;  // warp-uniform exit
       issue_half_copies(VAL ? p.ch[t1].cent_v16 : p.ch[t1].cent_k16, h, C, nxt.idx,
-                        block0 + (uint32_t)(s ^ 1) * kStage, rbase, 64 * g, lane);
+                        block0 + (uint32_t)sn * kStage, rbase, 64 * g, lane);
       tc::cp_async_commit();
     }
     t2 = t1; ti2 = ti1;
@@ -859,7 +415,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t hw[4];
 #pragma unroll
     for (int u = 0; u < 4; u++) hw[u] = f16pair(__uint_as_float(bw[u] << 16), __uint_as_float(bw[u] & 0xFFFF0000u));
-    *(uint4 *)(sm + P_OFF_Q + (x * 2 + b) * kBlk + tc::sw128_offset(rr, 8 * (ci % 8))) =
+    *(uint4 *)(sm + OFF_Q + (x * 2 + b) * kBlk + tc::sw128_offset(rr, 8 * (ci % 8))) =
         make_uint4(hw[0], hw[1], hw[2], hw[3]);
   }
   if (!WIDE && tid < 256) {
@@ -875,11 +431,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     code_lut[tid] = lo | (hi << 16);
   }
   if (tid == 0) {
-    for (int i = 0; i < 2; i++) {
+    for (int i = 0; i < kStages; i++) {
       tc::mbar_init(&bars.k_full[i], 2 * kProdWarps);  // both CTAs' producer warps (even CTA's copy used)
       tc::mbar_init(&bars.v_full[i], 2 * kProdWarps);
       tc::mbar_init(&bars.k_empty[i], 1);
       tc::mbar_init(&bars.v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; i++) {
       tc::mbar_init(&bars.s_full[i], 1);
       tc::mbar_init(&bars.p_ready[i], 8);              // both CTAs' 4 softmax warps of tile i
     }
@@ -1001,8 +559,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t idesc = tc::idesc_f16_f32(2 * BM, BN);
       const uint32_t idesc_pv = tc::idesc_f16_f32_bmn(2 * BM, D);
       const uint32_t tS[2] = {tmem, tmem + 128u}, tO[2] = {tmem + 256u, tmem + 384u};
-      const uint32_t sQ = tc::smem_u32(sm + P_OFF_Q), sK = tc::smem_u32(sm + P_OFF_K), sV = tc::smem_u32(sm + P_OFF_V);
-      const uint32_t sX = tc::smem_u32(sm + P_OFF_X), sQX = tc::smem_u32(sm + PXL<WIDE>::kOffQX);
+      const uint32_t sQ = tc::smem_u32(sm + OFF_Q), sK = tc::smem_u32(sm + OFF_K), sV = tc::smem_u32(sm + OFF_V);
+      const uint32_t sX = tc::smem_u32(sm + OFF_X), sQX = tc::smem_u32(sm + XL<WIDE>::kOffQX);
       constexpr uint16_t kBoth = 3;
       int t = 0, tile_in_chunk = 0, prev_stage = 0;
       bool ok = true;
@@ -1015,8 +573,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                       kk > 0);
         }
         for (int ks = 0; ks < nx; ks++)
-          tc::mma2_ss(tS[x], tc::desc_noswz(sQX + x * PXL<WIDE>::kQXBytes + 256u * ks, 128, XL<WIDE>::kSbo),
-                      tc::desc_noswz(sX + s * PXL<WIDE>::kXBytes + 256u * ks, 128, XL<WIDE>::kSbo), idesc, 1);
+          tc::mma2_ss(tS[x], tc::desc_noswz(sQX + x * XL<WIDE>::kQXBytes + 256u * ks, 128, XL<WIDE>::kSbo),
+                      tc::desc_noswz(sX + s * XL<WIDE>::kXBytes + 256u * ks, 128, XL<WIDE>::kSbo), idesc, 1);
       };
       auto pv = [&](int x, int s, bool first) {
 #pragma unroll
@@ -1025,10 +583,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                       (!first || kk > 0));
       };
       for (int j = 0; j < J; j++) {
-        const int s = j & 1;
+        const int s = j % kStages;
+        const uint32_t ph = (uint32_t)(j / kStages) & 1u;
         const AttnChunk &ch = p.ch[t];
         const int nx = (WIDE && ch.rank > 8) ? 2 : 1;
-        ok = tc::mbar_wait_cluster(&bars.k_full[s], (j >> 1) & 1, kWaitNs) && !*abort_v;
+        ok = tc::mbar_wait_cluster(&bars.k_full[s], ph, kWaitNs) && !*abort_v;
         if (!ok) break;
         tc::fence_after_sync();
         qk(0, s, nx);
@@ -1045,7 +604,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc::mma2_commit(&bars.k_empty[s], kBoth);
         const bool last_of_chunk = tile_in_chunk + 1 == ch.tiles;
         if (last_of_chunk) tc::mma2_commit(&bars.qx_free, kBoth);
-        ok = tc::mbar_wait_cluster(&bars.v_full[s], (j >> 1) & 1, kWaitNs) &&
+        ok = tc::mbar_wait_cluster(&bars.v_full[s], ph, kWaitNs) &&
              tc::mbar_wait_cluster(&bars.p_ready[0], j & 1, kWaitNs) && !*abort_v;
         if (!ok) break;
         tc::fence_after_sync();
@@ -1085,9 +644,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 template <bool WIDE, bool IDX16>
 cudaError_t launch_pair(const AttnParams &p, dim3 grid, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(attend_pair_kernel<WIDE, IDX16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       PXL<WIDE>::kSmemAlloc);
+                                       XL<WIDE>::kSmemAlloc);
   if (e != cudaSuccess) return e;
-  attend_pair_kernel<WIDE, IDX16><<<grid, kThreads, PXL<WIDE>::kSmemAlloc, st>>>(p);
+  attend_pair_kernel<WIDE, IDX16><<<grid, kThreads, XL<WIDE>::kSmemAlloc, st>>>(p);
   return cudaGetLastError();
 }
 
