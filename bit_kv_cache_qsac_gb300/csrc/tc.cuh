@@ -340,10 +340,14 @@ __device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
-// Arrive on an mbarrier anywhere in the cluster (shared::cluster address), releasing this
-// thread's prior writes at cluster scope.
+// Arrive on an mbarrier anywhere in the cluster (shared::cluster address), with the default
+// (release, CTA scope) semantics.  The data such an arrival hands over is read by the pair's
+// tensor cores: shared-memory tiles made visible to the async proxy by fence.proxy.async first,
+// or tensor-memory stores already completed by tcgen05.wait::st and ordered by
+// tcgen05.fence::before_thread_sync.  A cluster-scope release here costs ~1000 cycles per arrival
+// and buys nothing for those readers.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
