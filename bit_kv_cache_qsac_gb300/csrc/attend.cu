@@ -85,8 +85,10 @@ struct XL {
   static constexpr uint32_t kSbo = 16u * kCols;
   static constexpr int kXBytes = 64 * kCols * 2;    // one X stage: this CTA's 64 key rows
   static constexpr int kQXBytes = 128 * kCols * 2;  // one QX tile: this CTA's 128 Query rows
-  static constexpr int kOffQX = OFF_X + kStages * kXBytes;
-  static constexpr int kSmemBytes = kOffQX + NQT * kQXBytes;
+  static constexpr int kOffQX = OFF_X + kStages * kXBytes;  // 2 buffers (alternate chunks) x NQT tiles
+  static constexpr int kUBytes = 128 * (WIDE ? 16 : 8) * 4;  // U_r of one chunk as fp32 [128][kRU]
+  static constexpr int kOffU = kOffQX + 2 * NQT * kQXBytes;  // 2 buffers (alternate chunks)
+  static constexpr int kSmemBytes = kOffU + 2 * kUBytes;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;
   __host__ __device__ static constexpr uint32_t off(uint32_t row, uint32_t k) {
     return (row >> 3) * kSbo + (k >> 3) * 128u + (row & 7u) * 16u + (k & 7u) * 2u;
@@ -114,7 +116,7 @@ struct AttnParams {
 
 struct Bars {
   uint64_t k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
-  uint64_t s_full[2], p_ready[2], qx_free, o_done, drain;
+  uint64_t s_full[2], p_ready[2], qx_full[2], qx_free[2], u_ready[2], o_done, drain;
 };
 
 __device__ __forceinline__ void fail(int *abort_flag, int32_t *status) {
@@ -159,36 +161,32 @@ __device__ __forceinline__ void write_x_row(const Row &d, int R, uint32_t xs, in
                make_uint4(w[4 * kc], w[4 * kc + 1], w[4 * kc + 2], w[4 * kc + 3]));
 }
 
-// Query row rr of Query tile x: its row of the second MMA's A operand, [q U_r | 0 0 0 0 | 1 | 0 ...],
+// Query row rr of a Query tile: its row of the second MMA's A operand, [q U_r | 0 0 0 0 | 1 | 0 ...],
 // with q read from the tile's fp16 copy in shared memory (exact: bf16 Queries convert to fp16
-// exactly) and U_r (bf16, the chunk's basis) from global memory (a few KB, L1-resident).
+// exactly) and U_r from its fp32 copy in shared memory ([128 channels][kRU], zero past the rank;
+// every lane reads the same words, so the reads broadcast).
 template <bool WIDE>
-__device__ __forceinline__ void write_qx_row(const AttnChunk &ch, int h, bool live, uint32_t qtile, uint32_t dst,
-                                             int rr) {
-  const int R = ch.rank;
-  float acc[16];
+__device__ __forceinline__ void write_qx_row(int R, bool live, uint32_t qtile, uint32_t ubuf, uint32_t dst, int rr) {
+  constexpr int kRU = WIDE ? 16 : 8;
+  float acc[kRU];
 #pragma unroll
-  for (int k = 0; k < 16; k++) acc[k] = 0.f;
+  for (int k = 0; k < kRU; k++) acc[k] = 0.f;
   if (live && R > 0) {
-    const uint16_t *U = ch.u_r + (int64_t)h * D * R;
-#pragma unroll 1
+#pragma unroll 2
     for (int ci = 0; ci < D / 8; ci++) {
       const uint4 qv = tc::lds128(qtile + (uint32_t)(ci / 8) * kBlk + tc::sw128_offset(rr, 8 * (ci % 8)));
       const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
       for (int u = 0; u < 8; u++) {
         const float qc = __half2float(__ushort_as_half((uint16_t)(qw[u >> 1] >> (16 * (u & 1)))));
-        const int c = 8 * ci + u;
-        if (R == 8) {
-          const uint4 uv = *(const uint4 *)(U + c * 8);
-          const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
+        const uint32_t ua = ubuf + (uint32_t)(8 * ci + u) * (kRU * 4);
 #pragma unroll
-          for (int k = 0; k < 8; k++)
-            acc[k] = fmaf(qc, __uint_as_float((k & 1) ? (uw[k >> 1] & 0xFFFF0000u) : (uw[k >> 1] << 16)), acc[k]);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 16; k++)
-            if (k < R) acc[k] = fmaf(qc, bf16_to_f32(U[c * R + k]), acc[k]);
+        for (int k4 = 0; k4 < kRU / 4; k4++) {
+          const uint4 uv = tc::lds128(ua + 16u * k4);
+          acc[4 * k4] = fmaf(qc, __uint_as_float(uv.x), acc[4 * k4]);
+          acc[4 * k4 + 1] = fmaf(qc, __uint_as_float(uv.y), acc[4 * k4 + 1]);
+          acc[4 * k4 + 2] = fmaf(qc, __uint_as_float(uv.z), acc[4 * k4 + 2]);
+          acc[4 * k4 + 3] = fmaf(qc, __uint_as_float(uv.w), acc[4 * k4 + 3]);
         }
       }
     }
@@ -203,7 +201,7 @@ __device__ __forceinline__ void write_qx_row(const AttnChunk &ch, int h, bool li
     w[6] = one;
   } else {
 #pragma unroll
-    for (int i = 0; i < 8; i++) w[i] = f16pair(acc[2 * i], acc[2 * i + 1]);
+    for (int i = 0; i < kRU / 2; i++) w[i] = f16pair(acc[2 * i], acc[(2 * i + 1) % kRU]);
     w[10] = one;
   }
 #pragma unroll
@@ -326,6 +324,38 @@ __device__ __forceinline__ void producer_pair(const AttnParams &p, unsigned char
   constexpr uint32_t kStage = VAL ? (uint32_t)kBlk : 2u * kBlkH;
   const uint32_t block0 = tc::smem_u32(sm + (VAL ? OFF_V : OFF_K)) + (VAL ? 0u : (uint32_t)g * kBlkH);
   const uint32_t xs0 = tc::smem_u32(sm + OFF_X), qx0 = tc::smem_u32(sm + XL<WIDE>::kOffQX);
+  // Value producers: the second MMA's A operand [q U_r | 0 | 1] of chunk t for both Query tiles, into
+  // buffer t % 2 once chunk t - 2 has released it (row pr of each tile per thread)
+  auto build_qx = [&](int t) -> bool {
+    const int b = t & 1, R = p.ch[t].rank;
+    constexpr int kRU = WIDE ? 16 : 8;
+    if (t >= 2 && !tc::mbar_wait(&bars.qx_free[b], ((t >> 1) - 1) & 1, kWaitNs)) fail(abort_flag, p.status);
+    if (__any_sync(0xffffffffu, *abort_v != 0)) return false;  // warp-uniform exit
+    // U_r of chunk t -> fp32 buffer b (thread pr = channel pr); the four Value warps meet on u_ready[b]
+    // (buffer b was last read for chunk t - 2, before every warp's arrival for chunk t - 1)
+    const uint32_t ub = tc::smem_u32(sm + XL<WIDE>::kOffU) + (uint32_t)b * XL<WIDE>::kUBytes;
+    {
+      float u[kRU];
+#pragma unroll
+      for (int k = 0; k < kRU; k++) u[k] = (k < R) ? bf16_to_f32(p.ch[t].u_r[((int64_t)h * D + pr) * R + k]) : 0.f;
+#pragma unroll
+      for (int k4 = 0; k4 < kRU / 4; k4++)
+        tc::sts128(ub + (uint32_t)pr * (kRU * 4) + 16u * k4,
+                   make_uint4(__float_as_uint(u[4 * k4]), __float_as_uint(u[4 * k4 + 1]),
+                              __float_as_uint(u[4 * k4 + 2]), __float_as_uint(u[4 * k4 + 3])));
+    }
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(&bars.u_ready[b]);
+    if (!tc::mbar_wait(&bars.u_ready[b], (t >> 1) & 1, kWaitNs)) fail(abort_flag, p.status);
+    if (__any_sync(0xffffffffu, *abort_v != 0)) return false;  // warp-uniform exit
+    const uint32_t sq = tc::smem_u32(sm + OFF_Q), dst = qx0 + (uint32_t)(b * NQT) * XL<WIDE>::kQXBytes;
+    write_qx_row<WIDE>(R, qrow0 + pr < p.nq, sq, ub, dst, pr);
+    write_qx_row<WIDE>(R, qrow0 + 2 * BM + pr < p.nq, sq + 2u * kBlk, ub, dst + XL<WIDE>::kQXBytes, pr);
+    tc::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive_remote(tc::mapa(tc::smem_u32(&bars.qx_full[b]), 0));
+    return true;
+  };
   int t0 = 0, ti0 = 0, t1 = 0, ti1 = 0, t2 = 0, ti2 = 0;
   auto advance = [&](int &tt, int &ti) {
     if (++ti == p.ch[tt].tiles) { ti = 0; tt++; }
@@ -345,25 +375,20 @@ __device__ __forceinline__ void producer_pair(const AttnParams &p, unsigned char
   }
   issue_half_copies(VAL ? p.ch[0].cent_v16 : p.ch[0].cent_k16, h, C, A.idx, block0, rbase, 64 * g, lane);
   tc::cp_async_commit();
+  bool live = !VAL || build_qx(0);  // chunk 0's QX while the first copies fly
   auto step = [&](int j, HalfRow &cur, const HalfRow &nxt) -> bool {
     const int s = j % kStages;
     const AttnChunk &ch = p.ch[t0];
     tc::cp_async_wait<0>();
     __syncwarp();  // the warp's copies of tile j, made visible to every lane
     decode_half<!WIDE>(cur, block0 + (uint32_t)s * kStage, rr, lut);
-    if (!VAL) {
-      if (coef) write_x_row<WIDE>(cur, ch.rank, xs0 + (uint32_t)s * XL<WIDE>::kXBytes, rr);
-      if (ti0 == 0) {  // chunk start: the second MMA's A operand for both Query tiles
-        if (t0 > 0 && !tc::mbar_wait(&bars.qx_free, (t0 - 1) & 1, kWaitNs)) fail(abort_flag, p.status);
-        if (__any_sync(0xffffffffu, *abort_v != 0)) return false;  // warp-uniform exit
-        const uint32_t sq = tc::smem_u32(sm + OFF_Q);
-        write_qx_row<WIDE>(ch, h, qrow0 + pr < p.nq, sq, qx0, pr);
-        write_qx_row<WIDE>(ch, h, qrow0 + 2 * BM + pr < p.nq, sq + 2u * kBlk, qx0 + XL<WIDE>::kQXBytes, pr);
-      }
-    }
+    if (!VAL && coef) write_x_row<WIDE>(cur, ch.rank, xs0 + (uint32_t)s * XL<WIDE>::kXBytes, rr);
     tc::fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) tc::mbar_arrive_remote(full_base + 8u * (uint32_t)s);
+    if (VAL && ti0 == 0 && t0 + 1 < p.n_chunks) {  // chunk start: the next chunk's QX, ahead of time
+      if (!build_qx(t0 + 1)) return false;
+    }
     if (j + 1 < J) {  // copies of tile j+1 into its stage once tile j+1-kStages has released it
       const int sn = (j + 1) % kStages;
       if (j + 1 >= kStages && !tc::mbar_wait(&empty[sn], ((j + 1) / kStages - 1) & 1, kWaitNs))
@@ -382,7 +407,7 @@ __device__ __forceinline__ void producer_pair(const AttnParams &p, unsigned char
     t1 = t2; ti1 = ti2;
     return true;
   };
-  for (int j = 0; j < J; j += 2) {
+  for (int j = 0; live && j < J; j += 2) {
     if (!step(j, A, B)) break;
     if (j + 1 < J && !step(j + 1, B, A)) break;
   }
@@ -441,7 +466,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc::mbar_init(&bars.s_full[i], 1);
       tc::mbar_init(&bars.p_ready[i], 8);              // both CTAs' 4 softmax warps of tile i
     }
-    tc::mbar_init(&bars.qx_free, 1);
+    for (int i = 0; i < 2; i++) {
+      tc::mbar_init(&bars.qx_full[i], 2 * kProdWarps);  // both CTAs' Value producer warps
+      tc::mbar_init(&bars.qx_free[i], 1);
+      tc::mbar_init(&bars.u_ready[i], kProdWarps);      // this CTA's Value producer warps
+    }
     tc::mbar_init(&bars.o_done, 1);
     tc::mbar_init(&bars.drain, 1);
     abort_flag = 0;
@@ -564,7 +593,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       constexpr uint16_t kBoth = 3;
       int t = 0, tile_in_chunk = 0, prev_stage = 0;
       bool ok = true;
-      auto qk = [&](int x, int s, int nx) {
+      auto qk = [&](int x, int s, int nx, int qb) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; kk++) {
           const uint32_t qo = (uint32_t)((kk / 4) * kBlk + 32 * (kk % 4));
@@ -573,7 +602,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                       kk > 0);
         }
         for (int ks = 0; ks < nx; ks++)
-          tc::mma2_ss(tS[x], tc::desc_noswz(sQX + x * XL<WIDE>::kQXBytes + 256u * ks, 128, XL<WIDE>::kSbo),
+          tc::mma2_ss(tS[x], tc::desc_noswz(sQX + (qb * NQT + x) * XL<WIDE>::kQXBytes + 256u * ks, 128, XL<WIDE>::kSbo),
                       tc::desc_noswz(sX + s * XL<WIDE>::kXBytes + 256u * ks, 128, XL<WIDE>::kSbo), idesc, 1);
       };
       auto pv = [&](int x, int s, bool first) {
@@ -588,9 +617,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const AttnChunk &ch = p.ch[t];
         const int nx = (WIDE && ch.rank > 8) ? 2 : 1;
         ok = tc::mbar_wait_cluster(&bars.k_full[s], ph, kWaitNs) && !*abort_v;
+        if (ok && tile_in_chunk == 0) ok = tc::mbar_wait_cluster(&bars.qx_full[t & 1], (t >> 1) & 1, kWaitNs);
         if (!ok) break;
         tc::fence_after_sync();
-        qk(0, s, nx);
+        qk(0, s, nx, t & 1);
         tc::mma2_commit(&bars.s_full[0], kBoth);
         if (j > 0) {
           ok = tc::mbar_wait_cluster(&bars.p_ready[1], (j - 1) & 1, kWaitNs) && !*abort_v;
@@ -599,11 +629,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           pv(1, prev_stage, j - 1 == 0);
           tc::mma2_commit(&bars.v_empty[prev_stage], kBoth);
         }
-        qk(1, s, nx);
+        qk(1, s, nx, t & 1);
         tc::mma2_commit(&bars.s_full[1], kBoth);
         tc::mma2_commit(&bars.k_empty[s], kBoth);
         const bool last_of_chunk = tile_in_chunk + 1 == ch.tiles;
-        if (last_of_chunk) tc::mma2_commit(&bars.qx_free, kBoth);
+        if (last_of_chunk) tc::mma2_commit(&bars.qx_free[t & 1], kBoth);
         ok = tc::mbar_wait_cluster(&bars.v_full[s], ph, kWaitNs) &&
              tc::mbar_wait_cluster(&bars.p_ready[0], j & 1, kWaitNs) && !*abort_v;
         if (!ok) break;
