@@ -503,50 +503,57 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!tc::mbar_wait(&bars.s_full[x], j & 1, kWaitNs)) fail(&abort_flag, p.status);
       if (*abort_v) { ok = false; break; }
       tc::fence_after_sync();
+      // one pass over the tile, 32 columns at a time: the chunk's max, then its exponentials with the
+      // running max m_used; when a chunk raises the max by more than 2^8 (rare after the first
+      // chunk) the sum, O and the P chunks already stored for this tile are first rescaled
       uint32_t r[32];
-      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll 1
       for (int cq = 0; cq < 4; cq++) {
         tc::tmem_ld16(tS + 32u * cq, r);
         tc::tmem_ld16(tS + 32u * cq + 16u, r + 16);
         tc::tmem_ld_wait();
+        float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 32; i += 8) {
+        for (int i = 0; i < 32; i += 4) {
           mx0 = tc::max3(mx0, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
           mx1 = tc::max3(mx1, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
-          mx2 = tc::max3(mx2, __uint_as_float(r[i + 4]), __uint_as_float(r[i + 5]));
-          mx3 = tc::max3(mx3, __uint_as_float(r[i + 6]), __uint_as_float(r[i + 7]));
         }
-      }
-      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-      const float m_new = fmaxf(m_used, mx * sl2);
-      if (__any_sync(0xffffffffu, m_new > m_used + kRescaleThreshold)) {
-        if (j > 0) {
-          const float alpha = tc::ex2_approx(m_used - m_new);
+        const float m_new = fmaxf(m_used, fmaxf(mx0, mx1) * sl2);
+        if (__any_sync(0xffffffffu, m_new > m_used + kRescaleThreshold)) {
+          const float alpha = tc::ex2_approx(m_used - m_new);  // 0 while m_used is -inf
           const uint64_t a2 = pk64(__float_as_uint(alpha), __float_as_uint(alpha));
           acc0 = tc::fma2(acc0, a2, 0ull);
           acc1 = tc::fma2(acc1, a2, 0ull);
+          if (j > 0) {  // O of the earlier tiles (complete: S_x(j) finished after PV_x(j-1))
 #pragma unroll 1
-          for (int c = 0; c < D; c += 32) {
-            uint32_t o[32];
-            tc::tmem_ld32(tO + c, o);
+            for (int c = 0; c < D; c += 32) {
+              uint32_t o[32];
+              tc::tmem_ld32(tO + c, o);
+              tc::tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; i++) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tc::tmem_st32(tO + c, o);
+            }
+          }
+          tc::tmem_st_wait();
+#pragma unroll 1
+          for (int pc = 0; pc < cq; pc++) {  // P chunks of this tile already written
+            uint32_t pw[16];
+            tc::tmem_ld16(tS + 16u * pc, pw);
             tc::tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; i++) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tc::tmem_st32(tO + c, o);
+            for (int i = 0; i < 16; i++) {
+              const float2 v = __half22float2(*(const __half2 *)&pw[i]);
+              pw[i] = f16pair(v.x * alpha, v.y * alpha);
+            }
+            tc::tmem_st16(tS + 16u * pc, pw);
           }
+          m_used = m_new;
         }
-        m_used = m_new;
-      }
-      const uint64_t nm2 = pk64(__float_as_uint(-m_used), __float_as_uint(-m_used));
-#pragma unroll 1
-      for (int cq = 0; cq < 4; cq++) {
-        tc::tmem_ld16(tS + 32u * cq, r);
-        tc::tmem_ld16(tS + 32u * cq + 16u, r + 16);
-        tc::tmem_ld_wait();
+        const uint64_t nm2 = pk64(__float_as_uint(-m_used), __float_as_uint(-m_used));
         uint32_t pw[16];
 #pragma unroll
-        for (int i = 0; i < 16; i++) {
+        for (int i = 0; i < 16; i++) {  // packed fp32 pairs: x = S * scale - m, then 2^x
           const uint64_t x2 = tc::fma2(pk64(r[2 * i], r[2 * i + 1]), sc2, nm2);
           const float e0 = tc::ex2_approx(tc::f2lo(x2)), e1 = tc::ex2_approx(tc::f2hi(x2));
           const uint64_t e2 = pk64(__float_as_uint(e0), __float_as_uint(e1));
@@ -554,7 +561,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           else acc0 = tc::add2(acc0, e2);
           pw[i] = f16pair(e0, e1);
         }
-        tc::tmem_st16(tS + 16u * cq, pw);
+        tc::tmem_st16(tS + 16u * cq, pw);  // P (fp16 pairs) overlays logits already read
       }
       tc::tmem_st_wait();
       tc::fence_before_sync();

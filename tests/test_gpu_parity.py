@@ -312,6 +312,37 @@ def test_attend_psac_ranks(q, rank, C, n):
         assert _attn_err(out[h].cpu().numpy().astype(np.float64), ref) <= 2e-2
 
 
+def test_attend_growing_logits(q):
+    """A hand-built chunk whose logits rise steadily along the keys (about 10 log2 units per tile),
+    so the softmax raises its running maximum many times, inside tiles and across them (rescaling
+    its sum, O and the P chunks already written).  Every decoded key is an integer vector and every
+    Query a multiple of 1/8, so the logits are exact in the kernel's fp16 operands and the only
+    differences from the oracle are the rounding of P and of the exponentials."""
+    H, n, C, nq = 2, 1024, 256, 256
+    ctx = q.Context(heads=H, n_centroids=C, rank=0)
+    ch = q.Chunk.empty(ctx, n)
+    rng = np.random.default_rng(7)
+    u = np.where(rng.random(D) < 0.5, -1.0, 1.0)
+    ck = np.stack([np.round(20.0 * np.arange(C) / C)[:, None] * u[None, :]] * H)    # centroid j ~ (20 j / C) u
+    cv = rng.integers(-3, 4, size=(H, C, D)).astype(np.float64)
+    idx = np.broadcast_to(np.arange(n) // (n // C), (H, n)).astype(np.uint8)
+    for name in ("k_codes", "v_codes"):
+        getattr(ch, name).zero_()
+    for name in ("k_scale", "k_min", "v_scale", "v_min"):
+        getattr(ch, name).zero_()
+    ch.k_idx.copy_(torch.from_numpy(idx.copy())); ch.v_idx.copy_(torch.from_numpy(idx.copy()))
+    ch.cent_k.copy_(torch.from_numpy(ck).to(torch.bfloat16)); ch.cent_v.copy_(torch.from_numpy(cv).to(torch.bfloat16))
+    ch.cent_k16.copy_(torch.from_numpy(ck).to(torch.float16)); ch.cent_v16.copy_(torch.from_numpy(cv).to(torch.float16))
+    qf = 0.25 * u[None, None, :] + 0.125 * rng.integers(-2, 3, size=(H, nq, D))
+    qa = to_u16(torch.from_numpy(qf).to(torch.bfloat16))
+    out = torch.empty(H, nq, D, dtype=torch.float32, device="cuda")
+    q.qwm_attend(ctx, _bf(qa), nq, [ch], 1 / math.sqrt(D), out)
+    assert q.qwm_sync_status(ctx) == 0
+    for h in range(H):
+        ref = oracle.attend_rows(qa[h], np.arange(nq), [chunk_head(ch, h)], 1 / math.sqrt(D))
+        assert _attn_err(out[h].cpu().numpy().astype(np.float64), ref) <= 2e-3
+
+
 def test_attend_several_chunks_mixed_rank(q):
     """A cold-start chunk (no PSAC) followed by PSAC chunks with different bases and a ragged size."""
     w_ = synth.TINY
