@@ -169,10 +169,10 @@ def gen_layer(layer: int):
 
 
 # DRAM bytes per launch of the attention kernel (dram__bytes_read.sum + dram__bytes_write.sum from
-# one ncu capture, profiles/attend_tc_kernel_*.md), valid only for the kernel source they were taken
+# one ncu capture, profiles/attend_pair_kernel_*.md), valid only for the kernel source they were taken
 # on: the SHA-256 of csrc/attend.cu is checked, and the traffic reported as null otherwise.
-ATTEND_TRAFFIC = {"sha256": "63ebf9f4fe9e9ecf8be91b1144f8916911bc945257e83e87935c2ad5eee2e299",
-                  "720p": 473242880 + 192928256, "480p": 227208704 + 66112512}
+ATTEND_TRAFFIC = {"sha256": "a622608c7d9999142c4102acea976d8f31072dbe779fe1194a829b49ac7bdead",
+                  "720p": 476810496 + 190960640, "480p": 229728512 + 66204160}
 
 
 def attend_traffic(workload: str):
