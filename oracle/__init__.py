@@ -90,6 +90,9 @@ def lib():
             l.oracle_attend_rows.argtypes = [P, C.c_int, C.c_int, P, I64, C.POINTER(ChunkHead),
                                              C.c_int, C.c_double, P]
             l.oracle_dequantize_head.argtypes = [C.POINTER(ChunkHead), C.c_int, C.c_int, P, P, P, P]
+            l.oracle_prq_residual.argtypes = [P, I64, C.c_int, P, P, P]
+            l.oracle_kivi_quantize_head.argtypes = [P, P, I64, C.c_int, C.c_int, P, P, P, P, P, P]
+            l.oracle_kivi_dequantize_head.argtypes = [P, P, P, P, P, P, I64, C.c_int, C.c_int, P, P]
             l.oracle_fp16_val.argtypes = [C.c_uint16]
             l.oracle_fp16_val.restype = C.c_double
             l.oracle_round_fp16.argtypes = [C.c_double, C.c_int]
@@ -316,3 +319,70 @@ def round_fp16(x: float, direction: int) -> float:
 
 def bf16_rne(x: float) -> int:
     return lib().oracle_bf16_rne(float(x))
+
+
+# ---------------------------------------------------------------- comparison baselines
+
+
+def prq_residual(x_bf16: np.ndarray, cent_bf16: np.ndarray, idx: np.ndarray) -> np.ndarray:
+    """QVG progressive residual quantisation (Quant VideoGen summary §2B): the residual the next
+    stage quantises, bf16(x - mu_idx) for one head (x uint16 [n][d], cent uint16 [C][d])."""
+    x = _c(x_bf16, np.uint16); cent = _c(cent_bf16, np.uint16); ix = _c(idx, np.int32)
+    n, d = x.shape
+    out = np.empty_like(x)
+    if n:
+        lib().oracle_prq_residual(_p(x), n, d, _p(cent), _p(ix), _p(out))
+    return out
+
+
+def prq_head(k, v, cents_k: list, cents_v: list, group: int = 64):
+    """A QVG-style chunk for one head: len(cents) nearest-centroid stages (stage s quantises the
+    previous stage's residual with codebook cents[s]), then INT2 of the last residual.  Returns the
+    per-stage indices, the final stage's quantize_head output and the decoded K_hat, V_hat (double):
+    the sum of every stage's centroid and the INT2 reconstruction."""
+    rk, rv = _c(k, np.uint16), _c(v, np.uint16)
+    idx_k, idx_v = [], []
+    for s in range(len(cents_k) - 1):
+        o = quantize_head(rk, rv, cents_k[s], cents_v[s], None, None, group=group, top_m=1, rank=0)
+        idx_k.append(o["idx_k"]); idx_v.append(o["idx_v"])
+        rk = prq_residual(rk, cents_k[s], o["idx_k"])
+        rv = prq_residual(rv, cents_v[s], o["idx_v"])
+    last = quantize_head(rk, rv, cents_k[-1], cents_v[-1], None, None, group=group, top_m=1, rank=0)
+    idx_k.append(last["idx_k"]); idx_v.append(last["idx_v"])
+    ch = dict(idx_k=last["idx_k"], idx_v=last["idx_v"], k_codes=last["k_codes"], v_codes=last["v_codes"],
+              k_scale=last["k_scale"], k_min=last["k_min"], v_scale=last["v_scale"], v_min=last["v_min"],
+              cent_k=_c(cents_k[-1], np.uint16), cent_v=_c(cents_v[-1], np.uint16), rank=0)
+    _, _, kh, vh = dequantize_head(ch, group=group)
+    bf = lambda a: (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    for s in range(len(cents_k) - 1):
+        kh = kh + bf(_c(cents_k[s], np.uint16)[idx_k[s]])
+        vh = vh + bf(_c(cents_v[s], np.uint16)[idx_v[s]])
+    return dict(idx_k=idx_k, idx_v=idx_v, last=last, k_hat=kh, v_hat=vh)
+
+
+def kivi_quantize_head(k, v, group: int = 32):
+    """KIVI-style INT2 of one head: Keys per channel over groups of `group` tokens, Values per token
+    over groups of `group` channels (k, v uint16 bf16 [n][d])."""
+    k = _c(k, np.uint16); v = _c(v, np.uint16)
+    n, d = k.shape
+    ng = (n + group - 1) // group
+    o = dict(k_codes=np.zeros((n, d // 4), np.uint8), k_scale=np.zeros((ng, d), np.uint16),
+             k_min=np.zeros((ng, d), np.uint16), v_codes=np.zeros((n, d // 4), np.uint8),
+             v_scale=np.zeros((n, d // group), np.uint16), v_min=np.zeros((n, d // group), np.uint16))
+    if n:
+        lib().oracle_kivi_quantize_head(_p(k), _p(v), n, d, group, _p(o["k_codes"]), _p(o["k_scale"]),
+                                        _p(o["k_min"]), _p(o["v_codes"]), _p(o["v_scale"]), _p(o["v_min"]))
+    return o
+
+
+def kivi_dequantize_head(o: dict, group: int = 32):
+    """(K_hat, V_hat) as doubles [n][d] from kivi_quantize_head's output."""
+    n, d4 = o["k_codes"].shape
+    d = 4 * d4
+    kh = np.empty((n, d)); vh = np.empty((n, d))
+    arrs = {key: _c(o[key], np.uint8 if key.endswith("codes") else np.uint16) for key in o}
+    if n:
+        lib().oracle_kivi_dequantize_head(_p(arrs["k_codes"]), _p(arrs["k_scale"]), _p(arrs["k_min"]),
+                                          _p(arrs["v_codes"]), _p(arrs["v_scale"]), _p(arrs["v_min"]), n, d,
+                                          group, _p(kh), _p(vh))
+    return kh, vh

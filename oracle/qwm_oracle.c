@@ -11,7 +11,11 @@
  *             INT2 error estimate, PSAC logit form), "方法步骤详情" steps 1-5.
  *   [QWM-ko]  QuantWM summary (Korean), "무엇과 다른가" (QSAC), "어떻게 쓰나" (PSAC).
  *   [QWM-en]  QuantWM v2 summary, §4.1, §4.2, §5.1, §C.3, §D.1.
- *   [QVG-ko]  Quant VideoGen summary, §2A (k-means smoothing), §2C (streaming centroid caching).
+ *   [QVG-ko]  Quant VideoGen summary, §2A (k-means smoothing), §2B (progressive residual
+ *             quantisation), §2C (streaming centroid caching).
+ *   KIVI-style baseline: the QuantWM summaries name KIVI as a baseline with finer groups and a
+ *             bf16 recent window (Korean summary "전제와 한계"); its form here is the ablation
+ *             workload's: per-channel Key and per-token Value INT2 in groups of 32.
  *
  * Floating point: accumulations in double (fp64).  The two places where the
  * pages' format fixes a 32-bit computation -- the residual r = k - mu and the
@@ -670,6 +674,69 @@ void oracle_dequantize_head(const oracle_chunk_head *ch, int d, int group, uint1
     free(kh0);
     free(vh);
   }
+}
+
+/* ------------------------------------------------------------------ */
+/* comparison baselines of the ablation workload                        */
+/* ------------------------------------------------------------------ */
+
+/* QVG progressive residual quantisation ([QVG-ko] §2B), stage residual: the next stage quantises
+ * r = x - mu_idx, computed in float and rounded to bf16 (nearest-even) so that it can be fed to
+ * the next stage's k-means and quantiser like the tokens themselves.  x, cent: bf16 bits. */
+void oracle_prq_residual(const uint16_t *x, int64_t n, int d, const uint16_t *cent, const int32_t *idx,
+                         uint16_t *out) {
+  for (int64_t t = 0; t < n; t++)
+    for (int c = 0; c < d; c++) {
+      volatile float a = (float)bf16_val(x[t * d + c]), b = (float)bf16_val(cent[(int64_t)idx[t] * d + c]);
+      volatile float r = a - b;
+      out[t * d + c] = bf16_rne((double)r);
+    }
+}
+
+/* KIVI-style INT2 ([QWM-ko] "전제와 한계": finer groups; the ablation workload's reading):
+ * Keys per channel over groups of g consecutive tokens (the last group may be shorter), Values
+ * per token over groups of g consecutive channels; the same affine INT2 encoder as the QuantWM
+ * residuals, applied to the raw values.  Codes are packed per token like the QuantWM codes.
+ *   k_scale, k_min: fp16 [ceil(n/g)][d];  v_scale, v_min: fp16 [n][d/g]. */
+void oracle_kivi_quantize_head(const uint16_t *k, const uint16_t *v, int64_t n, int d, int g, uint8_t *k_codes,
+                               uint16_t *k_scale, uint16_t *k_min, uint8_t *v_codes, uint16_t *v_scale,
+                               uint16_t *v_min) {
+  float *r = (float *)malloc(sizeof(float) * (size_t)(g > d ? g : d));
+  uint8_t *q = (uint8_t *)malloc((size_t)(g > d ? g : d));
+  uint8_t *codes = (uint8_t *)calloc((size_t)(n > 0 ? n : 1) * d, 1);
+  const int64_t ng = (n + g - 1) / g;
+  for (int64_t tg = 0; tg < ng; tg++) {
+    const int len = (int)((n - tg * g) < g ? (n - tg * g) : g);
+    for (int c = 0; c < d; c++) {
+      for (int t = 0; t < len; t++) r[t] = (float)bf16_val(k[(tg * g + t) * d + c]);
+      oracle_int2_encode_group(r, len, q, &k_scale[tg * d + c], &k_min[tg * d + c]);
+      for (int t = 0; t < len; t++) codes[(tg * g + t) * d + c] = q[t];
+    }
+  }
+  for (int64_t t = 0; t < n; t++) oracle_pack2(codes + t * d, d, k_codes + t * (d / 4));
+  for (int64_t t = 0; t < n; t++) {
+    for (int cg = 0; cg < d / g; cg++) {
+      for (int c = 0; c < g; c++) r[c] = (float)bf16_val(v[t * d + cg * g + c]);
+      oracle_int2_encode_group(r, g, q, &v_scale[t * (d / g) + cg], &v_min[t * (d / g) + cg]);
+      for (int c = 0; c < g; c++) codes[t * d + cg * g + c] = q[c];
+    }
+    oracle_pack2(codes + t * d, d, v_codes + t * (d / 4));
+  }
+  free(r);
+  free(q);
+  free(codes);
+}
+
+/* KIVI-style decode: x_hat = m + s q per element (float, as for the residuals), as doubles. */
+void oracle_kivi_dequantize_head(const uint8_t *k_codes, const uint16_t *k_scale, const uint16_t *k_min,
+                                 const uint8_t *v_codes, const uint16_t *v_scale, const uint16_t *v_min, int64_t n,
+                                 int d, int g, double *k_hat, double *v_hat) {
+  for (int64_t t = 0; t < n; t++)
+    for (int c = 0; c < d; c++) {
+      const int64_t kg = (t / g) * d + c, vg = t * (d / g) + c / g;
+      k_hat[t * d + c] = (double)int2_decode(k_scale[kg], k_min[kg], unpack2(k_codes + t * (d / 4), c));
+      v_hat[t * d + c] = (double)int2_decode(v_scale[vg], v_min[vg], unpack2(v_codes + t * (d / 4), c));
+    }
 }
 
 /* Small helpers exported for the oracle's own tests. */

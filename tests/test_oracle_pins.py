@@ -410,3 +410,92 @@ def test_dequantize_bf16_is_rounded_float64():
     # where float32 holds the value exactly and within one bf16 step elsewhere
     for h, h64 in ((kh, kh64), (vh, vh64)):
         assert np.all(np.abs(f32(h) - h64) <= np.abs(h64) * 2 ** -8 + 1e-30)
+
+
+# ---------------------------------------------------------------- comparison baselines
+
+
+def _bf(a):
+    return (np.asarray(a, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _f16(a):
+    return np.asarray(a, np.uint16).view(np.float16).astype(np.float64)
+
+
+def test_prq_residual_zero_on_own_centroid_and_exact_second_stage():
+    """Quant VideoGen §2B: a token that is its own stage-1 centroid leaves a zero residual; a
+    stage-2 codebook holding the exact residuals reconstructs every token exactly (INT2 of zero)."""
+    k, v, _, _ = synth.small_case(1, 96, 128, 96, 8, seed=41)
+    k, v = k[0], v[0]
+    idx = np.arange(96)
+    assert not oracle.prq_residual(k, k, idx).any()
+    # stage 1: 16 centroids (tokens 0, 6, 12, ...); stage 2: each token's own residual
+    c1k, c1v = k[::6].copy(), v[::6].copy()
+    o1 = oracle.quantize_head(k, v, c1k, c1v, None, None, top_m=1, rank=0)
+    r1k = oracle.prq_residual(k, c1k, o1["idx_k"])
+    r1v = oracle.prq_residual(v, c1v, o1["idx_v"])
+    out = oracle.prq_head(k, v, [c1k, r1k], [c1v, r1v])
+    # the residual is rounded to bf16, so the reconstruction is x up to that rounding
+    rk = _bf(k) - _bf(c1k)[out["idx_k"][0]]
+    assert np.all(np.abs(out["k_hat"] - _bf(k)) <= np.abs(rk) * 2.0 ** -8 + 1e-30)
+    assert np.array_equal(out["idx_k"][1], np.arange(96)) or np.all(out["last"]["k_scale"] == 0)
+
+
+def test_prq_two_stage_error_bound():
+    """Decoded tokens of a two-stage chunk: |x - x_hat| <= s/2 (INT2 of the last residual) plus half a
+    bf16 step of the rounded stage-1 residual, per element."""
+    k, v, _, _ = synth.small_case(1, 300, 128, 64, 8, seed=42)
+    k, v = k[0], v[0]
+    c1k, _, _, _ = oracle.kmeans(k, 16, None, 3)
+    c1v, _, _, _ = oracle.kmeans(v, 16, None, 3)
+    o1 = oracle.quantize_head(k, v, c1k, c1v, None, None, top_m=1, rank=0)
+    r1 = oracle.prq_residual(k, c1k, o1["idx_k"])
+    c2k, _, _, _ = oracle.kmeans(r1, 16, None, 3)
+    r1v = oracle.prq_residual(v, c1v, o1["idx_v"])
+    c2v, _, _, _ = oracle.kmeans(r1v, 16, None, 3)
+    out = oracle.prq_head(k, v, [c1k, c2k], [c1v, c2v])
+    s = _f16(out["last"]["k_scale"])[:, np.arange(128) // 64]
+    exact_r1 = _bf(k) - _bf(c1k)[out["idx_k"][0]]
+    bound = s / 2 + np.abs(exact_r1) * 2.0 ** -8 + 1e-12  # half a bf16 step of r1 is at most |r1| 2^-8
+    assert np.all(np.abs(out["k_hat"] - _bf(k)) <= bound)
+    assert np.all(out["idx_k"][0] == o1["idx_k"])
+
+
+def _f16_down(x):
+    h = np.float16(x)
+    return h if float(h) <= x else np.nextafter(h, np.float16(-np.inf))
+
+
+def test_kivi_groups_error_bound_and_axes():
+    """KIVI-style INT2: Keys grouped per channel over 32 consecutive tokens (ragged last group),
+    Values per token over 32 consecutive channels.  Each group's offset is the fp16 round-down of
+    that group's minimum (brute force over the right axis), and every element is within s/2."""
+    k, v, _, _ = synth.small_case(1, 100, 128, 64, 8, seed=43)
+    k, v = k[0], v[0]
+    o = oracle.kivi_quantize_head(k, v, 32)
+    assert o["k_scale"].shape == (4, 128) and o["v_scale"].shape == (100, 4)
+    kf, vf = _bf(k), _bf(v)
+    for tg in range(4):
+        for c in (0, 5, 127):
+            seg = kf[32 * tg:32 * tg + 32, c]
+            assert _f16(o["k_min"][tg, c]) == float(_f16_down(seg.min()))
+    for t in (0, 50, 99):
+        for cg in range(4):
+            assert _f16(o["v_min"][t, cg]) == float(_f16_down(vf[t, 32 * cg:32 * cg + 32].min()))
+    kh, vh = oracle.kivi_dequantize_head(o, 32)
+    sk = _f16(o["k_scale"])[np.arange(100) // 32]
+    sv = _f16(o["v_scale"])[:, np.arange(128) // 32]
+    assert np.all(np.abs(kh - kf) <= sk / 2 + 1e-12)
+    assert np.all(np.abs(vh - vf) <= sv / 2 + 1e-12)
+
+
+def test_kivi_constant_groups_are_exact():
+    """A channel that is constant over a token group (Keys) or a channel group that is constant in a
+    token (Values) has s = 0 and decodes exactly."""
+    k = np.full((64, 128), synth.f32_to_bf16_bits(np.float32(1.5)), np.uint16)
+    v = np.full((64, 128), synth.f32_to_bf16_bits(np.float32(-0.25)), np.uint16)
+    o = oracle.kivi_quantize_head(k, v, 32)
+    assert not o["k_scale"].any() and not o["v_scale"].any()
+    kh, vh = oracle.kivi_dequantize_head(o, 32)
+    assert np.all(kh == 1.5) and np.all(vh == -0.25)
