@@ -32,7 +32,9 @@ QWM_OK, QWM_ERR_ARG, QWM_ERR_SHAPE, QWM_ERR_ALIGN, QWM_ERR_CUDA, QWM_ERR_NOT_CON
 
 EXPORTED = ("qwm_status_string", "qwm_workspace_bytes", "qwm_create", "qwm_destroy",
             "qwm_update_query_stats", "qwm_fit_centroids", "qwm_quantize_kv", "qwm_attend",
-            "qwm_dequantize", "qwm_sync_status", "qwm_update_query_stats_noalloc")
+            "qwm_dequantize", "qwm_sync_status", "qwm_update_query_stats_noalloc",
+            # comparison baselines (include/qwm_baselines.h)
+            "qwm_kivi_quantize", "qwm_kivi_dequantize", "qwm_prq_residual", "qwm_prq_dequantize")
 
 
 class QwmError(RuntimeError):
@@ -56,6 +58,11 @@ class qwm_chunk(C.Structure):
                 ("u_r", C.c_void_p), ("cent_k16", C.c_void_p), ("cent_v16", C.c_void_p)]
 
 
+class qwm_kivi_chunk(C.Structure):
+    _fields_ = [("n_tokens", C.c_int64), ("k_codes", C.c_void_p), ("v_codes", C.c_void_p),
+                ("k_scale", C.c_void_p), ("k_min", C.c_void_p), ("v_scale", C.c_void_p), ("v_min", C.c_void_p)]
+
+
 class qwm_debug(C.Structure):
     _fields_ = [("c_f32", C.c_void_p), ("cand", C.c_void_p), ("score", C.c_void_p)]
 
@@ -74,6 +81,10 @@ _lib.qwm_attend.argtypes = [_P, _P, C.c_int64, C.POINTER(qwm_chunk), C.c_int32, 
 _lib.qwm_dequantize.argtypes = [_P, C.POINTER(qwm_chunk), _P, _P, _P]
 _lib.qwm_sync_status.argtypes = [_P, _P]
 _lib.qwm_update_query_stats_noalloc.argtypes = [C.POINTER(qwm_config), _P, C.c_int64, _P, _P, _P, _P, _P, _P, _P]
+_lib.qwm_kivi_quantize.argtypes = [_P, _P, _P, C.c_int64, C.POINTER(qwm_kivi_chunk), _P]
+_lib.qwm_kivi_dequantize.argtypes = [_P, C.POINTER(qwm_kivi_chunk), _P, _P, _P]
+_lib.qwm_prq_residual.argtypes = [_P, _P, C.c_int64, _P, _P, _P, _P]
+_lib.qwm_prq_dequantize.argtypes = [_P, C.POINTER(qwm_chunk), _P, _P, _P, _P, _P, _P, _P]
 for _name in EXPORTED[2:]:
     getattr(_lib, _name).restype = C.c_int
 
@@ -276,3 +287,75 @@ def qwm_status_string(status: int) -> str:
 def raw_library() -> C.CDLL:
     """The loaded libqwm.so (for tests that inspect its exported symbols)."""
     return _lib
+
+
+# ---------------------------------------------------------------- comparison baselines (qwm_baselines.h)
+
+KIVI_GROUP = 32
+
+
+@dataclass
+class KiviChunk:
+    """Device tensors of one KIVI-style INT2 chunk (all heads), mirroring qwm_kivi_chunk."""
+    n_tokens: int
+    k_codes: torch.Tensor
+    v_codes: torch.Tensor
+    k_scale: torch.Tensor
+    k_min: torch.Tensor
+    v_scale: torch.Tensor
+    v_min: torch.Tensor
+
+    @staticmethod
+    def empty(ctx: Context, n: int, device=None) -> "KiviChunk":
+        H, d = ctx.cfg.heads, ctx.cfg.head_dim
+        dev = device or torch.device("cuda", torch.cuda.current_device())
+        ng = (n + KIVI_GROUP - 1) // KIVI_GROUP
+        u8 = dict(dtype=torch.uint8, device=dev)
+        f16 = dict(dtype=torch.float16, device=dev)
+        return KiviChunk(n, torch.empty(H, n, d // 4, **u8), torch.empty(H, n, d // 4, **u8),
+                         torch.empty(H, ng, d, **f16), torch.empty(H, ng, d, **f16),
+                         torch.empty(H, n, d // KIVI_GROUP, **f16), torch.empty(H, n, d // KIVI_GROUP, **f16))
+
+    def nbytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in (self.k_codes, self.v_codes, self.k_scale, self.k_min,
+                                                          self.v_scale, self.v_min))
+
+    def struct(self) -> qwm_kivi_chunk:
+        def p(t, width):
+            return _ptr(t, "kivi chunk field", width)
+        return qwm_kivi_chunk(self.n_tokens, p(self.k_codes, 1), p(self.v_codes, 1), p(self.k_scale, 2),
+                              p(self.k_min, 2), p(self.v_scale, 2), p(self.v_min, 2))
+
+
+def qwm_kivi_quantize(ctx: Context, k, v, n: int, out: KiviChunk, stream=None) -> None:
+    H, d = ctx.cfg.heads, ctx.cfg.head_dim
+    s = out.struct()
+    _check(_lib.qwm_kivi_quantize(ctx.handle, _ptr(k, "k", 2, (H, n, d)), _ptr(v, "v", 2, (H, n, d)), n,
+                                  C.byref(s), _stream(stream)), "qwm_kivi_quantize")
+
+
+def qwm_kivi_dequantize(ctx: Context, chunk: KiviChunk, k_hat, v_hat, stream=None) -> None:
+    H, d = ctx.cfg.heads, ctx.cfg.head_dim
+    s = chunk.struct()
+    _check(_lib.qwm_kivi_dequantize(ctx.handle, C.byref(s), _ptr(k_hat, "k_hat", 2, (H, chunk.n_tokens, d)),
+                                    _ptr(v_hat, "v_hat", 2, (H, chunk.n_tokens, d)), _stream(stream)),
+           "qwm_kivi_dequantize")
+
+
+def qwm_prq_residual(ctx: Context, x, n: int, cent, idx, out, stream=None) -> None:
+    H, d, Cn = ctx.cfg.heads, ctx.cfg.head_dim, ctx.cfg.n_centroids
+    _check(_lib.qwm_prq_residual(ctx.handle, _ptr(x, "x", 2, (H, n, d)), n, _ptr(cent, "cent", 2, (H, Cn, d)),
+                                 _ptr(idx, "idx", idx.element_size(), (H, n)), _ptr(out, "out", 2, (H, n, d)),
+                                 _stream(stream)), "qwm_prq_residual")
+
+
+def qwm_prq_dequantize(ctx: Context, last: Chunk, cent1_k, idx1_k, cent1_v, idx1_v, k_hat, v_hat,
+                       stream=None) -> None:
+    H, d, Cn, n = ctx.cfg.heads, ctx.cfg.head_dim, ctx.cfg.n_centroids, last.n_tokens
+    s = last.struct()
+    _check(_lib.qwm_prq_dequantize(ctx.handle, C.byref(s), _ptr(cent1_k, "cent1_k", 2, (H, Cn, d)),
+                                   _ptr(idx1_k, "idx1_k", idx1_k.element_size(), (H, n)),
+                                   _ptr(cent1_v, "cent1_v", 2, (H, Cn, d)),
+                                   _ptr(idx1_v, "idx1_v", idx1_v.element_size(), (H, n)),
+                                   _ptr(k_hat, "k_hat", 2, (H, n, d)), _ptr(v_hat, "v_hat", 2, (H, n, d)),
+                                   _stream(stream)), "qwm_prq_dequantize")

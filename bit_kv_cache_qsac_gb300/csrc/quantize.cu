@@ -112,27 +112,6 @@ __host__ __device__ constexpr uint32_t noswz16(uint32_t row, uint32_t k) {
   return (row >> 3) * 256u + (k >> 3) * 128u + (row & 7u) * 16u + (k & 7u) * 2u;
 }
 
-// INT2 parameters of one group from its fp32 residual min and max.
-__device__ __forceinline__ void int2_params(float mn, float mx, float &m, float &s, float &inv, uint16_t &m_bits,
-                                            uint16_t &s_bits, int32_t *status) {
-  const __half mh = __float2half_rd(mn);
-  m = __half2float(mh);
-  const float range = __fsub_ru(mx, m);
-  __half sh = __float2half_ru(__fdiv_ru(range, 3.0f));
-  if (range == 0.f) sh = __float2half_rn(0.f);
-  s = __half2float(sh);
-  if (!isfinite(m) || !isfinite(s)) qwm_dev_error(status, QWM_ERR_RANGE);
-  inv = s > 0.f ? __frcp_rn(s) : 0.f;
-  m_bits = __half_as_ushort(mh);
-  s_bits = __half_as_ushort(sh);
-}
-__device__ __forceinline__ uint32_t int2_code(float r, float m, float s, float inv) {
-  if (s == 0.f) return 0u;
-  float qf = rintf(__fmul_rn(__fsub_rn(r, m), inv));
-  qf = fminf(fmaxf(qf, 0.f), 3.f);
-  return (uint32_t)qf;
-}
-
 // Byte offset, inside a [128][64] x 2 swizzled tile, of this lane's 4 channels (4 lane .. 4 lane + 3)
 // of token row t.
 __device__ __forceinline__ uint32_t lane4_offset(int t, int lane) {

@@ -44,6 +44,30 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
 }
 __device__ __forceinline__ float f16_to_f32(uint16_t h) { return __half2float(__ushort_as_half(h)); }
 
+// INT2 encoder shared by the QuantWM quantiser and the KIVI-style baseline (affine, per group):
+// m = fp16 round-down of min r, s = fp16 round-up of (max r - m)/3 (0 when max r == m),
+// q = clamp(rint((r - m) * (1/s)), 0, 3), so |r - (m + s q)| <= s/2.
+// INT2 parameters of one group from its fp32 residual min and max.
+static __device__ __forceinline__ void int2_params(float mn, float mx, float &m, float &s, float &inv, uint16_t &m_bits,
+                                            uint16_t &s_bits, int32_t *status) {
+  const __half mh = __float2half_rd(mn);
+  m = __half2float(mh);
+  const float range = __fsub_ru(mx, m);
+  __half sh = __float2half_ru(__fdiv_ru(range, 3.0f));
+  if (range == 0.f) sh = __float2half_rn(0.f);
+  s = __half2float(sh);
+  if (!isfinite(m) || !isfinite(s)) qwm_dev_error(status, QWM_ERR_RANGE);
+  inv = s > 0.f ? __frcp_rn(s) : 0.f;
+  m_bits = __half_as_ushort(mh);
+  s_bits = __half_as_ushort(sh);
+}
+static __device__ __forceinline__ uint32_t int2_code(float r, float m, float s, float inv) {
+  if (s == 0.f) return 0u;
+  float qf = rintf(__fmul_rn(__fsub_rn(r, m), inv));
+  qf = fminf(fmaxf(qf, 0.f), 3.f);
+  return (uint32_t)qf;
+}
+
 // TMA tensor map (a 128-byte-aligned 128-byte blob, CUtensorMap) over rows of 128 bf16.
 struct alignas(128) TensorMap128 {
   unsigned char bytes[128];

@@ -1,5 +1,5 @@
 """Host-side checks of the C ABI (no GPU needed): the library loads, exports every
-symbol that include/qwm.h declares, and validates configurations before touching CUDA."""
+symbol that include/*.h declare, and validates configurations before touching CUDA."""
 import ctypes as C
 import os
 import re
@@ -10,7 +10,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def _declared():
-    src = open(os.path.join(ROOT, "include", "qwm.h")).read()
+    inc = os.path.join(ROOT, "include")
+    src = "".join(open(os.path.join(inc, f)).read() for f in sorted(os.listdir(inc)) if f.endswith(".h"))
     return sorted(set(re.findall(r"QWM_API\s+[\w\s\*]*?\b(qwm_\w+)\s*\(", src)))
 
 
