@@ -472,7 +472,7 @@ def _dev_bf16(a, device):
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
 
 
-def run_ablation(device):
+def run_ablation(device, sweep: bool = True):
     """Config-4 sweep on the 480p-shaped layer (40 heads, 8 chunks of 4,680 tokens): QSAC candidates
     M in {1, 4, 16}, PSAC rank r in {0, 8, 16}, codebook size C in {64, 256, 1024} (1024: uint16
     indices, codebook streamed through shared memory in slices).  Per configuration: packing time of the last
@@ -499,7 +499,7 @@ def run_ablation(device):
     del Kall
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     pairs = Hh * Wa.nq_attend * Wa.n_tokens
-    for C in (64, 256, 1024):
+    for C in ((64, 256, 1024) if sweep else ()):
         for M in (1, 4, 16):
             for r in (0, 8, 16):
                 ctx = q.Context(heads=Hh, n_centroids=C, top_m=M, rank=r, kmeans_iters=10)
@@ -533,6 +533,112 @@ def run_ablation(device):
                                   "compression": 2 * Hh * Wa.n_tokens * Dd * 2 / layer.nbytes()}), flush=True)
                 del layer, ctx, khat, L, out
                 torch.cuda.empty_cache()
+    run_ablation_baselines(device, K, V, Q, Qs, Lref, top_ref, ms2_ref)
+
+
+def run_ablation_baselines(device, K, V, Q, Qs, Lref, top_ref, ms2_ref):
+    """The two comparison methods of the ablation workload on the same cache (include/qwm_baselines.h):
+    QVG with two-stage progressive residual quantisation (256 + 256 centroids, nearest-centroid
+    assignment, no PSAC, INT2 of the last residual) and KIVI-style INT2 (per-channel Keys and
+    per-token Values in groups of 32, the last 2 latent frames kept in bf16).  Each packs chunk by
+    chunk with the library's kernels; 'pack_ms' is one chunk's packing.  Both methods decode to bf16
+    and then attend; 'attend_ms' is their decode of the whole cache (library kernels) plus a fused
+    bf16 attention (torch SDPA), the way these methods run."""
+    import torch
+    from torch.nn.attention import SDPBackend, sdpa_kernel
+    import bit_kv_cache_qsac_gb300 as q
+    Wa = synth.P480
+    Hh, Dd, T, n = Wa.heads, Wa.head_dim, Wa.n_chunks, Wa.chunk_tokens
+    scale = 1.0 / math.sqrt(Dd)
+    backends = [SDPBackend.CUDNN_ATTENTION, SDPBackend.FLASH_ATTENTION, SDPBackend.EFFICIENT_ATTENTION]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    bf16_bytes = 2 * Hh * Wa.n_tokens * Dd * 2
+
+    def report(name, pack_ms, khat, vhat, decode_fn, nbytes):
+        L = torch.einsum("hqd,hkd->hqk", Qs, khat.float()) * scale
+        mse = float(((L - Lref) ** 2).mean())
+        shift = float((L.argmax(-1) != top_ref).float().mean())
+        qb = Q[-1].unsqueeze(0)
+        for rep in range(2):  # the first pass warms up
+            ev[2].record()
+            kk, vv = decode_fn()
+            with sdpa_kernel(backends):
+                torch.nn.functional.scaled_dot_product_attention(qb, kk.unsqueeze(0), vv.unsqueeze(0))
+            ev[3].record()
+            torch.cuda.synchronize()
+        att = ev[2].elapsed_time(ev[3])
+        print(json.dumps({"report": "ablation", "workload": "480p-shaped layer, step 8 of 8", "method": name,
+                          "pack_ms": pack_ms, "pack_token_heads_per_s": Hh * n / (pack_ms / 1e3),
+                          "attend_ms": att, "attend_note": "decode of every chunk to bf16 + torch SDPA",
+                          "logit_mse": mse, "logit_mse_rel": mse / ms2_ref, "top1_shift": shift,
+                          "compression": bf16_bytes / nbytes}), flush=True)
+
+    # ---- QVG: two nearest-centroid stages, INT2 of the second residual ----
+    ctx = q.Context(heads=Hh, n_centroids=256, top_m=1, rank=0, kmeans_iters=10)
+    stages, pack_ms = [], 0.0
+    for t in range(T):
+        ev[0].record()
+        ch1 = q.Chunk.empty(ctx, n)
+        q.qwm_fit_centroids(ctx, K[t], n, None, ch1.cent_k)
+        q.qwm_fit_centroids(ctx, V[t], n, None, ch1.cent_v)
+        q.qwm_quantize_kv(ctx, K[t], V[t], n, None, None, ch1)
+        r1k, r1v = torch.empty_like(K[t]), torch.empty_like(V[t])
+        q.qwm_prq_residual(ctx, K[t], n, ch1.cent_k, ch1.k_idx, r1k)
+        q.qwm_prq_residual(ctx, V[t], n, ch1.cent_v, ch1.v_idx, r1v)
+        ch2 = q.Chunk.empty(ctx, n)
+        q.qwm_fit_centroids(ctx, r1k, n, None, ch2.cent_k)
+        q.qwm_fit_centroids(ctx, r1v, n, None, ch2.cent_v)
+        q.qwm_quantize_kv(ctx, r1k, r1v, n, None, None, ch2)
+        ev[1].record()
+        torch.cuda.synchronize()
+        pack_ms = ev[0].elapsed_time(ev[1])
+        stages.append((ch1, ch2))
+        del r1k, r1v
+    assert q.qwm_sync_status(ctx) == 0
+
+    def qvg_decode():
+        ks, vs = [], []
+        for ch1, ch2 in stages:
+            kh = torch.empty(Hh, n, Dd, dtype=torch.bfloat16, device=device); vh = torch.empty_like(kh)
+            q.qwm_prq_dequantize(ctx, ch2, ch1.cent_k, ch1.k_idx, ch1.cent_v, ch1.v_idx, kh, vh)
+            ks.append(kh); vs.append(vh)
+        return torch.cat(ks, dim=1), torch.cat(vs, dim=1)
+
+    kq, vq = qvg_decode()
+    qvg_bytes = sum(ch2.nbytes() + ch1.cent_k.numel() * 2 + ch1.cent_v.numel() * 2 + ch1.k_idx.numel() * 2
+                    for ch1, ch2 in stages)
+    report("QVG 2-stage PRQ (256 + 256 centroids)", pack_ms, kq, vq, qvg_decode, qvg_bytes)
+    del stages, kq, vq, ctx
+    torch.cuda.empty_cache()
+
+    # ---- KIVI-style: INT2 groups of 32, the last 2 latent frames in bf16 ----
+    ctx = q.Context(heads=Hh)
+    win = 2 * Wa.tokens_per_frame
+    parts = []
+    for t in range(T):
+        m = n - win if t == T - 1 else n  # tokens of this chunk that leave the bf16 window
+        kc = q.KiviChunk.empty(ctx, m)
+        ev[0].record()
+        q.qwm_kivi_quantize(ctx, K[t][:, :m].contiguous(), V[t][:, :m].contiguous(), m, kc)
+        ev[1].record()
+        torch.cuda.synchronize()
+        if m == n:
+            pack_ms = ev[0].elapsed_time(ev[1])
+        parts.append(kc)
+    assert q.qwm_sync_status(ctx) == 0
+    wk, wv = K[-1][:, n - win:].contiguous(), V[-1][:, n - win:].contiguous()
+
+    def kivi_decode():
+        ks, vs = [], []
+        for kc in parts:
+            kh = torch.empty(Hh, kc.n_tokens, Dd, dtype=torch.bfloat16, device=device); vh = torch.empty_like(kh)
+            q.qwm_kivi_dequantize(ctx, kc, kh, vh)
+            ks.append(kh); vs.append(vh)
+        return torch.cat(ks + [wk], dim=1), torch.cat(vs + [wv], dim=1)
+
+    kk, vk = kivi_decode()
+    kivi_bytes = sum(kc.nbytes() for kc in parts) + 2 * wk.numel() * 2
+    report("KIVI-style INT2 (groups of 32, 2-frame bf16 window)", pack_ms, kk, vk, kivi_decode, kivi_bytes)
 
 
 def run_full_model(device):
@@ -639,15 +745,18 @@ def main():
                     help="skip the dequantize+SDPA and bf16 SDPA context timings")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="720p",
                     help="720p-shaped layer (default) or 480p-shaped layer")
-    ap.add_argument("--report", choices=["ablation", "full-model"], default=None,
-                    help="instead of the benchmark line: the M x r x C sweep (config 4) or the 40-layer "
-                         "480p-shaped model (config 3)")
+    ap.add_argument("--report", choices=["ablation", "baselines", "full-model"], default=None,
+                    help="instead of the benchmark line: the M x r x C sweep and the QVG / KIVI baselines "
+                         "(config 4), the baselines alone, or the 40-layer 480p-shaped model (config 3)")
     args = ap.parse_args()
     if args.report:
         import torch
         device = torch.device("cuda", 0)
         torch.cuda.set_device(device)
-        run_ablation(device) if args.report == "ablation" else run_full_model(device)
+        if args.report == "full-model":
+            run_full_model(device)
+        else:
+            run_ablation(device, sweep=args.report == "ablation")
         return
     select_workload(args.workload)
     rank = int(os.environ.get("RANK", 0))
