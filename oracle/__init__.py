@@ -67,6 +67,7 @@ class ChunkHead(C.Structure):
         ("idx_k", P), ("idx_v", P), ("k_codes", P), ("v_codes", P),
         ("k_scale", P), ("k_min", P), ("v_scale", P), ("v_min", P),
         ("cent_k", P), ("cent_v", P), ("c", P), ("c_scale", P), ("u_r", P),
+        ("k_raw", P), ("v_raw", P), ("causal_tpf", I64),
     ]
 
 
@@ -266,11 +267,16 @@ def quantize_head(k, v, cent_k, cent_v, w=None, u_r=None, *, group=64, top_m=4, 
 
 def _chunk_struct(ch: dict, keep: list) -> ChunkHead:
     """ch: per-head dict with idx_k, idx_v, k_codes, v_codes, k_scale, k_min, v_scale, v_min,
-    cent_k, cent_v and, when rank > 0, c, c_scale, u_r."""
+    cent_k, cent_v and, when rank > 0, c, c_scale, u_r; or, for the chunk still being generated
+    (kept in bf16), k_raw and v_raw ([n][d] bf16 bits) and optionally causal_tpf (tokens per frame
+    of the block-causal mask, 0 = none)."""
     def arr(name, dtype):
         a = _c(ch[name], dtype)
         keep.append(a)
         return _p(a)
+    if "k_raw" in ch:
+        return ChunkHead(n=int(np.asarray(ch["k_raw"]).shape[0]), rank=0, k_raw=arr("k_raw", np.uint16),
+                         v_raw=arr("v_raw", np.uint16), causal_tpf=int(ch.get("causal_tpf", 0)))
     rank = int(ch.get("rank", 0))
     return ChunkHead(
         n=int(np.asarray(ch["idx_k"]).shape[0]), rank=rank,

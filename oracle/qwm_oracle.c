@@ -567,10 +567,23 @@ typedef struct {
   const int8_t *c;
   const uint16_t *c_scale;
   const uint16_t *u_r; /* [d][rank] */
+  /* The chunk still being generated, kept in bf16 ([QWM-en] §5.1, §D.1: a chunk is quantised once
+   * it is complete): k_raw != NULL makes every field above except n unused; keys are k_raw[j],
+   * values v_raw[j].  causal_tpf > 0 adds the block-causal mask of frames of causal_tpf tokens:
+   * the Query in row q (token q of this chunk) sees key j only when j / tpf <= q / tpf. */
+  const uint16_t *k_raw, *v_raw; /* [n][d] bf16 */
+  int64_t causal_tpf;
 } oracle_chunk_head;
 
 /* dequantised Key base k_hat_0 = mu_idx + r_hat and Value v_hat, as doubles */
 static void decode_token(const oracle_chunk_head *ch, int d, int group, int64_t j, double *kh0, double *vh) {
+  if (ch->k_raw) {
+    for (int c = 0; c < d; c++) {
+      kh0[c] = bf16_val(ch->k_raw[j * d + c]);
+      vh[c] = bf16_val(ch->v_raw[j * d + c]);
+    }
+    return;
+  }
   const int G = d / group;
   const uint16_t *muk = ch->cent_k + (int64_t)ch->idx_k[j] * d;
   const uint16_t *muv = ch->cent_v + (int64_t)ch->idx_v[j] * d;
@@ -611,6 +624,10 @@ void oracle_attend_rows(const uint16_t *q, int d, int group, const int64_t *rows
           qu[kk] = s;
         }
         for (int64_t j = 0; j < ch->n; j++) {
+          if (ch->k_raw && ch->causal_tpf > 0 && j / ch->causal_tpf > rows[ri] / ch->causal_tpf) {
+            l[off + j] = -INFINITY; /* a later frame of the chunk being generated */
+            continue;
+          }
           decode_token(ch, d, group, j, kh0, vh);
           double s = 0.0;
           for (int c = 0; c < d; c++) s += qd[c] * kh0[c];
@@ -630,6 +647,7 @@ void oracle_attend_rows(const uint16_t *q, int d, int group, const int64_t *rows
       for (int t = 0; t < n_chunks; t++) {
         const oracle_chunk_head *ch = &chunks[t];
         for (int64_t j = 0; j < ch->n; j++) {
+          if (l[off + j] == -INFINITY) continue;
           double p = exp(l[off + j] - lmax);
           denom += p;
           decode_token(ch, d, group, j, kh0, vh);

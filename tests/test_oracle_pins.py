@@ -499,3 +499,57 @@ def test_kivi_constant_groups_are_exact():
     assert not o["k_scale"].any() and not o["v_scale"].any()
     kh, vh = oracle.kivi_dequantize_head(o, 32)
     assert np.all(kh == 1.5) and np.all(vh == -0.25)
+
+
+# ---------------------------------------------------------------- the chunk still being generated (bf16)
+
+
+def _np_attention(q, k, v, scale, mask=None):
+    L = (q @ k.T) * scale
+    if mask is not None:
+        L = np.where(mask, L, -np.inf)
+    P = np.exp(L - L.max(1, keepdims=True))
+    return (P / P.sum(1, keepdims=True)) @ v
+
+
+def test_attend_bf16_chunk_is_textbook_attention():
+    k, v, _, qa = synth.small_case(1, 200, 128, 64, 40, seed=51)
+    raw = dict(k_raw=k[0], v_raw=v[0])
+    out = oracle.attend_rows(qa[0], np.arange(40), [raw], 0.09)
+    ref = _np_attention(_bf(qa[0]), _bf(k[0]), _bf(v[0]), 0.09)
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_attend_block_causal_mask():
+    """Frames of tpf tokens: row q sees key j only when j // tpf <= q // tpf.  Brute-force mask;
+    tpf = 1 makes row 0 attend to key 0 alone (its output is v_0 exactly); tpf = n removes the mask."""
+    n = 96
+    k, v, _, _ = synth.small_case(1, n, 128, 32, 8, seed=52)
+    q = synth.small_case(1, n, 128, 32, n, seed=53)[3][0]
+    rows = np.arange(n)
+    for tpf in (32, 7):
+        raw = dict(k_raw=k[0], v_raw=v[0], causal_tpf=tpf)
+        mask = (np.arange(n)[None, :] // tpf) <= (rows[:, None] // tpf)
+        out = oracle.attend_rows(q, rows, [raw], 0.1)
+        assert np.allclose(out, _np_attention(_bf(q), _bf(k[0]), _bf(v[0]), 0.1, mask), rtol=1e-12, atol=1e-12)
+    out1 = oracle.attend_rows(q, rows[:1], [dict(k_raw=k[0], v_raw=v[0], causal_tpf=1)], 0.1)
+    assert np.array_equal(out1[0], _bf(v[0])[0])
+    outn = oracle.attend_rows(q, rows, [dict(k_raw=k[0], v_raw=v[0], causal_tpf=n)], 0.1)
+    assert np.allclose(outn, oracle.attend_rows(q, rows, [dict(k_raw=k[0], v_raw=v[0])], 0.1), rtol=0, atol=0)
+
+
+def test_attend_packed_and_bf16_chunks_share_one_softmax():
+    """A packed chunk followed by a bf16 chunk: one softmax over the decoded packed keys and the raw
+    keys together."""
+    k, v, qs, qa = synth.small_case(1, 300, 128, 64, 24, seed=54)
+    ck, _, _, _ = oracle.kmeans(k[0, :200], 64, None, 3)
+    cv, _, _, _ = oracle.kmeans(v[0, :200], 64, None, 3)
+    o = oracle.quantize_head(k[0, :200], v[0, :200], ck, cv, None, None, top_m=1, rank=0)
+    packed = dict(idx_k=o["idx_k"], idx_v=o["idx_v"], k_codes=o["k_codes"], v_codes=o["v_codes"],
+                  k_scale=o["k_scale"], k_min=o["k_min"], v_scale=o["v_scale"], v_min=o["v_min"],
+                  cent_k=ck, cent_v=cv, rank=0)
+    _, _, kh, vh = oracle.dequantize_head(packed)
+    raw = dict(k_raw=k[0, 200:], v_raw=v[0, 200:])
+    out = oracle.attend_rows(qa[0], np.arange(24), [packed, raw], 0.08)
+    ref = _np_attention(_bf(qa[0]), np.concatenate([kh, _bf(k[0, 200:])]), np.concatenate([vh, _bf(v[0, 200:])]), 0.08)
+    assert np.allclose(out, ref, rtol=1e-10, atol=1e-12)
