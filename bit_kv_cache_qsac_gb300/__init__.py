@@ -51,11 +51,15 @@ class qwm_config(C.Structure):
 
 
 class qwm_chunk(C.Structure):
-    _fields_ = [("n_tokens", C.c_int64), ("rank_eff", C.c_int32), ("reserved", C.c_int32),
+    _fields_ = [("n_tokens", C.c_int64), ("rank_eff", C.c_int32), ("kind", C.c_int32),
                 ("k_codes", C.c_void_p), ("v_codes", C.c_void_p), ("k_idx", C.c_void_p), ("v_idx", C.c_void_p),
                 ("k_scale", C.c_void_p), ("k_min", C.c_void_p), ("v_scale", C.c_void_p), ("v_min", C.c_void_p),
                 ("cent_k", C.c_void_p), ("cent_v", C.c_void_p), ("c", C.c_void_p), ("c_scale", C.c_void_p),
-                ("u_r", C.c_void_p), ("cent_k16", C.c_void_p), ("cent_v16", C.c_void_p)]
+                ("u_r", C.c_void_p), ("cent_k16", C.c_void_p), ("cent_v16", C.c_void_p),
+                ("k_raw", C.c_void_p), ("v_raw", C.c_void_p), ("causal_tpf", C.c_int64)]
+
+
+QWM_CHUNK_PACKED, QWM_CHUNK_BF16 = 0, 1
 
 
 class qwm_kivi_chunk(C.Structure):
@@ -205,12 +209,34 @@ class Chunk:
     def struct(self) -> qwm_chunk:
         def p(t, width):
             return _ptr(t, "chunk field", width)
-        return qwm_chunk(self.n_tokens, self.rank_eff, 0,
+        return qwm_chunk(self.n_tokens, self.rank_eff, QWM_CHUNK_PACKED,
                          p(self.k_codes, 1), p(self.v_codes, 1),
                          p(self.k_idx, self.k_idx.element_size()), p(self.v_idx, self.v_idx.element_size()),
                          p(self.k_scale, 2), p(self.k_min, 2), p(self.v_scale, 2), p(self.v_min, 2),
                          p(self.cent_k, 2), p(self.cent_v, 2), p(self.c, 1), p(self.c_scale, 2), p(self.u_r, 2),
-                         p(self.cent_k16, 2), p(self.cent_v16, 2))
+                         p(self.cent_k16, 2), p(self.cent_v16, 2), None, None, 0)
+
+
+@dataclass
+class ActiveChunk:
+    """The chunk still being generated: its bf16 Keys and Values [H][N][d], attended beside the
+    packed chunks (qwm_chunk of kind QWM_CHUNK_BF16), with an optional block-causal mask over
+    frames of `causal_tpf` tokens (Query row i is token i of this chunk)."""
+    k: torch.Tensor
+    v: torch.Tensor
+    causal_tpf: int = 0
+
+    @property
+    def n_tokens(self) -> int:
+        return self.k.shape[1]
+
+    def struct(self) -> qwm_chunk:
+        s = qwm_chunk()
+        s.n_tokens, s.rank_eff, s.kind = self.n_tokens, 0, QWM_CHUNK_BF16
+        s.k_raw = _ptr(self.k, "active chunk k", 2)
+        s.v_raw = _ptr(self.v, "active chunk v", 2, tuple(self.k.shape))
+        s.causal_tpf = int(self.causal_tpf)
+        return s
 
 
 def qwm_update_query_stats(ctx: Context, q, nq: int, S, n, w, eigvals, u_r, stream=None) -> None:

@@ -55,6 +55,13 @@ qwm_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QWM_OK : QWM_E
 qwm_status check_chunk(const qwm_config &c, const qwm_chunk *ch, bool need_f16) {
   if (!ch) return QWM_ERR_ARG;
   if (ch->n_tokens < 0) return QWM_ERR_ARG;
+  if (ch->kind == QWM_CHUNK_BF16) {
+    if (ch->rank_eff != 0 || ch->causal_tpf < 0) return QWM_ERR_ARG;
+    if (!ch->k_raw || !ch->v_raw) return QWM_ERR_ARG;
+    if (!aligned16(ch->k_raw) || !aligned16(ch->v_raw)) return QWM_ERR_ALIGN;
+    return QWM_OK;
+  }
+  if (ch->kind != QWM_CHUNK_PACKED) return QWM_ERR_ARG;
   if (ch->rank_eff != 0 && ch->rank_eff != c.rank) return QWM_ERR_SHAPE;
   const void *req[] = {ch->k_codes, ch->v_codes, ch->k_idx,  ch->v_idx,  ch->k_scale,
                        ch->k_min,   ch->v_scale, ch->v_min, ch->cent_k, ch->cent_v};
@@ -190,6 +197,7 @@ qwm_status qwm_quantize_kv(qwm_ctx *ctx, const uint16_t *k, const uint16_t *v, i
   if (out->n_tokens != n) return QWM_ERR_SHAPE;
   if (n > ((int64_t)1 << 31) / QWM_D) return QWM_ERR_SHAPE;
   if (!aligned16(k) || !aligned16(v) || (w && !aligned16(w)) || (u_r && !aligned16(u_r))) return QWM_ERR_ALIGN;
+  if (out->kind != QWM_CHUNK_PACKED) return QWM_ERR_ARG;
   const bool psac = (u_r != nullptr) && ctx->cfg.rank > 0;
   out->rank_eff = psac ? ctx->cfg.rank : 0;
   qwm_status s = check_chunk(ctx->cfg, out, true);
@@ -228,6 +236,7 @@ qwm_status qwm_attend(qwm_ctx *ctx, const uint16_t *q, int64_t nq, const qwm_chu
 qwm_status qwm_dequantize(qwm_ctx *ctx, const qwm_chunk *chunk, uint16_t *k_hat, uint16_t *v_hat,
                           qwm_stream stream) {
   if (!ctx || !chunk) return QWM_ERR_ARG;
+  if (chunk->kind == QWM_CHUNK_BF16) return QWM_ERR_UNSUPPORTED;
   qwm_status s = check_chunk(ctx->cfg, chunk, false);
   if (s != QWM_OK) return s;
   if ((k_hat && !aligned16(k_hat)) || (v_hat && !aligned16(v_hat))) return QWM_ERR_ALIGN;

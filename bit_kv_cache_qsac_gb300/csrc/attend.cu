@@ -16,6 +16,12 @@
 // underflow to exactly 0) and 0 elsewhere.
 // O is written in fp32: the output is an average over thousands of keys, its largest entries are
 // ~16x its RMS, and rounding those to bf16 alone would cost ~0.03 x RMS(O).
+// The chunk still being generated (English v2 summary §5.1, §D.1: a chunk is quantised once it is
+// complete) may join the call as a bf16 chunk: its producers copy the rows themselves and convert
+// them to fp16 in place instead of decoding, its second-MMA operands carry only the padding mask,
+// and an optional block-causal mask (frames of tpf tokens; Query row i = token i of that chunk) is
+// applied by the softmax, which sets the logits of later frames to -inf.  Calls without such a
+// chunk run a variant compiled without any of it.
 //
 // Work split: a pair of CTAs (a cluster of two, cta_group::2 MMAs) takes one head x 512 Queries;
 // CTA c of the pair holds Query rows 256 x + 128 c .. 256 x + 128 c + 127 of its two tiles x = 0, 1.
@@ -99,6 +105,9 @@ struct AttnChunk {
   int64_t n;
   int rank;
   int tiles;
+  int raw;              // the chunk being generated: bf16 rows k_raw / v_raw instead of packed data
+  int64_t tpf;          // raw only: > 0 = block-causal mask over frames of tpf tokens
+  const uint16_t *k_raw, *v_raw;
   const uint8_t *k_codes, *v_codes, *k_idx, *v_idx;
   const uint16_t *k_scale, *k_min, *v_scale, *v_min, *cent_k16, *cent_v16, *c_scale, *u_r;
   const int8_t *c;
@@ -220,7 +229,7 @@ struct HalfRow {
   uint32_t csc;
 };
 
-template <bool VAL, bool IDX16>
+template <bool VAL, bool IDX16, bool RAW>
 __device__ __forceinline__ void load_half(const AttnChunk &c, int h, int64_t k0, int nk, int r, int g, bool coef,
                                           HalfRow &d) {
   d.idx = -1;
@@ -228,6 +237,10 @@ __device__ __forceinline__ void load_half(const AttnChunk &c, int h, int64_t k0,
   d.c = make_uint4(0, 0, 0, 0);
   d.ca = d.cb = make_uint2(0, 0);
   if (r >= nk) return;
+  if (RAW && c.raw) {  // the row of the chunk itself (a bf16 row: nothing to decode)
+    d.idx = (int)(k0 + r);
+    return;
+  }
   const int64_t gi = (int64_t)h * c.n + k0 + r;
   const uint8_t *ip = VAL ? c.v_idx : c.k_idx;
   d.idx = IDX16 ? (int)((const uint16_t *)ip)[gi] : (int)ip[gi];  // clamped where used
@@ -257,19 +270,21 @@ __device__ __forceinline__ void load_half(const AttnChunk &c, int h, int64_t k0,
   }
 }
 
-// Half rows (64 channels from channel ch0) of the centroids of this warp's 32 rows rbase .. rbase + 31
-// -> a [rows][64] swizzled block; each copy instruction moves four half rows (8 lanes each).
-__device__ __forceinline__ void issue_half_copies(const uint16_t *cent16, int h, int C, int idx, uint32_t block,
+// Half rows (64 channels from channel ch0) of this warp's 32 tile rows rbase .. rbase + 31 -> a
+// [rows][64] swizzled block: row `idx` (the lane's; < 0: zeros) of `base`, a [rows][d] fp16 or bf16
+// array of `nrows` rows (a codebook, or the bf16 chunk itself).  Each copy instruction moves four
+// half rows (8 lanes each).
+__device__ __forceinline__ void issue_half_copies(const uint16_t *base, int64_t nrows, int idx, uint32_t block,
                                                   int rbase, int ch0, int lane) {
   const uint32_t v = (uint32_t)lane & 7u;
 #pragma unroll
   for (int i = 0; i < 8; i++) {
     const int rl = 4 * i + (lane >> 3);
     int ix = __shfl_sync(0xffffffffu, idx, rl);
-    ix = ix < C ? ix : C - 1;  // never past the codebook
+    ix = ix < nrows ? ix : (int)nrows - 1;  // never past the array
     const uint32_t row = (uint32_t)(rbase + rl);
     const uint32_t dst = block + row * 128u + ((v ^ (row & 7u)) << 4);
-    const uint16_t *src = cent16 + ((int64_t)h * C + (ix >= 0 ? ix : 0)) * D + ch0 + 8 * v;
+    const uint16_t *src = base + (int64_t)(ix >= 0 ? ix : 0) * D + ch0 + 8 * v;
     tc::cp_async16_zfill(dst, src, ix >= 0 ? 16u : 0u);
   }
 }
@@ -305,10 +320,26 @@ __device__ __forceinline__ void decode_half(const HalfRow &d, uint32_t block, in
   }
 }
 
+// In-place bf16 -> fp16 of this thread's half row (a row of the chunk being generated).
+__device__ __forceinline__ void convert_half(const HalfRow &d, uint32_t block, int r) {
+  if (d.idx < 0) return;  // zero-filled by the copies
+  const uint32_t rowb = block + (uint32_t)r * 128u;
+#pragma unroll
+  for (int v = 0; v < 8; v++) {
+    const uint32_t addr = rowb + ((uint32_t)v << 4);  // the swizzle permutes whole 16-byte chunks
+    const uint4 b = tc::lds128(addr);
+    const uint32_t w[4] = {b.x, b.y, b.z, b.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int u = 0; u < 4; u++) o[u] = f16pair(__uint_as_float(w[u] << 16), __uint_as_float(w[u] & 0xFFFF0000u));
+    tc::sts128(addr, make_uint4(o[0], o[1], o[2], o[3]));
+  }
+}
+
 // Producer loop of one thread of a pair CTA (rank `cr`).  Keys: thread pr = (group g = pr / 64,
 // row pr % 64), decoding channel group g of key row 64 cr + pr % 64 of every tile.  Values: thread pr
 // = key row pr, decoding channel group cr.  Same schedule as the single-CTA producer.
-template <bool VAL, bool WIDE, bool IDX16>
+template <bool VAL, bool WIDE, bool IDX16, bool RAW>
 __device__ __forceinline__ void producer_pair(const AttnParams &p, unsigned char *sm, Bars &bars, int *abort_flag,
                                               uint32_t lut, int h, int64_t qrow0, int cr, int pr, int lane) {
   volatile int *abort_v = abort_flag;
@@ -364,7 +395,7 @@ __device__ __forceinline__ void producer_pair(const AttnParams &p, unsigned char
     const AttnChunk &c = p.ch[tt];
     const int64_t k0 = (int64_t)ti * BN;
     const int nk = (c.n - k0) < BN ? (int)(c.n - k0) : BN;
-    load_half<VAL, IDX16>(c, h, k0, nk, krow, g, coef, d);
+    load_half<VAL, IDX16, RAW>(c, h, k0, nk, krow, g, coef, d);
   };
   HalfRow A, B;
   B.idx = -1;
@@ -373,7 +404,15 @@ __device__ __forceinline__ void producer_pair(const AttnParams &p, unsigned char
     advance(t1, ti1);
     load_at(t1, ti1, B);
   }
-  issue_half_copies(VAL ? p.ch[0].cent_v16 : p.ch[0].cent_k16, h, C, A.idx, block0, rbase, 64 * g, lane);
+  // rows that the copies read: the chunk's fp16 codebook, or the bf16 chunk itself
+  auto copies = [&](int tt, int idx, uint32_t block) {
+    const AttnChunk &c = p.ch[tt];
+    if (RAW && c.raw)
+      issue_half_copies((VAL ? c.v_raw : c.k_raw) + (int64_t)h * c.n * D, c.n, idx, block, rbase, 64 * g, lane);
+    else
+      issue_half_copies((VAL ? c.cent_v16 : c.cent_k16) + (int64_t)h * C * D, C, idx, block, rbase, 64 * g, lane);
+  };
+  copies(0, A.idx, block0);
   tc::cp_async_commit();
   bool live = !VAL || build_qx(0);  // chunk 0's QX while the first copies fly
   auto step = [&](int j, HalfRow &cur, const HalfRow &nxt) -> bool {
@@ -381,7 +420,8 @@ __device__ __forceinline__ void producer_pair(const AttnParams &p, unsigned char
     const AttnChunk &ch = p.ch[t0];
     tc::cp_async_wait<0>();
     __syncwarp();  // the warp's copies of tile j, made visible to every lane
-    decode_half<!WIDE>(cur, block0 + (uint32_t)s * kStage, rr, lut);
+    if (RAW && ch.raw) convert_half(cur, block0 + (uint32_t)s * kStage, rr);
+    else decode_half<!WIDE>(cur, block0 + (uint32_t)s * kStage, rr, lut);
     if (!VAL && coef) write_x_row<WIDE>(cur, ch.rank, xs0 + (uint32_t)s * XL<WIDE>::kXBytes, rr);
     tc::fence_proxy_async_smem();
     __syncwarp();
@@ -394,8 +434,7 @@ __device__ __forceinline__ void producer_pair(const AttnParams &p, unsigned char
       if (j + 1 >= kStages && !tc::mbar_wait(&empty[sn], ((j + 1) / kStages - 1) & 1, kWaitNs))
         fail(abort_flag, p.status);
       if (__any_sync(0xffffffffu, *abort_v != 0)) return false;  // warp-uniform exit
-      issue_half_copies(VAL ? p.ch[t1].cent_v16 : p.ch[t1].cent_k16, h, C, nxt.idx,
-                        block0 + (uint32_t)sn * kStage, rbase, 64 * g, lane);
+      copies(t1, nxt.idx, block0 + (uint32_t)sn * kStage);
       tc::cp_async_commit();
     }
     t2 = t1; ti2 = ti1;
@@ -414,7 +453,9 @@ __device__ __forceinline__ void producer_pair(const AttnParams &p, unsigned char
   tc::cp_async_wait<0>();
 }
 
-template <bool WIDE, bool IDX16>
+// WIDE: PSAC ranks above 8 (32-column second-MMA operands).  IDX16: uint16 centroid indices.
+// RAW: the call includes a bf16 chunk (the chunk being generated).
+template <bool WIDE, bool IDX16, bool RAW>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     attend_pair_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -498,11 +539,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     float m_used = -INFINITY;
     uint64_t acc0 = 0ull, acc1 = 0ull;
     const uint64_t sc2 = pk64(__float_as_uint(sl2), __float_as_uint(sl2));
+    const int64_t qrow = qb + (int64_t)x * 2 * BM + row;  // this thread's Query row
+    int tc_ = 0, ti_ = 0;                                  // chunk and tile in chunk of tile j
     bool ok = true;
     for (int j = 0; j < J; j++) {
       if (!tc::mbar_wait(&bars.s_full[x], j & 1, kWaitNs)) fail(&abort_flag, p.status);
       if (*abort_v) { ok = false; break; }
       tc::fence_after_sync();
+      // block-causal mask of the chunk being generated: columns from `lim` on belong to a later frame
+      int lim = BN;
+      if (RAW) {
+        const AttnChunk &c = p.ch[tc_];
+        if (c.tpf > 0) {
+          const int64_t l = (qrow / c.tpf + 1) * c.tpf - (int64_t)ti_ * BN;
+          lim = l < 0 ? 0 : (l < BN ? (int)l : BN);
+        }
+        if (++ti_ == c.tiles) { ti_ = 0; tc_++; }
+      }
       // one pass over the tile, 32 columns at a time: the chunk's max, then its exponentials with the
       // running max m_used; when a chunk raises the max by more than 2^8 (rare after the first
       // chunk) the sum, O and the P chunks already stored for this tile are first rescaled
@@ -512,6 +565,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc::tmem_ld16(tS + 32u * cq, r);
         tc::tmem_ld16(tS + 32u * cq + 16u, r + 16);
         tc::tmem_ld_wait();
+        if (lim < 32 * cq + 32) {
+#pragma unroll
+          for (int i = 0; i < 32; i++)
+            if (32 * cq + i >= lim) r[i] = 0xFF800000u;  // -inf: weight exactly 0
+        }
         float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
@@ -550,7 +608,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           m_used = m_new;
         }
-        const uint64_t nm2 = pk64(__float_as_uint(-m_used), __float_as_uint(-m_used));
+        const float mneg = (RAW && m_used == -INFINITY) ? 0.f : -m_used;  // a row with no unmasked key yet
+        const uint64_t nm2 = pk64(__float_as_uint(mneg), __float_as_uint(mneg));
         uint32_t pw[16];
 #pragma unroll
         for (int i = 0; i < 16; i++) {  // packed fp32 pairs: x = S * scale - m, then 2^x
@@ -663,10 +722,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!tc::mbar_wait(&bars.drain, 0, kWaitNs)) qwm_dev_error(p.status, QWM_ERR_DEVICE_TIMEOUT);
     }
   } else if (warp < kVWarp0) {
-    producer_pair<false, WIDE, IDX16>(p, sm, bars, &abort_flag, tc::smem_u32(code_lut), h, qb, cr,
+    producer_pair<false, WIDE, IDX16, RAW>(p, sm, bars, &abort_flag, tc::smem_u32(code_lut), h, qb, cr,
                                       tid - 32 * kKWarp0, lane);
   } else {
-    producer_pair<true, WIDE, IDX16>(p, sm, bars, &abort_flag, tc::smem_u32(code_lut), h, qb, cr,
+    producer_pair<true, WIDE, IDX16, RAW>(p, sm, bars, &abort_flag, tc::smem_u32(code_lut), h, qb, cr,
                                      tid - 32 * kVWarp0, lane);
   }
   tc::fence_before_sync();
@@ -678,13 +737,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool WIDE, bool IDX16>
+template <bool WIDE, bool IDX16, bool RAW>
 cudaError_t launch_pair(const AttnParams &p, dim3 grid, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(attend_pair_kernel<WIDE, IDX16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       XL<WIDE>::kSmemAlloc);
+  cudaError_t e = cudaFuncSetAttribute(attend_pair_kernel<WIDE, IDX16, RAW>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, XL<WIDE>::kSmemAlloc);
   if (e != cudaSuccess) return e;
-  attend_pair_kernel<WIDE, IDX16><<<grid, kThreads, XL<WIDE>::kSmemAlloc, st>>>(p);
+  attend_pair_kernel<WIDE, IDX16, RAW><<<grid, kThreads, XL<WIDE>::kSmemAlloc, st>>>(p);
   return cudaGetLastError();
+}
+
+template <bool RAW>
+cudaError_t launch_pair_raw(const AttnParams &p, dim3 grid, bool wide, bool idx16, cudaStream_t st) {
+  if (wide && idx16) return launch_pair<true, true, RAW>(p, grid, st);
+  if (wide) return launch_pair<true, false, RAW>(p, grid, st);
+  if (idx16) return launch_pair<false, true, RAW>(p, grid, st);
+  return launch_pair<false, false, RAW>(p, grid, st);
 }
 
 }  // namespace
@@ -698,6 +765,7 @@ cudaError_t launch_attend(const qwm_config &cfg, const uint16_t *q, int64_t nq, 
   p.status = status;
   int used = 0, tiles = 0;
   bool wide = false;  // a chunk with PSAC rank above 8: the 32-column second-MMA operands
+  bool raw = false;   // a bf16 chunk (the chunk being generated)
   for (int i = 0; i < n_chunks; i++) {
     const qwm_chunk &c = chunks[i];
     if (c.n_tokens == 0) continue;  // empty chunks contribute nothing
@@ -708,6 +776,10 @@ cudaError_t launch_attend(const qwm_config &cfg, const uint16_t *q, int64_t nq, 
     a.k_idx = (const uint8_t *)c.k_idx; a.v_idx = (const uint8_t *)c.v_idx;
     a.k_scale = c.k_scale; a.k_min = c.k_min; a.v_scale = c.v_scale; a.v_min = c.v_min;
     a.cent_k16 = c.cent_k16; a.cent_v16 = c.cent_v16; a.c_scale = c.c_scale; a.u_r = c.u_r; a.c = c.c;
+    a.raw = c.kind == QWM_CHUNK_BF16;
+    raw |= a.raw != 0;
+    a.tpf = a.raw ? c.causal_tpf : 0;
+    a.k_raw = c.k_raw; a.v_raw = c.v_raw;
     tiles += a.tiles;
     wide |= a.rank > 8;
   }
@@ -716,10 +788,7 @@ cudaError_t launch_attend(const qwm_config &cfg, const uint16_t *q, int64_t nq, 
   const bool idx16 = cfg.n_centroids > 256;
   cudaError_t e;
   const dim3 grid((unsigned)(2 * ((nq + kPairQ - 1) / kPairQ)), cfg.heads);  // CTA pairs
-  if (wide && idx16) e = launch_pair<true, true>(p, grid, st);
-  else if (wide) e = launch_pair<true, false>(p, grid, st);
-  else if (idx16) e = launch_pair<false, true>(p, grid, st);
-  else e = launch_pair<false, false>(p, grid, st);
+  e = raw ? launch_pair_raw<true>(p, grid, wide, idx16, st) : launch_pair_raw<false>(p, grid, wide, idx16, st);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

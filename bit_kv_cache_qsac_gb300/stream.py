@@ -14,7 +14,7 @@ import math
 
 import torch
 
-from . import (Chunk, Context, qwm_attend, qwm_dequantize, qwm_fit_centroids, qwm_quantize_kv,
+from . import (ActiveChunk, Chunk, Context, qwm_attend, qwm_dequantize, qwm_fit_centroids, qwm_quantize_kv,
                qwm_sync_status, qwm_update_query_stats)
 
 
@@ -67,12 +67,14 @@ class CompressedLayer:
         return ch
 
     def attend(self, q: torch.Tensor, out: torch.Tensor | None = None, scale: float | None = None,
-               stream=None) -> torch.Tensor:
-        """Step 5: attention of Queries [H][nq][d] over every packed chunk."""
+               stream=None, active: "ActiveChunk | None" = None) -> torch.Tensor:
+        """Step 5: attention of Queries [H][nq][d] over every packed chunk and, when given, the
+        chunk still being generated (bf16, optionally block-causal) in the same softmax."""
         H, nq, d = q.shape
         if out is None:
             out = torch.empty(H, nq, d, dtype=torch.float32, device=q.device)
-        qwm_attend(self.ctx, q, nq, self.chunks, 1.0 / math.sqrt(d) if scale is None else scale, out, stream)
+        chunks = self.chunks + ([active] if active is not None else [])
+        qwm_attend(self.ctx, q, nq, chunks, 1.0 / math.sqrt(d) if scale is None else scale, out, stream)
         return out
 
     def dequantize(self, i: int, stream=None):

@@ -79,12 +79,19 @@ typedef struct {
 
 typedef struct qwm_ctx qwm_ctx;
 
+/* Kind of a chunk descriptor.  A chunk is quantised once it is complete; the chunk still being
+ * generated stays in bf16 and attends beside the packed history (English v2 summary §5.1, §D.1). */
+typedef enum {
+  QWM_CHUNK_PACKED = 0, /* written by qwm_quantize_kv */
+  QWM_CHUNK_BF16 = 1    /* k_raw / v_raw only (qwm_attend) */
+} qwm_chunk_kind;
+
 /* One compressed chunk of the cache, all heads.  Every pointer is caller-owned
  * device memory; N = n_tokens, H = heads, d = head_dim, G = d / group, r = rank. */
 typedef struct {
   int64_t n_tokens;      /* N >= 0 */
-  int32_t rank_eff;      /* r used for this chunk: 0 (cold start, PSAC off) or config.rank */
-  int32_t reserved;
+  int32_t rank_eff;      /* r used for this chunk: 0 (cold start, PSAC off) or config.rank; 0 for bf16 */
+  int32_t kind;          /* qwm_chunk_kind */
   uint8_t *k_codes;      /* [H][N][d/4]: channel 4j+t -> bits 2t..2t+1 of byte j */
   uint8_t *v_codes;      /* [H][N][d/4] */
   void *k_idx;           /* [H][N] Key centroid index: uint8 when C <= 256, uint16 when C = 1024 */
@@ -103,6 +110,12 @@ typedef struct {
                             value of magnitude in [2^-14, 65504] exactly; a centroid beyond 65504
                             records QWM_ERR_RANGE. */
   uint16_t *cent_v16;    /* fp16 [H][C][d]: the Value codebook, likewise */
+  /* QWM_CHUNK_BF16 only (every packed field above is then unused): */
+  const uint16_t *k_raw; /* bf16 [H][N][d] Keys of the chunk being generated */
+  const uint16_t *v_raw; /* bf16 [H][N][d] */
+  int64_t causal_tpf;    /* > 0: block-causal mask over frames of causal_tpf tokens: Query row i (the
+                            i-th row of qwm_attend's q, taken as token i of this chunk) sees key j of
+                            this chunk only when j / causal_tpf <= i / causal_tpf; 0: no mask */
 } qwm_chunk;
 
 /* Optional stage outputs of qwm_quantize_kv for parity checks (NULL members are skipped). */
@@ -169,7 +182,10 @@ QWM_API qwm_status qwm_quantize_kv(qwm_ctx *ctx, const uint16_t *k, const uint16
  * 选择": L = Q K^T / sqrt(d); "核心方法": PSAC logits Q K_hat_0^T + Q U_r C^T).
  *   q        bf16 [H][nq][d]
  *   chunks   HOST array of 1 <= n_chunks <= 128 chunk descriptors (device pointers inside);
- *            chunks with n_tokens == 0 are skipped
+ *            chunks with n_tokens == 0 are skipped.  QWM_CHUNK_BF16 chunks (the chunk still being
+ *            generated) attend with their bf16 Keys and Values (converted to the kernel's fp16
+ *            operands: exact for magnitudes in [2^-14, 65504]) in the same softmax, optionally
+ *            under their block-causal mask; a Query row must see at least one key
  *   softmax_scale  multiplies both logit terms (usually 1/sqrt(d))
  *   out      fp32 [H][nq][d] = softmax(l) V_hat over every token of every chunk (no mask); fp32
  *            because the output averages thousands of values and its largest entries are many
@@ -180,7 +196,8 @@ QWM_API qwm_status qwm_quantize_kv(qwm_ctx *ctx, const uint16_t *k, const uint16
 QWM_API qwm_status qwm_attend(qwm_ctx *ctx, const uint16_t *q, int64_t nq, const qwm_chunk *chunks, int32_t n_chunks,
                       float softmax_scale, float *out, qwm_stream stream);
 
-/* Step 5' -- BF16 reconstruction of one chunk (the pages' fused decoder, English v2 §D.1):
+/* Step 5' -- BF16 reconstruction of one packed chunk (the pages' fused decoder, English v2 §D.1;
+ * QWM_ERR_UNSUPPORTED for a QWM_CHUNK_BF16 descriptor):
  * K_hat = mu^K_idx + r_hat + C_hat U_r^T and V_hat = mu^V_idx + r_hat, rounded to nearest-even.
  *   k_hat, v_hat  bf16 [H][N][d] out (either may be NULL). */
 QWM_API qwm_status qwm_dequantize(qwm_ctx *ctx, const qwm_chunk *chunk, uint16_t *k_hat, uint16_t *v_hat,

@@ -343,6 +343,41 @@ def test_attend_growing_logits(q):
         assert _attn_err(out[h].cpu().numpy().astype(np.float64), ref) <= 2e-3
 
 
+@pytest.mark.parametrize("n,nq", [(1000, 300), (128, 1), (77, 64)])
+def test_attend_bf16_chunk_alone(q, n, nq):
+    """The chunk still being generated, alone: its bf16 rows attend as they are."""
+    H = 2
+    k = synth.keys(WIDE_W)[:H, :n]; v = synth.values(WIDE_W)[:H, :n]
+    ctx = q.Context(heads=H)
+    act = q.ActiveChunk(_bf(k), _bf(v))
+    qa = synth.queries(WIDE_W, 3, nq)
+    out = torch.empty(H, nq, D, dtype=torch.float32, device="cuda")
+    q.qwm_attend(ctx, _bf(qa), nq, [act], 1 / math.sqrt(D), out)
+    assert q.qwm_sync_status(ctx) == 0
+    for h in range(H):
+        ref = oracle.attend_rows(qa[h], np.arange(nq), [dict(k_raw=k[h], v_raw=v[h])], 1 / math.sqrt(D))
+        assert _attn_err(out[h].cpu().numpy().astype(np.float64), ref) <= 2e-2
+
+
+@pytest.mark.parametrize("tpf", [0, 256, 100])
+def test_attend_packed_history_and_causal_active_chunk(q, tpf):
+    """Packed history (1,024 tokens, PSAC) plus the chunk being generated (600 bf16 tokens) in one
+    softmax; with tpf > 0 Query row i (token i of the active chunk) sees only the active chunk's frames
+    up to its own."""
+    ctx, ch = _packed(q)
+    H, na = 2, 600
+    k = synth.keys(WIDE_W)[:H, 2000:2000 + na]; v = synth.values(WIDE_W)[:H, 2000:2000 + na]
+    act = q.ActiveChunk(_bf(np.ascontiguousarray(k)), _bf(np.ascontiguousarray(v)), causal_tpf=tpf)
+    qa = synth.queries(WIDE_W, 4, na)
+    out = torch.empty(H, na, D, dtype=torch.float32, device="cuda")
+    q.qwm_attend(ctx, _bf(qa), na, [ch, act], 1 / math.sqrt(D), out)
+    assert q.qwm_sync_status(ctx) == 0
+    for h in range(H):
+        ref = oracle.attend_rows(qa[h], np.arange(na),
+                                 [chunk_head(ch, h), dict(k_raw=k[h], v_raw=v[h], causal_tpf=tpf)], 1 / math.sqrt(D))
+        assert _attn_err(out[h].cpu().numpy().astype(np.float64), ref) <= 2e-2
+
+
 def test_attend_several_chunks_mixed_rank(q):
     """A cold-start chunk (no PSAC) followed by PSAC chunks with different bases and a ragged size."""
     w_ = synth.TINY
