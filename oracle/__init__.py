@@ -54,10 +54,12 @@ class QuantArgs(C.Structure):
         ("k", P), ("v", P), ("cent_k", P), ("cent_v", P), ("w", P), ("u_r", P), ("u_r_f64", P),
         ("force_idx_k", P), ("force_idx_v", P),
         ("n", I64), ("d", I32), ("C", I32), ("group", I32), ("top_m", I32), ("rank", I32),
+        ("storage", I32), ("psac_gate", I32),
         ("idx_k", P), ("idx_v", P), ("k_codes", P), ("v_codes", P),
         ("k_scale", P), ("k_min", P), ("v_scale", P), ("v_min", P),
         ("c", P), ("c_scale", P), ("c_real", P), ("cand", P), ("score2", P), ("dq_edge", P),
-        ("vdist2", P),
+        ("vdist2", P), ("k_s8", P), ("v_s8", P), ("k_zp", P), ("v_zp", P), ("k_sigma", P), ("v_sigma", P),
+        ("gate_err", P),
     ]
 
 
@@ -223,11 +225,14 @@ def int8_encode_token(Cf: np.ndarray):
 
 
 def quantize_head(k, v, cent_k, cent_v, w=None, u_r=None, *, group=64, top_m=4, rank=None,
-                  u_r_f64=None, force_idx_k=None, force_idx_v=None):
+                  u_r_f64=None, force_idx_k=None, force_idx_v=None, storage=0, psac_gate=0):
     """QSAC Key assignment, nearest-centroid Value assignment, INT2 residuals and PSAC for one head.
 
     k, v: uint16 [n][d]; cent_k, cent_v: uint16 [C][d]; w: float [d] or None (uniform);
-    u_r: uint16 [d][r] or None (PSAC off).  Returns a dict of every output and diagnostic."""
+    u_r: uint16 [d][r] or None (PSAC off).  storage 0: fp16 step and offset per (token, group);
+    storage 1: the compact metadata (8-bit step, 2-bit zero-point, power-of-two second-level scale
+    per 128-token tile).  psac_gate: keep C only where it lowers the w-weighted error.
+    Returns a dict of every output and diagnostic."""
     k = _c(k, np.uint16); v = _c(v, np.uint16)
     cent_k = _c(cent_k, np.uint16); cent_v = _c(cent_v, np.uint16)
     n, d = k.shape
@@ -249,10 +254,14 @@ def quantize_head(k, v, cent_k, cent_v, w=None, u_r=None, *, group=64, top_m=4, 
         c_real=np.zeros((n, max(rank, 1)), np.float64),
         cand=np.empty((n, top_m), np.int32), score2=np.empty((n, 2)), dq_edge=np.empty((n, 2)),
         vdist2=np.empty((n, 2)),
+        k_s8=np.zeros((n, G), np.uint8), v_s8=np.zeros((n, G), np.uint8),
+        k_zp=np.zeros(n, np.uint8), v_zp=np.zeros(n, np.uint8),
+        k_sigma=np.zeros(((n + 127) // 128, G), np.uint16), v_sigma=np.zeros(((n + 127) // 128, G), np.uint16),
+        gate_err=np.zeros((n, 2)),
     )
     a = QuantArgs(k=_p(k), v=_p(v), cent_k=_p(cent_k), cent_v=_p(cent_v), w=_p(w64), u_r=_p(ur),
                   u_r_f64=_p(ur64), force_idx_k=_p(fk), force_idx_v=_p(fv), n=n, d=d, C=Cn,
-                  group=group, top_m=top_m, rank=rank,
+                  group=group, top_m=top_m, rank=rank, storage=storage, psac_gate=psac_gate,
                   **{key: _p(val) for key, val in o.items()})
     if n:
         lib().oracle_quantize_head(C.byref(a))

@@ -426,6 +426,51 @@ static double qsac_score(const uint16_t *k, const uint16_t *mu, const double *w,
   return S;
 }
 
+/* The paper's compact metadata ([QWM-zh] step (3) "组缩放INT8+FP16二级缩放"; [QWM-en] §D.1
+ * "bit-packed INT2 zero-points"): r_hat = s (q - z) with an integer zero-point z in {0..3} and a step
+ * s = sigma * s8, s8 an unsigned 8-bit integer and sigma a second-level scale shared, per group of
+ * channels, by a tile of 128 tokens.  Readings (the pages give neither granularity nor rounding):
+ * sigma is a power of two (an fp16 value), so s and every s (q - z) are exact in fp16 and fp32; each
+ * (token, group) takes the zero-point whose grid [-z s, (3 - z) s] covers its residual range with the
+ * smallest s (lower z on ties); sigma is the smallest power of two with 255 sigma >= the tile's
+ * largest such s; s8 = ceil(s / sigma); q = clamp(rint(r (1/s) + z), 0, 3).  So |r - r_hat| <= s/2. */
+#define ZP_TILE 128
+static void zp_range(float a, float b, float *s_need, int *z_out) {
+  *s_need = 0.0f;
+  *z_out = 0;
+  if (a == 0.0f && b == 0.0f) return;
+  float best = INFINITY;
+  for (int z = 0; z < 4; z++) {
+    const float lo = (a >= 0.0f) ? 0.0f : (z > 0 ? f32_div_up(-a, (float)z) : INFINITY);
+    const float hi = (b <= 0.0f) ? 0.0f : (z < 3 ? f32_div_up(b, (float)(3 - z)) : INFINITY);
+    const float sz = lo > hi ? lo : hi;
+    if (sz < best) { best = sz; *z_out = z; }
+  }
+  *s_need = best;
+}
+static float pow2_sigma(float smax) {
+  if (smax == 0.0f) return 0.0f;
+  const float t = f32_div_up(smax, 255.0f);
+  int e;
+  const double m = frexp((double)t, &e); /* t = m 2^e, m in [1/2, 1) */
+  float sg = (m == 0.5) ? (float)ldexp(1.0, e - 1) : (float)ldexp(1.0, e);
+  if (sg < 5.9604644775390625e-08f) sg = 5.9604644775390625e-08f; /* 2^-24, the smallest fp16 */
+  return sg;
+}
+static void zp_encode_group(const float *r, int g, float s, int z, uint8_t *codes) {
+  if (s == 0.0f) {
+    for (int c = 0; c < g; c++) codes[c] = 0;
+    return;
+  }
+  const float inv = f32_rcp(s);
+  for (int c = 0; c < g; c++) {
+    float q = nearbyintf(f32_add(f32_mul(r[c], inv), (float)z));
+    if (q < 0.0f) q = 0.0f;
+    if (q > 3.0f) q = 3.0f;
+    codes[c] = (uint8_t)q;
+  }
+}
+
 typedef struct {
   /* inputs */
   const uint16_t *k, *v;          /* [n][d] bf16 */
@@ -437,6 +482,8 @@ typedef struct {
   const int32_t *force_idx_v;     /* [n] or NULL */
   int64_t n;
   int32_t d, C, group, top_m, rank;
+  int32_t storage;                /* 0: fp16 step and offset per group; 1: the compact metadata */
+  int32_t psac_gate;              /* 1: keep C only where it lowers sum_c w_c e_c^2 ([QWM-zh] step (4)) */
   /* outputs */
   int32_t *idx_k, *idx_v;         /* [n] */
   uint8_t *k_codes, *v_codes;     /* [n][d/4] */
@@ -448,12 +495,55 @@ typedef struct {
   double *score2;                 /* optional [n][2]: best and second-best S over the candidates */
   double *dq_edge;                /* optional [n][2]: the M-th and (M+1)-th smallest d_Q */
   double *vdist2;                 /* optional [n][2]: best and second-best Value distance */
+  uint8_t *k_s8, *v_s8;           /* storage 1: [n][d/group] steps */
+  uint8_t *k_zp, *v_zp;           /* storage 1: [n] zero-points, group g in bits 2g..2g+1 */
+  uint16_t *k_sigma, *v_sigma;    /* storage 1: fp16 [ceil(n/128)][d/group] second-level scales */
+  double *gate_err;               /* optional [n][2]: w-weighted error without and with C */
 } oracle_quant_args;
+
+/* Step 4 for one token: C = E U_r with E = K - K_hat_0 (double accumulation), INT8 per token; with
+ * the gate, C is kept only when sum_c w_c (E_c - (C_hat U_r^T)_c)^2 < sum_c w_c E_c^2 (C_hat the
+ * decoded INT8 coefficients), else stored as zeros with a zero scale. */
+static void psac_token(const oracle_quant_args *a, int64_t i, const uint16_t *k, const float *khat0,
+                       const double *w, float *Cf) {
+  const int d = a->d, r = a->rank;
+  for (int kk = 0; kk < r; kk++) {
+    double acc = 0.0;
+    for (int c = 0; c < d; c++) {
+      double e = (double)bf16_valf(k[c]) - (double)khat0[c];
+      acc += e * (a->u_r_f64 ? a->u_r_f64[c * r + kk] : bf16_val(a->u_r[c * r + kk]));
+    }
+    if (a->c_real) a->c_real[i * r + kk] = acc;
+    Cf[kk] = (float)acc;
+  }
+  oracle_int8_encode_token(Cf, r, a->c + i * r, a->c_scale + i);
+  if (a->psac_gate || a->gate_err) {
+    const double sc = oracle_fp16_val(a->c_scale[i]);
+    double e0 = 0.0, e1 = 0.0;
+    for (int c = 0; c < d; c++) {
+      const double e = (double)bf16_valf(k[c]) - (double)khat0[c];
+      double corr = 0.0;
+      for (int kk = 0; kk < r; kk++)
+        corr += sc * (double)a->c[i * r + kk] * (a->u_r_f64 ? a->u_r_f64[c * r + kk] : bf16_val(a->u_r[c * r + kk]));
+      e0 += w[c] * e * e;
+      e1 += w[c] * (e - corr) * (e - corr);
+    }
+    if (a->gate_err) { a->gate_err[2 * i] = e0; a->gate_err[2 * i + 1] = e1; }
+    if (a->psac_gate && !(e1 < e0)) {
+      for (int kk = 0; kk < r; kk++) a->c[i * r + kk] = 0;
+      a->c_scale[i] = 0;
+    }
+  }
+}
 
 void oracle_quantize_head(const oracle_quant_args *a) {
   const int d = a->d, C = a->C, G = d / a->group, M = a->top_m, r = a->rank;
+  const int compact = a->storage == 1;
   double *w = (double *)malloc(sizeof(double) * d);
   for (int c = 0; c < d; c++) w[c] = a->w ? a->w[c] : 1.0;
+  /* compact metadata: per (token, K/V, group) the needed step and zero-point, then sigma per tile */
+  float *s_need = compact ? (float *)malloc(sizeof(float) * (size_t)(a->n > 0 ? a->n : 1) * 2 * G) : NULL;
+  int *zp = compact ? (int *)malloc(sizeof(int) * (size_t)(a->n > 0 ? a->n : 1) * 2 * G) : NULL;
 #pragma omp parallel
   {
     double *dq = (double *)malloc(sizeof(double) * C);
@@ -515,10 +605,22 @@ void oracle_quantize_head(const oracle_quant_args *a) {
       for (int pass = 0; pass < 2; pass++) {
         const uint16_t *x = pass ? v : k;
         const uint16_t *mu = pass ? a->cent_v + (int64_t)jv * d : a->cent_k + (int64_t)jk * d;
+        for (int c = 0; c < d; c++) res[c] = f32_sub(bf16_valf(x[c]), bf16_valf(mu[c]));
+        if (compact) { /* the residual ranges only; the codes follow once sigma is known */
+          for (int g = 0; g < G; g++) {
+            float mn = res[g * a->group], mx = mn;
+            for (int c = 1; c < a->group; c++) {
+              const float t = res[g * a->group + c];
+              if (t < mn) mn = t;
+              if (t > mx) mx = t;
+            }
+            zp_range(mn, mx, &s_need[(i * 2 + pass) * G + g], &zp[(i * 2 + pass) * G + g]);
+          }
+          continue;
+        }
         uint8_t *packed = (pass ? a->v_codes : a->k_codes) + i * (d / 4);
         uint16_t *sc = (pass ? a->v_scale : a->k_scale) + i * G;
         uint16_t *mn = (pass ? a->v_min : a->k_min) + i * G;
-        for (int c = 0; c < d; c++) res[c] = f32_sub(bf16_valf(x[c]), bf16_valf(mu[c]));
         for (int g = 0; g < G; g++)
           oracle_int2_encode_group(res + g * a->group, a->group, codes + g * a->group, sc + g, mn + g);
         oracle_pack2(codes, d, packed);
@@ -528,18 +630,47 @@ void oracle_quantize_head(const oracle_quant_args *a) {
             khat0[c] = f32_add(bf16_valf(mu[c]), int2_decode(sc[g], mn[g], codes[c]));
           }
       }
-      /* ---- step 4: PSAC  E = K - K_hat_0,  C = E U_r ---- */
-      if ((a->u_r || a->u_r_f64) && r > 0) {
-        for (int kk = 0; kk < r; kk++) {
-          double acc = 0.0;
-          for (int c = 0; c < d; c++) {
-            double e = (double)bf16_valf(k[c]) - (double)khat0[c];
-            acc += e * (a->u_r_f64 ? a->u_r_f64[c * r + kk] : bf16_val(a->u_r[c * r + kk]));
+      /* ---- step 4: PSAC ---- */
+      if (!compact && (a->u_r || a->u_r_f64) && r > 0) psac_token(a, i, k, khat0, w, Cf);
+    }
+#pragma omp barrier
+    if (compact) {
+      /* second-level scales: per tile of 128 tokens and group, the power of two for the largest step */
+#pragma omp for schedule(static)
+      for (int64_t tg = 0; tg < (a->n + ZP_TILE - 1) / ZP_TILE; tg++)
+        for (int pass = 0; pass < 2; pass++)
+          for (int g = 0; g < G; g++) {
+            float smax = 0.0f;
+            for (int64_t i = tg * ZP_TILE; i < a->n && i < (tg + 1) * ZP_TILE; i++)
+              if (s_need[(i * 2 + pass) * G + g] > smax) smax = s_need[(i * 2 + pass) * G + g];
+            (pass ? a->v_sigma : a->k_sigma)[tg * G + g] = fp16_bits_of((double)pow2_sigma(smax));
           }
-          if (a->c_real) a->c_real[i * r + kk] = acc;
-          Cf[kk] = (float)acc;
+#pragma omp for schedule(static)
+      for (int64_t i = 0; i < a->n; i++) {
+        const uint16_t *k = a->k + i * d, *v = a->v + i * d;
+        for (int pass = 0; pass < 2; pass++) {
+          const uint16_t *x = pass ? v : k;
+          const int j = pass ? a->idx_v[i] : a->idx_k[i];
+          const uint16_t *mu = (pass ? a->cent_v : a->cent_k) + (int64_t)j * d;
+          uint8_t zbits = 0;
+          for (int c = 0; c < d; c++) res[c] = f32_sub(bf16_valf(x[c]), bf16_valf(mu[c]));
+          for (int g = 0; g < G; g++) {
+            const float sg = (float)oracle_fp16_val((pass ? a->v_sigma : a->k_sigma)[(i / ZP_TILE) * G + g]);
+            const float need = s_need[(i * 2 + pass) * G + g];
+            const int z = zp[(i * 2 + pass) * G + g];
+            const int s8 = (need == 0.0f) ? 0 : (int)ceilf(need / sg); /* exact: sigma is a power of two */
+            const float s = sg * (float)s8;                             /* exact */
+            (pass ? a->v_s8 : a->k_s8)[i * G + g] = (uint8_t)s8;
+            zbits |= (uint8_t)(z << (2 * g));
+            zp_encode_group(res + g * a->group, a->group, s, z, codes + g * a->group);
+            if (pass == 0)
+              for (int c = g * a->group; c < (g + 1) * a->group; c++)
+                khat0[c] = f32_add(bf16_valf(mu[c]), s * (float)((int)codes[c] - z)); /* s (q - z) exact */
+          }
+          (pass ? a->v_zp : a->k_zp)[i] = zbits;
+          oracle_pack2(codes, d, (pass ? a->v_codes : a->k_codes) + i * (d / 4));
         }
-        oracle_int8_encode_token(Cf, r, a->c + i * r, a->c_scale + i);
+        if ((a->u_r || a->u_r_f64) && r > 0) psac_token(a, i, k, khat0, w, Cf);
       }
     }
     free(dq);
@@ -550,6 +681,8 @@ void oracle_quantize_head(const oracle_quant_args *a) {
     free(Cf);
   }
   free(w);
+  free(s_need);
+  free(zp);
 }
 
 /* ------------------------------------------------------------------ */

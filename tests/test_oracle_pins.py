@@ -553,3 +553,83 @@ def test_attend_packed_and_bf16_chunks_share_one_softmax():
     out = oracle.attend_rows(qa[0], np.arange(24), [packed, raw], 0.08)
     ref = _np_attention(_bf(qa[0]), np.concatenate([kh, _bf(k[0, 200:])]), np.concatenate([vh, _bf(v[0, 200:])]), 0.08)
     assert np.allclose(out, ref, rtol=1e-10, atol=1e-12)
+
+
+# ---------------------------------------------------------------- compact metadata and the PSAC gate
+
+
+def _codes(packed):
+    n, d4 = packed.shape
+    out = np.zeros((n, 4 * d4), np.int64)
+    for c in range(4 * d4):
+        out[:, c] = (packed[:, c // 4] >> (2 * (c % 4))) & 3
+    return out
+
+
+def test_compact_metadata_bound_and_grid():
+    """Compact metadata (step (3): INT8 group scale + fp16 second-level scale; §D.1: INT2 zero-points):
+    r_hat = sigma s8 (q - z) reproduces every residual within s/2; sigma is a power of two per 128-token
+    tile and group, minimal for the tile's largest step (so that step's s8 lies in [128, 255]); a group
+    whose residuals are all >= 0 takes z = 0, all <= 0 takes z = 3; no zero-point gives a smaller step."""
+    k, v, _, _ = synth.small_case(1, 300, 128, 64, 8, seed=61)
+    k, v = k[0], v[0]
+    ck, _, _, _ = oracle.kmeans(k, 32, None, 3)
+    cv, _, _, _ = oracle.kmeans(v, 32, None, 3)
+    o = oracle.quantize_head(k, v, ck, cv, None, None, top_m=1, rank=0, storage=1)
+    for pre, x, cent in (("k", k, ck), ("v", v, cv)):
+        idx = o["idx_" + pre]
+        r = (_bf(x) - _bf(cent)[idx]).astype(np.float32).astype(np.float64)
+        sig = _f16(o[pre + "_sigma"])                      # [tiles][2]
+        s8 = o[pre + "_s8"].astype(np.float64)             # [n][2]
+        z = np.stack([(o[pre + "_zp"] >> (2 * g)) & 3 for g in range(2)], 1).astype(np.float64)
+        s = sig[np.arange(300) // 128] * s8
+        q = _codes(o[pre + "_codes"])
+        g = np.arange(128) // 64
+        rh = s[:, g] * (q - z[:, g])
+        assert np.all(np.abs(r - rh) <= s[:, g] / 2 + 1e-12)
+        nz = sig > 0
+        assert np.all(np.log2(sig[nz]) == np.round(np.log2(sig[nz])))
+        for t in range(3):
+            for gg in range(2):
+                rows = slice(128 * t, min(300, 128 * t + 128))
+                if sig[t, gg] > 0:
+                    assert 128 <= s8[rows, gg].max() <= 255
+        for i in range(0, 300, 7):
+            for gg in range(2):
+                a, b = r[i, 64 * gg:64 * gg + 64].min(), r[i, 64 * gg:64 * gg + 64].max()
+                if a >= 0 and b > 0:
+                    assert z[i, gg] == 0
+                if b <= 0 and a < 0:
+                    assert z[i, gg] == 3
+                # the smallest covering step over the four zero-points never exceeds the chosen one
+                need = min(max(-a / zz if zz else (0 if a >= 0 else np.inf), b / (3 - zz) if zz < 3 else (0 if b <= 0 else np.inf))
+                           for zz in range(4))
+                assert need <= s[i, gg] * (1 + 1e-6) + 1e-30
+
+
+def test_psac_gate_keeps_only_improving_coefficients():
+    """Step (4): C is kept only when it lowers the Query-weighted error.  With heavily uneven
+    weights some tokens' coefficients must be dropped; every dropped token has e1 >= e0 and every
+    kept one e1 < e0, recomputed here from the decoded K_hat_0 and C_hat."""
+    k, v, qs, _ = synth.small_case(1, 400, 128, 64, 256, seed=62)
+    S = np.zeros((1, 128, 128)); nn = np.zeros(1, np.int64)
+    w, _, ur, _, _ = oracle.update_query_stats(qs, S, nn, 8)
+    w = w[0].copy()
+    w[::3] *= 50.0                                          # uneven channel weights
+    ck, _, _, _ = oracle.kmeans(k[0], 64, None, 3)
+    cv, _, _, _ = oracle.kmeans(v[0], 64, None, 3)
+    base = oracle.quantize_head(k[0], v[0], ck, cv, w, ur[0], top_m=4, rank=8)
+    gated = oracle.quantize_head(k[0], v[0], ck, cv, w, ur[0], top_m=4, rank=8, psac_gate=1)
+    ch = dict(idx_k=base["idx_k"], idx_v=base["idx_v"], k_codes=base["k_codes"], v_codes=base["v_codes"],
+              k_scale=base["k_scale"], k_min=base["k_min"], v_scale=base["v_scale"], v_min=base["v_min"],
+              cent_k=ck, cent_v=cv, rank=0)
+    _, _, kh0, _ = oracle.dequantize_head(ch)
+    E = _bf(k[0]) - kh0
+    corr = (_f16(base["c_scale"])[:, None] * base["c"].astype(np.float64)) @ _bf(ur[0]).T
+    e0 = (w * E * E).sum(1)
+    e1 = (w * (E - corr) ** 2).sum(1)
+    drop = ~(e1 < e0)
+    assert drop.any() and (~drop).any()
+    assert np.all(gated["c"][drop] == 0) and np.all(gated["c_scale"][drop] == 0)
+    assert np.array_equal(gated["c"][~drop], base["c"][~drop])
+    assert np.array_equal(gated["c_scale"][~drop], base["c_scale"][~drop])
