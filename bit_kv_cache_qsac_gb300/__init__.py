@@ -47,7 +47,11 @@ class QwmError(RuntimeError):
 class qwm_config(C.Structure):
     _fields_ = [("heads", C.c_int32), ("head_dim", C.c_int32), ("n_centroids", C.c_int32),
                 ("group", C.c_int32), ("top_m", C.c_int32), ("rank", C.c_int32), ("bits", C.c_int32),
-                ("kmeans_iters", C.c_int32), ("seed", C.c_uint64)]
+                ("kmeans_iters", C.c_int32), ("seed", C.c_uint64), ("storage", C.c_int32),
+                ("psac_gate", C.c_int32)]
+
+
+QWM_STORAGE_FP16, QWM_STORAGE_COMPACT = 0, 1
 
 
 class qwm_chunk(C.Structure):
@@ -56,7 +60,9 @@ class qwm_chunk(C.Structure):
                 ("k_scale", C.c_void_p), ("k_min", C.c_void_p), ("v_scale", C.c_void_p), ("v_min", C.c_void_p),
                 ("cent_k", C.c_void_p), ("cent_v", C.c_void_p), ("c", C.c_void_p), ("c_scale", C.c_void_p),
                 ("u_r", C.c_void_p), ("cent_k16", C.c_void_p), ("cent_v16", C.c_void_p),
-                ("k_raw", C.c_void_p), ("v_raw", C.c_void_p), ("causal_tpf", C.c_int64)]
+                ("k_raw", C.c_void_p), ("v_raw", C.c_void_p), ("causal_tpf", C.c_int64),
+                ("k_s8", C.c_void_p), ("v_s8", C.c_void_p), ("k_zp", C.c_void_p), ("v_zp", C.c_void_p),
+                ("k_sigma", C.c_void_p), ("v_sigma", C.c_void_p)]
 
 
 QWM_CHUNK_PACKED, QWM_CHUNK_BF16 = 0, 1
@@ -68,7 +74,7 @@ class qwm_kivi_chunk(C.Structure):
 
 
 class qwm_debug(C.Structure):
-    _fields_ = [("c_f32", C.c_void_p), ("cand", C.c_void_p), ("score", C.c_void_p)]
+    _fields_ = [("c_f32", C.c_void_p), ("cand", C.c_void_p), ("score", C.c_void_p), ("gate_err", C.c_void_p)]
 
 
 _P = C.c_void_p
@@ -127,8 +133,10 @@ class Context:
     """Owns a qwm_ctx (its device workspace lives on the current device)."""
 
     def __init__(self, heads: int, n_centroids: int = 256, top_m: int = 4, rank: int = 8,
-                 kmeans_iters: int = 10, head_dim: int = 128, group: int = 64, bits: int = 2):
-        self.cfg = qwm_config(heads, head_dim, n_centroids, group, top_m, rank, bits, kmeans_iters, 0)
+                 kmeans_iters: int = 10, head_dim: int = 128, group: int = 64, bits: int = 2,
+                 storage: int = QWM_STORAGE_FP16, psac_gate: int = 0):
+        self.cfg = qwm_config(heads, head_dim, n_centroids, group, top_m, rank, bits, kmeans_iters, 0, storage,
+                              psac_gate)
         h = C.c_void_p()
         _check(_lib.qwm_create(C.byref(self.cfg), C.byref(h)), "qwm_create")
         self.handle = h
@@ -173,6 +181,17 @@ class Chunk:
     u_r: torch.Tensor
     cent_k16: torch.Tensor
     cent_v16: torch.Tensor
+    # QWM_STORAGE_COMPACT contexts: 8-bit steps, 2-bit zero-points, per-tile second-level scales
+    k_s8: torch.Tensor | None = None
+    v_s8: torch.Tensor | None = None
+    k_zp: torch.Tensor | None = None
+    v_zp: torch.Tensor | None = None
+    k_sigma: torch.Tensor | None = None
+    v_sigma: torch.Tensor | None = None
+
+    @property
+    def compact(self) -> bool:
+        return self.k_s8 is not None
 
     @staticmethod
     def empty(ctx: Context, n: int, device=None) -> "Chunk":
@@ -182,6 +201,22 @@ class Chunk:
         u8 = dict(dtype=torch.uint8, device=dev)
         f16 = dict(dtype=torch.float16, device=dev)
         ix = dict(dtype=torch.uint8 if Cn <= 256 else torch.int16, device=dev)  # int16 = uint16 bits
+        if cfg.storage == QWM_STORAGE_COMPACT:
+            nt = (n + 127) // 128
+            z = lambda *shape, **kw: torch.zeros(*shape, **kw)
+            return Chunk(n, 0,
+                         torch.empty(H, n, d // 4, **u8), torch.empty(H, n, d // 4, **u8),
+                         torch.empty(H, n, **ix), torch.empty(H, n, **ix),
+                         z(0, **f16), z(0, **f16), z(0, **f16), z(0, **f16),
+                         torch.empty(H, Cn, d, dtype=torch.bfloat16, device=dev),
+                         torch.empty(H, Cn, d, dtype=torch.bfloat16, device=dev),
+                         torch.zeros(H, n, max(r, 1), dtype=torch.int8, device=dev),
+                         torch.zeros(H, n, **f16),
+                         torch.zeros(H, d, max(r, 1), dtype=torch.bfloat16, device=dev),
+                         torch.empty(H, Cn, d, **f16), torch.empty(H, Cn, d, **f16),
+                         torch.empty(H, n, G, **u8), torch.empty(H, n, G, **u8),
+                         torch.empty(H, max(n, 1), **u8), torch.empty(H, max(n, 1), **u8),
+                         torch.empty(H, max(nt, 1), G, **f16), torch.empty(H, max(nt, 1), G, **f16))
         return Chunk(n, 0,
                      torch.empty(H, n, d // 4, **u8), torch.empty(H, n, d // 4, **u8),
                      torch.empty(H, n, **ix), torch.empty(H, n, **ix),
@@ -197,9 +232,12 @@ class Chunk:
     def nbytes(self, operand_copies: bool = False) -> int:
         """Bytes of the packed representation (codebooks and PSAC basis included); with
         `operand_copies`, also the fp16 codebook copies the attention kernel reads."""
+        meta = ((self.k_s8, self.v_s8, self.k_sigma, self.v_sigma) if self.compact
+                else (self.k_scale, self.k_min, self.v_scale, self.v_min))
         tot = sum(t.numel() * t.element_size() for t in (self.k_codes, self.v_codes, self.k_idx, self.v_idx,
-                                                         self.k_scale, self.k_min, self.v_scale, self.v_min,
-                                                         self.cent_k, self.cent_v))
+                                                         self.cent_k, self.cent_v) + meta)
+        if self.compact:  # the two groups' 2-bit zero-points of a token share one byte
+            tot += self.k_zp.numel() + self.v_zp.numel()
         if self.rank_eff:
             tot += sum(t.numel() * t.element_size() for t in (self.c, self.c_scale, self.u_r))
         if operand_copies:
@@ -214,7 +252,9 @@ class Chunk:
                          p(self.k_idx, self.k_idx.element_size()), p(self.v_idx, self.v_idx.element_size()),
                          p(self.k_scale, 2), p(self.k_min, 2), p(self.v_scale, 2), p(self.v_min, 2),
                          p(self.cent_k, 2), p(self.cent_v, 2), p(self.c, 1), p(self.c_scale, 2), p(self.u_r, 2),
-                         p(self.cent_k16, 2), p(self.cent_v16, 2), None, None, 0)
+                         p(self.cent_k16, 2), p(self.cent_v16, 2), None, None, 0,
+                         *(p(t, w) for t, w in ((self.k_s8, 1), (self.v_s8, 1), (self.k_zp, 1), (self.v_zp, 1),
+                                                (self.k_sigma, 2), (self.v_sigma, 2))))
 
 
 @dataclass
@@ -264,7 +304,7 @@ def qwm_quantize_kv(ctx: Context, k, v, n: int, w, u_r, out: Chunk, debug: dict 
     dbg = None
     if debug is not None:
         dbg = qwm_debug(_ptr(debug.get("c_f32"), "c_f32", 4), _ptr(debug.get("cand"), "cand", 4),
-                        _ptr(debug.get("score"), "score", 4))
+                        _ptr(debug.get("score"), "score", 4), _ptr(debug.get("gate_err"), "gate_err", 4))
     st = _lib.qwm_quantize_kv(ctx.handle, _ptr(k, "k", 2, (H, n, d)), _ptr(v, "v", 2, (H, n, d)), n,
                               _ptr(w, "w", 4, (H, d)), _ptr(u_r, "u_r", 2, (H, d, r)) if r else None,
                               C.byref(s), C.byref(dbg) if dbg is not None else None, _stream(stream))

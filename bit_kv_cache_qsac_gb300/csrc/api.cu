@@ -44,6 +44,8 @@ qwm_status check_config(const qwm_config *c) {
   if (c->rank > QWM_MAX_RANK) return QWM_ERR_SHAPE;
   if (c->kmeans_iters > 100) return QWM_ERR_SHAPE;
   if ((int64_t)c->heads > 4096) return QWM_ERR_SHAPE;
+  if (c->storage != QWM_STORAGE_FP16 && c->storage != QWM_STORAGE_COMPACT) return QWM_ERR_ARG;
+  if (c->psac_gate != 0 && c->psac_gate != 1) return QWM_ERR_ARG;
   return QWM_OK;
 }
 
@@ -63,8 +65,11 @@ qwm_status check_chunk(const qwm_config &c, const qwm_chunk *ch, bool need_f16) 
   }
   if (ch->kind != QWM_CHUNK_PACKED) return QWM_ERR_ARG;
   if (ch->rank_eff != 0 && ch->rank_eff != c.rank) return QWM_ERR_SHAPE;
-  const void *req[] = {ch->k_codes, ch->v_codes, ch->k_idx,  ch->v_idx,  ch->k_scale,
-                       ch->k_min,   ch->v_scale, ch->v_min, ch->cent_k, ch->cent_v};
+  const bool compact = c.storage == QWM_STORAGE_COMPACT;
+  const void *req[] = {ch->k_codes, ch->v_codes, ch->k_idx, ch->v_idx, ch->cent_k, ch->cent_v,
+                       compact ? (const void *)ch->k_s8 : ch->k_scale, compact ? (const void *)ch->k_zp : ch->k_min,
+                       compact ? (const void *)ch->v_s8 : ch->v_scale, compact ? (const void *)ch->v_zp : ch->v_min,
+                       compact ? (const void *)ch->k_sigma : ch->k_codes, compact ? (const void *)ch->v_sigma : ch->v_codes};
   for (const void *p : req) {
     if (!p) return QWM_ERR_ARG;
     if (!aligned16(p)) return QWM_ERR_ALIGN;

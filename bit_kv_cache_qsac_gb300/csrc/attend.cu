@@ -20,8 +20,10 @@
 // complete) may join the call as a bf16 chunk: its producers copy the rows themselves and convert
 // them to fp16 in place instead of decoding, its second-MMA operands carry only the padding mask,
 // and an optional block-causal mask (frames of tpf tokens; Query row i = token i of that chunk) is
-// applied by the softmax, which sets the logits of later frames to -inf.  Calls without such a
-// chunk run a variant compiled without any of it.
+// applied by the softmax, which sets the logits of later frames to -inf.  Chunks with the compact
+// INT2 metadata (8-bit step s8, 2-bit zero-point z, power-of-two second-level scale sigma per
+// 128-token tile) decode with s = sigma s8 and m = -z s, exact in fp16, through the same
+// fp16(mu + fp16(m + s q)).  Calls with neither run a variant compiled without any of it.
 //
 // Work split: a pair of CTAs (a cluster of two, cta_group::2 MMAs) takes one head x 512 Queries;
 // CTA c of the pair holds Query rows 256 x + 128 c .. 256 x + 128 c + 127 of its two tiles x = 0, 1.
@@ -108,6 +110,8 @@ struct AttnChunk {
   int raw;              // the chunk being generated: bf16 rows k_raw / v_raw instead of packed data
   int64_t tpf;          // raw only: > 0 = block-causal mask over frames of tpf tokens
   const uint16_t *k_raw, *v_raw;
+  const uint8_t *k_s8, *v_s8, *k_zp, *v_zp;  // compact metadata (steps, zero-points)
+  const uint16_t *k_sigma, *v_sigma;         // compact second-level scales [H][tiles][2]
   const uint8_t *k_codes, *v_codes, *k_idx, *v_idx;
   const uint16_t *k_scale, *k_min, *v_scale, *v_min, *cent_k16, *cent_v16, *c_scale, *u_r;
   const int8_t *c;
@@ -118,6 +122,7 @@ struct AttnParams {
   float *out;
   int64_t nq;
   int H, C, n_chunks, total_tiles;
+  int compact;       // the chunks' INT2 metadata is the compact form (8-bit step, 2-bit zero-point)
   float scale_log2;  // softmax_scale * log2(e)
   int32_t *status;
   AttnChunk ch[kMaxChunks];
@@ -229,25 +234,34 @@ struct HalfRow {
   uint32_t csc;
 };
 
-template <bool VAL, bool IDX16, bool RAW>
+template <bool VAL, bool IDX16, bool EXT>
 __device__ __forceinline__ void load_half(const AttnChunk &c, int h, int64_t k0, int nk, int r, int g, bool coef,
-                                          HalfRow &d) {
+                                          bool compact, HalfRow &d) {
   d.idx = -1;
   d.s2 = d.m2 = d.csc = 0u;
   d.c = make_uint4(0, 0, 0, 0);
   d.ca = d.cb = make_uint2(0, 0);
   if (r >= nk) return;
-  if (RAW && c.raw) {  // the row of the chunk itself (a bf16 row: nothing to decode)
+  if (EXT && c.raw) {  // the row of the chunk itself (a bf16 row: nothing to decode)
     d.idx = (int)(k0 + r);
     return;
   }
   const int64_t gi = (int64_t)h * c.n + k0 + r;
   const uint8_t *ip = VAL ? c.v_idx : c.k_idx;
   d.idx = IDX16 ? (int)((const uint16_t *)ip)[gi] : (int)ip[gi];  // clamped where used
-  const uint32_t sv = (VAL ? c.v_scale : c.k_scale)[gi * 2 + g];
-  const uint32_t mv = (VAL ? c.v_min : c.k_min)[gi * 2 + g];
-  d.s2 = sv | (sv << 16);
-  d.m2 = mv | (mv << 16);
+  if (EXT && compact) {  // s = sigma s8 and m = -z s, both exact in fp16
+    const float sg = f16_to_f32((VAL ? c.v_sigma : c.k_sigma)[((int64_t)h * c.tiles + k0 / BN) * 2 + g]);
+    const float st = sg * (float)(VAL ? c.v_s8 : c.k_s8)[gi * 2 + g];
+    const float z = (float)(((VAL ? c.v_zp : c.k_zp)[gi] >> (2 * g)) & 3u);
+    const uint32_t sv = __half_as_ushort(__float2half_rn(st)), mv = __half_as_ushort(__float2half_rn(-z * st));
+    d.s2 = sv | (sv << 16);
+    d.m2 = mv | (mv << 16);
+  } else {
+    const uint32_t sv = (VAL ? c.v_scale : c.k_scale)[gi * 2 + g];
+    const uint32_t mv = (VAL ? c.v_min : c.k_min)[gi * 2 + g];
+    d.s2 = sv | (sv << 16);
+    d.m2 = mv | (mv << 16);
+  }
   d.c = ((const uint4 *)((VAL ? c.v_codes : c.k_codes) + gi * (D / 4)))[g];
   if (!VAL && coef && c.rank > 0) {
     const int R = c.rank;
@@ -339,7 +353,7 @@ __device__ __forceinline__ void convert_half(const HalfRow &d, uint32_t block, i
 // Producer loop of one thread of a pair CTA (rank `cr`).  Keys: thread pr = (group g = pr / 64,
 // row pr % 64), decoding channel group g of key row 64 cr + pr % 64 of every tile.  Values: thread pr
 // = key row pr, decoding channel group cr.  Same schedule as the single-CTA producer.
-template <bool VAL, bool WIDE, bool IDX16, bool RAW>
+template <bool VAL, bool WIDE, bool IDX16, bool EXT>
 __device__ __forceinline__ void producer_pair(const AttnParams &p, unsigned char *sm, Bars &bars, int *abort_flag,
                                               uint32_t lut, int h, int64_t qrow0, int cr, int pr, int lane) {
   volatile int *abort_v = abort_flag;
@@ -395,7 +409,7 @@ __device__ __forceinline__ void producer_pair(const AttnParams &p, unsigned char
     const AttnChunk &c = p.ch[tt];
     const int64_t k0 = (int64_t)ti * BN;
     const int nk = (c.n - k0) < BN ? (int)(c.n - k0) : BN;
-    load_half<VAL, IDX16, RAW>(c, h, k0, nk, krow, g, coef, d);
+    load_half<VAL, IDX16, EXT>(c, h, k0, nk, krow, g, coef, p.compact != 0, d);
   };
   HalfRow A, B;
   B.idx = -1;
@@ -407,7 +421,7 @@ __device__ __forceinline__ void producer_pair(const AttnParams &p, unsigned char
   // rows that the copies read: the chunk's fp16 codebook, or the bf16 chunk itself
   auto copies = [&](int tt, int idx, uint32_t block) {
     const AttnChunk &c = p.ch[tt];
-    if (RAW && c.raw)
+    if (EXT && c.raw)
       issue_half_copies((VAL ? c.v_raw : c.k_raw) + (int64_t)h * c.n * D, c.n, idx, block, rbase, 64 * g, lane);
     else
       issue_half_copies((VAL ? c.cent_v16 : c.cent_k16) + (int64_t)h * C * D, C, idx, block, rbase, 64 * g, lane);
@@ -420,7 +434,7 @@ __device__ __forceinline__ void producer_pair(const AttnParams &p, unsigned char
     const AttnChunk &ch = p.ch[t0];
     tc::cp_async_wait<0>();
     __syncwarp();  // the warp's copies of tile j, made visible to every lane
-    if (RAW && ch.raw) convert_half(cur, block0 + (uint32_t)s * kStage, rr);
+    if (EXT && ch.raw) convert_half(cur, block0 + (uint32_t)s * kStage, rr);
     else decode_half<!WIDE>(cur, block0 + (uint32_t)s * kStage, rr, lut);
     if (!VAL && coef) write_x_row<WIDE>(cur, ch.rank, xs0 + (uint32_t)s * XL<WIDE>::kXBytes, rr);
     tc::fence_proxy_async_smem();
@@ -454,8 +468,8 @@ __device__ __forceinline__ void producer_pair(const AttnParams &p, unsigned char
 }
 
 // WIDE: PSAC ranks above 8 (32-column second-MMA operands).  IDX16: uint16 centroid indices.
-// RAW: the call includes a bf16 chunk (the chunk being generated).
-template <bool WIDE, bool IDX16, bool RAW>
+// EXT: the call includes a bf16 chunk (the chunk being generated) or compact INT2 metadata.
+template <bool WIDE, bool IDX16, bool EXT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     attend_pair_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -548,7 +562,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc::fence_after_sync();
       // block-causal mask of the chunk being generated: columns from `lim` on belong to a later frame
       int lim = BN;
-      if (RAW) {
+      if (EXT) {
         const AttnChunk &c = p.ch[tc_];
         if (c.tpf > 0) {
           const int64_t l = (qrow / c.tpf + 1) * c.tpf - (int64_t)ti_ * BN;
@@ -608,7 +622,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           m_used = m_new;
         }
-        const float mneg = (RAW && m_used == -INFINITY) ? 0.f : -m_used;  // a row with no unmasked key yet
+        const float mneg = (EXT && m_used == -INFINITY) ? 0.f : -m_used;  // a row with no unmasked key yet
         const uint64_t nm2 = pk64(__float_as_uint(mneg), __float_as_uint(mneg));
         uint32_t pw[16];
 #pragma unroll
@@ -722,10 +736,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!tc::mbar_wait(&bars.drain, 0, kWaitNs)) qwm_dev_error(p.status, QWM_ERR_DEVICE_TIMEOUT);
     }
   } else if (warp < kVWarp0) {
-    producer_pair<false, WIDE, IDX16, RAW>(p, sm, bars, &abort_flag, tc::smem_u32(code_lut), h, qb, cr,
+    producer_pair<false, WIDE, IDX16, EXT>(p, sm, bars, &abort_flag, tc::smem_u32(code_lut), h, qb, cr,
                                       tid - 32 * kKWarp0, lane);
   } else {
-    producer_pair<true, WIDE, IDX16, RAW>(p, sm, bars, &abort_flag, tc::smem_u32(code_lut), h, qb, cr,
+    producer_pair<true, WIDE, IDX16, EXT>(p, sm, bars, &abort_flag, tc::smem_u32(code_lut), h, qb, cr,
                                      tid - 32 * kVWarp0, lane);
   }
   tc::fence_before_sync();
@@ -737,21 +751,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool WIDE, bool IDX16, bool RAW>
+template <bool WIDE, bool IDX16, bool EXT>
 cudaError_t launch_pair(const AttnParams &p, dim3 grid, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(attend_pair_kernel<WIDE, IDX16, RAW>,
+  cudaError_t e = cudaFuncSetAttribute(attend_pair_kernel<WIDE, IDX16, EXT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, XL<WIDE>::kSmemAlloc);
   if (e != cudaSuccess) return e;
-  attend_pair_kernel<WIDE, IDX16, RAW><<<grid, kThreads, XL<WIDE>::kSmemAlloc, st>>>(p);
+  attend_pair_kernel<WIDE, IDX16, EXT><<<grid, kThreads, XL<WIDE>::kSmemAlloc, st>>>(p);
   return cudaGetLastError();
 }
 
-template <bool RAW>
-cudaError_t launch_pair_raw(const AttnParams &p, dim3 grid, bool wide, bool idx16, cudaStream_t st) {
-  if (wide && idx16) return launch_pair<true, true, RAW>(p, grid, st);
-  if (wide) return launch_pair<true, false, RAW>(p, grid, st);
-  if (idx16) return launch_pair<false, true, RAW>(p, grid, st);
-  return launch_pair<false, false, RAW>(p, grid, st);
+template <bool EXT>
+cudaError_t launch_pair_ext(const AttnParams &p, dim3 grid, bool wide, bool idx16, cudaStream_t st) {
+  if (wide && idx16) return launch_pair<true, true, EXT>(p, grid, st);
+  if (wide) return launch_pair<true, false, EXT>(p, grid, st);
+  if (idx16) return launch_pair<false, true, EXT>(p, grid, st);
+  return launch_pair<false, false, EXT>(p, grid, st);
 }
 
 }  // namespace
@@ -761,6 +775,7 @@ cudaError_t launch_attend(const qwm_config &cfg, const uint16_t *q, int64_t nq, 
   (void)num_sms;
   AttnParams p;  // passed by value (about 17 KB of kernel parameters)
   p.q = q; p.out = out; p.nq = nq; p.H = cfg.heads; p.C = cfg.n_centroids;
+  p.compact = cfg.storage == QWM_STORAGE_COMPACT;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = status;
   int used = 0, tiles = 0;
@@ -780,6 +795,8 @@ cudaError_t launch_attend(const qwm_config &cfg, const uint16_t *q, int64_t nq, 
     raw |= a.raw != 0;
     a.tpf = a.raw ? c.causal_tpf : 0;
     a.k_raw = c.k_raw; a.v_raw = c.v_raw;
+    a.k_s8 = c.k_s8; a.v_s8 = c.v_s8; a.k_zp = c.k_zp; a.v_zp = c.v_zp;
+    a.k_sigma = c.k_sigma; a.v_sigma = c.v_sigma;
     tiles += a.tiles;
     wide |= a.rank > 8;
   }
@@ -788,7 +805,8 @@ cudaError_t launch_attend(const qwm_config &cfg, const uint16_t *q, int64_t nq, 
   const bool idx16 = cfg.n_centroids > 256;
   cudaError_t e;
   const dim3 grid((unsigned)(2 * ((nq + kPairQ - 1) / kPairQ)), cfg.heads);  // CTA pairs
-  e = raw ? launch_pair_raw<true>(p, grid, wide, idx16, st) : launch_pair_raw<false>(p, grid, wide, idx16, st);
+  const bool ext = raw || p.compact;
+  e = ext ? launch_pair_ext<true>(p, grid, wide, idx16, st) : launch_pair_ext<false>(p, grid, wide, idx16, st);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

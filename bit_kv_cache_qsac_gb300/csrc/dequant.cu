@@ -9,7 +9,7 @@ namespace {
 
 constexpr int D = QWM_D;
 
-__global__ void dequant_kernel(qwm_chunk ch, int H, int C, int R, uint16_t *__restrict__ k_hat,
+__global__ void dequant_kernel(qwm_chunk ch, int H, int C, int R, int compact, uint16_t *__restrict__ k_hat,
                                uint16_t *__restrict__ v_hat) {
   const int64_t N = ch.n_tokens;
   const int64_t total = (int64_t)H * N * (D / 8);
@@ -27,7 +27,16 @@ __global__ void dequant_kernel(qwm_chunk ch, int H, int C, int R, uint16_t *__re
       const uint16_t *sc = pass ? ch.v_scale : ch.k_scale;
       const uint16_t *mn = pass ? ch.v_min : ch.k_min;
       const uint16_t *cent = pass ? ch.cent_v : ch.cent_k;
-      const float s = f16_to_f32(sc[row * G + g]), m = f16_to_f32(mn[row * G + g]);
+      float s, m;
+      if (compact) {  // s = sigma s8 (sigma a power of two), m = -z s: exact
+        const int64_t tiles = (N + 127) / 128;
+        const float sg = f16_to_f32((pass ? ch.v_sigma : ch.k_sigma)[((int64_t)h * tiles + (row - (int64_t)h * N) / 128) * G + g]);
+        s = sg * (float)(pass ? ch.v_s8 : ch.k_s8)[row * G + g];
+        m = -(float)(((pass ? ch.v_zp : ch.k_zp)[row] >> (2 * g)) & 3u) * s;
+      } else {
+        s = f16_to_f32(sc[row * G + g]);
+        m = f16_to_f32(mn[row * G + g]);
+      }
       const uint32_t b2 = *(const uint16_t *)(codes + row * (D / 4) + 2 * cb);  // 8 codes
       const int j = min(C > 256 ? (int)((const uint16_t *)idx)[row] : (int)((const uint8_t *)idx)[row],
                         C - 1);  // never read past the codebook
@@ -69,6 +78,7 @@ cudaError_t launch_dequantize(const qwm_config &cfg, const qwm_chunk &ch, uint16
   const int threads = 256;
   int64_t blocks = (total + threads - 1) / threads;
   if (blocks > 152 * 64) blocks = 152 * 64;
-  dequant_kernel<<<(int)blocks, threads, 0, st>>>(ch, cfg.heads, cfg.n_centroids, ch.rank_eff, k_hat, v_hat);
+  dequant_kernel<<<(int)blocks, threads, 0, st>>>(ch, cfg.heads, cfg.n_centroids, ch.rank_eff,
+                                                  cfg.storage == QWM_STORAGE_COMPACT ? 1 : 0, k_hat, v_hat);
   return cudaGetLastError();
 }

@@ -89,7 +89,12 @@ struct QParams {
   const float *img_max;      // WIDE: [H][2] max_j |b_j|, max_j |nw_j|
   uint8_t *codes;
   void *idx;                 // uint8 [H][n], or uint16 [H][n] (WIDE)
-  uint16_t *scale, *minv;
+  uint16_t *scale, *minv;    // fp16 storage: [H][n][2]
+  int compact, gate;         // compact metadata; PSAC keep-if-better
+  uint8_t *s8, *zp;          // compact: [H][n][2] steps, [H][n] zero-points (group g in bits 2g..2g+1)
+  uint16_t *sigma;           // compact: fp16 [H][ceil(n/128)][2] second-level scales
+  const float *wk;           // [H][D] channel weights of the gate (NULL: uniform)
+  float *dbg_gate;           // [H][n][2] w-weighted error without / with C, or NULL
   int8_t *c;
   uint16_t *c_scale;
   float *dbg_c;
@@ -110,6 +115,32 @@ __device__ __forceinline__ void bf16x8(const uint4 v, float (&f)[8]) {
 // byte offset of (row, column k) in a [rows][16] bf16 K-major operand without swizzle
 __host__ __device__ constexpr uint32_t noswz16(uint32_t row, uint32_t k) {
   return (row >> 3) * 256u + (k >> 3) * 128u + (row & 7u) * 16u + (k & 7u) * 2u;
+}
+
+// Compact metadata (the paper's packed form): the smallest step whose grid [-z s, (3 - z) s] covers
+// [a, b] over the four integer zero-points (lower z on ties), rounded up.
+__device__ __forceinline__ void zp_range(float a, float b, float &need, int &z) {
+  need = 0.f;
+  z = 0;
+  if (a == 0.f && b == 0.f) return;
+  float best = INFINITY;
+#pragma unroll
+  for (int zz = 0; zz < 4; zz++) {
+    const float lo = (a >= 0.f) ? 0.f : (zz > 0 ? __fdiv_ru(-a, (float)zz) : INFINITY);
+    const float hi = (b <= 0.f) ? 0.f : (zz < 3 ? __fdiv_ru(b, (float)(3 - zz)) : INFINITY);
+    const float sz = fmaxf(lo, hi);
+    if (sz < best) { best = sz; z = zz; }
+  }
+  need = best;
+}
+// The second-level scale: the smallest power of two sigma with 255 sigma >= smax (>= 2^-24).
+__device__ __forceinline__ float pow2_sigma(float smax) {
+  if (smax == 0.f) return 0.f;
+  const uint32_t t = __float_as_uint(__fdiv_ru(smax, 255.0f));
+  const uint32_t e = t >> 23, m = t & 0x7FFFFFu;
+  float sg = (m == 0u && e != 0u) ? __uint_as_float(t) : __uint_as_float((e + 1u) << 23);
+  if (e == 0u) sg = __uint_as_float(1u << 23);  // t subnormal: the smallest normal power of two
+  return fmaxf(sg, 5.9604644775390625e-08f);
 }
 
 // Byte offset, inside a [128][64] x 2 swizzled tile, of this lane's 4 channels (4 lane .. 4 lane + 3)
@@ -143,6 +174,8 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
   __shared__ float Wg[2], bmax_sh, nwmax_sh;
+  __shared__ float red_sg[2][2][4][2];  // compact: [group][tile parity][warp][channel group] step maxima
+  __shared__ uint64_t sg_bar[2];        // compact: the 4 warps of epilogue group e per tile
   const int C = p.C, M = KEY ? p.top_m : 1, R = KEY ? p.rank : 0;
   const int NW = C / 32;  // mask words per token
   const int NSL = WIDE ? C / kSlice : 1;
@@ -172,6 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
     }
     tc::mbar_init(&sl_full, 1);
     tc::mbar_init(&sl_empty, 1);
+    tc::mbar_init(&sg_bar[0], 4);
+    tc::mbar_init(&sg_bar[1], 4);
     tc::mbar_init(&drain, 1);
     abort_flag = 0;
     bmax_sh = WIDE ? p.img_max[2 * h] : 0.f;
@@ -595,10 +630,10 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
       }
       if (best >= C) best = 0;
       // ---- (4) INT2 codes of the chosen centroid's residual; PSAC coefficients (thread = token) ----
+      const int64_t grow = (int64_t)h * p.n + tok;
+      const uint16_t *mub = cent + (int64_t)best * D;
+      float mn0 = INFINITY, mx0 = -INFINITY, mn1 = INFINITY, mx1 = -INFINITY;
       if (valid) {
-        const int64_t grow = (int64_t)h * p.n + tok;
-        const uint16_t *mub = cent + (int64_t)best * D;
-        float mn0 = INFINITY, mx0 = -INFINITY, mn1 = INFINITY, mx1 = -INFINITY;
 #pragma unroll
         for (int ci = 0; ci < D / 8; ci++) {
           float f[8], mu[8];
@@ -611,10 +646,64 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
             else { mn1 = fminf(mn1, rr); mx1 = fmaxf(mx1, rr); }
           }
         }
-        float m0, s0, i0, m1, s1, i1;
-        uint16_t mb0, sb0, mb1, sb1;
+      }
+      // per group: r_hat = mm + ss q with q = clamp(rint(r ii + zz), 0, 3); fp16 storage: mm = offset,
+      // zz = 0; compact: mm = -z s (exact), zz = z
+      float m0, s0, i0, m1, s1, i1, z0f = 0.f, z1f = 0.f;
+      uint16_t mb0 = 0, sb0 = 0, mb1 = 0, sb1 = 0;
+      uint32_t s8w = 0, zbits = 0;
+      if (p.compact) {
+        float need0 = 0.f, need1 = 0.f;
+        int z0 = 0, z1 = 0;
+        if (valid) {
+          zp_range(mn0, mx0, need0, z0);
+          zp_range(mn1, mx1, need1, z1);
+        }
+        // the tile's largest step per group (the epilogue group's 4 warps meet on sg_bar[e])
+        float r0 = need0, r1 = need1;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          r0 = fmaxf(r0, __shfl_xor_sync(0xffffffffu, r0, o));
+          r1 = fmaxf(r1, __shfl_xor_sync(0xffffffffu, r1, o));
+        }
+        const int rb = (g >> 1) & 1;  // alternate buffers on alternate tiles of this group
+        if (lane == 0) {
+          red_sg[e][rb][sub][0] = r0;
+          red_sg[e][rb][sub][1] = r1;
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&sg_bar[e]);
+        const bool ok = tc::mbar_wait(&sg_bar[e], (g >> 1) & 1, kWaitNs);
+        if (__any_sync(0xffffffffu, !ok)) { *abort_v = 1; break; }
+        float smax0 = 0.f, smax1 = 0.f;
+#pragma unroll
+        for (int w4 = 0; w4 < 4; w4++) {
+          smax0 = fmaxf(smax0, red_sg[e][rb][w4][0]);
+          smax1 = fmaxf(smax1, red_sg[e][rb][w4][1]);
+        }
+        const float sg0 = pow2_sigma(smax0), sg1 = pow2_sigma(smax1);
+        if (sub == 0 && lane == 0)
+          *(uint32_t *)(p.sigma + ((int64_t)h * ((p.n + TILE - 1) / TILE) + tile0 + g) * 2) =
+              (uint32_t)__half_as_ushort(__float2half_rn(sg0)) | ((uint32_t)__half_as_ushort(__float2half_rn(sg1)) << 16);
+        // s8 = ceil(need / sigma): exact quotient (sigma is a power of two); s = sigma s8 exact
+        const float q0 = need0 == 0.f ? 0.f : ceilf(need0 * (1.0f / sg0));
+        const float q1 = need1 == 0.f ? 0.f : ceilf(need1 * (1.0f / sg1));
+        s0 = sg0 * q0;
+        s1 = sg1 * q1;
+        if (!(3.f * fmaxf(s0, s1) <= 65504.f)) qwm_dev_error(p.status, QWM_ERR_RANGE);  // z s must fit fp16
+        i0 = s0 > 0.f ? __frcp_rn(s0) : 0.f;
+        i1 = s1 > 0.f ? __frcp_rn(s1) : 0.f;
+        z0f = (float)z0;
+        z1f = (float)z1;
+        m0 = -z0f * s0;
+        m1 = -z1f * s1;
+        s8w = (uint32_t)q0 | ((uint32_t)q1 << 8);
+        zbits = (uint32_t)z0 | ((uint32_t)z1 << 2);
+      } else if (valid) {
         int2_params(mn0, mx0, m0, s0, i0, mb0, sb0, p.status);
         int2_params(mn1, mx1, m1, s1, i1, mb1, sb1, p.status);
+      }
+      if (valid) {
         uint32_t packed[8];
         float Cv[RMAX];
 #pragma unroll
@@ -625,11 +714,18 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
           bf16x8(tc::lds128(xts + (ci / 8) * TILE * 128 + tc::sw128_offset(row, 8 * (ci % 8))), f);
           bf16x8(*(const uint4 *)(mub + 8 * ci), mu);
           const bool g1 = ci >= 8;
-          const float mm = g1 ? m1 : m0, ss = g1 ? s1 : s0, ii = g1 ? i1 : i0;
+          const float mm = g1 ? m1 : m0, ss = g1 ? s1 : s0, ii = g1 ? i1 : i0, zz = g1 ? z1f : z0f;
           uint32_t bits = 0;
 #pragma unroll
           for (int u = 0; u < 8; u++) {
-            const uint32_t q = int2_code(__fsub_rn(f[u], mu[u]), mm, ss, ii);
+            const float rr = __fsub_rn(f[u], mu[u]);
+            uint32_t q;
+            if (p.compact) {
+              float qf = ss > 0.f ? rintf(__fadd_rn(__fmul_rn(rr, ii), zz)) : 0.f;
+              q = (uint32_t)fminf(fmaxf(qf, 0.f), 3.f);
+            } else {
+              q = int2_code(rr, mm, ss, ii);
+            }
             bits |= q << (2 * u);
             if (KEY && R > 0) {
               const float ev = __fsub_rn(f[u], __fadd_rn(mu[u], __fmaf_rn(ss, (float)q, mm)));
@@ -646,8 +742,13 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
         cdst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
         if (WIDE) ((uint16_t *)p.idx)[grow] = (uint16_t)best;
         else ((uint8_t *)p.idx)[grow] = (uint8_t)best;
-        *(uint32_t *)(p.scale + grow * 2) = (uint32_t)sb0 | ((uint32_t)sb1 << 16);
-        *(uint32_t *)(p.minv + grow * 2) = (uint32_t)mb0 | ((uint32_t)mb1 << 16);
+        if (p.compact) {
+          *(uint16_t *)(p.s8 + grow * 2) = (uint16_t)s8w;
+          p.zp[grow] = (uint8_t)zbits;
+        } else {
+          *(uint32_t *)(p.scale + grow * 2) = (uint32_t)sb0 | ((uint32_t)sb1 << 16);
+          *(uint32_t *)(p.minv + grow * 2) = (uint32_t)mb0 | ((uint32_t)mb1 << 16);
+        }
         if (KEY && p.dbg_score) p.dbg_score[grow] = best_S;
         if (KEY && R > 0) {
           float a = 0.f;
@@ -656,15 +757,53 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
             if (k < R) a = fmaxf(a, fabsf(Cv[k]));
           __half sch = __float2half_ru(__fdiv_ru(a, 127.0f));
           if (a == 0.f) sch = __float2half_rn(0.f);
-          const float sc = __half2float(sch);
+          float sc = __half2float(sch);
           if (!isfinite(sc)) qwm_dev_error(p.status, QWM_ERR_RANGE);
           const float inv = sc > 0.f ? __frcp_rn(sc) : 0.f;
+          int8_t c8[RMAX];
+#pragma unroll
+          for (int k = 0; k < RMAX; k++) {
+            float qf = (k < R && sc > 0.f) ? rintf(__fmul_rn(Cv[k], inv)) : 0.f;
+            c8[k] = (int8_t)fminf(fmaxf(qf, -127.f), 127.f);
+          }
+          if (p.gate || p.dbg_gate) {
+            // w-weighted error of the token without and with the decoded correction C_hat U_r^T
+            float e0 = 0.f, e1 = 0.f;
+#pragma unroll 2
+            for (int ci = 0; ci < D / 8; ci++) {
+              float f[8], mu[8];
+              bf16x8(tc::lds128(xts + (ci / 8) * TILE * 128 + tc::sw128_offset(row, 8 * (ci % 8))), f);
+              bf16x8(*(const uint4 *)(mub + 8 * ci), mu);
+              const bool g1 = ci >= 8;
+              const float mm = g1 ? m1 : m0, ss = g1 ? s1 : s0;
+              const uint32_t bits = packed[ci >> 1] >> (16 * (ci & 1));
+#pragma unroll
+              for (int u = 0; u < 8; u++) {
+                const int c = 8 * ci + u;
+                const float ev = __fsub_rn(f[u], __fadd_rn(mu[u], __fmaf_rn(ss, (float)((bits >> (2 * u)) & 3u), mm)));
+                float corr = 0.f;
+                const float *Uc = Us + c * 16;
+#pragma unroll
+                for (int k = 0; k < RMAX; k++) corr = fmaf(sc * (float)c8[k], Uc[k], corr);
+                const float wc = wv[c], d1 = ev - corr;
+                e0 = fmaf(wc, ev * ev, e0);
+                e1 = fmaf(wc, d1 * d1, e1);
+              }
+            }
+            if (p.dbg_gate) {
+              p.dbg_gate[grow * 2] = e0;
+              p.dbg_gate[grow * 2 + 1] = e1;
+            }
+            if (p.gate && !(e1 < e0)) {  // the correction does not help this token: drop it
+#pragma unroll
+              for (int k = 0; k < RMAX; k++) c8[k] = 0;
+              sch = __float2half_rn(0.f);
+            }
+          }
 #pragma unroll
           for (int k = 0; k < RMAX; k++) {
             if (k < R) {
-              float qf = sc > 0.f ? rintf(__fmul_rn(Cv[k], inv)) : 0.f;
-              qf = fminf(fmaxf(qf, -127.f), 127.f);
-              p.c[grow * R + k] = (int8_t)qf;
+              p.c[grow * R + k] = c8[k];
               if (p.dbg_c) p.dbg_c[grow * R + k] = Cv[k];
             }
           }
@@ -825,6 +964,12 @@ cudaError_t launch_quantize(const qwm_config &cfg, const uint16_t *k, const uint
     p.img = img; p.img_max = img_max;
     p.codes = key ? out.k_codes : out.v_codes; p.idx = key ? out.k_idx : out.v_idx;
     p.scale = key ? out.k_scale : out.v_scale; p.minv = key ? out.k_min : out.v_min;
+    p.compact = cfg.storage == QWM_STORAGE_COMPACT;
+    p.gate = (key && cfg.psac_gate) ? 1 : 0;
+    p.s8 = key ? out.k_s8 : out.v_s8; p.zp = key ? out.k_zp : out.v_zp;
+    p.sigma = key ? out.k_sigma : out.v_sigma;
+    p.wk = key ? w : nullptr;
+    p.dbg_gate = (key && dbg) ? dbg->gate_err : nullptr;
     p.c = out.c; p.c_scale = out.c_scale;
     p.dbg_c = (key && dbg) ? dbg->c_f32 : nullptr;
     p.dbg_cand = (key && dbg) ? dbg->cand : nullptr;

@@ -75,7 +75,22 @@ typedef struct {
   int32_t bits;         /* residual bits; must be 2 */
   int32_t kmeans_iters; /* Lloyd iterations per qwm_fit_centroids call, 1..100 */
   uint64_t seed;        /* reserved (no randomness on the path); pass 0 */
+  int32_t storage;      /* qwm_storage: how a chunk's INT2 metadata is stored */
+  int32_t psac_gate;    /* 1: keep a token's C only where it lowers sum_c w_c e_c^2 (Chinese summary
+                           step (4): "仅当降低Query加权误差时保留"); 0: always keep */
 } qwm_config;
+
+/* INT2 metadata layouts.
+ *  QWM_STORAGE_FP16: per (token, group of 64) an fp16 offset m (round-down of the minimum) and an
+ *    fp16 step s (round-up of the range / 3): r_hat = m + s q.
+ *  QWM_STORAGE_COMPACT: the paper's packed form (Chinese summary step (3) "组缩放INT8+FP16二级缩放";
+ *    English v2 §D.1 "bit-packed INT2 zero-points"): per (token, group) an 8-bit step s8 and a 2-bit
+ *    zero-point z, per (128-token tile, group) an fp16 second-level scale sigma, a power of two:
+ *    s = sigma s8, r_hat = s (q - z) (exact in fp16).  Each (token, group) takes the zero-point whose
+ *    grid [-z s, (3 - z) s] covers its residual range with the smallest step (lower z on ties); sigma
+ *    is the smallest power of two with 255 sigma >= the tile's largest such step; s8 = ceil(step /
+ *    sigma); q = clamp(rint(r (1/s) + z), 0, 3).  |r - r_hat| <= s/2. */
+typedef enum { QWM_STORAGE_FP16 = 0, QWM_STORAGE_COMPACT = 1 } qwm_storage;
 
 typedef struct qwm_ctx qwm_ctx;
 
@@ -116,6 +131,13 @@ typedef struct {
   int64_t causal_tpf;    /* > 0: block-causal mask over frames of causal_tpf tokens: Query row i (the
                             i-th row of qwm_attend's q, taken as token i of this chunk) sees key j of
                             this chunk only when j / causal_tpf <= i / causal_tpf; 0: no mask */
+  /* QWM_STORAGE_COMPACT contexts only (k_scale, k_min, v_scale, v_min are then unused): */
+  uint8_t *k_s8;         /* [H][N][G] 8-bit steps */
+  uint8_t *v_s8;         /* [H][N][G] */
+  uint8_t *k_zp;         /* [H][N] zero-points: group g in bits 2g..2g+1 */
+  uint8_t *v_zp;         /* [H][N] */
+  uint16_t *k_sigma;     /* fp16 [H][ceil(N/128)][G] second-level scales */
+  uint16_t *v_sigma;     /* fp16 [H][ceil(N/128)][G] */
 } qwm_chunk;
 
 /* Optional stage outputs of qwm_quantize_kv for parity checks (NULL members are skipped). */
@@ -123,6 +145,7 @@ typedef struct {
   float *c_f32;          /* [H][N][r] PSAC coefficients before INT8 */
   int32_t *cand;         /* [H][N][M] QSAC candidates (any order) */
   float *score;          /* [H][N] QSAC score S of the chosen Key centroid */
+  float *gate_err;       /* [H][N][2] sum_c w_c e_c^2 without and with the decoded PSAC correction */
 } qwm_debug;
 
 QWM_API const char *qwm_status_string(qwm_status s);

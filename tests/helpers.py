@@ -14,14 +14,34 @@ def from_u16(a: np.ndarray, dtype, device="cuda"):
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint16).view(np.int16)).to(device).view(dtype)
 
 
+def compact_as_fp16(s8, zp, sigma, n: int):
+    """Compact INT2 metadata of one head (steps s8 [n][G], zero-points zp [n], second-level scales
+    sigma fp16 bits [tiles][G]) re-expressed exactly as fp16 step and offset bits: s = sigma s8 and
+    m = -z s are fp16 values (sigma is a power of two), and m + s q = s (q - z)."""
+    G = s8.shape[1]
+    sig = np.asarray(sigma, np.uint16).view(np.float16).astype(np.float64)[np.arange(n) // 128]
+    z = np.stack([(zp >> (2 * g)) & 3 for g in range(G)], 1).astype(np.float64)
+    s = sig * s8.astype(np.float64)
+    m = -z * s
+    assert np.all(s.astype(np.float16).astype(np.float64) == s) and np.all(m.astype(np.float16).astype(np.float64) == m)
+    return s.astype(np.float16).view(np.uint16), m.astype(np.float16).view(np.uint16)
+
+
 def chunk_head(chunk, h: int) -> dict:
-    """Per-head numpy view of a packed chunk, in the oracle's chunk dict format."""
+    """Per-head numpy view of a packed chunk, in the oracle's chunk dict format (compact metadata
+    re-expressed exactly as fp16 step and offset)."""
     r = chunk.rank_eff
+    n = chunk.n_tokens
+    if getattr(chunk, "compact", False):
+        ks, km = compact_as_fp16(chunk.k_s8[h].cpu().numpy(), chunk.k_zp[h].cpu().numpy()[:n], to_u16(chunk.k_sigma[h]), n)
+        vs, vm = compact_as_fp16(chunk.v_s8[h].cpu().numpy(), chunk.v_zp[h].cpu().numpy()[:n], to_u16(chunk.v_sigma[h]), n)
+    else:
+        ks, km = to_u16(chunk.k_scale[h]), to_u16(chunk.k_min[h])
+        vs, vm = to_u16(chunk.v_scale[h]), to_u16(chunk.v_min[h])
     d = dict(
         idx_k=chunk.k_idx[h].cpu().numpy().astype(np.int32), idx_v=chunk.v_idx[h].cpu().numpy().astype(np.int32),
         k_codes=chunk.k_codes[h].cpu().numpy(), v_codes=chunk.v_codes[h].cpu().numpy(),
-        k_scale=to_u16(chunk.k_scale[h]), k_min=to_u16(chunk.k_min[h]),
-        v_scale=to_u16(chunk.v_scale[h]), v_min=to_u16(chunk.v_min[h]),
+        k_scale=ks, k_min=km, v_scale=vs, v_min=vm,
         cent_k=to_u16(chunk.cent_k[h]), cent_v=to_u16(chunk.cent_v[h]), rank=r,
     )
     if r:

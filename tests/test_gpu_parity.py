@@ -126,10 +126,10 @@ def test_kmeans_objective_1024_centroids(q):
         assert abs(j_gpu - j_ref) <= 1e-3 * j_ref, (h, j_gpu, j_ref)
 
 
-def _upstream(q, w_, H, n, C=256, top_m=4, rank=8, psac=True):
+def _upstream(q, w_, H, n, C=256, top_m=4, rank=8, psac=True, storage=0, gate=0):
     """GPU statistics and codebooks for a small case; returns numpy and device pieces."""
     k = synth.keys(w_)[:H, :n]; v = synth.values(w_)[:H, :n]
-    ctx = q.Context(heads=H, n_centroids=C, top_m=top_m, rank=rank)
+    ctx = q.Context(heads=H, n_centroids=C, top_m=top_m, rank=rank, storage=storage, psac_gate=gate)
     layer_S = torch.zeros(H, D, D, device="cuda"); n_ = torch.zeros(H, dtype=torch.int64, device="cuda")
     w = torch.empty(H, D, device="cuda"); lam = torch.empty(H, D, device="cuda")
     ur = torch.zeros(H, D, max(rank, 1), dtype=torch.bfloat16, device="cuda")
@@ -249,6 +249,68 @@ def test_quantize_duplicated_codebook(q, C):
         assert np.all((gk == o["idx_k"]) | k_free), (h, int(((gk != o["idx_k"]) & ~k_free).sum()))
         assert np.all((gv == o["idx_v"]) | v_free), (h, int(((gv != o["idx_v"]) & ~v_free).sum()))
         assert np.all(gk % 8 < M) and np.all(gv % 8 == 0)  # the lowest copies win
+
+
+@pytest.mark.parametrize("gate,n", [(0, 1000), (1, 1000), (1, 300)])
+def test_quantize_compact_storage_and_psac_gate(q, gate, n):
+    """The paper's compact metadata (8-bit step, 2-bit zero-point, power-of-two second-level scale per
+    128-token tile) bit-exact given the indices; with the gate, C dropped exactly where it does not lower
+    the w-weighted error (decisions within a relative 1e-3 of a tie may go either way)."""
+    H, M, R = 2, 4, 8
+    ctx, k, v, K, V, ch, w, ur = _upstream(q, synth.TINY, H, n, storage=1, gate=gate)
+    assert ch.compact
+    dbg = dict(c_f32=torch.zeros(H, n, R, device="cuda"), cand=torch.zeros(H, n, M, dtype=torch.int32, device="cuda"),
+               score=torch.zeros(H, n, device="cuda"), gate_err=torch.zeros(H, n, 2, device="cuda"))
+    q.qwm_quantize_kv(ctx, K, V, n, w, ur, ch, dbg)
+    assert q.qwm_sync_status(ctx) == 0
+    for h in range(H):
+        wh = w[h].cpu().numpy().astype(np.float64)
+        urh = to_u16(ur[h])[:, :R]
+        gk = ch.k_idx[h].cpu().numpy().astype(np.int32); gv = ch.v_idx[h].cpu().numpy().astype(np.int32)
+        o = oracle.quantize_head(k[h], v[h], to_u16(ch.cent_k[h]), to_u16(ch.cent_v[h]), wh, urh, top_m=M, rank=R,
+                                 storage=1, psac_gate=gate, force_idx_k=gk, force_idx_v=gv)
+        for name in ("k_codes", "v_codes", "k_s8", "v_s8"):
+            assert np.array_equal(getattr(ch, name)[h].cpu().numpy(), o[name]), name
+        for name in ("k_zp", "v_zp"):
+            assert np.array_equal(getattr(ch, name)[h].cpu().numpy()[:n], o[name]), name
+        for name in ("k_sigma", "v_sigma"):
+            assert np.array_equal(to_u16(getattr(ch, name)[h]), o[name]), name
+        cg = dbg["c_f32"][h].cpu().numpy().astype(np.float64)
+        cr = o["c_real"]
+        assert np.all(np.abs(cg - cr) <= 1e-3 * np.maximum(np.abs(cr).max(1, keepdims=True), 1e-30))
+        gc8, gsc = ch.c[h].cpu().numpy()[:, :R], to_u16(ch.c_scale[h])
+        e0, e1 = o["gate_err"][:, 0], o["gate_err"][:, 1]
+        near = np.abs(e1 - e0) <= 1e-3 * np.maximum(e0, 1e-30)
+        for i in range(n):
+            c8, sc = oracle.int8_encode_token(cg[i].astype(np.float32))
+            kept = gsc[i] == sc and np.array_equal(gc8[i], c8)
+            dropped = gsc[i] == 0 and not gc8[i].any()
+            assert kept or (gate and dropped), i
+            if gate and not near[i] and sc != 0:
+                assert kept == bool(e1[i] < e0[i]), (i, e0[i], e1[i])
+
+
+@pytest.mark.parametrize("C", [256, 1024])
+def test_attend_and_decode_compact_chunk(q, C):
+    H, n = 2, (1000 if C == 256 else 2600)
+    ctx, k, v, K, V, ch, w, ur = _upstream(q, WIDE_W if C > 256 else synth.TINY, H, n, C=C, storage=1, gate=1)
+    q.qwm_quantize_kv(ctx, K, V, n, w, ur, ch)
+    nq = 300
+    qa = synth.queries(synth.TINY, 5, nq)
+    out = torch.empty(H, nq, D, dtype=torch.float32, device="cuda")
+    q.qwm_attend(ctx, _bf(qa), nq, [ch], 1 / math.sqrt(D), out)
+    kh = torch.empty(H, n, D, dtype=torch.bfloat16, device="cuda"); vh = torch.empty_like(kh)
+    q.qwm_dequantize(ctx, ch, kh, vh)
+    assert q.qwm_sync_status(ctx) == 0
+    for h in range(H):
+        c = chunk_head(ch, h)
+        ref = oracle.attend_rows(qa[h], np.arange(nq), [c], 1 / math.sqrt(D))
+        assert _attn_err(out[h].cpu().numpy().astype(np.float64), ref) <= 2e-2
+        _, _, k64, v64 = oracle.dequantize_head(c)
+        for got, ref64, key in ((kh[h], k64, True), (vh[h], v64, False)):
+            g = (to_u16(got).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+            slack = 2.0 ** -20 * decode_term_magnitude(c, key)
+            assert (bf16_ulp_close(to_u16(got), ref64) | (np.abs(g - ref64) <= slack)).all()
 
 
 # ------------------------------------------------------------------ step 5', step 5
