@@ -472,7 +472,7 @@ def _dev_bf16(a, device):
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
 
 
-def run_ablation(device, sweep: bool = True):
+def run_ablation(device, parts=("sweep", "storage", "baselines")):
     """Config-4 sweep on the 480p-shaped layer (40 heads, 8 chunks of 4,680 tokens): QSAC candidates
     M in {1, 4, 16}, PSAC rank r in {0, 8, 16}, codebook size C in {64, 256, 1024} (1024: uint16
     indices, codebook streamed through shared memory in slices).  Per configuration: packing time of the last
@@ -499,7 +499,7 @@ def run_ablation(device, sweep: bool = True):
     del Kall
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     pairs = Hh * Wa.nq_attend * Wa.n_tokens
-    for C in ((64, 256, 1024) if sweep else ()):
+    for C in ((64, 256, 1024) if "sweep" in parts else ()):
         for M in (1, 4, 16):
             for r in (0, 8, 16):
                 ctx = q.Context(heads=Hh, n_centroids=C, top_m=M, rank=r, kmeans_iters=10)
@@ -533,7 +533,42 @@ def run_ablation(device, sweep: bool = True):
                                   "compression": 2 * Hh * Wa.n_tokens * Dd * 2 / layer.nbytes()}), flush=True)
                 del layer, ctx, khat, L, out
                 torch.cuda.empty_cache()
-    run_ablation_baselines(device, K, V, Q, Qs, Lref, top_ref, ms2_ref)
+    # the paper's packed form: compact INT2 metadata and the PSAC keep-if-better gate (256, M = 4, r = 8)
+    for C in ((256,) if "storage" in parts else ()):
+        for storage, gate in ((0, 1), (1, 0), (1, 1)):
+            ctx = q.Context(heads=Hh, n_centroids=C, top_m=4, rank=8, kmeans_iters=10, storage=storage,
+                            psac_gate=gate)
+            layer = CompressedLayer(ctx, device)
+            for t in range(T):
+                if t > 0:
+                    layer.fold_queries(Q[t - 1])
+                if t == T - 1:
+                    ev[0].record()
+                layer.append_chunk(K[t], V[t])
+                if t == T - 1:
+                    ev[1].record()
+            out = layer.attend(Q[-1])
+            ev[2].record()
+            out = layer.attend(Q[-1], out)
+            ev[3].record()
+            torch.cuda.synchronize()
+            assert layer.check() == 0
+            khat = torch.cat([layer.dequantize(i)[0] for i in range(T)], dim=1).float()
+            L = torch.einsum("hqd,hkd->hqk", Qs, khat) * scale
+            mse = float(((L - Lref) ** 2).mean())
+            kept = float(sum((c.c_scale != 0).float().mean() for c in layer.chunks[1:]) / (T - 1))
+            print(json.dumps({"report": "ablation", "workload": "480p-shaped layer, step 8 of 8",
+                              "n_centroids": C, "top_m": 4, "rank": 8,
+                              "storage": "compact (8-bit step, 2-bit zero-point)" if storage else "fp16 step/offset",
+                              "psac_gate": gate, "psac_kept_fraction": kept,
+                              "pack_ms": ev[0].elapsed_time(ev[1]), "attend_ms": ev[2].elapsed_time(ev[3]),
+                              "logit_mse": mse, "logit_mse_rel": mse / ms2_ref,
+                              "top1_shift": float((L.argmax(-1) != top_ref).float().mean()),
+                              "compression": 2 * Hh * Wa.n_tokens * Dd * 2 / layer.nbytes()}), flush=True)
+            del layer, ctx, khat, L, out
+            torch.cuda.empty_cache()
+    if "baselines" in parts:
+        run_ablation_baselines(device, K, V, Q, Qs, Lref, top_ref, ms2_ref)
 
 
 def run_ablation_baselines(device, K, V, Q, Qs, Lref, top_ref, ms2_ref):
@@ -641,7 +676,7 @@ def run_ablation_baselines(device, K, V, Q, Qs, Lref, top_ref, ms2_ref):
     report("KIVI-style INT2 (groups of 32, 2-frame bf16 window)", pack_ms, kk, vk, kivi_decode, kivi_bytes)
 
 
-def run_full_model(device):
+def run_full_model(device, storage: int = 0):
     """Config 3: 40 layers of the 480p-shaped workload streamed chunk by chunk (8 steps per layer:
     fold the previous chunk's Queries, fit and pack the chunk, attend with the chunk's Queries over
     every packed chunk).  Every layer's compressed cache stays resident; reports the compressed
@@ -652,7 +687,8 @@ def run_full_model(device):
     from bit_kv_cache_qsac_gb300.stream import CompressedLayer
     Wf, n_layers = synth.P480, 40
     Hh, Dd, T = Wf.heads, Wf.head_dim, Wf.n_chunks
-    ctx = q.Context(heads=Hh, n_centroids=Wf.n_centroids, top_m=Wf.top_m, rank=Wf.rank, kmeans_iters=10)
+    ctx = q.Context(heads=Hh, n_centroids=Wf.n_centroids, top_m=Wf.top_m, rank=Wf.rank, kmeans_iters=10,
+                    storage=storage, psac_gate=storage)
     from torch.nn.attention import SDPBackend, sdpa_kernel
     backends = [SDPBackend.CUDNN_ATTENTION, SDPBackend.FLASH_ATTENTION, SDPBackend.EFFICIENT_ATTENTION]
     stats_ms, pack_ms, att_ms, sdpa_ms = np.zeros(T), np.zeros(T), np.zeros(T), np.zeros(T)
@@ -698,6 +734,7 @@ def run_full_model(device):
     packed_ops = sum(sum(c.nbytes(operand_copies=True) for c in l.chunks) for l in layers)
     bf16 = 2 * n_layers * Hh * Wf.n_tokens * Dd * 2
     print(json.dumps({"report": "full_model", "workload": f"{n_layers} layers of the 480p-shaped layer",
+                      "storage": "compact INT2 metadata + PSAC gate" if storage else "fp16 INT2 metadata",
                       "bf16_bytes": bf16, "packed_bytes": packed, "packed_gib": packed / 2 ** 30,
                       "ratio": bf16 / packed, "ratio_with_fp16_codebook_copies": bf16 / packed_ops,
                       "per_step_ms_all_layers": {"stats_eig": stats_ms.tolist(), "fit_and_pack": pack_ms.tolist(),
@@ -745,7 +782,10 @@ def main():
                     help="skip the dequantize+SDPA and bf16 SDPA context timings")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="720p",
                     help="720p-shaped layer (default) or 480p-shaped layer")
-    ap.add_argument("--report", choices=["ablation", "baselines", "full-model"], default=None,
+    ap.add_argument("--storage", choices=["fp16", "compact"], default="fp16",
+                    help="INT2 metadata of the packed chunks in --report full-model: fp16 step/offset or the "
+                         "paper's compact form (8-bit step, 2-bit zero-point) with the PSAC keep-if-better gate")
+    ap.add_argument("--report", choices=["ablation", "storage", "baselines", "full-model"], default=None,
                     help="instead of the benchmark line: the M x r x C sweep and the QVG / KIVI baselines "
                          "(config 4), the baselines alone, or the 40-layer 480p-shaped model (config 3)")
     args = ap.parse_args()
@@ -754,9 +794,9 @@ def main():
         device = torch.device("cuda", 0)
         torch.cuda.set_device(device)
         if args.report == "full-model":
-            run_full_model(device)
+            run_full_model(device, 1 if args.storage == "compact" else 0)
         else:
-            run_ablation(device, sweep=args.report == "ablation")
+            run_ablation(device, ("sweep", "storage", "baselines") if args.report == "ablation" else (args.report,))
         return
     select_workload(args.workload)
     rank = int(os.environ.get("RANK", 0))

@@ -123,6 +123,7 @@ struct AttnParams {
   int64_t nq;
   int H, C, n_chunks, total_tiles;
   int compact;       // the chunks' INT2 metadata is the compact form (8-bit step, 2-bit zero-point)
+  int any_causal;    // a bf16 chunk with a block-causal mask
   float scale_log2;  // softmax_scale * log2(e)
   int32_t *status;
   AttnChunk ch[kMaxChunks];
@@ -562,7 +563,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc::fence_after_sync();
       // block-causal mask of the chunk being generated: columns from `lim` on belong to a later frame
       int lim = BN;
-      if (EXT) {
+      if (EXT && p.any_causal) {
         const AttnChunk &c = p.ch[tc_];
         if (c.tpf > 0) {
           const int64_t l = (qrow / c.tpf + 1) * c.tpf - (int64_t)ti_ * BN;
@@ -776,6 +777,7 @@ cudaError_t launch_attend(const qwm_config &cfg, const uint16_t *q, int64_t nq, 
   AttnParams p;  // passed by value (about 17 KB of kernel parameters)
   p.q = q; p.out = out; p.nq = nq; p.H = cfg.heads; p.C = cfg.n_centroids;
   p.compact = cfg.storage == QWM_STORAGE_COMPACT;
+  p.any_causal = 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = status;
   int used = 0, tiles = 0;
@@ -794,6 +796,7 @@ cudaError_t launch_attend(const qwm_config &cfg, const uint16_t *q, int64_t nq, 
     a.raw = c.kind == QWM_CHUNK_BF16;
     raw |= a.raw != 0;
     a.tpf = a.raw ? c.causal_tpf : 0;
+    if (a.tpf > 0) p.any_causal = 1;
     a.k_raw = c.k_raw; a.v_raw = c.v_raw;
     a.k_s8 = c.k_s8; a.v_s8 = c.v_s8; a.k_zp = c.k_zp; a.v_zp = c.v_zp;
     a.k_sigma = c.k_sigma; a.v_sigma = c.v_sigma;
