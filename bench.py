@@ -171,8 +171,8 @@ def gen_layer(layer: int):
 # DRAM bytes per launch of the attention kernel (dram__bytes_read.sum + dram__bytes_write.sum from
 # one ncu capture, profiles/attend_pair_kernel_*.md), valid only for the kernel source they were taken
 # on: the SHA-256 of csrc/attend.cu is checked, and the traffic reported as null otherwise.
-ATTEND_TRAFFIC = {"sha256": "a622608c7d9999142c4102acea976d8f31072dbe779fe1194a829b49ac7bdead",
-                  "720p": 476810496 + 190960640, "480p": 229728512 + 66204160}
+ATTEND_TRAFFIC = {"sha256": "8714211d69d6fd2150ca315f007c9e44c7e2a5891e2bcc9ecca3cdde1df209e0",
+                  "720p": 480708096 + 191165440, "480p": 229535488 + 67040768}
 
 
 def attend_traffic(workload: str):
