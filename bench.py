@@ -448,7 +448,7 @@ def oracle_sample(seconds_hint: float = 15.0):
     t0 = time.perf_counter()
     oracle.quantize_head(k, v, ck, cv, w[0], urb[0], top_m=W.top_m)
     t_quant = time.perf_counter() - t0
-    rows = 16
+    rows = 384  # about 10 s of oracle attention on 16 cores (one row costs ~0.4 s of one core)
     t0 = time.perf_counter()
     oracle.attend_rows(qa, np.arange(rows), chunks, 1.0 / math.sqrt(D))
     t_att = time.perf_counter() - t0
