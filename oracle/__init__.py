@@ -51,7 +51,7 @@ I32 = C.c_int32
 
 class QuantArgs(C.Structure):
     _fields_ = [
-        ("k", P), ("v", P), ("cent_k", P), ("cent_v", P), ("w", P), ("u_r", P), ("u_r_f64", P),
+        ("k", P), ("v", P), ("cent_k", P), ("cent_v", P), ("w", P), ("M_full", P), ("u_r", P), ("u_r_f64", P),
         ("force_idx_k", P), ("force_idx_v", P),
         ("n", I64), ("d", I32), ("C", I32), ("group", I32), ("top_m", I32), ("rank", I32),
         ("storage", I32), ("psac_gate", I32),
@@ -225,13 +225,15 @@ def int8_encode_token(Cf: np.ndarray):
 
 
 def quantize_head(k, v, cent_k, cent_v, w=None, u_r=None, *, group=64, top_m=4, rank=None,
-                  u_r_f64=None, force_idx_k=None, force_idx_v=None, storage=0, psac_gate=0):
+                  u_r_f64=None, force_idx_k=None, force_idx_v=None, storage=0, psac_gate=0, M_full=None):
     """QSAC Key assignment, nearest-centroid Value assignment, INT2 residuals and PSAC for one head.
 
     k, v: uint16 [n][d]; cent_k, cent_v: uint16 [C][d]; w: float [d] or None (uniform);
     u_r: uint16 [d][r] or None (PSAC off).  storage 0: fp16 step and offset per (token, group);
     storage 1: the compact metadata (8-bit step, 2-bit zero-point, power-of-two second-level scale
-    per 128-token tile).  psac_gate: keep C only where it lowers the w-weighted error.
+    per 128-token tile).  psac_gate: keep C only where it lowers the w-weighted error.  M_full
+    ([d][d], with w = diag(M_full)): rank the top-M candidates by the full quadratic form (English v2
+    summary §C.4 ablation).
     Returns a dict of every output and diagnostic."""
     k = _c(k, np.uint16); v = _c(v, np.uint16)
     cent_k = _c(cent_k, np.uint16); cent_v = _c(cent_v, np.uint16)
@@ -241,6 +243,7 @@ def quantize_head(k, v, cent_k, cent_v, w=None, u_r=None, *, group=64, top_m=4, 
         rank = 0 if (u_r is None and u_r_f64 is None) else (u_r if u_r is not None else u_r_f64).shape[1]
     G = d // group
     w64 = None if w is None else _c(w, np.float64)
+    mf = None if M_full is None else _c(M_full, np.float64)
     ur = None if u_r is None else _c(u_r, np.uint16)
     ur64 = None if u_r_f64 is None else _c(u_r_f64, np.float64)
     fk = None if force_idx_k is None else _c(force_idx_k, np.int32)
@@ -259,7 +262,7 @@ def quantize_head(k, v, cent_k, cent_v, w=None, u_r=None, *, group=64, top_m=4, 
         k_sigma=np.zeros(((n + 127) // 128, G), np.uint16), v_sigma=np.zeros(((n + 127) // 128, G), np.uint16),
         gate_err=np.zeros((n, 2)),
     )
-    a = QuantArgs(k=_p(k), v=_p(v), cent_k=_p(cent_k), cent_v=_p(cent_v), w=_p(w64), u_r=_p(ur),
+    a = QuantArgs(k=_p(k), v=_p(v), cent_k=_p(cent_k), cent_v=_p(cent_v), w=_p(w64), M_full=_p(mf), u_r=_p(ur),
                   u_r_f64=_p(ur64), force_idx_k=_p(fk), force_idx_v=_p(fv), n=n, d=d, C=Cn,
                   group=group, top_m=top_m, rank=rank, storage=storage, psac_gate=psac_gate,
                   **{key: _p(val) for key, val in o.items()})

@@ -407,6 +407,18 @@ static double dq_dist(const uint16_t *k, const uint16_t *mu, const double *w, in
   return s;
 }
 
+/* The full quadratic form of the Query-aware distance ([QWM-en] §C.4 ablation): (k - mu)^T M (k - mu). */
+static double dq_dist_full(const uint16_t *k, const uint16_t *mu, const double *M, int d, double *e) {
+  for (int c = 0; c < d; c++) e[c] = bf16_val(k[c]) - bf16_val(mu[c]);
+  double s = 0.0;
+  for (int c = 0; c < d; c++) {
+    double t = 0.0;
+    for (int c2 = 0; c2 < d; c2++) t += M[c * d + c2] * e[c2];
+    s += e[c] * t;
+  }
+  return s;
+}
+
 /* QSAC score S(k, mu) = sum_g (sum_{c in G_g} w_c) R_g(k - mu)^2 with R_g = max - min of the
  * residual over the group (INT2 error estimate R_g^2 / [12 (2^b - 1)^2] with the constant dropped). */
 static double qsac_score(const uint16_t *k, const uint16_t *mu, const double *w, int d, int group) {
@@ -476,6 +488,8 @@ typedef struct {
   const uint16_t *k, *v;          /* [n][d] bf16 */
   const uint16_t *cent_k, *cent_v;/* [C][d] bf16 */
   const double *w;                /* [d] or NULL (uniform) */
+  const double *M_full;           /* [d][d] or NULL: rank the top-M candidates by (k - mu)^T M (k - mu)
+                                     ([QWM-en] §C.4); w must then be diag(M) (the range score keeps w) */
   const uint16_t *u_r;            /* [d][rank] bf16 or NULL (PSAC off) */
   const double *u_r_f64;          /* optional [d][rank] double basis used instead of u_r (exactness checks) */
   const int32_t *force_idx_k;     /* [n] or NULL: use these Key centroids instead of QSAC */
@@ -552,12 +566,15 @@ void oracle_quantize_head(const oracle_quant_args *a) {
     uint8_t *codes = (uint8_t *)malloc(d);
     float *khat0 = (float *)malloc(sizeof(float) * d);
     float *Cf = (float *)malloc(sizeof(float) * (r > 0 ? r : 1));
+    double *khat0_e = (double *)malloc(sizeof(double) * d); /* scratch of the full-form distance */
 #pragma omp for schedule(static)
     for (int64_t i = 0; i < a->n; i++) {
       const uint16_t *k = a->k + i * d, *v = a->v + i * d;
       int jk;
       /* ---- step 2: QSAC Key centroid ---- */
-      for (int j = 0; j < C; j++) dq[j] = dq_dist(k, a->cent_k + (int64_t)j * d, w, d);
+      for (int j = 0; j < C; j++)
+        dq[j] = a->M_full ? dq_dist_full(k, a->cent_k + (int64_t)j * d, a->M_full, d, (double *)khat0_e)
+                          : dq_dist(k, a->cent_k + (int64_t)j * d, w, d);
       int nsel = (M + 1 <= C) ? M + 1 : C;
       for (int t = 0; t < nsel; t++) { /* t-th smallest d_Q, ties to the lower index */
         int best = -1;
@@ -679,6 +696,7 @@ void oracle_quantize_head(const oracle_quant_args *a) {
     free(codes);
     free(khat0);
     free(Cf);
+    free(khat0_e);
   }
   free(w);
   free(s_need);

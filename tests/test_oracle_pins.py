@@ -633,3 +633,31 @@ def test_psac_gate_keeps_only_improving_coefficients():
     assert np.all(gated["c"][drop] == 0) and np.all(gated["c_scale"][drop] == 0)
     assert np.array_equal(gated["c"][~drop], base["c"][~drop])
     assert np.array_equal(gated["c_scale"][~drop], base["c_scale"][~drop])
+
+
+# ---------------------------------------------------------------- full quadratic-form ranking (§C.4 ablation)
+
+
+def test_full_form_ranking_reduces_to_diagonal_and_matches_brute_force():
+    """English v2 §C.4: the ablation ranks candidates by (k - mu)^T M (k - mu).  With M diagonal it is
+    the diagonal QSAC exactly; with a general PSD M the candidates are the M smallest quadratic forms
+    (brute force with numpy), and the choice among them is still the range score with w = diag(M)."""
+    k, v, qs, _ = synth.small_case(1, 120, 128, 64, 200, seed=71)
+    k, v = k[0], v[0]
+    ck, _, _, _ = oracle.kmeans(k, 64, None, 3)
+    cv, _, _, _ = oracle.kmeans(v, 64, None, 3)
+    w = np.linspace(0.5, 2.0, 128)
+    diag = oracle.quantize_head(k, v, ck, cv, w, None, top_m=4, rank=0)
+    full_diag = oracle.quantize_head(k, v, ck, cv, w, None, top_m=4, rank=0, M_full=np.diag(w))
+    assert np.array_equal(diag["idx_k"], full_diag["idx_k"])
+    assert np.array_equal(np.sort(diag["cand"], 1), np.sort(full_diag["cand"], 1))
+    q = _bf(qs[0])
+    M = q.T @ q / q.shape[0]
+    o = oracle.quantize_head(k, v, ck, cv, np.diag(M).copy(), None, top_m=4, rank=0, M_full=M)
+    E = _bf(k)[:, None, :] - _bf(ck)[None, :, :]
+    dq = np.einsum("ijc,cd,ijd->ij", E, M, E)
+    srt = np.sort(dq, 1)
+    clear = (srt[:, 4] - srt[:, 3]) > 1e-9 * srt[:, 3]
+    ref = np.sort(np.argsort(dq, 1, kind="stable")[:, :4], 1)
+    assert np.array_equal(np.sort(o["cand"], 1)[clear], ref[clear])
+    assert np.all([o["idx_k"][i] in o["cand"][i] for i in range(120)])
