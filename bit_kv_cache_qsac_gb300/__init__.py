@@ -32,7 +32,7 @@ QWM_OK, QWM_ERR_ARG, QWM_ERR_SHAPE, QWM_ERR_ALIGN, QWM_ERR_CUDA, QWM_ERR_NOT_CON
 
 EXPORTED = ("qwm_status_string", "qwm_workspace_bytes", "qwm_create", "qwm_destroy",
             "qwm_update_query_stats", "qwm_fit_centroids", "qwm_quantize_kv", "qwm_attend",
-            "qwm_dequantize", "qwm_sync_status", "qwm_update_query_stats_noalloc",
+            "qwm_dequantize", "qwm_sync_status", "qwm_update_query_stats_noalloc", "qwm_quantize_kv_full",
             # comparison baselines (include/qwm_baselines.h)
             "qwm_kivi_quantize", "qwm_kivi_dequantize", "qwm_prq_residual", "qwm_prq_dequantize")
 
@@ -87,6 +87,8 @@ _lib.qwm_destroy.argtypes = [_P]
 _lib.qwm_update_query_stats.argtypes = [_P, _P, C.c_int64, _P, _P, _P, _P, _P, _P]
 _lib.qwm_fit_centroids.argtypes = [_P, _P, C.c_int64, _P, _P, _P]
 _lib.qwm_quantize_kv.argtypes = [_P, _P, _P, C.c_int64, _P, _P, C.POINTER(qwm_chunk), C.POINTER(qwm_debug), _P]
+_lib.qwm_quantize_kv_full.argtypes = [_P, _P, _P, C.c_int64, _P, _P, C.POINTER(qwm_chunk), C.POINTER(qwm_debug),
+                                       _P]
 _lib.qwm_attend.argtypes = [_P, _P, C.c_int64, C.POINTER(qwm_chunk), C.c_int32, C.c_float, _P, _P]
 _lib.qwm_dequantize.argtypes = [_P, C.POINTER(qwm_chunk), _P, _P, _P]
 _lib.qwm_sync_status.argtypes = [_P, _P]
@@ -425,3 +427,19 @@ def qwm_prq_dequantize(ctx: Context, last: Chunk, cent1_k, idx1_k, cent1_v, idx1
                                    _ptr(idx1_v, "idx1_v", idx1_v.element_size(), (H, n)),
                                    _ptr(k_hat, "k_hat", 2, (H, n, d)), _ptr(v_hat, "v_hat", 2, (H, n, d)),
                                    _stream(stream)), "qwm_prq_dequantize")
+
+
+def qwm_quantize_kv_full(ctx: Context, k, v, n: int, M, u_r, out: Chunk, debug: dict | None = None,
+                         stream=None) -> None:
+    """qwm_quantize_kv with the QSAC candidates ranked by (k - mu)^T M (k - mu) (M fp32 [H][d][d])."""
+    H, d, r = ctx.cfg.heads, ctx.cfg.head_dim, ctx.cfg.rank
+    s = out.struct()
+    dbg = None
+    if debug is not None:
+        dbg = qwm_debug(_ptr(debug.get("c_f32"), "c_f32", 4), _ptr(debug.get("cand"), "cand", 4),
+                        _ptr(debug.get("score"), "score", 4), _ptr(debug.get("gate_err"), "gate_err", 4))
+    st = _lib.qwm_quantize_kv_full(ctx.handle, _ptr(k, "k", 2, (H, n, d)), _ptr(v, "v", 2, (H, n, d)), n,
+                                   _ptr(M, "M", 4, (H, d, d)), _ptr(u_r, "u_r", 2, (H, d, r)) if r else None,
+                                   C.byref(s), C.byref(dbg) if dbg is not None else None, _stream(stream))
+    _check(st, "qwm_quantize_kv_full")
+    out.rank_eff = s.rank_eff

@@ -11,7 +11,7 @@ constexpr int kStatsSplits = 8;
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
-  size_t status, stats_part, km_sum, km_cnt, km_cent, jac_basis, jac_valid, km_img, q_img, total;
+  size_t status, stats_part, km_sum, km_cnt, km_cent, jac_basis, jac_valid, km_img, q_img, q_bfull, total;
 };
 
 Layout layout_of(const qwm_config &c) {
@@ -27,6 +27,7 @@ Layout layout_of(const qwm_config &c) {
   L.jac_valid = off; off = align_up(off + (size_t)c.heads * sizeof(int32_t), 256);
   L.km_img = off; off = align_up(off + kmeans_image_bytes(c.heads, c.n_centroids), 1024);
   L.q_img = off; off = align_up(off + quantize_image_bytes(c.heads, c.n_centroids), 1024);
+  L.q_bfull = off; off = align_up(off + (size_t)c.heads * c.n_centroids * QWM_D * sizeof(float), 256);
   L.total = off;
   return L;
 }
@@ -150,6 +151,7 @@ qwm_status qwm_create(const qwm_config *cfg, qwm_ctx **out) {
   ctx->jac_valid = (int32_t *)(base + L.jac_valid);
   ctx->km_img = (unsigned char *)(base + L.km_img);
   ctx->q_img = (unsigned char *)(base + L.q_img);
+  ctx->q_bfull = (float *)(base + L.q_bfull);
   *out = ctx;
   return QWM_OK;
 }
@@ -196,12 +198,14 @@ qwm_status qwm_fit_centroids(qwm_ctx *ctx, const uint16_t *x, int64_t n, const u
   return cuda_status(e);
 }
 
-qwm_status qwm_quantize_kv(qwm_ctx *ctx, const uint16_t *k, const uint16_t *v, int64_t n, const float *w,
-                           const uint16_t *u_r, qwm_chunk *out, const qwm_debug *dbg, qwm_stream stream) {
+static qwm_status quantize_impl(qwm_ctx *ctx, const uint16_t *k, const uint16_t *v, int64_t n, const float *w,
+                                const float *M, const uint16_t *u_r, qwm_chunk *out, const qwm_debug *dbg,
+                                qwm_stream stream) {
   if (!ctx || !k || !v || !out || n < 0) return QWM_ERR_ARG;
   if (out->n_tokens != n) return QWM_ERR_SHAPE;
   if (n > ((int64_t)1 << 31) / QWM_D) return QWM_ERR_SHAPE;
-  if (!aligned16(k) || !aligned16(v) || (w && !aligned16(w)) || (u_r && !aligned16(u_r))) return QWM_ERR_ALIGN;
+  if (!aligned16(k) || !aligned16(v) || (w && !aligned16(w)) || (M && !aligned16(M)) || (u_r && !aligned16(u_r)))
+    return QWM_ERR_ALIGN;
   if (out->kind != QWM_CHUNK_PACKED) return QWM_ERR_ARG;
   const bool psac = (u_r != nullptr) && ctx->cfg.rank > 0;
   out->rank_eff = psac ? ctx->cfg.rank : 0;
@@ -213,9 +217,20 @@ qwm_status qwm_quantize_kv(qwm_ctx *ctx, const uint16_t *k, const uint16_t *v, i
       return QWM_ERR_ALIGN;
   }
   if (n == 0) return QWM_OK;
-  cudaError_t e = launch_quantize(ctx->cfg, k, v, n, w, psac ? u_r : nullptr, *out, dbg, ctx->status,
-                                  ctx->num_sms, ctx->q_img, (cudaStream_t)stream);
+  cudaError_t e = launch_quantize(ctx->cfg, k, v, n, w, M, ctx->q_bfull, psac ? u_r : nullptr, *out, dbg,
+                                  ctx->status, ctx->num_sms, ctx->q_img, (cudaStream_t)stream);
   return cuda_status(e);
+}
+
+qwm_status qwm_quantize_kv(qwm_ctx *ctx, const uint16_t *k, const uint16_t *v, int64_t n, const float *w,
+                           const uint16_t *u_r, qwm_chunk *out, const qwm_debug *dbg, qwm_stream stream) {
+  return quantize_impl(ctx, k, v, n, w, nullptr, u_r, out, dbg, stream);
+}
+
+qwm_status qwm_quantize_kv_full(qwm_ctx *ctx, const uint16_t *k, const uint16_t *v, int64_t n, const float *M,
+                                const uint16_t *u_r, qwm_chunk *out, const qwm_debug *dbg, qwm_stream stream) {
+  if (!M) return QWM_ERR_ARG;
+  return quantize_impl(ctx, k, v, n, nullptr, M, u_r, out, dbg, stream);
 }
 
 qwm_status qwm_attend(qwm_ctx *ctx, const uint16_t *q, int64_t nq, const qwm_chunk *chunks, int32_t n_chunks,

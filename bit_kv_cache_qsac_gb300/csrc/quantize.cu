@@ -62,7 +62,7 @@ constexpr float kRelN = 1.0f / 131072.0f;  // 2^-17
 constexpr int kSlice = 128;                // centroids per streamed slice (WIDE)
 
 struct QSmem {
-  int bh, bl, bn, an, x, msk, wv, U, total;
+  int bh, bl, bn, an, x, msk, wv, U, ef, total;
   // CB = centroids held in shared memory at once: the whole codebook, or one slice (WIDE).  The
   // range [0, an) is also the layout of one slice of the global operand image.
   __host__ __device__ QSmem(int C, bool key, bool wide) {
@@ -75,7 +75,8 @@ struct QSmem {
     msk = x + 2 * 2 * TILE * 128;       // window masks: [8 warps][C/32 words][32 tokens]
     wv = msk + kEpiWarps * (C / 32) * 32 * 4;  // w[D]
     U = wv + 4 * D;                     // U_r as fp32 [D][16], zero past the rank (Keys)
-    total = U + (key ? 4 * D * 16 : 0);
+    ef = U + (key ? 4 * D * 16 : 0);    // Keys: per epilogue warp, one residual row (full-form fallback)
+    total = ef + (key ? kEpiWarps * D * 4 : 0);
   }
 };
 
@@ -94,6 +95,8 @@ struct QParams {
   uint8_t *s8, *zp;          // compact: [H][n][2] steps, [H][n] zero-points (group g in bits 2g..2g+1)
   uint16_t *sigma;           // compact: fp16 [H][ceil(n/128)][2] second-level scales
   const float *wk;           // [H][D] channel weights of the gate (NULL: uniform)
+  const float *Mq;           // full-form ranking: [H][D][D] Query second moment (NULL: diagonal w)
+  const float *Bq;           // full-form ranking: [H][C][D] b_j = M mu_j (the distance GEMM's operand)
   float *dbg_gate;           // [H][n][2] w-weighted error without / with C, or NULL
   int8_t *c;
   uint16_t *c_scale;
@@ -115,6 +118,23 @@ __device__ __forceinline__ void bf16x8(const uint4 v, float (&f)[8]) {
 // byte offset of (row, column k) in a [rows][16] bf16 K-major operand without swizzle
 __host__ __device__ constexpr uint32_t noswz16(uint32_t row, uint32_t k) {
   return (row >> 3) * 256u + (k >> 3) * 128u + (row & 7u) * 16u + (k & 7u) * 2u;
+}
+
+// The lane's share (channels 4 lane .. 4 lane + 3) of e^T M e for a residual row e in shared memory
+// (the rare exact pass of the full-form ranking; kept out of line so that it does not weigh on the
+// register allocation of the common path).
+__device__ __forceinline__ float quad_form_lane(const float *__restrict__ Mh, const float *er, int lane) {
+  float dq = 0.f;
+#pragma unroll 1
+  for (int u = 0; u < 4; u++) {
+    const int c = 4 * lane + u;
+    const float *row = Mh + (int64_t)c * D;
+    float t = 0.f;
+#pragma unroll 1
+    for (int c2 = 0; c2 < D; c2++) t = __fmaf_rn(row[c2], er[c2], t);
+    dq = __fmaf_rn(er[c], t, dq);
+  }
+  return dq;
 }
 
 // Compact metadata (the paper's packed form): the smallest step whose grid [-z s, (3 - z) s] covers
@@ -218,7 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
     tc::tmem_relinquish();
   }
   // ---- per-head constants: weights, basis, distance operands ----
-  for (int c = tid; c < D; c += kThreads) wv[c] = (KEY && p.w) ? p.w[(int64_t)h * D + c] : 1.0f;
+  for (int c = tid; c < D; c += kThreads)
+    wv[c] = (KEY && p.Mq) ? p.Mq[((int64_t)h * D + c) * D + c] : ((KEY && p.w) ? p.w[(int64_t)h * D + c] : 1.0f);
   if (KEY) {
     for (int e = tid; e < D * 16; e += kThreads) {
       const int c = e / 16, k = e % 16;
@@ -239,8 +260,9 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
     uint32_t hw[4], lw[4];
 #pragma unroll
     for (int u = 0; u < 4; u++) {
-      const float b0 = KEY ? __fmul_rn(wv[8 * ci + 2 * u], mu[2 * u]) : mu[2 * u];
-      const float b1 = KEY ? __fmul_rn(wv[8 * ci + 2 * u + 1], mu[2 * u + 1]) : mu[2 * u + 1];
+      const float *bq = (KEY && p.Bq) ? p.Bq + ((int64_t)h * C + j) * D + 8 * ci : nullptr;
+      const float b0 = bq ? bq[2 * u] : (KEY ? __fmul_rn(wv[8 * ci + 2 * u], mu[2 * u]) : mu[2 * u]);
+      const float b1 = bq ? bq[2 * u + 1] : (KEY ? __fmul_rn(wv[8 * ci + 2 * u + 1], mu[2 * u + 1]) : mu[2 * u + 1]);
       const float h0 = __bfloat162float(__float2bfloat16_rn(b0)), h1 = __bfloat162float(__float2bfloat16_rn(b1));
       hw[u] = (uint32_t)f32_to_bf16_rn(h0) | ((uint32_t)f32_to_bf16_rn(h1) << 16);
       lw[u] = (uint32_t)f32_to_bf16_rn(b0 - h0) | ((uint32_t)f32_to_bf16_rn(b1 - h1) << 16);
@@ -256,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
     float s = 0.f, bb = 0.f;
 #pragma unroll
     for (int u = 0; u < 4; u++) {
-      const float wm = __fmul_rn(wv[4 * lane + u], mu[u]);
+      const float wm = (KEY && p.Bq) ? p.Bq[((int64_t)h * C + j) * D + 4 * lane + u] : __fmul_rn(wv[4 * lane + u], mu[u]);
       s = fmaf(wm, mu[u], s);
       bb = fmaf(wm, wm, bb);
     }
@@ -515,10 +537,19 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
             float mu[4];
             unpack4(*(const uint2 *)(cent + (int64_t)j * D + 4 * lane), mu);
             float dq = 0.f;
+            if (KEY && p.Mq) {  // (x - mu)^T M (x - mu): the residual row through shared memory
+              float *er = (float *)(sm + L.ef) + ew * D;
 #pragma unroll
-            for (int u = 0; u < 4; u++) {
-              const float df = __fsub_rn(xf[u], mu[u]);
-              dq = __fmaf_rn(wl[u], __fmul_rn(df, df), dq);
+              for (int u = 0; u < 4; u++) er[4 * lane + u] = __fsub_rn(xf[u], mu[u]);
+              __syncwarp();
+              dq = quad_form_lane(p.Mq + (int64_t)h * D * D, er, lane);
+              __syncwarp();
+            } else {
+#pragma unroll
+              for (int u = 0; u < 4; u++) {
+                const float df = __fsub_rn(xf[u], mu[u]);
+                dq = __fmaf_rn(wl[u], __fmul_rn(df, df), dq);
+              }
             }
             dq = warp_sum(dq);  // identical on every lane
             // insert (dq, j) into the ascending exact list (j increasing: a strict comparison
@@ -852,8 +883,9 @@ __global__ void codebook_f16_kernel(const uint16_t *__restrict__ ck, const uint1
 // swizzled; the [-nw/2 hi, lo, 0 ...] rows), and raises the head's max |b_j| and max |nw_j| (img_max
 // zeroed beforehand; non-negative floats order as integers).
 __global__ void __launch_bounds__(256) quant_image_kernel(const uint16_t *__restrict__ cent_all,
-                                                          const float *__restrict__ w, int C, int key,
-                                                          unsigned char *__restrict__ img_all, float *img_max) {
+                                                          const float *__restrict__ w, const float *__restrict__ Bq,
+                                                          int C, int key, unsigned char *__restrict__ img_all,
+                                                          float *img_max) {
   __shared__ float wv[D];
   const int sl = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const QSmem L(C, key != 0, true);
@@ -869,8 +901,9 @@ __global__ void __launch_bounds__(256) quant_image_kernel(const uint16_t *__rest
     uint32_t hw[4], lw[4];
 #pragma unroll
     for (int u = 0; u < 4; u++) {
-      const float b0 = key ? __fmul_rn(wv[8 * ci + 2 * u], mu[2 * u]) : mu[2 * u];
-      const float b1 = key ? __fmul_rn(wv[8 * ci + 2 * u + 1], mu[2 * u + 1]) : mu[2 * u + 1];
+      const float *bq = (key && Bq) ? Bq + ((int64_t)h * C + (int64_t)sl * kSlice + j) * D + 8 * ci : nullptr;
+      const float b0 = bq ? bq[2 * u] : (key ? __fmul_rn(wv[8 * ci + 2 * u], mu[2 * u]) : mu[2 * u]);
+      const float b1 = bq ? bq[2 * u + 1] : (key ? __fmul_rn(wv[8 * ci + 2 * u + 1], mu[2 * u + 1]) : mu[2 * u + 1]);
       const float h0 = __bfloat162float(__float2bfloat16_rn(b0)), h1 = __bfloat162float(__float2bfloat16_rn(b1));
       hw[u] = (uint32_t)f32_to_bf16_rn(h0) | ((uint32_t)f32_to_bf16_rn(h1) << 16);
       lw[u] = (uint32_t)f32_to_bf16_rn(b0 - h0) | ((uint32_t)f32_to_bf16_rn(b1 - h1) << 16);
@@ -886,7 +919,8 @@ __global__ void __launch_bounds__(256) quant_image_kernel(const uint16_t *__rest
     float s = 0.f, bb = 0.f;
 #pragma unroll
     for (int u = 0; u < 4; u++) {
-      const float wm = __fmul_rn(wv[4 * lane + u], mu[u]);
+      const float wm = (key && Bq) ? Bq[((int64_t)h * C + (int64_t)sl * kSlice + j) * D + 4 * lane + u]
+                                   : __fmul_rn(wv[4 * lane + u], mu[u]);
       s = fmaf(wm, mu[u], s);
       bb = fmaf(wm, wm, bb);
     }
@@ -907,6 +941,20 @@ __global__ void __launch_bounds__(256) quant_image_kernel(const uint16_t *__rest
     atomicMax((int *)&img_max[2 * h], __float_as_int(bmax));
     atomicMax((int *)&img_max[2 * h + 1], __float_as_int(nwmax));
   }
+}
+
+// Full-form ranking operand: b_j = M mu_j for every centroid j of every head (M symmetric, so thread c
+// reads column c of M, coalesced across the block); mu_j staged in shared memory.
+__global__ void __launch_bounds__(128) mfull_b_kernel(const float *__restrict__ M, const uint16_t *__restrict__ cent,
+                                                      int C, float *__restrict__ Bq) {
+  __shared__ float mu[D];
+  const int j = blockIdx.x, h = blockIdx.y, c = threadIdx.x;
+  mu[c] = bf16_to_f32(cent[((int64_t)h * C + j) * D + c]);
+  __syncthreads();
+  const float *Mh = M + (int64_t)h * D * D;
+  float acc = 0.f;
+  for (int c2 = 0; c2 < D; c2++) acc = fmaf(Mh[(int64_t)c2 * D + c], mu[c2], acc);
+  Bq[((int64_t)h * C + j) * D + c] = acc;
 }
 
 template <bool KEY, int RMAX, int MP1, bool WIDE>
@@ -937,8 +985,8 @@ size_t quantize_image_bytes(int H, int C) {
 }
 
 cudaError_t launch_quantize(const qwm_config &cfg, const uint16_t *k, const uint16_t *v, int64_t n, const float *w,
-                            const uint16_t *u_r, const qwm_chunk &out, const qwm_debug *dbg, int32_t *status,
-                            int num_sms, unsigned char *img, cudaStream_t st) {
+                            const float *Mq, float *Bq, const uint16_t *u_r, const qwm_chunk &out, const qwm_debug *dbg,
+                            int32_t *status, int num_sms, unsigned char *img, cudaStream_t st) {
   const int H = cfg.heads, C = cfg.n_centroids;
   const bool wide = C > QWM_MAX_RESIDENT_CENTROIDS;
   float *img_max = wide ? (float *)(img + (size_t)H * (C / kSlice) * QSmem(C, true, true).an) : nullptr;
@@ -950,6 +998,11 @@ cudaError_t launch_quantize(const qwm_config &cfg, const uint16_t *k, const uint
   {
     const int64_t n8 = (int64_t)H * C * QWM_D / 8;
     codebook_f16_kernel<<<num_sms, 256, 0, st>>>(out.cent_k, out.cent_v, out.cent_k16, out.cent_v16, n8, status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (Mq) {  // full-form ranking: the Key distance operand b_j = M mu_j
+    mfull_b_kernel<<<dim3(C, H), D, 0, st>>>(Mq, out.cent_k, C, Bq);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -969,6 +1022,8 @@ cudaError_t launch_quantize(const qwm_config &cfg, const uint16_t *k, const uint
     p.s8 = key ? out.k_s8 : out.v_s8; p.zp = key ? out.k_zp : out.v_zp;
     p.sigma = key ? out.k_sigma : out.v_sigma;
     p.wk = key ? w : nullptr;
+    p.Mq = key ? Mq : nullptr;
+    p.Bq = (key && Mq) ? Bq : nullptr;
     p.dbg_gate = (key && dbg) ? dbg->gate_err : nullptr;
     p.c = out.c; p.c_scale = out.c_scale;
     p.dbg_c = (key && dbg) ? dbg->c_f32 : nullptr;
@@ -980,7 +1035,7 @@ cudaError_t launch_quantize(const qwm_config &cfg, const uint16_t *k, const uint
     if (wide) {  // this pass's operand image (the two passes reuse one buffer, in stream order)
       e = cudaMemsetAsync(img_max, 0, (size_t)H * 2 * sizeof(float), st);
       if (e != cudaSuccess) return e;
-      quant_image_kernel<<<dim3(C / kSlice, H), 256, 0, st>>>(p.cent, p.w, C, key ? 1 : 0, img, img_max);
+      quant_image_kernel<<<dim3(C / kSlice, H), 256, 0, st>>>(p.cent, p.w, p.Bq, C, key ? 1 : 0, img, img_max);
       e = cudaGetLastError();
       if (e != cudaSuccess) return e;
       e = launch_pass<true>(tmap, p, key, H, smem, st);

@@ -31,6 +31,7 @@ struct qwm_ctx {
   int32_t *jac_valid;    // [H] 1 once jac_basis holds a basis
   unsigned char *km_img; // 1024-centroid codebooks: k-means operand slices + norms
   unsigned char *q_img;  // 1024-centroid codebooks: quantiser operand slices + maxima
+  float *q_bfull;        // full-form ranking: b_j = M mu_j [H][C][d]
 };
 
 // record the first device-side error (kernels call this; never traps)
@@ -89,8 +90,8 @@ cudaError_t launch_kmeans(const uint16_t *x, int64_t n, int H, int C, const uint
                           int32_t *status, unsigned char *img, cudaStream_t st);
 size_t quantize_image_bytes(int H, int C);
 cudaError_t launch_quantize(const qwm_config &cfg, const uint16_t *k, const uint16_t *v, int64_t n,
-                            const float *w, const uint16_t *u_r, const qwm_chunk &out, const qwm_debug *dbg,
-                            int32_t *status, int num_sms, unsigned char *img, cudaStream_t st);
+                            const float *w, const float *Mq, float *Bq, const uint16_t *u_r, const qwm_chunk &out,
+                            const qwm_debug *dbg, int32_t *status, int num_sms, unsigned char *img, cudaStream_t st);
 cudaError_t launch_attend(const qwm_config &cfg, const uint16_t *q, int64_t nq, const qwm_chunk *chunks,
                           int n_chunks, float scale, float *out, int num_sms, int32_t *status, cudaStream_t st);
 cudaError_t launch_dequantize(const qwm_config &cfg, const qwm_chunk &ch, uint16_t *k_hat, uint16_t *v_hat,

@@ -201,6 +201,14 @@ QWM_API qwm_status qwm_fit_centroids(qwm_ctx *ctx, const uint16_t *x, int64_t n,
 QWM_API qwm_status qwm_quantize_kv(qwm_ctx *ctx, const uint16_t *k, const uint16_t *v, int64_t n, const float *w,
                            const uint16_t *u_r, qwm_chunk *out, const qwm_debug *dbg, qwm_stream stream);
 
+/* qwm_quantize_kv with the QSAC candidates ranked by the full quadratic form (k - mu)^T M (k - mu)
+ * instead of its diagonal (English v2 summary §C.4: the ablation of QSAC's diagonal approximation;
+ * the pages report no consistent gain).  The rest is unchanged, with w = diag(M) for the range score.
+ *   M   fp32 [H][d][d] symmetric Query second moment (S / n of qwm_update_query_stats). */
+QWM_API qwm_status qwm_quantize_kv_full(qwm_ctx *ctx, const uint16_t *k, const uint16_t *v, int64_t n,
+                                        const float *M, const uint16_t *u_r, qwm_chunk *out, const qwm_debug *dbg,
+                                        qwm_stream stream);
+
 /* Step 5 -- attention over the compressed cache (Chinese summary "注意力logits与时空token
  * 选择": L = Q K^T / sqrt(d); "核心方法": PSAC logits Q K_hat_0^T + Q U_r C^T).
  *   q        bf16 [H][nq][d]

@@ -145,20 +145,26 @@ def _upstream(q, w_, H, n, C=256, top_m=4, rank=8, psac=True, storage=0, gate=0)
     return ctx, k, v, K, V, ch, (w if psac else None), (ch.u_r if psac and rank else None)
 
 
-def _check_quantize(q, ctx, k, v, K, V, ch, w, ur, top_m, rank):
+def _check_quantize(q, ctx, k, v, K, V, ch, w, ur, top_m, rank, M=None):
     H, n = k.shape[:2]
     dbg = dict(c_f32=torch.zeros(H, n, max(rank, 1), device="cuda"),
                cand=torch.zeros(H, n, top_m, dtype=torch.int32, device="cuda"),
                score=torch.zeros(H, n, device="cuda"))
-    q.qwm_quantize_kv(ctx, K, V, n, w, ur, ch, dbg)
+    if M is None:
+        q.qwm_quantize_kv(ctx, K, V, n, w, ur, ch, dbg)
+    else:
+        q.qwm_quantize_kv_full(ctx, K, V, n, M, ur, ch, dbg)
     assert q.qwm_sync_status(ctx) == 0
     assert ch.rank_eff == (rank if ur is not None else 0)
     stats = dict(k_ties=0, v_ties=0, k_edge=0, tokens=H * n)
     for h in range(H):
         wh = None if w is None else w[h].cpu().numpy().astype(np.float64)
+        Mh = None if M is None else M[h].cpu().numpy().astype(np.float64)
+        if Mh is not None:
+            wh = np.diag(Mh).copy()
         urh = None if ur is None else to_u16(ur[h])[:, :rank]
         o = oracle.quantize_head(k[h], v[h], to_u16(ch.cent_k[h]), to_u16(ch.cent_v[h]), wh, urh,
-                                 top_m=top_m, rank=rank if ur is not None else 0)
+                                 top_m=top_m, rank=rank if ur is not None else 0, M_full=Mh)
         gk = ch.k_idx[h].cpu().numpy().astype(np.int32)
         gv = ch.v_idx[h].cpu().numpy().astype(np.int32)
         s2 = o["score2"]; de = o["dq_edge"]; vd = o["vdist2"]
@@ -176,7 +182,8 @@ def _check_quantize(q, ctx, k, v, K, V, ch, w, ur, top_m, rank):
         assert np.all((gc == oc).all(1) | k_edge)
         # re-encode with the GPU's indices: codes, scales and offsets bit-exact
         o2 = oracle.quantize_head(k[h], v[h], to_u16(ch.cent_k[h]), to_u16(ch.cent_v[h]), wh, urh,
-                                  top_m=top_m, rank=rank if ur is not None else 0, force_idx_k=gk, force_idx_v=gv)
+                                  top_m=top_m, rank=rank if ur is not None else 0, force_idx_k=gk, force_idx_v=gv,
+                                  M_full=Mh)
         for name in ("k_codes", "v_codes"):
             assert np.array_equal(getattr(ch, name)[h].cpu().numpy(), o2[name]), name
         for name in ("k_scale", "k_min", "v_scale", "v_min"):
@@ -210,6 +217,28 @@ def test_quantize_cold_start(q):
 def test_quantize_ragged_and_shapes(q, n, C, top_m, rank):
     ctx, k, v, K, V, ch, w, ur = _upstream(q, synth.TINY, 2, n, C=C, top_m=top_m, rank=rank)
     _check_quantize(q, ctx, k, v, K, V, ch, w, ur, top_m, rank)
+
+
+@pytest.mark.parametrize("C,n,top_m", [(256, 1000, 4), (64, 700, 16), (1024, 2000, 4)])
+def test_quantize_full_form_ranking(q, C, n, top_m):
+    """English v2 §C.4 ablation: candidates ranked by (k - mu)^T M (k - mu) with the full Query second
+    moment M (from the GPU statistics), the choice by the range score with w = diag(M)."""
+    w_ = WIDE_W if C > 256 else synth.TINY
+    H = 2
+    k = synth.keys(w_)[:H, :n]; v = synth.values(w_)[:H, :n]
+    ctx = q.Context(heads=H, n_centroids=C, top_m=top_m, rank=8)
+    S = torch.zeros(H, D, D, device="cuda"); cnt = torch.zeros(H, dtype=torch.int64, device="cuda")
+    w = torch.empty(H, D, device="cuda"); lam = torch.empty(H, D, device="cuda")
+    ur = torch.zeros(H, D, 8, dtype=torch.bfloat16, device="cuda")
+    q.qwm_update_query_stats(ctx, _bf(synth.queries(w_, -1, 256)[:H]), 256, S, cnt, w, lam, ur)
+    M = (S / cnt.view(H, 1, 1).float()).contiguous()
+    ch = q.Chunk.empty(ctx, n)
+    K, V = _bf(k), _bf(v)
+    q.qwm_fit_centroids(ctx, K, n, None, ch.cent_k)
+    q.qwm_fit_centroids(ctx, V, n, None, ch.cent_v)
+    ch.u_r.copy_(ur)
+    st = _check_quantize(q, ctx, k, v, K, V, ch, None, ch.u_r, top_m, 8, M=M)
+    print("tie fractions", {key: val / st["tokens"] for key, val in st.items() if key != "tokens"})
 
 
 @pytest.mark.parametrize("n,top_m,rank", [(2600, 4, 8), (1500, 16, 16), (1100, 1, 0)])
