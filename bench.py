@@ -535,10 +535,10 @@ def run_ablation(device, parts=("sweep", "storage", "baselines")):
                 torch.cuda.empty_cache()
     # the paper's packed form: compact INT2 metadata and the PSAC keep-if-better gate (256, M = 4, r = 8)
     for C in ((256,) if "storage" in parts else ()):
-        for storage, gate in ((0, 1), (1, 0), (1, 1)):
+        for storage, gate, full in ((0, 1, False), (1, 0, False), (1, 1, False), (0, 0, True)):
             ctx = q.Context(heads=Hh, n_centroids=C, top_m=4, rank=8, kmeans_iters=10, storage=storage,
                             psac_gate=gate)
-            layer = CompressedLayer(ctx, device)
+            layer = CompressedLayer(ctx, device, full_query=full)
             for t in range(T):
                 if t > 0:
                     layer.fold_queries(Q[t - 1])
@@ -561,6 +561,7 @@ def run_ablation(device, parts=("sweep", "storage", "baselines")):
                               "n_centroids": C, "top_m": 4, "rank": 8,
                               "storage": "compact (8-bit step, 2-bit zero-point)" if storage else "fp16 step/offset",
                               "psac_gate": gate, "psac_kept_fraction": kept,
+                              "qsac_ranking": "full (k-mu)^T M (k-mu)" if full else "diagonal w",
                               "pack_ms": ev[0].elapsed_time(ev[1]), "attend_ms": ev[2].elapsed_time(ev[3]),
                               "logit_mse": mse, "logit_mse_rel": mse / ms2_ref,
                               "top1_shift": float((L.argmax(-1) != top_ref).float().mean()),

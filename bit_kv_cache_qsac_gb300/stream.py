@@ -15,14 +15,18 @@ import math
 import torch
 
 from . import (ActiveChunk, Chunk, Context, qwm_attend, qwm_dequantize, qwm_fit_centroids, qwm_quantize_kv,
+               qwm_quantize_kv_full,
                qwm_sync_status, qwm_update_query_stats)
 
 
 class CompressedLayer:
     """Running state of one layer: Query statistics, basis, packed chunks, last codebooks."""
 
-    def __init__(self, ctx: Context, device=None):
+    def __init__(self, ctx: Context, device=None, full_query: bool = False):
+        """full_query: rank the QSAC candidates by the full Query second moment (English v2 §C.4
+        ablation) instead of its diagonal."""
         self.ctx = ctx
+        self.full_query = full_query
         cfg = ctx.cfg
         H, d, r = cfg.heads, cfg.head_dim, cfg.rank
         dev = device or torch.device("cuda", torch.cuda.current_device())
@@ -61,7 +65,11 @@ class CompressedLayer:
         if psac:
             ch.u_r.copy_(self.u_r)   # per-chunk snapshot of the basis
         w = self.w if self.n_seen > 0 else None
-        qwm_quantize_kv(self.ctx, k, v, n, w, ch.u_r if psac else None, ch, debug, stream)
+        if self.full_query and w is not None:
+            M = (self.S / self.n.view(-1, 1, 1).to(self.S.dtype)).contiguous()
+            qwm_quantize_kv_full(self.ctx, k, v, n, M, ch.u_r if psac else None, ch, debug, stream)
+        else:
+            qwm_quantize_kv(self.ctx, k, v, n, w, ch.u_r if psac else None, ch, debug, stream)
         self.chunks.append(ch)
         self.prev_cent_k, self.prev_cent_v = ch.cent_k, ch.cent_v
         return ch
