@@ -201,8 +201,14 @@ qwm_status qwm_fit_centroids(qwm_ctx *ctx, const uint16_t *x, int64_t n, const u
 static qwm_status quantize_impl(qwm_ctx *ctx, const uint16_t *k, const uint16_t *v, int64_t n, const float *w,
                                 const float *M, const uint16_t *u_r, qwm_chunk *out, const qwm_debug *dbg,
                                 qwm_stream stream) {
-  if (!ctx || !k || !v || !out || n < 0) return QWM_ERR_ARG;
+  if (!ctx || !out || n < 0) return QWM_ERR_ARG;
   if (out->n_tokens != n) return QWM_ERR_SHAPE;
+  if (out->kind != QWM_CHUNK_PACKED) return QWM_ERR_ARG;
+  if (n == 0) {  // nothing to read or write: the chunk's pointers may be NULL
+    out->rank_eff = (u_r != nullptr && ctx->cfg.rank > 0) ? ctx->cfg.rank : 0;
+    return QWM_OK;
+  }
+  if (!k || !v) return QWM_ERR_ARG;
   if (n > ((int64_t)1 << 31) / QWM_D) return QWM_ERR_SHAPE;
   if (!aligned16(k) || !aligned16(v) || (w && !aligned16(w)) || (M && !aligned16(M)) || (u_r && !aligned16(u_r)))
     return QWM_ERR_ALIGN;
@@ -235,13 +241,16 @@ qwm_status qwm_quantize_kv_full(qwm_ctx *ctx, const uint16_t *k, const uint16_t 
 
 qwm_status qwm_attend(qwm_ctx *ctx, const uint16_t *q, int64_t nq, const qwm_chunk *chunks, int32_t n_chunks,
                       float softmax_scale, float *out, qwm_stream stream) {
-  if (!ctx || !chunks || !out || nq < 0 || n_chunks < 1) return QWM_ERR_ARG;
+  if (!ctx || !chunks || nq < 0 || n_chunks < 1) return QWM_ERR_ARG;
+  if (nq > 0 && !out) return QWM_ERR_ARG;
   if (nq > 0 && !q) return QWM_ERR_ARG;
   if ((q && !aligned16(q)) || !aligned16(out)) return QWM_ERR_ALIGN;
   if (nq > ((int64_t)1 << 31) / QWM_D) return QWM_ERR_SHAPE;
   if (n_chunks > 128) return QWM_ERR_SHAPE;
   int64_t total = 0;
   for (int i = 0; i < n_chunks; i++) {
+    if (chunks[i].n_tokens < 0) return QWM_ERR_ARG;
+    if (chunks[i].n_tokens == 0) continue;  // skipped: its pointers may be NULL
     qwm_status s = check_chunk(ctx->cfg, &chunks[i], true);
     if (s != QWM_OK) return s;
     total += chunks[i].n_tokens;
@@ -255,8 +264,9 @@ qwm_status qwm_attend(qwm_ctx *ctx, const uint16_t *q, int64_t nq, const qwm_chu
 
 qwm_status qwm_dequantize(qwm_ctx *ctx, const qwm_chunk *chunk, uint16_t *k_hat, uint16_t *v_hat,
                           qwm_stream stream) {
-  if (!ctx || !chunk) return QWM_ERR_ARG;
+  if (!ctx || !chunk || chunk->n_tokens < 0) return QWM_ERR_ARG;
   if (chunk->kind == QWM_CHUNK_BF16) return QWM_ERR_UNSUPPORTED;
+  if (chunk->n_tokens == 0) return QWM_OK;
   qwm_status s = check_chunk(ctx->cfg, chunk, false);
   if (s != QWM_OK) return s;
   if ((k_hat && !aligned16(k_hat)) || (v_hat && !aligned16(v_hat))) return QWM_ERR_ALIGN;

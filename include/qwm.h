@@ -28,7 +28,9 @@
  *    memory only in qwm_create (its workspace, qwm_workspace_bytes() bytes)
  *    and frees it in qwm_destroy.
  *  - Every pointer must be 16-byte aligned and the tensor dense, in the layout
- *    given; bf16 and fp16 values travel as uint16_t bit patterns.
+ *    given; bf16 and fp16 values travel as uint16_t bit patterns.  Pointers to empty arrays
+ *    (a chunk with n_tokens == 0, Keys of a 0-token call, q and out of a 0-Query attention) may
+ *    be NULL: such calls and chunks do nothing.
  *  - Head-major layouts: [H][tokens][channels] with H = config.heads.
  *  - A context is not thread-safe; calls that share a context must be
  *    ordered on one stream (the workspace is reused between calls).

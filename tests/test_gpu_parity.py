@@ -504,3 +504,45 @@ def test_bad_arguments_raise(q):
     with pytest.raises(ValueError):
         q.qwm_fit_centroids(ctx, x, 299, None, cent)
     assert q.qwm_sync_status(ctx) == 0
+
+
+# ------------------------------------------------------------------ edge cases
+
+
+def test_edge_empty_inputs_and_limits(q):
+    """Empty chunks and Query sets, a single-token chunk, one head, the 128-chunk limit of one call."""
+    H = 1
+    ctx = q.Context(heads=H, n_centroids=64, top_m=4, rank=8)
+    k = synth.keys(synth.TINY)[:H, :256]; v = synth.values(synth.TINY)[:H, :256]
+    K, V = _bf(k), _bf(v)
+    # a codebook from 256 tokens, then chunks of 0, 1 and 17 tokens packed with it
+    full = q.Chunk.empty(ctx, 256)
+    q.qwm_fit_centroids(ctx, K, 256, None, full.cent_k)
+    q.qwm_fit_centroids(ctx, V, 256, None, full.cent_v)
+    chunks = []
+    for n in (0, 1, 17):
+        ch = q.Chunk.empty(ctx, n)
+        ch.cent_k.copy_(full.cent_k); ch.cent_v.copy_(full.cent_v)
+        q.qwm_quantize_kv(ctx, K[:, :n].contiguous(), V[:, :n].contiguous(), n, None, None, ch)
+        chunks.append(ch)
+    assert q.qwm_sync_status(ctx) == 0
+    qa = synth.queries(synth.TINY, 6, 40)[:H]
+    out = torch.empty(H, 40, D, dtype=torch.float32, device="cuda")
+    q.qwm_attend(ctx, _bf(qa), 40, chunks, 1 / math.sqrt(D), out)       # the empty chunk is skipped
+    assert q.qwm_sync_status(ctx) == 0
+    ref = oracle.attend_rows(qa[0], np.arange(40), [chunk_head(c, 0) for c in chunks[1:]], 1 / math.sqrt(D))
+    assert _attn_err(out[0].cpu().numpy().astype(np.float64), ref) <= 2e-2
+    q.qwm_attend(ctx, _bf(qa[:, :0].copy()), 0, chunks, 1 / math.sqrt(D), out[:, :0])   # no Queries: a no-op
+    with pytest.raises(q.QwmError) as e:
+        q.qwm_attend(ctx, _bf(qa), 40, chunks[:1], 1 / math.sqrt(D), out)   # no key at all
+    assert e.value.status == q.QWM_ERR_SHAPE
+    kh = torch.empty(H, 0, D, dtype=torch.bfloat16, device="cuda")
+    q.qwm_dequantize(ctx, chunks[0], kh, kh.clone())
+    # 128 chunks of 2 tokens each (the most one call takes), then 129 (rejected)
+    many = [chunks[2]] * 64 + [chunks[1]] * 64
+    q.qwm_attend(ctx, _bf(qa), 40, many, 1 / math.sqrt(D), out)
+    assert q.qwm_sync_status(ctx) == 0
+    ref = oracle.attend_rows(qa[0], np.arange(40), [chunk_head(c, 0) for c in many], 1 / math.sqrt(D))
+    assert _attn_err(out[0].cpu().numpy().astype(np.float64), ref) <= 2e-2
+    with pytest.raises(q.QwmError):
+        q.qwm_attend(ctx, _bf(qa), 40, many + [chunks[1]], 1 / math.sqrt(D), out)
