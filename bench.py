@@ -677,8 +677,46 @@ def run_ablation_baselines(device, K, V, Q, Qs, Lref, top_ref, ms2_ref):
     report("KIVI-style INT2 (groups of 32, 2-frame bf16 window)", pack_ms, kk, vk, kivi_decode, kivi_bytes)
 
 
+def run_steps(device):
+    """Every step of the streaming layer (720p- or 480p-shaped, --workload): at step t, fold Q_{t-1},
+    fit and pack chunk t, attend Q_t over chunks 1..t.  CUDA events per stage, after a warm-up pass
+    over all steps; the attention's TFLOP/s at 528 flops per (Query, key) pair."""
+    import torch
+    import bit_kv_cache_qsac_gb300 as q
+    from bit_kv_cache_qsac_gb300.stream import CompressedLayer
+    T = W.n_chunks
+    ks, vs, qs = gen_layer(layer=0)
+    K = [_dev_bf16(k, device) for k in ks]
+    V = [_dev_bf16(v, device) for v in vs]
+    Q = [_dev_bf16(x, device) for x in qs]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for rep_ in range(2):  # the first pass warms up
+        ctx = q.Context(heads=H, n_centroids=W.n_centroids, top_m=W.top_m, rank=W.rank, kmeans_iters=10)
+        layer = CompressedLayer(ctx, device)
+        rows = []
+        for t in range(T):
+            ev[0].record()
+            if t > 0:
+                layer.fold_queries(Q[t - 1])
+            ev[1].record()
+            layer.append_chunk(K[t], V[t])
+            ev[2].record()
+            layer.attend(Q[t])
+            ev[3].record()
+            ev[3].synchronize()
+            att = ev[2].elapsed_time(ev[3])
+            pairs = H * NQ * N_CHUNK * (t + 1)
+            rows.append({"step": t + 1, "cache_tokens": N_CHUNK * (t + 1), "stats_eig_ms": ev[0].elapsed_time(ev[1]),
+                         "fit_and_pack_ms": ev[1].elapsed_time(ev[2]), "attend_ms": att,
+                         "attend_tflops": pairs * 528 / (att / 1e3) / 1e12})
+        assert layer.check() == 0
+        del layer, ctx
+    print(json.dumps({"report": "steps", "workload": f"{W.name}-shaped layer", "heads": H, "queries": NQ,
+                      "steps": rows, "note": "stages timed one after another (host sync per step)"}), flush=True)
+
+
 def run_full_model(device, storage: int = 0):
-    """Config 3: 40 layers of the 480p-shaped workload streamed chunk by chunk (8 steps per layer:
+    """The full model: 40 layers of the 480p-shaped workload streamed chunk by chunk (8 steps per layer:
     fold the previous chunk's Queries, fit and pack the chunk, attend with the chunk's Queries over
     every packed chunk).  Every layer's compressed cache stays resident; reports the compressed
     size against the bf16 size and the per-step times summed over the layers (CUDA events), beside
@@ -786,9 +824,10 @@ def main():
     ap.add_argument("--storage", choices=["fp16", "compact"], default="fp16",
                     help="INT2 metadata of the packed chunks in --report full-model: fp16 step/offset or the "
                          "paper's compact form (8-bit step, 2-bit zero-point) with the PSAC keep-if-better gate")
-    ap.add_argument("--report", choices=["ablation", "storage", "baselines", "full-model"], default=None,
+    ap.add_argument("--report", choices=["ablation", "storage", "baselines", "full-model", "steps"], default=None,
                     help="instead of the benchmark line: the M x r x C sweep and the QVG / KIVI baselines "
-                         "(config 4), the baselines alone, or the 40-layer 480p-shaped model (config 3)")
+                         "at the 480p-shaped chunk, the baselines alone, the 40-layer 480p-shaped model, or every "
+                         "streaming step of the --workload layer with per-stage times")
     args = ap.parse_args()
     if args.report:
         import torch
@@ -796,6 +835,9 @@ def main():
         torch.cuda.set_device(device)
         if args.report == "full-model":
             run_full_model(device, 1 if args.storage == "compact" else 0)
+        elif args.report == "steps":
+            select_workload(args.workload)
+            run_steps(device)
         else:
             run_ablation(device, ("sweep", "storage", "baselines") if args.report == "ablation" else (args.report,))
         return
