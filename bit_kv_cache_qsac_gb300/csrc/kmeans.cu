@@ -21,10 +21,13 @@
 // memory (over the codebook area; lane l adds channels l, l + 32, l + 64, l + 96, so the 32 lanes
 // of an add hit 32 different banks); the CTA adds them to its own slice of the workspace and
 // km_update_kernel reduces the slices in a fixed order.
-// Codebooks of 1024 centroids (WIDE) do not fit in shared memory: km_image_kernel writes each
-// head's hi/lo operands as 128-centroid slices in global memory (with the squared norms), the
-// producer streams the slices through one shared-memory buffer for every tile, and the argmin runs
-// slice by slice over two 128-column TMEM halves per epilogue group.  The cluster sums then come
+// The kernels that produce centroids (kmeans_init_kernel, km_update_kernel) also write the next
+// assignment's operands: each head's hi/lo bf16 blocks, 128-byte swizzled exactly as the MMA reads
+// them, and the squared norms ||mu_j||^2, so that the assignment kernel starts with one bulk copy
+// instead of converting the fp32 codebook itself.  Codebooks of up to 256 centroids are one slice
+// held in shared memory for the whole launch.  Codebooks of 1024 centroids (WIDE) do not fit: their
+// operands are 128-centroid slices that the producer streams through one shared-memory buffer for
+// every tile, and the argmin runs slice by slice over two 128-column TMEM halves per epilogue group.  The cluster sums then come
 // from a stable counting sort of the super-chunk's assignments and one warp per centroid adding its
 // members' rows in token order (no one-hot matrix: it would not fit).
 // All waits are bounded; on expiry the kernel records QWM_ERR_DEVICE_TIMEOUT and stops.
@@ -60,38 +63,46 @@ struct KmSmem {  // offsets from a 1024-aligned base, for a codebook of C centro
   }
 };
 
-__global__ void kmeans_init_kernel(const uint16_t *__restrict__ x, int64_t n, int C, const uint16_t *__restrict__ init,
-                                   float *__restrict__ cent) {
-  const int h = blockIdx.y, j = blockIdx.x, c = threadIdx.x;
-  const uint16_t *src = init ? init + ((int64_t)h * C + j) * D : x + ((int64_t)h * n + (int64_t)j * n / C) * D;
-  cent[((int64_t)h * C + j) * D + c] = bf16_to_f32(src[c]);
-}
 
-// WIDE operand image of the fp32 centroids: [H][C / kSlice] slices of (hi, lo) 128-byte-swizzled
-// [kSlice][64] block pairs, exactly as the kernel's slice buffer; norms [H][C] = ||mu_j||^2.
-__global__ void km_image_kernel(const float *__restrict__ cent, int C, unsigned char *__restrict__ img,
-                                float *__restrict__ norms) {
+// Centroids per operand slice: the whole codebook when it stays in shared memory, else kSlice.
+__host__ __device__ __forceinline__ int slice_cents(int C) { return C > QWM_MAX_RESIDENT_CENTROIDS ? kSlice : C; }
+
+// Operand image of one head's fp32 codebook: [C / CB] slices, each the (hi, lo) pair of
+// 128-byte-swizzled [CB][64]-channel block pairs (CB = slice_cents(C)), mu = hi + lo with hi, lo bf16;
+// then norms[j] = ||mu_j||^2.  Called by all D threads of a block, thread c holding channel c of
+// centroid j.
+__device__ __forceinline__ void write_operand(unsigned char *__restrict__ img, float *__restrict__ norms, int C, int j,
+                                              int c, float mu) {
   __shared__ float part[D / 32];
-  const int h = blockIdx.y, j = blockIdx.x, c = threadIdx.x;
-  const float mu = cent[((int64_t)h * C + j) * D + c];
+  const int CB = slice_cents(C);
   const float hi = __bfloat162float(__float2bfloat16_rn(mu));
-  unsigned char *sl = img + ((int64_t)h * (C / kSlice) + j / kSlice) * kSliceBytes;
-  const uint32_t off = (uint32_t)(c / 64) * kSlice * 128u + tc::sw128_offset(j % kSlice, c % 64);
+  unsigned char *sl = img + (int64_t)(j / CB) * 4 * CB * 128;
+  const uint32_t off = (uint32_t)(c / 64) * CB * 128u + tc::sw128_offset(j % CB, c % 64);
   *(uint16_t *)(sl + off) = f32_to_bf16_rn(hi);
-  *(uint16_t *)(sl + 2 * kSlice * 128 + off) = f32_to_bf16_rn(mu - hi);
+  *(uint16_t *)(sl + 2 * CB * 128 + off) = f32_to_bf16_rn(mu - hi);
   float s = mu * mu;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
   if ((c & 31) == 0) part[c >> 5] = s;
   __syncthreads();
-  if (c == 0) norms[(int64_t)h * C + j] = (part[0] + part[1]) + (part[2] + part[3]);
+  if (c == 0) norms[j] = (part[0] + part[1]) + (part[2] + part[3]);
+}
+
+// Initial centroids: the warm-start codebook, or tokens floor(j n / C) of the chunk.
+__global__ void __launch_bounds__(D) kmeans_init_kernel(const uint16_t *__restrict__ x, int64_t n, int C,
+                                                        const uint16_t *__restrict__ init, float *__restrict__ cent,
+                                                        unsigned char *__restrict__ img, float *__restrict__ norms) {
+  const int h = blockIdx.y, j = blockIdx.x, c = threadIdx.x;
+  const uint16_t *src = init ? init + ((int64_t)h * C + j) * D : x + ((int64_t)h * n + (int64_t)j * n / C) * D;
+  const float mu = bf16_to_f32(src[c]);
+  cent[((int64_t)h * C + j) * D + c] = mu;
+  write_operand(img + (int64_t)h * C * 512, norms + (int64_t)h * C, C, j, c, mu);
 }
 
 struct AssignParams {
   const uint16_t *x;     // [H][n][D] bf16
-  const float *cent;     // [H][C][D] fp32
-  const unsigned char *img;  // WIDE: operand slices
-  const float *norms;        // WIDE: [H][C]
+  const unsigned char *img;  // operand image [H][C / CB][slice]
+  const float *norms;        // [H][C]
   float *part_sum;       // [H][G][C][D]
   int32_t *part_cnt;     // [H][G][C]
   int64_t n;
@@ -107,6 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
   __shared__ uint64_t x_full[2], x_empty[2], t_full[2], t_empty[2], drain;
   __shared__ uint64_t p2_full[2], p2_empty[2], a_full[2], a_empty[2], p2_done;
   __shared__ uint64_t tw_full[4], tw_empty[4], sl_full, sl_empty;  // WIDE: TMEM halves, slice buffer
+  __shared__ uint64_t cb_full;  // operands and norms of the codebook
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
   const int C = p.C;
@@ -142,6 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
     tc::mbar_init(&sl_full, 1);
     tc::mbar_init(&sl_empty, 1);
     tc::mbar_init(&p2_done, 1);
+    tc::mbar_init(&cb_full, 1);
     tc::mbar_init(&drain, 1);
     abort_flag = 0;
     tc::fence_mbar_init();
@@ -154,47 +167,29 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base_sh;
-  const float *cent = p.cent + (int64_t)h * C * D;
   float *psum = p.part_sum + ((int64_t)h * p.G + cta) * C * D;
   int32_t *pcnt = p.part_cnt + ((int64_t)h * p.G + cta) * C;
   int64_t g_tile = 0;  // tiles this CTA has processed (barrier phases)
   int64_t g2 = 0;      // tiles re-read by phase 2 (barrier phases)
   int n_sc = 0;        // super-chunks done (phase of p2_done)
+  int n_cb = 0;        // operand loads done (phase of cb_full)
   for (int64_t sc0 = tile0, first = 1; first || sc0 < tile1; sc0 += kMaxTok / TILE, first = 0) {
     const int64_t left = tile1 - sc0;
     const int nt = left <= 0 ? 0 : (left < kMaxTok / TILE ? (int)left : kMaxTok / TILE);
-    // ---- codebook -> hi/lo bf16 operand blocks, and squared norms (WIDE: norms only) ----
-    if (WIDE)
-      for (int j = tid; j < C; j += kThreads) norm[j] = p.norms[(int64_t)h * C + j];
-    for (int e = tid; e < (WIDE ? 0 : C) * (D / 8); e += kThreads) {
-      const int j = e / (D / 8), ci = e % (D / 8);
-      const float4 a = *(const float4 *)(cent + (int64_t)j * D + 8 * ci);
-      const float4 b = *(const float4 *)(cent + (int64_t)j * D + 8 * ci + 4);
-      const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-      uint32_t hw[4], lw[4];
-#pragma unroll
-      for (int u = 0; u < 4; u++) {
-        const float h0 = __bfloat162float(__float2bfloat16_rn(v[2 * u]));
-        const float h1 = __bfloat162float(__float2bfloat16_rn(v[2 * u + 1]));
-        hw[u] = (uint32_t)f32_to_bf16_rn(h0) | ((uint32_t)f32_to_bf16_rn(h1) << 16);
-        lw[u] = (uint32_t)f32_to_bf16_rn(v[2 * u] - h0) | ((uint32_t)f32_to_bf16_rn(v[2 * u + 1] - h1) << 16);
-      }
-      const uint32_t off = (ci / 8) * C * 128 + tc::sw128_offset(j, 8 * (ci % 8));
-      *(uint4 *)(sm + L.bh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-      *(uint4 *)(sm + L.bl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-    }
-    for (int j = warp; j < (WIDE ? 0 : C); j += kThreads / 32) {  // one warp per centroid, 4 channels per lane
-      const float4 a = *(const float4 *)(cent + (int64_t)j * D + 4 * lane);
-      float s = a.x * a.x;
-      s = fmaf(a.y, a.y, s);
-      s = fmaf(a.z, a.z, s);
-      s = fmaf(a.w, a.w, s);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (lane == 0) norm[j] = s;
-    }
+    // ---- operands of the codebook (resident: hi/lo blocks; WIDE: streamed per tile) and norms ----
+    // (the previous super-chunk wrote the one-hot buffers and counts over these areas)
     tc::fence_proxy_async_smem();
     __syncthreads();
+    if (tid == 0) {
+      const uint32_t img_bytes = WIDE ? 0u : (uint32_t)C * 512u;
+      tc::mbar_arrive_expect_tx(&cb_full, img_bytes + 4u * (uint32_t)C);
+      if (!WIDE) tc::bulk_load(tc::smem_u32(sm + L.bh), p.img + (int64_t)h * C * 512, img_bytes, &cb_full);
+      tc::bulk_load(tc::smem_u32(norm), p.norms + (int64_t)h * C, 4u * (uint32_t)C, &cb_full);
+    }
+    if (!tc::mbar_wait(&cb_full, (uint32_t)(n_cb & 1), kWaitNs)) *abort_v = 1;
+    n_cb++;
+    __syncthreads();
+    if (*abort_v) break;
     // ---- phase 1: assignments of nt tiles ----
     if (warp == 0) {
       if (lane == 0) {
@@ -553,9 +548,13 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
   }
 }
 
-// New centroid = (sum of the G partial sums, in order) / count; empty clusters keep theirs.
-__global__ void km_update_kernel(int C, int G, float *__restrict__ cent, const float *__restrict__ part_sum,
-                                 const int32_t *__restrict__ part_cnt, uint16_t *__restrict__ out_bf16) {
+// New centroid = (sum of the G partial sums, in order) / count; empty clusters keep theirs.  Also
+// writes the next assignment's operands (write_operand).
+__global__ void __launch_bounds__(D) km_update_kernel(int C, int G, float *__restrict__ cent,
+                                                      const float *__restrict__ part_sum,
+                                                      const int32_t *__restrict__ part_cnt,
+                                                      uint16_t *__restrict__ out_bf16, unsigned char *__restrict__ img,
+                                                      float *__restrict__ norms) {
   const int h = blockIdx.y, j = blockIdx.x, c = threadIdx.x;
   float s = 0.f;
   int cnt = 0;
@@ -568,6 +567,7 @@ __global__ void km_update_kernel(int C, int G, float *__restrict__ cent, const f
   if (cnt > 0) mu = __fdiv_rn(s, (float)cnt);  // counts are exact in fp32 (< 2^24)
   cent[e] = mu;
   if (out_bf16) out_bf16[e] = f32_to_bf16_rn(mu);
+  else write_operand(img + (int64_t)h * C * 512, norms + (int64_t)h * C, C, j, c, mu);
 }
 
 }  // namespace
@@ -575,36 +575,30 @@ __global__ void km_update_kernel(int C, int G, float *__restrict__ cent, const f
 // CTAs per head: one wave at most (each CTA holds ~200 KB of shared memory).
 int kmeans_ctas_per_head(int H, int num_sms) { return num_sms / H > 1 ? num_sms / H : 1; }
 
-// Workspace of the WIDE operand images: [H][C / kSlice] slices, then the norms [H][C].
-size_t kmeans_image_bytes(int H, int C) {
-  if (C <= QWM_MAX_RESIDENT_CENTROIDS) return 0;
-  return (size_t)H * (C / kSlice) * kSliceBytes + (size_t)H * C * sizeof(float);
-}
+// Workspace of the operand images: [H] heads of C x 512 bytes, then the norms [H][C].
+size_t kmeans_image_bytes(int H, int C) { return (size_t)H * C * 512 + (size_t)H * C * sizeof(float); }
 
 cudaError_t launch_kmeans(const uint16_t *x, int64_t n, int H, int C, const uint16_t *init, int iters,
                           uint16_t *cent, float *km_cent, float *km_sum, int32_t *km_cnt, int num_sms,
                           int32_t *status, unsigned char *img, cudaStream_t st) {
   TensorMap128 tmap;
   if (!make_tmap_rows128_bf16(&tmap, x, (uint64_t)H * n, TILE)) return cudaErrorInvalidValue;
-  kmeans_init_kernel<<<dim3(C, H), D, 0, st>>>(x, n, C, init, km_cent);
+  float *norms = (float *)(img + (size_t)H * C * 512);
+  kmeans_init_kernel<<<dim3(C, H), D, 0, st>>>(x, n, C, init, km_cent, img, norms);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const bool wide = C > QWM_MAX_RESIDENT_CENTROIDS;
-  float *norms = wide ? (float *)(img + (size_t)H * (C / kSlice) * kSliceBytes) : nullptr;
   const int G = kmeans_ctas_per_head(H, num_sms);
   const int smem = KmSmem(C, wide).total + 1024;
   e = wide ? cudaFuncSetAttribute(km_assign_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
            : cudaFuncSetAttribute(km_assign_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  AssignParams p{x, km_cent, img, norms, km_sum, km_cnt, n, C, G, status};
+  AssignParams p{x, img, norms, km_sum, km_cnt, n, C, G, status};
   for (int it = 0; it < iters; it++) {
-    if (wide) {
-      km_image_kernel<<<dim3(C, H), D, 0, st>>>(km_cent, C, img, norms);
-      km_assign_kernel<true><<<dim3(G, H), kThreads, smem, st>>>(tmap, p);
-    } else {
-      km_assign_kernel<false><<<dim3(G, H), kThreads, smem, st>>>(tmap, p);
-    }
-    km_update_kernel<<<dim3(C, H), D, 0, st>>>(C, G, km_cent, km_sum, km_cnt, it == iters - 1 ? cent : nullptr);
+    if (wide) km_assign_kernel<true><<<dim3(G, H), kThreads, smem, st>>>(tmap, p);
+    else km_assign_kernel<false><<<dim3(G, H), kThreads, smem, st>>>(tmap, p);
+    km_update_kernel<<<dim3(C, H), D, 0, st>>>(C, G, km_cent, km_sum, km_cnt, it == iters - 1 ? cent : nullptr, img,
+                                                norms);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
