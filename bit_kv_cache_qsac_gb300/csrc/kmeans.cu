@@ -16,20 +16,20 @@
 //   warp 1    TMEM owner and MMA issuer: D[128 x C] = X hi^T + X lo^T into 2 TMEM buffers
 //   warps 2-9 epilogue, two warpgroups taking alternate tiles: thread = token = TMEM lane;
 //             argmin over the C columns (two interleaved chains, lower index on ties)
-// The assignments of up to 4096 tokens stay in shared memory; then the token tiles stream through
-// the token stages again (TMA) and the warps add each token into per-CTA cluster sums in shared
-// memory (over the codebook area; lane l adds channels l, l + 32, l + 64, l + 96, so the 32 lanes
-// of an add hit 32 different banks); the CTA adds them to its own slice of the workspace and
-// km_update_kernel reduces the slices in a fixed order.
+// The assignments of up to 4096 tokens stay in shared memory.  Then the cluster sums: the token
+// tiles stream through the token stages again (TMA), pairs of epilogue warps write the one-hot
+// assignment matrix of each 64-token half-tile into one of four buffers over the codebook area, and
+// the MMA warp accumulates sums = onehot^T X in TMEM; the CTA adds them to its own slice of the
+// workspace and km_update_kernel reduces the slices in a fixed order.
 // The kernels that produce centroids (kmeans_init_kernel, km_update_kernel) also write the next
 // assignment's operands: each head's hi/lo bf16 blocks, 128-byte swizzled exactly as the MMA reads
 // them, and the squared norms ||mu_j||^2, so that the assignment kernel starts with one bulk copy
 // instead of converting the fp32 codebook itself.  Codebooks of up to 256 centroids are one slice
 // held in shared memory for the whole launch.  Codebooks of 1024 centroids (WIDE) do not fit: their
 // operands are 128-centroid slices that the producer streams through one shared-memory buffer for
-// every tile, and the argmin runs slice by slice over two 128-column TMEM halves per epilogue group.  The cluster sums then come
-// from a stable counting sort of the super-chunk's assignments and one warp per centroid adding its
-// members' rows in token order (no one-hot matrix: it would not fit).
+// every tile, and the argmin runs slice by slice over two 128-column TMEM halves per epilogue
+// group.  Their cluster sums come from a stable counting sort of the super-chunk's assignments and
+// one warp per centroid adding its members' rows in token order (a one-hot matrix would not fit).
 // All waits are bounded; on expiry the kernel records QWM_ERR_DEVICE_TIMEOUT and stops.
 #include "qwm_internal.cuh"
 #include "tc.cuh"
@@ -51,7 +51,7 @@ struct KmSmem {  // offsets from a 1024-aligned base, for a codebook of C centro
     const int CB = wide ? kSlice : C;  // centroids held in shared memory at once
     bh = 0;                        // 2 blocks of [CB][64] bf16 (hi)
     bl = bh + 2 * CB * 128;        // 2 blocks of [CB][64] bf16 (lo)
-    // resident: the codebook area doubles as the two one-hot buffers of the cluster sums
+    // resident: the codebook area doubles as the four one-hot buffers of the cluster sums
     const int onehot = wide ? 0 : 2 * ((C + 127) / 128) * 2 * TILE * 128;
     x = 4 * CB * 128 > onehot ? 4 * CB * 128 : onehot;  // 2 stages x 2 blocks of [128][64]
     norm = x + 2 * 2 * TILE * 128; // C floats
@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
   extern __shared__ __align__(16) unsigned char smem_raw[];
   unsigned char *sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ uint64_t x_full[2], x_empty[2], t_full[2], t_empty[2], drain;
-  __shared__ uint64_t p2_full[2], p2_empty[2], a_full[2], a_empty[2], p2_done;
+  __shared__ uint64_t p2_full[2], p2_empty[2], a_full[4], a_empty[4], p2_done;
   __shared__ uint64_t tw_full[4], tw_empty[4], sl_full, sl_empty;  // WIDE: TMEM halves, slice buffer
   __shared__ uint64_t cb_full;  // operands and norms of the codebook
   __shared__ uint32_t tmem_base_sh;
@@ -144,7 +144,9 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
       tc::mbar_init(&t_empty[i], 4);
       tc::mbar_init(&p2_full[i], 1);
       tc::mbar_init(&p2_empty[i], 1);
-      tc::mbar_init(&a_full[i], kThreads / 32 - 2);
+    }
+    for (int i = 0; i < 4; i++) {
+      tc::mbar_init(&a_full[i], 2);  // the two warps that build buffer i
       tc::mbar_init(&a_empty[i], 1);
     }
     for (int i = 0; i < 4; i++) {
@@ -338,6 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
         asg[i * TILE + row] = (uint8_t)arg;
       }
     }
+    __syncwarp();  // idle lanes of the TMA and MMA warps wait for lane 0 here
     __syncthreads();
     if (*abort_v) break;
     g_tile += nt;
@@ -406,22 +409,26 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
       continue;
     }
     // ---- phase 2: cluster sums of this super-chunk on the tensor cores ----
-    // sums[C][D] = A^T X accumulated over the tiles, A = the tile's one-hot assignment matrix
-    // ([C][128 tokens] bf16, 1 where token t belongs to cluster j), X = the token tile ([tokens][D],
-    // read as an N-major B operand); M = 128 centroids per MMA (two MMAs for C = 256) into TMEM
-    // columns 0 .. C-1 (lane = centroid mod 128).  The one-hot matrices (two buffers) live over the
-    // codebook area; the token tiles stream through the token stages again (TMA).
-    const int Mb = (C + 127) / 128;              // 128-centroid blocks
-    const uint32_t aBytes = (uint32_t)Mb * 2u * TILE * 128u;  // one one-hot buffer
-    for (int e = tid; e < (int)(2u * aBytes / 16u); e += kThreads) *(uint4 *)(sm + 16 * e) = make_uint4(0, 0, 0, 0);
+    // sums[C][D] = A^T X accumulated over half-tiles of 64 tokens, A = the half-tile's one-hot
+    // assignment matrix ([C][64 tokens] bf16, 1 where token t belongs to cluster j), X = the token
+    // rows ([tokens][D], read as an N-major B operand); M = 128 centroids per MMA (two MMAs for
+    // C = 256) into TMEM columns 0 .. C-1 (lane = centroid mod 128).  The one-hot matrices live in
+    // kOneHot buffers over the codebook area, each written by its own pair of warps, so that
+    // building one half-tile's matrix overlaps the MMAs of the others; the token tiles stream
+    // through the token stages again (TMA).
+    constexpr int kOneHot = 4;
+    const int Mb = (C + 127) / 128;                         // 128-centroid blocks
+    const uint32_t aBytes = (uint32_t)Mb * TILE * 128u;     // one one-hot buffer: Mb x [128][64 tokens]
+    for (int e = tid; e < (int)(kOneHot * aBytes / 16u); e += kThreads) *(uint4 *)(sm + 16 * e) = make_uint4(0, 0, 0, 0);
     for (int j = tid; j < C; j += kThreads) cnts[j] = 0;
     tc::fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    auto onehot_off = [&](int j, int t) -> uint32_t {  // byte offset of A[j][t] inside a buffer
-      return (uint32_t)(j >> 7) * 2u * TILE * 128u + (uint32_t)(t >> 6) * TILE * 128u + tc::sw128_offset(j & 127, t & 63);
+    auto onehot_off = [&](int j, int t) -> uint32_t {  // byte offset of A[j][t] inside a buffer (t < 64)
+      return (uint32_t)(j >> 7) * TILE * 128u + tc::sw128_offset(j & 127, t);
     };
+    const int64_t u0 = 2 * g2;  // half-tiles before this super-chunk (barrier phases)
     if (warp == 0) {
       if (lane == 0) {  // TMA: token tiles
         for (int i = 0; i < nt && !*abort_v; i++) {
@@ -440,62 +447,67 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
       }
     } else if (warp == 1) {
       if (lane == 0) {  // MMA: sums += A^T X
-        const uint32_t idesc = tc::idesc_bf16_f32(TILE, D) | (1u << 16);  // B (token tile) N-major
+        const uint32_t idesc = tc::idesc_bf16_f32(TILE, D) | (1u << 16);  // B (token rows) N-major
         const uint32_t sx = tc::smem_u32(sm + L.x), sa = tc::smem_u32(sm);
         for (int i = 0; i < nt && !*abort_v; i++) {
           const int64_t g = g2 + i;
           const int s = (int)(g & 1);
-          if (!tc::mbar_wait(&p2_full[s], (uint32_t)((g >> 1) & 1), kWaitNs) ||
-              !tc::mbar_wait(&a_full[s], (uint32_t)((g >> 1) & 1), kWaitNs)) {
-            *abort_v = 1;
-            break;
-          }
-          tc::fence_after_sync();
-          for (int mb = 0; mb < Mb; mb++) {
+          if (!tc::mbar_wait(&p2_full[s], (uint32_t)((g >> 1) & 1), kWaitNs)) { *abort_v = 1; break; }
+          for (int hh = 0; hh < 2; hh++) {
+            const int64_t U = u0 + 2 * i + hh;
+            const int b = (int)(U % kOneHot);
+            if (!tc::mbar_wait(&a_full[b], (uint32_t)((U / kOneHot) & 1), kWaitNs)) { *abort_v = 1; break; }
+            tc::fence_after_sync();
+            for (int mb = 0; mb < Mb; mb++) {
 #pragma unroll
-            for (int kk = 0; kk < TILE / 16; kk++) {  // 16 tokens per K step
-              const uint32_t ao = sa + (uint32_t)s * aBytes + (uint32_t)mb * 2u * TILE * 128u +
-                                  (uint32_t)(kk / 4) * TILE * 128u + 32u * (kk % 4);
-              const uint32_t bo = sx + (uint32_t)s * 2u * TILE * 128u + 2048u * kk;
-              tc::mma_ss(tmem + 128u * mb, tc::desc_sw128(ao), tc::desc_sw128_mn(bo, TILE * 128, 1024), idesc,
-                         (i > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < 4; kk++) {  // 16 tokens per K step
+                const uint32_t ao = sa + (uint32_t)b * aBytes + (uint32_t)mb * TILE * 128u + 32u * kk;
+                const uint32_t bo = sx + (uint32_t)s * 2u * TILE * 128u + 2048u * (4 * hh + kk);
+                tc::mma_ss(tmem + 128u * mb, tc::desc_sw128(ao), tc::desc_sw128_mn(bo, TILE * 128, 1024), idesc,
+                           (i > 0 || hh > 0 || kk > 0) ? 1u : 0u);
+              }
             }
+            tc::mma_commit(&a_empty[b]);
           }
+          if (*abort_v) break;
           tc::mma_commit(&p2_empty[s]);
-          tc::mma_commit(&a_empty[s]);
         }
         tc::mma_commit(&p2_done);
       }
-    } else {  // warps 2-9 build the one-hot matrices: thread = token of the tile (128 of 256)
-      const int bt = tid - 64;
-      for (int i = 0; i < nt; i++) {
-        const int64_t g = g2 + i;
-        const int s = (int)(g & 1);
-        const bool ok = g < 2 || tc::mbar_wait(&a_empty[s], (uint32_t)(((g >> 1) - 1) & 1), kWaitNs);
+    } else {  // warps 2-9: warp pair b builds the one-hot matrices of buffer b; thread = token
+      const int b = (warp - 2) >> 1, lt = ((warp - 2) & 1) * 32 + lane;
+      int u = (int)(((b - u0) % kOneHot + kOneHot) % kOneHot);  // this super-chunk's first half-tile in buffer b
+      for (; u < 2 * nt; u += kOneHot) {
+        const int64_t U = u0 + u;
+        const bool ok = U < kOneHot || tc::mbar_wait(&a_empty[b], (uint32_t)(((U / kOneHot) - 1) & 1), kWaitNs);
         if (__any_sync(0xffffffffu, !ok || *abort_v != 0)) {  // warp-uniform exit
           *abort_v = 1;
           break;
         }
-        unsigned char *abuf = sm + (uint32_t)s * aBytes;
-        const int64_t tok0 = (sc0 + i) * TILE;
-        const int rows = (int)((p.n - tok0) < TILE ? (p.n - tok0) : TILE);
-        if (bt < TILE) {
-          if (i >= 2) {  // clear this buffer's ones of two tiles ago (same super-chunk)
-            const int64_t tokp = (sc0 + i - 2) * TILE;
-            const int rowsp = (int)((p.n - tokp) < TILE ? (p.n - tokp) : TILE);
-            if (bt < rowsp) *(uint16_t *)(abuf + onehot_off(asg[(i - 2) * TILE + bt], bt)) = 0;
-          }
-          if (bt < rows) {
-            const int j = asg[i * TILE + bt];
-            *(uint16_t *)(abuf + onehot_off(j, bt)) = 0x3F80u;  // bf16 1.0
-            atomicAdd(cnts + j, 1);
-          }
+        unsigned char *abuf = sm + (uint32_t)b * aBytes;
+        const int bt = 64 * (u & 1) + lt;                 // token within its tile
+        if (u >= kOneHot) {  // clear this buffer's ones of its previous half-tile (same super-chunk)
+          const int up = u - kOneHot;
+          const int64_t tokp = (sc0 + (up >> 1)) * TILE;
+          const int rowsp = (int)((p.n - tokp) < TILE ? (p.n - tokp) : TILE);
+          const int btp = 64 * (up & 1) + lt;
+          if (btp < rowsp) *(uint16_t *)(abuf + onehot_off(asg[(up >> 1) * TILE + btp], lt)) = 0;
         }
+        const int64_t tok0 = (sc0 + (u >> 1)) * TILE;
+        const int rows = (int)((p.n - tok0) < TILE ? (p.n - tok0) : TILE);
+        const bool valid = bt < rows;
+        const int j = valid ? asg[(u >> 1) * TILE + bt] : -1 - lane;
+        if (valid) *(uint16_t *)(abuf + onehot_off(j, lt)) = 0x3F80u;  // bf16 1.0
+        const uint32_t peers = __match_any_sync(0xffffffffu, j);  // one count update per cluster
+        if (valid && (peers & ((1u << lane) - 1u)) == 0) atomicAdd(cnts + j, __popc(peers));
         tc::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&a_full[s]);
+        if (lane == 0) tc::mbar_arrive(&a_full[b]);
       }
     }
+    // the idle lanes of the TMA and MMA warps wait here for lane 0, not in the spin below: a lane
+    // polling an mbarrier holds up the diverged lane 0 of its own warp
+    __syncwarp();
     g2 += nt;
     if (!*abort_v && !tc::mbar_wait(&p2_done, (uint32_t)(n_sc & 1), kWaitNs)) *abort_v = 1;
     n_sc++;

@@ -845,6 +845,7 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
       if (lane == 0) tc::mbar_arrive(&x_empty[s]);
     }
   }
+  __syncwarp();  // idle lanes of the TMA and MMA warps wait for lane 0 here
   __syncthreads();
   if (*abort_v && tid == 0) qwm_dev_error(p.status, QWM_ERR_DEVICE_TIMEOUT);
   tc::fence_before_sync();
