@@ -241,7 +241,7 @@ def run_ours(args, rank, world, device):
         ev[4].record(stream)
 
     # kernels launched per step (counted from the library's launch sequence):
-    # statistics 3 (partial sums, finish, Jacobi); each fit 1 + 2 x iterations (assign, update);
+    # statistics 3 (partial sums, finish, eigensolver); each fit 1 + 2 x iterations (assign, update);
     # packing 3 (fp16 codebook copies, Keys, Values); attention 1
     launches_per_step = 3 + 2 * (1 + 2 * 10) + 3 + 1
 

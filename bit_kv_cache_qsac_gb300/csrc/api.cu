@@ -11,7 +11,7 @@ constexpr int kStatsSplits = 8;
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
-  size_t status, stats_part, km_sum, km_cnt, km_cent, jac_basis, jac_valid, km_img, q_img, q_bfull, total;
+  size_t status, stats_part, km_sum, km_cnt, km_cent, km_img, q_img, q_bfull, total;
 };
 
 Layout layout_of(const qwm_config &c) {
@@ -23,8 +23,6 @@ Layout layout_of(const qwm_config &c) {
   L.km_sum = off; off = align_up(off + G * c.heads * c.n_centroids * QWM_D * sizeof(float), 256);
   L.km_cnt = off; off = align_up(off + G * c.heads * c.n_centroids * sizeof(int32_t), 256);
   L.km_cent = off; off = align_up(off + (size_t)c.heads * c.n_centroids * QWM_D * sizeof(float), 256);
-  L.jac_basis = off; off = align_up(off + (size_t)c.heads * QWM_D * QWM_D * sizeof(float), 256);
-  L.jac_valid = off; off = align_up(off + (size_t)c.heads * sizeof(int32_t), 256);
   L.km_img = off; off = align_up(off + kmeans_image_bytes(c.heads, c.n_centroids), 1024);
   L.q_img = off; off = align_up(off + quantize_image_bytes(c.heads, c.n_centroids), 1024);
   L.q_bfull = off; off = align_up(off + (size_t)c.heads * c.n_centroids * QWM_D * sizeof(float), 256);
@@ -147,8 +145,6 @@ qwm_status qwm_create(const qwm_config *cfg, qwm_ctx **out) {
   ctx->km_sum = (float *)(base + L.km_sum);
   ctx->km_cnt = (int32_t *)(base + L.km_cnt);
   ctx->km_cent = (float *)(base + L.km_cent);
-  ctx->jac_basis = (float *)(base + L.jac_basis);
-  ctx->jac_valid = (int32_t *)(base + L.jac_valid);
   ctx->km_img = (unsigned char *)(base + L.km_img);
   ctx->q_img = (unsigned char *)(base + L.q_img);
   ctx->q_bfull = (float *)(base + L.q_bfull);
@@ -181,7 +177,7 @@ qwm_status qwm_update_query_stats(qwm_ctx *ctx, const uint16_t *q, int64_t nq, f
   if (nq > 0) e = launch_stats_partial(q, nq, H, ctx->stats_part, splits, ctx->status, st);
   if (e == cudaSuccess) e = launch_stats_finish(ctx->stats_part, nq > 0 ? splits : 0, nq, H, S, n, w, st);
   if (e == cudaSuccess)
-    e = launch_jacobi(S, n, nq, H, ctx->cfg.rank, eigvals, u_r, ctx->status, ctx->jac_basis, ctx->jac_valid, st);
+    e = launch_eig(S, n, nq, H, ctx->cfg.rank, eigvals, u_r, ctx->status, st);
   return cuda_status(e);
 }
 

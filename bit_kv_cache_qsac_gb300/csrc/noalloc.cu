@@ -1,8 +1,8 @@
 // qwm_update_query_stats_noalloc: the Query statistics / weights / basis update of
 // qwm_update_query_stats for callers that cannot allocate device memory.
 //
-// The scratch the kernels need (per-split partial sums of q q^T and the eigensolver's basis and
-// flags) lives in one file-scope device array of fixed size instead of a context's workspace.
+// The scratch the kernels need (per-split partial sums of q q^T) lives in one file-scope device
+// array of fixed size instead of a context's workspace.
 // Every GPU that loads this library holds that array until the process exits.  Host code only
 // ever passes the array's device address, obtained once per device with cudaGetSymbolAddress.
 #include <mutex>
@@ -14,8 +14,7 @@ namespace {
 constexpr int kMaxHeads = 64;  // largest head count this entry point accepts
 constexpr int kSplits = 2;     // partial sums per head
 constexpr size_t kPartFloats = (size_t)kSplits * kMaxHeads * QWM_D * QWM_D;  // 8 MiB
-constexpr size_t kBasisFloats = (size_t)kMaxHeads * QWM_D * QWM_D;           // 4 MiB
-constexpr size_t kScratchBytes = (kPartFloats + kBasisFloats) * sizeof(float) + kMaxHeads * sizeof(int32_t);
+constexpr size_t kScratchBytes = kPartFloats * sizeof(float);
 
 static __device__ __align__(256) unsigned char g_stats_scratch[kScratchBytes];
 
@@ -56,16 +55,12 @@ extern "C" qwm_status qwm_update_query_stats_noalloc(const qwm_config *cfg, cons
   unsigned char *base = nullptr;
   qwm_status s = scratch_on_current_device(&base);
   if (s != QWM_OK) return s;
-  float *part = (float *)base;
-  float *basis = part + kPartFloats;
-  int32_t *valid = (int32_t *)(basis + kBasisFloats);
+  float *part = (float *)base;  // overwritten in full by every call
   cudaStream_t st = (cudaStream_t)stream;
   const int H = cfg->heads;
-  // the eigensolver starts from the identity on every call: clear the basis flags left by the
-  // previous call (the partial sums are overwritten in full by every call)
-  cudaError_t e = cudaMemsetAsync(valid, 0, (size_t)H * sizeof(int32_t), st);
-  if (e == cudaSuccess && nq > 0) e = launch_stats_partial(q, nq, H, part, kSplits, dev_status, st);
+  cudaError_t e = cudaSuccess;
+  if (nq > 0) e = launch_stats_partial(q, nq, H, part, kSplits, dev_status, st);
   if (e == cudaSuccess) e = launch_stats_finish(part, nq > 0 ? kSplits : 0, nq, H, S, n, w, st);
-  if (e == cudaSuccess) e = launch_jacobi(S, n, nq, H, cfg->rank, eigvals, u_r, dev_status, basis, valid, st);
+  if (e == cudaSuccess) e = launch_eig(S, n, nq, H, cfg->rank, eigvals, u_r, dev_status, st);
   return e == cudaSuccess ? QWM_OK : QWM_ERR_CUDA;
 }

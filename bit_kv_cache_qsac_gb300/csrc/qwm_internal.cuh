@@ -27,8 +27,6 @@ struct qwm_ctx {
   float *km_sum;         // [H][G][C][d] k-means per-CTA cluster sums (G CTAs per head)
   int32_t *km_cnt;       // [H][G][C] k-means per-CTA cluster counts
   float *km_cent;        // [H][C][d] fp32 centroids during the iterations
-  float *jac_basis;      // [H][d][d] last eigenbasis per head (Jacobi warm start)
-  int32_t *jac_valid;    // [H] 1 once jac_basis holds a basis
   unsigned char *km_img; // 1024-centroid codebooks: k-means operand slices + norms
   unsigned char *q_img;  // 1024-centroid codebooks: quantiser operand slices + maxima
   float *q_bfull;        // full-form ranking: b_j = M mu_j [H][C][d]
@@ -80,8 +78,8 @@ cudaError_t launch_stats_partial(const uint16_t *q, int64_t nq, int H, float *pa
                                  cudaStream_t st);
 cudaError_t launch_stats_finish(const float *part, int splits, int64_t nq, int H, float *S, int64_t *n, float *w,
                                 cudaStream_t st);
-cudaError_t launch_jacobi(const float *S, int64_t *n, int64_t nq, int H, int rank, float *eigvals, uint16_t *u_r,
-                          int32_t *status, float *basis, int32_t *valid, cudaStream_t st);
+cudaError_t launch_eig(const float *S, int64_t *n, int64_t nq, int H, int rank, float *eigvals, uint16_t *u_r,
+                       int32_t *status, cudaStream_t st);
 #define QWM_MAX_SMS 192  // workspace sizing bound on the SM count
 int kmeans_ctas_per_head(int H, int num_sms);
 size_t kmeans_image_bytes(int H, int C);

@@ -9,9 +9,10 @@
 //   stats_partial_kernel  grid (splits, H): each CTA sums q q^T over a slice of the Queries
 //                         on the tensor cores into a private fp32 partial (no atomics).
 //   stats_finish_kernel   adds the partials to S in a fixed order and writes w.
-//   jacobi_kernel         one CTA per head: parallel cyclic Jacobi on the 128x128 M_h in
-//                         shared memory (round-robin pairing, 64 disjoint rotations per
-//                         round), then sort, sign convention, U_r to bf16.
+//   eig_kernel            one CTA per head: Householder tridiagonalisation of M_h in shared
+//                         memory, all eigenvalues by multisection on Sturm counts, the top-r
+//                         eigenvectors by inverse iteration and back-transformation, sign
+//                         convention, U_r to bf16.
 #include "qwm_internal.cuh"
 #include "tc.cuh"
 
@@ -35,7 +36,7 @@ __global__ void __launch_bounds__(kStatsThreads, 1) stats_partial_kernel(const u
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
   const int h = blockIdx.y, sp = blockIdx.x, H = gridDim.y;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int64_t tiles = (nq + kStatsTile - 1) / kStatsTile;
   const int64_t per = (tiles + splits - 1) / splits;
   const int64_t t0 = (int64_t)sp * per;
@@ -138,225 +139,289 @@ __global__ void stats_finish_kernel(const float *__restrict__ part, int splits, 
   }
 }
 
-constexpr int kJacThreads = 512;
-constexpr int LD = D + 4;  // padded row stride of the shared matrices (16-byte aligned rows)
-constexpr int NP = D / 2;  // disjoint pairs per round
-constexpr int kMaxSweeps = 30;
-// rotate (p,q) while |a_pq| > kRotTol sqrt(|a_pp a_qq|) ...: a left-over off-diagonal entry at
-// that level moves an eigenvalue by at most about 1e-5 of its size (the noise eigenvalues form a
-// near-degenerate cluster, where the move is first order) and a well-separated eigenvector by
-// far less
-constexpr float kRotTol = 1e-5f;
-constexpr float kAbsTol = 1.2e-7f;  // ... and |a_pq| > kAbsTol ||A||_F (fp32 rounding level of A)
+constexpr int kEigThreads = 512;
+constexpr int LDA = D + 1;     // odd row stride: conflict-free row and column access
+constexpr int kRounds = 14;    // multisection rounds: the Gershgorin interval shrinks 5x per round
+constexpr int LU = 4 * D + 1;  // per-vector scratch of the tridiagonal solve (padded across banks)
 
-// C = op(X) Y for 128x128 shared matrices (row stride LD), op(X) = X or X^T; 512 threads, each
-// owning an 8x4 block of C.
-__device__ __forceinline__ void smem_gemm128(const float *X, bool transX, const float *Y, float *Cm) {
-  const int tid = threadIdx.x, ty = tid / 32, tx = tid % 32;
-  float acc[8][4];
+__device__ __forceinline__ float warp_sum_f(float s) {
 #pragma unroll
-  for (int i = 0; i < 8; i++)
-#pragma unroll
-    for (int j = 0; j < 4; j++) acc[i][j] = 0.f;
-  for (int k = 0; k < D; k++) {
-    float a[8];
-#pragma unroll
-    for (int i = 0; i < 8; i++) a[i] = transX ? X[k * LD + 8 * ty + i] : X[(8 * ty + i) * LD + k];
-    const float4 b = *(const float4 *)(Y + k * LD + 4 * tx);
-#pragma unroll
-    for (int i = 0; i < 8; i++) {
-      acc[i][0] = fmaf(a[i], b.x, acc[i][0]);
-      acc[i][1] = fmaf(a[i], b.y, acc[i][1]);
-      acc[i][2] = fmaf(a[i], b.z, acc[i][2]);
-      acc[i][3] = fmaf(a[i], b.w, acc[i][3]);
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < 8; i++)
-    *(float4 *)(Cm + (8 * ty + i) * LD + 4 * tx) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return s;
 }
 
-// basis: [H][D][D] fp32 workspace holding each head's last full eigenbasis (columns sorted),
-// valid: [H] flags.  When valid, the rotations start from that basis: A = U^T M U is nearly
-// diagonal when the statistics moved little since the previous chunk, so few sweeps are needed.
-__global__ void __launch_bounds__(kJacThreads) jacobi_kernel(const float *__restrict__ S, int64_t *__restrict__ n,
-                                                             int64_t nq, int rank, float *__restrict__ eigvals,
-                                                             uint16_t *__restrict__ u_r, int32_t *status,
-                                                             float *__restrict__ basis, int32_t *__restrict__ valid) {
-  extern __shared__ __align__(16) float jsm[];
-  float *A = jsm;               // [D][LD]
-  float *V = jsm + D * LD;      // [D][LD]
-  float *T = jsm + 2 * D * LD;  // [D][LD] scratch for the warm start
-  __shared__ float cs[NP], sn[NP];
-  __shared__ int pp[NP], qq[NP];
-  __shared__ int order[D];
-  __shared__ int rotated;
-  const int h = blockIdx.x, tid = threadIdx.x;
+// Deterministic start vector of inverse iteration k (entries in [-0.5, 0.5)): a different vector per
+// k, so that eigenvalues closer than the solve can separate still give independent vectors.
+__device__ __forceinline__ float start_entry(int i, int k) {
+  uint32_t x = (uint32_t)(i + 1) * 2654435761u ^ (uint32_t)(k + 1) * 40503u;
+  x ^= x >> 15; x *= 2246822519u; x ^= x >> 13; x *= 3266489917u; x ^= x >> 16;
+  return (float)(x >> 8) * (1.0f / 16777216.0f) - 0.5f;
+}
+
+// One CTA per head.  Eigenvalues of M = S / n, descending, and the top-r eigenvectors:
+//  1. Householder reduction of M to a symmetric tridiagonal T = Q^T M Q (Golub & Van Loan,
+//     Algorithm 8.3.1, with the reflector of Algorithm 5.1.1): 126 reflections in shared memory;
+//     reflector k is kept in row k of the matrix for step 4.
+//  2. Every eigenvalue of T by multisection on Sturm counts (the number of negative pivots of
+//     T - x I): four threads per eigenvalue test four interior points per round.
+//  3. Inverse iteration on T for each of the r largest eigenvalues (two solves with partial
+//     pivoting, each from its own start vector), then modified Gram-Schmidt within clusters of
+//     eigenvalues closer than 1e-3 ||T||.
+//  4. Back-transformation u = Q z (one warp per vector) and the sign convention: the largest-
+//     magnitude component is made positive, the lowest channel on ties.
+__global__ void __launch_bounds__(kEigThreads) eig_kernel(const float *__restrict__ S, int64_t *__restrict__ n,
+                                                          int64_t nq, int rank, float *__restrict__ eigvals,
+                                                          uint16_t *__restrict__ u_r, int32_t *status) {
+  extern __shared__ __align__(16) float esm[];
+  float *A = esm;                    // [D][LDA]
+  float *lu = A + D * LDA;           // [QWM_MAX_RANK][LU]: solve scratch, then the vectors z
+  __shared__ float dg[D], e2[D], ev[D], tau[D], vv[D], pv[D], wv[D], lam[D];
+  __shared__ float sc[4];            // tau_k, 1 / v0, K; Gershgorin and pivot bounds below
+  __shared__ float gs[3];
+  __shared__ int bad;
+  const int h = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t nn = n[h] + nq;
   if (nn == 0) {  // cold start: no statistics yet
-    for (int i = tid; i < D; i += kJacThreads) eigvals[(int64_t)h * D + i] = 0.f;
-    for (int i = tid; i < D * rank; i += kJacThreads) u_r[(int64_t)h * D * rank + i] = 0;
+    for (int i = tid; i < D; i += kEigThreads) eigvals[(int64_t)h * D + i] = 0.f;
+    for (int i = tid; i < D * rank; i += kEigThreads) u_r[(int64_t)h * D * rank + i] = 0;
     return;
   }
   const float inv = (float)(1.0 / (double)nn);
-  const bool warm = valid[h] != 0;
-  float *Bh = basis + (int64_t)h * D * D;
-  for (int i = tid; i < D * D; i += kJacThreads) {
-    const int r = i / D, c = i % D;
-    A[r * LD + c] = S[(int64_t)h * D * D + i] * inv;
-    V[r * LD + c] = warm ? Bh[i] : ((r == c) ? 1.f : 0.f);
-  }
+  for (int i = tid; i < D * D; i += kEigThreads) A[(i / D) * LDA + i % D] = S[(int64_t)h * D * D + i] * inv;
+  if (tid == 0) bad = 0;
   __syncthreads();
-  if (warm) {  // A <- V^T A V, symmetrised
-    smem_gemm128(A, false, V, T);
-    __syncthreads();
-    smem_gemm128(V, true, T, A);
-    __syncthreads();
-    for (int i = tid; i < D * D; i += kJacThreads) {
-      const int r = i / D, c = i % D;
-      if (r < c) {
-        const float m = 0.5f * (A[r * LD + c] + A[c * LD + r]);
-        A[r * LD + c] = m;
-        A[c * LD + r] = m;
-      }
-    }
-    __syncthreads();
-  }
-  // ||A||_F, reduced in a fixed order: off-diagonal entries at the rounding level of A carry no
-  // information and would otherwise keep the sweeps going on rotation noise
-  __shared__ float fro_part[kJacThreads / 32];
-  __shared__ float abs_tol;
-  {
-    float f = 0.f;
-    for (int i = tid; i < D * D; i += kJacThreads) {
-      const float a = A[(i / D) * LD + i % D];
-      f = fmaf(a, a, f);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) f += __shfl_xor_sync(0xffffffffu, f, o);
-    if ((tid & 31) == 0) fro_part[tid / 32] = f;
-    __syncthreads();
-    if (tid == 0) {
-      float t = 0.f;
-      for (int w = 0; w < kJacThreads / 32; w++) t += fro_part[w];
-      abs_tol = kAbsTol * sqrtf(t);
-    }
-    __syncthreads();
-  }
-  const float atol = abs_tol;
-  bool converged = false;
-  for (int sweep = 0; sweep < kMaxSweeps; sweep++) {
-    if (tid == 0) rotated = 0;
-    __syncthreads();
-    for (int round = 0; round < D - 1; round++) {
-      if (tid < NP) {
-        // round-robin ("circle") schedule: player D-1 is fixed, the others rotate
-        int a, b;
-        if (tid == 0) { a = D - 1; b = round; }
-        else { a = (round + tid) % (D - 1); b = (round - tid + (D - 1)) % (D - 1); }
-        const int p = min(a, b), qd = max(a, b);
-        const float apq = A[p * LD + qd], app = A[p * LD + p], aqq = A[qd * LD + qd];
-        float c = 1.f, s = 0.f;
-        if (fabsf(apq) > atol && fabsf(apq) > kRotTol * sqrtf(fabsf(app * aqq))) {
-          // Golub & Van Loan, sym.schur2: the rotation that diagonalises [[app, apq], [apq, aqq]]
-          const float tau = (aqq - app) / (2.f * apq);
-          const float t = (tau >= 0.f ? 1.f : -1.f) / (fabsf(tau) + sqrtf(1.f + tau * tau));
-          c = rsqrtf(1.f + t * t);
-          s = t * c;
-          rotated = 1;
-        }
-        cs[tid] = c; sn[tid] = s; pp[tid] = p; qq[tid] = qd;
-      }
-      __syncthreads();
-      // A <- L A L^T block by block: 2x2 block (P,R) becomes L_P B L_R^T, L = [[c,-s],[s,c]].
-      for (int b = tid; b < NP * NP; b += kJacThreads) {
-        const int P = b / NP, R = b % NP;
-        if (P > R) continue;
-        const float c1 = cs[P], s1 = sn[P], c2 = cs[R], s2 = sn[R];
-        if (s1 == 0.f && s2 == 0.f) continue;
-        const int p1 = pp[P], q1 = qq[P], p2 = pp[R], q2 = qq[R];
-        const float b00 = A[p1 * LD + p2], b01 = A[p1 * LD + q2], b10 = A[q1 * LD + p2], b11 = A[q1 * LD + q2];
-        const float t00 = c1 * b00 - s1 * b10, t01 = c1 * b01 - s1 * b11;
-        const float t10 = s1 * b00 + c1 * b10, t11 = s1 * b01 + c1 * b11;
-        const float n00 = c2 * t00 - s2 * t01, n01 = s2 * t00 + c2 * t01;
-        const float n10 = c2 * t10 - s2 * t11, n11 = s2 * t10 + c2 * t11;
-        if (P == R) {
-          A[p1 * LD + p1] = n00;
-          A[q1 * LD + q1] = n11;
-          A[p1 * LD + q1] = 0.f;
-          A[q1 * LD + p1] = 0.f;
+
+  // ---- 1. tridiagonalisation ----
+  for (int k = 0; k < D - 2; k++) {
+    const int m = D - 1 - k;  // length of the column below the diagonal
+    const float *xk = A + k * LDA + k + 1;
+    if (warp == 0) {
+      float sg = 0.f;
+      for (int j = 1 + lane; j < m; j += 32) sg = fmaf(xk[j], xk[j], sg);
+      sg = warp_sum_f(sg);
+      if (lane == 0) {
+        const float x0 = xk[0];
+        dg[k] = A[k * LDA + k];
+        if (sg == 0.f) {  // already reduced: no reflection
+          sc[0] = 0.f; sc[1] = 0.f; ev[k] = x0;
         } else {
-          A[p1 * LD + p2] = n00; A[p1 * LD + q2] = n01; A[q1 * LD + p2] = n10; A[q1 * LD + q2] = n11;
-          A[p2 * LD + p1] = n00; A[q2 * LD + p1] = n01; A[p2 * LD + q1] = n10; A[q2 * LD + q1] = n11;
+          const float mu = sqrtf(fmaf(x0, x0, sg));
+          const float v0 = x0 <= 0.f ? x0 - mu : -sg / (x0 + mu);
+          sc[0] = 2.f * v0 * v0 / (sg + v0 * v0);
+          sc[1] = 1.f / v0;
+          ev[k] = mu;
         }
+        tau[k] = sc[0];
       }
-      // V <- V L^T (column pairs)
-      for (int i = tid; i < D * NP; i += kJacThreads) {
-        const int row = i / NP, P = i % NP;
-        const float s = sn[P];
-        if (s == 0.f) continue;
-        const float c = cs[P];
-        const int p = pp[P], qd = qq[P];
-        const float vp = V[row * LD + p], vq = V[row * LD + qd];
-        V[row * LD + p] = c * vp - s * vq;
-        V[row * LD + qd] = s * vp + c * vq;
-      }
-      __syncthreads();
     }
-    const bool none = (rotated == 0);
     __syncthreads();
-    if (none) { converged = true; break; }
-  }
-  if (!converged && tid == 0) qwm_dev_error(status, QWM_ERR_NOT_CONVERGED);
-  // descending order, ties to the lower index
-  if (tid < D) {
-    const float li = A[tid * LD + tid];
-    int rk = 0;
-    for (int j = 0; j < D; j++) {
-      const float lj = A[j * LD + j];
-      rk += (lj > li) || (lj == li && j < tid);
+    const float tk = sc[0], iv0 = sc[1];
+    // p = tau A_t v, v = (1, x_1 / v0, ...): four threads per row
+    {
+      const int i = tid >> 2, part = tid & 3;
+      float acc = 0.f;
+      if (i < m && tk != 0.f) {
+        const float *row = A + (k + 1 + i) * LDA + k + 1;
+        for (int j = part; j < m; j += 4) acc = fmaf(row[j], j == 0 ? 1.f : xk[j] * iv0, acc);
+      }
+      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+      if (i < m && part == 0) pv[i] = tk * acc;
     }
-    order[rk] = tid;
-  }
-  __syncthreads();
-  if (tid < D) eigvals[(int64_t)h * D + tid] = A[order[tid] * LD + order[tid]];
-  // top-r eigenvectors: largest-magnitude component made positive (lowest channel on ties)
-  const int warp = tid / 32, lane = tid % 32;
-  for (int k = warp; k < rank; k += kJacThreads / 32) {
-    const int src = order[k];
-    float best = -1.f;
-    int arg = D;
-    for (int c = lane; c < D; c += 32) {
-      const float a = fabsf(V[c * LD + src]);
-      if (a > best) { best = a; arg = c; }
+    __syncthreads();
+    // K = tau / 2 (p . v); w = p - K v
+    if (warp == 0) {
+      float s2 = 0.f;
+      for (int j = lane; j < m; j += 32) {
+        const float v = j == 0 ? 1.f : xk[j] * iv0;
+        vv[j] = v;
+        s2 = fmaf(pv[j], v, s2);
+      }
+      const float K = 0.5f * tk * warp_sum_f(s2);
+      for (int j = lane; j < m; j += 32) wv[j] = pv[j] - K * vv[j];
     }
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ob = __shfl_xor_sync(0xffffffffu, best, off);
-      const int oa = __shfl_xor_sync(0xffffffffu, arg, off);
-      if (ob > best || (ob == best && oa < arg)) { best = ob; arg = oa; }
+    __syncthreads();
+    // A_t -= v w^T + w v^T; row k keeps the reflector
+    if (tk != 0.f) {
+      for (int i = warp; i < m; i += kEigThreads / 32) {
+        const float vi = vv[i], wi = wv[i];
+        float *row = A + (k + 1 + i) * LDA + k + 1;
+        for (int j = lane; j < m; j += 32) row[j] -= fmaf(vi, wv[j], wi * vv[j]);
+      }
     }
-    const float sg = V[arg * LD + src] < 0.f ? -1.f : 1.f;
-    for (int c = lane; c < D; c += 32) u_r[((int64_t)h * D + c) * rank + k] = f32_to_bf16_rn(sg * V[c * LD + src]);
-  }
-  // full basis, sorted and sign-fixed like u_r, for the next call's warm start
-  for (int k = warp; k < D; k += kJacThreads / 32) {
-    const int src = order[k];
-    float best = -1.f;
-    int arg = D;
-    for (int c = lane; c < D; c += 32) {
-      const float a = fabsf(V[c * LD + src]);
-      if (a > best) { best = a; arg = c; }
-    }
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ob = __shfl_xor_sync(0xffffffffu, best, off);
-      const int oa = __shfl_xor_sync(0xffffffffu, arg, off);
-      if (ob > best || (ob == best && oa < arg)) { best = ob; arg = oa; }
-    }
-    const float sg = V[arg * LD + src] < 0.f ? -1.f : 1.f;
-    for (int c = lane; c < D; c += 32) Bh[c * D + k] = sg * V[c * LD + src];
+    for (int j = tid; j < m; j += kEigThreads) A[k * LDA + k + 1 + j] = tk != 0.f ? vv[j] : (j == 0 ? 1.f : 0.f);
+    __syncthreads();
   }
   if (tid == 0) {
-    valid[h] = 1;
+    dg[D - 2] = A[(D - 2) * LDA + D - 2];
+    dg[D - 1] = A[(D - 1) * LDA + D - 1];
+    ev[D - 2] = A[(D - 2) * LDA + D - 1];
+    ev[D - 1] = 0.f;
+    tau[D - 2] = 0.f;
+  }
+  __syncthreads();
+  if (tid < D) e2[tid] = ev[tid] * ev[tid];
+  // Gershgorin interval and the pivot floor of the Sturm counts
+  if (warp == 0) {
+    float lo = INFINITY, hi = -INFINITY, emax = 0.f;
+    for (int i = lane; i < D; i += 32) {
+      const float r = fabsf(ev[i]) + (i > 0 ? fabsf(ev[i - 1]) : 0.f);
+      lo = fminf(lo, dg[i] - r);
+      hi = fmaxf(hi, dg[i] + r);
+      emax = fmaxf(emax, ev[i] * ev[i]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+      emax = fmaxf(emax, __shfl_xor_sync(0xffffffffu, emax, o));
+    }
+    if (lane == 0) {
+      const float span = fmaxf(hi - lo, 1e-30f);
+      gs[0] = lo - 1e-6f * span;
+      gs[1] = hi + 1e-6f * span;
+      gs[2] = 1e-30f * fmaxf(1.f, emax);
+    }
+  }
+  __syncthreads();
+
+  // ---- 2. eigenvalues: thread group of 4 per eigenvalue (ascending index a) ----
+  {
+    const int a = tid >> 2, s = tid & 3;
+    const float pivmin = gs[2];
+    float lo = gs[0], hi = gs[1];
+    for (int r = 0; r < kRounds; r++) {
+      float x[4];
+#pragma unroll
+      for (int u = 0; u < 4; u++) x[u] = lo + (hi - lo) * (0.2f * (float)(u + 1));
+      const float xs = x[s];
+      float qv = dg[0] - xs;
+      if (fabsf(qv) < pivmin) qv = -pivmin;
+      int c = qv < 0.f;
+      for (int i = 1; i < D; i++) {
+        qv = (dg[i] - xs) - __fdividef(e2[i - 1], qv);
+        if (fabsf(qv) < pivmin) qv = -pivmin;
+        c += qv < 0.f;
+      }
+      int cs[4];
+#pragma unroll
+      for (int u = 0; u < 4; u++) cs[u] = __shfl_sync(0xffffffffu, c, (lane & ~3) | u);
+      // eigenvalue a lies in the first sub-interval whose right end counts more than a below it
+      float nlo = lo, nhi = hi;
+      bool found = false;
+#pragma unroll
+      for (int u = 0; u < 4; u++) {
+        if (!found) {
+          if (cs[u] > a) { nhi = x[u]; found = true; }
+          else nlo = x[u];
+        }
+      }
+      lo = nlo;
+      hi = nhi;
+    }
+    if (s == 0) lam[a] = 0.5f * (lo + hi);
+  }
+  __syncthreads();
+  if (tid < D) eigvals[(int64_t)h * D + tid] = lam[D - 1 - tid];
+  if (rank == 0) {
+    if (tid == 0) n[h] = nn;
+    return;
+  }
+  const float tnorm = fmaxf(fabsf(gs[0]), fabsf(gs[1]));
+
+  // ---- 3. inverse iteration, one thread per vector (vector k: k-th largest eigenvalue) ----
+  if (tid < rank) {
+    const int k = tid;
+    const float sh = lam[D - 1 - k], tiny = 1.2e-7f * tnorm;
+    float *dgv = lu + k * LU, *s1 = dgv + D, *s2 = s1 + D, *z = s2 + D;
+    for (int i = 0; i < D; i++) z[i] = start_entry(i, k);
+    for (int it = 0; it < 2; it++) {
+      // Gaussian elimination with partial pivoting of T - sh I; U has two superdiagonals
+      float cd = dg[0] - sh, c1 = ev[0], c2 = 0.f, cr = z[0];
+      for (int i = 0; i < D - 1; i++) {
+        const float sub = ev[i], nd = dg[i + 1] - sh, n1 = (i + 1 < D - 1) ? ev[i + 1] : 0.f, nr = z[i + 1];
+        if (fabsf(sub) > fabsf(cd)) {  // swap rows i and i + 1
+          const float f = cd / sub;
+          dgv[i] = sub; s1[i] = nd; s2[i] = n1; z[i] = nr;
+          cd = c1 - f * nd; c1 = c2 - f * n1; c2 = 0.f; cr = cr - f * nr;
+        } else {
+          if (cd == 0.f) cd = tiny;
+          const float f = sub / cd;
+          dgv[i] = cd; s1[i] = c1; s2[i] = c2; z[i] = cr;
+          cd = nd - f * c1; c1 = n1 - f * c2; c2 = 0.f; cr = nr - f * cr;
+        }
+      }
+      dgv[D - 1] = cd == 0.f ? tiny : cd; s1[D - 1] = 0.f; s2[D - 1] = 0.f; z[D - 1] = cr;
+      float big = 0.f;
+      for (int i = D - 1; i >= 0; i--) {
+        float t = z[i];
+        if (i + 1 < D) t -= s1[i] * z[i + 1];
+        if (i + 2 < D) t -= s2[i] * z[i + 2];
+        const float dd = dgv[i] == 0.f ? tiny : dgv[i];
+        z[i] = t / dd;
+        big = fmaxf(big, fabsf(z[i]));
+      }
+      const float sc2 = big > 0.f && big < INFINITY ? 1.f / big : 0.f;
+      if (sc2 == 0.f) bad = 1;
+      for (int i = 0; i < D; i++) z[i] *= sc2;
+    }
+  }
+  __syncthreads();
+  // modified Gram-Schmidt within clusters, in order of k (warp 0); then unit length
+  if (warp == 0) {
+    for (int k = 0; k < rank; k++) {
+      float *zk = lu + k * LU + 3 * D;
+      for (int j = 0; j < k; j++) {
+        if (fabsf(lam[D - 1 - j] - lam[D - 1 - k]) > 1e-3f * tnorm) continue;
+        const float *zj = lu + j * LU + 3 * D;
+        float dt = 0.f;
+        for (int i = lane; i < D; i += 32) dt = fmaf(zj[i], zk[i], dt);
+        dt = warp_sum_f(dt);
+        for (int i = lane; i < D; i += 32) zk[i] -= dt * zj[i];
+        __syncwarp();
+      }
+      float nr = 0.f;
+      for (int i = lane; i < D; i += 32) nr = fmaf(zk[i], zk[i], nr);
+      nr = warp_sum_f(nr);
+      const float in = nr > 0.f ? rsqrtf(nr) : 0.f;
+      if (nr == 0.f && lane == 0) bad = 1;
+      for (int i = lane; i < D; i += 32) zk[i] *= in;
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+
+  // ---- 4. back-transformation u = H_0 ... H_{D-3} z, one warp per vector; sign; bf16 ----
+  if (warp < rank) {
+    const int k = warp;
+    float *u = lu + k * LU + 3 * D;
+    for (int kk = D - 3; kk >= 0; kk--) {
+      const float t = tau[kk];
+      if (t == 0.f) continue;
+      const float *v = A + kk * LDA + kk + 1;  // reflector kk acts on rows kk+1 .. D-1
+      const int m = D - 1 - kk;
+      float dt = 0.f;
+      for (int j = lane; j < m; j += 32) dt = fmaf(v[j], u[kk + 1 + j], dt);
+      dt = t * warp_sum_f(dt);
+      for (int j = lane; j < m; j += 32) u[kk + 1 + j] -= dt * v[j];
+      __syncwarp();
+    }
+    float best = -1.f;
+    int arg = D;
+    for (int c = lane; c < D; c += 32) {
+      const float a = fabsf(u[c]);
+      if (a > best) { best = a; arg = c; }
+    }
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ob = __shfl_xor_sync(0xffffffffu, best, off);
+      const int oa = __shfl_xor_sync(0xffffffffu, arg, off);
+      if (ob > best || (ob == best && oa < arg)) { best = ob; arg = oa; }
+    }
+    const float sg = u[arg] < 0.f ? -1.f : 1.f;
+    for (int c = lane; c < D; c += 32) u_r[((int64_t)h * D + c) * rank + k] = f32_to_bf16_rn(sg * u[c]);
+  }
+  if (tid == 0) {
+    if (bad) qwm_dev_error(status, QWM_ERR_NOT_CONVERGED);
     n[h] = nn;
   }
 }
@@ -378,12 +443,12 @@ cudaError_t launch_stats_finish(const float *part, int splits, int64_t nq, int H
   return cudaGetLastError();
 }
 
-cudaError_t launch_jacobi(const float *S, int64_t *n, int64_t nq, int H, int rank, float *eigvals, uint16_t *u_r,
-                          int32_t *status, float *basis, int32_t *valid, cudaStream_t st) {
+cudaError_t launch_eig(const float *S, int64_t *n, int64_t nq, int H, int rank, float *eigvals, uint16_t *u_r,
+                       int32_t *status, cudaStream_t st) {
   // n is read here and advanced by n += nq at the end of each head's solve
-  const size_t smem = 3 * D * LD * sizeof(float);
-  cudaError_t e = cudaFuncSetAttribute(jacobi_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const size_t smem = ((size_t)D * LDA + (size_t)QWM_MAX_RANK * LU) * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(eig_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  jacobi_kernel<<<H, kJacThreads, smem, st>>>(S, n, nq, rank, eigvals, u_r, status, basis, valid);
+  eig_kernel<<<H, kEigThreads, smem, st>>>(S, n, nq, rank, eigvals, u_r, status);
   return cudaGetLastError();
 }

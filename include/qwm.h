@@ -21,7 +21,7 @@
  * Conventions (every entry point):
  *  - Returns a qwm_status; no exception or abort crosses the ABI.
  *  - Asynchronous on the caller's stream.  Errors that only the device can see
- *    (a Jacobi solve that ran out of sweeps, a residual out of fp16 range) are
+ *    (an eigenvector that inverse iteration could not form, a residual out of fp16 range) are
  *    recorded in a status word inside the context; qwm_sync_status() waits on
  *    the stream, returns the first recorded error and clears it.
  *  - Every device buffer is owned by the caller.  The library allocates device
@@ -59,7 +59,7 @@ typedef enum {
   QWM_ERR_SHAPE = 2,         /* a size the kernels do not support (see qwm_config) */
   QWM_ERR_ALIGN = 3,         /* a pointer that is not 16-byte aligned */
   QWM_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
-  QWM_ERR_NOT_CONVERGED = 5, /* the Jacobi eigensolver hit its sweep limit (results still written) */
+  QWM_ERR_NOT_CONVERGED = 5, /* the eigensolver could not form an eigenvector (results still written) */
   QWM_ERR_UNSUPPORTED = 6,   /* a configuration this build does not implement */
   QWM_ERR_RANGE = 7,         /* a residual, scale or coefficient outside the fp16 range */
   QWM_ERR_DEVICE_TIMEOUT = 8 /* a kernel's internal wait ran past its time limit and the kernel gave up */
@@ -171,8 +171,10 @@ QWM_API qwm_status qwm_destroy(qwm_ctx *ctx);
  *   u_r      bf16 [H][d][r] out   top-r eigenvectors of M (column k = k-th), rounded to
  *                                 nearest-even; each column's largest-magnitude component
  *                                 is positive.  May be NULL when config.rank == 0.
- * The eigensolver is a parallel cyclic Jacobi method (fp32) with a sweep limit;
- * reaching it records QWM_ERR_NOT_CONVERGED in the status word. */
+ * The eigensolver (fp32, one thread block per head) reduces M to tridiagonal form by Householder
+ * reflections, finds every eigenvalue by bisection on Sturm counts and the top-r eigenvectors by
+ * inverse iteration; an eigenvector whose solve overflowed or vanished records
+ * QWM_ERR_NOT_CONVERGED in the status word. */
 QWM_API qwm_status qwm_update_query_stats(qwm_ctx *ctx, const uint16_t *q, int64_t nq, float *S, int64_t *n,
                                   float *w, float *eigvals, uint16_t *u_r, qwm_stream stream);
 
@@ -248,8 +250,8 @@ QWM_API qwm_status qwm_sync_status(qwm_ctx *ctx, qwm_stream stream);
  * qwm_create allocates the context's workspace.  This call needs no context: it computes
  * exactly what qwm_update_query_stats computes (same arguments, layouts and meaning, with the
  * configuration passed directly) and allocates nothing -- no cudaMalloc, no cudaFree, no
- * allocating library routine.  Its scratch memory (partial sums and the eigensolver's basis) is
- * one fixed array inside the library, about 12 MiB, that every GPU which loads the library
+ * allocating library routine.  Its scratch memory (the partial sums of q q^T) is
+ * one fixed array inside the library, 8 MiB, that every GPU which loads the library
  * keeps until the process exits.
  *   cfg          only heads (1..64), head_dim (128) and rank (0..16) are used; heads > 64 is
  *                rejected with QWM_ERR_SHAPE
@@ -258,8 +260,7 @@ QWM_API qwm_status qwm_sync_status(qwm_ctx *ctx, qwm_stream stream);
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
  * that device current; make that first call before any stream capture.  All calls share the one
  * array and each call leaves its contents behind: calls that can run on the GPU at the same time
- * (on different streams) race on it and must be ordered by the caller.  The eigensolver starts
- * from the identity on every call (no warm start). */
+ * (on different streams) race on it and must be ordered by the caller. */
 QWM_API qwm_status qwm_update_query_stats_noalloc(const qwm_config *cfg, const uint16_t *q, int64_t nq, float *S,
                                                   int64_t *n, float *w, float *eigvals, uint16_t *u_r,
                                                   int32_t *dev_status, qwm_stream stream);
