@@ -17,8 +17,8 @@
 //   warps 2-9 epilogue, two warpgroups taking alternate tiles: thread = token = TMEM lane;
 //             argmin over the C columns (two interleaved chains, lower index on ties)
 // The assignments of up to 4096 tokens stay in shared memory.  Then the cluster sums: the token
-// tiles stream through the token stages again (TMA), pairs of epilogue warps write the one-hot
-// assignment matrix of each 64-token half-tile into one of four buffers over the codebook area, and
+// tiles stream through up to four token stages again (TMA), pairs of epilogue warps write the one-hot
+// assignment matrix of each 64-token half-tile into one of three buffers over the codebook area, and
 // the MMA warp accumulates sums = onehot^T X in TMEM; the CTA adds them to its own slice of the
 // workspace and km_update_kernel reduces the slices in a fixed order.
 // The kernels that produce centroids (kmeans_init_kernel, km_update_kernel) also write the next
@@ -51,7 +51,7 @@ struct KmSmem {  // offsets from a 1024-aligned base, for a codebook of C centro
     const int CB = wide ? kSlice : C;  // centroids held in shared memory at once
     bh = 0;                        // 2 blocks of [CB][64] bf16 (hi)
     bl = bh + 2 * CB * 128;        // 2 blocks of [CB][64] bf16 (lo)
-    // resident: the codebook area doubles as the four one-hot buffers of the cluster sums
+    // resident: the codebook area doubles as the one-hot buffers and extra token stages of the cluster sums
     const int onehot = wide ? 0 : 2 * ((C + 127) / 128) * 2 * TILE * 128;
     x = 4 * CB * 128 > onehot ? 4 * CB * 128 : onehot;  // 2 stages x 2 blocks of [128][64]
     norm = x + 2 * 2 * TILE * 128; // C floats
@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
   extern __shared__ __align__(16) unsigned char smem_raw[];
   unsigned char *sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ uint64_t x_full[2], x_empty[2], t_full[2], t_empty[2], drain;
-  __shared__ uint64_t p2_full[2], p2_empty[2], a_full[4], a_empty[4], p2_done;
+  __shared__ uint64_t p2_full[4], p2_empty[4], a_full[3], a_empty[3], p2_done;
   __shared__ uint64_t tw_full[4], tw_empty[4], sl_full, sl_empty;  // WIDE: TMEM halves, slice buffer
   __shared__ uint64_t cb_full;  // operands and norms of the codebook
   __shared__ uint32_t tmem_base_sh;
@@ -142,12 +142,14 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
       tc::mbar_init(&x_empty[i], 1);
       tc::mbar_init(&t_full[i], 1);
       tc::mbar_init(&t_empty[i], 4);
-      tc::mbar_init(&p2_full[i], 1);
-      tc::mbar_init(&p2_empty[i], 1);
+    }
+    for (int i = 0; i < 3; i++) {
+      tc::mbar_init(&a_full[i], 2);  // the two warps that build one-hot buffer i
+      tc::mbar_init(&a_empty[i], 1);
     }
     for (int i = 0; i < 4; i++) {
-      tc::mbar_init(&a_full[i], 2);  // the two warps that build buffer i
-      tc::mbar_init(&a_empty[i], 1);
+      tc::mbar_init(&p2_full[i], 1);
+      tc::mbar_init(&p2_empty[i], 1);
     }
     for (int i = 0; i < 4; i++) {
       tc::mbar_init(&tw_full[i], 1);
@@ -413,12 +415,19 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
     // assignment matrix ([C][64 tokens] bf16, 1 where token t belongs to cluster j), X = the token
     // rows ([tokens][D], read as an N-major B operand); M = 128 centroids per MMA (two MMAs for
     // C = 256) into TMEM columns 0 .. C-1 (lane = centroid mod 128).  The one-hot matrices live in
-    // kOneHot buffers over the codebook area, each written by its own pair of warps, so that
-    // building one half-tile's matrix overlaps the MMAs of the others; the token tiles stream
-    // through the token stages again (TMA).
-    constexpr int kOneHot = 4;
+    // kOneHot buffers at the start of the codebook area, each written by its own pair of warps, so
+    // that building one half-tile's matrix overlaps the MMAs of the other; the token tiles stream
+    // through the two token stages again (TMA) plus the stages that fit in the rest of the codebook
+    // area (nxs in all: the re-read comes mostly from HBM, and a deeper ring hides its latency).
+    constexpr int kOneHot = 3;
     const int Mb = (C + 127) / 128;                         // 128-centroid blocks
     const uint32_t aBytes = (uint32_t)Mb * TILE * 128u;     // one one-hot buffer: Mb x [128][64 tokens]
+    constexpr uint32_t kStage = 2u * TILE * 128u;           // one token tile
+    const int nxs_extra = L.x > (int)(kOneHot * aBytes) ? (int)(((uint32_t)L.x - kOneHot * aBytes) / kStage) : 0;
+    const int nxs = 2 + (nxs_extra < 2 ? nxs_extra : 2);    // 2 to 4 token stages
+    auto xstage = [&](int s) -> uint32_t {                   // byte offset of token stage s
+      return s < 2 ? (uint32_t)L.x + (uint32_t)s * kStage : kOneHot * aBytes + (uint32_t)(s - 2) * kStage;
+    };
     for (int e = tid; e < (int)(kOneHot * aBytes / 16u); e += kThreads) *(uint4 *)(sm + 16 * e) = make_uint4(0, 0, 0, 0);
     for (int j = tid; j < C; j += kThreads) cnts[j] = 0;
     tc::fence_proxy_async_smem();
@@ -433,14 +442,14 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
       if (lane == 0) {  // TMA: token tiles
         for (int i = 0; i < nt && !*abort_v; i++) {
           const int64_t g = g2 + i;
-          const int s = (int)(g & 1);
-          if (g >= 2 && !tc::mbar_wait(&p2_empty[s], (uint32_t)(((g >> 1) - 1) & 1), kWaitNs)) {
+          const int s = (int)(g % nxs);
+          if (g >= nxs && !tc::mbar_wait(&p2_empty[s], (uint32_t)(((g / nxs) - 1) & 1), kWaitNs)) {
             *abort_v = 1;
             break;
           }
           tc::mbar_arrive_expect_tx(&p2_full[s], 2 * TILE * 128);
           const int row = (int)((int64_t)h * p.n + (sc0 + i) * TILE);
-          unsigned char *dst = sm + L.x + s * 2 * TILE * 128;
+          unsigned char *dst = sm + xstage(s);
           tc::tma_load_2d(dst, &tmap, 0, row, &p2_full[s]);
           tc::tma_load_2d(dst + TILE * 128, &tmap, 64, row, &p2_full[s]);
         }
@@ -448,11 +457,12 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
     } else if (warp == 1) {
       if (lane == 0) {  // MMA: sums += A^T X
         const uint32_t idesc = tc::idesc_bf16_f32(TILE, D) | (1u << 16);  // B (token rows) N-major
-        const uint32_t sx = tc::smem_u32(sm + L.x), sa = tc::smem_u32(sm);
+        const uint32_t sa = tc::smem_u32(sm);
         for (int i = 0; i < nt && !*abort_v; i++) {
           const int64_t g = g2 + i;
-          const int s = (int)(g & 1);
-          if (!tc::mbar_wait(&p2_full[s], (uint32_t)((g >> 1) & 1), kWaitNs)) { *abort_v = 1; break; }
+          const int s = (int)(g % nxs);
+          if (!tc::mbar_wait(&p2_full[s], (uint32_t)((g / nxs) & 1), kWaitNs)) { *abort_v = 1; break; }
+          const uint32_t sx = sa + xstage(s);
           for (int hh = 0; hh < 2; hh++) {
             const int64_t U = u0 + 2 * i + hh;
             const int b = (int)(U % kOneHot);
@@ -462,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
 #pragma unroll
               for (int kk = 0; kk < 4; kk++) {  // 16 tokens per K step
                 const uint32_t ao = sa + (uint32_t)b * aBytes + (uint32_t)mb * TILE * 128u + 32u * kk;
-                const uint32_t bo = sx + (uint32_t)s * 2u * TILE * 128u + 2048u * (4 * hh + kk);
+                const uint32_t bo = sx + 2048u * (4 * hh + kk);
                 tc::mma_ss(tmem + 128u * mb, tc::desc_sw128(ao), tc::desc_sw128_mn(bo, TILE * 128, 1024), idesc,
                            (i > 0 || hh > 0 || kk > 0) ? 1u : 0u);
               }
@@ -474,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
         }
         tc::mma_commit(&p2_done);
       }
-    } else {  // warps 2-9: warp pair b builds the one-hot matrices of buffer b; thread = token
+    } else if (warp < 2 + 2 * kOneHot) {  // warp pair b builds the one-hot matrices of buffer b; thread = token
       const int b = (warp - 2) >> 1, lt = ((warp - 2) & 1) * 32 + lane;
       int u = (int)(((b - u0) % kOneHot + kOneHot) % kOneHot);  // this super-chunk's first half-tile in buffer b
       for (; u < 2 * nt; u += kOneHot) {
