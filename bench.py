@@ -3,11 +3,12 @@
 Workload: 40 heads, head_dim 128, a cache of 24 latent frames x 45 x 80 tokens streamed in
 8 chunks of 3 frames (10,800 tokens).  Seven chunks are packed before timing; one timed
 step is the last chunk step of the stream:
-  1. fold the previous chunk's 10,800 Queries into the statistics, recompute w and U_r;
-  2. fit the new chunk's Key and Value codebooks (256 centroids, 10 Lloyd iterations,
+  1. fit the new chunk's Key and Value codebooks (256 centroids, 10 Lloyd iterations,
      warm-started from the previous chunk's);
-  3. QSAC + INT2 + PSAC packing of the chunk's 10,800 Keys and Values;
-  4. attention of the chunk's 10,800 Queries over all 86,400 packed tokens.
+  2. QSAC + INT2 + PSAC packing of the chunk's 10,800 Keys and Values with the statistics of
+     every earlier chunk's Queries;
+  3. attention of the chunk's 10,800 Queries over all 86,400 packed tokens, and beside it (second
+     stream) the fold of those Queries into the statistics: w and U_r for the next chunk.
 The metric is KV token-heads quantised per second of that whole step (10,800 tokens x 40
 heads per step); the attention's TFLOP/s and the packing's token-heads/s are reported
 beside it with their roofline fractions.
@@ -206,10 +207,11 @@ def run_ours(args, rank, world, device):
     ctx = q.Context(heads=H, n_centroids=W.n_centroids, top_m=W.top_m, rank=RANK, kmeans_iters=10)
     layer = CompressedLayer(ctx, device)
     last = W.n_chunks - 1
-    for t in range(last):                       # history: chunks 1..7 packed, statistics of Q_1..Q_6
+    for t in range(last):                       # history: chunks 1..7 packed, statistics of Q_1..Q_7
         if t > 0:
             layer.fold_queries(Q[t - 1])
         layer.append_chunk(K[t], V[t])
+    layer.fold_queries(Q[last - 1])
     assert layer.check() == 0
     prev = layer.chunks[-1]
     ch = q.Chunk.empty(ctx, N_CHUNK, device)
@@ -219,36 +221,42 @@ def run_ours(args, rank, world, device):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream()
     side = torch.cuda.Stream(device)
-    # events: 0 step start, 1 statistics done (side stream), 2 codebook fits done, 5 both done,
-    # 3 packing done, 4 attention done
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    u_next = layer.u_r                          # basis for the next chunk, written by the statistics
+    # events: 0 step start, 2 codebook fits done, 3 packing done, 1 statistics done (side stream),
+    # 4 step done
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    stats_done = torch.cuda.Event()
+    stats_done.record(stream)
 
-    def step(Qp, Kc, Vc, Qc, o):
-        # the statistics update and the codebook fits are independent: the statistics run on a
-        # second stream beside the fits, and packing waits for both
+    def step(Kc, Vc, Qc, o):
+        # pack the chunk with the statistics folded so far (Queries of the previous chunks), attend
+        # with this chunk's Queries, and fold those into the statistics for the next chunk on a
+        # second stream while the attention runs; the step ends when both are done
         ev[0].record(stream)
-        side.wait_event(ev[0])
-        q.qwm_update_query_stats(ctx, Qp, NQ, layer.S, layer.n, layer.w, layer.eigvals, ch.u_r, side)
-        ev[1].record(side)
         q.qwm_fit_centroids(ctx, Kc, N_CHUNK, prev.cent_k, ch.cent_k, stream)
         q.qwm_fit_centroids(ctx, Vc, N_CHUNK, prev.cent_v, ch.cent_v, stream)
         ev[2].record(stream)
-        stream.wait_event(ev[1])
-        ev[5].record(stream)
+        stream.wait_event(stats_done)
+        ch.u_r.copy_(u_next)                    # the chunk's own snapshot of the basis
         q.qwm_quantize_kv(ctx, Kc, Vc, N_CHUNK, layer.w, ch.u_r, ch, None, stream)
         ev[3].record(stream)
+        side.wait_event(ev[3])                  # w and the basis have been read by the packing
+        q.qwm_update_query_stats(ctx, Qc, NQ, layer.S, layer.n, layer.w, layer.eigvals, u_next, side)
+        ev[1].record(side)
+        stats_done.record(side)
         q.qwm_attend(ctx, Qc, NQ, chunks, scale, o, stream)
+        stream.wait_event(ev[1])
         ev[4].record(stream)
 
     # kernels launched per step (counted from the library's launch sequence):
-    # statistics 3 (partial sums, finish, eigensolver); each fit 1 + 2 x iterations (assign, update);
-    # packing 3 (fp16 codebook copies, Keys, Values); attention 1
-    launches_per_step = 3 + 2 * (1 + 2 * 10) + 3 + 1
+    # each fit 1 + 2 x iterations (init; assign, update); packing 3 (fp16 codebook copies, Keys,
+    # Values); statistics 3 (partial sums, finish, eigensolver); attention 1
+    launches_per_step = 2 * (1 + 2 * 10) + 3 + 3 + 1
 
     clk = ClockSampler(device.index if device.index is not None else 0).__enter__()
     for _ in range(args.warmup):
         flush.zero_()
-        step(Q[last - 1], K[last], V[last], Q[last], out)
+        step(K[last], V[last], Q[last], out)
     torch.cuda.synchronize()
     assert q.qwm_sync_status(ctx) == 0
 
@@ -264,10 +272,10 @@ def run_ours(args, rank, world, device):
     for _ in range(args.steps):
         flush.zero_()                       # L2 flush between steps, outside the events
         torch.cuda.nvtx.range_push("qwm_step")
-        step(Q[last - 1], K[last], V[last], Q[last], out)
+        step(K[last], V[last], Q[last], out)
         torch.cuda.nvtx.range_pop()
         ev[4].synchronize()
-        times = [ev[0].elapsed_time(ev[1]), ev[0].elapsed_time(ev[2]), ev[5].elapsed_time(ev[3]),
+        times = [ev[3].elapsed_time(ev[1]), ev[0].elapsed_time(ev[2]), ev[2].elapsed_time(ev[3]),
                  ev[3].elapsed_time(ev[4])]
         stage += times
         total_ms += ev[0].elapsed_time(ev[4])
@@ -278,13 +286,19 @@ def run_ours(args, rank, world, device):
     assert status == 0, q.qwm_status_string(status)
     ms = total_ms / args.steps
     stage /= args.steps
+    # the statistics update alone (outside the timed steps; in the step it fills the attention's tail)
+    ev[0].record(stream)
+    q.qwm_update_query_stats(ctx, Q[last], NQ, layer.S, layer.n, layer.w, layer.eigvals, u_next, stream)
+    ev[1].record(stream)
+    ev[1].synchronize()
+    stats_alone_ms = ev[0].elapsed_time(ev[1])
 
-    # end to end through the C ABI with host buffers: H2D of the step's inputs (previous Queries,
-    # Keys, Values, Queries) from pinned memory and D2H of the attention output, each step
-    hQp, hK, hV, hQ = pinned(qs[last - 1]), pinned(ks[last]), pinned(vs[last]), pinned(qs[last])
+    # end to end through the C ABI with host buffers: H2D of the step's inputs (Keys, Values,
+    # Queries) from pinned memory and D2H of the attention output, each step
+    hK, hV, hQ = pinned(ks[last]), pinned(vs[last]), pinned(qs[last])
     hO = torch.empty(H, NQ, D, dtype=torch.float32).pin_memory()
-    dQp, dK, dV, dQ = (torch.empty_like(x, device=device) for x in (hQp, hK, hV, hQ))
-    h2d = sum(x.numel() * x.element_size() for x in (hQp, hK, hV, hQ))
+    dK, dV, dQ = (torch.empty_like(x, device=device) for x in (hK, hV, hQ))
+    h2d = sum(x.numel() * x.element_size() for x in (hK, hV, hQ))
     d2h = hO.numel() * hO.element_size()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_ms = 0.0
@@ -292,9 +306,9 @@ def run_ours(args, rank, world, device):
     for _ in range(e2e_steps):
         flush.zero_()
         e0.record(stream)
-        for hsrc, ddst in ((hQp, dQp), (hK, dK), (hV, dV), (hQ, dQ)):
+        for hsrc, ddst in ((hK, dK), (hV, dV), (hQ, dQ)):
             ddst.copy_(hsrc, non_blocking=True)
-        step(dQp, dK, dV, dQ, out)
+        step(dK, dV, dQ, out)
         hO.copy_(out, non_blocking=True)
         e1.record(stream)
         e1.synchronize()
@@ -326,8 +340,10 @@ def run_ours(args, rank, world, device):
                    "n_centroids": W.n_centroids, "group": W.group, "top_m": W.top_m, "rank": RANK,
                    "kmeans_iters": 10, "l2": "flushed between steps (256 MiB write, outside the timed events)",
                    "parallelism": f"layer per GPU x{world}"},
-        "stages_ms": {"stats_eig": stage[0], "fit_k_v": stage[1], "quantize": stage[2], "attend": stage[3],
-                      "note": "stats_eig runs on a second stream beside fit_k_v; ms_per_step is start to end"},
+        "stages_ms": {"fit_k_v": stage[1], "quantize": stage[2], "attend": stage[3],
+                      "stats_eig_end_after_quantize": stage[0], "stats_eig_alone": stats_alone_ms,
+                      "note": "the statistics fold the step's Queries for the next chunk on a second stream "
+                              "beside attend, whose tail they fill; ms_per_step is start to end of both"},
         "attend_tflops": attend_tflops,
         "quantize_token_heads_per_s": units / (stage[2] / 1e3),
         "roofline": {"bound": "tensor", "kernel": "attend", "achieved": attend_tflops, "peak": peak_tf,
@@ -678,10 +694,11 @@ def run_ablation_baselines(device, K, V, Q, Qs, Lref, top_ref, ms2_ref):
 
 
 def run_steps(device):
-    """Every step of the streaming layer (720p- or 480p-shaped, --workload): at step t, fold Q_{t-1}
-    into the statistics on a second stream while the chunk's codebooks are fitted, pack chunk t, and
-    attend Q_t over chunks 1..t (the schedule of the timed step).  CUDA events per stage, after a
-    warm-up pass over all steps; the attention's TFLOP/s at 528 flops per (Query, key) pair."""
+    """Every step of the streaming layer (720p- or 480p-shaped, --workload), in the schedule of the
+    timed step: at step t, fit chunk t's codebooks, pack it with the statistics of Q_1..Q_{t-1},
+    attend Q_t over chunks 1..t, and fold Q_t into the statistics on a second stream beside the
+    attention.  CUDA events per stage, after a warm-up pass over all steps; the attention's TFLOP/s
+    at 528 flops per (Query, key) pair."""
     import torch
     import bit_kv_cache_qsac_gb300 as q
     from bit_kv_cache_qsac_gb300.stream import CompressedLayer
@@ -696,21 +713,19 @@ def run_steps(device):
         ctx = q.Context(heads=H, n_centroids=W.n_centroids, top_m=W.top_m, rank=W.rank, kmeans_iters=10)
         layer = CompressedLayer(ctx, device)
         rows = []
+        stats_done = None
         for t in range(T):
-            # 0 start, 1 statistics done (side), 2 fits done, 3 packing done, 4 attention done
+            # 0 start, 2 fits done, 3 packing done, 1 statistics done (side), 4 step done
             ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
             ev[0].record(main)
-            side.wait_event(ev[0])
-            if t > 0:
-                layer.fold_queries(Q[t - 1], side)
-            ev[1].record(side)
             n = K[t].shape[1]
             ch = q.Chunk.empty(ctx, n, device)
             init_k, init_v = (layer.chunks[-1].cent_k, layer.chunks[-1].cent_v) if layer.chunks else (None, None)
             q.qwm_fit_centroids(ctx, K[t], n, init_k, ch.cent_k, main)
             q.qwm_fit_centroids(ctx, V[t], n, init_v, ch.cent_v, main)
             ev[2].record(main)
-            main.wait_event(ev[1])
+            if stats_done is not None:
+                main.wait_event(stats_done)
             psac = layer.n_seen > 0 and ctx.cfg.rank > 0
             if psac:
                 ch.u_r.copy_(layer.u_r)
@@ -718,20 +733,25 @@ def run_steps(device):
                               ch.u_r if psac else None, ch, None, main)
             layer.chunks.append(ch)
             ev[3].record(main)
+            side.wait_event(ev[3])
+            layer.fold_queries(Q[t], side)
+            ev[1].record(side)
+            stats_done = ev[1]
             layer.attend(Q[t], stream=main)
+            main.wait_event(ev[1])
             ev[4].record(main)
             ev[4].synchronize()
-            att = ev[3].elapsed_time(ev[4])
+            step_ms = ev[0].elapsed_time(ev[4])
             pairs = H * NQ * N_CHUNK * (t + 1)
-            rows.append({"step": t + 1, "cache_tokens": N_CHUNK * (t + 1), "stats_eig_ms": ev[0].elapsed_time(ev[1]),
-                         "fit_ms": ev[0].elapsed_time(ev[2]), "pack_ms": ev[2].elapsed_time(ev[3]),
-                         "attend_ms": att, "step_ms": ev[0].elapsed_time(ev[4]),
-                         "attend_tflops": pairs * 528 / (att / 1e3) / 1e12})
+            rows.append({"step": t + 1, "cache_tokens": N_CHUNK * (t + 1), "fit_ms": ev[0].elapsed_time(ev[2]),
+                         "pack_ms": ev[2].elapsed_time(ev[3]), "stats_eig_ms": ev[3].elapsed_time(ev[1]),
+                         "attend_and_stats_ms": ev[3].elapsed_time(ev[4]), "step_ms": step_ms,
+                         "attend_tflops_lower_bound": pairs * 528 / (ev[3].elapsed_time(ev[4]) / 1e3) / 1e12})
         assert layer.check() == 0
         del layer, ctx
     print(json.dumps({"report": "steps", "workload": f"{W.name}-shaped layer", "heads": H, "queries": NQ,
-                      "steps": rows, "note": "statistics on a second stream beside the fits; pack_ms "
-                      "counts from the end of the fits (it also waits for the statistics)"}), flush=True)
+                      "steps": rows, "note": "the statistics of step t's Queries run on a second stream beside "
+                      "its attention (they serve chunk t+1); attend_and_stats_ms spans both"}), flush=True)
 
 
 def run_full_model(device, storage: int = 0):

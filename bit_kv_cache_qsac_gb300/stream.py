@@ -41,6 +41,7 @@ class CompressedLayer:
         self.prev_cent_k = None
         self.prev_cent_v = None
         self._side = None        # second stream for the statistics update of step()
+        self._stats_pending = None  # stream_step(): the fold the next packing waits for
 
     def fold_queries(self, q: torch.Tensor, stream=None) -> None:
         """Step 1: fold Queries [H][nq][d] into the statistics and recompute w and U_r."""
@@ -59,11 +60,13 @@ class CompressedLayer:
         init_v = self.prev_cent_v if warm_start else None
         qwm_fit_centroids(self.ctx, k, n, init_k, ch.cent_k, stream)
         qwm_fit_centroids(self.ctx, v, n, init_v, ch.cent_v, stream)
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
         if stats_done is not None:
-            (stream if stream is not None else torch.cuda.current_stream(self.device)).wait_event(stats_done)
+            s.wait_event(stats_done)
         psac = self.n_seen > 0 and self.ctx.cfg.rank > 0
         if psac:
-            ch.u_r.copy_(self.u_r)   # per-chunk snapshot of the basis
+            with torch.cuda.stream(s):
+                ch.u_r.copy_(self.u_r)   # per-chunk snapshot of the basis
         w = self.w if self.n_seen > 0 else None
         if self.full_query and w is not None:
             M = (self.S / self.n.view(-1, 1, 1).to(self.S.dtype)).contiguous()
@@ -110,6 +113,27 @@ class CompressedLayer:
             done.record(self._side)
         self.append_chunk(k, v, stream=main, stats_done=done)
         return self.attend(q, stream=main)
+
+    def stream_step(self, k, v, q, stream=None) -> torch.Tensor:
+        """One streaming step in pipelined order: pack (k, v) with the statistics of every Query
+        folded so far, attend with q, and fold q into the statistics on a second stream while the
+        attention runs; the next call's packing waits for that fold.  The same work as
+        step(q_prev, k, v, q) with q_prev the previous call's q, with the statistics beside the
+        attention instead of beside the codebook fits."""
+        main = stream if stream is not None else torch.cuda.current_stream(self.device)
+        self.append_chunk(k, v, stream=main, stats_done=self._stats_pending)
+        packed = torch.cuda.Event()
+        packed.record(main)
+        if self._side is None:
+            self._side = torch.cuda.Stream(self.device)
+        self._side.wait_event(packed)          # the packing has read w and the basis
+        q.record_stream(self._side)
+        self.fold_queries(q, self._side)
+        self._stats_pending = torch.cuda.Event()
+        self._stats_pending.record(self._side)
+        out = self.attend(q, stream=main)
+        main.wait_event(self._stats_pending)   # the step ends when both are done
+        return out
 
     def check(self, stream=None) -> int:
         return qwm_sync_status(self.ctx, stream)

@@ -491,6 +491,36 @@ def test_attend_several_chunks_mixed_rank(q):
         assert _attn_err(out[h].cpu().numpy().astype(np.float64), ref) <= 2e-2
 
 
+def test_stream_step_matches_step(q):
+    """The pipelined schedule (fold each step's Queries beside its attention) does the same work as
+    folding the previous step's Queries before the packing: identical chunks and outputs."""
+    w_ = synth.TINY
+    H = w_.heads
+    from bit_kv_cache_qsac_gb300 import stream
+    kk, vv = synth.keys(w_), synth.values(w_)
+    parts = [(0, 300), (300, 700), (700, 1024)]
+    qs = [_bf(synth.queries(w_, 20 + i, 96)) for i in range(len(parts))]
+    ka = q.Context(heads=H)
+    kb = q.Context(heads=H)
+    la, lb = stream.CompressedLayer(ka), stream.CompressedLayer(kb)
+    outs_a, outs_b = [], []
+    for i, (a, b) in enumerate(parts):
+        k_ = _bf(np.ascontiguousarray(kk[:, a:b]))
+        v_ = _bf(np.ascontiguousarray(vv[:, a:b]))
+        outs_a.append(la.step(qs[i - 1] if i > 0 else None, k_, v_, qs[i]).clone())
+        outs_b.append(lb.stream_step(k_, v_, qs[i]).clone())
+    torch.cuda.synchronize()
+    assert la.check() == 0 and lb.check() == 0
+    assert [c.rank_eff for c in lb.chunks] == [0, 8, 8]
+    for oa, ob in zip(outs_a, outs_b):
+        assert torch.equal(oa, ob)
+    for ca, cb in zip(la.chunks, lb.chunks):
+        for name in ("k_idx", "v_idx", "k_codes", "v_codes", "c", "c_scale", "u_r"):
+            assert torch.equal(getattr(ca, name), getattr(cb, name)), name
+    # lb has also folded the last step's Queries: one more batch than la
+    assert int(lb.n[0]) == int(la.n[0]) + 96
+
+
 def test_bad_arguments_raise(q):
     ctx = q.Context(heads=2)
     x = torch.zeros(2, 300, D, dtype=torch.bfloat16, device="cuda")
