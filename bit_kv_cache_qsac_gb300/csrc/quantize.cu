@@ -581,78 +581,80 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
         }
         __syncwarp();
       }
-      // ---- (3) Keys: range score S of every candidate (warp-cooperative), best per token ----
+      // ---- (3) Keys: range score S of every candidate (thread = token), best per token ----
       int best = 0;
       float best_S = 0.f;
+      float bmn0 = INFINITY, bmx0 = -INFINITY, bmn1 = INFINITY, bmx1 = -INFINITY;  // the best one's ranges
+      bool have_range = false;
       if (KEY) {
-        // Each token's candidate rows (this lane's 4 channels of each) are loaded one token ahead,
-        // all at once, so a token costs one load latency, overlapped with the previous token's
-        // scores.  Candidates are kept newest first; ties in S go to the lower index explicitly.
+        // The token's candidates from its window mask (newest first), then one pass over its 16
+        // eight-channel chunks: the chunk of x from shared memory once, the same chunk of every
+        // candidate row from global memory (independent loads: their latencies overlap), and the
+        // per-group min / max of each candidate's residual.  Ties in S go to the lower index.
         constexpr int KM = MP1 - 1;
-        const int tmax = (int)((p.n - tok0) < 32 ? (p.n - tok0) : 32);
-        auto prep = [&](int t, int (&cj)[KM], uint2 (&mu2)[KM]) -> int {
-          int cnt = 0;
-          for (int wi = 0; wi < NW; wi++) {
-            uint32_t m = msk[wi * 32 + t];
-            while (m) {
-              const int j = 32 * wi + __ffs(m) - 1;
-              m &= m - 1;
+        int cj[KM];
+        int cnt = 0;
 #pragma unroll
-              for (int k = KM - 1; k >= 1; k--) cj[k] = cj[k - 1];
-              cj[0] = j;
-              cnt++;
-            }
-          }
-          cnt = cnt < KM ? cnt : KM;
+        for (int k = 0; k < KM; k++) cj[k] = 0;
+        for (int wi = 0; wi < NW; wi++) {
+          uint32_t m = msk[wi * 32 + lane];
+          while (m) {
+            const int j = 32 * wi + __ffs(m) - 1;
+            m &= m - 1;
 #pragma unroll
-          for (int k = 0; k < KM; k++)
-            if (k < cnt) mu2[k] = *(const uint2 *)(cent + (int64_t)cj[k] * D + 4 * lane);
-          return cnt;
-        };
-        auto score = [&](int t, int cnt, const int (&cj)[KM], const uint2 (&mu2)[KM]) {
-          float xf[4];
-          unpack4(*(const uint2 *)(xt + lane4_offset(32 * sub + t, lane)), xf);
-          float bS = INFINITY;
-          int bj = C;
-#pragma unroll
-          for (int k = 0; k < KM; k++) {
-            if (k >= cnt) break;
-            const int j = cj[k];
-            float mu[4];
-            unpack4(mu2[k], mu);
-            float mn = INFINITY, mx = -INFINITY;
-#pragma unroll
-            for (int u = 0; u < 4; u++) {
-              const float rr = __fsub_rn(xf[u], mu[u]);
-              mn = fminf(mn, rr);
-              mx = fmaxf(mx, rr);
-            }
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1) {  // within each half-warp (= one group)
-              mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            }
-            const float Rg = __fsub_rn(mx, mn);
-            const float Ro = __shfl_xor_sync(0xffffffffu, Rg, 16);
-            const float R0 = lane < 16 ? Rg : Ro, R1 = lane < 16 ? Ro : Rg;
-            const float S = __fadd_rn(__fmul_rn(W0, __fmul_rn(R0, R0)), __fmul_rn(W1, __fmul_rn(R1, R1)));
-            if (S < bS || (S == bS && j < bj)) { bS = S; bj = j; }
-            if (p.dbg_cand && lane == 0 && k < M) p.dbg_cand[((int64_t)h * p.n + tok0 + t) * M + k] = j;
-          }
-          if (lane == t) { best = bj; best_S = bS; }
-        };
-        int cA[KM], cB[KM];
-        uint2 uA[KM], uB[KM];
-        int nA = 0, nB = 0;
-        if (tmax > 0) nA = prep(0, cA, uA);
-        for (int t = 0; t < tmax; t += 2) {
-          if (t + 1 < tmax) nB = prep(t + 1, cB, uB);
-          score(t, nA, cA, uA);
-          if (t + 1 < tmax) {
-            if (t + 2 < tmax) nA = prep(t + 2, cA, uA);
-            score(t + 1, nB, cB, uB);
+            for (int k = KM - 1; k >= 1; k--) cj[k] = cj[k - 1];
+            cj[0] = j;
+            cnt++;
           }
         }
+        cnt = valid ? (cnt < KM ? cnt : KM) : 0;
+        float mnv[KM][2], mxv[KM][2];
+#pragma unroll
+        for (int k = 0; k < KM; k++) {
+          mnv[k][0] = mnv[k][1] = INFINITY;
+          mxv[k][0] = mxv[k][1] = -INFINITY;
+        }
+        if (cnt > 0) {
+#pragma unroll
+          for (int gi = 0; gi < 2; gi++) {  // the two groups of 64 channels
+#pragma unroll 4
+          for (int cc = 0; cc < 8; cc++) {
+            const int ci = 8 * gi + cc;
+            float f[8];
+            bf16x8(tc::lds128(xts + gi * TILE * 128 + tc::sw128_offset(row, 8 * cc)), f);
+#pragma unroll
+            for (int k = 0; k < KM; k++) {
+              if (k < cnt) {
+                float mu[8];
+                bf16x8(*(const uint4 *)(cent + (int64_t)cj[k] * D + 8 * ci), mu);
+#pragma unroll
+                for (int u = 0; u < 8; u++) {
+                  const float rr = __fsub_rn(f[u], mu[u]);
+                  mnv[k][gi] = fminf(mnv[k][gi], rr);
+                  mxv[k][gi] = fmaxf(mxv[k][gi], rr);
+                }
+              }
+            }
+          }
+          }
+        }
+        float bS = INFINITY;
+        int bj = C;
+#pragma unroll
+        for (int k = 0; k < KM; k++) {
+          if (k < cnt) {
+            const float R0 = __fsub_rn(mxv[k][0], mnv[k][0]), R1 = __fsub_rn(mxv[k][1], mnv[k][1]);
+            const float S = __fadd_rn(__fmul_rn(W0, __fmul_rn(R0, R0)), __fmul_rn(W1, __fmul_rn(R1, R1)));
+            if (S < bS || (S == bS && cj[k] < bj)) {
+              bS = S; bj = cj[k];
+              bmn0 = mnv[k][0]; bmx0 = mxv[k][0]; bmn1 = mnv[k][1]; bmx1 = mxv[k][1];
+            }
+            if (p.dbg_cand && k < M) p.dbg_cand[((int64_t)h * p.n + tok) * M + k] = cj[k];
+          }
+        }
+        best = bj;
+        best_S = bS;
+        have_range = cnt > 0;
       } else {
         for (int wi = 0; wi < NW; wi++) {
           const uint32_t m = msk[wi * 32 + lane];
@@ -663,8 +665,8 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
       // ---- (4) INT2 codes of the chosen centroid's residual; PSAC coefficients (thread = token) ----
       const int64_t grow = (int64_t)h * p.n + tok;
       const uint16_t *mub = cent + (int64_t)best * D;
-      float mn0 = INFINITY, mx0 = -INFINITY, mn1 = INFINITY, mx1 = -INFINITY;
-      if (valid) {
+      float mn0 = bmn0, mx0 = bmx0, mn1 = bmn1, mx1 = bmx1;  // Keys: the ranges of the scoring pass
+      if (valid && !have_range) {
 #pragma unroll
         for (int ci = 0; ci < D / 8; ci++) {
           float f[8], mu[8];
