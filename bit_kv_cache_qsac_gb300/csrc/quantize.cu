@@ -668,15 +668,21 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
       float mn0 = bmn0, mx0 = bmx0, mn1 = bmn1, mx1 = bmx1;  // Keys: the ranges of the scoring pass
       if (valid && !have_range) {
 #pragma unroll
-        for (int ci = 0; ci < D / 8; ci++) {
-          float f[8], mu[8];
-          bf16x8(tc::lds128(xts + (ci / 8) * TILE * 128 + tc::sw128_offset(row, 8 * (ci % 8))), f);
-          bf16x8(*(const uint4 *)(mub + 8 * ci), mu);
+        for (int gi = 0; gi < 2; gi++) {
+          uint4 mv[8];
 #pragma unroll
-          for (int u = 0; u < 8; u++) {
-            const float rr = __fsub_rn(f[u], mu[u]);
-            if (ci < 8) { mn0 = fminf(mn0, rr); mx0 = fmaxf(mx0, rr); }
-            else { mn1 = fminf(mn1, rr); mx1 = fmaxf(mx1, rr); }
+          for (int cc = 0; cc < 8; cc++) mv[cc] = *(const uint4 *)(mub + 64 * gi + 8 * cc);
+#pragma unroll
+          for (int cc = 0; cc < 8; cc++) {
+            float f[8], mu[8];
+            bf16x8(tc::lds128(xts + gi * TILE * 128 + tc::sw128_offset(row, 8 * cc)), f);
+            bf16x8(mv[cc], mu);
+#pragma unroll
+            for (int u = 0; u < 8; u++) {
+              const float rr = __fsub_rn(f[u], mu[u]);
+              if (gi == 0) { mn0 = fminf(mn0, rr); mx0 = fmaxf(mx0, rr); }
+              else { mn1 = fminf(mn1, rr); mx1 = fmaxf(mx1, rr); }
+            }
           }
         }
       }
@@ -742,11 +748,17 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
 #pragma unroll
         for (int k = 0; k < RMAX; k++) Cv[k] = 0.f;
 #pragma unroll
-        for (int ci = 0; ci < D / 8; ci++) {
+        for (int gi = 0; gi < 2; gi++) {
+        uint4 mv[8];  // the group's half of the centroid row, loaded at once (one L2 latency per group)
+#pragma unroll
+        for (int cc = 0; cc < 8; cc++) mv[cc] = *(const uint4 *)(mub + 64 * gi + 8 * cc);
+#pragma unroll
+        for (int cc = 0; cc < 8; cc++) {
+          const int ci = 8 * gi + cc;
           float f[8], mu[8];
-          bf16x8(tc::lds128(xts + (ci / 8) * TILE * 128 + tc::sw128_offset(row, 8 * (ci % 8))), f);
-          bf16x8(*(const uint4 *)(mub + 8 * ci), mu);
-          const bool g1 = ci >= 8;
+          bf16x8(tc::lds128(xts + gi * TILE * 128 + tc::sw128_offset(row, 8 * cc)), f);
+          bf16x8(mv[cc], mu);
+          const bool g1 = gi == 1;
           const float mm = g1 ? m1 : m0, ss = g1 ? s1 : s0, ii = g1 ? i1 : i0, zz = g1 ? z1f : z0f;
           uint32_t bits = 0;
 #pragma unroll
@@ -769,6 +781,7 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
           }
           if (ci & 1) packed[ci >> 1] |= bits << 16;
           else packed[ci >> 1] = bits;
+        }
         }
         uint4 *cdst = (uint4 *)(p.codes + grow * (D / 4));
         cdst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
