@@ -182,8 +182,8 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // KEY: Keys (QSAC + PSAC) or Values (nearest centroid).  RMAX: 8 or 16, bound on the PSAC rank.
-// MP1: length of the largest-T list, top_m + 1 (exact for the common M; QWM_MAX_TOPM + 1 covers
-// every M, with the list's tail unused).  WIDE: the codebook streams through in slices.
+// MP1: length of the largest-T list, at least top_m + 1 (5 serves top_m 1..4; QWM_MAX_TOPM + 1
+// covers every M, with the list's tail unused).  WIDE: the codebook streams through in slices.
 template <bool KEY, int RMAX, int MP1, bool WIDE>
 __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constant__ TensorMap128 tmap,
                                                              const QParams p) {
@@ -984,10 +984,11 @@ cudaError_t launch_one(const TensorMap128 &tmap, const QParams &p, int H, int sm
 
 template <bool WIDE>
 cudaError_t launch_pass(const TensorMap128 &tmap, const QParams &p, bool key, int H, int smem, cudaStream_t st) {
+  // MP1 bounds the candidate count (top_m <= MP1 - 1): the small variant serves top_m 1..4
   if (!key) return launch_one<false, 8, 2, WIDE>(tmap, p, H, smem, st);
-  if (p.rank <= 8 && p.top_m == 4) return launch_one<true, 8, 5, WIDE>(tmap, p, H, smem, st);
+  if (p.rank <= 8 && p.top_m <= 4) return launch_one<true, 8, 5, WIDE>(tmap, p, H, smem, st);
   if (p.rank <= 8) return launch_one<true, 8, QWM_MAX_TOPM + 1, WIDE>(tmap, p, H, smem, st);
-  if (p.top_m == 4) return launch_one<true, 16, 5, WIDE>(tmap, p, H, smem, st);
+  if (p.top_m <= 4) return launch_one<true, 16, 5, WIDE>(tmap, p, H, smem, st);
   return launch_one<true, 16, QWM_MAX_TOPM + 1, WIDE>(tmap, p, H, smem, st);
 }
 

@@ -213,7 +213,7 @@ def test_quantize_cold_start(q):
     _check_quantize(q, ctx, k, v, K, V, ch, None, None, 4, 8)
 
 
-@pytest.mark.parametrize("n,C,top_m,rank", [(333, 64, 16, 16), (257, 128, 1, 0), (300, 256, 4, 8)])
+@pytest.mark.parametrize("n,C,top_m,rank", [(333, 64, 16, 16), (257, 128, 1, 0), (300, 256, 4, 8), (401, 256, 2, 8)])
 def test_quantize_ragged_and_shapes(q, n, C, top_m, rank):
     ctx, k, v, K, V, ch, w, ur = _upstream(q, synth.TINY, 2, n, C=C, top_m=top_m, rank=rank)
     _check_quantize(q, ctx, k, v, K, V, ch, w, ur, top_m, rank)
