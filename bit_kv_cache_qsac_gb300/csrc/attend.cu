@@ -491,6 +491,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int item = !ragged ? (int)(blockIdx.x >> 1) : (r < nfull ? r % (nqt - 1) : nqt - 1);
   const int cr = (int)tc::cluster_ctarank();
   const int64_t qb = (int64_t)item * kPairQ + (int64_t)cr * BM;  // this CTA's row 0 of tile 0
+  // a short last item whose second 256-row Query tile is empty runs the first tile only
+  const bool skip1 = (int64_t)item * kPairQ + 2 * BM >= p.nq;
   volatile int *abort_v = &abort_flag;
 
   // ---- this CTA's two Query tiles (rows qb + 256 x + rr) -> shared memory as fp16 ----
@@ -555,6 +557,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp < kSoftmaxWarps) {
     // ======================= softmax (Query tile x, row = TMEM lane) =======================
     const int x = warp / 4, sub = warp % 4, row = 32 * sub + lane;
+    const int Jx = (x == 1 && skip1) ? 0 : J;  // tiles this softmax group sees
     const uint32_t lane_addr = (uint32_t)(32 * sub) << 16;
     const uint32_t tS = tmem + lane_addr + 128u * x, tO = tmem + lane_addr + 256u + 128u * x;
     const uint32_t p_ready0 = tc::mapa(tc::smem_u32(&bars.p_ready[x]), 0);
@@ -565,7 +568,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int64_t qrow = qb + (int64_t)x * 2 * BM + row;  // this thread's Query row
     int tc_ = 0, ti_ = 0;                                  // chunk and tile in chunk of tile j
     bool ok = true;
-    for (int j = 0; j < J; j++) {
+    for (int j = 0; j < Jx; j++) {
       if (!tc::mbar_wait(&bars.s_full[x], j & 1, kWaitNs)) fail(&abort_flag, p.status);
       if (*abort_v) { ok = false; break; }
       tc::fence_after_sync();
@@ -650,8 +653,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) tc::mbar_arrive_remote(p_ready0);
     }
-    if (ok && !tc::mbar_wait(&bars.o_done, 0, kWaitNs)) fail(&abort_flag, p.status);
-    if (ok && !*abort_v) {
+    if (ok && Jx > 0 && !tc::mbar_wait(&bars.o_done, 0, kWaitNs)) fail(&abort_flag, p.status);
+    if (ok && Jx > 0 && !*abort_v) {
       tc::fence_after_sync();
       const uint64_t lsum = tc::add2(acc0, acc1);
       const float l = tc::f2lo(lsum) + tc::f2hi(lsum);
@@ -711,15 +714,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc::fence_after_sync();
         qk(0, s, nx, t & 1);
         tc::mma2_commit(&bars.s_full[0], kBoth);
-        if (j > 0) {
+        if (j > 0 && !skip1) {
           ok = tc::mbar_wait_cluster(&bars.p_ready[1], (j - 1) & 1, kWaitNs) && !*abort_v;
           if (!ok) break;
           tc::fence_after_sync();
           pv(1, prev_stage, j - 1 == 0);
           tc::mma2_commit(&bars.v_empty[prev_stage], kBoth);
         }
-        qk(1, s, nx, t & 1);
-        tc::mma2_commit(&bars.s_full[1], kBoth);
+        if (!skip1) {
+          qk(1, s, nx, t & 1);
+          tc::mma2_commit(&bars.s_full[1], kBoth);
+        }
         tc::mma2_commit(&bars.k_empty[s], kBoth);
         const bool last_of_chunk = tile_in_chunk + 1 == ch.tiles;
         if (last_of_chunk) tc::mma2_commit(&bars.qx_free[t & 1], kBoth);
@@ -728,17 +733,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc::fence_after_sync();
         pv(0, s, j == 0);
+        if (skip1) tc::mma2_commit(&bars.v_empty[s], kBoth);  // no second tile reads this stage
         prev_stage = s;
         if (last_of_chunk) { tile_in_chunk = 0; t++; }
         else tile_in_chunk++;
       }
       if (ok && J > 0) {
-        ok = tc::mbar_wait_cluster(&bars.p_ready[1], (J - 1) & 1, kWaitNs) && !*abort_v;
-        if (ok) {
-          tc::fence_after_sync();
-          pv(1, prev_stage, J - 1 == 0);
-          tc::mma2_commit(&bars.o_done, kBoth);
+        if (!skip1) {
+          ok = tc::mbar_wait_cluster(&bars.p_ready[1], (J - 1) & 1, kWaitNs) && !*abort_v;
+          if (ok) {
+            tc::fence_after_sync();
+            pv(1, prev_stage, J - 1 == 0);
+          }
         }
+        if (ok) tc::mma2_commit(&bars.o_done, kBoth);
       }
       if (!ok) fail(&abort_flag, p.status);
       tc::mma2_commit(&bars.drain, 1);  // every MMA issued above completes before TMEM is released
