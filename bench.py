@@ -172,8 +172,8 @@ def gen_layer(layer: int):
 # DRAM bytes per launch of the attention kernel (dram__bytes_read.sum + dram__bytes_write.sum from
 # one ncu capture, profiles/attend_pair_kernel_*.md), valid only for the kernel source they were taken
 # on: the SHA-256 of csrc/attend.cu is checked, and the traffic reported as null otherwise.
-ATTEND_TRAFFIC = {"sha256": "8714211d69d6fd2150ca315f007c9e44c7e2a5891e2bcc9ecca3cdde1df209e0",
-                  "720p": 480708096 + 191165440, "480p": 229535488 + 67040768}
+ATTEND_TRAFFIC = {"sha256": "8e38218c31e3d74b6f21e85f9b27fe178100a327181f3c0d75869429c334cd1c",
+                  "720p": 476568320 + 192466176, "480p": 227467776 + 66667520}
 
 
 def attend_traffic(workload: str):

@@ -480,15 +480,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __shared__ int abort_flag;
   __shared__ __align__(64) uint32_t code_lut[WIDE ? 16 : 512];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Work order (the pairs start roughly in launch order): the full 512-Query items of every head
-  // first, head by head, then each head's shorter last item, so that the short items fill the
-  // tail of the last wave instead of sitting in every wave.
-  const int nqt = (int)gridDim.x >> 1;
-  const int r = (int)blockIdx.y * nqt + (int)(blockIdx.x >> 1);
-  const int nfull = (int)gridDim.y * (nqt - 1);
-  const bool ragged = p.nq % kPairQ != 0 && nqt > 1;
-  const int h = !ragged ? (int)blockIdx.y : (r < nfull ? r / (nqt - 1) : r - nfull);
-  const int item = !ragged ? (int)(blockIdx.x >> 1) : (r < nfull ? r % (nqt - 1) : nqt - 1);
+  // one head's items run next to each other (launch order): its packed cache stays in L2
+  const int h = (int)blockIdx.y, item = (int)(blockIdx.x >> 1);
   const int cr = (int)tc::cluster_ctarank();
   const int64_t qb = (int64_t)item * kPairQ + (int64_t)cr * BM;  // this CTA's row 0 of tile 0
   // a short last item whose second 256-row Query tile is empty runs the first tile only
