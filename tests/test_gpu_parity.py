@@ -81,6 +81,35 @@ def test_stats_weights_and_basis(q):
             assert np.mean(bf16_ulp_close(to_u16(ur[h]), oU[h][:, :8], 1.0)) > 0.95
 
 
+def test_basis_rank16_eigenpairs(q):
+    """Rank 16 reaches into the noise eigenvalues: every returned column is an eigenvector of M
+    (residual at the bf16 rounding level), the columns are orthonormal to that level, the first 8
+    match the oracle's, and all 128 eigenvalues agree."""
+    w_ = synth.TINY
+    H = w_.heads
+    ctx = q.Context(heads=H, rank=16)
+    S = torch.zeros(H, D, D, device="cuda"); n = torch.zeros(H, dtype=torch.int64, device="cuda")
+    w = torch.empty(H, D, device="cuda"); lam = torch.empty(H, D, device="cuda")
+    ur = torch.empty(H, D, 16, dtype=torch.bfloat16, device="cuda")
+    qb = synth.queries(w_, 7, 300)
+    q.qwm_update_query_stats(ctx, _bf(qb), 300, S, n, w, lam, ur)
+    assert q.qwm_sync_status(ctx) == 0
+    S64 = np.zeros((H, D, D)); n64 = np.zeros(H, np.int64)
+    ow, olam, our, oU, _ = oracle.update_query_stats(qb, S64, n64, 16)
+    gl = lam.cpu().numpy()
+    assert np.all(np.abs(gl - olam) <= 1e-3 * np.abs(olam) + 1e-6 * np.abs(olam).max())
+    gu = _f32(to_u16(ur))
+    for h in range(H):
+        M = S64[h] / n64[h]
+        U = gu[h]
+        assert np.abs(U.T @ U - np.eye(16)).max() < 1e-2
+        for k in range(16):
+            res = np.linalg.norm(M @ U[:, k] - olam[h, k] * U[:, k])
+            assert res <= 5e-3 * olam[h, 0], (h, k, res)
+        for k in range(8):
+            assert U[:, k] @ oU[h][:, k] / np.linalg.norm(U[:, k]) > 0.999
+
+
 # ------------------------------------------------------------------ step 2a
 
 
