@@ -617,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
         if (cnt > 0) {
 #pragma unroll
           for (int gi = 0; gi < 2; gi++) {  // the two groups of 64 channels
-#pragma unroll 4
+#pragma unroll
           for (int cc = 0; cc < 8; cc++) {
             const int ci = 8 * gi + cc;
             float f[8];
