@@ -165,8 +165,9 @@ __device__ __forceinline__ float start_entry(int i, int k) {
 //  2. Every eigenvalue of T by multisection on Sturm counts (the number of negative pivots of
 //     T - x I): four threads per eigenvalue test four interior points per round.
 //  3. Inverse iteration on T for each of the r largest eigenvalues (two solves with partial
-//     pivoting, each from its own start vector), then modified Gram-Schmidt within clusters of
-//     eigenvalues closer than 1e-3 ||T||.
+//     pivoting, each from its own start vector; the back-substitution rescales the system when
+//     near-zero pivots of a repeated eigenvalue make it grow), then modified Gram-Schmidt within
+//     clusters of eigenvalues closer than 1e-3 ||T||.
 //  4. Back-transformation u = Q z (one warp per vector) and the sign convention: the largest-
 //     magnitude component is made positive, the lowest channel on ties.
 __global__ void __launch_bounds__(kEigThreads) eig_kernel(const float *__restrict__ S, int64_t *__restrict__ n,
@@ -332,7 +333,7 @@ __global__ void __launch_bounds__(kEigThreads) eig_kernel(const float *__restric
   // ---- 3. inverse iteration, one thread per vector (vector k: k-th largest eigenvalue) ----
   if (tid < rank) {
     const int k = tid;
-    const float sh = lam[D - 1 - k], tiny = 1.2e-7f * tnorm;
+    const float sh = lam[D - 1 - k], tiny = fmaxf(1.2e-7f * tnorm, 1e-30f);
     float *dgv = lu + k * LU, *s1 = dgv + D, *s2 = s1 + D, *z = s2 + D;
     for (int i = 0; i < D; i++) z[i] = start_entry(i, k);
     for (int it = 0; it < 2; it++) {
@@ -358,6 +359,14 @@ __global__ void __launch_bounds__(kEigThreads) eig_kernel(const float *__restric
         if (i + 1 < D) t -= s1[i] * z[i + 1];
         if (i + 2 < D) t -= s2[i] * z[i + 2];
         const float dd = dgv[i] == 0.f ? tiny : dgv[i];
+        if (!(fabsf(t) <= 1e20f * fabsf(dd))) {
+          // growth through near-zero pivots (an eigenvalue of high multiplicity, e.g. fewer Queries
+          // than channels): scale the whole system down, solved part and remaining right-hand side
+          const float f = (1e20f * fabsf(dd)) / fabsf(t);
+          for (int j = 0; j < D; j++) z[j] *= f;
+          big *= f;
+          t *= f;
+        }
         z[i] = t / dd;
         big = fmaxf(big, fabsf(z[i]));
       }

@@ -110,6 +110,36 @@ def test_basis_rank16_eigenpairs(q):
             assert U[:, k] @ oU[h][:, k] / np.linalg.norm(U[:, k]) > 0.999
 
 
+@pytest.mark.parametrize("nq", [3, 1])
+def test_basis_fewer_queries_than_rank(q, nq):
+    """M of rank nq < r: the eigenvalue 0 has multiplicity 128 - nq.  No error is recorded, the
+    nonzero eigenpairs match the oracle's, and the remaining columns are orthonormal vectors of the
+    null space (any such basis is an eigenbasis there)."""
+    w_ = synth.TINY
+    H = w_.heads
+    ctx = q.Context(heads=H, rank=8)
+    S = torch.zeros(H, D, D, device="cuda"); n = torch.zeros(H, dtype=torch.int64, device="cuda")
+    w = torch.empty(H, D, device="cuda"); lam = torch.empty(H, D, device="cuda")
+    ur = torch.empty(H, D, 8, dtype=torch.bfloat16, device="cuda")
+    qb = synth.queries(w_, 9, nq)
+    q.qwm_update_query_stats(ctx, _bf(qb), nq, S, n, w, lam, ur)
+    assert q.qwm_sync_status(ctx) == 0
+    S64 = np.zeros((H, D, D)); n64 = np.zeros(H, np.int64)
+    ow, olam, our, oU, _ = oracle.update_query_stats(qb, S64, n64, 8)
+    gl = lam.cpu().numpy()
+    assert np.all(np.abs(gl - olam) <= 1e-3 * np.abs(olam) + 1e-6 * np.abs(olam).max())
+    gu = _f32(to_u16(ur))
+    for h in range(H):
+        U = gu[h]
+        assert np.isfinite(U).all()
+        assert np.abs(U.T @ U - np.eye(8)).max() < 1e-2
+        for k in range(nq):
+            assert U[:, k] @ oU[h][:, k] / np.linalg.norm(U[:, k]) > 0.999
+        M = S64[h] / n64[h]
+        for k in range(nq, 8):
+            assert np.linalg.norm(M @ U[:, k]) <= 5e-3 * olam[h, 0], (h, k)
+
+
 # ------------------------------------------------------------------ step 2a
 
 
