@@ -114,6 +114,33 @@ def test_eig_diagonal_and_degenerate():
     assert U[1, 0] == 1.0 and U[3, 1] == 1.0
 
 
+def test_eig_rank_one_and_two_closed_form():
+    """M = q q^T has the single nonzero eigenvalue |q|^2 with eigenvector q / |q|; M = a a^T + b b^T
+    with a, b orthogonal has |a|^2, |b|^2 with a / |a|, b / |b|.  The sign convention makes the
+    largest-magnitude component positive; every other eigenvalue is 0."""
+    rng = np.random.default_rng(11)
+    q = rng.standard_normal(D)
+    lam, U, _ = oracle.eig(np.outer(q, q))
+    assert abs(lam[0] - q @ q) <= 1e-12 * (q @ q)
+    assert np.abs(lam[1:]).max() <= 1e-12 * (q @ q)
+    u = q / np.linalg.norm(q)
+    u = u if u[np.argmax(np.abs(u))] > 0 else -u
+    assert np.abs(U[:, 0] - u).max() <= 1e-10
+    a = rng.standard_normal(D)
+    b = rng.standard_normal(D)
+    b -= (a @ b) / (a @ a) * a
+    a *= 3.0
+    lam, U, _ = oracle.eig(np.outer(a, a) + np.outer(b, b))
+    assert abs(lam[0] - a @ a) <= 1e-10 * (a @ a) and abs(lam[1] - b @ b) <= 1e-10 * (a @ a)
+    for k, v in ((0, a), (1, b)):
+        v = v / np.linalg.norm(v)
+        v = v if v[np.argmax(np.abs(v))] > 0 else -v
+        assert np.abs(U[:, k] - v).max() <= 1e-9
+    # the eigenvectors are orthonormal and the remaining eigenvalues vanish
+    assert np.abs(U.T @ U - np.eye(D)).max() <= 1e-10
+    assert np.abs(lam[2:]).max() <= 1e-10 * (a @ a)
+
+
 def test_generator_top8_energy():
     """The Query recipe puts (19.34 + 8 * 0.09) / (19.34 + 128 * 0.09) = 0.65 of the energy in the
     top-8 directions (QuantWM reports more than 60%)."""
