@@ -60,7 +60,7 @@ typedef enum {
   QWM_ERR_ALIGN = 3,         /* a pointer that is not 16-byte aligned */
   QWM_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
   QWM_ERR_NOT_CONVERGED = 5, /* the eigensolver could not form an eigenvector (results still written) */
-  QWM_ERR_UNSUPPORTED = 6,   /* a configuration this build does not implement */
+  QWM_ERR_UNSUPPORTED = 6,   /* a configuration the library does not implement */
   QWM_ERR_RANGE = 7,         /* a residual, scale or coefficient outside the fp16 range */
   QWM_ERR_DEVICE_TIMEOUT = 8 /* a kernel's internal wait ran past its time limit and the kernel gave up */
 } qwm_status;
