@@ -502,6 +502,53 @@ def oracle_sample(seconds_hint: float = 15.0):
                         "attend": H * t_att * NQ / rows}}
 
 
+def oracle_full_model_sample(layers=(0, 39), rows: int = 64):
+    """The oracle's time for the full model (40 layers of the 480p-shaped layer, 8 steps each),
+    estimated from head 0 of `layers`: at step 8, statistics + eigen-solve of the chunk's Queries,
+    k-means of its Keys and Values, packing, and `rows` Query rows attending over the 8-chunk
+    cache.  Per layer: 8 x (statistics + fit + packing), and the attention summed over the steps
+    (step t attends over t chunks: sum t = 36 chunk-lengths per Query).  Averaged over the sampled
+    layers, then x40 heads x40 layers."""
+    import oracle
+    oracle.build()
+    Wf, n_layers = synth.P480, 40
+    d, nq, nc, r = Wf.head_dim, Wf.nq_attend, Wf.chunk_tokens, Wf.rank
+    per_layer, sample_s = [], 0.0
+    for layer in layers:
+        T = Wf.n_chunks
+        chunks, ur = [], None
+        for t in range(T):   # untimed: a packed cache for head 0 (codebooks seeded from tokens)
+            kt = synth.keys(Wf, layer, *synth.chunk_range(Wf, t))[0]
+            vt = synth.values(Wf, layer, *synth.chunk_range(Wf, t))[0]
+            sel = (np.arange(Wf.n_centroids) * nc) // Wf.n_centroids
+            if t > 0:
+                ur = oracle.basis_bf16(np.linalg.qr(np.random.default_rng(t).standard_normal((d, d)))[0], r)
+            o = oracle.quantize_head(kt, vt, kt[sel], vt[sel], None, ur, top_m=Wf.top_m)
+            chunks.append(dict(o, cent_k=kt[sel], cent_v=vt[sel],
+                               u_r=ur if ur is not None else np.zeros((d, r), np.uint16), rank=o["rank"]))
+        k = synth.keys(Wf, layer, *synth.chunk_range(Wf, T - 1))[0]
+        v = synth.values(Wf, layer, *synth.chunk_range(Wf, T - 1))[0]
+        qs = synth.queries(Wf, T - 1, nq, layer)[0]
+        t0 = time.perf_counter()
+        S = np.zeros((1, d, d)); n = np.zeros(1, np.int64)
+        w, lam, urb, U, _ = oracle.update_query_stats(qs[None], S, n, r)
+        ck, _, _, _ = oracle.kmeans(k, Wf.n_centroids, chunks[-2]["cent_k"], 10)
+        cv, _, _, _ = oracle.kmeans(v, Wf.n_centroids, chunks[-2]["cent_v"], 10)
+        oracle.quantize_head(k, v, ck, cv, w[0], urb[0], top_m=Wf.top_m)
+        t_pack = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        oracle.attend_rows(qs, np.arange(rows), chunks, 1.0 / math.sqrt(d))
+        t_att8 = time.perf_counter() - t0   # rows over 8 chunks
+        sample_s += t_pack + t_att8
+        per_layer.append(T * t_pack + t_att8 * (nq / rows) * (T * (T + 1) / 2) / T)
+    est = float(np.mean(per_layer)) * Wf.heads * n_layers
+    return {"kind": "oracle", "cores": len(os.sched_getaffinity(0)), "estimated_s": est,
+            "sample": f"head 0 of layers {list(layers)}: step-8 statistics, codebooks and packing of {nc} tokens, "
+                      f"{rows} of {nq} Query rows over the 8-chunk cache; extrapolated to 8 steps, "
+                      f"{Wf.heads} heads and {n_layers} layers",
+            "sample_seconds": sample_s}
+
+
 # ---------------------------------------------------------------------------- extra reports
 
 
@@ -841,6 +888,7 @@ def run_full_model(device, storage: int = 0):
                                                  "attend": att_ms.tolist(),
                                                  "bf16_sdpa_uncompressed": sdpa_ms.tolist()},
                       "total_gpu_ms": float(stats_ms.sum() + pack_ms.sum() + att_ms.sum()),
+                      "cpu_baseline": oracle_full_model_sample(),
                       "total_bf16_sdpa_ms": float(sdpa_ms.sum()),
                       "note": "each stage is timed alone with a host sync after every layer step, so the "
                               "per-step figures include launch gaps",
