@@ -404,3 +404,96 @@ def kivi_dequantize_head(o: dict, group: int = 32):
                                           _p(arrs["v_codes"]), _p(arrs["v_scale"]), _p(arrs["v_min"]), n, d,
                                           group, _p(kh), _p(vh))
     return kh, vh
+
+
+# ---------------------------------------------------------------- PSAC rank per head, coefficient layouts
+#
+# The Chinese summary's critique ("独立分析的弱点", weakness three) notes that how much of the Query
+# energy the top directions hold differs by model and layer, so one global r is a compromise; the
+# English v2 summary (§C.2) reports that a larger r still helps.  The rank per (chunk, head) below is
+# the plainest rule that follows from the eigenvalues the statistics step already computes: the
+# smallest r whose top-r eigenvalues hold a given share of tr M.  The packed coefficient layouts
+# follow the English v2 summary §D.1 ("selects the smaller dense or sparse coefficient layout,
+# including sparse-index storage"): a token whose stored correction is zero (sC = 0: the gate of
+# step (4) dropped it, or its coefficients were all zero) needs no row in the sparse layout.
+
+
+def adaptive_rank(lam, r_max: int, energy: float) -> int:
+    """Smallest r in 0..r_max whose r largest eigenvalues hold at least `energy` of their sum
+    (tr M, summed in descending order in double precision); r_max when no r <= r_max does; 0 when
+    the sum is not positive (no Query seen)."""
+    lam = np.sort(np.asarray(lam, np.float64))[::-1]
+    tr = 0.0
+    for x in lam:
+        tr += float(x)
+    if not tr > 0.0:
+        return 0
+    cum = 0.0
+    for r in range(r_max + 1):
+        if cum >= energy * tr:
+            return r
+        if r < lam.size:
+            cum += float(lam[r])
+    return r_max
+
+
+SPARSE_TILE = 128  # tokens per bitmap tile of the sparse layout
+
+
+def psac_sparse_encode(c: np.ndarray, c_scale: np.ndarray):
+    """Sparse layout of one head's coefficients: c int8 [n][r], c_scale fp16 bits [n] ->
+    (mask uint32 [tiles][4]: bit b of word w of tile t set when token 128 t + 32 w + b keeps a
+    row; tile_rank int32 [tiles]: kept tokens before tile t; rows int8 [K][r] and scales uint16 [K]
+    of the kept tokens in token order).  A token keeps its row when its scale is not zero."""
+    c = np.asarray(c, np.int8)
+    sc = np.asarray(c_scale, np.uint16)
+    n = sc.size
+    tiles = (n + SPARSE_TILE - 1) // SPARSE_TILE
+    keep = sc != 0
+    mask = np.zeros((tiles, 4), np.uint32)
+    for i in np.nonzero(keep)[0]:
+        t, b = divmod(int(i), SPARSE_TILE)
+        mask[t, b // 32] |= np.uint32(1 << (b % 32))
+    tile_rank = np.zeros(tiles, np.int32)
+    total = 0
+    for t in range(tiles):
+        tile_rank[t] = total
+        total += int(keep[t * SPARSE_TILE:(t + 1) * SPARSE_TILE].sum())
+    return mask, tile_rank, c[keep].copy(), sc[keep].copy()
+
+
+def psac_sparse_decode(mask, tile_rank, rows, scales, n: int, r: int):
+    """Dense (c int8 [n][r], c_scale uint16 [n]) of a sparse layout: token i's row is found from the
+    bitmap alone (its tile's kept count plus the set bits below it in its tile)."""
+    c = np.zeros((n, r), np.int8)
+    sc = np.zeros(n, np.uint16)
+    for i in range(n):
+        t, b = divmod(i, SPARSE_TILE)
+        w, bit = divmod(b, 32)
+        if not (int(mask[t, w]) >> bit) & 1:
+            continue
+        below = sum(bin(int(mask[t, x])).count("1") for x in range(w)) + bin(int(mask[t, w]) & ((1 << bit) - 1)).count("1")
+        slot = int(tile_rank[t]) + below
+        c[i] = rows[slot]
+        sc[i] = scales[slot]
+    return c, sc
+
+
+def psac_layout_bytes(n: int, rank: int, kept: int) -> tuple[int, int]:
+    """Bytes of one head's coefficients (int8 rows of `rank` bytes and an fp16 scale per stored row)
+    in the dense layout (every token) and in the sparse layout (kept tokens, plus a 16-byte bitmap
+    and a 4-byte kept count per 128-token tile).  A head of rank 0 stores nothing."""
+    if rank == 0:
+        return 0, 0
+    tiles = (n + SPARSE_TILE - 1) // SPARSE_TILE
+    return n * (rank + 2), kept * (rank + 2) + tiles * 20
+
+
+def psac_plan(n: int, ranks, kept):
+    """Per head: (sparse?, rows stored) choosing the smaller layout (dense on a tie)."""
+    plan = []
+    for r, k in zip(ranks, kept):
+        dense, sparse = psac_layout_bytes(n, int(r), int(k))
+        use_sparse = int(r) > 0 and sparse < dense
+        plan.append((use_sparse, (int(k) if use_sparse else n) if int(r) > 0 else 0))
+    return plan

@@ -688,3 +688,83 @@ def test_full_form_ranking_reduces_to_diagonal_and_matches_brute_force():
     ref = np.sort(np.argsort(dq, 1, kind="stable")[:, :4], 1)
     assert np.array_equal(np.sort(o["cand"], 1)[clear], ref[clear])
     assert np.all([o["idx_k"][i] in o["cand"][i] for i in range(120)])
+
+
+# ---------------------------------------------------------------- PSAC rank per head and coefficient layouts
+
+
+def test_adaptive_rank_closed_form_spectra():
+    """The smallest r whose top-r eigenvalues hold a share of tr M, on spectra whose cumulative
+    shares are known in closed form."""
+    geo = 2.0 ** -np.arange(128)                            # share after r: (1 - 2^-r) / (1 - 2^-128)
+    assert oracle.adaptive_rank(geo, 16, 0.9) == 4          # 0.875 < 0.9 <= 0.9375
+    assert oracle.adaptive_rank(geo, 16, 0.5) == 1
+    assert oracle.adaptive_rank(geo, 3, 0.99) == 3          # capped at r_max
+    flat = np.ones(128)                                     # share after r: r / 128
+    assert oracle.adaptive_rank(flat, 16, 10 / 128) == 10
+    assert oracle.adaptive_rank(flat, 16, 0.5) == 16        # 64 needed, capped
+    one = np.zeros(128); one[17] = 5.0                      # rank one (order of input irrelevant)
+    assert oracle.adaptive_rank(one, 8, 1.0) == 1
+    assert oracle.adaptive_rank(np.zeros(128), 8, 0.5) == 0  # no Query seen
+    assert oracle.adaptive_rank(geo, 8, 0.0) == 0
+
+
+def test_adaptive_rank_brute_force():
+    rng = np.random.default_rng(71)
+    for _ in range(200):
+        lam = np.sort(rng.gamma(0.5, 1.0, 128))[::-1]
+        tau, rmax = rng.uniform(0, 1), int(rng.integers(0, 17))
+        share = np.concatenate([[0.0], np.cumsum(lam)]) / lam.sum()
+        ok = [r for r in range(rmax + 1) if share[r] >= tau - 1e-12]
+        assert oracle.adaptive_rank(lam, rmax, tau) == (ok[0] if ok else rmax)
+
+
+@pytest.mark.parametrize("n,frac", [(300, 0.3), (1000, 1.0), (257, 0.0), (10800, 0.9)])
+def test_psac_sparse_layout_round_trip(n, frac):
+    """The sparse layout decodes to the dense one exactly: every kept token (non-zero scale) finds
+    its row through the bitmap and the per-tile counts; a dropped token decodes to zeros."""
+    rng = np.random.default_rng(n)
+    r = 8
+    c = rng.integers(-127, 128, size=(n, r)).astype(np.int8)
+    sc = rng.integers(1, 0x7BFF, size=n).astype(np.uint16)
+    drop = rng.random(n) >= frac
+    sc[drop] = 0
+    c[drop] = 0                                             # what the gate stores for a dropped token
+    mask, tile_rank, rows, scales = oracle.psac_sparse_encode(c, sc)
+    assert rows.shape == ((~drop).sum(), r)
+    pop = np.array([sum(bin(int(x)).count("1") for x in m) for m in mask])
+    assert pop.sum() == (~drop).sum()
+    assert np.array_equal(tile_rank, np.concatenate([[0], np.cumsum(pop)[:-1]]).astype(np.int32))
+    c2, sc2 = oracle.psac_sparse_decode(mask, tile_rank, rows, scales, n, r)
+    assert np.array_equal(c2, c) and np.array_equal(sc2, sc)
+
+
+def test_psac_layout_choice_is_the_smaller():
+    n, r = 10800, 8
+    tiles = (n + 127) // 128
+    for kept in (0, 5000, 10629, 10630, 10631, n):
+        dense, sparse = oracle.psac_layout_bytes(n, r, kept)
+        assert dense == n * 10 and sparse == kept * 10 + tiles * 20
+        (use_sparse, rows), = oracle.psac_plan(n, [r], [kept])
+        assert use_sparse == (kept * 10 + 1700 < 108000) and rows == (kept if use_sparse else n)
+    assert oracle.psac_plan(n, [0], [0]) == [(False, 0)]     # a head without PSAC stores nothing
+
+
+def test_psac_gate_drops_every_token_when_the_basis_sees_only_unweighted_channels():
+    """With zero weight on channels 64..127 and a basis supported there, the correction never
+    changes the Query-weighted error, so the gate (strict improvement) drops every token and the
+    sparse layout stores no row; moving part of the basis onto weighted channels keeps some."""
+    k, v, qs, _ = synth.small_case(1, 300, 128, 64, 256, seed=72)
+    ck, _, _, _ = oracle.kmeans(k[0], 64, None, 3)
+    cv, _, _, _ = oracle.kmeans(v[0], 64, None, 3)
+    w = np.r_[np.ones(64), np.zeros(64)]
+    U = np.zeros((128, 8)); U[64 + np.arange(8) * 8, np.arange(8)] = 1.0
+    o = oracle.quantize_head(k[0], v[0], ck, cv, w, bf16(U), top_m=4, rank=8, psac_gate=1)
+    assert np.all(o["c_scale"] == 0) and np.all(o["c"] == 0)
+    (use_sparse, rows), = oracle.psac_plan(300, [8], [0])
+    assert use_sparse and rows == 0
+    U2 = U.copy(); U2[np.arange(8) * 8, np.arange(8)] = 0.5
+    U2 /= np.linalg.norm(U2, axis=0)
+    o2 = oracle.quantize_head(k[0], v[0], ck, cv, w, bf16(U2), top_m=4, rank=8, psac_gate=1)
+    kept = int((o2["c_scale"] != 0).sum())
+    assert 0 < kept <= 300
