@@ -69,7 +69,7 @@ class ChunkHead(C.Structure):
         ("idx_k", P), ("idx_v", P), ("k_codes", P), ("v_codes", P),
         ("k_scale", P), ("k_min", P), ("v_scale", P), ("v_min", P),
         ("cent_k", P), ("cent_v", P), ("c", P), ("c_scale", P), ("u_r", P),
-        ("k_raw", P), ("v_raw", P), ("causal_tpf", I64),
+        ("k_raw", P), ("v_raw", P), ("causal_tpf", I64), ("cent_fp16", I32),
     ]
 
 
@@ -279,9 +279,10 @@ def quantize_head(k, v, cent_k, cent_v, w=None, u_r=None, *, group=64, top_m=4, 
 
 def _chunk_struct(ch: dict, keep: list) -> ChunkHead:
     """ch: per-head dict with idx_k, idx_v, k_codes, v_codes, k_scale, k_min, v_scale, v_min,
-    cent_k, cent_v and, when rank > 0, c, c_scale, u_r; or, for the chunk still being generated
-    (kept in bf16), k_raw and v_raw ([n][d] bf16 bits) and optionally causal_tpf (tokens per frame
-    of the block-causal mask, 0 = none)."""
+    the codebooks (cent_k, cent_v as bf16 bits, or the stored cent_k16, cent_v16 as fp16 bits, which
+    then take precedence) and, when rank > 0, c, c_scale, u_r; or, for the chunk still being
+    generated (kept in bf16), k_raw and v_raw ([n][d] bf16 bits) and optionally causal_tpf (tokens
+    per frame of the block-causal mask, 0 = none)."""
     def arr(name, dtype):
         a = _c(ch[name], dtype)
         keep.append(a)
@@ -290,15 +291,16 @@ def _chunk_struct(ch: dict, keep: list) -> ChunkHead:
         return ChunkHead(n=int(np.asarray(ch["k_raw"]).shape[0]), rank=0, k_raw=arr("k_raw", np.uint16),
                          v_raw=arr("v_raw", np.uint16), causal_tpf=int(ch.get("causal_tpf", 0)))
     rank = int(ch.get("rank", 0))
+    f16 = "cent_k16" in ch
     return ChunkHead(
         n=int(np.asarray(ch["idx_k"]).shape[0]), rank=rank,
         idx_k=arr("idx_k", np.int32), idx_v=arr("idx_v", np.int32),
         k_codes=arr("k_codes", np.uint8), v_codes=arr("v_codes", np.uint8),
         k_scale=arr("k_scale", np.uint16), k_min=arr("k_min", np.uint16),
         v_scale=arr("v_scale", np.uint16), v_min=arr("v_min", np.uint16),
-        cent_k=arr("cent_k", np.uint16), cent_v=arr("cent_v", np.uint16),
+        cent_k=arr("cent_k16" if f16 else "cent_k", np.uint16), cent_v=arr("cent_v16" if f16 else "cent_v", np.uint16),
         c=arr("c", np.int8) if rank else None, c_scale=arr("c_scale", np.uint16) if rank else None,
-        u_r=arr("u_r", np.uint16) if rank else None,
+        u_r=arr("u_r", np.uint16) if rank else None, cent_fp16=1 if f16 else 0,
     )
 
 
@@ -497,3 +499,14 @@ def psac_plan(n: int, ranks, kept):
         use_sparse = int(r) > 0 and sparse < dense
         plan.append((use_sparse, (int(k) if use_sparse else n) if int(r) > 0 else 0))
     return plan
+
+
+def codebook_fp16(cent_bf16: np.ndarray) -> np.ndarray:
+    """The stored codebook: the fp16 value (round to nearest even) of every bf16 centroid element,
+    as fp16 bit patterns.  Exact for magnitudes in [2^-17, 65504] and for 0."""
+    x = (np.asarray(cent_bf16, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    out = np.empty(x.size, np.uint16)
+    flat = x.ravel()
+    for i in range(flat.size):
+        out[i] = lib().oracle_fp16_bits(lib().oracle_round_fp16(float(flat[i]), 0))
+    return out.reshape(np.shape(cent_bf16))

@@ -724,7 +724,14 @@ typedef struct {
    * the Query in row q (token q of this chunk) sees key j only when j / tpf <= q / tpf. */
   const uint16_t *k_raw, *v_raw; /* [n][d] bf16 */
   int64_t causal_tpf;
+  /* 1: cent_k / cent_v hold the chunk's stored codebooks as fp16 bit patterns (the fp16 value of
+   * each bf16 centroid element) instead of the bf16 codebooks; decoding uses the values given. */
+  int32_t cent_fp16;
 } oracle_chunk_head;
+
+static double centroid_val(const oracle_chunk_head *ch, uint16_t b) {
+  return ch->cent_fp16 ? oracle_fp16_val(b) : bf16_val(b);
+}
 
 /* dequantised Key base k_hat_0 = mu_idx + r_hat and Value v_hat, as doubles */
 static void decode_token(const oracle_chunk_head *ch, int d, int group, int64_t j, double *kh0, double *vh) {
@@ -740,10 +747,10 @@ static void decode_token(const oracle_chunk_head *ch, int d, int group, int64_t 
   const uint16_t *muv = ch->cent_v + (int64_t)ch->idx_v[j] * d;
   for (int c = 0; c < d; c++) {
     int g = c / group;
-    kh0[c] = bf16_val(muk[c]) + (double)int2_decode(ch->k_scale[j * G + g], ch->k_min[j * G + g],
-                                                    unpack2(ch->k_codes + j * (d / 4), c));
-    vh[c] = bf16_val(muv[c]) + (double)int2_decode(ch->v_scale[j * G + g], ch->v_min[j * G + g],
-                                                   unpack2(ch->v_codes + j * (d / 4), c));
+    kh0[c] = centroid_val(ch, muk[c]) + (double)int2_decode(ch->k_scale[j * G + g], ch->k_min[j * G + g],
+                                                            unpack2(ch->k_codes + j * (d / 4), c));
+    vh[c] = centroid_val(ch, muv[c]) + (double)int2_decode(ch->v_scale[j * G + g], ch->v_min[j * G + g],
+                                                           unpack2(ch->v_codes + j * (d / 4), c));
   }
 }
 

@@ -768,3 +768,44 @@ def test_psac_gate_drops_every_token_when_the_basis_sees_only_unweighted_channel
     o2 = oracle.quantize_head(k[0], v[0], ck, cv, w, bf16(U2), top_m=4, rank=8, psac_gate=1)
     kept = int((o2["c_scale"] != 0).sum())
     assert 0 < kept <= 300
+
+
+def test_codebook_fp16_is_round_to_nearest_of_the_bf16_values():
+    """The stored codebook is the fp16 value of each bf16 centroid element: numpy's float16
+    conversion (round to nearest even), exact for magnitudes in [2^-17, 65504] and for 0."""
+    rng = np.random.default_rng(81)
+    x = np.concatenate([rng.standard_normal(2000), rng.standard_normal(200) * 2.0 ** -16,
+                        rng.standard_normal(100) * 2.0 ** -20, [0.0, -0.0, 65504.0, 1e5, 2.0 ** -17, 3 * 2.0 ** -19]])
+    b = bf16(x)
+    got = oracle.codebook_fp16(b)
+    with np.errstate(over="ignore"):                        # 1e5 overflows to inf, as in the oracle
+        want = f32(b).astype(np.float16).view(np.uint16)
+    assert np.array_equal(got, want)
+    v = f32(b).astype(np.float64)
+    exact = (np.abs(v) >= 2.0 ** -17) & (np.abs(v) <= 65504.0) | (v == 0)
+    assert np.all(want[exact].view(np.float16).astype(np.float64) == v[exact])
+
+
+def test_decode_from_stored_fp16_codebook():
+    """Decoding with the stored fp16 codebook equals decoding with the bf16 one when every element is
+    exact in fp16; an element below 2^-17 decodes through its fp16 rounding."""
+    k, v, qs, _ = synth.small_case(1, 200, 128, 64, 64, seed=82)
+    ck, _, _, _ = oracle.kmeans(k[0], 64, None, 3)
+    cv, _, _, _ = oracle.kmeans(v[0], 64, None, 3)
+    ckv = f32(ck).astype(np.float64)
+    ck = np.where((np.abs(ckv) < 2.0 ** -17) & (ckv != 0), bf16(np.full(ck.shape, 0.5)), ck)  # all exact
+    o = oracle.quantize_head(k[0], v[0], ck, cv, None, None, top_m=4)
+    base = dict(idx_k=o["idx_k"], idx_v=o["idx_v"], k_codes=o["k_codes"], v_codes=o["v_codes"],
+                k_scale=o["k_scale"], k_min=o["k_min"], v_scale=o["v_scale"], v_min=o["v_min"], rank=0)
+    a = oracle.dequantize_head(dict(base, cent_k=ck, cent_v=cv))
+    b = oracle.dequantize_head(dict(base, cent_k16=oracle.codebook_fp16(ck), cent_v16=oracle.codebook_fp16(cv)))
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+    tiny = ck.copy()
+    j = int(o["idx_k"][0])
+    tiny[j, 5] = bf16([3.3e-6])[0]                          # below 2^-17: rounds in fp16
+    c16 = oracle.codebook_fp16(tiny)
+    _, _, k64, _ = oracle.dequantize_head(dict(base, cent_k16=c16, cent_v16=oracle.codebook_fp16(cv)))
+    _, _, k64b, _ = oracle.dequantize_head(dict(base, cent_k=tiny, cent_v=cv))
+    d = k64[0, 5] - k64b[0, 5]
+    assert d == np.float16(f32(tiny[j, 5])).astype(np.float64) - f32(tiny[j, 5]).astype(np.float64) and d != 0
