@@ -33,6 +33,7 @@ QWM_OK, QWM_ERR_ARG, QWM_ERR_SHAPE, QWM_ERR_ALIGN, QWM_ERR_CUDA, QWM_ERR_NOT_CON
 EXPORTED = ("qwm_status_string", "qwm_workspace_bytes", "qwm_create", "qwm_destroy",
             "qwm_update_query_stats", "qwm_fit_centroids", "qwm_quantize_kv", "qwm_attend",
             "qwm_dequantize", "qwm_sync_status", "qwm_update_query_stats_noalloc", "qwm_quantize_kv_full",
+            "qwm_dequantize_chunks", "qwm_select_rank", "qwm_psac_kept", "qwm_psac_plan", "qwm_psac_pack",
             # comparison baselines (include/qwm_baselines.h)
             "qwm_kivi_quantize", "qwm_kivi_dequantize", "qwm_prq_residual", "qwm_prq_dequantize")
 
@@ -48,10 +49,11 @@ class qwm_config(C.Structure):
     _fields_ = [("heads", C.c_int32), ("head_dim", C.c_int32), ("n_centroids", C.c_int32),
                 ("group", C.c_int32), ("top_m", C.c_int32), ("rank", C.c_int32), ("bits", C.c_int32),
                 ("kmeans_iters", C.c_int32), ("seed", C.c_uint64), ("storage", C.c_int32),
-                ("psac_gate", C.c_int32)]
+                ("psac_gate", C.c_int32), ("test_flags", C.c_int32)]
 
 
 QWM_STORAGE_FP16, QWM_STORAGE_COMPACT = 0, 1
+QWM_TEST_EXPIRE_WAIT = 1  # qwm_config.test_flags: one wait of qwm_attend runs out (tests of the error path)
 
 
 class qwm_chunk(C.Structure):
@@ -62,7 +64,16 @@ class qwm_chunk(C.Structure):
                 ("u_r", C.c_void_p), ("cent_k16", C.c_void_p), ("cent_v16", C.c_void_p),
                 ("k_raw", C.c_void_p), ("v_raw", C.c_void_p), ("causal_tpf", C.c_int64),
                 ("k_s8", C.c_void_p), ("v_s8", C.c_void_p), ("k_zp", C.c_void_p), ("v_zp", C.c_void_p),
-                ("k_sigma", C.c_void_p), ("v_sigma", C.c_void_p)]
+                ("k_sigma", C.c_void_p), ("v_sigma", C.c_void_p),
+                ("c_layout", C.c_int32), ("c_heads", C.c_void_p), ("c_mask", C.c_void_p),
+                ("c_tile_rank", C.c_void_p)]
+
+
+QWM_C_DENSE, QWM_C_PER_HEAD = 0, 1
+
+
+class qwm_psac_head(C.Structure):
+    _fields_ = [("c_off", C.c_int64), ("s_off", C.c_int64), ("rank", C.c_int32), ("sparse", C.c_int32)]
 
 
 QWM_CHUNK_PACKED, QWM_CHUNK_BF16 = 0, 1
@@ -87,10 +98,16 @@ _lib.qwm_destroy.argtypes = [_P]
 _lib.qwm_update_query_stats.argtypes = [_P, _P, C.c_int64, _P, _P, _P, _P, _P, _P]
 _lib.qwm_fit_centroids.argtypes = [_P, _P, C.c_int64, _P, _P, _P]
 _lib.qwm_quantize_kv.argtypes = [_P, _P, _P, C.c_int64, _P, _P, C.POINTER(qwm_chunk), C.POINTER(qwm_debug), _P]
-_lib.qwm_quantize_kv_full.argtypes = [_P, _P, _P, C.c_int64, _P, _P, C.POINTER(qwm_chunk), C.POINTER(qwm_debug),
+_lib.qwm_quantize_kv_full.argtypes = [_P, _P, _P, C.c_int64, _P, _P, _P, C.POINTER(qwm_chunk), C.POINTER(qwm_debug),
                                        _P]
 _lib.qwm_attend.argtypes = [_P, _P, C.c_int64, C.POINTER(qwm_chunk), C.c_int32, C.c_float, _P, _P]
 _lib.qwm_dequantize.argtypes = [_P, C.POINTER(qwm_chunk), _P, _P, _P]
+_lib.qwm_dequantize_chunks.argtypes = [_P, C.POINTER(qwm_chunk), C.c_int32, _P, _P, _P]
+_lib.qwm_select_rank.argtypes = [_P, _P, C.c_float, _P, _P, _P]
+_lib.qwm_psac_kept.argtypes = [_P, C.POINTER(qwm_chunk), _P, _P]
+_lib.qwm_psac_plan.argtypes = [C.POINTER(qwm_config), C.c_int64, _P, _P, C.POINTER(qwm_psac_head),
+                               C.POINTER(C.c_int64), C.POINTER(C.c_int64)]
+_lib.qwm_psac_pack.argtypes = [_P, C.POINTER(qwm_chunk), _P, _P, _P, _P, _P, _P]
 _lib.qwm_sync_status.argtypes = [_P, _P]
 _lib.qwm_update_query_stats_noalloc.argtypes = [C.POINTER(qwm_config), _P, C.c_int64, _P, _P, _P, _P, _P, _P, _P]
 _lib.qwm_kivi_quantize.argtypes = [_P, _P, _P, C.c_int64, C.POINTER(qwm_kivi_chunk), _P]
@@ -136,9 +153,9 @@ class Context:
 
     def __init__(self, heads: int, n_centroids: int = 256, top_m: int = 4, rank: int = 8,
                  kmeans_iters: int = 10, head_dim: int = 128, group: int = 64, bits: int = 2,
-                 storage: int = QWM_STORAGE_FP16, psac_gate: int = 0):
+                 storage: int = QWM_STORAGE_FP16, psac_gate: int = 0, test_flags: int = 0):
         self.cfg = qwm_config(heads, head_dim, n_centroids, group, top_m, rank, bits, kmeans_iters, 0, storage,
-                              psac_gate)
+                              psac_gate, test_flags)
         h = C.c_void_p()
         _check(_lib.qwm_create(C.byref(self.cfg), C.byref(h)), "qwm_create")
         self.handle = h
@@ -165,7 +182,9 @@ def qwm_workspace_bytes(cfg: qwm_config) -> int:
 
 @dataclass
 class Chunk:
-    """Device tensors of one packed chunk (all heads), mirroring qwm_chunk."""
+    """Device tensors of one packed chunk (all heads), mirroring qwm_chunk.  cent_k / cent_v are the
+    bf16 codebooks the chunk is packed with (qwm_quantize_kv's input; `release_fit_codebooks` drops
+    them); cent_k16 / cent_v16 are the chunk's stored codebooks."""
     n_tokens: int
     rank_eff: int
     k_codes: torch.Tensor
@@ -176,8 +195,8 @@ class Chunk:
     k_min: torch.Tensor
     v_scale: torch.Tensor
     v_min: torch.Tensor
-    cent_k: torch.Tensor
-    cent_v: torch.Tensor
+    cent_k: torch.Tensor | None
+    cent_v: torch.Tensor | None
     c: torch.Tensor
     c_scale: torch.Tensor
     u_r: torch.Tensor
@@ -190,6 +209,13 @@ class Chunk:
     v_zp: torch.Tensor | None = None
     k_sigma: torch.Tensor | None = None
     v_sigma: torch.Tensor | None = None
+    # per-head PSAC ranks (qwm_select_rank) and the per-head coefficient layout (qwm_psac_pack)
+    head_rank: torch.Tensor | None = None    # int32 [H]
+    c_layout: int = QWM_C_DENSE
+    c_heads: torch.Tensor | None = None      # uint8 [H * 24]: the qwm_psac_head entries
+    c_mask: torch.Tensor | None = None       # int32 (uint32 bits) [H][tiles][4]
+    c_tile_rank: torch.Tensor | None = None  # int32 [H][tiles]
+    plan: list | None = None                 # host copy of the entries: (c_off, s_off, rank, sparse)
 
     @property
     def compact(self) -> bool:
@@ -203,6 +229,11 @@ class Chunk:
         u8 = dict(dtype=torch.uint8, device=dev)
         f16 = dict(dtype=torch.float16, device=dev)
         ix = dict(dtype=torch.uint8 if Cn <= 256 else torch.int16, device=dev)  # int16 = uint16 bits
+        books = (torch.empty(H, Cn, d, dtype=torch.bfloat16, device=dev),
+                 torch.empty(H, Cn, d, dtype=torch.bfloat16, device=dev))
+        psac = (torch.zeros(H, n, max(r, 1), dtype=torch.int8, device=dev), torch.zeros(H, n, **f16),
+                torch.zeros(H, d, max(r, 1), dtype=torch.bfloat16, device=dev))
+        stored = (torch.empty(H, Cn, d, **f16), torch.empty(H, Cn, d, **f16))
         if cfg.storage == QWM_STORAGE_COMPACT:
             nt = (n + 127) // 128
             z = lambda *shape, **kw: torch.zeros(*shape, **kw)
@@ -210,12 +241,7 @@ class Chunk:
                          torch.empty(H, n, d // 4, **u8), torch.empty(H, n, d // 4, **u8),
                          torch.empty(H, n, **ix), torch.empty(H, n, **ix),
                          z(0, **f16), z(0, **f16), z(0, **f16), z(0, **f16),
-                         torch.empty(H, Cn, d, dtype=torch.bfloat16, device=dev),
-                         torch.empty(H, Cn, d, dtype=torch.bfloat16, device=dev),
-                         torch.zeros(H, n, max(r, 1), dtype=torch.int8, device=dev),
-                         torch.zeros(H, n, **f16),
-                         torch.zeros(H, d, max(r, 1), dtype=torch.bfloat16, device=dev),
-                         torch.empty(H, Cn, d, **f16), torch.empty(H, Cn, d, **f16),
+                         *books, *psac, *stored,
                          torch.empty(H, n, G, **u8), torch.empty(H, n, G, **u8),
                          torch.empty(H, max(n, 1), **u8), torch.empty(H, max(n, 1), **u8),
                          torch.empty(H, max(nt, 1), G, **f16), torch.empty(H, max(nt, 1), G, **f16))
@@ -224,39 +250,43 @@ class Chunk:
                      torch.empty(H, n, **ix), torch.empty(H, n, **ix),
                      torch.empty(H, n, G, **f16), torch.empty(H, n, G, **f16),
                      torch.empty(H, n, G, **f16), torch.empty(H, n, G, **f16),
-                     torch.empty(H, Cn, d, dtype=torch.bfloat16, device=dev),
-                     torch.empty(H, Cn, d, dtype=torch.bfloat16, device=dev),
-                     torch.zeros(H, n, max(r, 1), dtype=torch.int8, device=dev),
-                     torch.zeros(H, n, **f16),
-                     torch.zeros(H, d, max(r, 1), dtype=torch.bfloat16, device=dev),
-                     torch.empty(H, Cn, d, **f16), torch.empty(H, Cn, d, **f16))
+                     *books, *psac, *stored)
 
-    def nbytes(self, operand_copies: bool = False) -> int:
-        """Bytes of the packed representation (codebooks and PSAC basis included); with
-        `operand_copies`, also the fp16 codebook copies the attention kernel reads."""
+    def release_fit_codebooks(self) -> None:
+        """Drop the bf16 codebooks (needed only by qwm_quantize_kv); the stored fp16 ones remain."""
+        self.cent_k = None
+        self.cent_v = None
+
+    def nbytes(self) -> int:
+        """Bytes of the packed representation: everything qwm_attend and qwm_dequantize read (codes,
+        indices, INT2 metadata, stored codebooks, PSAC coefficients, their layout and the basis)."""
         meta = ((self.k_s8, self.v_s8, self.k_sigma, self.v_sigma) if self.compact
                 else (self.k_scale, self.k_min, self.v_scale, self.v_min))
-        tot = sum(t.numel() * t.element_size() for t in (self.k_codes, self.v_codes, self.k_idx, self.v_idx,
-                                                         self.cent_k, self.cent_v) + meta)
+        nb = lambda ts: sum(t.numel() * t.element_size() for t in ts)
+        tot = nb((self.k_codes, self.v_codes, self.k_idx, self.v_idx, self.cent_k16, self.cent_v16) + meta)
         if self.compact:  # the two groups' 2-bit zero-points of a token share one byte
             tot += self.k_zp.numel() + self.v_zp.numel()
         if self.rank_eff:
-            tot += sum(t.numel() * t.element_size() for t in (self.c, self.c_scale, self.u_r))
-        if operand_copies:
-            tot += sum(t.numel() * t.element_size() for t in (self.cent_k16, self.cent_v16))
+            tot += nb((self.c, self.c_scale, self.u_r))
+            if self.c_layout == QWM_C_PER_HEAD:
+                tot += nb((self.c_heads, self.c_mask, self.c_tile_rank))
         return tot
 
     def struct(self) -> qwm_chunk:
         def p(t, width):
             return _ptr(t, "chunk field", width)
+        ph = self.c_layout == QWM_C_PER_HEAD
         return qwm_chunk(self.n_tokens, self.rank_eff, QWM_CHUNK_PACKED,
                          p(self.k_codes, 1), p(self.v_codes, 1),
                          p(self.k_idx, self.k_idx.element_size()), p(self.v_idx, self.v_idx.element_size()),
                          p(self.k_scale, 2), p(self.k_min, 2), p(self.v_scale, 2), p(self.v_min, 2),
                          p(self.cent_k, 2), p(self.cent_v, 2), p(self.c, 1), p(self.c_scale, 2), p(self.u_r, 2),
-                         p(self.cent_k16, 2), p(self.cent_v16, 2), None, None, 0,
+                         p(self.cent_k16, 2), p(self.cent_v16, 2),
+                         None, None, 0,
                          *(p(t, w) for t, w in ((self.k_s8, 1), (self.v_s8, 1), (self.k_zp, 1), (self.v_zp, 1),
-                                                (self.k_sigma, 2), (self.v_sigma, 2))))
+                                                (self.k_sigma, 2), (self.v_sigma, 2))),
+                         self.c_layout, p(self.c_heads, 1) if ph else None, p(self.c_mask, 4) if ph else None,
+                         p(self.c_tile_rank, 4) if ph else None)
 
 
 @dataclass
@@ -330,6 +360,16 @@ def qwm_dequantize(ctx: Context, chunk: Chunk, k_hat, v_hat, stream=None) -> Non
     _check(st, "qwm_dequantize")
 
 
+def qwm_dequantize_chunks(ctx: Context, chunks, k_hat, v_hat, stream=None) -> None:
+    """Decode several packed chunks in one launch into [H][sum N][d] (chunks in order)."""
+    H, d = ctx.cfg.heads, ctx.cfg.head_dim
+    total = sum(c.n_tokens for c in chunks)
+    arr = (qwm_chunk * len(chunks))(*[c.struct() for c in chunks])
+    st = _lib.qwm_dequantize_chunks(ctx.handle, arr, len(chunks), _ptr(k_hat, "k_hat", 2, (H, total, d)),
+                                    _ptr(v_hat, "v_hat", 2, (H, total, d)), _stream(stream))
+    _check(st, "qwm_dequantize_chunks")
+
+
 def qwm_sync_status(ctx: Context, stream=None) -> int:
     """Wait for the stream and return (and clear) the first device-side error status (0 = none)."""
     return _lib.qwm_sync_status(ctx.handle, _stream(stream))
@@ -346,6 +386,70 @@ def qwm_update_query_stats_noalloc(cfg: qwm_config, q, nq: int, S, n, w, eigvals
         _ptr(eigvals, "eigvals", 4, (H, d)), _ptr(u_r, "u_r", 2, (H, d, r)) if r else None,
         _ptr(dev_status, "dev_status", 4, (1,)), _stream(stream))
     _check(st, "qwm_update_query_stats_noalloc")
+
+
+def qwm_select_rank(ctx: Context, eigvals, energy: float, u_r, head_rank, stream=None) -> None:
+    """Per-head PSAC rank from the eigen-energy share (columns of u_r past each head's rank zeroed)."""
+    H, d, r = ctx.cfg.heads, ctx.cfg.head_dim, ctx.cfg.rank
+    st = _lib.qwm_select_rank(ctx.handle, _ptr(eigvals, "eigvals", 4, (H, d)), float(energy),
+                              _ptr(u_r, "u_r", 2, (H, d, r)) if r else None, _ptr(head_rank, "head_rank", 4, (H,)),
+                              _stream(stream))
+    _check(st, "qwm_select_rank")
+
+
+def qwm_psac_kept(ctx: Context, chunk: "Chunk", kept, stream=None) -> None:
+    s = chunk.struct()
+    st = _lib.qwm_psac_kept(ctx.handle, C.byref(s), _ptr(kept, "kept", 4, (ctx.cfg.heads,)), _stream(stream))
+    _check(st, "qwm_psac_kept")
+
+
+def qwm_psac_plan(cfg: qwm_config, n: int, head_rank, kept):
+    """Host: (plan entries [(c_off, s_off, rank, sparse)] per head, bytes of c, scales of c_scale)."""
+    H = cfg.heads
+    hr = (C.c_int32 * H)(*[int(x) for x in head_rank])
+    kp = (C.c_int32 * H)(*[int(x) for x in kept])
+    plan = (qwm_psac_head * H)()
+    cb, ns = C.c_int64(), C.c_int64()
+    _check(_lib.qwm_psac_plan(C.byref(cfg), n, C.cast(hr, _P), C.cast(kp, _P), plan, C.byref(cb), C.byref(ns)),
+           "qwm_psac_plan")
+    return [(e.c_off, e.s_off, e.rank, e.sparse) for e in plan], cb.value, ns.value, bytes(plan)
+
+
+def qwm_psac_pack(ctx: Context, dense: "Chunk", plan_dev, c, c_scale, c_mask, c_tile_rank, stream=None) -> None:
+    s = dense.struct()
+    st = _lib.qwm_psac_pack(ctx.handle, C.byref(s), _ptr(plan_dev, "plan", 1), _ptr(c, "c", 1),
+                            _ptr(c_scale, "c_scale", 2), _ptr(c_mask, "c_mask", 4), _ptr(c_tile_rank, "c_tile_rank", 4),
+                            _stream(stream))
+    _check(st, "qwm_psac_pack")
+
+
+def pack_psac_layout(ctx: Context, chunk: "Chunk", head_rank=None, stream=None) -> None:
+    """Repack a dense chunk's PSAC coefficients into the per-head layout (each head its rank r_h and
+    the smaller of the dense and sparse layouts): count the kept tokens per head, plan on the host
+    (a synchronisation), allocate exactly the planned buffers, pack.  head_rank: device int32 [H]
+    (qwm_select_rank's output), or None for config.rank on every head."""
+    if not chunk.rank_eff or chunk.c_layout != QWM_C_DENSE or chunk.n_tokens == 0:
+        return
+    cfg = ctx.cfg
+    H, n = cfg.heads, chunk.n_tokens
+    dev = chunk.c.device
+    kept = torch.empty(H, dtype=torch.int32, device=dev)
+    qwm_psac_kept(ctx, chunk, kept, stream)
+    (stream if stream is not None else torch.cuda.current_stream(dev)).synchronize()
+    ranks = head_rank.cpu().tolist() if head_rank is not None else [chunk.rank_eff] * H
+    plan, c_bytes, n_scales, raw = qwm_psac_plan(cfg, n, ranks, kept.cpu().tolist())
+    tiles = (n + 127) // 128
+    plan_dev = torch.frombuffer(bytearray(raw), dtype=torch.uint8).to(dev)
+    c = torch.zeros(max(c_bytes, 1), dtype=torch.int8, device=dev)
+    sc = torch.zeros(max(n_scales, 1), dtype=torch.float16, device=dev)
+    mask = torch.zeros(H, tiles, 4, dtype=torch.int32, device=dev)
+    trank = torch.zeros(H, tiles, dtype=torch.int32, device=dev)
+    qwm_psac_pack(ctx, chunk, plan_dev, c, sc, mask, trank, stream)
+    chunk.c, chunk.c_scale = c, sc
+    chunk.c_heads, chunk.c_mask, chunk.c_tile_rank = plan_dev, mask, trank
+    chunk.c_layout, chunk.plan = QWM_C_PER_HEAD, plan
+    if head_rank is not None:
+        chunk.head_rank = head_rank
 
 
 def qwm_status_string(status: int) -> str:
@@ -429,9 +533,10 @@ def qwm_prq_dequantize(ctx: Context, last: Chunk, cent1_k, idx1_k, cent1_v, idx1
                                    _stream(stream)), "qwm_prq_dequantize")
 
 
-def qwm_quantize_kv_full(ctx: Context, k, v, n: int, M, u_r, out: Chunk, debug: dict | None = None,
+def qwm_quantize_kv_full(ctx: Context, k, v, n: int, S, n_seen, u_r, out: Chunk, debug: dict | None = None,
                          stream=None) -> None:
-    """qwm_quantize_kv with the QSAC candidates ranked by (k - mu)^T M (k - mu) (M fp32 [H][d][d])."""
+    """qwm_quantize_kv with the QSAC candidates ranked by (k - mu)^T M (k - mu), M = S / n_seen formed
+    by the library from the running statistics (S fp32 [H][d][d], n_seen int64 [H])."""
     H, d, r = ctx.cfg.heads, ctx.cfg.head_dim, ctx.cfg.rank
     s = out.struct()
     dbg = None
@@ -439,7 +544,8 @@ def qwm_quantize_kv_full(ctx: Context, k, v, n: int, M, u_r, out: Chunk, debug: 
         dbg = qwm_debug(_ptr(debug.get("c_f32"), "c_f32", 4), _ptr(debug.get("cand"), "cand", 4),
                         _ptr(debug.get("score"), "score", 4), _ptr(debug.get("gate_err"), "gate_err", 4))
     st = _lib.qwm_quantize_kv_full(ctx.handle, _ptr(k, "k", 2, (H, n, d)), _ptr(v, "v", 2, (H, n, d)), n,
-                                   _ptr(M, "M", 4, (H, d, d)), _ptr(u_r, "u_r", 2, (H, d, r)) if r else None,
+                                   _ptr(S, "S", 4, (H, d, d)), _ptr(n_seen, "n_seen", 8, (H,)),
+                                   _ptr(u_r, "u_r", 2, (H, d, r)) if r else None,
                                    C.byref(s), C.byref(dbg) if dbg is not None else None, _stream(stream))
     _check(st, "qwm_quantize_kv_full")
     out.rank_eff = s.rank_eff

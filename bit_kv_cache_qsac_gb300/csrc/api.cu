@@ -11,7 +11,7 @@ constexpr int kStatsSplits = 8;
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
-  size_t status, stats_part, km_sum, km_cnt, km_cent, km_img, q_img, q_bfull, total;
+  size_t status, stats_part, km_sum, km_cnt, km_cent, km_img, q_img, q_bfull, q_mfull, total;
 };
 
 Layout layout_of(const qwm_config &c) {
@@ -26,6 +26,7 @@ Layout layout_of(const qwm_config &c) {
   L.km_img = off; off = align_up(off + kmeans_image_bytes(c.heads, c.n_centroids), 1024);
   L.q_img = off; off = align_up(off + quantize_image_bytes(c.heads, c.n_centroids), 1024);
   L.q_bfull = off; off = align_up(off + (size_t)c.heads * c.n_centroids * QWM_D * sizeof(float), 256);
+  L.q_mfull = off; off = align_up(off + (size_t)c.heads * QWM_D * QWM_D * sizeof(float), 256);
   L.total = off;
   return L;
 }
@@ -45,6 +46,7 @@ qwm_status check_config(const qwm_config *c) {
   if ((int64_t)c->heads > 4096) return QWM_ERR_SHAPE;
   if (c->storage != QWM_STORAGE_FP16 && c->storage != QWM_STORAGE_COMPACT) return QWM_ERR_ARG;
   if (c->psac_gate != 0 && c->psac_gate != 1) return QWM_ERR_ARG;
+  if (c->test_flags & ~QWM_TEST_EXPIRE_WAIT) return QWM_ERR_ARG;
   return QWM_OK;
 }
 
@@ -53,7 +55,10 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 qwm_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QWM_OK : QWM_ERR_CUDA; }
 
 // A chunk descriptor is usable when every pointer it needs is set and aligned.
-qwm_status check_chunk(const qwm_config &c, const qwm_chunk *ch, bool need_f16) {
+// A chunk descriptor is usable when every pointer it needs is set and aligned.  `packing`: for
+// qwm_quantize_kv (the bf16 codebooks are read, the stored fp16 ones written); otherwise for
+// qwm_attend / qwm_dequantize (the stored codebooks and the coefficient layout are read).
+qwm_status check_chunk(const qwm_config &c, const qwm_chunk *ch, bool packing) {
   if (!ch) return QWM_ERR_ARG;
   if (ch->n_tokens < 0) return QWM_ERR_ARG;
   if (ch->kind == QWM_CHUNK_BF16) {
@@ -64,27 +69,29 @@ qwm_status check_chunk(const qwm_config &c, const qwm_chunk *ch, bool need_f16) 
   }
   if (ch->kind != QWM_CHUNK_PACKED) return QWM_ERR_ARG;
   if (ch->rank_eff != 0 && ch->rank_eff != c.rank) return QWM_ERR_SHAPE;
+  if (ch->c_layout != QWM_C_DENSE && ch->c_layout != QWM_C_PER_HEAD) return QWM_ERR_ARG;
+  if (packing && ch->c_layout != QWM_C_DENSE) return QWM_ERR_ARG;
   const bool compact = c.storage == QWM_STORAGE_COMPACT;
-  const void *req[] = {ch->k_codes, ch->v_codes, ch->k_idx, ch->v_idx, ch->cent_k, ch->cent_v,
+  const void *req[] = {ch->k_codes, ch->v_codes, ch->k_idx, ch->v_idx, ch->cent_k16, ch->cent_v16,
                        compact ? (const void *)ch->k_s8 : ch->k_scale, compact ? (const void *)ch->k_zp : ch->k_min,
                        compact ? (const void *)ch->v_s8 : ch->v_scale, compact ? (const void *)ch->v_zp : ch->v_min,
-                       compact ? (const void *)ch->k_sigma : ch->k_codes, compact ? (const void *)ch->v_sigma : ch->v_codes};
+                       compact ? (const void *)ch->k_sigma : ch->k_codes, compact ? (const void *)ch->v_sigma : ch->v_codes,
+                       packing ? (const void *)ch->cent_k : ch->k_codes, packing ? (const void *)ch->cent_v : ch->k_codes};
   for (const void *p : req) {
     if (!p) return QWM_ERR_ARG;
     if (!aligned16(p)) return QWM_ERR_ALIGN;
-  }
-  if (need_f16) {  // fp16 codebook copies: written by qwm_quantize_kv, read by qwm_attend
-    const void *f16[] = {ch->cent_k16, ch->cent_v16};
-    for (const void *p : f16) {
-      if (!p) return QWM_ERR_ARG;
-      if (!aligned16(p)) return QWM_ERR_ALIGN;
-    }
   }
   if (ch->rank_eff > 0) {
     const void *psac[] = {ch->c, ch->c_scale, ch->u_r};
     for (const void *p : psac) {
       if (!p) return QWM_ERR_ARG;
-      if (!aligned16(p)) return QWM_ERR_ALIGN;
+      if (ch->c_layout == QWM_C_DENSE && !aligned16(p)) return QWM_ERR_ALIGN;
+    }
+    if (ch->c_layout == QWM_C_PER_HEAD) {  // rows of r_h bytes: c and c_scale need no 16-byte alignment
+      if (!ch->c_heads || !ch->c_mask || !ch->c_tile_rank) return QWM_ERR_ARG;
+      if (!aligned16(ch->c_heads) || !aligned16(ch->c_mask) || !aligned16(ch->c_tile_rank) || !aligned16(ch->u_r) ||
+          ((uintptr_t)ch->c_scale & 1u))
+        return QWM_ERR_ALIGN;
     }
   }
   return QWM_OK;
@@ -148,13 +155,31 @@ qwm_status qwm_create(const qwm_config *cfg, qwm_ctx **out) {
   ctx->km_img = (unsigned char *)(base + L.km_img);
   ctx->q_img = (unsigned char *)(base + L.q_img);
   ctx->q_bfull = (float *)(base + L.q_bfull);
+  ctx->q_mfull = (float *)(base + L.q_mfull);
+  if (cudaStreamCreateWithFlags(&ctx->side, cudaStreamNonBlocking) != cudaSuccess) {
+    cudaFree(ctx->ws);
+    free(ctx);
+    return QWM_ERR_CUDA;
+  }
+  if (cudaEventCreateWithFlags(&ctx->fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&ctx->join, cudaEventDisableTiming) != cudaSuccess) {
+    if (ctx->fork) cudaEventDestroy(ctx->fork);
+    cudaStreamDestroy(ctx->side);
+    cudaFree(ctx->ws);
+    free(ctx);
+    return QWM_ERR_CUDA;
+  }
   *out = ctx;
   return QWM_OK;
 }
 
 qwm_status qwm_destroy(qwm_ctx *ctx) {
   if (!ctx) return QWM_ERR_ARG;
-  cudaError_t e = cudaFree(ctx->ws);
+  cudaError_t e = cudaStreamSynchronize(ctx->side);
+  if (cudaEventDestroy(ctx->fork) != cudaSuccess) e = cudaErrorUnknown;
+  if (cudaEventDestroy(ctx->join) != cudaSuccess) e = cudaErrorUnknown;
+  if (cudaStreamDestroy(ctx->side) != cudaSuccess) e = cudaErrorUnknown;
+  if (cudaFree(ctx->ws) != cudaSuccess) e = cudaErrorUnknown;
   free(ctx);
   return cuda_status(e);
 }
@@ -195,8 +220,8 @@ qwm_status qwm_fit_centroids(qwm_ctx *ctx, const uint16_t *x, int64_t n, const u
 }
 
 static qwm_status quantize_impl(qwm_ctx *ctx, const uint16_t *k, const uint16_t *v, int64_t n, const float *w,
-                                const float *M, const uint16_t *u_r, qwm_chunk *out, const qwm_debug *dbg,
-                                qwm_stream stream) {
+                                const float *S, const int64_t *n_seen, const uint16_t *u_r, qwm_chunk *out,
+                                const qwm_debug *dbg, qwm_stream stream) {
   if (!ctx || !out || n < 0) return QWM_ERR_ARG;
   if (out->n_tokens != n) return QWM_ERR_SHAPE;
   if (out->kind != QWM_CHUNK_PACKED) return QWM_ERR_ARG;
@@ -206,7 +231,8 @@ static qwm_status quantize_impl(qwm_ctx *ctx, const uint16_t *k, const uint16_t 
   }
   if (!k || !v) return QWM_ERR_ARG;
   if (n > ((int64_t)1 << 31) / QWM_D) return QWM_ERR_SHAPE;
-  if (!aligned16(k) || !aligned16(v) || (w && !aligned16(w)) || (M && !aligned16(M)) || (u_r && !aligned16(u_r)))
+  if (!aligned16(k) || !aligned16(v) || (w && !aligned16(w)) || (S && !aligned16(S)) ||
+      (n_seen && !aligned16(n_seen)) || (u_r && !aligned16(u_r)))
     return QWM_ERR_ALIGN;
   if (out->kind != QWM_CHUNK_PACKED) return QWM_ERR_ARG;
   const bool psac = (u_r != nullptr) && ctx->cfg.rank > 0;
@@ -219,20 +245,22 @@ static qwm_status quantize_impl(qwm_ctx *ctx, const uint16_t *k, const uint16_t 
       return QWM_ERR_ALIGN;
   }
   if (n == 0) return QWM_OK;
-  cudaError_t e = launch_quantize(ctx->cfg, k, v, n, w, M, ctx->q_bfull, psac ? u_r : nullptr, *out, dbg,
-                                  ctx->status, ctx->num_sms, ctx->q_img, (cudaStream_t)stream);
+  cudaError_t e = launch_quantize(ctx->cfg, k, v, n, w, S, n_seen, ctx->q_mfull, ctx->q_bfull, psac ? u_r : nullptr,
+                                  *out, dbg, ctx->status, ctx->num_sms, ctx->q_img, (cudaStream_t)stream, ctx->side,
+                                  ctx->fork, ctx->join);
   return cuda_status(e);
 }
 
 qwm_status qwm_quantize_kv(qwm_ctx *ctx, const uint16_t *k, const uint16_t *v, int64_t n, const float *w,
                            const uint16_t *u_r, qwm_chunk *out, const qwm_debug *dbg, qwm_stream stream) {
-  return quantize_impl(ctx, k, v, n, w, nullptr, u_r, out, dbg, stream);
+  return quantize_impl(ctx, k, v, n, w, nullptr, nullptr, u_r, out, dbg, stream);
 }
 
-qwm_status qwm_quantize_kv_full(qwm_ctx *ctx, const uint16_t *k, const uint16_t *v, int64_t n, const float *M,
-                                const uint16_t *u_r, qwm_chunk *out, const qwm_debug *dbg, qwm_stream stream) {
-  if (!M) return QWM_ERR_ARG;
-  return quantize_impl(ctx, k, v, n, nullptr, M, u_r, out, dbg, stream);
+qwm_status qwm_quantize_kv_full(qwm_ctx *ctx, const uint16_t *k, const uint16_t *v, int64_t n, const float *S,
+                                const int64_t *n_seen, const uint16_t *u_r, qwm_chunk *out, const qwm_debug *dbg,
+                                qwm_stream stream) {
+  if (!S || !n_seen) return QWM_ERR_ARG;
+  return quantize_impl(ctx, k, v, n, nullptr, S, n_seen, u_r, out, dbg, stream);
 }
 
 qwm_status qwm_attend(qwm_ctx *ctx, const uint16_t *q, int64_t nq, const qwm_chunk *chunks, int32_t n_chunks,
@@ -247,7 +275,7 @@ qwm_status qwm_attend(qwm_ctx *ctx, const uint16_t *q, int64_t nq, const qwm_chu
   for (int i = 0; i < n_chunks; i++) {
     if (chunks[i].n_tokens < 0) return QWM_ERR_ARG;
     if (chunks[i].n_tokens == 0) continue;  // skipped: its pointers may be NULL
-    qwm_status s = check_chunk(ctx->cfg, &chunks[i], true);
+    qwm_status s = check_chunk(ctx->cfg, &chunks[i], false);
     if (s != QWM_OK) return s;
     total += chunks[i].n_tokens;
   }
@@ -267,8 +295,64 @@ qwm_status qwm_dequantize(qwm_ctx *ctx, const qwm_chunk *chunk, uint16_t *k_hat,
   if (s != QWM_OK) return s;
   if ((k_hat && !aligned16(k_hat)) || (v_hat && !aligned16(v_hat))) return QWM_ERR_ALIGN;
   if (chunk->n_tokens == 0 || (!k_hat && !v_hat)) return QWM_OK;
-  cudaError_t e = launch_dequantize(ctx->cfg, *chunk, k_hat, v_hat, (cudaStream_t)stream);
+  cudaError_t e = launch_dequantize(ctx->cfg, chunk, 1, k_hat, v_hat, (cudaStream_t)stream);
   return cuda_status(e);
+}
+
+qwm_status qwm_dequantize_chunks(qwm_ctx *ctx, const qwm_chunk *chunks, int32_t n_chunks, uint16_t *k_hat,
+                                 uint16_t *v_hat, qwm_stream stream) {
+  if (!ctx || !chunks || n_chunks < 1) return QWM_ERR_ARG;
+  if (n_chunks > 128) return QWM_ERR_SHAPE;
+  for (int i = 0; i < n_chunks; i++) {
+    if (chunks[i].n_tokens < 0) return QWM_ERR_ARG;
+    if (chunks[i].kind == QWM_CHUNK_BF16) return QWM_ERR_UNSUPPORTED;
+    if (chunks[i].n_tokens == 0) continue;  // skipped: its pointers may be NULL
+    qwm_status s = check_chunk(ctx->cfg, &chunks[i], false);
+    if (s != QWM_OK) return s;
+  }
+  if ((k_hat && !aligned16(k_hat)) || (v_hat && !aligned16(v_hat))) return QWM_ERR_ALIGN;
+  cudaError_t e = launch_dequantize(ctx->cfg, chunks, n_chunks, k_hat, v_hat, (cudaStream_t)stream);
+  return cuda_status(e);
+}
+
+qwm_status qwm_select_rank(qwm_ctx *ctx, const float *eigvals, float energy, uint16_t *u_r, int32_t *head_rank,
+                           qwm_stream stream) {
+  if (!ctx || !eigvals || !head_rank) return QWM_ERR_ARG;
+  if (!(energy >= 0.f && energy <= 1.f)) return QWM_ERR_ARG;
+  if (ctx->cfg.rank > 0 && !u_r) return QWM_ERR_ARG;
+  if (!aligned16(eigvals) || !aligned16(head_rank) || (u_r && !aligned16(u_r))) return QWM_ERR_ALIGN;
+  return cuda_status(launch_select_rank(eigvals, energy, ctx->cfg.heads, ctx->cfg.rank, u_r, head_rank,
+                                        (cudaStream_t)stream));
+}
+
+qwm_status qwm_psac_kept(qwm_ctx *ctx, const qwm_chunk *chunk, int32_t *kept, qwm_stream stream) {
+  if (!ctx || !chunk || !kept) return QWM_ERR_ARG;
+  if (chunk->kind != QWM_CHUNK_PACKED || chunk->c_layout != QWM_C_DENSE || chunk->rank_eff < 1) return QWM_ERR_ARG;
+  if (chunk->n_tokens < 0 || !chunk->c_scale) return QWM_ERR_ARG;
+  if (!aligned16(kept) || !aligned16(chunk->c_scale)) return QWM_ERR_ALIGN;
+  return cuda_status(launch_psac_kept(chunk->c_scale, chunk->n_tokens, ctx->cfg.heads, kept, (cudaStream_t)stream));
+}
+
+qwm_status qwm_psac_plan(const qwm_config *cfg, int64_t n, const int32_t *head_rank, const int32_t *kept,
+                         qwm_psac_head *plan, int64_t *c_bytes, int64_t *n_scales) {
+  qwm_status s = check_config(cfg);
+  if (s != QWM_OK) return s;
+  if (n < 0 || !head_rank || !kept || !plan) return QWM_ERR_ARG;
+  for (int h = 0; h < cfg->heads; h++)
+    if (head_rank[h] < 0 || head_rank[h] > cfg->rank || kept[h] < 0 || kept[h] > n) return QWM_ERR_ARG;
+  psac_plan_host(cfg->heads, n, head_rank, kept, plan, c_bytes, n_scales);
+  return QWM_OK;
+}
+
+qwm_status qwm_psac_pack(qwm_ctx *ctx, const qwm_chunk *dense, const qwm_psac_head *plan, int8_t *c,
+                         uint16_t *c_scale, uint32_t *c_mask, int32_t *c_tile_rank, qwm_stream stream) {
+  if (!ctx || !dense || !plan || !c_mask || !c_tile_rank) return QWM_ERR_ARG;
+  if (dense->kind != QWM_CHUNK_PACKED || dense->c_layout != QWM_C_DENSE || dense->rank_eff < 1) return QWM_ERR_ARG;
+  if (dense->n_tokens < 1 || !dense->c || !dense->c_scale) return QWM_ERR_ARG;
+  if (!aligned16(plan) || !aligned16(c_mask) || !aligned16(c_tile_rank) || ((uintptr_t)c_scale & 1u))
+    return QWM_ERR_ALIGN;
+  return cuda_status(launch_psac_pack(dense->c, dense->c_scale, dense->n_tokens, ctx->cfg.heads, dense->rank_eff, plan,
+                                      c, c_scale, c_mask, c_tile_rank, (cudaStream_t)stream));
 }
 
 qwm_status qwm_sync_status(qwm_ctx *ctx, qwm_stream stream) {

@@ -7,23 +7,28 @@
 // packed chunk inside the kernel.  Nothing decoded is written to global memory.
 //
 // Arithmetic.  Both MMAs take fp16 operands (fp32 accumulate): fp16's 11-bit significand keeps the
-// logits of the outlier channels (|k| up to ~40) accurate where bf16 would not, and Q (bf16 in
-// memory) converts to fp16 exactly.  A Key or Value row is decoded in packed fp16 pairs from an
-// fp16 copy of the codebook as fp16(mu + fp16(m + s q_code)): the small residual first, as in
-// the packing, then the centroid (two roundings, both at the scale of their results).  The PSAC
-// term rides on a small second MMA whose K columns are [q U_r | 0 | 1] against [c_hat | 0 | mask],
-// where mask = -60000 on the zero rows that pad the last tile of a chunk (their probabilities
-// underflow to exactly 0) and 0 elsewhere.
+// logits of the outlier channels (|k| up to ~40) accurate where bf16 would not.  Q (bf16 in memory)
+// converts to fp16 exactly for magnitudes in [2^-24, 65504] (an element beyond 65504 records
+// QWM_ERR_RANGE; smaller ones round to fp16's subnormal grid, far below any logit's rounding).  A Key
+// or Value row is decoded in packed fp16 pairs from the chunk's fp16 codebook row as
+// fp16(mu + fp16(m + s q_code)): the small residual first, as in the packing, then the centroid (two
+// roundings, both at the scale of their results).  The PSAC term rides on a
+// small second MMA whose K columns are [q U_r | 0 | 1] against [c_hat | 0 | mask], where mask = -inf
+// (fp16) on the zero rows that pad the last tile of a chunk and 0 elsewhere: their logits are -inf
+// whatever the softmax scale and their weights exactly 0.
 // O is written in fp32: the output is an average over thousands of keys, its largest entries are
 // ~16x its RMS, and rounding those to bf16 alone would cost ~0.03 x RMS(O).
 // The chunk still being generated (English v2 summary §5.1, §D.1: a chunk is quantised once it is
 // complete) may join the call as a bf16 chunk: its producers copy the rows themselves and convert
-// them to fp16 in place instead of decoding, its second-MMA operands carry only the padding mask,
-// and an optional block-causal mask (frames of tpf tokens; Query row i = token i of that chunk) is
-// applied by the softmax, which sets the logits of later frames to -inf.  Chunks with the compact
-// INT2 metadata (8-bit step s8, 2-bit zero-point z, power-of-two second-level scale sigma per
-// 128-token tile) decode with s = sigma s8 and m = -z s, exact in fp16, through the same
-// fp16(mu + fp16(m + s q)).  Calls with neither run a variant compiled without any of it.
+// them to fp16 in place instead of decoding (an element beyond the fp16 range records
+// QWM_ERR_RANGE), its second-MMA operands carry only the padding mask, and an optional block-causal
+// mask (frames of tpf tokens; Query row i = token i of that chunk) is applied by the softmax, which
+// sets the logits of later frames to -inf.  Chunks with the compact INT2 metadata (8-bit step s8, 2-bit zero-point z,
+// power-of-two second-level scale sigma per 128-token tile) decode with s = sigma s8 and m = -z s,
+// exact in fp16, through the same fp16(mu + fp16(m + s q)).  Chunks whose PSAC coefficients are in
+// the per-head layout (each head its own rank, rows for every token or only for the kept ones) have
+// each Key row's coefficients looked up through the head's entry and, for a sparse head, the tile
+// bitmap.  Calls with none of these run a variant compiled without any of it.
 //
 // Work split: a pair of CTAs (a cluster of two, cta_group::2 MMAs) takes one head x 512 Queries;
 // CTA c of the pair holds Query rows 256 x + 128 c .. 256 x + 128 c + 127 of its two tiles x = 0, 1.
@@ -68,8 +73,9 @@ constexpr int kSoftmaxWarps = 8, kMmaWarp = 8, kKWarp0 = 9, kVWarp0 = 13, kProdW
 constexpr int kThreads = 32 * (kSoftmaxWarps + 1 + 2 * kProdWarps);  // 544
 constexpr int kMaxChunks = 128;
 constexpr uint64_t kWaitNs = 1000000000ull;
+constexpr uint64_t kTestWaitNs = 1000000ull;  // the test hook's wait limit
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
-constexpr uint32_t kMaskBits = 0xFB53u;    // fp16 -60000
+constexpr uint32_t kMaskBits = 0xFC00u;    // fp16 -inf: the logit of a row that pads a chunk's last tile
 
 constexpr int kStages = 3;                 // K / V / X stages in shared memory
 constexpr int kPairQ = 2 * NQT * BM;       // Queries per CTA pair
@@ -115,6 +121,10 @@ struct AttnChunk {
   const uint8_t *k_codes, *v_codes, *k_idx, *v_idx;
   const uint16_t *k_scale, *k_min, *v_scale, *v_min, *cent_k16, *cent_v16, *c_scale, *u_r;
   const int8_t *c;
+  int per_head;                       // QWM_C_PER_HEAD coefficients (c_heads, c_mask, c_tile_rank)
+  const qwm_psac_head *c_heads;
+  const uint32_t *c_mask;
+  const int32_t *c_tile_rank;
 };
 
 struct AttnParams {
@@ -125,6 +135,7 @@ struct AttnParams {
   int compact;       // the chunks' INT2 metadata is the compact form (8-bit step, 2-bit zero-point)
   int any_causal;    // a bf16 chunk with a block-causal mask
   float scale_log2;  // softmax_scale * log2(e)
+  int test_expire;   // QWM_TEST_EXPIRE_WAIT: the MMA thread's wait before tile 1 runs out
   int32_t *status;
   AttnChunk ch[kMaxChunks];
 };
@@ -132,6 +143,7 @@ struct AttnParams {
 struct Bars {
   uint64_t k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
   uint64_t s_full[2], p_ready[2], qx_full[2], qx_free[2], u_ready[2], o_done, drain;
+  uint64_t never;  // test hook: a barrier nothing completes
 };
 
 __device__ __forceinline__ void fail(int *abort_flag, int32_t *status) {
@@ -177,8 +189,7 @@ __device__ __forceinline__ void write_x_row(const Row &d, int R, uint32_t xs, in
 }
 
 // Query row rr of a Query tile: its row of the second MMA's A operand, [q U_r | 0 0 0 0 | 1 | 0 ...],
-// with q read from the tile's fp16 copy in shared memory (exact: bf16 Queries convert to fp16
-// exactly) and U_r from its fp32 copy in shared memory ([128 channels][kRU], zero past the rank;
+// with q read from the tile's fp16 copy in shared memory and U_r from its fp32 copy in shared memory ([128 channels][kRU], zero past the rank;
 // every lane reads the same words, so the reads broadcast).
 template <bool WIDE>
 __device__ __forceinline__ void write_qx_row(int R, bool live, uint32_t qtile, uint32_t ubuf, uint32_t dst, int rr) {
@@ -209,7 +220,7 @@ __device__ __forceinline__ void write_qx_row(int R, bool live, uint32_t qtile, u
   uint32_t w[16];
 #pragma unroll
   for (int i = 0; i < 16; i++) w[i] = 0u;
-  const uint32_t one = live ? 0x3C00u : 0u;
+  const uint32_t one = 0x3C00u;  // also on the zero rows past nq: their logits stay finite (0 or -inf)
   if (R <= 8) {
 #pragma unroll
     for (int i = 0; i < 4; i++) w[i] = f16pair(acc[2 * i], acc[2 * i + 1]);
@@ -264,7 +275,20 @@ __device__ __forceinline__ void load_half(const AttnChunk &c, int h, int64_t k0,
     d.m2 = mv | (mv << 16);
   }
   d.c = ((const uint4 *)((VAL ? c.v_codes : c.k_codes) + gi * (D / 4)))[g];
-  if (!VAL && coef && c.rank > 0) {
+  if (EXT && !VAL && coef && c.rank > 0 && c.per_head) {  // the head's own rank and layout
+    const qwm_psac_head hd = c.c_heads[h];
+    int64_t row;
+    if (psac_row(hd, c.c_mask, c.c_tile_rank, c.tiles, h, k0 + r, row)) {
+      const int8_t *src = c.c + hd.c_off + row * hd.rank;
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int k = 0; k < 16; k++)
+        if (k < hd.rank) w[k >> 2] |= ((uint32_t)(uint8_t)src[k]) << (8 * (k & 3));
+      d.ca = make_uint2(w[0], w[1]);
+      d.cb = make_uint2(w[2], w[3]);
+      d.csc = c.c_scale[hd.s_off + row];
+    }
+  } else if (!VAL && coef && c.rank > 0) {
     const int R = c.rank;
     const int8_t *src = c.c + gi * R;
     if (R == 8) {
@@ -304,6 +328,12 @@ __device__ __forceinline__ void issue_half_copies(const uint16_t *base, int64_t 
   }
 }
 
+// Two bf16 values (one 32-bit word) -> two fp16 values, rounded to nearest (exact for magnitudes in
+// [2^-17, 65504] and for 0).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  return f16pair(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
 // In-place decode of this thread's half row (one 128-byte row of a swizzled block).
 template <bool BYTE_LUT>
 __device__ __forceinline__ void decode_half(const HalfRow &d, uint32_t block, int r, uint32_t lut) {
@@ -335,10 +365,17 @@ __device__ __forceinline__ void decode_half(const HalfRow &d, uint32_t block, in
   }
 }
 
-// In-place bf16 -> fp16 of this thread's half row (a row of the chunk being generated).
-__device__ __forceinline__ void convert_half(const HalfRow &d, uint32_t block, int r) {
+// A pair of fp16 values one of which is infinite or NaN (exponent field all ones).
+__device__ __forceinline__ bool f16pair_nonfinite(uint32_t h) {
+  return (h & 0x7C00u) == 0x7C00u || (h & 0x7C000000u) == 0x7C000000u;
+}
+
+// In-place bf16 -> fp16 of this thread's half row (a row of the chunk being generated); an element
+// beyond the fp16 range records QWM_ERR_RANGE.
+__device__ __forceinline__ void convert_half(const HalfRow &d, uint32_t block, int r, int32_t *status) {
   if (d.idx < 0) return;  // zero-filled by the copies
   const uint32_t rowb = block + (uint32_t)r * 128u;
+  bool bad = false;
 #pragma unroll
   for (int v = 0; v < 8; v++) {
     const uint32_t addr = rowb + ((uint32_t)v << 4);  // the swizzle permutes whole 16-byte chunks
@@ -346,9 +383,13 @@ __device__ __forceinline__ void convert_half(const HalfRow &d, uint32_t block, i
     const uint32_t w[4] = {b.x, b.y, b.z, b.w};
     uint32_t o[4];
 #pragma unroll
-    for (int u = 0; u < 4; u++) o[u] = f16pair(__uint_as_float(w[u] << 16), __uint_as_float(w[u] & 0xFFFF0000u));
+    for (int u = 0; u < 4; u++) {
+      o[u] = bf16x2_to_f16x2(w[u]);
+      bad |= f16pair_nonfinite(o[u]);
+    }
     tc::sts128(addr, make_uint4(o[0], o[1], o[2], o[3]));
   }
+  if (bad) qwm_dev_error(status, QWM_ERR_RANGE);
 }
 
 // Producer loop of one thread of a pair CTA (rank `cr`).  Keys: thread pr = (group g = pr / 64,
@@ -435,7 +476,7 @@ __device__ __forceinline__ void producer_pair(const AttnParams &p, unsigned char
     const AttnChunk &ch = p.ch[t0];
     tc::cp_async_wait<0>();
     __syncwarp();  // the warp's copies of tile j, made visible to every lane
-    if (EXT && ch.raw) convert_half(cur, block0 + (uint32_t)s * kStage, rr);
+    if (EXT && ch.raw) convert_half(cur, block0 + (uint32_t)s * kStage, rr, p.status);
     else decode_half<!WIDE>(cur, block0 + (uint32_t)s * kStage, rr, lut);
     if (!VAL && coef) write_x_row<WIDE>(cur, ch.rank, xs0 + (uint32_t)s * XL<WIDE>::kXBytes, rr);
     tc::fence_proxy_async_smem();
@@ -469,7 +510,8 @@ __device__ __forceinline__ void producer_pair(const AttnParams &p, unsigned char
 }
 
 // WIDE: PSAC ranks above 8 (32-column second-MMA operands).  IDX16: uint16 centroid indices.
-// EXT: the call includes a bf16 chunk (the chunk being generated) or compact INT2 metadata.
+// EXT: the call includes a bf16 chunk (the chunk being generated), compact INT2 metadata or per-head
+// PSAC coefficient layouts.
 template <bool WIDE, bool IDX16, bool EXT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     attend_pair_kernel(const __grid_constant__ AttnParams p) {
@@ -497,8 +539,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (qi < p.nq) v = *(const uint4 *)(p.q + ((int64_t)h * p.nq + qi) * D + 8 * ci);
     const uint32_t bw[4] = {v.x, v.y, v.z, v.w};
     uint32_t hw[4];
+    bool bad = false;
 #pragma unroll
-    for (int u = 0; u < 4; u++) hw[u] = f16pair(__uint_as_float(bw[u] << 16), __uint_as_float(bw[u] & 0xFFFF0000u));
+    for (int u = 0; u < 4; u++) {
+      hw[u] = bf16x2_to_f16x2(bw[u]);
+      bad |= f16pair_nonfinite(hw[u]);
+    }
+    if (bad) qwm_dev_error(p.status, QWM_ERR_RANGE);  // a Query element beyond the fp16 range
     *(uint4 *)(sm + OFF_Q + (x * 2 + b) * kBlk + tc::sw128_offset(rr, 8 * (ci % 8))) =
         make_uint4(hw[0], hw[1], hw[2], hw[3]);
   }
@@ -532,6 +579,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     tc::mbar_init(&bars.o_done, 1);
     tc::mbar_init(&bars.drain, 1);
+    tc::mbar_init(&bars.never, 1);
     abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -701,6 +749,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t ph = (uint32_t)(j / kStages) & 1u;
         const AttnChunk &ch = p.ch[t];
         const int nx = (WIDE && ch.rank > 8) ? 2 : 1;
+        if (p.test_expire && j == (J > 1 ? 1 : 0)) {  // test hook: a wait that nothing ends
+          ok = tc::mbar_wait(&bars.never, 0, kTestWaitNs);
+          if (!ok) break;
+        }
         ok = tc::mbar_wait_cluster(&bars.k_full[s], ph, kWaitNs) && !*abort_v;
         if (ok && tile_in_chunk == 0) ok = tc::mbar_wait_cluster(&bars.qx_full[t & 1], (t >> 1) & 1, kWaitNs);
         if (!ok) break;
@@ -788,10 +840,12 @@ cudaError_t launch_attend(const qwm_config &cfg, const uint16_t *q, int64_t nq, 
   p.compact = cfg.storage == QWM_STORAGE_COMPACT;
   p.any_causal = 0;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.test_expire = (cfg.test_flags & QWM_TEST_EXPIRE_WAIT) != 0;
   p.status = status;
   int used = 0, tiles = 0;
   bool wide = false;  // a chunk with PSAC rank above 8: the 32-column second-MMA operands
   bool raw = false;   // a bf16 chunk (the chunk being generated)
+  bool per_head = false;  // a chunk with per-head PSAC ranks and layouts
   for (int i = 0; i < n_chunks; i++) {
     const qwm_chunk &c = chunks[i];
     if (c.n_tokens == 0) continue;  // empty chunks contribute nothing
@@ -809,6 +863,9 @@ cudaError_t launch_attend(const qwm_config &cfg, const uint16_t *q, int64_t nq, 
     a.k_raw = c.k_raw; a.v_raw = c.v_raw;
     a.k_s8 = c.k_s8; a.v_s8 = c.v_s8; a.k_zp = c.k_zp; a.v_zp = c.v_zp;
     a.k_sigma = c.k_sigma; a.v_sigma = c.v_sigma;
+    a.per_head = c.kind == QWM_CHUNK_PACKED && c.rank_eff > 0 && c.c_layout == QWM_C_PER_HEAD;
+    a.c_heads = c.c_heads; a.c_mask = c.c_mask; a.c_tile_rank = c.c_tile_rank;
+    per_head |= a.per_head != 0;
     tiles += a.tiles;
     wide |= a.rank > 8;
   }
@@ -817,7 +874,7 @@ cudaError_t launch_attend(const qwm_config &cfg, const uint16_t *q, int64_t nq, 
   const bool idx16 = cfg.n_centroids > 256;
   cudaError_t e;
   const dim3 grid((unsigned)(2 * ((nq + kPairQ - 1) / kPairQ)), cfg.heads);  // CTA pairs
-  const bool ext = raw || p.compact;
+  const bool ext = raw || p.compact || per_head;
   e = ext ? launch_pair_ext<true>(p, grid, wide, idx16, st) : launch_pair_ext<false>(p, grid, wide, idx16, st);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

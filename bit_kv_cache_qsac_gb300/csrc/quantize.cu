@@ -615,18 +615,31 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
           mxv[k][0] = mxv[k][1] = -INFINITY;
         }
         if (cnt > 0) {
+          // candidate rows come from L2: with up to 4 candidates the loads run two chunks ahead of
+          // their use (three sets in flight), so the latency is paid about once per token
+          constexpr int PF = KM <= 4 ? 2 : 0;
+          uint4 mq[PF + 1][KM];
 #pragma unroll
-          for (int gi = 0; gi < 2; gi++) {  // the two groups of 64 channels
+          for (int a = 0; a < PF; a++)
 #pragma unroll
-          for (int cc = 0; cc < 8; cc++) {
-            const int ci = 8 * gi + cc;
+            for (int k = 0; k < KM; k++)
+              mq[a][k] = k < cnt ? *(const uint4 *)(cent + (int64_t)cj[k] * D + 8 * a) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int ci = 0; ci < D / 8; ci++) {
+            const int gi = ci >> 3, cc = ci & 7;
+            if (ci + PF < D / 8) {
+#pragma unroll
+              for (int k = 0; k < KM; k++)
+                mq[(ci + PF) % (PF + 1)][k] =
+                    k < cnt ? *(const uint4 *)(cent + (int64_t)cj[k] * D + 8 * (ci + PF)) : make_uint4(0, 0, 0, 0);
+            }
             float f[8];
             bf16x8(tc::lds128(xts + gi * TILE * 128 + tc::sw128_offset(row, 8 * cc)), f);
 #pragma unroll
             for (int k = 0; k < KM; k++) {
               if (k < cnt) {
                 float mu[8];
-                bf16x8(*(const uint4 *)(cent + (int64_t)cj[k] * D + 8 * ci), mu);
+                bf16x8(mq[ci % (PF + 1)][k], mu);
 #pragma unroll
                 for (int u = 0; u < 8; u++) {
                   const float rr = __fsub_rn(f[u], mu[u]);
@@ -635,7 +648,6 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
                 }
               }
             }
-          }
           }
         }
         float bS = INFINITY;
@@ -871,8 +883,9 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
   }
 }
 
-// fp16 copies of both codebooks for the attention kernel (exact for bf16 values of normal fp16
-// magnitude; a centroid beyond the fp16 range records QWM_ERR_RANGE).
+// The chunk's stored codebooks: the fp16 value of every bf16 centroid element (exact for magnitudes
+// in [2^-17, 65504] and for 0; an element beyond the fp16 range records QWM_ERR_RANGE).  The
+// attention's tensor cores take them as fp16 operands and the decoder reads them.
 __global__ void codebook_f16_kernel(const uint16_t *__restrict__ ck, const uint16_t *__restrict__ cv, uint16_t *ok,
                                     uint16_t *ov, int64_t n8, int32_t *status) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < 2 * n8; i += (int64_t)gridDim.x * blockDim.x) {
@@ -959,6 +972,16 @@ __global__ void __launch_bounds__(256) quant_image_kernel(const uint16_t *__rest
   }
 }
 
+// The Query second moment M = S / n of every head (IEEE division in fp32); the identity while no Query
+// has been seen (n = 0: uniform weights, as at a cold start).
+__global__ void __launch_bounds__(256) mfull_kernel(const float *__restrict__ S, const int64_t *__restrict__ n_seen,
+                                                    float *__restrict__ M) {
+  const int h = blockIdx.y, e = blockIdx.x * 256 + threadIdx.x;
+  const int64_t nh = n_seen[h];
+  const int64_t i = (int64_t)h * D * D + e;
+  M[i] = nh > 0 ? __fdiv_rn(S[i], (float)nh) : (e / D == e % D ? 1.0f : 0.0f);
+}
+
 // Full-form ranking operand: b_j = M mu_j for every centroid j of every head (M symmetric, so thread c
 // reads column c of M, coalesced across the block); mu_j staged in shared memory.
 __global__ void __launch_bounds__(128) mfull_b_kernel(const float *__restrict__ M, const uint16_t *__restrict__ cent,
@@ -1002,8 +1025,11 @@ size_t quantize_image_bytes(int H, int C) {
 }
 
 cudaError_t launch_quantize(const qwm_config &cfg, const uint16_t *k, const uint16_t *v, int64_t n, const float *w,
-                            const float *Mq, float *Bq, const uint16_t *u_r, const qwm_chunk &out, const qwm_debug *dbg,
-                            int32_t *status, int num_sms, unsigned char *img, cudaStream_t st) {
+                            const float *S, const int64_t *n_seen, float *Mq_ws, float *Bq, const uint16_t *u_r,
+                            const qwm_chunk &out, const qwm_debug *dbg, int32_t *status, int num_sms,
+                            unsigned char *img, cudaStream_t st, cudaStream_t side, cudaEvent_t fork,
+                            cudaEvent_t join) {
+  const float *Mq = S ? Mq_ws : nullptr;
   const int H = cfg.heads, C = cfg.n_centroids;
   const bool wide = C > QWM_MAX_RESIDENT_CENTROIDS;
   float *img_max = wide ? (float *)(img + (size_t)H * (C / kSlice) * QSmem(C, true, true).an) : nullptr;
@@ -1018,13 +1044,24 @@ cudaError_t launch_quantize(const qwm_config &cfg, const uint16_t *k, const uint
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  if (Mq) {  // full-form ranking: the Key distance operand b_j = M mu_j
+  if (Mq) {  // full-form ranking: M = S / n, then the Key distance operand b_j = M mu_j
+    mfull_kernel<<<dim3(D * D / 256, H), 256, 0, st>>>(S, n_seen, Mq_ws);
     mfull_b_kernel<<<dim3(C, H), D, 0, st>>>(Mq, out.cent_k, C, Bq);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
+  // The Value pass runs on the context's second stream beside the Key pass (the two read and write
+  // disjoint data), and the caller's stream waits for it at the end.  With streamed 1024-centroid
+  // codebooks both passes share one operand image, so they run one after the other.
+  const bool concurrent = !wide;
+  if (concurrent) {
+    cudaError_t e = cudaEventRecord(fork, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side, fork, 0);
+    if (e != cudaSuccess) return e;
+  }
   for (int pass = 0; pass < 2; pass++) {
     const bool key = pass == 0;
+    cudaStream_t ps = (concurrent && !key) ? side : st;
     TensorMap128 tmap;
     if (!make_tmap_rows128_bf16(&tmap, key ? k : v, (uint64_t)H * n, TILE)) return cudaErrorInvalidValue;
     QParams p;
@@ -1057,8 +1094,13 @@ cudaError_t launch_quantize(const qwm_config &cfg, const uint16_t *k, const uint
       if (e != cudaSuccess) return e;
       e = launch_pass<true>(tmap, p, key, H, smem, st);
     } else {
-      e = launch_pass<false>(tmap, p, key, H, smem, st);
+      e = launch_pass<false>(tmap, p, key, H, smem, ps);
     }
+    if (e != cudaSuccess) return e;
+  }
+  if (concurrent) {
+    cudaError_t e = cudaEventRecord(join, side);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, join, 0);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

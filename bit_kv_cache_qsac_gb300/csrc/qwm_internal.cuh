@@ -30,6 +30,11 @@ struct qwm_ctx {
   unsigned char *km_img; // 1024-centroid codebooks: k-means operand slices + norms
   unsigned char *q_img;  // 1024-centroid codebooks: quantiser operand slices + maxima
   float *q_bfull;        // full-form ranking: b_j = M mu_j [H][C][d]
+  float *q_mfull;        // full-form ranking: M = S / n [H][d][d]
+  // a second stream (and fork / join events) on which the Value pass of qwm_quantize_kv runs beside
+  // the Key pass; the caller's stream waits for it before anything it issues next
+  cudaStream_t side;
+  cudaEvent_t fork, join;
 };
 
 // record the first device-side error (kernels call this; never traps)
@@ -67,6 +72,26 @@ static __device__ __forceinline__ uint32_t int2_code(float r, float m, float s, 
   return (uint32_t)qf;
 }
 
+// Where token `tok` (of a chunk with `tiles` 128-token tiles) of head h keeps its PSAC row in a
+// QWM_C_PER_HEAD chunk: false when it keeps none (a sparse head, scale zero); else `row` = its row
+// index in the head's region (the token itself for a dense head; for a sparse head the rows stored
+// before its tile plus the set bits of its tile's bitmap below it).
+__device__ __forceinline__ bool psac_row(const qwm_psac_head &hd, const uint32_t *c_mask, const int32_t *c_tile_rank,
+                                         int64_t tiles, int h, int64_t tok, int64_t &row) {
+  row = tok;
+  if (hd.rank == 0) return false;
+  if (!hd.sparse) return true;
+  const int64_t t = tok >> 7;
+  const int b = (int)(tok & 127), w = b >> 5, bit = b & 31;
+  const uint4 m4 = *(const uint4 *)(c_mask + ((int64_t)h * tiles + t) * 4);
+  const uint32_t word = w == 0 ? m4.x : (w == 1 ? m4.y : (w == 2 ? m4.z : m4.w));
+  if (!((word >> bit) & 1u)) return false;
+  const int below = __popc(word & ((1u << bit) - 1u)) + (w > 0 ? __popc(m4.x) : 0) + (w > 1 ? __popc(m4.y) : 0) +
+                    (w > 2 ? __popc(m4.z) : 0);
+  row = (int64_t)c_tile_rank[(int64_t)h * tiles + t] + below;
+  return true;
+}
+
 // TMA tensor map (a 128-byte-aligned 128-byte blob, CUtensorMap) over rows of 128 bf16.
 struct alignas(128) TensorMap128 {
   unsigned char bytes[128];
@@ -88,9 +113,19 @@ cudaError_t launch_kmeans(const uint16_t *x, int64_t n, int H, int C, const uint
                           int32_t *status, unsigned char *img, cudaStream_t st);
 size_t quantize_image_bytes(int H, int C);
 cudaError_t launch_quantize(const qwm_config &cfg, const uint16_t *k, const uint16_t *v, int64_t n,
-                            const float *w, const float *Mq, float *Bq, const uint16_t *u_r, const qwm_chunk &out,
-                            const qwm_debug *dbg, int32_t *status, int num_sms, unsigned char *img, cudaStream_t st);
+                            const float *w, const float *S, const int64_t *n_seen, float *Mq, float *Bq,
+                            const uint16_t *u_r, const qwm_chunk &out, const qwm_debug *dbg, int32_t *status,
+                            int num_sms, unsigned char *img, cudaStream_t st, cudaStream_t side, cudaEvent_t fork,
+                            cudaEvent_t join);
 cudaError_t launch_attend(const qwm_config &cfg, const uint16_t *q, int64_t nq, const qwm_chunk *chunks,
                           int n_chunks, float scale, float *out, int num_sms, int32_t *status, cudaStream_t st);
-cudaError_t launch_dequantize(const qwm_config &cfg, const qwm_chunk &ch, uint16_t *k_hat, uint16_t *v_hat,
-                              cudaStream_t st);
+cudaError_t launch_dequantize(const qwm_config &cfg, const qwm_chunk *chunks, int n_chunks, uint16_t *k_hat,
+                              uint16_t *v_hat, cudaStream_t st);
+cudaError_t launch_select_rank(const float *eigvals, float energy, int H, int R, uint16_t *u_r, int32_t *head_rank,
+                               cudaStream_t st);
+cudaError_t launch_psac_kept(const uint16_t *c_scale, int64_t n, int H, int32_t *kept, cudaStream_t st);
+cudaError_t launch_psac_pack(const int8_t *c_dense, const uint16_t *s_dense, int64_t n, int H, int R,
+                             const qwm_psac_head *plan, int8_t *c_out, uint16_t *s_out, uint32_t *c_mask,
+                             int32_t *c_tile_rank, cudaStream_t st);
+void psac_plan_host(int H, int64_t n, const int32_t *head_rank, const int32_t *kept, qwm_psac_head *plan,
+                    int64_t *c_bytes, int64_t *n_scales);

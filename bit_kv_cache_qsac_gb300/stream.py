@@ -14,19 +14,27 @@ import math
 
 import torch
 
-from . import (ActiveChunk, Chunk, Context, qwm_attend, qwm_dequantize, qwm_fit_centroids, qwm_quantize_kv,
-               qwm_quantize_kv_full,
-               qwm_sync_status, qwm_update_query_stats)
+from . import (ActiveChunk, Chunk, Context, pack_psac_layout, qwm_attend, qwm_dequantize, qwm_fit_centroids,
+               qwm_quantize_kv, qwm_quantize_kv_full, qwm_select_rank, qwm_sync_status, qwm_update_query_stats)
 
 
 class CompressedLayer:
     """Running state of one layer: Query statistics, basis, packed chunks, last codebooks."""
 
-    def __init__(self, ctx: Context, device=None, full_query: bool = False):
+    def __init__(self, ctx: Context, device=None, full_query: bool = False, rank_energy: float | None = None,
+                 psac_per_head: bool = False, keep_fit_codebooks: bool = False):
         """full_query: rank the QSAC candidates by the full Query second moment (English v2 §C.4
-        ablation) instead of its diagonal."""
+        ablation) instead of its diagonal.  rank_energy: choose each head's PSAC rank per chunk as the
+        smallest r <= config.rank whose top-r eigenvalues hold this share of tr M (qwm_select_rank);
+        implies the per-head coefficient layout.  psac_per_head: repack each chunk's coefficients into
+        the per-head layout (the smaller of dense and sparse per head).  keep_fit_codebooks: keep
+        every chunk's bf16 codebooks (only the packing reads them; by default only the last chunk's
+        stay, as the next chunk's k-means start)."""
         self.ctx = ctx
         self.full_query = full_query
+        self.rank_energy = rank_energy
+        self.psac_per_head = psac_per_head or rank_energy is not None
+        self.keep_fit_codebooks = keep_fit_codebooks
         cfg = ctx.cfg
         H, d, r = cfg.heads, cfg.head_dim, cfg.rank
         dev = device or torch.device("cuda", torch.cuda.current_device())
@@ -64,17 +72,24 @@ class CompressedLayer:
         if stats_done is not None:
             s.wait_event(stats_done)
         psac = self.n_seen > 0 and self.ctx.cfg.rank > 0
+        head_rank = None
         if psac:
             with torch.cuda.stream(s):
                 ch.u_r.copy_(self.u_r)   # per-chunk snapshot of the basis
+            if self.rank_energy is not None:   # per-head rank: basis columns past it zeroed
+                head_rank = torch.empty(self.ctx.cfg.heads, dtype=torch.int32, device=self.device)
+                qwm_select_rank(self.ctx, self.eigvals, self.rank_energy, ch.u_r, head_rank, stream)
         w = self.w if self.n_seen > 0 else None
         if self.full_query and w is not None:
-            M = (self.S / self.n.view(-1, 1, 1).to(self.S.dtype)).contiguous()
-            qwm_quantize_kv_full(self.ctx, k, v, n, M, ch.u_r if psac else None, ch, debug, stream)
+            qwm_quantize_kv_full(self.ctx, k, v, n, self.S, self.n, ch.u_r if psac else None, ch, debug, stream)
         else:
             qwm_quantize_kv(self.ctx, k, v, n, w, ch.u_r if psac else None, ch, debug, stream)
+        if psac and self.psac_per_head:
+            pack_psac_layout(self.ctx, ch, head_rank, stream)
         self.chunks.append(ch)
         self.prev_cent_k, self.prev_cent_v = ch.cent_k, ch.cent_v
+        if not self.keep_fit_codebooks:
+            ch.release_fit_codebooks()   # the stored fp16 codebooks remain; prev_cent_* keeps this one
         return ch
 
     def attend(self, q: torch.Tensor, out: torch.Tensor | None = None, scale: float | None = None,

@@ -80,7 +80,17 @@ typedef struct {
   int32_t storage;      /* qwm_storage: how a chunk's INT2 metadata is stored */
   int32_t psac_gate;    /* 1: keep a token's C only where it lowers sum_c w_c e_c^2 (Chinese summary
                            step (4): "仅当降低Query加权误差时保留"); 0: always keep */
+  int32_t test_flags;   /* 0 in production; QWM_TEST_EXPIRE_WAIT for tests of the error path */
 } qwm_config;
+
+/* Test hooks (qwm_config.test_flags).
+ *  QWM_TEST_EXPIRE_WAIT: in qwm_attend, the thread that issues the tensor-core work waits, before
+ *    its second key tile, on a barrier that nothing completes, with a 1 ms limit.  The wait runs
+ *    out, the kernel takes the path every expired wait takes (it records QWM_ERR_DEVICE_TIMEOUT,
+ *    every role stops within its own bounded waits, issued tensor-core work is drained and tensor
+ *    memory freed) and the call's output is undefined; the context stays usable.  This exercises
+ *    the recovery path without a GPU fault. */
+enum { QWM_TEST_EXPIRE_WAIT = 1 };
 
 /* INT2 metadata layouts.
  *  QWM_STORAGE_FP16: per (token, group of 64) an fp16 offset m (round-down of the minimum) and an
@@ -103,6 +113,24 @@ typedef enum {
   QWM_CHUNK_BF16 = 1    /* k_raw / v_raw only (qwm_attend) */
 } qwm_chunk_kind;
 
+/* Layout of a packed chunk's PSAC coefficients (c and c_scale).
+ *  QWM_C_DENSE: c int8 [H][N][r] and c_scale fp16 [H][N], r = rank_eff, as qwm_quantize_kv writes them.
+ *  QWM_C_PER_HEAD: what qwm_psac_pack writes: each head h has its own rank r_h <= rank_eff (columns
+ *    past r_h of its basis are zero, so its coefficients there are zero and not stored) and its own
+ *    layout, dense (a row of r_h bytes and a scale per token) or sparse (rows only for the tokens
+ *    whose scale is not zero, found through a 128-token-tile bitmap and per-tile counts), the smaller
+ *    of the two (English v2 summary §D.1: the smaller dense or sparse coefficient layout, with
+ *    sparse-index storage; Chinese summary step (4): C kept only where it lowers the Query-weighted
+ *    error).  c_heads[h] locates head h's rows in c and scales in c_scale. */
+typedef enum { QWM_C_DENSE = 0, QWM_C_PER_HEAD = 1 } qwm_c_layout;
+
+typedef struct {
+  int64_t c_off;   /* byte offset of the head's first row in chunk.c */
+  int64_t s_off;   /* element offset of the head's first scale in chunk.c_scale */
+  int32_t rank;    /* r_h: bytes per row (0: the head stores nothing and has no PSAC term) */
+  int32_t sparse;  /* 0: a row per token; 1: rows of the kept tokens only (c_mask, c_tile_rank) */
+} qwm_psac_head;
+
 /* One compressed chunk of the cache, all heads.  Every pointer is caller-owned
  * device memory; N = n_tokens, H = heads, d = head_dim, G = d / group, r = rank. */
 typedef struct {
@@ -117,16 +145,18 @@ typedef struct {
   uint16_t *k_min;       /* fp16 [H][N][G]: INT2 offset m (r_hat = m + s q) */
   uint16_t *v_scale;     /* fp16 [H][N][G] */
   uint16_t *v_min;       /* fp16 [H][N][G] */
-  uint16_t *cent_k;      /* bf16 [H][C][d] Key codebook of this chunk */
-  uint16_t *cent_v;      /* bf16 [H][C][d] Value codebook of this chunk */
+  uint16_t *cent_k;      /* bf16 [H][C][d] Key codebook the chunk is packed with (qwm_fit_centroids'
+                            output); read by qwm_quantize_kv only: the caller may release it after */
+  uint16_t *cent_v;      /* bf16 [H][C][d] Value codebook, likewise */
   int8_t *c;             /* [H][N][r] PSAC coefficients (unused when rank_eff == 0) */
   uint16_t *c_scale;     /* fp16 [H][N]: C_hat = c_scale * c */
   uint16_t *u_r;         /* bf16 [H][d][r]: the basis C was built with (snapshot per chunk) */
-  uint16_t *cent_k16;    /* fp16 [H][C][d]: the Key codebook converted to fp16 by qwm_quantize_kv;
-                            qwm_attend reads it as a tensor-core operand.  fp16 holds every bf16
-                            value of magnitude in [2^-14, 65504] exactly; a centroid beyond 65504
-                            records QWM_ERR_RANGE. */
-  uint16_t *cent_v16;    /* fp16 [H][C][d]: the Value codebook, likewise */
+  uint16_t *cent_k16;    /* fp16 [H][C][d]: the chunk's stored Key codebook, written by qwm_quantize_kv
+                            as the fp16 value of every bf16 centroid element (the same value for
+                            magnitudes in [2^-17, 65504] and for 0; an element beyond 65504 records
+                            QWM_ERR_RANGE); qwm_attend (as tensor-core operands) and qwm_dequantize
+                            read it */
+  uint16_t *cent_v16;    /* fp16 [H][C][d]: the stored Value codebook, likewise */
   /* QWM_CHUNK_BF16 only (every packed field above is then unused): */
   const uint16_t *k_raw; /* bf16 [H][N][d] Keys of the chunk being generated */
   const uint16_t *v_raw; /* bf16 [H][N][d] */
@@ -140,6 +170,13 @@ typedef struct {
   uint8_t *v_zp;         /* [H][N] */
   uint16_t *k_sigma;     /* fp16 [H][ceil(N/128)][G] second-level scales */
   uint16_t *v_sigma;     /* fp16 [H][ceil(N/128)][G] */
+  /* PSAC coefficient layout (packed chunks with rank_eff > 0): */
+  int32_t c_layout;      /* qwm_c_layout */
+  const qwm_psac_head *c_heads; /* QWM_C_PER_HEAD: device [H] */
+  const uint32_t *c_mask;       /* QWM_C_PER_HEAD: device [H][ceil(N/128)][4]: bit b of word w of tile t
+                                   set when token 128 t + 32 w + b has a row (sparse heads) */
+  const int32_t *c_tile_rank;   /* QWM_C_PER_HEAD: device [H][ceil(N/128)]: rows of the head stored
+                                   for the tokens before tile t (sparse heads) */
 } qwm_chunk;
 
 /* Optional stage outputs of qwm_quantize_kv for parity checks (NULL members are skipped). */
@@ -194,24 +231,67 @@ QWM_API qwm_status qwm_fit_centroids(qwm_ctx *ctx, const uint16_t *x, int64_t n,
  *   w     fp32 [H][d]      channel weights, or NULL for uniform weights (cold start)
  *   u_r   bf16 [H][d][r]   PSAC basis, or NULL to switch PSAC off (cold start)
  *   out   chunk to fill: out->n_tokens must equal n, out->cent_k / out->cent_v must hold the
- *         chunk's codebooks; the codes, indices, scales, the fp16 codebook copies
- *         out->cent_k16 / out->cent_v16 and (when u_r) c, c_scale are written,
+ *         chunk's codebooks; the codes, indices, scales, the stored fp16 codebooks
+ *         out->cent_k16 / out->cent_v16 and (when u_r) c, c_scale (QWM_C_DENSE) are written,
  *         out->rank_eff is set on the host (r or 0) and, when u_r is given, out->u_r must
  *         point at a caller-owned copy of the basis (the library does not copy it).
  *   dbg   optional stage outputs, or NULL.
  * INT2 per (token, group): m = fp16 round-down of min r, s = fp16 round-up of
  * (max r - m)/3 (s = 0 when max r == m), q = clamp(rint((r - m)/s), 0, 3); so |r - r_hat| <= s/2.
- * INT8 per token: sC = fp16 round-up of max|C|/127, c = clamp(rint(C/sC), -127, 127). */
+ * INT8 per token: sC = fp16 round-up of max|C|/127, c = clamp(rint(C/sC), -127, 127).
+ * The Value pass runs on a second stream of the context beside the Key pass (forked from and joined
+ * back into `stream` with events), so work issued on `stream` afterwards sees both. */
 QWM_API qwm_status qwm_quantize_kv(qwm_ctx *ctx, const uint16_t *k, const uint16_t *v, int64_t n, const float *w,
                            const uint16_t *u_r, qwm_chunk *out, const qwm_debug *dbg, qwm_stream stream);
 
 /* qwm_quantize_kv with the QSAC candidates ranked by the full quadratic form (k - mu)^T M (k - mu)
  * instead of its diagonal (English v2 summary §C.4: the ablation of QSAC's diagonal approximation;
  * the pages report no consistent gain).  The rest is unchanged, with w = diag(M) for the range score.
- *   M   fp32 [H][d][d] symmetric Query second moment (S / n of qwm_update_query_stats). */
+ *   S       fp32 [H][d][d] running sum of q q^T and
+ *   n_seen  int64 [H]      running Query count, both as qwm_update_query_stats leaves them: the
+ *                          library forms M = S / n (fp32, IEEE division) in its workspace, or the
+ *                          identity for a head with n == 0 (uniform weights, as at a cold start). */
 QWM_API qwm_status qwm_quantize_kv_full(qwm_ctx *ctx, const uint16_t *k, const uint16_t *v, int64_t n,
-                                        const float *M, const uint16_t *u_r, qwm_chunk *out, const qwm_debug *dbg,
-                                        qwm_stream stream);
+                                        const float *S, const int64_t *n_seen, const uint16_t *u_r, qwm_chunk *out,
+                                        const qwm_debug *dbg, qwm_stream stream);
+
+/* PSAC rank per (chunk, head) (Chinese summary "独立分析的弱点", weakness three: the Query energy's
+ * concentration differs by model and layer, so one global r is a compromise; English v2 summary §C.2:
+ * a larger r still helps).  For each head, the smallest r_h in 0..config.rank whose r_h largest
+ * eigenvalues hold at least `energy` of their sum (tr M; the sum taken in descending order in double
+ * precision; r_h = config.rank when no smaller one does, 0 when the sum is not positive), then
+ * columns r_h.. of that head's basis set to zero, so that qwm_quantize_kv with this basis writes zero
+ * coefficients past r_h (and its INT8 scale and gate see only the first r_h).
+ *   eigvals    fp32 [H][d] descending (qwm_update_query_stats' output)
+ *   energy     share of tr M to reach, in [0, 1]
+ *   u_r        bf16 [H][d][config.rank] inout: the chunk's basis snapshot
+ *   head_rank  int32 [H] out: r_h */
+QWM_API qwm_status qwm_select_rank(qwm_ctx *ctx, const float *eigvals, float energy, uint16_t *u_r,
+                                   int32_t *head_rank, qwm_stream stream);
+
+/* Tokens per head whose PSAC scale is not zero (the tokens that keep a coefficient row in the sparse
+ * layout) of a QWM_C_DENSE packed chunk.  kept: device int32 [H] out. */
+QWM_API qwm_status qwm_psac_kept(qwm_ctx *ctx, const qwm_chunk *chunk, int32_t *kept, qwm_stream stream);
+
+/* Host-only: the per-head layout of a QWM_C_PER_HEAD chunk of n tokens from each head's rank and kept
+ * count: the dense layout takes n (r_h + 2) bytes, the sparse one kept (r_h + 2) + 20 ceil(n/128) bytes
+ * (16-byte bitmap and 4-byte count per tile); each head takes the smaller (dense on a tie; a head with
+ * r_h = 0 stores nothing).  Heads are laid out one after the other in c and c_scale.
+ *   head_rank, kept  HOST int32 [H]
+ *   plan             HOST [H] out (copy it to device memory for qwm_psac_pack and the chunk)
+ *   c_bytes          out: bytes of c; n_scales: out: fp16 elements of c_scale (either may be NULL) */
+QWM_API qwm_status qwm_psac_plan(const qwm_config *cfg, int64_t n, const int32_t *head_rank, const int32_t *kept,
+                                 qwm_psac_head *plan, int64_t *c_bytes, int64_t *n_scales);
+
+/* Repack a QWM_C_DENSE chunk's coefficients into the QWM_C_PER_HEAD layout of `plan`.
+ *   dense        the packed chunk (c_layout QWM_C_DENSE, rank_eff > 0)
+ *   plan         device [H], as qwm_psac_plan computed it for this chunk
+ *   c            int8 [c_bytes] out; c_scale fp16 [n_scales] out
+ *   c_mask       uint32 [H][ceil(N/128)][4] out; c_tile_rank int32 [H][ceil(N/128)] out
+ * The caller then describes the chunk with c_layout = QWM_C_PER_HEAD and these buffers (the dense
+ * c and c_scale may be released). */
+QWM_API qwm_status qwm_psac_pack(qwm_ctx *ctx, const qwm_chunk *dense, const qwm_psac_head *plan, int8_t *c,
+                                 uint16_t *c_scale, uint32_t *c_mask, int32_t *c_tile_rank, qwm_stream stream);
 
 /* Step 5 -- attention over the compressed cache (Chinese summary "注意力logits与时空token
  * 选择": L = Q K^T / sqrt(d); "核心方法": PSAC logits Q K_hat_0^T + Q U_r C^T).
@@ -238,6 +318,13 @@ QWM_API qwm_status qwm_attend(qwm_ctx *ctx, const uint16_t *q, int64_t nq, const
 QWM_API qwm_status qwm_dequantize(qwm_ctx *ctx, const qwm_chunk *chunk, uint16_t *k_hat, uint16_t *v_hat,
                           qwm_stream stream);
 
+/* qwm_dequantize of several packed chunks in one launch, written one after the other along the
+ * token axis: the decoded cache [H][sum N][d] in the order of `chunks` (the layout a bf16 attention
+ * over the whole cache takes).  chunks: HOST array of 1 <= n_chunks <= 128 packed descriptors
+ * (n_tokens == 0 ones skipped); k_hat, v_hat bf16 [H][sum of n_tokens][d] out (either may be NULL). */
+QWM_API qwm_status qwm_dequantize_chunks(qwm_ctx *ctx, const qwm_chunk *chunks, int32_t n_chunks, uint16_t *k_hat,
+                                         uint16_t *v_hat, qwm_stream stream);
+
 /* Wait for `stream`, return (and clear) the first error recorded on the device since
  * the last call, else QWM_OK. */
 QWM_API qwm_status qwm_sync_status(qwm_ctx *ctx, qwm_stream stream);
@@ -257,10 +344,14 @@ QWM_API qwm_status qwm_sync_status(qwm_ctx *ctx, qwm_stream stream);
  *                rejected with QWM_ERR_SHAPE
  *   dev_status   device int32 where a device-side error (QWM_ERR_NOT_CONVERGED, ...) is recorded
  *                if the word is still 0, or NULL
- * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
- * that device current; make that first call before any stream capture.  All calls share the one
- * array and each call leaves its contents behind: calls that can run on the GPU at the same time
- * (on different streams) race on it and must be ordered by the caller. */
+ * The first call in each CUDA context (a device's primary context, or a context the caller made
+ * current itself) looks up the array's device address in that context (cudaGetSymbolAddress);
+ * make that first call before any stream capture.  With lazy module loading (the CUDA default)
+ * the array is reserved on the device when the library's module loads, which is that first
+ * call: a caller whose memory budget is fixed at start-up should make one call at start-up (with
+ * nq == 0 and its own S, n, w, eigvals, u_r buffers, which that call recomputes from S and n).
+ * All calls share the one array and each call leaves its contents behind: calls that can run on
+ * the GPU at the same time (on different streams) race on it and must be ordered by the caller. */
 QWM_API qwm_status qwm_update_query_stats_noalloc(const qwm_config *cfg, const uint16_t *q, int64_t nq, float *S,
                                                   int64_t *n, float *w, float *eigvals, uint16_t *u_r,
                                                   int32_t *dev_status, qwm_stream stream);

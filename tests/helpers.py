@@ -42,12 +42,44 @@ def chunk_head(chunk, h: int) -> dict:
         idx_k=chunk.k_idx[h].cpu().numpy().astype(np.int32), idx_v=chunk.v_idx[h].cpu().numpy().astype(np.int32),
         k_codes=chunk.k_codes[h].cpu().numpy(), v_codes=chunk.v_codes[h].cpu().numpy(),
         k_scale=ks, k_min=km, v_scale=vs, v_min=vm,
-        cent_k=to_u16(chunk.cent_k[h]), cent_v=to_u16(chunk.cent_v[h]), rank=r,
+        cent_k16=to_u16(chunk.cent_k16[h]), cent_v16=to_u16(chunk.cent_v16[h]), rank=r,
     )
     if r:
-        d.update(c=chunk.c[h].cpu().numpy()[:, :r], c_scale=to_u16(chunk.c_scale[h]),
-                 u_r=to_u16(chunk.u_r[h])[:, :r])
+        c, sc = psac_dense_head(chunk, h)
+        d.update(c=c, c_scale=sc, u_r=to_u16(chunk.u_r[h])[:, :r])
     return d
+
+
+def psac_dense_head(chunk, h: int):
+    """One head's PSAC coefficients (int8 [n][rank_eff], fp16 bits [n]) of a chunk in either layout:
+    the dense arrays, or the per-head layout read back through the oracle's sparse decoder (a head's
+    rank r_h <= rank_eff: its columns past r_h are zero)."""
+    import oracle
+    r, n = chunk.rank_eff, chunk.n_tokens
+    if getattr(chunk, "c_layout", 0) == 0:
+        return chunk.c[h].cpu().numpy()[:, :r], to_u16(chunk.c_scale[h])
+    c_off, s_off, rh, sparse = chunk.plan[h]
+    c = np.zeros((n, r), np.int8)
+    sc = np.zeros(n, np.uint16)
+    if rh == 0:
+        return c, sc
+    allc = chunk.c.cpu().numpy()
+    alls = to_u16(chunk.c_scale)
+    if not sparse:
+        c[:, :rh] = allc[c_off:c_off + n * rh].reshape(n, rh)
+        sc[:] = alls[s_off:s_off + n]
+        return c, sc
+    mask = chunk.c_mask[h].cpu().numpy().view(np.uint32)
+    trank = chunk.c_tile_rank[h].cpu().numpy()
+    kept = int(bin_count(mask))
+    rows = allc[c_off:c_off + kept * rh].reshape(kept, rh)
+    c2, sc2 = oracle.psac_sparse_decode(mask, trank, rows, alls[s_off:s_off + kept], n, rh)
+    c[:, :rh] = c2
+    return c, sc2
+
+
+def bin_count(mask) -> int:
+    return sum(bin(int(x)).count("1") for x in np.asarray(mask).ravel())
 
 
 def bf16_ulp_close(a_bits: np.ndarray, b: np.ndarray, ulps: float = 1.0) -> np.ndarray:
@@ -72,7 +104,8 @@ def decode_term_magnitude(ch: dict, key: bool, group: int = 64) -> np.ndarray:
         q[:, c] = (codes[:, c // 4] >> (2 * (c % 4))) & 3
     g = np.arange(d) // group
     s, m = f16(ch[pre + "_scale"])[:, g], f16(ch[pre + "_min"])[:, g]
-    t = np.abs(bf(ch["cent_" + pre][idx])) + np.abs(m) + np.abs(s * q)
+    mu = f16(ch["cent_" + pre + "16"]) if ("cent_" + pre + "16") in ch else bf(ch["cent_" + pre])
+    t = np.abs(mu[idx]) + np.abs(m) + np.abs(s * q)
     if key and ch["rank"]:
         chat = f16(ch["c_scale"])[:, None] * ch["c"].astype(np.float64)
         t += np.abs(chat) @ np.abs(bf(ch["u_r"])).T

@@ -75,3 +75,38 @@ def test_product_path_has_no_oracle_or_cpu_fallback():
                 txt = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in txt and "from oracle" not in txt, f
                 assert "liboracle" not in txt, f
+
+
+def test_new_calls_reject_null_arguments(qwm):
+    lib = qwm.raw_library()
+    assert lib.qwm_dequantize_chunks(None, None, 0, None, None, None) == qwm.QWM_ERR_ARG
+    assert lib.qwm_select_rank(None, None, 0.5, None, None, None) == qwm.QWM_ERR_ARG
+    assert lib.qwm_psac_kept(None, None, None, None) == qwm.QWM_ERR_ARG
+    assert lib.qwm_psac_pack(None, None, None, None, None, None, None, None) == qwm.QWM_ERR_ARG
+    bad = qwm.qwm_config(4, 128, 256, 64, 4, 8, 2, 10, 0, 0, 0, 2)     # an unknown test flag
+    assert qwm.qwm_workspace_bytes(bad) == 0
+
+
+def test_psac_plan_matches_the_oracle_rule(qwm):
+    """The per-head layout plan (host only): each head the smaller of dense and sparse, laid out one
+    after the other, as the oracle's byte-count rule chooses."""
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(5)
+    for n in (1, 127, 128, 4680, 10800):
+        H = 40
+        cfg = qwm.qwm_config(H, 128, 256, 64, 4, 16, 2, 10, 0)
+        ranks = rng.integers(0, 17, H)
+        kept = rng.integers(0, n + 1, H)
+        plan, c_bytes, n_scales, _ = qwm.qwm_psac_plan(cfg, n, ranks, kept)
+        want = oracle.psac_plan(n, ranks, kept)
+        off_c = off_s = 0
+        for h in range(H):
+            c_off, s_off, r, sparse = plan[h]
+            assert (bool(sparse), r) == (want[h][0], int(ranks[h]))
+            assert (c_off, s_off) == (off_c, off_s)
+            off_c += want[h][1] * int(ranks[h])
+            off_s += want[h][1]
+        assert (c_bytes, n_scales) == (off_c, off_s)
+    with pytest.raises(qwm.QwmError):
+        qwm.qwm_psac_plan(qwm.qwm_config(2, 128, 256, 64, 4, 8, 2, 10, 0), 100, [9, 1], [5, 5])   # rank > config

@@ -104,7 +104,10 @@ def test_prq_two_stage(q):
         for name in ("k_scale", "k_min", "v_scale", "v_min"):
             assert np.array_equal(to_u16(getattr(ch2, name)[h]), o2[name]), name
         # fused decode: mu1 + (mu2 + r_hat) against the oracle's double sum
+        # (the two-stage decoder reads the stage codebooks in bf16, as QVG stores them)
         c2 = chunk_head(ch2, h)
+        del c2["cent_k16"], c2["cent_v16"]
+        c2["cent_k"], c2["cent_v"] = to_u16(ch2.cent_k[h]), to_u16(ch2.cent_v[h])
         _, _, k2, v2 = oracle.dequantize_head(c2)
         for got, ref2, cent1, i1, key in ((kh[h], k2, c1k, i1k, "k"), (vh[h], v2, c1v, i1v, "v")):
             ref = ref2 + _f64(cent1[i1])

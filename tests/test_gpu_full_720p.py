@@ -27,7 +27,7 @@ def run():
     import bit_kv_cache_qsac_gb300 as q
     from bit_kv_cache_qsac_gb300.stream import CompressedLayer
     ctx = q.Context(heads=W.heads)
-    layer = CompressedLayer(ctx)
+    layer = CompressedLayer(ctx, keep_fit_codebooks=True)
     ks, vs, qs = [], [], []
     for t in range(W.n_chunks):
         a, b = synth.chunk_range(W, t)

@@ -204,7 +204,7 @@ def _upstream(q, w_, H, n, C=256, top_m=4, rank=8, psac=True, storage=0, gate=0)
     return ctx, k, v, K, V, ch, (w if psac else None), (ch.u_r if psac and rank else None)
 
 
-def _check_quantize(q, ctx, k, v, K, V, ch, w, ur, top_m, rank, M=None):
+def _check_quantize(q, ctx, k, v, K, V, ch, w, ur, top_m, rank, M=None, Sn=None):
     H, n = k.shape[:2]
     dbg = dict(c_f32=torch.zeros(H, n, max(rank, 1), device="cuda"),
                cand=torch.zeros(H, n, top_m, dtype=torch.int32, device="cuda"),
@@ -212,7 +212,7 @@ def _check_quantize(q, ctx, k, v, K, V, ch, w, ur, top_m, rank, M=None):
     if M is None:
         q.qwm_quantize_kv(ctx, K, V, n, w, ur, ch, dbg)
     else:
-        q.qwm_quantize_kv_full(ctx, K, V, n, M, ur, ch, dbg)
+        q.qwm_quantize_kv_full(ctx, K, V, n, Sn[0], Sn[1], ur, ch, dbg)
     assert q.qwm_sync_status(ctx) == 0
     assert ch.rank_eff == (rank if ur is not None else 0)
     stats = dict(k_ties=0, v_ties=0, k_edge=0, tokens=H * n)
@@ -290,13 +290,14 @@ def test_quantize_full_form_ranking(q, C, n, top_m):
     w = torch.empty(H, D, device="cuda"); lam = torch.empty(H, D, device="cuda")
     ur = torch.zeros(H, D, 8, dtype=torch.bfloat16, device="cuda")
     q.qwm_update_query_stats(ctx, _bf(synth.queries(w_, -1, 256)[:H]), 256, S, cnt, w, lam, ur)
-    M = (S / cnt.view(H, 1, 1).float()).contiguous()
+    # the library forms M = S / n in fp32 (IEEE division); the oracle ranks with the same values
+    M = torch.from_numpy(S.cpu().numpy() / cnt.cpu().numpy().astype(np.float32)[:, None, None])
     ch = q.Chunk.empty(ctx, n)
     K, V = _bf(k), _bf(v)
     q.qwm_fit_centroids(ctx, K, n, None, ch.cent_k)
     q.qwm_fit_centroids(ctx, V, n, None, ch.cent_v)
     ch.u_r.copy_(ur)
-    st = _check_quantize(q, ctx, k, v, K, V, ch, None, ch.u_r, top_m, 8, M=M)
+    st = _check_quantize(q, ctx, k, v, K, V, ch, None, ch.u_r, top_m, 8, M=M, Sn=(S, cnt))
     print("tie fractions", {key: val / st["tokens"] for key, val in st.items() if key != "tokens"})
 
 
@@ -428,6 +429,40 @@ def test_dequantize_within_one_bf16_step(q, psac, C, n):
             assert (bf16_ulp_close(to_u16(got), ref) | (np.abs(g - ref) <= slack)).all()
 
 
+def test_dequantize_chunks_one_launch(q):
+    """Several chunks (cold start without PSAC, then PSAC chunks with their own bases, ragged sizes)
+    decoded in one launch into [H][sum N][d]: identical to decoding each chunk alone, and each
+    chunk's rows within one bf16 step of the oracle's decoder (plus the cancellation slack)."""
+    w_ = synth.TINY
+    H = 2
+    ctx = q.Context(heads=H)
+    from bit_kv_cache_qsac_gb300 import stream
+    layer = stream.CompressedLayer(ctx)
+    kk, vv = synth.keys(w_), synth.values(w_)
+    parts = [(0, 300), (300, 700), (700, 1024)]
+    for i, (a, b) in enumerate(parts):
+        if i > 0:
+            layer.fold_queries(_bf(synth.queries(w_, 30 + i, 128)))
+        layer.append_chunk(_bf(np.ascontiguousarray(kk[:, a:b])), _bf(np.ascontiguousarray(vv[:, a:b])))
+    total = sum(c.n_tokens for c in layer.chunks)
+    kh = torch.empty(H, total, D, dtype=torch.bfloat16, device="cuda"); vh = torch.empty_like(kh)
+    q.qwm_dequantize_chunks(ctx, layer.chunks, kh, vh)
+    assert q.qwm_sync_status(ctx) == 0
+    row = 0
+    for i, ch in enumerate(layer.chunks):
+        k1, v1 = layer.dequantize(i)
+        n = ch.n_tokens
+        assert torch.equal(kh[:, row:row + n], k1) and torch.equal(vh[:, row:row + n], v1)
+        for h in range(H):
+            c = chunk_head(ch, h)
+            _, _, k64, v64 = oracle.dequantize_head(c)
+            for got, ref, key in ((kh[h, row:row + n], k64, True), (vh[h, row:row + n], v64, False)):
+                g = (to_u16(got).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+                slack = 2.0 ** -20 * decode_term_magnitude(c, key)
+                assert (bf16_ulp_close(to_u16(got), ref) | (np.abs(g - ref) <= slack)).all()
+        row += n
+
+
 def _attn_err(got, ref):
     return np.abs(got - ref).max() / math.sqrt(np.mean(ref ** 2))
 
@@ -482,7 +517,6 @@ def test_attend_growing_logits(q):
         getattr(ch, name).zero_()
     ch.k_idx.copy_(torch.from_numpy(idx.copy())); ch.v_idx.copy_(torch.from_numpy(idx.copy()))
     ch.cent_k.copy_(torch.from_numpy(ck).to(torch.bfloat16)); ch.cent_v.copy_(torch.from_numpy(cv).to(torch.bfloat16))
-    ch.cent_k16.copy_(torch.from_numpy(ck).to(torch.float16)); ch.cent_v16.copy_(torch.from_numpy(cv).to(torch.float16))
     qf = 0.25 * u[None, None, :] + 0.125 * rng.integers(-2, 3, size=(H, nq, D))
     qa = to_u16(torch.from_numpy(qf).to(torch.bfloat16))
     out = torch.empty(H, nq, D, dtype=torch.float32, device="cuda")
@@ -525,6 +559,63 @@ def test_attend_packed_history_and_causal_active_chunk(q, tpf):
     for h in range(H):
         ref = oracle.attend_rows(qa[h], np.arange(na),
                                  [chunk_head(ch, h), dict(k_raw=k[h], v_raw=v[h], causal_tpf=tpf)], 1 / math.sqrt(D))
+        assert _attn_err(out[h].cpu().numpy().astype(np.float64), ref) <= 2e-2
+
+
+@pytest.mark.parametrize("scale", [1e-6, 1e-3])
+def test_attend_softmax_scale_and_padded_rows(q, scale):
+    """A ragged chunk (513 tokens: 4 full tiles and one of a single row) at softmax scales far below
+    1/sqrt(d): the 127 rows that pad the last tile get weight exactly 0 whatever the scale (at 1e-6
+    the softmax is almost flat, so weight left on the zero pad rows would shrink O by ~20%)."""
+    ctx, ch = _packed(q, n=513)
+    H, nq = 2, 130
+    qa = synth.queries(synth.TINY, 2, nq)
+    out = torch.empty(H, nq, D, dtype=torch.float32, device="cuda")
+    q.qwm_attend(ctx, _bf(qa), nq, [ch], scale, out)
+    assert q.qwm_sync_status(ctx) == 0
+    for h in range(H):
+        ref = oracle.attend_rows(qa[h], np.arange(nq), [chunk_head(ch, h)], scale)
+        assert _attn_err(out[h].cpu().numpy().astype(np.float64), ref) <= 2e-2
+
+
+def test_attend_fp16_range_errors(q):
+    """A Query element or an element of the chunk being generated beyond the fp16 range (the
+    tensor cores' operand type) records QWM_ERR_RANGE; elements inside it do not."""
+    ctx, ch = _packed(q)
+    H, nq = 2, 64
+    qa = synth.queries(synth.TINY, 3, nq)
+    out = torch.empty(H, nq, D, dtype=torch.float32, device="cuda")
+    big = synth.f32_to_bf16_bits(np.array([1.0e5], np.float32))[0]
+    edge = synth.f32_to_bf16_bits(np.array([65280.0], np.float32))[0]   # the largest bf16 below 65504
+    qb = qa.copy(); qb[1, 7, 33] = big
+    q.qwm_attend(ctx, _bf(qb), nq, [ch], 1 / math.sqrt(D), out)
+    assert q.qwm_sync_status(ctx) == q.QWM_ERR_RANGE
+    qb = qa.copy(); qb[1, 7, 33] = edge
+    q.qwm_attend(ctx, _bf(qb), nq, [ch], 1 / math.sqrt(D), out)
+    assert q.qwm_sync_status(ctx) == 0
+    k = synth.keys(WIDE_W)[:H, :200].copy(); v = synth.values(WIDE_W)[:H, :200].copy()
+    v[0, 150, 3] = big
+    act = q.ActiveChunk(_bf(k), _bf(v))
+    q.qwm_attend(ctx, _bf(qa), nq, [ch, act], 1 / math.sqrt(D), out)
+    assert q.qwm_sync_status(ctx) == q.QWM_ERR_RANGE
+
+
+def test_attend_expired_wait_recovers(q):
+    """The test hook makes one bounded wait of the attention kernel run out: the call reports
+    QWM_ERR_DEVICE_TIMEOUT, and the GPU and the library stay usable (a normal call that follows
+    gives the oracle's output)."""
+    ctx, ch = _packed(q)
+    H, nq = 2, 256
+    qa = synth.queries(synth.TINY, 5, nq)
+    out = torch.empty(H, nq, D, dtype=torch.float32, device="cuda")
+    hook = q.Context(heads=H, test_flags=q.QWM_TEST_EXPIRE_WAIT)
+    q.qwm_attend(hook, _bf(qa), nq, [ch], 1 / math.sqrt(D), out)
+    assert q.qwm_sync_status(hook) == q.QWM_ERR_DEVICE_TIMEOUT
+    assert q.qwm_sync_status(hook) == 0          # the status word was cleared
+    q.qwm_attend(ctx, _bf(qa), nq, [ch], 1 / math.sqrt(D), out)
+    assert q.qwm_sync_status(ctx) == 0
+    for h in range(H):
+        ref = oracle.attend_rows(qa[h], np.arange(nq), [chunk_head(ch, h)], 1 / math.sqrt(D))
         assert _attn_err(out[h].cpu().numpy().astype(np.float64), ref) <= 2e-2
 
 
