@@ -135,7 +135,7 @@ struct AttnParams {
   int compact;       // the chunks' INT2 metadata is the compact form (8-bit step, 2-bit zero-point)
   int any_causal;    // a bf16 chunk with a block-causal mask
   float scale_log2;  // softmax_scale * log2(e)
-  int test_expire;   // QWM_TEST_EXPIRE_WAIT: the MMA thread's wait before tile 1 runs out
+  int test_expire;   // QWM_TEST_EXPIRE_WAIT: the MMA thread's wait before its first tile runs out
   int32_t *status;
   AttnChunk ch[kMaxChunks];
 };
@@ -744,15 +744,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tc::mma2_ts(tO[x], tS[x] + 8u * kk, tc::desc_sw128_mn(sV + s * kBlk + 2048u * kk, kBlk, 1024), idesc_pv,
                       (!first || kk > 0));
       };
-      for (int j = 0; j < J; j++) {
+      if (p.test_expire) ok = tc::mbar_wait(&bars.never, 0, kTestWaitNs);  // test hook: a wait nothing ends
+      for (int j = 0; ok && j < J; j++) {
         const int s = j % kStages;
         const uint32_t ph = (uint32_t)(j / kStages) & 1u;
         const AttnChunk &ch = p.ch[t];
         const int nx = (WIDE && ch.rank > 8) ? 2 : 1;
-        if (p.test_expire && j == (J > 1 ? 1 : 0)) {  // test hook: a wait that nothing ends
-          ok = tc::mbar_wait(&bars.never, 0, kTestWaitNs);
-          if (!ok) break;
-        }
         ok = tc::mbar_wait_cluster(&bars.k_full[s], ph, kWaitNs) && !*abort_v;
         if (ok && tile_in_chunk == 0) ok = tc::mbar_wait_cluster(&bars.qx_full[t & 1], (t >> 1) & 1, kWaitNs);
         if (!ok) break;

@@ -14,6 +14,7 @@
 // fp16 codebook; the PSAC coefficients from the dense [H][N][r] arrays or, in the per-head layout,
 // through the head's entry (its rank, and for a sparse head the tile bitmap).
 #include "qwm_internal.cuh"
+#include "tc.cuh"
 
 namespace {
 
@@ -43,6 +44,10 @@ struct DqParams {
   uint16_t *k_hat, *v_hat;
   DqChunk ch[kMaxChunks];
 };
+
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
+}
 
 __device__ __forceinline__ uint4 to_bf16x8(const float (&x)[8]) {
   uint32_t o[4];
@@ -148,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, RU > 8 ? 1 : 2) dequant_kernel(const
   }
   // ---- U_r: this thread's 8 rows (fp32, zero past the rank) ----
   const int cb = tid & 15, c0 = 8 * cb, g = c0 / QWM_GROUP;
-  float U[8][RU > 0 ? RU : 1];
+  float U[8][RU > 0 ? RU : 1];  // (packed in pairs of channels below for the fp32x2 FMAs)
   if (RU > 0) {
 #pragma unroll
     for (int u = 0; u < 8; u++) {
@@ -170,6 +175,12 @@ __global__ void __launch_bounds__(kThreads, RU > 8 ? 1 : 2) dequant_kernel(const
       }
     }
   }
+  // the rows of U_r of channel pairs (2i, 2i+1), packed for the fp32x2 FMAs
+  uint64_t U2[4][RU > 0 ? RU : 1];
+#pragma unroll
+  for (int u = 0; u < 4; u++)
+#pragma unroll
+    for (int k = 0; k < (RU > 0 ? RU : 1); k++) U2[u][k] = RU > 0 ? pk2(U[2 * u][k], U[2 * u + 1][k]) : 0ull;
   __syncthreads();
   // ---- decode: 16 threads per token (8 channels each), 16 tokens per pass.  The centroid rows of
   // four passes are gathered first (the loads cannot move past the output stores on their own: the
@@ -216,11 +227,18 @@ __global__ void __launch_bounds__(kThreads, RU > 8 ? 1 : 2) dequant_kernel(const
           const uint4 cw = st.c[tt];
           const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
+          uint64_t x2[4];
+#pragma unroll
+          for (int u = 0; u < 4; u++) x2[u] = pk2(x[2 * u], x[2 * u + 1]);
+#pragma unroll
           for (int k = 0; k < (RU > 0 ? RU : 1); k++) {
             const float chat = sC * (float)(int8_t)((w[k >> 2] >> (8 * (k & 3))) & 0xFFu);  // exact
+            const uint64_t c2 = pk2(chat, chat);
 #pragma unroll
-            for (int u = 0; u < 8; u++) x[u] = fmaf(chat, U[u][k], x[u]);
+            for (int u = 0; u < 4; u++) x2[u] = tc::fma2(c2, U2[u][k], x2[u]);  // one rounding each, as fmaf
           }
+#pragma unroll
+          for (int u = 0; u < 4; u++) { x[2 * u] = tc::f2lo(x2[u]); x[2 * u + 1] = tc::f2hi(x2[u]); }
         }
         *(uint4 *)(p.k_hat + orow * D + c0) = to_bf16x8(x);
       }

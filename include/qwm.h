@@ -85,7 +85,7 @@ typedef struct {
 
 /* Test hooks (qwm_config.test_flags).
  *  QWM_TEST_EXPIRE_WAIT: in qwm_attend, the thread that issues the tensor-core work waits, before
- *    its second key tile, on a barrier that nothing completes, with a 1 ms limit.  The wait runs
+ *    its first key tile, on a barrier that nothing completes, with a 1 ms limit.  The wait runs
  *    out, the kernel takes the path every expired wait takes (it records QWM_ERR_DEVICE_TIMEOUT,
  *    every role stops within its own bounded waits, issued tensor-core work is drained and tensor
  *    memory freed) and the call's output is undefined; the context stays usable.  This exercises
