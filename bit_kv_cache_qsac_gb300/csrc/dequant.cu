@@ -58,32 +58,32 @@ __device__ __forceinline__ uint4 to_bf16x8(const float (&x)[8]) {
 
 // A CTA's token metadata, staged in shared memory by one coalesced pass (thread = token) so that the
 // decode loop reads it from there: codes, centroid indices, the INT2 step and offset of both groups
-// (fp16 pairs; the compact form's s = sigma s8 and m = -z s are exact fp16 values), and the Keys'
-// PSAC row resolved from either coefficient layout (dense [H][N][r], or per head through its entry).
+// (fp16 pairs; the compact form's s = sigma s8 and m = -z s are exact fp16 values), and, for Keys,
+// the PSAC row resolved from either coefficient layout (dense [H][N][r], or per head through its
+// entry).
 struct DqStage {
-  uint4 codes[2][kTok][2];   // [Keys, Values][token][32 bytes]
-  uint32_t s2[2][kTok];      // fp16 step of group 0 | group 1 << 16
-  uint32_t m2[2][kTok];      // fp16 offset, likewise
-  uint16_t idx[2][kTok];
-  uint4 c[kTok];             // up to 16 PSAC coefficient bytes (zero past the row's rank)
-  float sc[kTok];            // PSAC scale sC (0: no correction)
+  uint4 codes[kTok][2];  // [token][32 bytes]
+  uint32_t s2[kTok];     // fp16 step of group 0 | group 1 << 16
+  uint32_t m2[kTok];     // fp16 offset, likewise
+  uint16_t idx[kTok];
+  uint4 c[kTok];         // Keys: up to 16 PSAC coefficient bytes (zero past the row's rank)
+  float sc[kTok];        // Keys: PSAC scale sC (0: no correction)
 };
 
-template <bool IDX16, bool COMPACT>
-__device__ __forceinline__ void stage_tensor(const DqChunk &c, bool val, int h, int64_t tok, int C, DqStage &st,
-                                             int t) {
+template <bool VAL, bool IDX16, bool COMPACT>
+__device__ __forceinline__ void stage_tensor(const DqChunk &c, int h, int64_t tok, int C, DqStage &st, int t) {
   const int64_t row = (int64_t)h * c.n + tok;
-  const uint4 *cp = (const uint4 *)((val ? c.v_codes : c.k_codes) + row * (D / 4));
-  st.codes[val][t][0] = cp[0];
-  st.codes[val][t][1] = cp[1];
-  const uint8_t *ip = val ? c.v_idx : c.k_idx;
+  const uint4 *cp = (const uint4 *)((VAL ? c.v_codes : c.k_codes) + row * (D / 4));
+  st.codes[t][0] = cp[0];
+  st.codes[t][1] = cp[1];
+  const uint8_t *ip = VAL ? c.v_idx : c.k_idx;
   const int j = IDX16 ? (int)((const uint16_t *)ip)[row] : (int)ip[row];
-  st.idx[val][t] = (uint16_t)(j < C ? j : C - 1);  // never read past the codebook
+  st.idx[t] = (uint16_t)(j < C ? j : C - 1);  // never read past the codebook
   if (COMPACT) {
     const int64_t tiles = (c.n + 127) / 128;
-    const uint32_t sg2 = *(const uint32_t *)((val ? c.v_sigma : c.k_sigma) + ((int64_t)h * tiles + tok / 128) * 2);
-    const uint32_t s8 = *(const uint16_t *)((val ? c.v_s8 : c.k_s8) + row * 2);
-    const uint32_t z = (val ? c.v_zp : c.k_zp)[row];
+    const uint32_t sg2 = *(const uint32_t *)((VAL ? c.v_sigma : c.k_sigma) + ((int64_t)h * tiles + tok / 128) * 2);
+    const uint32_t s8 = *(const uint16_t *)((VAL ? c.v_s8 : c.k_s8) + row * 2);
+    const uint32_t z = (VAL ? c.v_zp : c.k_zp)[row];
     uint32_t s2 = 0, m2 = 0;
 #pragma unroll
     for (int g = 0; g < 2; g++) {
@@ -92,17 +92,20 @@ __device__ __forceinline__ void stage_tensor(const DqChunk &c, bool val, int h, 
       s2 |= (uint32_t)__half_as_ushort(__float2half_rn(sv)) << (16 * g);
       m2 |= (uint32_t)__half_as_ushort(__float2half_rn(mv)) << (16 * g);
     }
-    st.s2[val][t] = s2;
-    st.m2[val][t] = m2;
+    st.s2[t] = s2;
+    st.m2[t] = m2;
   } else {
-    st.s2[val][t] = *(const uint32_t *)((val ? c.v_scale : c.k_scale) + row * 2);
-    st.m2[val][t] = *(const uint32_t *)((val ? c.v_min : c.k_min) + row * 2);
+    st.s2[t] = *(const uint32_t *)((VAL ? c.v_scale : c.k_scale) + row * 2);
+    st.m2[t] = *(const uint32_t *)((VAL ? c.v_min : c.k_min) + row * 2);
   }
 }
 
-// RU: bound on the PSAC rank of the call's chunks (0, 8 or 16).
-template <int RU, bool IDX16, bool COMPACT>
-__global__ void __launch_bounds__(kThreads, RU > 8 ? 1 : 2) dequant_kernel(const __grid_constant__ DqParams p) {
+// One tensor per launch (VAL: Values, else Keys), so that the Value decoder, which holds no basis,
+// runs at the occupancy its smaller register footprint allows.  RU: bound on the PSAC rank of the
+// call's chunks (0, 8 or 16; 0 for Values).
+template <bool VAL, int RU, bool IDX16, bool COMPACT>
+__global__ void __launch_bounds__(kThreads, RU > 8 ? 1 : (RU > 0 ? 2 : 3))
+    dequant_kernel(const __grid_constant__ DqParams p) {
   __shared__ DqStage st;
   const int h = blockIdx.y, tid = threadIdx.x;
   int t = 0;  // the chunk of this CTA column (chunks are in column order)
@@ -110,14 +113,14 @@ __global__ void __launch_bounds__(kThreads, RU > 8 ? 1 : 2) dequant_kernel(const
   const DqChunk &c = p.ch[t];
   const int64_t tok0 = (int64_t)((int)blockIdx.x - c.tile0) * kTok;
   const int R = c.rank;
-  const bool psac = RU > 0 && p.k_hat && R > 0;
+  const bool psac = !VAL && RU > 0 && R > 0;
+  uint16_t *out = VAL ? p.v_hat : p.k_hat;
   // ---- staging: thread = token ----
   {
     const int64_t tok = tok0 + tid;
     if (tok < c.n) {
-      if (p.k_hat) stage_tensor<IDX16, COMPACT>(c, false, h, tok, p.C, st, tid);
-      if (p.v_hat) stage_tensor<IDX16, COMPACT>(c, true, h, tok, p.C, st, tid);
-      if (RU > 0) {
+      stage_tensor<VAL, IDX16, COMPACT>(c, h, tok, p.C, st, tid);
+      if (!VAL && RU > 0) {
         uint32_t w[4] = {0u, 0u, 0u, 0u};
         float sc = 0.f;
         if (psac) {
@@ -151,111 +154,112 @@ __global__ void __launch_bounds__(kThreads, RU > 8 ? 1 : 2) dequant_kernel(const
       }
     }
   }
-  // ---- U_r: this thread's 8 rows (fp32, zero past the rank) ----
+  // ---- Keys: this thread's 8 rows of U_r (zero past the rank), packed in pairs of channels ----
   const int cb = tid & 15, c0 = 8 * cb, g = c0 / QWM_GROUP;
-  float U[8][RU > 0 ? RU : 1];  // (packed in pairs of channels below for the fp32x2 FMAs)
-  if (RU > 0) {
+  constexpr int kRU = RU > 0 ? RU : 1;
+  uint64_t U2[4][kRU];
+#pragma unroll
+  for (int u = 0; u < 4; u++)
+#pragma unroll
+    for (int k = 0; k < kRU; k++) U2[u][k] = 0ull;
+  if (RU > 0 && psac) {
 #pragma unroll
     for (int u = 0; u < 8; u++) {
       const uint16_t *ur = c.u_r + ((int64_t)h * D + c0 + u) * R;
-      if (psac && R == RU) {  // a full row: 16-byte loads
+      float uf[kRU];
+      if (R == RU) {  // a full row: 16-byte loads
 #pragma unroll
-        for (int k8 = 0; k8 < (RU > 0 ? RU : 8) / 8; k8++) {
+        for (int k8 = 0; k8 < (kRU + 7) / 8; k8++) {
           const uint4 v = ((const uint4 *)ur)[k8];
           const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
           for (int q = 0; q < 4; q++) {
-            U[u][8 * k8 + 2 * q] = __uint_as_float(w[q] << 16);
-            U[u][8 * k8 + 2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+            if (8 * k8 + 2 * q + 1 < kRU) {
+              uf[8 * k8 + 2 * q] = __uint_as_float(w[q] << 16);
+              uf[8 * k8 + 2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+            }
           }
         }
       } else {
 #pragma unroll
-        for (int k = 0; k < (RU > 0 ? RU : 1); k++) U[u][k] = (psac && k < R) ? bf16_to_f32(ur[k]) : 0.f;
+        for (int k = 0; k < kRU; k++) uf[k] = k < R ? bf16_to_f32(ur[k]) : 0.f;
       }
+#pragma unroll
+      for (int k = 0; k < kRU; k++) U2[u >> 1][k] |= (uint64_t)__float_as_uint(uf[k]) << (32 * (u & 1));
     }
   }
-  // the rows of U_r of channel pairs (2i, 2i+1), packed for the fp32x2 FMAs
-  uint64_t U2[4][RU > 0 ? RU : 1];
-#pragma unroll
-  for (int u = 0; u < 4; u++)
-#pragma unroll
-    for (int k = 0; k < (RU > 0 ? RU : 1); k++) U2[u][k] = RU > 0 ? pk2(U[2 * u][k], U[2 * u + 1][k]) : 0ull;
   __syncthreads();
   // ---- decode: 16 threads per token (8 channels each), 16 tokens per pass.  The centroid rows of
   // four passes are gathered first (the loads cannot move past the output stores on their own: the
   // compiler has to assume the output may alias the codebook) ----
-  constexpr int kU = 4;
-  const uint16_t *ck = c.cent_k16 + (int64_t)h * p.C * D + c0, *cv = c.cent_v16 + (int64_t)h * p.C * D + c0;
-  auto decode8 = [&](bool val, int tt, const uint4 &mu, float (&x)[8]) {
-    const uint4 cw = st.codes[val][tt][cb >> 3];
-    const uint32_t cword = (cb & 4) ? ((cb & 2) ? cw.w : cw.z) : ((cb & 2) ? cw.y : cw.x);
-    const uint32_t b2 = (cb & 1) ? (cword >> 16) : (cword & 0xFFFFu);  // the 8 codes of channels c0..c0+7
-    const float s = f16_to_f32((uint16_t)(st.s2[val][tt] >> (16 * g)));
-    const float m = f16_to_f32((uint16_t)(st.m2[val][tt] >> (16 * g)));
-    const uint32_t muw[4] = {mu.x, mu.y, mu.z, mu.w};
-#pragma unroll
-    for (int u = 0; u < 8; u++) {
-      const float q = (float)((b2 >> (2 * u)) & 3u);
-      const float muf = f16_to_f32((uint16_t)(muw[u / 2] >> (16 * (u & 1))));
-      x[u] = __fadd_rn(muf, __fmaf_rn(s, q, m));
-    }
-  };
+  constexpr int kU = VAL ? 8 : 4;  // passes whose centroid rows are gathered together
+  const uint16_t *cent = (VAL ? c.cent_v16 : c.cent_k16) + (int64_t)h * p.C * D + c0;
   const int nt = (int)((c.n - tok0) < kTok ? (c.n - tok0) : kTok);  // tokens of this CTA
 #pragma unroll 1
   for (int p0 = 0; p0 < kPasses; p0 += kU) {
-    uint4 muk[kU], muv[kU];
+    uint4 mu[kU];
 #pragma unroll
     for (int a = 0; a < kU; a++) {
       const int tt = (p0 + a) * (kThreads / 16) + (tid >> 4);
-      muk[a] = muv[a] = make_uint4(0, 0, 0, 0);
-      if (tt < nt) {
-        if (p.k_hat) muk[a] = *(const uint4 *)(ck + (int64_t)st.idx[0][tt] * D);
-        if (p.v_hat) muv[a] = *(const uint4 *)(cv + (int64_t)st.idx[1][tt] * D);
-      }
+      mu[a] = tt < nt ? *(const uint4 *)(cent + (int64_t)st.idx[tt] * D) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int a = 0; a < kU; a++) {
       const int tt = (p0 + a) * (kThreads / 16) + (tid >> 4);
       if (tt >= nt) continue;
-      const int64_t orow = (int64_t)h * p.n_out + c.out0 + tok0 + tt;
-      if (p.k_hat) {
-        float x[8];
-        decode8(false, tt, muk[a], x);
-        if (RU > 0 && psac) {
-          const float sC = st.sc[tt];
-          const uint4 cw = st.c[tt];
-          const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
+      const uint4 cw = st.codes[tt][cb >> 3];
+      const uint32_t cword = (cb & 4) ? ((cb & 2) ? cw.w : cw.z) : ((cb & 2) ? cw.y : cw.x);
+      const uint32_t b2 = (cb & 1) ? (cword >> 16) : (cword & 0xFFFFu);  // the 8 codes of channels c0..c0+7
+      const float s = f16_to_f32((uint16_t)(st.s2[tt] >> (16 * g)));
+      const float m = f16_to_f32((uint16_t)(st.m2[tt] >> (16 * g)));
+      const uint32_t muw[4] = {mu[a].x, mu[a].y, mu[a].z, mu[a].w};
+      float x[8];
 #pragma unroll
-          uint64_t x2[4];
+      for (int u = 0; u < 8; u++) {
+        const float q = (float)((b2 >> (2 * u)) & 3u);
+        const float muf = f16_to_f32((uint16_t)(muw[u / 2] >> (16 * (u & 1))));
+        x[u] = __fadd_rn(muf, __fmaf_rn(s, q, m));
+      }
+      if (RU > 0 && psac) {
+        const float sC = st.sc[tt];
+        const uint4 cw2 = st.c[tt];
+        const uint32_t w[4] = {cw2.x, cw2.y, cw2.z, cw2.w};
+        uint64_t x2[4];
 #pragma unroll
-          for (int u = 0; u < 4; u++) x2[u] = pk2(x[2 * u], x[2 * u + 1]);
+        for (int u = 0; u < 4; u++) x2[u] = pk2(x[2 * u], x[2 * u + 1]);
 #pragma unroll
-          for (int k = 0; k < (RU > 0 ? RU : 1); k++) {
-            const float chat = sC * (float)(int8_t)((w[k >> 2] >> (8 * (k & 3))) & 0xFFu);  // exact
-            const uint64_t c2 = pk2(chat, chat);
+        for (int k = 0; k < kRU; k++) {
+          const float chat = sC * (float)(int8_t)((w[k >> 2] >> (8 * (k & 3))) & 0xFFu);  // exact
+          const uint64_t c2 = pk2(chat, chat);
 #pragma unroll
-            for (int u = 0; u < 4; u++) x2[u] = tc::fma2(c2, U2[u][k], x2[u]);  // one rounding each, as fmaf
-          }
-#pragma unroll
-          for (int u = 0; u < 4; u++) { x[2 * u] = tc::f2lo(x2[u]); x[2 * u + 1] = tc::f2hi(x2[u]); }
+          for (int u = 0; u < 4; u++) x2[u] = tc::fma2(c2, U2[u][k], x2[u]);  // one rounding each, as fmaf
         }
-        *(uint4 *)(p.k_hat + orow * D + c0) = to_bf16x8(x);
+#pragma unroll
+        for (int u = 0; u < 4; u++) { x[2 * u] = tc::f2lo(x2[u]); x[2 * u + 1] = tc::f2hi(x2[u]); }
       }
-      if (p.v_hat) {
-        float x[8];
-        decode8(true, tt, muv[a], x);
-        *(uint4 *)(p.v_hat + orow * D + c0) = to_bf16x8(x);
-      }
+      const int64_t orow = (int64_t)h * p.n_out + c.out0 + tok0 + tt;
+      *(uint4 *)(out + orow * D + c0) = to_bf16x8(x);
     }
   }
 }
 
-template <int RU, bool IDX16>
-cudaError_t launch_ru(const DqParams &p, dim3 grid, bool compact, cudaStream_t st) {
-  if (compact) dequant_kernel<RU, IDX16, true><<<grid, kThreads, 0, st>>>(p);
-  else dequant_kernel<RU, IDX16, false><<<grid, kThreads, 0, st>>>(p);
+template <bool VAL, int RU, bool IDX16>
+cudaError_t launch_one(const DqParams &p, dim3 grid, bool compact, cudaStream_t st) {
+  if (compact) dequant_kernel<VAL, RU, IDX16, true><<<grid, kThreads, 0, st>>>(p);
+  else dequant_kernel<VAL, RU, IDX16, false><<<grid, kThreads, 0, st>>>(p);
   return cudaGetLastError();
+}
+
+template <bool IDX16>
+cudaError_t launch_idx(const DqParams &p, dim3 grid, bool compact, int rmax, cudaStream_t st) {
+  cudaError_t e = cudaSuccess;
+  if (p.k_hat) {
+    if (rmax == 0) e = launch_one<false, 0, IDX16>(p, grid, compact, st);
+    else if (rmax <= 8) e = launch_one<false, 8, IDX16>(p, grid, compact, st);
+    else e = launch_one<false, 16, IDX16>(p, grid, compact, st);
+  }
+  if (e == cudaSuccess && p.v_hat) e = launch_one<true, 0, IDX16>(p, grid, compact, st);
+  return e;
 }
 
 }  // namespace
@@ -292,7 +296,5 @@ cudaError_t launch_dequantize(const qwm_config &cfg, const qwm_chunk *chunks, in
   if (used == 0 || (!k_hat && !v_hat)) return cudaSuccess;
   const dim3 grid((unsigned)tiles, (unsigned)cfg.heads);
   const bool idx16 = cfg.n_centroids > 256, compact = cfg.storage == QWM_STORAGE_COMPACT;
-  if (rmax == 0 || !k_hat) return idx16 ? launch_ru<0, true>(p, grid, compact, st) : launch_ru<0, false>(p, grid, compact, st);
-  if (rmax <= 8) return idx16 ? launch_ru<8, true>(p, grid, compact, st) : launch_ru<8, false>(p, grid, compact, st);
-  return idx16 ? launch_ru<16, true>(p, grid, compact, st) : launch_ru<16, false>(p, grid, compact, st);
+  return idx16 ? launch_idx<true>(p, grid, compact, rmax, st) : launch_idx<false>(p, grid, compact, rmax, st);
 }

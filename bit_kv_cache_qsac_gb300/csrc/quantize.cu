@@ -615,31 +615,18 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
           mxv[k][0] = mxv[k][1] = -INFINITY;
         }
         if (cnt > 0) {
-          // candidate rows come from L2: with up to 4 candidates the loads run two chunks ahead of
-          // their use (three sets in flight), so the latency is paid about once per token
-          constexpr int PF = KM <= 4 ? 2 : 0;
-          uint4 mq[PF + 1][KM];
 #pragma unroll
-          for (int a = 0; a < PF; a++)
+          for (int gi = 0; gi < 2; gi++) {  // the two groups of 64 channels
 #pragma unroll
-            for (int k = 0; k < KM; k++)
-              mq[a][k] = k < cnt ? *(const uint4 *)(cent + (int64_t)cj[k] * D + 8 * a) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-          for (int ci = 0; ci < D / 8; ci++) {
-            const int gi = ci >> 3, cc = ci & 7;
-            if (ci + PF < D / 8) {
-#pragma unroll
-              for (int k = 0; k < KM; k++)
-                mq[(ci + PF) % (PF + 1)][k] =
-                    k < cnt ? *(const uint4 *)(cent + (int64_t)cj[k] * D + 8 * (ci + PF)) : make_uint4(0, 0, 0, 0);
-            }
+          for (int cc = 0; cc < 8; cc++) {
+            const int ci = 8 * gi + cc;
             float f[8];
             bf16x8(tc::lds128(xts + gi * TILE * 128 + tc::sw128_offset(row, 8 * cc)), f);
 #pragma unroll
             for (int k = 0; k < KM; k++) {
               if (k < cnt) {
                 float mu[8];
-                bf16x8(mq[ci % (PF + 1)][k], mu);
+                bf16x8(*(const uint4 *)(cent + (int64_t)cj[k] * D + 8 * ci), mu);
 #pragma unroll
                 for (int u = 0; u < 8; u++) {
                   const float rr = __fsub_rn(f[u], mu[u]);
@@ -648,6 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
                 }
               }
             }
+          }
           }
         }
         float bS = INFINITY;
