@@ -249,9 +249,9 @@ def run_ours(args, rank, world, device):
         ev[4].record(stream)
 
     # kernels launched per step (counted from the library's launch sequence):
-    # each fit 1 + 2 x iterations (init; assign, update); packing 2 (Keys, Values); statistics 3
-    # (partial sums, finish, eigensolver); attention 1
-    launches_per_step = 2 * (1 + 2 * 10) + 2 + 3 + 1
+    # each fit 1 + 2 x iterations (init; assign, update); packing 3 (stored fp16 codebooks, Keys,
+    # Values); statistics 3 (partial sums, finish, eigensolver); attention 1
+    launches_per_step = 2 * (1 + 2 * 10) + 3 + 3 + 1
 
     clk = ClockSampler(device.index if device.index is not None else 0).__enter__()
     for _ in range(args.warmup):
