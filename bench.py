@@ -169,21 +169,29 @@ def gen_layer(layer: int):
     return ks, vs, qs
 
 
-# DRAM bytes per launch of the attention kernel (dram__bytes_read.sum + dram__bytes_write.sum from
-# one ncu capture of this workload), valid only for the kernel source they were taken on: the
-# SHA-256 of csrc/attend.cu is checked, and the traffic reported as null otherwise.
-ATTEND_TRAFFIC = {"sha256": "8e38218c31e3d74b6f21e85f9b27fe178100a327181f3c0d75869429c334cd1c",
-                  "720p": 476568320 + 192466176, "480p": 227467776 + 66667520}
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch, from ncu captures of the
+# kernel sources whose SHA-256 is given (the traffic is reported as null for any other source):
+# attention per launch; packing per step (the Key and the Value pass).  The packing's 720p figure is
+# its 480p capture scaled by the tokens processed (10,800 / 4,680): each pass reads its input once
+# (its outputs stay in L2 when it ends), so its traffic grows in proportion.
+TRAFFIC = {
+    "attend.cu": {"sha256": "88b6a5df901f45795f665fce436100c791bdb22dc863825c58f44bb5b53079b2",
+                  "480p": 228292608 + 67828224},
+    "quantize.cu": {"sha256": "e84e7a59bd241f42592420dd3afd237f9448e979a2bcc2ad1e6ad52abc89c82d",
+                    "480p": (50848000 + 270848) + (50659840 + 256),
+                    "720p": round(((50848000 + 270848) + (50659840 + 256)) * 10800 / 4680)},
+}
 
 
-def attend_traffic(workload: str):
+def kernel_traffic(source: str, workload: str):
     import hashlib
-    src = os.path.join(ROOT, "bit_kv_cache_qsac_gb300", "csrc", "attend.cu")
+    src = os.path.join(ROOT, "bit_kv_cache_qsac_gb300", "csrc", source)
     try:
         digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
     except OSError:
         return None
-    return ATTEND_TRAFFIC.get(workload) if digest == ATTEND_TRAFFIC["sha256"] else None
+    entry = TRAFFIC.get(source, {})
+    return entry.get(workload) if digest == entry.get("sha256") else None
 
 
 def run_ours(args, rank, world, device):
@@ -386,11 +394,15 @@ def run_ours(args, rank, world, device):
         "roofline": {"bound": "tensor", "kernel": "attend", "achieved": attend_tflops, "peak": peak_tf,
                      "unit": "TFLOP/s", "frac": attend_tflops / peak_tf if peak_tf else None,
                      "peak_source": f"dense bf16 {peak_tf_kind}, {peak_kind}; fp16 MMAs run at the bf16 rate",
-                     "traffic": attend_traffic(W.name),
+                     "traffic": kernel_traffic("attend.cu", W.name),
                      "algorithmic": f"{FLOPS_PER_PAIR} flops per (query, key) pair x {pairs} pairs"},
-        "roofline_quantize": {"bound": "hbm", "kernel": "quantize", "achieved": q_gbs, "peak": peak_bw,
+        "roofline_quantize": {"bound": "hbm", "kernel": "quantize",
+                              "scope": "qwm_quantize_kv only (stored codebooks, Key pass, Value pass); the k-means "
+                                       "fits are the separate roofline_fit",
+                              "achieved": q_gbs, "peak": peak_bw,
                               "unit": "GB/s", "frac": q_gbs / peak_bw if peak_bw else None,
-                              "peak_source": f"hbm copy, {peak_kind}", "traffic": None,
+                              "peak_source": f"hbm copy, {peak_kind}",
+                              "traffic": kernel_traffic("quantize.cu", W.name),
                               "algorithmic": f"{QUANT_BYTES_PER_TOKEN_HEAD} B per token-head + "
                                              f"{QUANT_BYTES_PER_HEAD} B per head"},
         "roofline_fit": {"bound": "hbm", "kernel": "fit_k_v (kmeans_init, km_assign, km_update)",
