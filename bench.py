@@ -439,7 +439,8 @@ def comparisons(q, ctx, chunks, ks, vs, Qc, device, stream, flush):
     """Context for the attention timing (not part of the step): the pages' own decode path
     (qwm_dequantize every chunk to bf16, then a fused bf16 attention) and the same attention on the
     uncompressed bf16 Keys/Values, both through torch's scaled_dot_product_attention with a fused
-    backend (never the unfused math one), timed with CUDA events after one warm-up."""
+    backend (never the unfused math one), timed with CUDA events after one warm-up (the decode path:
+    the median of five passes, each after an L2 flush)."""
     import torch
     from torch.nn.attention import SDPBackend, sdpa_kernel
     backends = [SDPBackend.CUDNN_ATTENTION, SDPBackend.FLASH_ATTENTION, SDPBackend.EFFICIENT_ATTENTION]
@@ -449,7 +450,8 @@ def comparisons(q, ctx, chunks, ks, vs, Qc, device, stream, flush):
         kh = torch.empty(1, H, N_CACHE, D, dtype=torch.bfloat16, device=device)
         vh = torch.empty_like(kh)
         qb = Qc.unsqueeze(0)
-        for rep in range(2):                     # the first pass warms up
+        deqs, sdpas = [], []
+        for rep in range(6):                     # the first pass warms up; the median of the other five
             flush.zero_()
             ev[0].record(stream)
             q.qwm_dequantize_chunks(ctx, chunks, kh[0], vh[0], stream)
@@ -458,7 +460,10 @@ def comparisons(q, ctx, chunks, ks, vs, Qc, device, stream, flush):
                 o = torch.nn.functional.scaled_dot_product_attention(qb, kh, vh)
             ev[2].record(stream)
             ev[2].synchronize()
-        deq, sdpa = ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])
+            if rep > 0:
+                deqs.append(ev[0].elapsed_time(ev[1]))
+                sdpas.append(ev[1].elapsed_time(ev[2]))
+        deq, sdpa = float(np.median(deqs)), float(np.median(sdpas))
         pairs = H * NQ * N_CACHE
         # the decoder's algorithmic bytes: the packed cache read once, bf16 K_hat and V_hat written once
         deq_bytes = sum(c.nbytes() for c in chunks) + 2 * H * N_CACHE * D * 2

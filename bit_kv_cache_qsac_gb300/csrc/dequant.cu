@@ -1,18 +1,26 @@
 // Step 5': BF16 reconstruction of packed chunks (QuantWM English v2 summary §D.1: the fused decoder
 // unpacks the INT2 residuals, rebuilds the affine parameters, gathers the centroids and adds the
 // PSAC term; Chinese summary step (5)).
-//   K_hat = (mu^K_idx + (m + s q)) + sum_k (sC c_k) U_r[:, k],   V_hat = mu^V_idx + (m + s q),
-// evaluated in fp32 (m + s q is exact: s q is exact and both are fp16 values) and rounded to bf16.
+//   K_hat = (mu^K_idx + (m + s q)) + sC * sum_k c_k U_r[:, k],   V_hat = mu^V_idx + (m + s q),
+// evaluated in fp32 and rounded to bf16.
 //
-// A bandwidth kernel: per token-head it reads 92 bytes of packed data (plus a codebook row that
-// stays in L2) and writes 512 bytes of bf16, so it is bound by the HBM write stream.  One CTA takes
-// 256 tokens of one chunk for one head, 16 threads per token (8 channels each, one 16-byte store per
-// tensor), in passes of 16 tokens; the token metadata is staged in shared memory first, and the
-// centroid rows of four passes are gathered before they are used.  A thread keeps the same 8 channels for the whole
-// CTA, so it holds their rows of U_r (fp32) in registers, loaded once (16-byte loads).  All chunks of a call go in one launch, each chunk's
-// rows written at its offset in the [H][sum N][d] output.  The centroids come from the chunk's stored
-// fp16 codebook; the PSAC coefficients from the dense [H][N][r] arrays or, in the per-head layout,
-// through the head's entry (its rank, and for a sparse head the tile bitmap).
+// A bandwidth kernel: per token-head it reads about 50 bytes of packed data (plus a codebook row that
+// stays in L2) and writes 256 bytes of bf16, so it is bound by the HBM write stream.  One CTA takes
+// 256 tokens of one chunk for one head; the token metadata is staged in shared memory first (one
+// coalesced pass, thread = token), and every centroid gather of a thread is issued before its first
+// store (the compiler has to assume the output may alias the codebook, so it cannot move the loads
+// past the stores by itself).
+// Values (and Keys without PSAC): 16 threads per token, 8 channels each, one 16-byte store per
+// token.  Keys with PSAC: the correction sum_k c_k U_r[:, k] of 16 tokens x 128 channels is one
+// warp's set of mma.sync m16n8k8 (rank <= 8) or m16n8k16 products: bf16 operands (the int8
+// coefficients and the bf16 basis are exact bf16 values, so every product is exact) with fp32
+// accumulation.  The n-tiles' columns are permuted so that each thread's accumulators are 4 runs of
+// 8 consecutive channels (32 i + 8 t .. + 7 for the thread's t = lane % 4) of its two tokens (rows
+// lane / 4 and lane / 4 + 8), decoded in place and stored 16 bytes at a time.  All chunks of a call
+// go in one launch, each chunk's rows written at its offset in the [H][sum N][d] output.  The
+// centroids come from the chunk's stored fp16 codebook; the PSAC coefficients from the dense
+// [H][N][r] arrays or, in the per-head layout, through the head's entry (its rank, and for a
+// sparse head the tile bitmap).
 #include "qwm_internal.cuh"
 #include "tc.cuh"
 
@@ -44,17 +52,6 @@ struct DqParams {
   uint16_t *k_hat, *v_hat;
   DqChunk ch[kMaxChunks];
 };
-
-__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
-  return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
-}
-
-__device__ __forceinline__ uint4 to_bf16x8(const float (&x)[8]) {
-  uint32_t o[4];
-#pragma unroll
-  for (int u = 0; u < 4; u++) o[u] = (uint32_t)f32_to_bf16_rn(x[2 * u]) | ((uint32_t)f32_to_bf16_rn(x[2 * u + 1]) << 16);
-  return make_uint4(o[0], o[1], o[2], o[3]);
-}
 
 // A CTA's token metadata, staged in shared memory by one coalesced pass (thread = token) so that the
 // decode loop reads it from there: codes, centroid indices, the INT2 step and offset of both groups
@@ -100,108 +97,110 @@ __device__ __forceinline__ void stage_tensor(const DqChunk &c, int h, int64_t to
   }
 }
 
-// One tensor per launch (VAL: Values, else Keys), so that the Value decoder, which holds no basis,
-// runs at the occupancy its smaller register footprint allows.  RU: bound on the PSAC rank of the
-// call's chunks (0, 8 or 16; 0 for Values).
-template <bool VAL, int RU, bool IDX16, bool COMPACT>
-__global__ void __launch_bounds__(kThreads, RU > 8 ? 1 : (RU > 0 ? 2 : 3))
-    dequant_kernel(const __grid_constant__ DqParams p) {
+// Eight channels of one token: x_u = mu_u + (m + s q_u) (+ sC corr_u), rounded to bf16.  `bits` holds
+// the 8 two-bit codes (channel u in bits 2u..2u+1), `mu` the 8 fp16 centroid elements.
+template <bool CORR>
+__device__ __forceinline__ uint4 decode8(const uint4 mu, uint32_t bits, float s, float m, float sc,
+                                         const float (&corr)[8]) {
+  const uint32_t muw[4] = {mu.x, mu.y, mu.z, mu.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int v = 0; v < 4; v++) {
+    float x[2];
+#pragma unroll
+    for (int e = 0; e < 2; e++) {
+      const int u = 2 * v + e;
+      const float q = (float)((bits >> (2 * u)) & 3u);
+      const float muf = f16_to_f32((uint16_t)(muw[v] >> (16 * e)));
+      x[e] = __fadd_rn(muf, __fmaf_rn(s, q, m));
+      if (CORR) x[e] = __fmaf_rn(sc, corr[u], x[e]);
+    }
+    o[v] = tc::pack_bf16x2(x[0], x[1]);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Staging of one CTA's token metadata (thread = token; tokens past the chunk staged as zeros, so
+// that every later read of the stage is in bounds and decodes to finite values).
+template <bool VAL, bool PSAC, bool IDX16, bool COMPACT>
+__device__ __forceinline__ void stage_cta(const DqChunk &c, int h, int64_t tok0, int C, DqStage &st, int tid) {
+  const int64_t tok = tok0 + tid;
+  if (tok >= c.n) {
+    st.codes[tid][0] = st.codes[tid][1] = make_uint4(0, 0, 0, 0);
+    st.s2[tid] = st.m2[tid] = 0u;
+    st.idx[tid] = 0;
+    if (PSAC) {
+      st.c[tid] = make_uint4(0, 0, 0, 0);
+      st.sc[tid] = 0.f;
+    }
+    return;
+  }
+  stage_tensor<VAL, IDX16, COMPACT>(c, h, tok, C, st, tid);
+  if (PSAC) {
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    float sc = 0.f;
+    if (c.rank > 0) {
+      int64_t crow = (int64_t)h * c.n + tok;
+      int rr = c.rank;
+      const int8_t *cbase = c.c;
+      const uint16_t *sbase = c.c_scale;
+      bool has = true;
+      if (c.per_head) {  // the head's rank and layout
+        const qwm_psac_head hd = c.c_heads[h];
+        has = psac_row(hd, c.c_mask, c.c_tile_rank, (c.n + 127) / 128, h, tok, crow);
+        rr = hd.rank;
+        cbase += hd.c_off;
+        sbase += hd.s_off;
+      }
+      if (has) {
+        sc = f16_to_f32(sbase[crow]);
+        const int8_t *cc = cbase + crow * rr;
+        if (!c.per_head && rr == 8) {
+          const uint2 v = *(const uint2 *)cc;
+          w[0] = v.x; w[1] = v.y;
+        } else {
+#pragma unroll
+          for (int k = 0; k < 16; k++)
+            if (k < rr) w[k >> 2] |= ((uint32_t)(uint8_t)cc[k]) << (8 * (k & 3));
+        }
+      }
+    }
+    st.c[tid] = make_uint4(w[0], w[1], w[2], w[3]);
+    st.sc[tid] = sc;
+  }
+}
+
+__device__ __forceinline__ int chunk_of_cta(const DqParams &p) {
+  int t = 0;  // chunks are in CTA-column order
+  while (t + 1 < p.n_chunks && p.ch[t + 1].tile0 <= (int)blockIdx.x) t++;
+  return t;
+}
+
+// Values, or Keys without any PSAC term in the call: 16 threads per token (8 channels each), 16
+// tokens per pass; the centroid rows of 8 passes are gathered before they are used (the compiler has
+// to assume the output may alias the codebook, so the loads cannot move past the stores by themselves).
+template <bool VAL, bool IDX16, bool COMPACT>
+__global__ void __launch_bounds__(kThreads, 3) dequant_kernel(const __grid_constant__ DqParams p) {
   __shared__ DqStage st;
   const int h = blockIdx.y, tid = threadIdx.x;
-  int t = 0;  // the chunk of this CTA column (chunks are in column order)
-  while (t + 1 < p.n_chunks && p.ch[t + 1].tile0 <= (int)blockIdx.x) t++;
-  const DqChunk &c = p.ch[t];
+  const DqChunk &c = p.ch[chunk_of_cta(p)];
   const int64_t tok0 = (int64_t)((int)blockIdx.x - c.tile0) * kTok;
-  const int R = c.rank;
-  const bool psac = !VAL && RU > 0 && R > 0;
-  uint16_t *out = VAL ? p.v_hat : p.k_hat;
-  // ---- staging: thread = token ----
-  {
-    const int64_t tok = tok0 + tid;
-    if (tok < c.n) {
-      stage_tensor<VAL, IDX16, COMPACT>(c, h, tok, p.C, st, tid);
-      if (!VAL && RU > 0) {
-        uint32_t w[4] = {0u, 0u, 0u, 0u};
-        float sc = 0.f;
-        if (psac) {
-          int64_t crow = (int64_t)h * c.n + tok;
-          int rr = R;
-          const int8_t *cbase = c.c;
-          const uint16_t *sbase = c.c_scale;
-          bool has = true;
-          if (c.per_head) {  // the head's rank and layout
-            const qwm_psac_head hd = c.c_heads[h];
-            has = psac_row(hd, c.c_mask, c.c_tile_rank, (c.n + 127) / 128, h, tok, crow);
-            rr = hd.rank;
-            cbase += hd.c_off;
-            sbase += hd.s_off;
-          }
-          if (has) {
-            sc = f16_to_f32(sbase[crow]);
-            const int8_t *cc = cbase + crow * rr;
-            if (!c.per_head && rr == 8) {
-              const uint2 v = *(const uint2 *)cc;
-              w[0] = v.x; w[1] = v.y;
-            } else {
-#pragma unroll
-              for (int k = 0; k < 16; k++)
-                if (k < rr) w[k >> 2] |= ((uint32_t)(uint8_t)cc[k]) << (8 * (k & 3));
-            }
-          }
-        }
-        st.c[tid] = make_uint4(w[0], w[1], w[2], w[3]);
-        st.sc[tid] = sc;
-      }
-    }
-  }
-  // ---- Keys: this thread's 8 rows of U_r (zero past the rank), packed in pairs of channels ----
-  const int cb = tid & 15, c0 = 8 * cb, g = c0 / QWM_GROUP;
-  constexpr int kRU = RU > 0 ? RU : 1;
-  uint64_t U2[4][kRU];
-#pragma unroll
-  for (int u = 0; u < 4; u++)
-#pragma unroll
-    for (int k = 0; k < kRU; k++) U2[u][k] = 0ull;
-  if (RU > 0 && psac) {
-#pragma unroll
-    for (int u = 0; u < 8; u++) {
-      const uint16_t *ur = c.u_r + ((int64_t)h * D + c0 + u) * R;
-      float uf[kRU];
-      if (R == RU) {  // a full row: 16-byte loads
-#pragma unroll
-        for (int k8 = 0; k8 < (kRU + 7) / 8; k8++) {
-          const uint4 v = ((const uint4 *)ur)[k8];
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int q = 0; q < 4; q++) {
-            if (8 * k8 + 2 * q + 1 < kRU) {
-              uf[8 * k8 + 2 * q] = __uint_as_float(w[q] << 16);
-              uf[8 * k8 + 2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
-            }
-          }
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < kRU; k++) uf[k] = k < R ? bf16_to_f32(ur[k]) : 0.f;
-      }
-#pragma unroll
-      for (int k = 0; k < kRU; k++) U2[u >> 1][k] |= (uint64_t)__float_as_uint(uf[k]) << (32 * (u & 1));
-    }
-  }
+  stage_cta<VAL, false, IDX16, COMPACT>(c, h, tok0, p.C, st, tid);
   __syncthreads();
-  // ---- decode: 16 threads per token (8 channels each), 16 tokens per pass.  The centroid rows of
-  // four passes are gathered first (the loads cannot move past the output stores on their own: the
-  // compiler has to assume the output may alias the codebook) ----
-  constexpr int kU = VAL ? 8 : 4;  // passes whose centroid rows are gathered together
+  constexpr int kU = 8;
+  const int cb = tid & 15, c0 = 8 * cb, g = c0 / QWM_GROUP;
   const uint16_t *cent = (VAL ? c.cent_v16 : c.cent_k16) + (int64_t)h * p.C * D + c0;
+  uint16_t *out = (VAL ? p.v_hat : p.k_hat) + ((int64_t)h * p.n_out + c.out0 + tok0) * D + c0;
   const int nt = (int)((c.n - tok0) < kTok ? (c.n - tok0) : kTok);  // tokens of this CTA
+  const float none[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
   for (int p0 = 0; p0 < kPasses; p0 += kU) {
+    if (p0 * (kThreads / 16) >= nt) break;
     uint4 mu[kU];
 #pragma unroll
     for (int a = 0; a < kU; a++) {
       const int tt = (p0 + a) * (kThreads / 16) + (tid >> 4);
-      mu[a] = tt < nt ? *(const uint4 *)(cent + (int64_t)st.idx[tt] * D) : make_uint4(0, 0, 0, 0);
+      mu[a] = *(const uint4 *)(cent + (int64_t)st.idx[tt] * D);  // staged index 0 past the chunk
     }
 #pragma unroll
     for (int a = 0; a < kU; a++) {
@@ -212,41 +211,134 @@ __global__ void __launch_bounds__(kThreads, RU > 8 ? 1 : (RU > 0 ? 2 : 3))
       const uint32_t b2 = (cb & 1) ? (cword >> 16) : (cword & 0xFFFFu);  // the 8 codes of channels c0..c0+7
       const float s = f16_to_f32((uint16_t)(st.s2[tt] >> (16 * g)));
       const float m = f16_to_f32((uint16_t)(st.m2[tt] >> (16 * g)));
-      const uint32_t muw[4] = {mu[a].x, mu[a].y, mu[a].z, mu[a].w};
-      float x[8];
-#pragma unroll
-      for (int u = 0; u < 8; u++) {
-        const float q = (float)((b2 >> (2 * u)) & 3u);
-        const float muf = f16_to_f32((uint16_t)(muw[u / 2] >> (16 * (u & 1))));
-        x[u] = __fadd_rn(muf, __fmaf_rn(s, q, m));
-      }
-      if (RU > 0 && psac) {
-        const float sC = st.sc[tt];
-        const uint4 cw2 = st.c[tt];
-        const uint32_t w[4] = {cw2.x, cw2.y, cw2.z, cw2.w};
-        uint64_t x2[4];
-#pragma unroll
-        for (int u = 0; u < 4; u++) x2[u] = pk2(x[2 * u], x[2 * u + 1]);
-#pragma unroll
-        for (int k = 0; k < kRU; k++) {
-          const float chat = sC * (float)(int8_t)((w[k >> 2] >> (8 * (k & 3))) & 0xFFu);  // exact
-          const uint64_t c2 = pk2(chat, chat);
-#pragma unroll
-          for (int u = 0; u < 4; u++) x2[u] = tc::fma2(c2, U2[u][k], x2[u]);  // one rounding each, as fmaf
-        }
-#pragma unroll
-        for (int u = 0; u < 4; u++) { x[2 * u] = tc::f2lo(x2[u]); x[2 * u + 1] = tc::f2hi(x2[u]); }
-      }
-      const int64_t orow = (int64_t)h * p.n_out + c.out0 + tok0 + tt;
-      *(uint4 *)(out + orow * D + c0) = to_bf16x8(x);
+      *(uint4 *)(out + (int64_t)tt * D) = decode8<false>(mu[a], b2, s, m, 0.f, none);
     }
   }
 }
 
-template <bool VAL, int RU, bool IDX16>
-cudaError_t launch_one(const DqParams &p, dim3 grid, bool compact, cudaStream_t st) {
-  if (compact) dequant_kernel<VAL, RU, IDX16, true><<<grid, kThreads, 0, st>>>(p);
-  else dequant_kernel<VAL, RU, IDX16, false><<<grid, kThreads, 0, st>>>(p);
+// One warp-level product D[16][8] += A[16][K] B[K][8] (bf16 A, B; fp32 D), K = 8 or 16.
+template <int KS>
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[KS / 4], const uint32_t (&b)[KS / 8]) {
+  if constexpr (KS == 8) {
+    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(b[0]));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+  }
+}
+
+// Coefficients k = 2 t, 2 t + 1 (+ 8 kb) of a staged row as a bf16 pair (int8 values: exact).
+__device__ __forceinline__ uint32_t coef_pair(const uint4 cw, int t, int kb) {
+  const uint32_t w = kb == 0 ? ((t >> 1) ? cw.y : cw.x) : ((t >> 1) ? cw.w : cw.z);
+  const uint32_t hw = (t & 1) ? (w >> 16) : (w & 0xFFFFu);
+  return tc::pack_bf16x2((float)(int8_t)(hw & 0xFFu), (float)(int8_t)(hw >> 8));
+}
+
+// Keys with PSAC (RU: bound on the call's ranks, 8 or 16).  Warp w decodes the 16-token tiles w and
+// w + 8 of the CTA; thread (g, t) = (lane / 4, lane % 4) owns tokens g and g + 8 of a tile and
+// channels 32 i + 8 t .. 32 i + 8 t + 7, i = 0..3.  Column j of n-tile n = 4 i + a is channel
+// 32 i + 8 (j / 2) + 2 a + j % 2, so the accumulator pair (a, 2 t + e) of the fragment layout is the
+// thread's channel 32 i + 8 t + 2 a + e.
+template <int RU, bool IDX16, bool COMPACT>
+__global__ void __launch_bounds__(kThreads, 3) dequant_key_kernel(const __grid_constant__ DqParams p) {
+  constexpr int KS = RU > 8 ? 16 : 8, KB = KS / 8;
+  __shared__ DqStage st;
+  const int h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
+  const DqChunk &c = p.ch[chunk_of_cta(p)];
+  const int64_t tok0 = (int64_t)((int)blockIdx.x - c.tile0) * kTok;
+  const int R = c.rank;
+  // B fragments in shared memory, in fragment order: word (n * KB + kb) * 32 + lane holds, for lane
+  // (g, t), the basis entries k = 2 t + 8 kb, k + 1 of column g of n-tile n (zero past the rank)
+  __shared__ uint32_t ufrag[16 * KB * 32];
+  for (int e = tid; e < 16 * KB * 32; e += kThreads) {
+    const int ln = e & 31, n = (e >> 5) / KB, kb = (e >> 5) % KB, gg = ln >> 2, tt = ln & 3;
+    const int ch = 32 * (n >> 2) + 8 * (gg >> 1) + 2 * (n & 3) + (gg & 1);
+    const uint16_t *ur = c.u_r + ((int64_t)h * D + ch) * R;
+    const int k = 2 * tt + 8 * kb;
+    uint32_t v = 0u;
+    if ((R & 1) == 0) {
+      if (k < R) v = *(const uint32_t *)(ur + k);  // 4-byte aligned: R and k even
+    } else {
+      if (k < R) v = ur[k];
+      if (k + 1 < R) v |= (uint32_t)ur[k + 1] << 16;
+    }
+    ufrag[e] = v;
+  }
+  stage_cta<false, true, IDX16, COMPACT>(c, h, tok0, p.C, st, tid);
+  __syncthreads();
+  const int nt = (int)((c.n - tok0) < kTok ? (c.n - tok0) : kTok);
+  const uint16_t *cent = c.cent_k16 + (int64_t)h * p.C * D + 8 * t4;
+  uint16_t *out = p.k_hat + ((int64_t)h * p.n_out + c.out0 + tok0) * D + 8 * t4;
+  const uint32_t *codes32 = (const uint32_t *)&st.codes[0][0];
+#pragma unroll 1
+  for (int wt = warp; 16 * wt < nt; wt += kThreads / 32) {
+    const int r0 = 16 * wt + g, r1 = r0 + 8;
+    // the two tokens' centroid chunks, all gathered before the first store
+    uint4 mu0[4], mu1[4];
+    const uint16_t *row0 = cent + (int)st.idx[r0] * D, *row1 = cent + (int)st.idx[r1] * D;
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+      mu0[i] = *(const uint4 *)(row0 + 32 * i);
+      mu1[i] = *(const uint4 *)(row1 + 32 * i);
+    }
+    const uint4 cA = st.c[r0], cB = st.c[r1];
+    uint32_t af[KS / 4];
+    af[0] = coef_pair(cA, t4, 0);
+    af[1] = coef_pair(cB, t4, 0);
+    if constexpr (KS == 16) {
+      af[2] = coef_pair(cA, t4, 1);
+      af[3] = coef_pair(cB, t4, 1);
+    }
+    const uint32_t sA = st.s2[r0], mA = st.m2[r0], sB = st.s2[r1], mB = st.m2[r1];
+    const float scA = st.sc[r0], scB = st.sc[r1];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+      float acc[4][4];
+#pragma unroll
+      for (int a = 0; a < 4; a++) {
+        acc[a][0] = acc[a][1] = acc[a][2] = acc[a][3] = 0.f;
+        uint32_t bfr[KB];
+#pragma unroll
+        for (int kb = 0; kb < KB; kb++) bfr[kb] = ufrag[((4 * i + a) * KB + kb) * 32 + lane];
+        mma_bf16<KS>(acc[a], af, bfr);
+      }
+      const int gi = i >> 1, sh = 16 * (t4 & 1);
+      // the 8 codes of channels 32 i + 8 t .. + 7: halfword (t % 2) of word 2 i + t / 2 of the row
+      const uint32_t bA = (codes32[8 * r0 + 2 * i + (t4 >> 1)] >> sh) & 0xFFFFu;
+      const uint32_t bB = (codes32[8 * r1 + 2 * i + (t4 >> 1)] >> sh) & 0xFFFFu;
+      float cr0[8], cr1[8];
+#pragma unroll
+      for (int u = 0; u < 8; u++) {
+        cr0[u] = acc[u >> 1][u & 1];
+        cr1[u] = acc[u >> 1][2 + (u & 1)];
+      }
+      if (r0 < nt)
+        *(uint4 *)(out + (int64_t)r0 * D + 32 * i) =
+            decode8<true>(mu0[i], bA, f16_to_f32((uint16_t)(sA >> (16 * gi))), f16_to_f32((uint16_t)(mA >> (16 * gi))),
+                          scA, cr0);
+      if (r1 < nt)
+        *(uint4 *)(out + (int64_t)r1 * D + 32 * i) =
+            decode8<true>(mu1[i], bB, f16_to_f32((uint16_t)(sB >> (16 * gi))), f16_to_f32((uint16_t)(mB >> (16 * gi))),
+                          scB, cr1);
+    }
+  }
+}
+
+template <bool VAL, bool IDX16>
+cudaError_t launch_plain(const DqParams &p, dim3 grid, bool compact, cudaStream_t st) {
+  if (compact) dequant_kernel<VAL, IDX16, true><<<grid, kThreads, 0, st>>>(p);
+  else dequant_kernel<VAL, IDX16, false><<<grid, kThreads, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <int RU, bool IDX16>
+cudaError_t launch_keys(const DqParams &p, dim3 grid, bool compact, cudaStream_t st) {
+  if (compact) dequant_key_kernel<RU, IDX16, true><<<grid, kThreads, 0, st>>>(p);
+  else dequant_key_kernel<RU, IDX16, false><<<grid, kThreads, 0, st>>>(p);
   return cudaGetLastError();
 }
 
@@ -254,11 +346,11 @@ template <bool IDX16>
 cudaError_t launch_idx(const DqParams &p, dim3 grid, bool compact, int rmax, cudaStream_t st) {
   cudaError_t e = cudaSuccess;
   if (p.k_hat) {
-    if (rmax == 0) e = launch_one<false, 0, IDX16>(p, grid, compact, st);
-    else if (rmax <= 8) e = launch_one<false, 8, IDX16>(p, grid, compact, st);
-    else e = launch_one<false, 16, IDX16>(p, grid, compact, st);
+    if (rmax == 0) e = launch_plain<false, IDX16>(p, grid, compact, st);
+    else if (rmax <= 8) e = launch_keys<8, IDX16>(p, grid, compact, st);
+    else e = launch_keys<16, IDX16>(p, grid, compact, st);
   }
-  if (e == cudaSuccess && p.v_hat) e = launch_one<true, 0, IDX16>(p, grid, compact, st);
+  if (e == cudaSuccess && p.v_hat) e = launch_plain<true, IDX16>(p, grid, compact, st);
   return e;
 }
 
