@@ -11,7 +11,7 @@ constexpr int kStatsSplits = 8;
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
-  size_t status, stats_part, km_sum, km_cnt, km_cent, km_img, q_img, q_bfull, q_mfull, total;
+  size_t status, stats_part, km_sum, km_cnt, km_cent, km_img, km_prev, q_img, q_bfull, q_mfull, total;
 };
 
 Layout layout_of(const qwm_config &c) {
@@ -24,6 +24,8 @@ Layout layout_of(const qwm_config &c) {
   L.km_cnt = off; off = align_up(off + G * c.heads * c.n_centroids * sizeof(int32_t), 256);
   L.km_cent = off; off = align_up(off + (size_t)c.heads * c.n_centroids * QWM_D * sizeof(float), 256);
   L.km_img = off; off = align_up(off + kmeans_image_bytes(c.heads, c.n_centroids), 1024);
+  L.km_prev = off;  // resident codebooks only (uint8 assignments)
+  off = align_up(off + (c.n_centroids <= QWM_MAX_RESIDENT_CENTROIDS ? (size_t)c.heads * kKmPrevTokens : 0), 256);
   L.q_img = off; off = align_up(off + quantize_image_bytes(c.heads, c.n_centroids), 1024);
   L.q_bfull = off; off = align_up(off + (size_t)c.heads * c.n_centroids * QWM_D * sizeof(float), 256);
   L.q_mfull = off; off = align_up(off + (size_t)c.heads * QWM_D * QWM_D * sizeof(float), 256);
@@ -153,6 +155,7 @@ qwm_status qwm_create(const qwm_config *cfg, qwm_ctx **out) {
   ctx->km_cnt = (int32_t *)(base + L.km_cnt);
   ctx->km_cent = (float *)(base + L.km_cent);
   ctx->km_img = (unsigned char *)(base + L.km_img);
+  ctx->km_prev = ctx->cfg.n_centroids <= QWM_MAX_RESIDENT_CENTROIDS ? (uint8_t *)(base + L.km_prev) : nullptr;
   ctx->q_img = (unsigned char *)(base + L.q_img);
   ctx->q_bfull = (float *)(base + L.q_bfull);
   ctx->q_mfull = (float *)(base + L.q_mfull);
@@ -214,8 +217,8 @@ qwm_status qwm_fit_centroids(qwm_ctx *ctx, const uint16_t *x, int64_t n, const u
   if (!aligned16(x) || !aligned16(cent) || (init && !aligned16(init))) return QWM_ERR_ALIGN;
   const int sms = ctx->num_sms < QWM_MAX_SMS ? ctx->num_sms : QWM_MAX_SMS;
   cudaError_t e = launch_kmeans(x, n, ctx->cfg.heads, ctx->cfg.n_centroids, init, ctx->cfg.kmeans_iters, cent,
-                                ctx->km_cent, ctx->km_sum, ctx->km_cnt, sms, ctx->status, ctx->km_img,
-                                (cudaStream_t)stream);
+                                ctx->km_cent, ctx->km_sum, ctx->km_cnt, sms, ctx->status, ctx->km_img, ctx->km_prev,
+                                kKmPrevTokens, (cudaStream_t)stream);
   return cuda_status(e);
 }
 

@@ -21,6 +21,13 @@
 // assignment matrix of each 64-token half-tile into one of three buffers over the codebook area, and
 // the MMA warp accumulates sums = onehot^T X in TMEM; the CTA adds them to its own slice of the
 // workspace and km_update_kernel reduces the slices in a fixed order.
+// Resident codebooks also keep every token's assignment in a workspace array between iterations:
+// from the second iteration on, phase 1 flags the 64-token half-tiles in which a token changed
+// cluster, phase 2 re-reads only the tiles holding one, its one-hot matrix carries +1 at a moved
+// token's new cluster and -1 at its old one, and the CTA adds the result (and the count changes) to
+// its slice, which therefore holds the sums of the current assignment; only the centroids a moved
+// token left or joined are written back.  After a warm start about 1% of the tokens move in the
+// second iteration and fewer than 0.1% from the sixth on.
 // The kernels that produce centroids (kmeans_init_kernel, km_update_kernel) also write the next
 // assignment's operands: each head's hi/lo bf16 blocks, 128-byte swizzled exactly as the MMA reads
 // them, and the squared norms ||mu_j||^2, so that the assignment kernel starts with one bulk copy
@@ -46,7 +53,7 @@ constexpr int kSlice = 128;      // centroids per streamed slice (WIDE)
 constexpr int kSliceBytes = 4 * kSlice * 128;  // hi and lo blocks of one slice
 
 struct KmSmem {  // offsets from a 1024-aligned base, for a codebook of C centroids
-  int bh, bl, x, norm, asg, cnt, cur, mem, total;
+  int bh, bl, x, norm, asg, cnt, cur, mem, old, flg, lst, total;
   __host__ __device__ KmSmem(int C, bool wide) {
     const int CB = wide ? kSlice : C;  // centroids held in shared memory at once
     bh = 0;                        // 2 blocks of [CB][64] bf16 (hi)
@@ -59,7 +66,10 @@ struct KmSmem {  // offsets from a 1024-aligned base, for a codebook of C centro
     cnt = asg + (wide ? 2 : 1) * kMaxTok;  // WIDE cluster sums: counts [C], cursors [C], members
     cur = cnt + (wide ? 4 * C : 0);
     mem = cur + (wide ? 4 * C : 0);
-    total = mem + (wide ? 2 * kMaxTok : 0);
+    old = mem + (wide ? 2 * kMaxTok : 0);  // resident: previous assignments of the super-chunk
+    flg = old + (wide ? 0 : kMaxTok);      // resident: per tile, bit h = half-tile h has a changed token
+    lst = flg + (wide ? 0 : 4 * (kMaxTok / TILE));  // resident: tiles whose sums phase 2 reads
+    total = lst + (wide ? 0 : 4 * (kMaxTok / TILE));
   }
 };
 
@@ -105,8 +115,10 @@ struct AssignParams {
   const float *norms;        // [H][C]
   float *part_sum;       // [H][G][C][D]
   int32_t *part_cnt;     // [H][G][C]
+  uint8_t *prev;         // resident codebooks: [H][n] assignments of the previous iteration, or NULL
   int64_t n;
   int C, G;
+  int delta;             // 1: update the CTA's sums with the tokens whose assignment changed
   int32_t *status;
 };
 
@@ -121,6 +133,8 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
   __shared__ uint64_t cb_full;  // operands and norms of the codebook
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
+  __shared__ int nl_sh;
+  __shared__ uint32_t touched[QWM_MAX_RESIDENT_CENTROIDS / 32];  // delta: centroids a moved token left or joined
   const int C = p.C;
   const int NSL = WIDE ? C / kSlice : 1;
   const KmSmem L(C, WIDE);
@@ -134,6 +148,10 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
   float *norm = (float *)(sm + L.norm);
   uint8_t *asg = sm + L.asg;
   uint16_t *asg16 = (uint16_t *)(sm + L.asg);  // WIDE
+  uint8_t *asg_old = sm + L.old;               // delta: the previous assignments
+  uint32_t *tflag = (uint32_t *)(sm + L.flg);
+  int32_t *tlist = (int32_t *)(sm + L.lst);
+  const bool delta = !WIDE && p.delta != 0;
   volatile int *abort_v = &abort_flag;
 
   if (tid == 0) {
@@ -177,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
   int64_t g2 = 0;      // tiles re-read by phase 2 (barrier phases)
   int n_sc = 0;        // super-chunks done (phase of p2_done)
   int n_cb = 0;        // operand loads done (phase of cb_full)
-  for (int64_t sc0 = tile0, first = 1; first || sc0 < tile1; sc0 += kMaxTok / TILE, first = 0) {
+  for (int64_t sc0 = tile0, first = 1; (first && !delta) || sc0 < tile1; sc0 += kMaxTok / TILE, first = 0) {
     const int64_t left = tile1 - sc0;
     const int nt = left <= 0 ? 0 : (left < kMaxTok / TILE ? (int)left : kMaxTok / TILE);
     // ---- operands of the codebook (resident: hi/lo blocks; WIDE: streamed per tile) and norms ----
@@ -192,6 +210,8 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
     }
     if (!tc::mbar_wait(&cb_full, (uint32_t)(n_cb & 1), kWaitNs)) *abort_v = 1;
     n_cb++;
+    if (delta)
+      for (int i = tid; i < kMaxTok / TILE; i += kThreads) tflag[i] = 0u;
     __syncthreads();
     if (*abort_v) break;
     // ---- phase 1: assignments of nt tiles ----
@@ -340,12 +360,33 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&t_empty[s]);
         asg[i * TILE + row] = (uint8_t)arg;
+        const int64_t tok = (sc0 + i) * TILE + row;
+        const bool tvalid = tok < p.n;
+        if (delta) {  // the token's previous assignment; a half-tile with a change is re-read in phase 2
+          const int old = tvalid ? (int)p.prev[(int64_t)h * p.n + tok] : arg;
+          asg_old[i * TILE + row] = (uint8_t)old;
+          const uint32_t moved = __ballot_sync(__activemask(), old != arg);
+          if (lane == 0 && moved) atomicOr(tflag + i, 1u << (sub >> 1));
+        }
+        if (p.prev && tvalid) p.prev[(int64_t)h * p.n + tok] = (uint8_t)arg;
       }
     }
     __syncwarp();  // idle lanes of the TMA and MMA warps wait for lane 0 here
     __syncthreads();
     if (*abort_v) break;
     g_tile += nt;
+    int nl = nt;  // tiles phase 2 re-reads: every tile, or (delta) those with a changed token
+    if (delta) {
+      if (tid == 0) {
+        int c = 0;
+        for (int i = 0; i < nt; i++)
+          if (tflag[i]) tlist[c++] = i;
+        nl_sh = c;
+      }
+      __syncthreads();
+      nl = nl_sh;
+      if (nl == 0) continue;  // no token of this super-chunk moved: its sums stand
+    }
     if (WIDE) {
       // ---- phase 2 (WIDE): stable counting sort of the assignments, then per-centroid sums ----
       int32_t *cnt = (int32_t *)(sm + L.cnt), *cur = (int32_t *)(sm + L.cur);
@@ -430,6 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
     };
     for (int e = tid; e < (int)(kOneHot * aBytes / 16u); e += kThreads) *(uint4 *)(sm + 16 * e) = make_uint4(0, 0, 0, 0);
     for (int j = tid; j < C; j += kThreads) cnts[j] = 0;
+    if (tid < QWM_MAX_RESIDENT_CENTROIDS / 32) touched[tid] = 0u;
     tc::fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
@@ -440,8 +482,9 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
     const int64_t u0 = 2 * g2;  // half-tiles before this super-chunk (barrier phases)
     if (warp == 0) {
       if (lane == 0) {  // TMA: token tiles
-        for (int i = 0; i < nt && !*abort_v; i++) {
-          const int64_t g = g2 + i;
+        for (int li = 0; li < nl && !*abort_v; li++) {
+          const int i = delta ? tlist[li] : li;
+          const int64_t g = g2 + li;
           const int s = (int)(g % nxs);
           if (g >= nxs && !tc::mbar_wait(&p2_empty[s], (uint32_t)(((g / nxs) - 1) & 1), kWaitNs)) {
             *abort_v = 1;
@@ -458,13 +501,13 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
       if (lane == 0) {  // MMA: sums += A^T X
         const uint32_t idesc = tc::idesc_bf16_f32(TILE, D) | (1u << 16);  // B (token rows) N-major
         const uint32_t sa = tc::smem_u32(sm);
-        for (int i = 0; i < nt && !*abort_v; i++) {
-          const int64_t g = g2 + i;
+        for (int li = 0; li < nl && !*abort_v; li++) {
+          const int64_t g = g2 + li;
           const int s = (int)(g % nxs);
           if (!tc::mbar_wait(&p2_full[s], (uint32_t)((g / nxs) & 1), kWaitNs)) { *abort_v = 1; break; }
           const uint32_t sx = sa + xstage(s);
           for (int hh = 0; hh < 2; hh++) {
-            const int64_t U = u0 + 2 * i + hh;
+            const int64_t U = u0 + 2 * li + hh;
             const int b = (int)(U % kOneHot);
             if (!tc::mbar_wait(&a_full[b], (uint32_t)((U / kOneHot) & 1), kWaitNs)) { *abort_v = 1; break; }
             tc::fence_after_sync();
@@ -474,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
                 const uint32_t ao = sa + (uint32_t)b * aBytes + (uint32_t)mb * TILE * 128u + 32u * kk;
                 const uint32_t bo = sx + 2048u * (4 * hh + kk);
                 tc::mma_ss(tmem + 128u * mb, tc::desc_sw128(ao), tc::desc_sw128_mn(bo, TILE * 128, 1024), idesc,
-                           (i > 0 || hh > 0 || kk > 0) ? 1u : 0u);
+                           (li > 0 || hh > 0 || kk > 0) ? 1u : 0u);
               }
             }
             tc::mma_commit(&a_empty[b]);
@@ -487,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
     } else if (warp < 2 + 2 * kOneHot) {  // warp pair b builds the one-hot matrices of buffer b; thread = token
       const int b = (warp - 2) >> 1, lt = ((warp - 2) & 1) * 32 + lane;
       int u = (int)(((b - u0) % kOneHot + kOneHot) % kOneHot);  // this super-chunk's first half-tile in buffer b
-      for (; u < 2 * nt; u += kOneHot) {
+      for (; u < 2 * nl; u += kOneHot) {
         const int64_t U = u0 + u;
         const bool ok = U < kOneHot || tc::mbar_wait(&a_empty[b], (uint32_t)(((U / kOneHot) - 1) & 1), kWaitNs);
         if (__any_sync(0xffffffffu, !ok || *abort_v != 0)) {  // warp-uniform exit
@@ -496,20 +539,42 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
         }
         unsigned char *abuf = sm + (uint32_t)b * aBytes;
         const int bt = 64 * (u & 1) + lt;                 // token within its tile
-        if (u >= kOneHot) {  // clear this buffer's ones of its previous half-tile (same super-chunk)
+        if (u >= kOneHot) {  // clear this buffer's entries of its previous half-tile (same super-chunk)
           const int up = u - kOneHot;
-          const int64_t tokp = (sc0 + (up >> 1)) * TILE;
+          const int tp = delta ? tlist[up >> 1] : (up >> 1);
+          const int64_t tokp = (sc0 + tp) * TILE;
           const int rowsp = (int)((p.n - tokp) < TILE ? (p.n - tokp) : TILE);
           const int btp = 64 * (up & 1) + lt;
-          if (btp < rowsp) *(uint16_t *)(abuf + onehot_off(asg[(up >> 1) * TILE + btp], lt)) = 0;
+          if (btp < rowsp) {
+            const int jn = asg[tp * TILE + btp];
+            if (!delta) {
+              *(uint16_t *)(abuf + onehot_off(jn, lt)) = 0;
+            } else if (asg_old[tp * TILE + btp] != jn) {
+              *(uint16_t *)(abuf + onehot_off(jn, lt)) = 0;
+              *(uint16_t *)(abuf + onehot_off(asg_old[tp * TILE + btp], lt)) = 0;
+            }
+          }
         }
-        const int64_t tok0 = (sc0 + (u >> 1)) * TILE;
+        const int ti = delta ? tlist[u >> 1] : (u >> 1);
+        const int64_t tok0 = (sc0 + ti) * TILE;
         const int rows = (int)((p.n - tok0) < TILE ? (p.n - tok0) : TILE);
         const bool valid = bt < rows;
-        const int j = valid ? asg[(u >> 1) * TILE + bt] : -1 - lane;
-        if (valid) *(uint16_t *)(abuf + onehot_off(j, lt)) = 0x3F80u;  // bf16 1.0
-        const uint32_t peers = __match_any_sync(0xffffffffu, j);  // one count update per cluster
-        if (valid && (peers & ((1u << lane) - 1u)) == 0) atomicAdd(cnts + j, __popc(peers));
+        if (!delta) {  // +1 at the token's cluster
+          const int j = valid ? asg[ti * TILE + bt] : -1 - lane;
+          if (valid) *(uint16_t *)(abuf + onehot_off(j, lt)) = 0x3F80u;  // bf16 1.0
+          const uint32_t peers = __match_any_sync(0xffffffffu, j);  // one count update per cluster
+          if (valid && (peers & ((1u << lane) - 1u)) == 0) atomicAdd(cnts + j, __popc(peers));
+        } else if (valid) {  // a moved token: +1 at its new cluster, -1 at its old one
+          const int jn = asg[ti * TILE + bt], jo = asg_old[ti * TILE + bt];
+          if (jn != jo) {
+            *(uint16_t *)(abuf + onehot_off(jn, lt)) = 0x3F80u;  // bf16 1.0
+            *(uint16_t *)(abuf + onehot_off(jo, lt)) = 0xBF80u;  // bf16 -1.0
+            atomicAdd(cnts + jn, 1);
+            atomicAdd(cnts + jo, -1);
+            atomicOr(touched + (jn >> 5), 1u << (jn & 31));
+            atomicOr(touched + (jo >> 5), 1u << (jo & 31));
+          }
+        }
         tc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&a_full[b]);
@@ -518,29 +583,31 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
     // the idle lanes of the TMA and MMA warps wait here for lane 0, not in the spin below: a lane
     // polling an mbarrier holds up the diverged lane 0 of its own warp
     __syncwarp();
-    g2 += nt;
+    g2 += nl;
     if (!*abort_v && !tc::mbar_wait(&p2_done, (uint32_t)(n_sc & 1), kWaitNs)) *abort_v = 1;
     n_sc++;
     tc::fence_after_sync();
     __syncthreads();
     if (*abort_v) break;
     // sums from TMEM (warps 2-9: lane quarter warp % 4, centroid block (warp - 2) / 4) -> the workspace
+    // (delta: only the centroids a moved token left or joined change)
     if (warp >= 2) {
       const int mb = (warp - 2) >> 2, sub = warp & 3;
       const int j = 128 * mb + 32 * sub + lane;
-      if (mb < Mb) {
+      const bool mine = !delta || ((touched[j >> 5] >> (j & 31)) & 1u);
+      if (mb < Mb && __any_sync(0xffffffffu, mine)) {
         uint32_t r[32];
         for (int c0 = 0; c0 < D; c0 += 32) {
           tc::tmem_ld32(tmem + ((uint32_t)(32 * sub) << 16) + 128u * mb + c0, r);
           tc::tmem_ld_wait();
-          if (j < C) {
+          if (j < C && mine) {
             float4 *dst = (float4 *)(psum + (int64_t)j * D + c0);
 #pragma unroll
             for (int v = 0; v < 8; v++) {
               float4 a = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
                                      __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
               if (nt == 0) a = make_float4(0.f, 0.f, 0.f, 0.f);  // no tiles: no MMA wrote TMEM
-              if (!first) {
+              if (!first || delta) {
                 const float4 o = dst[v];
                 a.x += o.x; a.y += o.y; a.z += o.z; a.w += o.w;
               }
@@ -550,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
         }
       }
     }
-    for (int j = tid; j < C; j += kThreads) pcnt[j] = first ? cnts[j] : pcnt[j] + cnts[j];
+    for (int j = tid; j < C; j += kThreads) pcnt[j] = (first && !delta) ? cnts[j] : pcnt[j] + cnts[j];
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
@@ -602,7 +669,7 @@ size_t kmeans_image_bytes(int H, int C) { return (size_t)H * C * 512 + (size_t)H
 
 cudaError_t launch_kmeans(const uint16_t *x, int64_t n, int H, int C, const uint16_t *init, int iters,
                           uint16_t *cent, float *km_cent, float *km_sum, int32_t *km_cnt, int num_sms,
-                          int32_t *status, unsigned char *img, cudaStream_t st) {
+                          int32_t *status, unsigned char *img, uint8_t *prev, int64_t prev_cap, cudaStream_t st) {
   TensorMap128 tmap;
   if (!make_tmap_rows128_bf16(&tmap, x, (uint64_t)H * n, TILE)) return cudaErrorInvalidValue;
   float *norms = (float *)(img + (size_t)H * C * 512);
@@ -615,8 +682,12 @@ cudaError_t launch_kmeans(const uint16_t *x, int64_t n, int H, int C, const uint
   e = wide ? cudaFuncSetAttribute(km_assign_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
            : cudaFuncSetAttribute(km_assign_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  AssignParams p{x, img, norms, km_sum, km_cnt, n, C, G, status};
+  // Resident codebooks keep every token's assignment between iterations (when the chunk fits the
+  // buffer): from the second iteration on, each CTA adds to its sums only the tokens that moved.
+  uint8_t *keep = (!wide && prev && n <= prev_cap) ? prev : nullptr;
+  AssignParams p{x, img, norms, km_sum, km_cnt, keep, n, C, G, 0, status};
   for (int it = 0; it < iters; it++) {
+    p.delta = (keep && it > 0) ? 1 : 0;
     if (wide) km_assign_kernel<true><<<dim3(G, H), kThreads, smem, st>>>(tmap, p);
     else km_assign_kernel<false><<<dim3(G, H), kThreads, smem, st>>>(tmap, p);
     km_update_kernel<<<dim3(C, H), D, 0, st>>>(C, G, km_cent, km_sum, km_cnt, it == iters - 1 ? cent : nullptr, img,

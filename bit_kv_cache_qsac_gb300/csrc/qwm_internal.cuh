@@ -24,6 +24,7 @@ struct qwm_ctx {
   int32_t *status;       // [1] first device-side error (qwm_status), 0 if none
   float *stats_part;     // [splits][H][d][d] per-split partial sums of q q^T
   int stats_splits;
+  uint8_t *km_prev;      // [H][kKmPrevTokens] k-means assignments between iterations (resident codebooks)
   float *km_sum;         // [H][G][C][d] k-means per-CTA cluster sums (G CTAs per head)
   int32_t *km_cnt;       // [H][G][C] k-means per-CTA cluster counts
   float *km_cent;        // [H][C][d] fp32 centroids during the iterations
@@ -106,11 +107,14 @@ cudaError_t launch_stats_finish(const float *part, int splits, int64_t nq, int H
 cudaError_t launch_eig(const float *S, int64_t *n, int64_t nq, int H, int rank, float *eigvals, uint16_t *u_r,
                        int32_t *status, cudaStream_t st);
 #define QWM_MAX_SMS 192  // workspace sizing bound on the SM count
+constexpr int64_t kKmPrevTokens = 65536;  // tokens per head whose k-means assignments the workspace keeps
 int kmeans_ctas_per_head(int H, int num_sms);
 size_t kmeans_image_bytes(int H, int C);
+// kmeans `prev`: [H][prev_cap] bytes for the assignments kept between Lloyd iterations (resident
+// codebooks; chunks longer than prev_cap tokens recompute every iteration's sums in full).
 cudaError_t launch_kmeans(const uint16_t *x, int64_t n, int H, int C, const uint16_t *init, int iters,
                           uint16_t *cent, float *km_cent, float *km_sum, int32_t *km_cnt, int num_sms,
-                          int32_t *status, unsigned char *img, cudaStream_t st);
+                          int32_t *status, unsigned char *img, uint8_t *prev, int64_t prev_cap, cudaStream_t st);
 size_t quantize_image_bytes(int H, int C);
 cudaError_t launch_quantize(const qwm_config &cfg, const uint16_t *k, const uint16_t *v, int64_t n,
                             const float *w, const float *S, const int64_t *n_seen, float *Mq, float *Bq,
