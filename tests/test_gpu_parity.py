@@ -497,6 +497,26 @@ def test_attend_psac_ranks(q, rank, C, n):
         assert _attn_err(out[h].cpu().numpy().astype(np.float64), ref) <= 2e-2
 
 
+@pytest.mark.parametrize("rank,C,n", [(5, 64, 300), (7, 256, 513), (11, 128, 777), (12, 128, 777),
+                                       (16, 256, 1024)])
+def test_dequantize_psac_ranks(q, rank, C, n):
+    """The Key decoder's PSAC term on warp-level MMAs at odd and even ranks on both sides of 8: ranks up
+    to 8 take the K = 8 products, above 8 the K = 16 ones; an odd rank reads the basis in 16-bit
+    halves.  Every element within one bf16 step of the oracle's decoder (plus the cancellation slack)."""
+    ctx, ch = _packed(q, n=n, C=C, rank=rank)
+    H = 2
+    kh = torch.empty(H, n, D, dtype=torch.bfloat16, device="cuda"); vh = torch.empty_like(kh)
+    q.qwm_dequantize(ctx, ch, kh, vh)
+    assert q.qwm_sync_status(ctx) == 0
+    for h in range(H):
+        c = chunk_head(ch, h)
+        _, _, k64, v64 = oracle.dequantize_head(c)
+        for got, ref, key in ((kh[h], k64, True), (vh[h], v64, False)):
+            g = (to_u16(got).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+            slack = 2.0 ** -20 * decode_term_magnitude(c, key)
+            assert (bf16_ulp_close(to_u16(got), ref) | (np.abs(g - ref) <= slack)).all()
+
+
 def test_attend_growing_logits(q):
     """A hand-built chunk whose logits rise steadily along the keys (about 10 log2 units per tile),
     so the softmax raises its running maximum many times, inside tiles and across them (rescaling
