@@ -169,17 +169,22 @@ def gen_layer(layer: int):
     return ks, vs, qs
 
 
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch, from ncu captures of the
-# kernel sources whose SHA-256 is given (the traffic is reported as null for any other source):
-# attention per launch; packing per step (the Key and the Value pass).  The packing's 720p figure is
-# its 480p capture scaled by the tokens processed (10,800 / 4,680): each pass reads its input once
-# (its outputs stay in L2 when it ends), so its traffic grows in proportion.
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per step of each stage's kernels, from ncu
+# captures of the kernel sources whose SHA-256 is given (the traffic is reported as null for any
+# other source): the attention launch; the packing's Key and Value passes with the stored-codebook
+# kernel; the fits' init, assignment and update launches (20 of each); the statistics kernels.  720p:
+# one capture of a whole timed step (all 50 launches, one pass each); 480p: the attention and the two
+# packing passes of one step.
 TRAFFIC = {
     "attend.cu": {"sha256": "88b6a5df901f45795f665fce436100c791bdb22dc863825c58f44bb5b53079b2",
-                  "480p": 228292608 + 67828224},
+                  "480p": 228292608 + 67828224, "720p": 477642496 + 189113344},
     "quantize.cu": {"sha256": "e84e7a59bd241f42592420dd3afd237f9448e979a2bcc2ad1e6ad52abc89c82d",
                     "480p": (50848000 + 270848) + (50659840 + 256),
-                    "720p": round(((50848000 + 270848) + (50659840 + 256)) * 10800 / 4680)},
+                    "720p": (114320896 + 6914304) + (114473216 + 5387776) + 5248256},
+    "kmeans.cu": {"sha256": "138d0617038ae1d6f4dce3fdfdd3dd3d2d5fcbb419c35ed45fa2beb3bdc4e521",
+                  "720p": 5256448 + (2707933440 + 7023872) + (422108416 + 31232)},
+    "stats_eig.cu": {"sha256": "7c25a04ea010919b3b31a5ee19d2ad368ac47731e5b9026db35675c949bb223c",
+                     "720p": (110627328 + 57856) + 13115904 + 2694656},
 }
 
 
@@ -408,7 +413,7 @@ def run_ours(args, rank, world, device):
         "roofline_fit": {"bound": "hbm", "kernel": "fit_k_v (kmeans_init, km_assign, km_update)",
                          "achieved": fit_gbs, "peak": peak_bw, "unit": "GB/s",
                          "frac": fit_gbs / peak_bw if peak_bw else None, "peak_source": f"hbm copy, {peak_kind}",
-                         "traffic": None,
+                         "traffic": kernel_traffic("kmeans.cu", W.name),
                          "algorithmic": f"10 iterations x 2 tensors x {H * N_CHUNK} token-heads x {D * 2} B read "
                                         f"= {fit_bytes} B; {fit_flops:.3e} distance flops "
                                         f"({fit_flops / (peak_tf_dense or 1) / 1e9:.3f} ms at the dense peak, "
@@ -416,7 +421,8 @@ def run_ours(args, rank, world, device):
         "roofline_stats_eig": {"bound": "hbm", "kernel": "stats_partial + stats_finish + eig (alone)",
                                "achieved": stats_gbs, "peak": peak_bw, "unit": "GB/s",
                                "frac": stats_gbs / peak_bw if peak_bw else None,
-                               "peak_source": f"hbm copy, {peak_kind}", "traffic": None,
+                               "peak_source": f"hbm copy, {peak_kind}",
+                               "traffic": kernel_traffic("stats_eig.cu", W.name),
                                "algorithmic": f"{H * NQ} Queries x {D * 2} B read = {stats_bytes} B; the "
                                               "eigen-solve (one block per head) is latency-bound"},
         "e2e": {"value": job_throughput(units, world, e2e_ms), "unit": "KV token-heads/s",
