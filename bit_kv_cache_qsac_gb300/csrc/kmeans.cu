@@ -638,25 +638,47 @@ __global__ void __launch_bounds__(kThreads, 1) km_assign_kernel(const __grid_con
 }
 
 // New centroid = (sum of the G partial sums, in order) / count; empty clusters keep theirs.  Also
-// writes the next assignment's operands (write_operand).
+// writes the next assignment's operands (write_operand).  One block takes kUpd centroids of a head
+// (thread = channel), with all their partial sums and counts loaded before the first is used.
+constexpr int kUpd = 4;
 __global__ void __launch_bounds__(D) km_update_kernel(int C, int G, float *__restrict__ cent,
                                                       const float *__restrict__ part_sum,
                                                       const int32_t *__restrict__ part_cnt,
                                                       uint16_t *__restrict__ out_bf16, unsigned char *__restrict__ img,
                                                       float *__restrict__ norms) {
-  const int h = blockIdx.y, j = blockIdx.x, c = threadIdx.x;
-  float s = 0.f;
-  int cnt = 0;
-  for (int g = 0; g < G; g++) {
-    s += part_sum[(((int64_t)h * G + g) * C + j) * D + c];
-    cnt += part_cnt[((int64_t)h * G + g) * C + j];
+  const int h = blockIdx.y, j0 = blockIdx.x * kUpd, c = threadIdx.x;
+  float s[kUpd], old[kUpd];
+  int cnt[kUpd];
+#pragma unroll
+  for (int u = 0; u < kUpd; u++) {
+    s[u] = 0.f;
+    cnt[u] = 0;
+    old[u] = j0 + u < C ? cent[((int64_t)h * C + j0 + u) * D + c] : 0.f;
   }
-  const int64_t e = ((int64_t)h * C + j) * D + c;
-  float mu = cent[e];
-  if (cnt > 0) mu = __fdiv_rn(s, (float)cnt);  // counts are exact in fp32 (< 2^24)
-  cent[e] = mu;
-  if (out_bf16) out_bf16[e] = f32_to_bf16_rn(mu);
-  else write_operand(img + (int64_t)h * C * 512, norms + (int64_t)h * C, C, j, c, mu);
+  for (int g = 0; g < G; g++) {
+#pragma unroll
+    for (int u = 0; u < kUpd; u++) {
+      if (j0 + u < C) {
+        s[u] += part_sum[(((int64_t)h * G + g) * C + j0 + u) * D + c];
+        cnt[u] += part_cnt[((int64_t)h * G + g) * C + j0 + u];
+      }
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kUpd; u++) {
+    const int j = j0 + u;
+    if (j >= C) break;  // block-uniform
+    const int64_t e = ((int64_t)h * C + j) * D + c;
+    float mu = old[u];
+    if (cnt[u] > 0) mu = __fdiv_rn(s[u], (float)cnt[u]);  // counts are exact in fp32 (< 2^24)
+    cent[e] = mu;
+    if (out_bf16) {
+      out_bf16[e] = f32_to_bf16_rn(mu);
+    } else {
+      write_operand(img + (int64_t)h * C * 512, norms + (int64_t)h * C, C, j, c, mu);
+      __syncthreads();  // write_operand's norm buffer is read by thread 0 before the next centroid reuses it
+    }
+  }
 }
 
 }  // namespace
@@ -690,8 +712,8 @@ cudaError_t launch_kmeans(const uint16_t *x, int64_t n, int H, int C, const uint
     p.delta = (keep && it > 0) ? 1 : 0;
     if (wide) km_assign_kernel<true><<<dim3(G, H), kThreads, smem, st>>>(tmap, p);
     else km_assign_kernel<false><<<dim3(G, H), kThreads, smem, st>>>(tmap, p);
-    km_update_kernel<<<dim3(C, H), D, 0, st>>>(C, G, km_cent, km_sum, km_cnt, it == iters - 1 ? cent : nullptr, img,
-                                                norms);
+    km_update_kernel<<<dim3((C + kUpd - 1) / kUpd, H), D, 0, st>>>(C, G, km_cent, km_sum, km_cnt,
+                                                                    it == iters - 1 ? cent : nullptr, img, norms);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
