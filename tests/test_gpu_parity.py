@@ -537,6 +537,8 @@ def test_attend_growing_logits(q):
         getattr(ch, name).zero_()
     ch.k_idx.copy_(torch.from_numpy(idx.copy())); ch.v_idx.copy_(torch.from_numpy(idx.copy()))
     ch.cent_k.copy_(torch.from_numpy(ck).to(torch.bfloat16)); ch.cent_v.copy_(torch.from_numpy(cv).to(torch.bfloat16))
+    # the stored codebooks the attention reads (integers: exact in fp16)
+    ch.cent_k16.copy_(torch.from_numpy(ck).to(torch.float16)); ch.cent_v16.copy_(torch.from_numpy(cv).to(torch.float16))
     qf = 0.25 * u[None, None, :] + 0.125 * rng.integers(-2, 3, size=(H, nq, D))
     qa = to_u16(torch.from_numpy(qf).to(torch.bfloat16))
     out = torch.empty(H, nq, D, dtype=torch.float32, device="cuda")
