@@ -177,14 +177,14 @@ def gen_layer(layer: int):
 # packing passes of one step.
 TRAFFIC = {
     "attend.cu": {"sha256": "88b6a5df901f45795f665fce436100c791bdb22dc863825c58f44bb5b53079b2",
-                  "480p": 228292608 + 67828224, "720p": 477642496 + 189113344},
+                  "480p": 228292608 + 67828224, "720p": 476583424 + 189769472},
     "quantize.cu": {"sha256": "e84e7a59bd241f42592420dd3afd237f9448e979a2bcc2ad1e6ad52abc89c82d",
                     "480p": (50848000 + 270848) + (50659840 + 256),
-                    "720p": (114320896 + 6914304) + (114473216 + 5387776) + 5248256},
-    "kmeans.cu": {"sha256": "138d0617038ae1d6f4dce3fdfdd3dd3d2d5fcbb419c35ed45fa2beb3bdc4e521",
-                  "720p": 5256448 + (2707933440 + 7023872) + (422108416 + 31232)},
+                    "720p": (114323968 + 6860544) + (114517504 + 6001152) + 5248000},
+    "kmeans.cu": {"sha256": "afd8b926ed71beda0ee83b01b6b1f3ba6c1a22ea3a25fa4f43f2b1ae805eacae",
+                  "720p": 5256704 + (2707316992 + 5027072) + (422241024 + 2048)},
     "stats_eig.cu": {"sha256": "7c25a04ea010919b3b31a5ee19d2ad368ac47731e5b9026db35675c949bb223c",
-                     "720p": (110627328 + 57856) + 13115904 + 2694656},
+                     "720p": (110614528 + 75520) + 13122304 + 2692864},
 }
 
 
