@@ -171,6 +171,21 @@ WIDE_W = synth.Workload("ablation-2-heads", 4, heads=2, frames=6, hs=30, ws=52, 
                         nq_stats=256, nq_attend=256, n_centroids=1024)
 
 
+def test_kmeans_objective_past_the_kept_assignments(q):
+    """A chunk longer than the 65,536 tokens per head whose assignments the context keeps between Lloyd
+    iterations: every iteration then recomputes its cluster sums in full (152 CTAs on one head)."""
+    n, C = 70000, 64
+    x = np.ascontiguousarray(synth.keys(synth.P720, 0, 0, n)[:1])
+    ctx = q.Context(heads=1, n_centroids=C, top_m=4)
+    cent = torch.empty(1, C, D, dtype=torch.bfloat16, device="cuda")
+    q.qwm_fit_centroids(ctx, _bf(x), n, None, cent)
+    assert q.qwm_sync_status(ctx) == 0
+    ref, _, _, _ = oracle.kmeans(x[0], C, None, 10)
+    j_gpu = oracle.kmeans_objective(x[0], to_u16(cent[0]))
+    j_ref = oracle.kmeans_objective(x[0], ref)
+    assert abs(j_gpu - j_ref) <= 1e-3 * j_ref, (j_gpu, j_ref)
+
+
 def test_kmeans_objective_1024_centroids(q):
     H, n, C = 2, 2600, 1024
     x = synth.keys(WIDE_W)[:, :n]
