@@ -177,10 +177,10 @@ __device__ __forceinline__ int chunk_of_cta(const DqParams &p) {
 }
 
 // Values, or Keys without any PSAC term in the call: 16 threads per token (8 channels each), 16
-// tokens per pass; the centroid rows of 8 passes are gathered before they are used (the compiler has
-// to assume the output may alias the codebook, so the loads cannot move past the stores by themselves).
+// tokens per pass; the centroid rows of 8 passes are gathered before they are used.  Four CTAs per
+// SM (64 registers); the Key kernel below, with its MMA fragments, keeps three.
 template <bool VAL, bool IDX16, bool COMPACT>
-__global__ void __launch_bounds__(kThreads, 3) dequant_kernel(const __grid_constant__ DqParams p) {
+__global__ void __launch_bounds__(kThreads, 4) dequant_kernel(const __grid_constant__ DqParams p) {
   __shared__ DqStage st;
   const int h = blockIdx.y, tid = threadIdx.x;
   const DqChunk &c = p.ch[chunk_of_cta(p)];
