@@ -7,9 +7,9 @@
 // A bandwidth kernel: per token-head it reads about 50 bytes of packed data (plus a codebook row that
 // stays in L2) and writes 256 bytes of bf16, so it is bound by the HBM write stream.  One CTA takes
 // 256 tokens of one chunk for one head; the token metadata is staged in shared memory first (one
-// coalesced pass, thread = token), and every centroid gather of a thread is issued before its first
-// store (the compiler has to assume the output may alias the codebook, so it cannot move the loads
-// past the stores by itself).
+// coalesced pass, thread = token), and each centroid gather is issued ahead of the stores that come
+// before its use (the compiler has to assume the output may alias the codebook, so it cannot move
+// the loads past the stores by itself).
 // Values (and Keys without PSAC): 16 threads per token, 8 channels each, one 16-byte store per
 // token.  Keys with PSAC: the correction sum_k c_k U_r[:, k] of 16 tokens x 128 channels is one
 // warp's set of mma.sync m16n8k8 (rank <= 8) or m16n8k16 products: bf16 operands (the int8
@@ -178,7 +178,7 @@ __device__ __forceinline__ int chunk_of_cta(const DqParams &p) {
 
 // Values, or Keys without any PSAC term in the call: 16 threads per token (8 channels each), 16
 // tokens per pass; the centroid rows of 8 passes are gathered before they are used.  Four CTAs per
-// SM (64 registers); the Key kernel below, with its MMA fragments, keeps three.
+// SM (64 registers), as the Key kernel below.
 template <bool VAL, bool IDX16, bool COMPACT>
 __global__ void __launch_bounds__(kThreads, 4) dequant_kernel(const __grid_constant__ DqParams p) {
   __shared__ DqStage st;
@@ -244,7 +244,7 @@ __device__ __forceinline__ uint32_t coef_pair(const uint4 cw, int t, int kb) {
 // 32 i + 8 (j / 2) + 2 a + j % 2, so the accumulator pair (a, 2 t + e) of the fragment layout is the
 // thread's channel 32 i + 8 t + 2 a + e.
 template <int RU, bool IDX16, bool COMPACT>
-__global__ void __launch_bounds__(kThreads, 3) dequant_key_kernel(const __grid_constant__ DqParams p) {
+__global__ void __launch_bounds__(kThreads, 4) dequant_key_kernel(const __grid_constant__ DqParams p) {
   constexpr int KS = RU > 8 ? 16 : 8, KB = KS / 8;
   __shared__ DqStage st;
   const int h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
@@ -277,14 +277,9 @@ __global__ void __launch_bounds__(kThreads, 3) dequant_key_kernel(const __grid_c
 #pragma unroll 1
   for (int wt = warp; 16 * wt < nt; wt += kThreads / 32) {
     const int r0 = 16 * wt + g, r1 = r0 + 8;
-    // the two tokens' centroid chunks, all gathered before the first store
-    uint4 mu0[4], mu1[4];
+    // the two tokens' centroid chunks, gathered one run of 8 channels ahead of the stores
     const uint16_t *row0 = cent + (int)st.idx[r0] * D, *row1 = cent + (int)st.idx[r1] * D;
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-      mu0[i] = *(const uint4 *)(row0 + 32 * i);
-      mu1[i] = *(const uint4 *)(row1 + 32 * i);
-    }
+    uint4 mu0c = *(const uint4 *)row0, mu1c = *(const uint4 *)row1;
     const uint4 cA = st.c[r0], cB = st.c[r1];
     uint32_t af[KS / 4];
     af[0] = coef_pair(cA, t4, 0);
@@ -297,6 +292,11 @@ __global__ void __launch_bounds__(kThreads, 3) dequant_key_kernel(const __grid_c
     const float scA = st.sc[r0], scB = st.sc[r1];
 #pragma unroll
     for (int i = 0; i < 4; i++) {
+      uint4 mu0n = mu0c, mu1n = mu1c;
+      if (i < 3) {  // the next run's chunks, loaded before this run's stores
+        mu0n = *(const uint4 *)(row0 + 32 * (i + 1));
+        mu1n = *(const uint4 *)(row1 + 32 * (i + 1));
+      }
       float acc[4][4];
 #pragma unroll
       for (int a = 0; a < 4; a++) {
@@ -318,12 +318,14 @@ __global__ void __launch_bounds__(kThreads, 3) dequant_key_kernel(const __grid_c
       }
       if (r0 < nt)
         *(uint4 *)(out + (int64_t)r0 * D + 32 * i) =
-            decode8<true>(mu0[i], bA, f16_to_f32((uint16_t)(sA >> (16 * gi))), f16_to_f32((uint16_t)(mA >> (16 * gi))),
+            decode8<true>(mu0c, bA, f16_to_f32((uint16_t)(sA >> (16 * gi))), f16_to_f32((uint16_t)(mA >> (16 * gi))),
                           scA, cr0);
       if (r1 < nt)
         *(uint4 *)(out + (int64_t)r1 * D + 32 * i) =
-            decode8<true>(mu1[i], bB, f16_to_f32((uint16_t)(sB >> (16 * gi))), f16_to_f32((uint16_t)(mB >> (16 * gi))),
+            decode8<true>(mu1c, bB, f16_to_f32((uint16_t)(sB >> (16 * gi))), f16_to_f32((uint16_t)(mB >> (16 * gi))),
                           scB, cr1);
+      mu0c = mu0n;
+      mu1c = mu1n;
     }
   }
 }
