@@ -60,6 +60,7 @@ constexpr uint64_t kWaitNs = 1000000000ull;
 constexpr float kRel = 1.0f / 32768.0f;    // 2^-15
 constexpr float kRelN = 1.0f / 131072.0f;  // 2^-17
 constexpr int kSlice = 128;                // centroids per streamed slice (WIDE)
+constexpr float kRint = 8388608.0f;        // 2^23: x + 2^23 - 2^23 = rint(x) for 0 <= x < 2^22
 
 struct QSmem {
   int bh, bl, bn, an, x, msk, wv, U, ef, total;
@@ -114,6 +115,15 @@ __device__ __forceinline__ void bf16x8(const uint4 v, float (&f)[8]) {
     f[2 * u + 1] = __uint_as_float(w[u] & 0xFFFF0000u);
   }
 }
+
+// Eight bf16 values (channels 2u, 2u + 1 in word u) as four fp32 pairs {channel 2u, channel 2u + 1}
+// for the packed f32x2 instructions.
+__device__ __forceinline__ void bf16x8_pairs(const uint4 v, uint64_t (&f)[4]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int u = 0; u < 4; u++) f[u] = ((uint64_t)(w[u] & 0xFFFF0000u) << 32) | (uint64_t)(w[u] << 16);
+}
+__device__ __forceinline__ uint64_t u2(uint32_t lo, uint32_t hi) { return ((uint64_t)hi << 32) | (uint64_t)lo; }
 
 // byte offset of (row, column k) in a [rows][16] bf16 K-major operand without swizzle
 __host__ __device__ constexpr uint32_t noswz16(uint32_t row, uint32_t k) {
@@ -620,18 +630,18 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
 #pragma unroll
           for (int cc = 0; cc < 8; cc++) {
             const int ci = 8 * gi + cc;
-            float f[8];
-            bf16x8(tc::lds128(xts + gi * TILE * 128 + tc::sw128_offset(row, 8 * cc)), f);
+            uint64_t f2[4];
+            bf16x8_pairs(tc::lds128(xts + gi * TILE * 128 + tc::sw128_offset(row, 8 * cc)), f2);
 #pragma unroll
             for (int k = 0; k < KM; k++) {
               if (k < cnt) {
-                float mu[8];
-                bf16x8(*(const uint4 *)(cent + (int64_t)cj[k] * D + 8 * ci), mu);
+                uint64_t m2[4];
+                bf16x8_pairs(*(const uint4 *)(cent + (int64_t)cj[k] * D + 8 * ci), m2);
 #pragma unroll
-                for (int u = 0; u < 8; u++) {
-                  const float rr = __fsub_rn(f[u], mu[u]);
-                  mnv[k][gi] = fminf(mnv[k][gi], rr);
-                  mxv[k][gi] = fmaxf(mxv[k][gi], rr);
+                for (int u = 0; u < 4; u++) {  // two channels per packed subtraction
+                  const uint64_t rr = tc::sub2(f2[u], m2[u]);
+                  mnv[k][gi] = tc::min3(mnv[k][gi], tc::f2lo(rr), tc::f2hi(rr));
+                  mxv[k][gi] = tc::max3(mxv[k][gi], tc::f2lo(rr), tc::f2hi(rr));
                 }
               }
             }
@@ -744,9 +754,9 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
       }
       if (valid) {
         uint32_t packed[8];
-        float Cv[RMAX];
+        uint64_t Cv2[RMAX / 2];  // the PSAC coefficients as fp32 pairs {k, k + 1}
 #pragma unroll
-        for (int k = 0; k < RMAX; k++) Cv[k] = 0.f;
+        for (int k = 0; k < RMAX / 2; k++) Cv2[k] = 0ull;
 #pragma unroll
         for (int gi = 0; gi < 2; gi++) {
         uint4 mv[8];  // the group's half of the centroid row, loaded at once (one L2 latency per group)
@@ -755,28 +765,54 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
 #pragma unroll
         for (int cc = 0; cc < 8; cc++) {
           const int ci = 8 * gi + cc;
-          float f[8], mu[8];
-          bf16x8(tc::lds128(xts + gi * TILE * 128 + tc::sw128_offset(row, 8 * cc)), f);
-          bf16x8(mv[cc], mu);
+          uint64_t f2[4], m2[4];
+          bf16x8_pairs(tc::lds128(xts + gi * TILE * 128 + tc::sw128_offset(row, 8 * cc)), f2);
+          bf16x8_pairs(mv[cc], m2);
           const bool g1 = gi == 1;
           const float mm = g1 ? m1 : m0, ss = g1 ? s1 : s0, ii = g1 ? i1 : i0, zz = g1 ? z1f : z0f;
+          const uint64_t mm2 = tc::f2(mm, mm), ss2 = tc::f2(ss, ss), ii2 = tc::f2(ii, ii);
+          const uint64_t mg2 = tc::f2(kRint, kRint);
           uint32_t bits = 0;
 #pragma unroll
-          for (int u = 0; u < 8; u++) {
-            const float rr = __fsub_rn(f[u], mu[u]);
-            uint32_t q;
+          for (int u = 0; u < 4; u++) {  // channels 8 ci + 2u, 8 ci + 2u + 1 as one fp32 pair
+            const uint64_t rr2 = tc::sub2(f2[u], m2[u]);
+            uint32_t q0, q1;
+            uint64_t qf2;
             if (p.compact) {
-              float qf = ss > 0.f ? rintf(__fadd_rn(__fmul_rn(rr, ii), zz)) : 0.f;
-              q = (uint32_t)fminf(fmaxf(qf, 0.f), 3.f);
+              const float r0 = tc::f2lo(rr2), r1 = tc::f2hi(rr2);
+              const float a0 = ss > 0.f ? rintf(__fadd_rn(__fmul_rn(r0, ii), zz)) : 0.f;
+              const float a1 = ss > 0.f ? rintf(__fadd_rn(__fmul_rn(r1, ii), zz)) : 0.f;
+              q0 = (uint32_t)fminf(fmaxf(a0, 0.f), 3.f);
+              q1 = (uint32_t)fminf(fmaxf(a1, 0.f), 3.f);
+              qf2 = tc::f2((float)q0, (float)q1);
             } else {
-              q = int2_code(rr, mm, ss, ii);
+              // q = rint((r - m) * (1/s)): the rounded product lies in [0, 3] up to rounding (m <= r
+              // and s >= (max r - m) / 3), so adding 2^23 rounds it to the integer q (ties to even)
+              // in the low bits; with s = 0 (1/s taken as 0) the product is 0.  The max with 0 (a
+              // no-op here) keeps the assembler from contracting the packed multiply and add into
+              // one FMA, whose unrounded product would round the ties differently.
+              const uint64_t y2 = tc::mul2(tc::sub2(rr2, mm2), ii2);
+              const uint64_t z2 = tc::add2(tc::f2(fmaxf(tc::f2lo(y2), 0.f), fmaxf(tc::f2hi(y2), 0.f)), mg2);
+              q0 = (uint32_t)z2 & 3u;
+              q1 = (uint32_t)(z2 >> 32) & 3u;
+              qf2 = tc::sub2(z2, mg2);
             }
-            bits |= q << (2 * u);
+            bits |= (q0 | (q1 << 2)) << (4 * u);
             if (KEY && R > 0) {
-              const float ev = __fsub_rn(f[u], __fadd_rn(mu[u], __fmaf_rn(ss, (float)q, mm)));
-              const float *Uc = Us + (8 * ci + u) * 16;
+              // E = K - (mu + (m + s q)), then C += E_c U_r[c][:] channel by channel
+              const uint64_t ev2 = tc::sub2(f2[u], tc::add2(m2[u], tc::fma2(ss2, qf2, mm2)));
 #pragma unroll
-              for (int k = 0; k < RMAX; k++) Cv[k] = fmaf(ev, Uc[k], Cv[k]);
+              for (int hc = 0; hc < 2; hc++) {
+                const float ev = hc ? tc::f2hi(ev2) : tc::f2lo(ev2);
+                const uint64_t evd = tc::f2(ev, ev);
+                const float *Uc = Us + (8 * ci + 2 * u + hc) * 16;
+#pragma unroll
+                for (int k4 = 0; k4 < RMAX / 4; k4++) {
+                  const uint4 uv = *(const uint4 *)(Uc + 4 * k4);
+                  Cv2[2 * k4] = tc::fma2(evd, u2(uv.x, uv.y), Cv2[2 * k4]);
+                  Cv2[2 * k4 + 1] = tc::fma2(evd, u2(uv.z, uv.w), Cv2[2 * k4 + 1]);
+                }
+              }
             }
           }
           if (ci & 1) packed[ci >> 1] |= bits << 16;
@@ -796,6 +832,12 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
           *(uint32_t *)(p.minv + grow * 2) = (uint32_t)mb0 | ((uint32_t)mb1 << 16);
         }
         if (KEY && p.dbg_score) p.dbg_score[grow] = best_S;
+        float Cv[RMAX];
+#pragma unroll
+        for (int k = 0; k < RMAX / 2; k++) {
+          Cv[2 * k] = tc::f2lo(Cv2[k]);
+          Cv[2 * k + 1] = tc::f2hi(Cv2[k]);
+        }
         if (KEY && R > 0) {
           float a = 0.f;
 #pragma unroll
