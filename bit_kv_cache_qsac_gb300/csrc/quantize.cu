@@ -420,14 +420,15 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
       const int64_t tok = tok0 + lane;
       const bool valid = tok < p.n;
       // ---- (1) the M+1 largest T, then the window mask (thread = token) ----
-      float kn2 = 0.f;
+      uint64_t kn2p = 0ull;  // ||k||^2 as two interleaved partial sums (it only sizes the window)
 #pragma unroll
       for (int ci = 0; ci < D / 8; ci++) {
-        float f[8];
-        bf16x8(tc::lds128(xts + (ci / 8) * TILE * 128 + tc::sw128_offset(row, 8 * (ci % 8))), f);
+        uint64_t f2[4];
+        bf16x8_pairs(tc::lds128(xts + (ci / 8) * TILE * 128 + tc::sw128_offset(row, 8 * (ci % 8))), f2);
 #pragma unroll
-        for (int u = 0; u < 8; u++) kn2 = fmaf(f[u], f[u], kn2);
+        for (int u = 0; u < 4; u++) kn2p = tc::fma2(f2[u], f2[u], kn2p);
       }
+      const float kn2 = tc::f2lo(kn2p) + tc::f2hi(kn2p);
       const float delta2 = 2.f * (dcoef * sqrtf(kn2) + dconst);
       uint32_t r[32];
       bool amb;
@@ -498,12 +499,15 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
           tc::tmem_ld16(tmem + lane_addr + 256u * s + c0 + 16, r + 16);
           tc::tmem_ld_wait();
 #pragma unroll
-          for (int k = 0; k < 32; k++) {
-            const float v = __uint_as_float(r[k]);
-            // descending list: new tv[i] = median(tv[i-1], tv[i], v), updated from the bottom up
+          for (int k = 0; k < 32; k += 2) {
+            // two values at a time: the sorted pair a >= b merged into the descending list,
+            // new tv[i] = max(tv[i], min(tv[i-1], a), min(tv[i-2], b)), updated from the bottom up
+            const float v0 = __uint_as_float(r[k]), v1 = __uint_as_float(r[k + 1]);
+            const float a = fmaxf(v0, v1), b = fminf(v0, v1);
 #pragma unroll
-            for (int i = MP1 - 1; i >= 1; i--) tv[i] = fminf(tv[i - 1], fmaxf(tv[i], v));
-            tv[0] = fmaxf(tv[0], v);
+            for (int i = MP1 - 1; i >= 2; i--) tv[i] = tc::max3(tv[i], fminf(tv[i - 1], a), fminf(tv[i - 2], b));
+            tv[1] = tc::max3(tv[1], fminf(tv[0], a), b);
+            tv[0] = fmaxf(tv[0], a);
           }
         }
         float tM = tv[0], tM1 = tv[0];  // the M-th and (M+1)-th largest (compile-time indexing)
@@ -684,14 +688,19 @@ __global__ void __launch_bounds__(kThreads, 1) quant_kernel(const __grid_constan
           for (int cc = 0; cc < 8; cc++) mv[cc] = *(const uint4 *)(mub + 64 * gi + 8 * cc);
 #pragma unroll
           for (int cc = 0; cc < 8; cc++) {
-            float f[8], mu[8];
-            bf16x8(tc::lds128(xts + gi * TILE * 128 + tc::sw128_offset(row, 8 * cc)), f);
-            bf16x8(mv[cc], mu);
+            uint64_t f2[4], m2[4];
+            bf16x8_pairs(tc::lds128(xts + gi * TILE * 128 + tc::sw128_offset(row, 8 * cc)), f2);
+            bf16x8_pairs(mv[cc], m2);
 #pragma unroll
-            for (int u = 0; u < 8; u++) {
-              const float rr = __fsub_rn(f[u], mu[u]);
-              if (gi == 0) { mn0 = fminf(mn0, rr); mx0 = fmaxf(mx0, rr); }
-              else { mn1 = fminf(mn1, rr); mx1 = fmaxf(mx1, rr); }
+            for (int u = 0; u < 4; u++) {
+              const uint64_t rr = tc::sub2(f2[u], m2[u]);
+              if (gi == 0) {
+                mn0 = tc::min3(mn0, tc::f2lo(rr), tc::f2hi(rr));
+                mx0 = tc::max3(mx0, tc::f2lo(rr), tc::f2hi(rr));
+              } else {
+                mn1 = tc::min3(mn1, tc::f2lo(rr), tc::f2hi(rr));
+                mx1 = tc::max3(mx1, tc::f2lo(rr), tc::f2hi(rr));
+              }
             }
           }
         }
