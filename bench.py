@@ -173,18 +173,16 @@ def gen_layer(layer: int):
 # captures of the kernel sources whose SHA-256 is given (the traffic is reported as null for any
 # other source): the attention launch; the packing's Key and Value passes with the stored-codebook
 # kernel; the fits' init, assignment and update launches (20 of each); the statistics kernels.  720p:
-# one capture of a whole timed step (all 50 launches, one pass each); 480p: the attention and the two
-# packing passes of one step.
+# one capture of a whole timed step (all 50 launches, one pass each); 480p: the attention of one step.
 TRAFFIC = {
     "attend.cu": {"sha256": "88b6a5df901f45795f665fce436100c791bdb22dc863825c58f44bb5b53079b2",
-                  "480p": 228292608 + 67828224, "720p": 476583424 + 189769472},
-    "quantize.cu": {"sha256": "e84e7a59bd241f42592420dd3afd237f9448e979a2bcc2ad1e6ad52abc89c82d",
-                    "480p": (50848000 + 270848) + (50659840 + 256),
-                    "720p": (114323968 + 6860544) + (114517504 + 6001152) + 5248000},
+                  "480p": 228292608 + 67828224, "720p": 472390144 + 186562304},
+    "quantize.cu": {"sha256": "36110a04e9f439a7f0bf411d8e2811938ccd3db314210bd37e48033969ae7420",
+                    "720p": (114315008 + 7234304) + (114438656 + 5317120) + 5248256},
     "kmeans.cu": {"sha256": "afd8b926ed71beda0ee83b01b6b1f3ba6c1a22ea3a25fa4f43f2b1ae805eacae",
-                  "720p": 5256704 + (2707316992 + 5027072) + (422241024 + 2048)},
+                  "720p": 5257216 + (2710714112 + 4509952) + (422221312 + 3584)},
     "stats_eig.cu": {"sha256": "7c25a04ea010919b3b31a5ee19d2ad368ac47731e5b9026db35675c949bb223c",
-                     "720p": (110614528 + 75520) + 13122304 + 2692864},
+                     "720p": (110628352 + 51456) + 13116160 + 2718976},
 }
 
 
@@ -246,8 +244,7 @@ def run_ours(args, rank, world, device):
         # with this chunk's Queries, and fold those into the statistics for the next chunk on a
         # second stream while the attention runs; the step ends when both are done
         ev[0].record(stream)
-        q.qwm_fit_centroids(ctx, Kc, N_CHUNK, prev_k, ch.cent_k, stream)
-        q.qwm_fit_centroids(ctx, Vc, N_CHUNK, prev_v, ch.cent_v, stream)
+        q.qwm_fit_centroids_kv(ctx, Kc, Vc, N_CHUNK, prev_k, prev_v, ch.cent_k, ch.cent_v, stream)
         ev[2].record(stream)
         stream.wait_event(stats_done)
         ch.u_r.copy_(u_next)                    # the chunk's own snapshot of the basis
@@ -433,7 +430,7 @@ def run_ours(args, rank, world, device):
         "compression": {"packed_bytes": cache_bytes, "bf16_bytes": 2 * H * N_CACHE * D * 2,
                         "ratio": 2 * H * N_CACHE * D * 2 / cache_bytes,
                         "note": "packed bytes = everything qwm_attend reads (codes, indices, INT2 metadata, "
-                                "bf16 codebooks, PSAC coefficients and bases)"},
+                                "fp16 codebooks, PSAC coefficients and bases)"},
         "setup_s": {"generate": gen_s},
     }
     if rank == 0 and not args.no_comparisons:
@@ -876,8 +873,7 @@ def run_steps(device):
             n = K[t].shape[1]
             ch = q.Chunk.empty(ctx, n, device)
             init_k, init_v = layer.prev_cent_k, layer.prev_cent_v
-            q.qwm_fit_centroids(ctx, K[t], n, init_k, ch.cent_k, main)
-            q.qwm_fit_centroids(ctx, V[t], n, init_v, ch.cent_v, main)
+            q.qwm_fit_centroids_kv(ctx, K[t], V[t], n, init_k, init_v, ch.cent_k, ch.cent_v, main)
             ev[2].record(main)
             if stats_done is not None:
                 main.wait_event(stats_done)

@@ -31,7 +31,7 @@ QWM_OK, QWM_ERR_ARG, QWM_ERR_SHAPE, QWM_ERR_ALIGN, QWM_ERR_CUDA, QWM_ERR_NOT_CON
     QWM_ERR_UNSUPPORTED, QWM_ERR_RANGE, QWM_ERR_DEVICE_TIMEOUT = range(9)
 
 EXPORTED = ("qwm_status_string", "qwm_workspace_bytes", "qwm_create", "qwm_destroy",
-            "qwm_update_query_stats", "qwm_fit_centroids", "qwm_quantize_kv", "qwm_attend",
+            "qwm_update_query_stats", "qwm_fit_centroids", "qwm_fit_centroids_kv", "qwm_quantize_kv", "qwm_attend",
             "qwm_dequantize", "qwm_sync_status", "qwm_update_query_stats_noalloc", "qwm_quantize_kv_full",
             "qwm_dequantize_chunks", "qwm_select_rank", "qwm_psac_kept", "qwm_psac_plan", "qwm_psac_pack",
             # comparison baselines (include/qwm_baselines.h)
@@ -97,6 +97,7 @@ _lib.qwm_create.argtypes = [C.POINTER(qwm_config), C.POINTER(C.c_void_p)]
 _lib.qwm_destroy.argtypes = [_P]
 _lib.qwm_update_query_stats.argtypes = [_P, _P, C.c_int64, _P, _P, _P, _P, _P, _P]
 _lib.qwm_fit_centroids.argtypes = [_P, _P, C.c_int64, _P, _P, _P]
+_lib.qwm_fit_centroids_kv.argtypes = [_P, _P, _P, C.c_int64, _P, _P, _P, _P, _P]
 _lib.qwm_quantize_kv.argtypes = [_P, _P, _P, C.c_int64, _P, _P, C.POINTER(qwm_chunk), C.POINTER(qwm_debug), _P]
 _lib.qwm_quantize_kv_full.argtypes = [_P, _P, _P, C.c_int64, _P, _P, _P, C.POINTER(qwm_chunk), C.POINTER(qwm_debug),
                                        _P]
@@ -325,6 +326,17 @@ def qwm_fit_centroids(ctx: Context, x, n: int, init, cent, stream=None) -> None:
     st = _lib.qwm_fit_centroids(ctx.handle, _ptr(x, "x", 2, (H, n, d)), n, _ptr(init, "init", 2, (H, Cn, d)),
                                 _ptr(cent, "cent", 2, (H, Cn, d)), _stream(stream))
     _check(st, "qwm_fit_centroids")
+
+
+def qwm_fit_centroids_kv(ctx: Context, k, v, n: int, init_k, init_v, cent_k, cent_v, stream=None) -> None:
+    """The Key and Value codebooks of one chunk, the two fits side by side (same results as two
+    qwm_fit_centroids calls)."""
+    H, d, Cn = ctx.cfg.heads, ctx.cfg.head_dim, ctx.cfg.n_centroids
+    st = _lib.qwm_fit_centroids_kv(ctx.handle, _ptr(k, "k", 2, (H, n, d)), _ptr(v, "v", 2, (H, n, d)), n,
+                                   _ptr(init_k, "init_k", 2, (H, Cn, d)), _ptr(init_v, "init_v", 2, (H, Cn, d)),
+                                   _ptr(cent_k, "cent_k", 2, (H, Cn, d)), _ptr(cent_v, "cent_v", 2, (H, Cn, d)),
+                                   _stream(stream))
+    _check(st, "qwm_fit_centroids_kv")
 
 
 def qwm_quantize_kv(ctx: Context, k, v, n: int, w, u_r, out: Chunk, debug: dict | None = None,

@@ -11,7 +11,8 @@ constexpr int kStatsSplits = 8;
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
-  size_t status, stats_part, km_sum, km_cnt, km_cent, km_img, km_prev, q_img, q_bfull, q_mfull, total;
+  size_t status, stats_part, q_img, q_bfull, q_mfull, total;
+  size_t km_sum[2], km_cnt[2], km_cent[2], km_img[2], km_prev[2];  // two k-means workspaces (Keys, Values)
 };
 
 Layout layout_of(const qwm_config &c) {
@@ -20,12 +21,15 @@ Layout layout_of(const qwm_config &c) {
   L.status = off; off = align_up(off + 256, 256);
   L.stats_part = off; off = align_up(off + (size_t)kStatsSplits * c.heads * QWM_D * QWM_D * sizeof(float), 256);
   const size_t G = (size_t)kmeans_ctas_per_head(c.heads, QWM_MAX_SMS);
-  L.km_sum = off; off = align_up(off + G * c.heads * c.n_centroids * QWM_D * sizeof(float), 256);
-  L.km_cnt = off; off = align_up(off + G * c.heads * c.n_centroids * sizeof(int32_t), 256);
-  L.km_cent = off; off = align_up(off + (size_t)c.heads * c.n_centroids * QWM_D * sizeof(float), 256);
-  L.km_img = off; off = align_up(off + kmeans_image_bytes(c.heads, c.n_centroids), 1024);
-  L.km_prev = off;  // resident codebooks only (uint8 assignments)
-  off = align_up(off + (c.n_centroids <= QWM_MAX_RESIDENT_CENTROIDS ? (size_t)c.heads * kKmPrevTokens : 0), 256);
+  for (int i = 0; i < 2; i++) {
+    L.km_sum[i] = off; off = align_up(off + G * c.heads * c.n_centroids * QWM_D * sizeof(float), 256);
+    L.km_cnt[i] = off; off = align_up(off + G * c.heads * c.n_centroids * sizeof(int32_t), 256);
+    L.km_cent[i] = off; off = align_up(off + (size_t)c.heads * c.n_centroids * QWM_D * sizeof(float), 256);
+    off = align_up(off, 1024);
+    L.km_img[i] = off; off = align_up(off + kmeans_image_bytes(c.heads, c.n_centroids), 1024);
+    L.km_prev[i] = off;  // resident codebooks only (uint8 assignments)
+    off = align_up(off + (c.n_centroids <= QWM_MAX_RESIDENT_CENTROIDS ? (size_t)c.heads * kKmPrevTokens : 0), 256);
+  }
   L.q_img = off; off = align_up(off + quantize_image_bytes(c.heads, c.n_centroids), 1024);
   L.q_bfull = off; off = align_up(off + (size_t)c.heads * c.n_centroids * QWM_D * sizeof(float), 256);
   L.q_mfull = off; off = align_up(off + (size_t)c.heads * QWM_D * QWM_D * sizeof(float), 256);
@@ -151,11 +155,14 @@ qwm_status qwm_create(const qwm_config *cfg, qwm_ctx **out) {
   ctx->status = (int32_t *)(base + L.status);
   ctx->stats_part = (float *)(base + L.stats_part);
   ctx->stats_splits = kStatsSplits;
-  ctx->km_sum = (float *)(base + L.km_sum);
-  ctx->km_cnt = (int32_t *)(base + L.km_cnt);
-  ctx->km_cent = (float *)(base + L.km_cent);
-  ctx->km_img = (unsigned char *)(base + L.km_img);
-  ctx->km_prev = ctx->cfg.n_centroids <= QWM_MAX_RESIDENT_CENTROIDS ? (uint8_t *)(base + L.km_prev) : nullptr;
+  for (int i = 0; i < 2; i++) {
+    ctx->km[i].sum = (float *)(base + L.km_sum[i]);
+    ctx->km[i].cnt = (int32_t *)(base + L.km_cnt[i]);
+    ctx->km[i].cent = (float *)(base + L.km_cent[i]);
+    ctx->km[i].img = (unsigned char *)(base + L.km_img[i]);
+    ctx->km[i].prev =
+        ctx->cfg.n_centroids <= QWM_MAX_RESIDENT_CENTROIDS ? (uint8_t *)(base + L.km_prev[i]) : nullptr;
+  }
   ctx->q_img = (unsigned char *)(base + L.q_img);
   ctx->q_bfull = (float *)(base + L.q_bfull);
   ctx->q_mfull = (float *)(base + L.q_mfull);
@@ -209,16 +216,43 @@ qwm_status qwm_update_query_stats(qwm_ctx *ctx, const uint16_t *q, int64_t nq, f
   return cuda_status(e);
 }
 
-qwm_status qwm_fit_centroids(qwm_ctx *ctx, const uint16_t *x, int64_t n, const uint16_t *init, uint16_t *cent,
-                             qwm_stream stream) {
+static qwm_status check_fit(const qwm_ctx *ctx, const uint16_t *x, int64_t n, const uint16_t *init,
+                            const uint16_t *cent) {
   if (!ctx || !x || !cent || n < 0) return QWM_ERR_ARG;
   if (n < ctx->cfg.n_centroids) return QWM_ERR_SHAPE;
   if (n * ctx->cfg.heads >= ((int64_t)1 << 31)) return QWM_ERR_SHAPE;
   if (!aligned16(x) || !aligned16(cent) || (init && !aligned16(init))) return QWM_ERR_ALIGN;
+  return QWM_OK;
+}
+
+// One fit with k-means workspace `ws` on stream st.
+static cudaError_t fit_on(qwm_ctx *ctx, int ws, const uint16_t *x, int64_t n, const uint16_t *init, uint16_t *cent,
+                          cudaStream_t st) {
   const int sms = ctx->num_sms < QWM_MAX_SMS ? ctx->num_sms : QWM_MAX_SMS;
-  cudaError_t e = launch_kmeans(x, n, ctx->cfg.heads, ctx->cfg.n_centroids, init, ctx->cfg.kmeans_iters, cent,
-                                ctx->km_cent, ctx->km_sum, ctx->km_cnt, sms, ctx->status, ctx->km_img, ctx->km_prev,
-                                kKmPrevTokens, (cudaStream_t)stream);
+  const KmWorkspace &w = ctx->km[ws];
+  return launch_kmeans(x, n, ctx->cfg.heads, ctx->cfg.n_centroids, init, ctx->cfg.kmeans_iters, cent, w.cent, w.sum,
+                       w.cnt, sms, ctx->status, w.img, w.prev, kKmPrevTokens, st);
+}
+
+qwm_status qwm_fit_centroids(qwm_ctx *ctx, const uint16_t *x, int64_t n, const uint16_t *init, uint16_t *cent,
+                             qwm_stream stream) {
+  qwm_status s = check_fit(ctx, x, n, init, cent);
+  if (s != QWM_OK) return s;
+  return cuda_status(fit_on(ctx, 0, x, n, init, cent, (cudaStream_t)stream));
+}
+
+qwm_status qwm_fit_centroids_kv(qwm_ctx *ctx, const uint16_t *k, const uint16_t *v, int64_t n, const uint16_t *init_k,
+                                const uint16_t *init_v, uint16_t *cent_k, uint16_t *cent_v, qwm_stream stream) {
+  qwm_status s = check_fit(ctx, k, n, init_k, cent_k);
+  if (s == QWM_OK) s = check_fit(ctx, v, n, init_v, cent_v);
+  if (s != QWM_OK) return s;
+  const cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = cudaEventRecord(ctx->fork, st);  // the Value fit starts after the work st holds
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->side, ctx->fork, 0);
+  if (e == cudaSuccess) e = fit_on(ctx, 0, k, n, init_k, cent_k, st);
+  if (e == cudaSuccess) e = fit_on(ctx, 1, v, n, init_v, cent_v, ctx->side);
+  if (e == cudaSuccess) e = cudaEventRecord(ctx->join, ctx->side);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ctx->join, 0);
   return cuda_status(e);
 }
 

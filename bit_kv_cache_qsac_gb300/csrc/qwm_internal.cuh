@@ -14,6 +14,16 @@
 #define QWM_MAX_TOPM 16
 #define QWM_MAX_RESIDENT_CENTROIDS 256  // larger codebooks (1024) stream through in slices
 
+// One k-means workspace: a fit's fp32 centroids, per-CTA cluster sums and counts, operand image and
+// kept assignments.  A context holds two, so that a chunk's Key and Value fits can run side by side.
+struct KmWorkspace {
+  uint8_t *prev;       // [H][kKmPrevTokens] assignments between iterations (resident codebooks), else NULL
+  float *sum;          // [H][G][C][d] per-CTA cluster sums (G CTAs per head)
+  int32_t *cnt;        // [H][G][C] per-CTA cluster counts
+  float *cent;         // [H][C][d] fp32 centroids during the iterations
+  unsigned char *img;  // the assignment kernel's operand image (hi/lo bf16 blocks) and squared norms
+};
+
 struct qwm_ctx {
   qwm_config cfg;
   int device;
@@ -24,16 +34,13 @@ struct qwm_ctx {
   int32_t *status;       // [1] first device-side error (qwm_status), 0 if none
   float *stats_part;     // [splits][H][d][d] per-split partial sums of q q^T
   int stats_splits;
-  uint8_t *km_prev;      // [H][kKmPrevTokens] k-means assignments between iterations (resident codebooks)
-  float *km_sum;         // [H][G][C][d] k-means per-CTA cluster sums (G CTAs per head)
-  int32_t *km_cnt;       // [H][G][C] k-means per-CTA cluster counts
-  float *km_cent;        // [H][C][d] fp32 centroids during the iterations
-  unsigned char *km_img; // 1024-centroid codebooks: k-means operand slices + norms
+  KmWorkspace km[2];     // k-means workspaces: [0] qwm_fit_centroids and the Key fit, [1] the Value fit
   unsigned char *q_img;  // 1024-centroid codebooks: quantiser operand slices + maxima
   float *q_bfull;        // full-form ranking: b_j = M mu_j [H][C][d]
   float *q_mfull;        // full-form ranking: M = S / n [H][d][d]
-  // a second stream (and fork / join events) on which the Value pass of qwm_quantize_kv runs beside
-  // the Key pass; the caller's stream waits for it before anything it issues next
+  // a second stream (and fork / join events) on which the Value fit of qwm_fit_centroids_kv and the
+  // Value pass of qwm_quantize_kv run beside the Key ones; the caller's stream waits for it before
+  // anything it issues next
   cudaStream_t side;
   cudaEvent_t fork, join;
 };

@@ -14,7 +14,7 @@ import math
 
 import torch
 
-from . import (ActiveChunk, Chunk, Context, pack_psac_layout, qwm_attend, qwm_dequantize, qwm_fit_centroids,
+from . import (ActiveChunk, Chunk, Context, pack_psac_layout, qwm_attend, qwm_dequantize, qwm_fit_centroids_kv,
                qwm_quantize_kv, qwm_quantize_kv_full, qwm_select_rank, qwm_sync_status, qwm_update_query_stats)
 
 
@@ -66,8 +66,7 @@ class CompressedLayer:
         ch = Chunk.empty(self.ctx, n, self.device)
         init_k = self.prev_cent_k if warm_start else None
         init_v = self.prev_cent_v if warm_start else None
-        qwm_fit_centroids(self.ctx, k, n, init_k, ch.cent_k, stream)
-        qwm_fit_centroids(self.ctx, v, n, init_v, ch.cent_v, stream)
+        qwm_fit_centroids_kv(self.ctx, k, v, n, init_k, init_v, ch.cent_k, ch.cent_v, stream)
         s = stream if stream is not None else torch.cuda.current_stream(self.device)
         if stats_done is not None:
             s.wait_event(stats_done)

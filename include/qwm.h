@@ -225,6 +225,21 @@ QWM_API qwm_status qwm_update_query_stats(qwm_ctx *ctx, const uint16_t *q, int64
 QWM_API qwm_status qwm_fit_centroids(qwm_ctx *ctx, const uint16_t *x, int64_t n, const uint16_t *init, uint16_t *cent,
                              qwm_stream stream);
 
+/* Step 2a for the Keys and the Values of one chunk in one call: the same two fits as
+ * qwm_fit_centroids(ctx, k, n, init_k, cent_k) and qwm_fit_centroids(ctx, v, n, init_v, cent_v),
+ * with bit-identical results, run side by side.  The Key fit runs on `stream`, the Value fit on
+ * the context's second stream with a k-means workspace of its own (the two fits read and write
+ * disjoint data); the second stream starts after the work `stream` already holds and `stream`
+ * waits for it at the end, so the call is ordered on `stream` like any other.  Each fit uses
+ * about 120 of the GPU's SMs at 40 heads, so side by side they fill the SMs one fit leaves idle.
+ *   k, v           bf16 [H][n][d]  the chunk's Keys and Values (n >= config.n_centroids)
+ *   init_k, init_v bf16 [H][C][d]  starting centroids of each, or NULL (as qwm_fit_centroids)
+ *   cent_k, cent_v bf16 [H][C][d]  out: the two codebooks
+ * Errors as qwm_fit_centroids; on an error nothing is launched. */
+QWM_API qwm_status qwm_fit_centroids_kv(qwm_ctx *ctx, const uint16_t *k, const uint16_t *v, int64_t n,
+                                const uint16_t *init_k, const uint16_t *init_v, uint16_t *cent_k,
+                                uint16_t *cent_v, qwm_stream stream);
+
 /* Steps 2-4 -- QSAC assignment, INT2 residual codes and PSAC coefficients for one chunk
  * (Chinese summary "核心方法" and steps (2)-(4); Korean summary "무엇과 다른가", "어떻게 쓰나").
  *   k, v  bf16 [H][n][d]   the chunk's Keys and Values

@@ -59,6 +59,7 @@ def test_null_arguments_rejected_before_cuda(qwm):
     assert lib.qwm_destroy(None) == qwm.QWM_ERR_ARG
     assert lib.qwm_update_query_stats(None, None, 0, None, None, None, None, None, None) == qwm.QWM_ERR_ARG
     assert lib.qwm_fit_centroids(None, None, 0, None, None, None) == qwm.QWM_ERR_ARG
+    assert lib.qwm_fit_centroids_kv(None, None, None, 0, None, None, None, None, None) == qwm.QWM_ERR_ARG
     assert lib.qwm_quantize_kv(None, None, None, 0, None, None, None, None, None) == qwm.QWM_ERR_ARG
     assert lib.qwm_attend(None, None, 0, None, 0, 1.0, None, None) == qwm.QWM_ERR_ARG
     assert lib.qwm_dequantize(None, None, None, None, None) == qwm.QWM_ERR_ARG

@@ -186,6 +186,30 @@ def test_kmeans_objective_past_the_kept_assignments(q):
     assert abs(j_gpu - j_ref) <= 1e-3 * j_ref, (j_gpu, j_ref)
 
 
+@pytest.mark.parametrize("C,warm", [(64, False), (256, True), (1024, False)], ids=["c64", "c256_warm", "c1024"])
+def test_fit_centroids_kv_equals_two_fits(q, C, warm):
+    """The paired call (the Value fit on the context's second stream with its own workspace) gives
+    the two codebooks of two qwm_fit_centroids calls bit for bit, and the context stays usable for
+    single fits afterwards."""
+    H, n = 2, 2600
+    k = _bf(synth.keys(WIDE_W)[:, :n]); v = _bf(synth.values(WIDE_W)[:, :n])
+    ctx = q.Context(heads=H, n_centroids=C, top_m=4)
+    init_k = init_v = None
+    if warm:  # the previous chunk's codebooks as the starting points
+        init_k = torch.empty(H, C, D, dtype=torch.bfloat16, device="cuda"); init_v = torch.empty_like(init_k)
+        q.qwm_fit_centroids(ctx, _bf(synth.keys(WIDE_W)[:, n:2 * n]), n, None, init_k)
+        q.qwm_fit_centroids(ctx, _bf(synth.values(WIDE_W)[:, n:2 * n]), n, None, init_v)
+    ref_k = torch.empty(H, C, D, dtype=torch.bfloat16, device="cuda"); ref_v = torch.empty_like(ref_k)
+    q.qwm_fit_centroids(ctx, k, n, init_k, ref_k)
+    q.qwm_fit_centroids(ctx, v, n, init_v, ref_v)
+    ck, cv = torch.empty_like(ref_k), torch.empty_like(ref_k)
+    q.qwm_fit_centroids_kv(ctx, k, v, n, init_k, init_v, ck, cv)
+    again = torch.empty_like(ref_k)
+    q.qwm_fit_centroids(ctx, v, n, init_v, again)
+    assert q.qwm_sync_status(ctx) == 0
+    assert torch.equal(ck, ref_k) and torch.equal(cv, ref_v) and torch.equal(again, ref_v)
+
+
 def test_kmeans_objective_1024_centroids(q):
     H, n, C = 2, 2600, 1024
     x = synth.keys(WIDE_W)[:, :n]
