@@ -173,16 +173,16 @@ def gen_layer(layer: int):
 # captures of the kernel sources whose SHA-256 is given (the traffic is reported as null for any
 # other source): the attention launch; the packing's Key and Value passes with the stored-codebook
 # kernel; the fits' init, assignment and update launches (20 of each); the statistics kernels.  720p:
-# one capture of a whole timed step (all 50 launches, one pass each); 480p: the attention of one step.
+# one capture of a whole timed step (all 50 launches, one pass each).
 TRAFFIC = {
-    "attend.cu": {"sha256": "88b6a5df901f45795f665fce436100c791bdb22dc863825c58f44bb5b53079b2",
-                  "480p": 228292608 + 67828224, "720p": 472390144 + 186562304},
+    "attend.cu": {"sha256": "c6f7bd88b526b4fad14240d024bdb371b639a638ab8aa3c24cd8621bd9a9061e",
+                  "720p": 473975040 + 187103744},
     "quantize.cu": {"sha256": "36110a04e9f439a7f0bf411d8e2811938ccd3db314210bd37e48033969ae7420",
-                    "720p": (114315008 + 7234304) + (114438656 + 5317120) + 5248256},
+                    "720p": (114317568 + 6869504) + (114441216 + 5344512) + 5248000},
     "kmeans.cu": {"sha256": "afd8b926ed71beda0ee83b01b6b1f3ba6c1a22ea3a25fa4f43f2b1ae805eacae",
-                  "720p": 5257216 + (2710714112 + 4509952) + (422221312 + 3584)},
+                  "720p": (5257216 + 5888) + (2710160384 + 6042624) + 422226944},
     "stats_eig.cu": {"sha256": "7c25a04ea010919b3b31a5ee19d2ad368ac47731e5b9026db35675c949bb223c",
-                     "720p": (110628352 + 51456) + 13116160 + 2718976},
+                     "720p": (110627328 + 123392) + 13116160 + 2694144},
 }
 
 

@@ -31,7 +31,7 @@ QWM_OK, QWM_ERR_ARG, QWM_ERR_SHAPE, QWM_ERR_ALIGN, QWM_ERR_CUDA, QWM_ERR_NOT_CON
     QWM_ERR_UNSUPPORTED, QWM_ERR_RANGE, QWM_ERR_DEVICE_TIMEOUT = range(9)
 
 EXPORTED = ("qwm_status_string", "qwm_workspace_bytes", "qwm_create", "qwm_destroy",
-            "qwm_update_query_stats", "qwm_fit_centroids", "qwm_fit_centroids_kv", "qwm_quantize_kv", "qwm_attend",
+            "qwm_update_query_stats", "qwm_fit_centroids", "qwm_fit_centroids_kv", "qwm_quantize_kv", "qwm_attend", "qwm_attend_merge",
             "qwm_dequantize", "qwm_sync_status", "qwm_update_query_stats_noalloc", "qwm_quantize_kv_full",
             "qwm_dequantize_chunks", "qwm_select_rank", "qwm_psac_kept", "qwm_psac_plan", "qwm_psac_pack",
             # comparison baselines (include/qwm_baselines.h)
@@ -102,6 +102,7 @@ _lib.qwm_quantize_kv.argtypes = [_P, _P, _P, C.c_int64, _P, _P, C.POINTER(qwm_ch
 _lib.qwm_quantize_kv_full.argtypes = [_P, _P, _P, C.c_int64, _P, _P, _P, C.POINTER(qwm_chunk), C.POINTER(qwm_debug),
                                        _P]
 _lib.qwm_attend.argtypes = [_P, _P, C.c_int64, C.POINTER(qwm_chunk), C.c_int32, C.c_float, _P, _P]
+_lib.qwm_attend_merge.argtypes = [_P, _P, C.c_int64, C.POINTER(qwm_chunk), C.c_int32, C.c_float, _P, _P, C.c_int32, _P]
 _lib.qwm_dequantize.argtypes = [_P, C.POINTER(qwm_chunk), _P, _P, _P]
 _lib.qwm_dequantize_chunks.argtypes = [_P, C.POINTER(qwm_chunk), C.c_int32, _P, _P, _P]
 _lib.qwm_select_rank.argtypes = [_P, _P, C.c_float, _P, _P, _P]
@@ -362,6 +363,18 @@ def qwm_attend(ctx: Context, q, nq: int, chunks: list, softmax_scale: float, out
     st = _lib.qwm_attend(ctx.handle, _ptr(q, "q", 2, (H, nq, d)), nq, arr, len(chunks), float(softmax_scale),
                          _ptr(out, "out", 4, (H, nq, d)), _stream(stream))
     _check(st, "qwm_attend")
+
+
+def qwm_attend_merge(ctx: Context, q, nq: int, chunks: list, softmax_scale: float, out, lse, merge: bool,
+                     stream=None) -> None:
+    """qwm_attend over some of a cache's chunks with the rows' log-sum-exp: merge=False writes out and
+    lse; merge=True merges this call's chunks into the result already in out and lse."""
+    H, d = ctx.cfg.heads, ctx.cfg.head_dim
+    arr = (qwm_chunk * len(chunks))(*[c.struct() for c in chunks])
+    st = _lib.qwm_attend_merge(ctx.handle, _ptr(q, "q", 2, (H, nq, d)), nq, arr, len(chunks), float(softmax_scale),
+                               _ptr(out, "out", 4, (H, nq, d)), _ptr(lse, "lse", 4, (H, nq)), 1 if merge else 0,
+                               _stream(stream))
+    _check(st, "qwm_attend_merge")
 
 
 def qwm_dequantize(ctx: Context, chunk: Chunk, k_hat, v_hat, stream=None) -> None:

@@ -300,8 +300,9 @@ qwm_status qwm_quantize_kv_full(qwm_ctx *ctx, const uint16_t *k, const uint16_t 
   return quantize_impl(ctx, k, v, n, nullptr, S, n_seen, u_r, out, dbg, stream);
 }
 
-qwm_status qwm_attend(qwm_ctx *ctx, const uint16_t *q, int64_t nq, const qwm_chunk *chunks, int32_t n_chunks,
-                      float softmax_scale, float *out, qwm_stream stream) {
+static qwm_status attend_impl(qwm_ctx *ctx, const uint16_t *q, int64_t nq, const qwm_chunk *chunks,
+                              int32_t n_chunks, float softmax_scale, float *out, float *lse, int merge,
+                              qwm_stream stream) {
   if (!ctx || !chunks || nq < 0 || n_chunks < 1) return QWM_ERR_ARG;
   if (nq > 0 && !out) return QWM_ERR_ARG;
   if (nq > 0 && !q) return QWM_ERR_ARG;
@@ -318,9 +319,22 @@ qwm_status qwm_attend(qwm_ctx *ctx, const uint16_t *q, int64_t nq, const qwm_chu
   }
   if (total < 1) return QWM_ERR_SHAPE;
   if (nq == 0) return QWM_OK;
-  cudaError_t e = launch_attend(ctx->cfg, q, nq, chunks, n_chunks, softmax_scale, out, ctx->num_sms, ctx->status,
-                                (cudaStream_t)stream);
+  cudaError_t e = launch_attend(ctx->cfg, q, nq, chunks, n_chunks, softmax_scale, out, lse, merge, ctx->num_sms,
+                                ctx->status, (cudaStream_t)stream);
   return cuda_status(e);
+}
+
+qwm_status qwm_attend(qwm_ctx *ctx, const uint16_t *q, int64_t nq, const qwm_chunk *chunks, int32_t n_chunks,
+                      float softmax_scale, float *out, qwm_stream stream) {
+  return attend_impl(ctx, q, nq, chunks, n_chunks, softmax_scale, out, nullptr, 0, stream);
+}
+
+qwm_status qwm_attend_merge(qwm_ctx *ctx, const uint16_t *q, int64_t nq, const qwm_chunk *chunks, int32_t n_chunks,
+                            float softmax_scale, float *out, float *lse, int32_t merge, qwm_stream stream) {
+  if (merge != 0 && merge != 1) return QWM_ERR_ARG;
+  if (nq > 0 && !lse) return QWM_ERR_ARG;
+  if (lse && !aligned16(lse)) return QWM_ERR_ALIGN;
+  return attend_impl(ctx, q, nq, chunks, n_chunks, softmax_scale, out, lse, merge, stream);
 }
 
 qwm_status qwm_dequantize(qwm_ctx *ctx, const qwm_chunk *chunk, uint16_t *k_hat, uint16_t *v_hat,

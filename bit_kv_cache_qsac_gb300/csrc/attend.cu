@@ -130,6 +130,8 @@ struct AttnChunk {
 struct AttnParams {
   const uint16_t *q;
   float *out;
+  float *lse;        // [H][nq] log2-sum-exp of the scaled logits, or NULL
+  int merge;         // 1: out and lse hold a result over other keys; merge this call's into them
   int64_t nq;
   int H, C, n_chunks, total_tiles;
   int compact;       // the chunks' INT2 metadata is the compact form (8-bit step, 2-bit zero-point)
@@ -511,8 +513,8 @@ __device__ __forceinline__ void producer_pair(const AttnParams &p, unsigned char
 
 // WIDE: PSAC ranks above 8 (32-column second-MMA operands).  IDX16: uint16 centroid indices.
 // EXT: the call includes a bf16 chunk (the chunk being generated), compact INT2 metadata or per-head
-// PSAC coefficient layouts.
-template <bool WIDE, bool IDX16, bool EXT>
+// PSAC coefficient layouts.  LSE: the rows' log-sum-exp is written (and, merging, read with O).
+template <bool WIDE, bool IDX16, bool EXT, bool LSE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     attend_pair_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -700,7 +702,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t lsum = tc::add2(acc0, acc1);
       const float l = tc::f2lo(lsum) + tc::f2hi(lsum);
       const int64_t qi = qb + (int64_t)x * 2 * BM + row;
-      const float inv = 1.f / l;
+      float inv = 1.f / l;
+      float keep = 0.f;  // merge: the weight of the result already in out
+      if (LSE && qi < p.nq) {
+        // log2 of this call's exponential sum: sum_j 2^(S_j * scale * log2 e) = 2^m_used * l
+        float *lp = p.lse + (int64_t)h * p.nq + qi;
+        const float L = m_used + log2f(l);
+        float Lout = L;
+        if (p.merge) {  // out = w_prev out + w_this O / l, the weights the parts' shares of the union's sum
+          const float Lp = *lp, Lm = fmaxf(Lp, L);
+          const float wp = exp2f(Lp - Lm), wt = exp2f(L - Lm), den = wp + wt;
+          keep = wp / den;
+          inv = wt > 0.f ? wt / (den * l) : 0.f;
+          Lout = Lm + log2f(den);
+        }
+        *lp = Lout;
+      }
       uint32_t o[32];
 #pragma unroll 1
       for (int c = 0; c < D; c += 32) {
@@ -708,10 +725,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc::tmem_ld_wait();
         if (qi < p.nq) {
           float4 *dst = (float4 *)(p.out + ((int64_t)h * p.nq + qi) * D + c);
+          if (LSE && keep > 0.f) {
 #pragma unroll
-          for (int v = 0; v < 8; v++)
-            dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
-                                 __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
+            for (int v = 0; v < 8; v++) {
+              const float4 a = dst[v];
+              dst[v] = make_float4(fmaf(keep, a.x, __uint_as_float(o[4 * v]) * inv),
+                                   fmaf(keep, a.y, __uint_as_float(o[4 * v + 1]) * inv),
+                                   fmaf(keep, a.z, __uint_as_float(o[4 * v + 2]) * inv),
+                                   fmaf(keep, a.w, __uint_as_float(o[4 * v + 3]) * inv));
+            }
+          } else {
+#pragma unroll
+            for (int v = 0; v < 8; v++)
+              dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
+                                   __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
+          }
         }
       }
     }
@@ -810,30 +838,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool WIDE, bool IDX16, bool EXT>
+template <bool WIDE, bool IDX16, bool EXT, bool LSE>
 cudaError_t launch_pair(const AttnParams &p, dim3 grid, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(attend_pair_kernel<WIDE, IDX16, EXT>,
+  cudaError_t e = cudaFuncSetAttribute(attend_pair_kernel<WIDE, IDX16, EXT, LSE>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, XL<WIDE>::kSmemAlloc);
   if (e != cudaSuccess) return e;
-  attend_pair_kernel<WIDE, IDX16, EXT><<<grid, kThreads, XL<WIDE>::kSmemAlloc, st>>>(p);
+  attend_pair_kernel<WIDE, IDX16, EXT, LSE><<<grid, kThreads, XL<WIDE>::kSmemAlloc, st>>>(p);
   return cudaGetLastError();
 }
 
-template <bool EXT>
+template <bool EXT, bool LSE>
 cudaError_t launch_pair_ext(const AttnParams &p, dim3 grid, bool wide, bool idx16, cudaStream_t st) {
-  if (wide && idx16) return launch_pair<true, true, EXT>(p, grid, st);
-  if (wide) return launch_pair<true, false, EXT>(p, grid, st);
-  if (idx16) return launch_pair<false, true, EXT>(p, grid, st);
-  return launch_pair<false, false, EXT>(p, grid, st);
+  if (wide && idx16) return launch_pair<true, true, EXT, LSE>(p, grid, st);
+  if (wide) return launch_pair<true, false, EXT, LSE>(p, grid, st);
+  if (idx16) return launch_pair<false, true, EXT, LSE>(p, grid, st);
+  return launch_pair<false, false, EXT, LSE>(p, grid, st);
 }
 
 }  // namespace
 
 cudaError_t launch_attend(const qwm_config &cfg, const uint16_t *q, int64_t nq, const qwm_chunk *chunks,
-                          int n_chunks, float scale, float *out, int num_sms, int32_t *status, cudaStream_t st) {
+                          int n_chunks, float scale, float *out, float *lse, int merge, int num_sms, int32_t *status,
+                          cudaStream_t st) {
   (void)num_sms;
   AttnParams p;  // passed by value (about 17 KB of kernel parameters)
-  p.q = q; p.out = out; p.nq = nq; p.H = cfg.heads; p.C = cfg.n_centroids;
+  p.q = q; p.out = out; p.lse = lse; p.merge = lse ? merge : 0; p.nq = nq; p.H = cfg.heads; p.C = cfg.n_centroids;
   p.compact = cfg.storage == QWM_STORAGE_COMPACT;
   p.any_causal = 0;
   p.scale_log2 = scale * 1.4426950408889634f;
@@ -872,7 +901,11 @@ cudaError_t launch_attend(const qwm_config &cfg, const uint16_t *q, int64_t nq, 
   cudaError_t e;
   const dim3 grid((unsigned)(2 * ((nq + kPairQ - 1) / kPairQ)), cfg.heads);  // CTA pairs
   const bool ext = raw || p.compact || per_head;
-  e = ext ? launch_pair_ext<true>(p, grid, wide, idx16, st) : launch_pair_ext<false>(p, grid, wide, idx16, st);
+  if (lse)
+    e = ext ? launch_pair_ext<true, true>(p, grid, wide, idx16, st) : launch_pair_ext<false, true>(p, grid, wide, idx16, st);
+  else
+    e = ext ? launch_pair_ext<true, false>(p, grid, wide, idx16, st)
+            : launch_pair_ext<false, false>(p, grid, wide, idx16, st);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -129,7 +129,8 @@ cudaError_t launch_quantize(const qwm_config &cfg, const uint16_t *k, const uint
                             int num_sms, unsigned char *img, cudaStream_t st, cudaStream_t side, cudaEvent_t fork,
                             cudaEvent_t join);
 cudaError_t launch_attend(const qwm_config &cfg, const uint16_t *q, int64_t nq, const qwm_chunk *chunks,
-                          int n_chunks, float scale, float *out, int num_sms, int32_t *status, cudaStream_t st);
+                          int n_chunks, float scale, float *out, float *lse, int merge, int num_sms, int32_t *status,
+                          cudaStream_t st);
 cudaError_t launch_dequantize(const qwm_config &cfg, const qwm_chunk *chunks, int n_chunks, uint16_t *k_hat,
                               uint16_t *v_hat, cudaStream_t st);
 cudaError_t launch_select_rank(const float *eigvals, float energy, int H, int R, uint16_t *u_r, int32_t *head_rank,

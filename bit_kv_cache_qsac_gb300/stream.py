@@ -14,7 +14,8 @@ import math
 
 import torch
 
-from . import (ActiveChunk, Chunk, Context, pack_psac_layout, qwm_attend, qwm_dequantize, qwm_fit_centroids_kv,
+from . import (ActiveChunk, Chunk, Context, pack_psac_layout, qwm_attend, qwm_attend_merge, qwm_dequantize,
+               qwm_fit_centroids_kv,
                qwm_quantize_kv, qwm_quantize_kv_full, qwm_select_rank, qwm_sync_status, qwm_update_query_stats)
 
 
@@ -50,6 +51,7 @@ class CompressedLayer:
         self.prev_cent_v = None
         self._side = None        # second stream for the statistics update of step()
         self._stats_pending = None  # stream_step(): the fold the next packing waits for
+        self._hist = None        # stream_step(overlap=True): high-priority stream of the history attention
 
     def fold_queries(self, q: torch.Tensor, stream=None) -> None:
         """Step 1: fold Queries [H][nq][d] into the statistics and recompute w and U_r."""
@@ -128,13 +130,31 @@ class CompressedLayer:
         self.append_chunk(k, v, stream=main, stats_done=done)
         return self.attend(q, stream=main)
 
-    def stream_step(self, k, v, q, stream=None) -> torch.Tensor:
+    def stream_step(self, k, v, q, stream=None, overlap: bool = False) -> torch.Tensor:
         """One streaming step in pipelined order: pack (k, v) with the statistics of every Query
         folded so far, attend with q, and fold q into the statistics on a second stream while the
         attention runs; the next call's packing waits for that fold.  The same work as
         step(q_prev, k, v, q) with q_prev the previous call's q, with the statistics beside the
-        attention instead of beside the codebook fits."""
+        attention instead of beside the codebook fits.
+
+        overlap: the attention over the chunks already in the cache runs on a high-priority stream
+        beside the new chunk's fits and packing (it does not depend on them), and the new chunk's
+        attention then merges into it through the rows' log-sum-exp (qwm_attend_merge); the same
+        output up to rounding."""
         main = stream if stream is not None else torch.cuda.current_stream(self.device)
+        H, nq, d = q.shape
+        scale = 1.0 / math.sqrt(d)
+        history = None
+        if overlap and self.chunks:
+            if self._hist is None:
+                self._hist = torch.cuda.Stream(self.device, priority=-1)
+            out = torch.empty(H, nq, d, dtype=torch.float32, device=q.device)
+            lse = torch.empty(H, nq, dtype=torch.float32, device=q.device)
+            self._hist.wait_stream(main)
+            for t in (q, out, lse):
+                t.record_stream(self._hist)
+            qwm_attend_merge(self.ctx, q, nq, list(self.chunks), scale, out, lse, False, self._hist)
+            history = True
         self.append_chunk(k, v, stream=main, stats_done=self._stats_pending)
         packed = torch.cuda.Event()
         packed.record(main)
@@ -145,7 +165,14 @@ class CompressedLayer:
         self.fold_queries(q, self._side)
         self._stats_pending = torch.cuda.Event()
         self._stats_pending.record(self._side)
-        out = self.attend(q, stream=main)
+        if history is not None:
+            # the new chunk merged in on the same high-priority stream (the statistics fold beside it
+            # fills the SMs it leaves)
+            self._hist.wait_event(packed)
+            qwm_attend_merge(self.ctx, q, nq, [self.chunks[-1]], scale, out, lse, True, self._hist)
+            main.wait_stream(self._hist)
+        else:
+            out = self.attend(q, stream=main)
         main.wait_event(self._stats_pending)   # the step ends when both are done
         return out
 

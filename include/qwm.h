@@ -326,6 +326,24 @@ QWM_API qwm_status qwm_psac_pack(qwm_ctx *ctx, const qwm_chunk *dense, const qwm
 QWM_API qwm_status qwm_attend(qwm_ctx *ctx, const uint16_t *q, int64_t nq, const qwm_chunk *chunks, int32_t n_chunks,
                       float softmax_scale, float *out, qwm_stream stream);
 
+/* qwm_attend over a subset of a cache's chunks, in two parts that merge: the softmax over a union of
+ * chunk sets is the weighted mean of the softmaxes over its parts, each weighted by its share of the
+ * exponential sum.  So the attention over the chunks already packed can run while the newest chunk is
+ * still being fitted and packed, and the newest chunk's attention then merges into it.
+ *   q, nq, chunks, n_chunks, softmax_scale  as qwm_attend
+ *   out      fp32 [H][nq][d]   merge == 0: out; merge == 1: inout
+ *   lse      fp32 [H][nq]      merge == 0: out; merge == 1: inout: log2 of the sum over the call's keys
+ *                              of 2^(softmax_scale * log2(e) * l_ij), l_ij the logit as in qwm_attend
+ *   merge    0: out and lse are this call's softmax output and log-sum-exp;
+ *            1: out and lse hold a result over other keys of the same Queries (a merge == 0 call, or
+ *               earlier merges) and become the result over those keys and this call's together
+ * The merged output equals one qwm_attend over the union of the chunks up to rounding (the parts'
+ * weights 2^(lse_part - lse_union) are computed in fp32 with CUDA's exp2f and log2f).  A Query row must
+ * see at least one key in a merge == 0 call. */
+QWM_API qwm_status qwm_attend_merge(qwm_ctx *ctx, const uint16_t *q, int64_t nq, const qwm_chunk *chunks,
+                            int32_t n_chunks, float softmax_scale, float *out, float *lse, int32_t merge,
+                            qwm_stream stream);
+
 /* Step 5' -- BF16 reconstruction of one packed chunk (the pages' fused decoder, English v2 §D.1;
  * QWM_ERR_UNSUPPORTED for a QWM_CHUNK_BF16 descriptor):
  * K_hat = mu^K_idx + r_hat + C_hat U_r^T and V_hat = mu^V_idx + r_hat, rounded to nearest-even.

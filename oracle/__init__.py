@@ -91,7 +91,7 @@ def lib():
             l.oracle_int8_encode_token.argtypes = [P, C.c_int, P, P]
             l.oracle_quantize_head.argtypes = [C.POINTER(QuantArgs)]
             l.oracle_attend_rows.argtypes = [P, C.c_int, C.c_int, P, I64, C.POINTER(ChunkHead),
-                                             C.c_int, C.c_double, P]
+                                             C.c_int, C.c_double, P, P]
             l.oracle_dequantize_head.argtypes = [C.POINTER(ChunkHead), C.c_int, C.c_int, P, P, P, P]
             l.oracle_prq_residual.argtypes = [P, I64, C.c_int, P, P, P]
             l.oracle_kivi_quantize_head.argtypes = [P, P, I64, C.c_int, C.c_int, P, P, P, P, P, P]
@@ -304,17 +304,21 @@ def _chunk_struct(ch: dict, keep: list) -> ChunkHead:
     )
 
 
-def attend_rows(q_bf16: np.ndarray, rows, chunks: list[dict], scale: float, group: int = 64) -> np.ndarray:
+def attend_rows(q_bf16: np.ndarray, rows, chunks: list[dict], scale: float, group: int = 64,
+                with_lse: bool = False):
     """Attention output (float64 [len(rows)][d]) of the listed query rows of one head over
-    every token of every chunk in `chunks` (per-head chunk dicts)."""
+    every token of every chunk in `chunks` (per-head chunk dicts); with_lse: also the rows'
+    base-2 log-sum-exp of the logits, (output, lse)."""
     q = _c(q_bf16, np.uint16)
     rows = _c(np.asarray(rows), np.int64)
     d = q.shape[1]
     keep: list = []
     arr = (ChunkHead * max(1, len(chunks)))(*[_chunk_struct(ch, keep) for ch in chunks])
     out = np.empty((rows.size, d), np.float64)
-    lib().oracle_attend_rows(_p(q), d, group, _p(rows), rows.size, arr, len(chunks), float(scale), _p(out))
-    return out
+    lse = np.empty(rows.size, np.float64) if with_lse else None
+    lib().oracle_attend_rows(_p(q), d, group, _p(rows), rows.size, arr, len(chunks), float(scale), _p(out),
+                             _p(lse) if with_lse else None)
+    return (out, lse) if with_lse else out
 
 
 def dequantize_head(ch: dict, d: int = 128, group: int = 64):

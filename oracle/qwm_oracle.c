@@ -756,9 +756,10 @@ static void decode_token(const oracle_chunk_head *ch, int d, int group, int64_t 
 
 /* For each listed query row, o = softmax(l) V_hat over every token of every chunk, with
  * l_j = scale * (q . k_hat_0_j + (q U_r^(chunk)) . c_hat_j),  c_hat = sC * c.
- * Softmax in double with the running maximum subtracted.  out[rows][d] double. */
+ * Softmax in double with the running maximum subtracted.  out[rows][d] double.  lse (may be NULL):
+ * [rows] double, the base-2 log of sum_j exp(l_j) = (lmax + ln(sum_j exp(l_j - lmax))) / ln 2. */
 void oracle_attend_rows(const uint16_t *q, int d, int group, const int64_t *rows, int64_t n_rows,
-                        const oracle_chunk_head *chunks, int n_chunks, double scale, double *out) {
+                        const oracle_chunk_head *chunks, int n_chunks, double scale, double *out, double *lse) {
   int64_t total = 0;
   for (int t = 0; t < n_chunks; t++) total += chunks[t].n;
 #pragma omp parallel
@@ -814,6 +815,7 @@ void oracle_attend_rows(const uint16_t *q, int d, int group, const int64_t *rows
         off += ch->n;
       }
       for (int c = 0; c < d; c++) o[c] /= denom;
+      if (lse) lse[ri] = (lmax + log(denom)) / log(2.0);
     }
     free(l);
     free(kh0);

@@ -62,6 +62,7 @@ def test_null_arguments_rejected_before_cuda(qwm):
     assert lib.qwm_fit_centroids_kv(None, None, None, 0, None, None, None, None, None) == qwm.QWM_ERR_ARG
     assert lib.qwm_quantize_kv(None, None, None, 0, None, None, None, None, None) == qwm.QWM_ERR_ARG
     assert lib.qwm_attend(None, None, 0, None, 0, 1.0, None, None) == qwm.QWM_ERR_ARG
+    assert lib.qwm_attend_merge(None, None, 0, None, 0, 1.0, None, None, 0, None) == qwm.QWM_ERR_ARG
     assert lib.qwm_dequantize(None, None, None, None, None) == qwm.QWM_ERR_ARG
     assert lib.qwm_sync_status(None, None) == qwm.QWM_ERR_ARG
     assert qwm.qwm_status_string(qwm.QWM_ERR_NOT_CONVERGED).startswith("eigensolver")

@@ -732,6 +732,78 @@ def test_stream_step_matches_step(q):
     assert int(lb.n[0]) == int(la.n[0]) + 96
 
 
+@pytest.mark.parametrize("with_active", [False, True], ids=["packed", "packed_then_active"])
+def test_attend_merge_parts(q, with_active):
+    """Two calls of qwm_attend_merge -- the first two packed chunks, then the third (and the chunk being
+    generated, block-causal) merged in -- against the oracle over the union: the output within the
+    attention's bar, each call's log-sum-exp within 0.02 (log2 units) of the oracle's; and against
+    one call over the union: the same output and log-sum-exp up to the merge's fp32 rounding."""
+    w_ = synth.TINY
+    H = 2
+    ctx = q.Context(heads=H)
+    from bit_kv_cache_qsac_gb300 import stream
+    layer = stream.CompressedLayer(ctx)
+    kk, vv = synth.keys(w_), synth.values(w_)
+    for i, (a, b) in enumerate([(0, 300), (300, 700), (700, 1024)]):
+        if i > 0:
+            layer.fold_queries(_bf(synth.queries(w_, 40 + i, 128)))
+        layer.append_chunk(_bf(np.ascontiguousarray(kk[:, a:b])), _bf(np.ascontiguousarray(vv[:, a:b])))
+    nq, tpf = 300, 100
+    qa = synth.queries(WIDE_W, 5, nq)
+    part_b = [layer.chunks[2]]
+    ka = kv = None
+    if with_active:
+        ka = synth.keys(WIDE_W)[:H, 3000:3000 + nq]; kv = synth.values(WIDE_W)[:H, 3000:3000 + nq]
+        part_b.append(q.ActiveChunk(_bf(np.ascontiguousarray(ka)), _bf(np.ascontiguousarray(kv)), causal_tpf=tpf))
+    scale = 1 / math.sqrt(D)
+    out = torch.empty(H, nq, D, dtype=torch.float32, device="cuda"); lse = torch.empty(H, nq, device="cuda")
+    q.qwm_attend_merge(ctx, _bf(qa), nq, layer.chunks[:2], scale, out, lse, False)
+    lse_a = lse.clone()
+    q.qwm_attend_merge(ctx, _bf(qa), nq, part_b, scale, out, lse, True)
+    one = torch.empty_like(out); lse1 = torch.empty_like(lse)
+    q.qwm_attend_merge(ctx, _bf(qa), nq, layer.chunks[:2] + part_b, scale, one, lse1, False)
+    assert q.qwm_sync_status(ctx) == 0
+    for h in range(H):
+        heads = [chunk_head(c, h) for c in layer.chunks]
+        union = heads + ([dict(k_raw=ka[h], v_raw=kv[h], causal_tpf=tpf)] if with_active else [])
+        ref, ref_lse = oracle.attend_rows(qa[h], np.arange(nq), union, scale, with_lse=True)
+        _, ref_lse_a = oracle.attend_rows(qa[h], np.arange(nq), heads[:2], scale, with_lse=True)
+        assert _attn_err(out[h].cpu().numpy().astype(np.float64), ref) <= 2e-2
+        assert np.abs(lse[h].cpu().numpy() - ref_lse).max() <= 0.02
+        assert np.abs(lse_a[h].cpu().numpy() - ref_lse_a).max() <= 0.02
+    # each call rounds its weights P to fp16 relative to its own running maximum, so the two results'
+    # weights differ by up to 2^-11 relative: O by at most about 2 * 2^-11 of its largest entries
+    assert (out - one).abs().max().item() <= 1e-3 * one.abs().max().item()
+    assert (lse - lse1).abs().max().item() <= 1e-5 * lse1.abs().max().item() + 1e-5
+
+
+def test_stream_step_overlap_matches(q):
+    """The overlapped schedule (history attention beside the new chunk's fits and packing, then the
+    new chunk merged in) packs identical chunks and gives the sequential schedule's outputs up to
+    the merge's rounding."""
+    w_ = synth.TINY
+    H = w_.heads
+    from bit_kv_cache_qsac_gb300 import stream
+    kk, vv = synth.keys(w_), synth.values(w_)
+    parts = [(0, 300), (300, 700), (700, 1024)]
+    qs = [_bf(synth.queries(w_, 20 + i, 96)) for i in range(len(parts))]
+    la, lb = stream.CompressedLayer(q.Context(heads=H)), stream.CompressedLayer(q.Context(heads=H))
+    outs_a, outs_b = [], []
+    for i, (a, b) in enumerate(parts):
+        k_ = _bf(np.ascontiguousarray(kk[:, a:b]))
+        v_ = _bf(np.ascontiguousarray(vv[:, a:b]))
+        outs_a.append(la.stream_step(k_, v_, qs[i]).clone())
+        outs_b.append(lb.stream_step(k_, v_, qs[i], overlap=True).clone())
+    torch.cuda.synchronize()
+    assert la.check() == 0 and lb.check() == 0
+    assert torch.equal(outs_a[0], outs_b[0])   # no history: the same single call
+    for oa, ob in zip(outs_a[1:], outs_b[1:]):   # the fp16 weights' rounding, as in test_attend_merge_parts
+        assert (oa - ob).abs().max().item() <= 1e-3 * oa.abs().max().item()
+    for ca, cb in zip(la.chunks, lb.chunks):
+        for name in ("k_idx", "v_idx", "k_codes", "v_codes", "c", "c_scale", "u_r"):
+            assert torch.equal(getattr(ca, name), getattr(cb, name)), name
+
+
 def test_bad_arguments_raise(q):
     ctx = q.Context(heads=2)
     x = torch.zeros(2, 300, D, dtype=torch.bfloat16, device="cuda")

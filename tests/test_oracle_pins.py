@@ -582,6 +582,34 @@ def test_attend_packed_and_bf16_chunks_share_one_softmax():
     assert np.allclose(out, ref, rtol=1e-10, atol=1e-12)
 
 
+def test_attend_log_sum_exp_and_merge_identity():
+    """The rows' base-2 log-sum-exp of the logits equals scipy's logsumexp / ln 2 on textbook logits
+    (raw bf16 keys); and the softmax over a union of chunks is the mean of the parts' softmaxes
+    weighted by 2^(lse_part - lse_union), lse_union = log2(2^lse_A + 2^lse_B) -- the identity the GPU's
+    merging attention relies on -- with a packed and a bf16 chunk as the parts."""
+    special = pytest.importorskip("scipy.special")
+    k, v, _, qa = synth.small_case(1, 200, 128, 64, 40, seed=55)
+    raw = dict(k_raw=k[0], v_raw=v[0])
+    _, lse = oracle.attend_rows(qa[0], np.arange(40), [raw], 0.09, with_lse=True)
+    logits = (_bf(qa[0]) @ _bf(k[0]).T) * 0.09
+    assert np.allclose(lse, special.logsumexp(logits, axis=1) / np.log(2.0), rtol=1e-13, atol=1e-12)
+    k, v, _, qa = synth.small_case(1, 300, 128, 64, 24, seed=54)
+    ck, _, _, _ = oracle.kmeans(k[0, :200], 64, None, 3)
+    cv, _, _, _ = oracle.kmeans(v[0, :200], 64, None, 3)
+    o = oracle.quantize_head(k[0, :200], v[0, :200], ck, cv, None, None, top_m=1, rank=0)
+    packed = dict(idx_k=o["idx_k"], idx_v=o["idx_v"], k_codes=o["k_codes"], v_codes=o["v_codes"],
+                  k_scale=o["k_scale"], k_min=o["k_min"], v_scale=o["v_scale"], v_min=o["v_min"],
+                  cent_k=ck, cent_v=cv, rank=0)
+    raw = dict(k_raw=k[0, 200:], v_raw=v[0, 200:])
+    rows = np.arange(24)
+    oa, la = oracle.attend_rows(qa[0], rows, [packed], 0.08, with_lse=True)
+    ob, lb = oracle.attend_rows(qa[0], rows, [raw], 0.08, with_lse=True)
+    ou, lu = oracle.attend_rows(qa[0], rows, [packed, raw], 0.08, with_lse=True)
+    assert np.allclose(lu, np.logaddexp2(la, lb), rtol=1e-13, atol=1e-12)
+    wa, wb = np.exp2(la - lu)[:, None], np.exp2(lb - lu)[:, None]
+    assert np.allclose(ou, wa * oa + wb * ob, rtol=1e-10, atol=1e-12)
+
+
 # ---------------------------------------------------------------- compact metadata and the PSAC gate
 
 
