@@ -32,8 +32,15 @@
  *    (a chunk with n_tokens == 0, Keys of a 0-token call, q and out of a 0-Query attention) may
  *    be NULL: such calls and chunks do nothing.
  *  - Head-major layouts: [H][tokens][channels] with H = config.heads.
- *  - A context is not thread-safe; calls that share a context must be
- *    ordered on one stream (the workspace is reused between calls).
+ *  - A context is not thread-safe: its calls are made from one host thread at a time.  Calls that
+ *    share part of its workspace must be ordered on one stream (the workspace is reused between
+ *    calls): qwm_fit_centroids, qwm_fit_centroids_kv and qwm_quantize_kv (the k-means and packing
+ *    workspaces, the context's second stream and its events) with one another, and
+ *    qwm_update_query_stats with itself (its partial sums).  Those two groups use disjoint
+ *    workspace, and qwm_attend, qwm_attend_merge, qwm_dequantize, qwm_dequantize_chunks,
+ *    qwm_select_rank and the coefficient-layout calls use none (only the status word, which any
+ *    number of kernels may write), so these may run on other streams beside the rest, ordered
+ *    only by their own data.
  */
 #ifndef QWM_H_
 #define QWM_H_
