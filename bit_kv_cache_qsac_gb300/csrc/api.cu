@@ -246,6 +246,9 @@ qwm_status qwm_fit_centroids_kv(qwm_ctx *ctx, const uint16_t *k, const uint16_t 
   qwm_status s = check_fit(ctx, k, n, init_k, cent_k);
   if (s == QWM_OK) s = check_fit(ctx, v, n, init_v, cent_v);
   if (s != QWM_OK) return s;
+  const size_t cb = (size_t)ctx->cfg.heads * ctx->cfg.n_centroids * QWM_D * sizeof(uint16_t);
+  const uintptr_t a0 = (uintptr_t)cent_k, b0 = (uintptr_t)cent_v;
+  if (a0 < b0 + cb && b0 < a0 + cb) return QWM_ERR_ARG;  // the two outputs overlap
   const cudaStream_t st = (cudaStream_t)stream;
   cudaError_t e = cudaEventRecord(ctx->fork, st);  // the Value fit starts after the work st holds
   if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->side, ctx->fork, 0);

@@ -241,7 +241,8 @@ QWM_API qwm_status qwm_fit_centroids(qwm_ctx *ctx, const uint16_t *x, int64_t n,
  * about 120 of the GPU's SMs at 40 heads, so side by side they fill the SMs one fit leaves idle.
  *   k, v           bf16 [H][n][d]  the chunk's Keys and Values (n >= config.n_centroids)
  *   init_k, init_v bf16 [H][C][d]  starting centroids of each, or NULL (as qwm_fit_centroids)
- *   cent_k, cent_v bf16 [H][C][d]  out: the two codebooks
+ *   cent_k, cent_v bf16 [H][C][d]  out: the two codebooks (distinct buffers: the two fits write them
+ *                                  at the same time)
  * Errors as qwm_fit_centroids; on an error nothing is launched. */
 QWM_API qwm_status qwm_fit_centroids_kv(qwm_ctx *ctx, const uint16_t *k, const uint16_t *v, int64_t n,
                                 const uint16_t *init_k, const uint16_t *init_v, uint16_t *cent_k,

@@ -208,6 +208,9 @@ def test_fit_centroids_kv_equals_two_fits(q, C, warm):
     q.qwm_fit_centroids(ctx, v, n, init_v, again)
     assert q.qwm_sync_status(ctx) == 0
     assert torch.equal(ck, ref_k) and torch.equal(cv, ref_v) and torch.equal(again, ref_v)
+    with pytest.raises(q.QwmError) as e:   # one buffer for both codebooks
+        q.qwm_fit_centroids_kv(ctx, k, v, n, init_k, init_v, ck, ck)
+    assert e.value.status == q.QWM_ERR_ARG
 
 
 def test_kmeans_objective_1024_centroids(q):
